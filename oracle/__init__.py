@@ -1,0 +1,18 @@
+"""fp64 CPU oracle for the hybrid (ordinary + frozen) causal attention layer.
+
+TEST INFRASTRUCTURE ONLY. Nothing on the product path imports this package:
+only the tests, the smoke check in ``__graft_entry__`` and the CPU-baseline
+leg of ``bench.py`` may call it. It shares no code with the CUDA library.
+
+See ``oracle/saf_oracle.py`` for the definitions and their citations.
+"""
+from .saf_oracle import (  # noqa: F401
+    frozen_logits,
+    frozen_pattern,
+    log_normaliser,
+    ordinary_pattern,
+    head_fwd,
+    head_bwd,
+    attn_fwd,
+    attn_bwd,
+)

@@ -1,0 +1,241 @@
+"""Plain fp64 reference for the hybrid causal-attention layer of Selective
+Attention Freezing (SAF).
+
+TEST INFRASTRUCTURE ONLY: called by tests/, by __graft_entry__.smoke() and by
+bench.py's CPU-baseline leg; never by the library. It is deliberately slow
+and literal: dense matrices, one exp per element, NumPy matmuls.
+
+Source: "When Can Attention Heads Be Statically Defined?" (arXiv 2609.34650).
+
+* Ordinary heads (App. A.1, Eqs. 5-7): S = Q K^T / sqrt(d_h),
+  A = softmax_causal(S), Z = A V. softmax_causal masks keys j > i and
+  normalises each query row.
+* Frozen heads (§3.2, Eq. 3): P(i, j) = exp(alpha(j) + rho(i - j)) / Z(i) for
+  j <= i, else 0, with Z(i) = sum_{k <= i} exp(alpha(k) + rho(i - k)). The head
+  output is P V (§3, "the head output"). The pattern does not look at Q or K.
+* Backward of a frozen head (§3.3 "Fused computation", App. D.2): only
+  dV = P^T dZ; alpha, rho and the normalisers receive no gradient (§3.3), and
+  a frozen head has no query/key slot, so dQ = dK = 0.
+* Backward of an ordinary head: the gradient of Eqs. 5-7 by the chain rule,
+  dV = A^T dO, dP = dO V^T, D_i = sum_j A_ij dP_ij, dS = A o (dP - D),
+  dQ = dS K / sqrt(d_h), dK = dS^T Q / sqrt(d_h).
+
+Indexing: the paper is 1-based (alpha over keys 1..T, rho over offsets
+0..T-1). Here everything is 0-based: alpha(j) -> a[j], rho(delta) -> r[delta],
+and Z(i) sums over j = 0..i. a and r may be longer than T (a stored prior of
+length >= T, App. D.2 tests prior length 192 with T = 129); only their first
+T entries are used.
+
+lse: for ordinary rows the natural-log normaliser of the scaled scores,
+m_i + log sum_j exp(S_ij - m_i); for frozen rows log Z(i).
+
+Row blocking: every quantity except dV and dK is local to one query row, so
+the functions below process query rows in blocks to bound memory at large T.
+dV and dK sum over query rows; blocking only changes the order of that sum.
+"""
+from __future__ import annotations
+
+import concurrent.futures as _cf
+import math
+
+import numpy as np
+
+_NEG_INF = -np.inf
+
+
+def _as64(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+# ---------------------------------------------------------------------------
+# Frozen-head pattern, Eq. 3
+# ---------------------------------------------------------------------------
+
+def frozen_logits(a, r, T, rows=None):
+    """L[i, j] = a[j] + r[i - j] for j <= i, -inf for j > i (Eq. 3 exponent).
+
+    Returns an array of shape [len(rows), T] (rows default to 0..T-1).
+    """
+    a = _as64(a)[:T]
+    r = _as64(r)[:T]
+    i = np.arange(T) if rows is None else np.asarray(rows)
+    j = np.arange(T)
+    delta = i[:, None] - j[None, :]
+    L = np.full(delta.shape, _NEG_INF)
+    keep = delta >= 0
+    L[keep] = (a[None, :] + r[np.where(keep, delta, 0)])[keep]
+    return L
+
+
+def _row_softmax(L):
+    """Row-wise softmax of a matrix whose masked entries are -inf."""
+    m = np.max(L, axis=1, keepdims=True)
+    e = np.exp(L - m)
+    return e / np.sum(e, axis=1, keepdims=True)
+
+
+def _row_logsumexp(L):
+    m = np.max(L, axis=1)
+    return m + np.log(np.sum(np.exp(L - m[:, None]), axis=1))
+
+
+def frozen_pattern(a, r, T, rows=None):
+    """Dense P-hat of Eq. 3 for the given query rows.
+
+    P(i, j) = exp(a[j] + r[i - j]) / Z(i), j <= i. Z(i) is the row sum of the
+    numerators, so P is the row softmax of frozen_logits; the row maximum is
+    subtracted before exp, which leaves every ratio unchanged.
+    """
+    return _row_softmax(frozen_logits(a, r, T, rows))
+
+
+def log_normaliser(a, r, T):
+    """log Z(i), i = 0..T-1, with Z(i) = sum_{k <= i} exp(a[k] + r[i - k]) (Eq. 3)."""
+    return _row_logsumexp(frozen_logits(a, r, T))
+
+
+# ---------------------------------------------------------------------------
+# Ordinary head, Eqs. 5-7
+# ---------------------------------------------------------------------------
+
+def _causal_scores(q_rows, k, rows, scale):
+    """S = Q K^T * scale on the given query rows, keys j > i set to -inf."""
+    S = (q_rows @ k.T) * scale
+    T = k.shape[0]
+    S[np.arange(T)[None, :] > np.asarray(rows)[:, None]] = _NEG_INF
+    return S
+
+
+def ordinary_pattern(q, k, rows=None):
+    """A = softmax_causal(Q K^T / sqrt(d)) on the given query rows (Eqs. 5-6)."""
+    q = _as64(q)
+    k = _as64(k)
+    T, d = k.shape
+    rows = np.arange(T) if rows is None else np.asarray(rows)
+    return _row_softmax(_causal_scores(q[rows], k, rows, 1.0 / math.sqrt(d)))
+
+
+# ---------------------------------------------------------------------------
+# One (batch, head) slice
+# ---------------------------------------------------------------------------
+
+def _blocks(rows, block):
+    for s in range(0, len(rows), block):
+        yield rows[s:s + block]
+
+
+def head_fwd(q, k, v, a, r, frozen, rows=None, block=1024):
+    """Forward of one head on one sequence.
+
+    q, k, v: [T, d]; a, r: [>= T]; frozen: bool. Returns (o, lse) on the given
+    query rows (default all): o [len(rows), d], lse [len(rows)]. Frozen heads
+    never read q or k.
+    """
+    v = _as64(v)
+    T, d = v.shape
+    rows = np.arange(T) if rows is None else np.asarray(rows)
+    o = np.empty((len(rows), d))
+    lse = np.empty(len(rows))
+    if not frozen:
+        q = _as64(q)
+        k = _as64(k)
+        scale = 1.0 / math.sqrt(d)
+    pos = 0
+    for blk in _blocks(rows, block):
+        if frozen:
+            L = frozen_logits(a, r, T, blk)                 # Eq. 3 exponent
+        else:
+            L = _causal_scores(q[blk], k, blk, scale)       # Eq. 5 + causal mask
+        P = _row_softmax(L)                                 # Eq. 3 / Eq. 6
+        o[pos:pos + len(blk)] = P @ v                       # P V / Eq. 7
+        lse[pos:pos + len(blk)] = _row_logsumexp(L)
+        pos += len(blk)
+    return o, lse
+
+
+def head_bwd(q, k, v, do, a, r, frozen, block=1024):
+    """Backward of one head on one sequence, given the output gradient dO.
+
+    Returns (dq, dk, dv), each [T, d]. For a frozen head dq = dk = 0 exactly
+    and dv = P^T dO; for an ordinary head the chain rule through Eqs. 5-7.
+    """
+    v = _as64(v)
+    do = _as64(do)
+    T, d = v.shape
+    rows = np.arange(T)
+    dv = np.zeros((T, d))
+    dq = np.zeros((T, d))
+    dk = np.zeros((T, d))
+    if frozen:
+        for blk in _blocks(rows, block):
+            P = frozen_pattern(a, r, T, blk)
+            dv += P.T @ do[blk]                             # dV = P^T dZ
+        return dq, dk, dv
+    q = _as64(q)
+    k = _as64(k)
+    scale = 1.0 / math.sqrt(d)
+    for blk in _blocks(rows, block):
+        A = _row_softmax(_causal_scores(q[blk], k, blk, scale))
+        dv += A.T @ do[blk]                                 # dV = A^T dO
+        dP = do[blk] @ v.T                                  # dP = dO V^T
+        D = np.sum(A * dP, axis=1, keepdims=True)           # D_i = sum_j A_ij dP_ij
+        dS = A * (dP - D)                                   # softmax Jacobian
+        dq[blk] = (dS @ k) * scale                          # dQ = dS K / sqrt(d)
+        dk += (dS.T @ q[blk]) * scale                       # dK = dS^T Q / sqrt(d)
+    return dq, dk, dv
+
+
+# ---------------------------------------------------------------------------
+# Whole layer [B, H, T, d]
+# ---------------------------------------------------------------------------
+
+def _map(fn, items, threads):
+    if threads <= 1:
+        return [fn(x) for x in items]
+    with _cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        return list(ex.map(fn, items))
+
+
+def attn_fwd(q, k, v, a, r, frozen, threads=1):
+    """Layer forward. q, k, v [B, H, T, d]; a, r [H, >= T]; frozen: H flags.
+
+    Returns o [B, H, T, d] and lse [B, H, T] in fp64. Output heads keep their
+    original order (App. D.2).
+    """
+    v = _as64(v)
+    B, H, T, d = v.shape
+    q = _as64(q)
+    k = _as64(k)
+    a = _as64(a)
+    r = _as64(r)
+    o = np.empty((B, H, T, d))
+    lse = np.empty((B, H, T))
+
+    def one(bh):
+        b, h = bh
+        o[b, h], lse[b, h] = head_fwd(q[b, h], k[b, h], v[b, h], a[h], r[h], bool(frozen[h]))
+
+    _map(one, [(b, h) for b in range(B) for h in range(H)], threads)
+    return o, lse
+
+
+def attn_bwd(q, k, v, do, a, r, frozen, threads=1):
+    """Layer backward. Returns dq, dk, dv [B, H, T, d] in fp64."""
+    v = _as64(v)
+    B, H, T, d = v.shape
+    q = _as64(q)
+    k = _as64(k)
+    do = _as64(do)
+    a = _as64(a)
+    r = _as64(r)
+    dq = np.empty((B, H, T, d))
+    dk = np.empty((B, H, T, d))
+    dv = np.empty((B, H, T, d))
+
+    def one(bh):
+        b, h = bh
+        dq[b, h], dk[b, h], dv[b, h] = head_bwd(q[b, h], k[b, h], v[b, h], do[b, h],
+                                                a[h], r[h], bool(frozen[h]))
+
+    _map(one, [(b, h) for b in range(B) for h in range(H)], threads)
+    return dq, dk, dv

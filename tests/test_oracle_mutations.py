@@ -1,0 +1,74 @@
+"""Plant plausible mistakes in a private copy of the oracle and check that the
+pins in test_oracle.py catch every one of them.
+
+The copy is built from the oracle's source text with one substitution each;
+the real oracle module is never modified.
+"""
+import inspect
+import types
+
+import pytest
+
+import oracle.saf_oracle as real
+import tests.test_oracle as pins
+
+MUTATIONS = {
+    # Eq. 3: wrong index into the relative preference (r[i] instead of r[i-j])
+    "relative_index": ("r[np.where(keep, delta, 0)]", "r[np.where(keep, i[:, None] + 0 * delta, 0)]"),
+    # Eq. 3: absolute preference indexed by the query instead of the key
+    "absolute_index": ("(a[None, :] + r", "(a[i][:, None] + r"),
+    # Eq. 3: dropped absolute term
+    "dropped_alpha": ("(a[None, :] + r", "(0.0 * a[None, :] + r"),
+    # causal mask off by one (diagonal excluded)
+    "mask_diagonal": ("keep = delta >= 0", "keep = delta >= 1"),
+    # Eq. 5: missing 1/sqrt(d)
+    "missing_scale": ("return _row_softmax(_causal_scores(q[rows], k, rows, 1.0 / math.sqrt(d)))",
+                      "return _row_softmax(_causal_scores(q[rows], k, rows, 1.0))"),
+    "missing_scale_fwd": ("scale = 1.0 / math.sqrt(d)\n    pos = 0", "scale = 1.0\n    pos = 0"),
+    # backward: sign error in the softmax Jacobian
+    "dS_sign": ("dS = A * (dP - D)", "dS = A * (D - dP)"),
+    # backward: D without the A weights
+    "D_unweighted": ("D = np.sum(A * dP, axis=1, keepdims=True)", "D = np.sum(dP, axis=1, keepdims=True)"),
+    # backward: transposed operand in dK
+    "dK_transposed": ("dk += (dS.T @ q[blk]) * scale", "dk += (dS.T @ k[blk]) * scale"),
+    # backward: frozen dV with the pattern untransposed
+    "frozen_dV_untransposed": ("dv += P.T @ do[blk]", "dv[:len(blk)] += P[:, :len(blk)] @ do[blk]"),
+    # lse: forgot the max shift
+    "lse_no_max": ("return m + np.log(np.sum(np.exp(L - m[:, None]), axis=1))",
+                   "return np.log(np.sum(np.exp(L - m[:, None]), axis=1))"),
+}
+
+PIN_TESTS = [(n, f) for n, f in inspect.getmembers(pins, inspect.isfunction) if n.startswith("test_")]
+
+
+def _mutant(src, old, new, name):
+    assert old in src, f"mutation anchor for {name} not found in oracle source"
+    mod = types.ModuleType(f"oracle_mutant_{name}")
+    exec(compile(src.replace(old, new, 1), mod.__name__, "exec"), mod.__dict__)
+    return mod
+
+
+def _call(fn):
+    cases = [()]
+    for m in getattr(fn, "pytestmark", []):
+        if m.name == "parametrize":
+            cases = [(v,) for v in m.args[1]]
+    for case in cases:
+        fn(*case)
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_planted_mistake(name, monkeypatch):
+    pytest.importorskip("mpmath")
+    src = inspect.getsource(real)
+    old, new = MUTATIONS[name]
+    mutant = _mutant(src, old, new, name)
+    monkeypatch.setattr(pins, "oracle", mutant)
+    caught = []
+    for tname, fn in PIN_TESTS:
+        try:
+            _call(fn)
+        except Exception:  # an assertion or a shape error both expose the mistake
+            caught.append(tname)
+    assert caught, f"no pin caught mutation {name}"
+
