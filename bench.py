@@ -1,0 +1,450 @@
+#!/usr/bin/env python
+"""Benchmark of the hybrid (ordinary + frozen heads) causal attention layer.
+
+One step = forward + backward of the layer over one synthetic batch, through
+the C ABI of libsaf.so. Default workload: GPT-2-124M-shaped layer with 25% of
+heads frozen (B=8, H=12 with heads 3, 7, 11 frozen, T=4096, d=64, bf16).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0). Under torchrun each rank runs its own batch of
+the same workload (weak scaling, no collective on the data path); the time
+is the max over ranks and the value the work of all ranks over that time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from softmax_attention_hybrid_gb300 import flops as F  # noqa: E402
+from softmax_attention_hybrid_gb300.inputs import WORKLOADS, make_inputs, Workload  # noqa: E402
+
+METRIC = "hybrid attention fwd+bwd TFLOP/s and tokens/s at 1 GB300; % of bf16 tensor peak"
+DEFAULT_WORKLOAD = "gpt2_124m_25"
+L2_FLUSH_BYTES = 256 << 20  # larger than the 129 MB L2
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0}, \
+        "fallback"
+
+
+def _src_hash():
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "softmax_attention_hybrid_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".h", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    with open(os.path.join(ROOT, "include", "saf.h"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index=0):
+        self.proc = None
+        self.path = None
+        self.dev = device_index
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            uuid = None
+            try:
+                uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
+                uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            except Exception:
+                uuid = None
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+            if uuid:
+                cmd += ["-i", uuid]
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            for nm, val in zip(names, r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        loaded = [x for x in sm if x > 0.5 * (max(sm) if sm else 1)]
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; no collective on the data path)
+# ---------------------------------------------------------------------------
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def dist_init(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+# ---------------------------------------------------------------------------
+# oracle timing (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w: Workload, x):
+    """A bounded sample of the workload for the fp64 CPU oracle: the first
+    ordinary head and the first frozen head of batch entry 0, forward and
+    backward (forward only for forward-only workloads). Returns (fn, flops,
+    description)."""
+    import oracle
+    fz = [h for h in range(w.H) if x["frozen"][h]]
+    od = [h for h in range(w.H) if not x["frozen"][h]]
+    heads = ([od[0]] if od else []) + ([fz[0]] if fz else [])
+    a, r = x["a"].double().numpy(), x["r"].double().numpy()
+    sl = {h: [x[n][0, h].double().numpy() for n in ("q", "k", "v", "do")] for h in heads}
+    c = 2 * F.pairs(w.T) * w.d
+    flops = 0
+    for h in heads:
+        units = (2 if not x["frozen"][h] else 1) + (0 if w.fwd_only else (5 if not x["frozen"][h] else 1))
+        flops += units * c
+
+    def run():
+        for h in heads:
+            q, k, v, do = sl[h]
+            fzh = bool(x["frozen"][h])
+            oracle.head_fwd(q, k, v, a[h], r[h], fzh)
+            if not w.fwd_only:
+                oracle.head_bwd(q, k, v, do, a[h], r[h], fzh)
+
+    desc = (f"batch 0, heads {heads} (one ordinary, one frozen) of {w.name}, T={w.T}, "
+            f"{'fwd' if w.fwd_only else 'fwd+bwd'}, fp64 NumPy/OpenBLAS")
+    return run, flops, desc
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, w):
+    rank, world, local = dist_info()
+    if rank != 0:
+        return 0
+    x = make_inputs(w, seed=0)
+    run, flops, desc = oracle_sample(w, x)
+    for _ in range(args.warmup):
+        run()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        run()
+        times.append(time.perf_counter() - t0)
+    mean = sum(times) / len(times)
+    value = flops / mean / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "F": w.F, "T": w.T, "d": w.d,
+                   "sample": desc},
+        # tokens/s of the full layer at the sample's FLOP rate
+        "tokens_per_s": w.B * w.T * value * 1e12 / F.layer_flops(w.B, w.H, w.F, w.T, w.d, not w.fwd_only),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores(), "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+KERNEL_FLOP_UNITS = {
+    # (ordinary contractions, frozen contractions) per (batch, head) per launch
+    "fwd": (2, 1),
+    "bwd_kv": (4, 1),     # S recompute, dV, dP, dK | dV
+    "bwd_q": (1, 0),      # dQ (its S and dP recomputes are not counted)
+    "bwd": (5, 1),
+}
+
+
+# what bounds each kernel: the fp32 CUDA-core kernels are FMA-bound ("alu")
+KERNEL_BOUND = {"fwd": "alu", "bwd_kv": "alu", "bwd_q": "alu", "bwd": "tensor"}
+
+
+def run_ours(args, w):
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    dist_init(world, "nccl")
+    dev = torch.device("cuda", local)
+    from softmax_attention_hybrid_gb300 import saf
+
+    x = make_inputs(w, seed=rank)
+    frozen = x["frozen"]
+    g = {n: x[n].to(dev) for n in ("q", "k", "v", "do", "a", "r")}
+    B, H, T, d = w.B, w.H, w.T, w.d
+    o = torch.empty_like(g["v"])
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(g["v"]) for _ in range(3))
+    ws = saf.alloc_workspace(B, H, T, d, g["v"].dtype, True, dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(mask):
+        saf.saf_attn_fwd(g["q"], g["k"], g["v"], g["a"], g["r"], mask, o=o, lse=lse, workspace=ws)
+        if not w.fwd_only:
+            saf.saf_attn_bwd(g["q"], g["k"], g["v"], o, g["do"], lse, g["a"], g["r"], mask, dq=dq, dk=dk, dv=dv,
+                             workspace=ws)
+
+    kernels = {"fwd": saf.SAF_KERNEL_FWD}
+    if not w.fwd_only:
+        kernels.update({"bwd_kv": saf.SAF_KERNEL_BWD_KV, "bwd_q": saf.SAF_KERNEL_BWD_Q, "bwd": saf.SAF_KERNEL_BWD})
+
+    def timed(mask, K, trace):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        kev = {nm: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+               for nm in kernels} if trace else {}
+        barrier(world)
+        torch.cuda.synchronize()
+        n0 = saf.saf_launch_count()
+        for i in range(K):
+            flush.fill_(float(i))
+            for nm, kid in kernels.items():
+                if trace:
+                    saf.saf_set_trace_events(kid, kev[nm][i][0], kev[nm][i][1])
+            evs[i][0].record(stream)
+            step(mask)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        saf.saf_set_trace_events(saf.SAF_KERNEL_NONE)
+        launches = saf.saf_launch_count() - n0
+        ms = [s.elapsed_time(e) for s, e in evs]
+        kms = {}
+        for nm in kernels:
+            if trace:
+                try:
+                    vals = [s.elapsed_time(e) for s, e in kev[nm]]
+                    kms[nm] = sum(vals) / len(vals)
+                except RuntimeError:   # kernel not launched on this path
+                    pass
+        return ms, kms, launches
+
+    for _ in range(args.warmup):
+        step(frozen)
+    torch.cuda.synchronize()
+    status = saf.saf_device_status(ws)
+    if status != saf.SAF_OK:
+        raise RuntimeError(f"device status after warm-up: {saf.saf_error_string(status)}")
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    t_wall0 = time.perf_counter()
+    ms, kms, launches = timed(frozen, args.steps, True)
+    t_wall = time.perf_counter() - t_wall0
+    clk = clocks.stop()
+
+    step_ms = max_over_ranks(sum(ms) / len(ms), world, dev)
+    total_flops = F.layer_flops(B, H, w.F, T, d, backward=not w.fwd_only) * world
+    value = total_flops / (step_ms * 1e-3) / 1e12
+    tokens = B * T * world / (step_ms * 1e-3)
+
+    # all-ordinary run of the same kernels on the same inputs
+    allord = None
+    if args.all_ordinary and w.F > 0:
+        for _ in range(max(1, args.warmup // 2)):
+            step([0] * H)
+        ms0, _, _ = timed([0] * H, args.steps, False)
+        ao_ms = max_over_ranks(sum(ms0) / len(ms0), world, dev)
+        allord = {"ms_per_step": ao_ms, "speedup": ao_ms / step_ms,
+                  "ideal_speedup": F.layer_flops(B, H, 0, T, d, not w.fwd_only) /
+                  F.layer_flops(B, H, w.F, T, d, not w.fwd_only)}
+
+    # end to end: host buffers in, host buffers out, through the same C ABI
+    e2e = None
+    if args.e2e:
+        host_in = {n: x[n].pin_memory() for n in ("q", "k", "v", "do", "a", "r")}
+        host_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                    for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+        if w.fwd_only:
+            for n in ("dq", "dk", "dv"):
+                host_out.pop(n)
+        in_names = ("q", "k", "v", "a", "r") + (() if w.fwd_only else ("do",))
+        h2d = sum(host_in[n].numel() * host_in[n].element_size() for n in in_names)
+        d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+        dev_out = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+
+        def e2e_step():
+            for n in in_names:
+                g[n].copy_(host_in[n], non_blocking=True)
+            step(frozen)
+            for n, t in host_out.items():
+                t.copy_(dev_out[n], non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        K = args.steps
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        barrier(world)
+        for i in range(K):
+            flush.fill_(float(i))
+            evs[i][0].record(stream)
+            e2e_step()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in evs) / K, world, dev)
+        e2e = {"value": total_flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    if rank != 0:
+        return 0
+
+    peaks, peak_src = _peaks()
+    # dominant kernel: the longest traced kernel of the step
+    roofline = None
+    if kms:
+        name = max(kms, key=kms.get)
+        units_o, units_f = KERNEL_FLOP_UNITS[name]
+        c = 2 * F.pairs(T) * d
+        kflops = B * ((H - w.F) * units_o + w.F * units_f) * c
+        achieved = kflops / (kms[name] * 1e-3) / 1e12
+        if KERNEL_BOUND.get(name) == "tensor":
+            peak = peaks["bf16_tflops"]
+            bound, note = "tensor", f"bf16 dense, burst, {peak_src}"
+        else:
+            # fp32 FMA pipes: 152 SMs x 128 FMA/clk x 2 FLOP at the max SM clock
+            peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+            bound, note = "alu", "fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x max SM clock (derived)"
+        traffic = None
+        tpath = os.path.join(ROOT, "profiles", "traffic.json")
+        if os.path.exists(tpath):
+            with open(tpath) as f:
+                tt = json.load(f)
+            ent = tt.get(f"{name}|{w.name}|{_src_hash()}")
+            traffic = ent if ent is not None else None
+        roofline = {"kernel": name, "bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": traffic, "peak_source": note,
+                    "flops_per_launch": kflops, "ms_per_launch": kms[name],
+                    "kernel_ms": kms}
+
+    cpu = None
+    if args.cpu_baseline and world == 1:
+        run, sflops, desc = oracle_sample(w, x)
+        t0 = time.perf_counter()
+        run()
+        dt = time.perf_counter() - t0
+        cpu = {"value": sflops / dt / 1e12, "unit": "TFLOP/s", "cores": cores(), "kind": "oracle",
+               "sample": desc, "seconds": dt}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "F": w.F, "T": w.T, "d": w.d,
+                   "frozen_heads": [h for h in range(H) if frozen[h]],
+                   "l2": "flushed (256 MB write) before every timed step; inputs also exceed L2",
+                   "parallelism": f"replicas x{world}, one batch per GPU"},
+        "tokens_per_s": tokens,
+        "frac_of_bf16_peak": value / world / peaks["bf16_tflops"],
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "all_ordinary": allord,
+        "gpu_launches": launches,
+        "clocks": clk,
+        "wall_s_timed_region": t_wall,
+        "peaks": {"source": peak_src, "bf16_tflops": peaks["bf16_tflops"], "hbm_gbs": peaks["hbm_gbs"]},
+        "src": _src_hash(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--no-all-ordinary", dest="all_ordinary", action="store_false")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

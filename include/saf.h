@@ -1,0 +1,156 @@
+/*
+ * saf.h - C ABI of the hybrid causal-attention layer of Selective Attention
+ * Freezing (SAF), forward and backward, on one NVIDIA GB300 (sm_103a).
+ *
+ * Source: "When Can Attention Heads Be Statically Defined?" (arXiv 2609.34650).
+ *
+ *   Ordinary head (App. A.1, Eqs. 5-7):
+ *       S = Q K^T / sqrt(d),  A = softmax_causal(S),  O = A V.
+ *   Frozen head (§3.2, Eq. 3; §3.3 "Fused computation"):
+ *       W(i, j) = exp(a[j] + r[i - j]) / Z(i) for j <= i, 0 for j > i,
+ *       Z(i)    = sum_{k <= i} exp(a[k] + r[i - k]),        O = W V.
+ *     The pattern never looks at Q or K. Its backward pass is only
+ *     dV = W^T dO (§3.3, App. D.2); a frozen head has no query/key slot, so
+ *     its dQ and dK are zero, and a, r and the normalisers take no gradient.
+ *   Both kinds of head run in one fused launch per pass and write their
+ *   outputs in the original head order (App. D.2).
+ *
+ * Indexing is 0-based: the paper's alpha(j) (keys 1..T) is a[j-1] and its
+ * rho(delta) (offsets 0..T-1) is r[delta].
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors q, k, v, o, dO, dq, dk, dv have layout [B, H, T, d], contiguous,
+ *    element type `dt` (bf16 or fp32). lse and the normalisers are fp32.
+ *    Every tensor pointer must be 16-byte aligned (SAF_EALIGN otherwise).
+ *  - a, r: fp32 [H, ld_prior] device arrays, ld_prior >= T; row h holds the
+ *    absolute-key preference a and the relative-distance preference r of
+ *    head h. Only a[h, 0..T-1], r[h, 0..T-1] of frozen heads are read, so a
+ *    stored prior longer than T may be passed (App. D.2 tests prior length
+ *    192 at T = 129). a and r may be NULL when no head is frozen.
+ *  - frozen: HOST array of H bytes, nonzero = frozen head. NULL means no
+ *    frozen head. H <= SAF_MAX_HEADS.
+ *  - q and k of frozen heads are never read (they may hold anything,
+ *    including NaN); q and k may be NULL only when every head is frozen.
+ *  - workspace: caller-owned DEVICE scratch of at least
+ *    saf_attn_workspace_bytes(...) bytes, 256-byte aligned. The library
+ *    allocates no memory and keeps no state across calls other than cached
+ *    device attributes, CUDA function attributes, a launch counter and the
+ *    optional trace hook below. Calls that share a workspace must be
+ *    ordered on one stream.
+ *  - stream: a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    All device work is enqueued on it; no entry point synchronises except
+ *    saf_device_status.
+ *  - Return value: SAF_OK (0) or a negative saf_status_t. Argument, shape,
+ *    alignment and device errors are returned synchronously before any
+ *    work is enqueued. An error raised while kernels run (a bounded device
+ *    wait that expired) is recorded in the workspace and reported by
+ *    saf_device_status.
+ *  - T == 0 or B == 0 is a valid empty call: nothing is launched.
+ */
+#ifndef SAF_H_
+#define SAF_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SAF_MAX_HEADS 256
+
+#if defined(__GNUC__)
+#define SAF_API __attribute__((visibility("default")))
+#else
+#define SAF_API
+#endif
+
+typedef enum { SAF_BF16 = 0, SAF_FP32 = 1 } saf_dtype_t;
+
+typedef enum {
+    SAF_OK = 0,
+    SAF_EINVAL = -1,        /* null pointer, bad shape, ld_prior < T, H > SAF_MAX_HEADS   */
+    SAF_EALIGN = -2,        /* a tensor or the workspace is not aligned                   */
+    SAF_EUNSUPPORTED = -3,  /* device is not sm_103, or d / dtype not supported          */
+    SAF_ELAUNCH = -4,       /* a kernel launch or an async CUDA call failed               */
+    SAF_EWORKSPACE = -5,    /* workspace NULL or smaller than saf_attn_workspace_bytes    */
+    SAF_ETIMEOUT = -6,      /* a bounded device wait expired (from saf_device_status)    */
+    SAF_ECUDA = -8          /* a CUDA runtime query failed (no device, driver error)    */
+} saf_status_t;
+
+/* Bytes of device workspace that saf_attn_fwd (backward = 0) or
+ * saf_attn_bwd (backward = 1) needs for these sizes. Returns 0 for an
+ * invalid size. */
+SAF_API size_t saf_attn_workspace_bytes(int B, int H, int T, int d, saf_dtype_t dt, int backward);
+
+/* Forward pass of the hybrid layer.
+ *
+ * In:  q, k, v [B,H,T,d] (dt); a, r [H, ld_prior] fp32; frozen [H] host bytes.
+ * Out: o [B,H,T,d] (dt): ordinary heads A V (Eqs. 5-7), frozen heads W V
+ *      (Eq. 3); lse [B,H,T] fp32: for ordinary rows the natural-log
+ *      normaliser of the scaled scores, m_i + log sum_j exp(S_ij - m_i); for
+ *      frozen rows log Z(i). saf_attn_bwd consumes lse.
+ * The normalisers log Z of the frozen heads are computed here ("precomputed
+ * normalisers", §3.3), once per head, independent of the batch.
+ * Supported: d == 64; dt SAF_BF16 (tensor cores, fp32 accumulation) or
+ * SAF_FP32 (fp32 arithmetic throughout). */
+SAF_API int saf_attn_fwd(const void* q, const void* k, const void* v,
+                 const float* a, const float* r, int ld_prior, const uint8_t* frozen,
+                 int B, int H, int T, int d, saf_dtype_t dt,
+                 void* o, float* lse,
+                 void* workspace, size_t ws_bytes, void* stream);
+
+/* Backward pass of the hybrid layer, given dO = dL/dO.
+ *
+ * In:  q, k, v, o, dO [B,H,T,d] (dt), lse [B,H,T] from saf_attn_fwd with the
+ *      same inputs; a, r, frozen as in saf_attn_fwd.
+ * Out: dq, dk, dv [B,H,T,d] (dt). Ordinary heads: the gradient of Eqs. 5-7.
+ *      Frozen heads: dv = W^T dO; dq and dk are written as exact zeros
+ *      (§3.3, App. D.2). */
+SAF_API int saf_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                 const float* lse, const float* a, const float* r, int ld_prior,
+                 const uint8_t* frozen, int B, int H, int T, int d, saf_dtype_t dt,
+                 void* dq, void* dk, void* dv,
+                 void* workspace, size_t ws_bytes, void* stream);
+
+/* Waits for `stream`, then reads the error word that the kernels of the last
+ * call on `workspace` left there. Returns SAF_OK, SAF_ETIMEOUT, or
+ * SAF_ECUDA if the stream reported a CUDA error. */
+SAF_API int saf_device_status(const void* workspace, void* stream);
+
+/* Static, human-readable text for a status code. Never NULL. */
+SAF_API const char* saf_error_string(int status);
+
+/* ABI version of this library (major * 100 + minor). */
+SAF_API int saf_version(void);
+
+/* ---- Profiling hooks (not part of the layer's arithmetic) ----------------
+ * Kernel identifiers for saf_set_trace_events. */
+typedef enum {
+    SAF_KERNEL_NONE = 0,
+    SAF_KERNEL_LOGNORM = 1,     /* log Z of the frozen heads                    */
+    SAF_KERNEL_FWD = 2,         /* fused forward (both kinds of head)           */
+    SAF_KERNEL_BWD_DELTA = 3,   /* D_i = sum_c dO_ic O_ic                       */
+    SAF_KERNEL_BWD_KV = 4,      /* backward key-block pass (dV, dK)            */
+    SAF_KERNEL_BWD_Q = 5,       /* backward query-block pass (dQ)              */
+    SAF_KERNEL_BWD = 6          /* fused backward (dQ, dK, dV in one launch)   */
+} saf_kernel_t;
+
+/* From the next call on, record `start` (a cudaEvent_t as void*) on the
+ * call's stream right before every launch of `kernel`, and `stop` right
+ * after it. Each kernel id has its own pair; NULL events switch that id
+ * off, SAF_KERNEL_NONE switches every id off. The hook is process-wide and
+ * not thread-safe; it is meant for benchmarks. Returns SAF_OK or
+ * SAF_EINVAL for an unknown id. */
+SAF_API int saf_set_trace_events(int kernel, void* start, void* stop);
+
+/* Number of kernels this library has launched since it was loaded
+ * (host-side counter, all devices and streams). */
+SAF_API unsigned long long saf_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SAF_H_ */

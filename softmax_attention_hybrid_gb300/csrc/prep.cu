@@ -1,0 +1,145 @@
+// Per-call preparation kernels of the hybrid attention layer.
+//
+//  * lognorm: the row normalisers log Z(i) of every frozen head
+//    ("When Can Attention Heads Be Statically Defined?", §3.2 Eq. 3; §3.3
+//    "precomputed normalisers"). They do not depend on the batch.
+//  * bwd_delta: D_i = sum_c dO_ic O_ic for the ordinary-head backward
+//    (the softmax Jacobian term of Eqs. 5-7 differentiated; App. D.2).
+#include <math.h>
+
+#include "saf_internal.h"
+
+namespace saf {
+namespace {
+
+constexpr int kPrepThreads = 256;
+
+__device__ float block_max(float x, float* red) {
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        x = lane < (int)(blockDim.x >> 5) ? red[lane] : -INFINITY;
+        for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+        if (lane == 0) red[0] = x;
+    }
+    __syncthreads();
+    x = red[0];
+    __syncthreads();
+    return x;
+}
+
+// Eq. 3 factorises: exp(a[j] + r[i-j]) = e^{A+R} * ea[j] * er[i-j] with
+// ea = exp(a - A), er = exp(r - R), A = max a, R = max r. So
+//     Z(i) = e^{A+R} * sum_{j<=i} ea[j] er[i-j],
+// a causal convolution that needs no exp per term. Every factor lies in
+// (0, 1]. If the shifted sum falls below 1e-28, terms that matter may have
+// left the normal fp32 range; that row is recomputed exactly by a running
+// log-sum-exp and the head is flagged (kStatusRange) for the fast kernels,
+// which rely on the factorised form.
+//
+// Grid: (ceil(T / 256), H); one thread per row i of head h.
+__global__ void __launch_bounds__(kPrepThreads)
+lognorm_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all, int ld, HeadMask mask,
+               int T, float* __restrict__ lz, uint32_t* __restrict__ hflag, uint32_t* __restrict__ status) {
+    const int h = blockIdx.y;
+    if (!head_frozen(mask, h)) return;
+    const float* a = a_all + (size_t)h * ld;
+    const float* r = r_all + (size_t)h * ld;
+    __shared__ float red[32];
+    __shared__ float ea_s[kPrepThreads];
+    __shared__ float er_s[2 * kPrepThreads];
+
+    float ma = -INFINITY, mr = -INFINITY;
+    for (int j = threadIdx.x; j < T; j += blockDim.x) {
+        ma = fmaxf(ma, a[j]);
+        mr = fmaxf(mr, r[j]);
+    }
+    const float A = block_max(ma, red);
+    const float R = block_max(mr, red);
+
+    const int i0 = blockIdx.x * kPrepThreads;
+    const int i = i0 + threadIdx.x;
+    const int imax = min(i0 + kPrepThreads - 1, T - 1);
+    float z = 0.f;
+    for (int j0 = 0; j0 <= imax; j0 += kPrepThreads) {
+        const int jt = j0 + threadIdx.x;
+        ea_s[threadIdx.x] = (jt <= imax) ? expf(a[jt] - A) : 0.f;
+        // offsets needed by rows i0..i0+255 against keys j0..j0+255
+        const int base = i0 - j0 - (kPrepThreads - 1);
+        for (int t = threadIdx.x; t < 2 * kPrepThreads; t += blockDim.x) {
+            const int dlt = base + t;
+            er_s[t] = (dlt >= 0 && dlt < T) ? expf(r[dlt] - R) : 0.f;
+        }
+        __syncthreads();
+        if (i < T) {
+            // er_s[(i - j) - base] with j = j0 + jj; keys j > i meet er_s = 0 (negative offset).
+            const float* e = er_s + (i - i0) + (kPrepThreads - 1);
+#pragma unroll 8
+            for (int jj = 0; jj < kPrepThreads; ++jj) z = fmaf(ea_s[jj], e[-jj], z);
+        }
+        __syncthreads();
+    }
+    if (i >= T) return;
+    float out;
+    if (z >= 1e-28f) {
+        out = logf(z) + A + R;
+    } else {
+        // exact running log-sum-exp over j <= i
+        float m = -INFINITY, s = 0.f;
+        for (int j = 0; j <= i; ++j) {
+            const float x = a[j] + r[i - j];
+            if (x > m) {
+                s = s * expf(m - x) + 1.f;
+                m = x;
+            } else {
+                s += expf(x - m);
+            }
+        }
+        out = m + logf(s);
+        atomicOr(hflag + h, 1u);
+        atomicOr(status, kStatusRange);
+    }
+    lz[(size_t)h * T + i] = out;
+}
+
+// D_i = sum_c dO_ic * O_ic, one warp per row (d = 64: two elements per lane).
+template <typename E>
+__global__ void __launch_bounds__(256)
+bwd_delta_kernel(const E* __restrict__ o, const E* __restrict__ dO, float* __restrict__ delta, long long rows) {
+    const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const int lane = threadIdx.x & 31;
+    const E* po = o + row * kHeadDim;
+    const E* pd = dO + row * kHeadDim;
+    float x = 0.f;
+    for (int c = lane; c < kHeadDim; c += 32) x = fmaf(to_f(po[c]), to_f(pd[c]), x);
+    for (int s = 16; s > 0; s >>= 1) x += __shfl_xor_sync(0xffffffffu, x, s);
+    if (lane == 0) delta[row] = x;
+}
+
+}  // namespace
+
+cudaError_t launch_lognorm(const LayerArgs& p, cudaStream_t s) {
+    dim3 grid((p.T + kPrepThreads - 1) / kPrepThreads, p.H);
+    before_launch(SAF_KERNEL_LOGNORM, s);
+    lognorm_kernel<<<grid, kPrepThreads, 0, s>>>(p.a, p.r, p.ld_prior, p.mask, p.T, p.lz, p.hflag, p.status);
+    after_launch(SAF_KERNEL_LOGNORM, s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_delta(const LayerArgs& p, bool bf16, cudaStream_t s) {
+    const long long rows = (long long)p.B * p.H * p.T;
+    const unsigned blocks = (unsigned)((rows + 7) / 8);
+    before_launch(SAF_KERNEL_BWD_DELTA, s);
+    if (bf16)
+        bwd_delta_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
+            (const __nv_bfloat16*)p.o, (const __nv_bfloat16*)p.dO, p.delta, rows);
+    else
+        bwd_delta_kernel<float><<<blocks, 256, 0, s>>>((const float*)p.o, (const float*)p.dO, p.delta, rows);
+    after_launch(SAF_KERNEL_BWD_DELTA, s);
+    return cudaGetLastError();
+}
+
+}  // namespace saf

@@ -1,0 +1,242 @@
+// Host entry points of the C ABI declared in include/saf.h: argument
+// validation, workspace carving, and the launch sequence of each pass.
+#include <string.h>
+
+#include "saf_internal.h"
+
+namespace saf {
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+WorkspaceLayout workspace_layout(int B, int H, int T, int backward) {
+    WorkspaceLayout L;
+    size_t off = 0;
+    L.status = off;
+    off += kStatusBytes;
+    L.lz = off;
+    off = align_up(off + (size_t)H * T * sizeof(float), 256);
+    L.hflag = off;
+    off = align_up(off + (size_t)H * sizeof(uint32_t), 256);
+    if (backward) {
+        L.delta = off;
+        off = align_up(off + (size_t)B * H * T * sizeof(float), 256);
+    }
+    L.total = off;
+    return L;
+}
+
+namespace {
+constexpr int kNumKernelIds = SAF_KERNEL_BWD + 1;
+cudaEvent_t g_trace_start[kNumKernelIds] = {};
+cudaEvent_t g_trace_stop[kNumKernelIds] = {};
+unsigned long long g_launches = 0;
+}  // namespace
+
+void before_launch(int kernel, cudaStream_t s) {
+    ++g_launches;
+    if (g_trace_start[kernel]) cudaEventRecord(g_trace_start[kernel], s);
+}
+
+void after_launch(int kernel, cudaStream_t s) {
+    if (g_trace_stop[kernel]) cudaEventRecord(g_trace_stop[kernel], s);
+}
+
+namespace {
+
+int g_device_ok = -1;  // cached: 1 = sm_103 device present, 0 = not
+
+int check_device() {
+    if (g_device_ok >= 0) return g_device_ok ? SAF_OK : SAF_EUNSUPPORTED;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SAF_ECUDA;
+    }
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SAF_ECUDA;
+    }
+    g_device_ok = (prop.major == 10 && prop.minor == 3) ? 1 : 0;
+    return g_device_ok ? SAF_OK : SAF_EUNSUPPORTED;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+struct Common {
+    HeadMask mask;
+    int nfrozen;
+};
+
+// Shape, pointer and workspace checks shared by both passes.
+int validate(const void* q, const void* k, const void* v, const float* a, const float* r, int ld_prior,
+             const uint8_t* frozen, int B, int H, int T, int d, saf_dtype_t dt, void* workspace,
+             size_t ws_bytes, int backward, Common* c) {
+    if (B < 0 || H <= 0 || T < 0) return SAF_EINVAL;
+    if (H > SAF_MAX_HEADS) return SAF_EINVAL;
+    if (dt != SAF_BF16 && dt != SAF_FP32) return SAF_EINVAL;
+    if (d != kHeadDim) return SAF_EUNSUPPORTED;
+    if ((long long)B * H * T * d > (1ll << 40)) return SAF_EINVAL;
+    memset(c, 0, sizeof(*c));
+    for (int h = 0; h < H; ++h) {
+        if (frozen && frozen[h]) {
+            c->mask.w[h >> 6] |= 1ull << (h & 63);
+            c->nfrozen++;
+        }
+    }
+    if (B == 0 || T == 0) return SAF_OK;  // empty call: nothing to check further
+    if (!v) return SAF_EINVAL;
+    if (c->nfrozen < H && (!q || !k)) return SAF_EINVAL;
+    if (c->nfrozen > 0 && (!a || !r || ld_prior < T)) return SAF_EINVAL;
+    if (!aligned16(v) || (q && !aligned16(q)) || (k && !aligned16(k))) return SAF_EALIGN;
+    if ((a && ((uintptr_t)a & 3u)) || (r && ((uintptr_t)r & 3u))) return SAF_EALIGN;
+    if (!workspace) return SAF_EWORKSPACE;
+    if (((uintptr_t)workspace & 255u) != 0) return SAF_EALIGN;
+    if (ws_bytes < workspace_layout(B, H, T, backward).total) return SAF_EWORKSPACE;
+    return SAF_OK;
+}
+
+LayerArgs make_args(const void* q, const void* k, const void* v, const float* a, const float* r, int ld_prior,
+                    int B, int H, int T, const Common& c, void* workspace, int backward) {
+    LayerArgs p;
+    memset(&p, 0, sizeof(p));
+    const WorkspaceLayout L = workspace_layout(B, H, T, backward);
+    char* ws = (char*)workspace;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.a = a;
+    p.r = r;
+    p.B = B;
+    p.H = H;
+    p.T = T;
+    p.ld_prior = ld_prior;
+    p.mask = c.mask;
+    p.status = (uint32_t*)(ws + L.status);
+    p.lz = (float*)(ws + L.lz);
+    p.hflag = (uint32_t*)(ws + L.hflag);
+    p.delta = backward ? (float*)(ws + L.delta) : nullptr;
+    return p;
+}
+
+int launch_status(cudaError_t e) {
+    if (e == cudaSuccess) return SAF_OK;
+    cudaGetLastError();
+    return SAF_ELAUNCH;
+}
+
+// Clear the error words and per-head flags, then compute log Z of the frozen heads.
+cudaError_t begin_call(const LayerArgs& p, const Common& c, cudaStream_t s) {
+    const WorkspaceLayout L = workspace_layout(p.B, p.H, p.T, 0);
+    cudaError_t e = cudaMemsetAsync(p.status, 0, kStatusBytes, s);
+    if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(p.hflag, 0, L.total - L.hflag, s);
+    if (e != cudaSuccess) return e;
+    if (c.nfrozen > 0) return launch_lognorm(p, s);
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace saf
+
+using namespace saf;
+
+extern "C" {
+
+int saf_version(void) { return 100; }
+
+int saf_set_trace_events(int kernel, void* start, void* stop) {
+    if (kernel < SAF_KERNEL_NONE || kernel > SAF_KERNEL_BWD) return SAF_EINVAL;
+    if (kernel == SAF_KERNEL_NONE) {
+        for (int i = 0; i < kNumKernelIds; ++i) g_trace_start[i] = g_trace_stop[i] = nullptr;
+        return SAF_OK;
+    }
+    const bool on = start && stop;
+    g_trace_start[kernel] = on ? (cudaEvent_t)start : nullptr;
+    g_trace_stop[kernel] = on ? (cudaEvent_t)stop : nullptr;
+    return SAF_OK;
+}
+
+unsigned long long saf_launch_count(void) { return g_launches; }
+
+size_t saf_attn_workspace_bytes(int B, int H, int T, int d, saf_dtype_t dt, int backward) {
+    if (B < 0 || H <= 0 || T < 0 || H > SAF_MAX_HEADS || d != kHeadDim) return 0;
+    if (dt != SAF_BF16 && dt != SAF_FP32) return 0;
+    return workspace_layout(B, H, T, backward ? 1 : 0).total;
+}
+
+int saf_attn_fwd(const void* q, const void* k, const void* v, const float* a, const float* r, int ld_prior,
+                 const uint8_t* frozen, int B, int H, int T, int d, saf_dtype_t dt, void* o, float* lse,
+                 void* workspace, size_t ws_bytes, void* stream) {
+    Common c;
+    int st = validate(q, k, v, a, r, ld_prior, frozen, B, H, T, d, dt, workspace, ws_bytes, 0, &c);
+    if (st != SAF_OK) return st;
+    if (B == 0 || T == 0) return SAF_OK;
+    if (!o || !lse) return SAF_EINVAL;
+    if (!aligned16(o) || !aligned16(lse)) return SAF_EALIGN;
+    if ((st = check_device()) != SAF_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    LayerArgs p = make_args(q, k, v, a, r, ld_prior, B, H, T, c, workspace, 0);
+    p.out = o;
+    p.lse_out = lse;
+    const bool bf16 = dt == SAF_BF16;
+    cudaError_t e = begin_call(p, c, s);
+    if (e == cudaSuccess) e = launch_simt_fwd(p, bf16, s);
+    return launch_status(e);
+}
+
+int saf_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                 const float* a, const float* r, int ld_prior, const uint8_t* frozen, int B, int H, int T, int d,
+                 saf_dtype_t dt, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes, void* stream) {
+    Common c;
+    int st = validate(q, k, v, a, r, ld_prior, frozen, B, H, T, d, dt, workspace, ws_bytes, 1, &c);
+    if (st != SAF_OK) return st;
+    if (B == 0 || T == 0) return SAF_OK;
+    if (!o || !dO || !lse || !dq || !dk || !dv) return SAF_EINVAL;
+    if (!aligned16(o) || !aligned16(dO) || !aligned16(lse) || !aligned16(dq) || !aligned16(dk) ||
+        !aligned16(dv))
+        return SAF_EALIGN;
+    if ((st = check_device()) != SAF_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    LayerArgs p = make_args(q, k, v, a, r, ld_prior, B, H, T, c, workspace, 1);
+    p.o = o;
+    p.dO = dO;
+    p.lse = lse;
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    const bool bf16 = dt == SAF_BF16;
+    cudaError_t e = begin_call(p, c, s);
+    if (e == cudaSuccess && c.nfrozen < H) e = launch_bwd_delta(p, bf16, s);
+    if (e == cudaSuccess) e = launch_simt_bwd(p, bf16, s);
+    return launch_status(e);
+}
+
+int saf_device_status(const void* workspace, void* stream) {
+    if (!workspace) return SAF_EWORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    uint32_t words[2] = {0, 0};
+    if (cudaMemcpyAsync(words, workspace, sizeof(words), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return SAF_ECUDA;
+    }
+    if (words[0] & kStatusTimeout) return SAF_ETIMEOUT;
+    return SAF_OK;
+}
+
+const char* saf_error_string(int status) {
+    switch (status) {
+        case SAF_OK: return "ok";
+        case SAF_EINVAL: return "invalid argument (null pointer, bad shape, ld_prior < T or too many heads)";
+        case SAF_EALIGN: return "misaligned pointer (tensors need 16-byte, workspace 256-byte alignment)";
+        case SAF_EUNSUPPORTED: return "unsupported device, head dimension or dtype";
+        case SAF_ELAUNCH: return "kernel launch or asynchronous CUDA call failed";
+        case SAF_EWORKSPACE: return "workspace missing or smaller than saf_attn_workspace_bytes";
+        case SAF_ETIMEOUT: return "a bounded device wait expired";
+        case SAF_ECUDA: return "CUDA runtime error";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

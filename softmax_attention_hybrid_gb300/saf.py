@@ -1,0 +1,187 @@
+"""Thin Python binding of the C ABI in include/saf.h (ctypes).
+
+The functions here have the C names and only marshal arguments: torch CUDA
+tensors become device pointers, the current torch stream becomes the
+cudaStream_t, and a nonzero status becomes SafError. Every step of the layer
+runs in the CUDA library; if libsaf.so is missing, importing this module
+raises instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libsaf.so")
+
+SAF_BF16 = 0
+SAF_FP32 = 1
+
+SAF_OK = 0
+SAF_EINVAL = -1
+SAF_EALIGN = -2
+SAF_EUNSUPPORTED = -3
+SAF_ELAUNCH = -4
+SAF_EWORKSPACE = -5
+SAF_ETIMEOUT = -6
+SAF_ECUDA = -8
+
+# Every symbol that include/saf.h declares.
+EXPORTED = ("saf_attn_workspace_bytes", "saf_attn_fwd", "saf_attn_bwd", "saf_device_status",
+            "saf_error_string", "saf_version", "saf_set_trace_events", "saf_launch_count")
+
+SAF_KERNEL_NONE = 0
+SAF_KERNEL_LOGNORM = 1
+SAF_KERNEL_FWD = 2
+SAF_KERNEL_BWD_DELTA = 3
+SAF_KERNEL_BWD_KV = 4
+SAF_KERNEL_BWD_Q = 5
+SAF_KERNEL_BWD = 6
+
+
+class SafError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status} ({_lib.saf_error_string(status).decode()})")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          "`python -m softmax_attention_hybrid_gb300.build_lib`")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.saf_attn_workspace_bytes.argtypes = [i, i, i, i, i, i]
+    lib.saf_attn_workspace_bytes.restype = sz
+    lib.saf_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, vp, vp, vp, sz, vp]
+    lib.saf_attn_fwd.restype = i
+    lib.saf_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, vp, vp, vp, vp, sz, vp]
+    lib.saf_attn_bwd.restype = i
+    lib.saf_device_status.argtypes = [vp, vp]
+    lib.saf_device_status.restype = i
+    lib.saf_error_string.argtypes = [i]
+    lib.saf_error_string.restype = ctypes.c_char_p
+    lib.saf_version.argtypes = []
+    lib.saf_version.restype = i
+    lib.saf_set_trace_events.argtypes = [i, vp, vp]
+    lib.saf_set_trace_events.restype = i
+    lib.saf_launch_count.argtypes = []
+    lib.saf_launch_count.restype = ctypes.c_ulonglong
+    return lib
+
+
+_lib = _load()
+
+
+def library():
+    """The loaded ctypes handle of libsaf.so."""
+    return _lib
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return SAF_BF16
+    if t.dtype == torch.float32:
+        return SAF_FP32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _frozen_bytes(frozen, H):
+    if frozen is None:
+        return None
+    vals = [1 if int(x) else 0 for x in (frozen.tolist() if torch.is_tensor(frozen) else frozen)]
+    if len(vals) != H:
+        raise ValueError("frozen mask must have H entries")
+    return (ctypes.c_uint8 * H)(*vals)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def saf_error_string(status: int) -> str:
+    return _lib.saf_error_string(int(status)).decode()
+
+
+def saf_version() -> int:
+    return _lib.saf_version()
+
+
+def saf_attn_workspace_bytes(B, H, T, d, dtype, backward) -> int:
+    dt = SAF_BF16 if dtype in (torch.bfloat16, SAF_BF16, "bf16") else SAF_FP32
+    return int(_lib.saf_attn_workspace_bytes(int(B), int(H), int(T), int(d), dt, 1 if backward else 0))
+
+
+def alloc_workspace(B, H, T, d, dtype, backward, device="cuda"):
+    """A workspace buffer for saf_attn_fwd / saf_attn_bwd (256-byte aligned by torch)."""
+    n = saf_attn_workspace_bytes(B, H, T, d, dtype, backward)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def saf_attn_fwd(q, k, v, a, r, frozen, o=None, lse=None, workspace=None, stream=None):
+    """Forward pass; returns (o, lse). q, k, v: [B, H, T, d] CUDA tensors;
+    a, r: [H, ld_prior] fp32 CUDA tensors (or None when nothing is frozen);
+    frozen: H flags (list or tensor, read on the host)."""
+    B, H, T, d = v.shape
+    if o is None:
+        o = torch.empty_like(v)
+    if lse is None:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=v.device)
+    if workspace is None:
+        workspace = alloc_workspace(B, H, T, d, v.dtype, False, v.device)
+    ld = a.shape[1] if a is not None else T
+    st = _lib.saf_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(r), int(ld), _frozen_bytes(frozen, H),
+                           B, H, T, d, _dt(v), _ptr(o), _ptr(lse), _ptr(workspace), workspace.numel(),
+                           _stream(stream))
+    if st != SAF_OK:
+        raise SafError(st, "saf_attn_fwd")
+    return o, lse
+
+
+def saf_attn_bwd(q, k, v, o, do, lse, a, r, frozen, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward pass; returns (dq, dk, dv)."""
+    B, H, T, d = v.shape
+    dq = torch.empty_like(v) if dq is None else dq
+    dk = torch.empty_like(v) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = alloc_workspace(B, H, T, d, v.dtype, True, v.device)
+    ld = a.shape[1] if a is not None else T
+    st = _lib.saf_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(a), _ptr(r), int(ld),
+                           _frozen_bytes(frozen, H), B, H, T, d, _dt(v), _ptr(dq), _ptr(dk), _ptr(dv),
+                           _ptr(workspace), workspace.numel(), _stream(stream))
+    if st != SAF_OK:
+        raise SafError(st, "saf_attn_bwd")
+    return dq, dk, dv
+
+
+def saf_set_trace_events(kernel: int, start=None, stop=None) -> None:
+    """Record torch.cuda.Event `start`/`stop` around every launch of `kernel`
+    (a SAF_KERNEL_* id) from now on; kernel 0 or None events switch it off."""
+    sp = ctypes.c_void_p(start.cuda_event) if start is not None else None
+    ep = ctypes.c_void_p(stop.cuda_event) if stop is not None else None
+    st = _lib.saf_set_trace_events(int(kernel), sp, ep)
+    if st != SAF_OK:
+        raise SafError(st, "saf_set_trace_events")
+
+
+def saf_launch_count() -> int:
+    return int(_lib.saf_launch_count())
+
+
+def saf_device_status(workspace, stream=None) -> int:
+    return int(_lib.saf_device_status(_ptr(workspace), _stream(stream)))

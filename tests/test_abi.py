@@ -1,0 +1,125 @@
+"""Host-side checks of the C ABI: the library loads, exports every symbol the
+header declares, sizes its workspace, and rejects bad arguments before any
+device work. No kernel runs here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "saf.h")
+
+
+@pytest.fixture(scope="module")
+def saf():
+    from softmax_attention_hybrid_gb300 import build_lib
+    if not os.path.exists(build_lib.LIB):
+        build_lib.build()
+    from softmax_attention_hybrid_gb300 import saf as mod
+    return mod
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(saf_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    names = _declared_functions()
+    assert {"saf_attn_fwd", "saf_attn_bwd", "saf_attn_workspace_bytes", "saf_device_status",
+            "saf_error_string"} <= set(names)
+
+
+def test_library_exports_every_declared_symbol(saf):
+    lib = saf.library()
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    assert set(_declared_functions()) == set(saf.EXPORTED)
+
+
+def test_version_and_error_strings(saf):
+    assert saf.saf_version() >= 100
+    for st in (0, -1, -2, -3, -4, -5, -6, -8, -99):
+        s = saf.saf_error_string(st)
+        assert isinstance(s, str) and s
+
+
+def test_workspace_bytes(saf):
+    f = saf.saf_attn_workspace_bytes
+    assert f(8, 12, 4096, 64, "bf16", 0) > 0
+    assert f(8, 12, 4096, 64, "bf16", 1) > f(8, 12, 4096, 64, "bf16", 0)
+    assert f(8, 12, 4096, 64, "bf16", 1) % 256 == 0
+    assert f(1, 4, 256, 32, "bf16", 0) == 0        # unsupported d
+    assert f(1, 0, 256, 64, "bf16", 0) == 0        # no heads
+    assert f(1, 300, 256, 64, "bf16", 0) == 0      # more than SAF_MAX_HEADS
+    assert f(0, 4, 0, 64, "fp32", 1) > 0           # empty call still has the status words
+
+
+FAKE = 0x10000  # 64 KiB-aligned fake device address: the calls below must fail before any access
+
+
+def _fwd(lib, **kw):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, a=FAKE, r=FAKE, ld=256, frozen=None, B=1, H=4, T=256, d=64, dt=0,
+                o=FAKE, lse=FAKE, ws=FAKE, wsb=1 << 30, stream=None)
+    args.update(kw)
+    fz = args["frozen"]
+    fzp = (ctypes.c_uint8 * len(fz))(*fz) if fz is not None else None
+    return lib.saf_attn_fwd(args["q"], args["k"], args["v"], args["a"], args["r"], args["ld"], fzp, args["B"],
+                            args["H"], args["T"], args["d"], args["dt"], args["o"], args["lse"], args["ws"],
+                            args["wsb"], args["stream"])
+
+
+def test_argument_errors_return_before_device_work(saf):
+    lib = saf.library()
+    assert _fwd(lib, H=0) == saf.SAF_EINVAL
+    assert _fwd(lib, B=-1) == saf.SAF_EINVAL
+    assert _fwd(lib, H=257, frozen=None) == saf.SAF_EINVAL
+    assert _fwd(lib, d=128) == saf.SAF_EUNSUPPORTED
+    assert _fwd(lib, dt=7) == saf.SAF_EINVAL
+    assert _fwd(lib, v=None) == saf.SAF_EINVAL
+    assert _fwd(lib, q=None) == saf.SAF_EINVAL                           # ordinary heads need q
+    assert _fwd(lib, frozen=[1, 1, 1, 1], q=None, k=None, ws=None) == saf.SAF_EWORKSPACE  # q, k unused
+    assert _fwd(lib, frozen=[0, 1, 0, 0], a=None) == saf.SAF_EINVAL      # frozen heads need a, r
+    assert _fwd(lib, frozen=[0, 1, 0, 0], ld=255) == saf.SAF_EINVAL      # ld_prior < T
+    assert _fwd(lib, v=FAKE + 8) == saf.SAF_EALIGN
+    assert _fwd(lib, ws=FAKE + 16) == saf.SAF_EALIGN
+    assert _fwd(lib, ws=None) == saf.SAF_EWORKSPACE
+    assert _fwd(lib, wsb=16) == saf.SAF_EWORKSPACE
+
+
+def test_empty_call_is_a_no_op(saf):
+    lib = saf.library()
+    assert _fwd(lib, T=0, q=None, k=None, v=None, o=None, lse=None, ws=None) == saf.SAF_OK
+    assert _fwd(lib, B=0, q=None, k=None, v=None, o=None, lse=None, ws=None) == saf.SAF_OK
+
+
+def test_bwd_argument_errors(saf):
+    lib = saf.library()
+    F = FAKE
+
+    def bwd(**kw):
+        a = dict(q=F, k=F, v=F, o=F, do=F, lse=F, a=F, r=F, ld=256, B=1, H=4, T=256, d=64, dt=0,
+                 dq=F, dk=F, dv=F, ws=F, wsb=1 << 30)
+        a.update(kw)
+        return lib.saf_attn_bwd(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["a"], a["r"], a["ld"],
+                                None, a["B"], a["H"], a["T"], a["d"], a["dt"], a["dq"], a["dk"], a["dv"],
+                                a["ws"], a["wsb"], None)
+
+    assert bwd(dq=None) == saf.SAF_EINVAL
+    assert bwd(do=F + 4) == saf.SAF_EALIGN
+    assert bwd(wsb=1024) == saf.SAF_EWORKSPACE
+    assert bwd(T=0) == saf.SAF_OK
+
+
+def test_device_status_rejects_null(saf):
+    assert saf.library().saf_device_status(None, None) == saf.SAF_EWORKSPACE
+
+
+def test_no_device_is_reported_not_faked(saf):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # every argument valid: the call reaches the device check and must fail there
+    assert _fwd(saf.library()) in (saf.SAF_ECUDA, saf.SAF_EUNSUPPORTED)

@@ -194,13 +194,15 @@ def test_ordinary_matches_torch_sdpa():
     want = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True).numpy()
     o, lse = oracle.attn_fwd(q.numpy(), k.numpy(), v.numpy(), np.zeros((H, T)), np.zeros((H, T)),
                              [0] * H)
-    assert np.max(np.abs(o - want)) < 1e-13
+    assert np.max(np.abs(o - want)) < 1e-13, np.max(np.abs(o - want))
     S = (q @ k.transpose(-1, -2)) / math.sqrt(d)
     S = S.masked_fill(torch.ones(T, T, dtype=torch.bool).triu(1), float("-inf"))
-    assert np.max(np.abs(lse - torch.logsumexp(S, dim=-1).numpy())) < 1e-12
+    e = np.max(np.abs(lse - torch.logsumexp(S, dim=-1).numpy()))
+    assert e < 1e-12, e
     # the dense pattern itself: A V reproduces the library output, rows are stochastic
     A = oracle.ordinary_pattern(q[0, 1].numpy(), k[0, 1].numpy())
-    assert np.max(np.abs(A @ v[0, 1].numpy() - want[0, 1])) < 1e-13
+    e = np.max(np.abs(A @ v[0, 1].numpy() - want[0, 1]))
+    assert e < 1e-13, e
     assert np.all(np.triu(A, 1) == 0.0) and np.max(np.abs(A.sum(1) - 1)) < 1e-13
 
 
