@@ -293,7 +293,7 @@ def run_ours(args, w):
                 try:
                     vals = [s.elapsed_time(e) for s, e in kev[nm]]
                     kms[nm] = sum(vals) / len(vals)
-                except RuntimeError:   # kernel not launched on this path
+                except (RuntimeError, ValueError):   # kernel not launched on this path
                     pass
         return ms, kms, launches
 
