@@ -291,11 +291,12 @@ def run_ours(args, w):
         kms = {}
         for nm in kernels:
             if trace:
-                try:
-                    vals = [s.elapsed_time(e) for s, e in kev[nm]]
-                    kms[nm] = sum(vals) / len(vals)
-                except (RuntimeError, ValueError):   # kernel not launched on this path
-                    pass
+                # a kernel this path never launches keeps the events' creation
+                # records, which precede the step's start event
+                if evs[0][0].elapsed_time(kev[nm][0][0]) < 0:
+                    continue
+                vals = [s.elapsed_time(e) for s, e in kev[nm]]
+                kms[nm] = sum(vals) / len(vals)
         return ms, kms, launches
 
     for _ in range(args.warmup):
