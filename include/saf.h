@@ -76,7 +76,9 @@ typedef enum {
     SAF_ELAUNCH = -4,       /* a kernel launch or an async CUDA call failed               */
     SAF_EWORKSPACE = -5,    /* workspace NULL or smaller than saf_attn_workspace_bytes    */
     SAF_ETIMEOUT = -6,      /* a bounded device wait expired (from saf_device_status)    */
-    SAF_ECUDA = -8          /* a CUDA runtime query failed (no device, driver error)    */
+    SAF_ECUDA = -8,         /* a CUDA runtime query failed (no device, driver error)    */
+    SAF_ESCRATCH = -9       /* saf_attn_fwd_noalloc: the problem needs more workspace
+                               than its fixed device scratch holds                     */
 } saf_status_t;
 
 /* Bytes of device workspace that saf_attn_fwd (backward = 0) or
@@ -100,6 +102,37 @@ SAF_API int saf_attn_fwd(const void* q, const void* k, const void* v,
                  int B, int H, int T, int d, saf_dtype_t dt,
                  void* o, float* lse,
                  void* workspace, size_t ws_bytes, void* stream);
+
+/* Forward pass for callers that cannot allocate device memory.
+ *
+ * The paper has no counterpart to this entry point; it exists for callers
+ * that cannot hand the library a workspace: code that runs where
+ * cudaMalloc is not allowed (for example inside a framework that owns every
+ * allocation and passes plugins only their input and output buffers, or in
+ * a context where allocating could deadlock or fragment a caching
+ * allocator). It computes exactly what saf_attn_fwd computes, with the same
+ * kernels, arguments and outputs, but takes its workspace from a fixed
+ * array of 8 MiB in device memory that the library declares statically;
+ * every GPU that loads the library holds that array until the process
+ * exits. It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ *  - Size limit: saf_attn_workspace_bytes(B, H, T, d, dt, 0) must be at most
+ *    8 MiB (about H * T <= 2,000,000 for the forward pass); larger problems
+ *    return SAF_ESCRATCH and enqueue nothing.
+ *  - Set-up: the first call on each device looks up the array's device
+ *    address (cudaGetSymbolAddress, with that device current) and caches
+ *    it. Make that first call before any stream capture begins.
+ *  - Sharing: every call on a device uses the same array, which keeps the
+ *    contents the last call left. Each call clears the parts that must
+ *    start at zero before its kernels run. Calls whose work overlaps on the
+ *    GPU (two streams, or two host threads) race on the array: order them
+ *    on one stream.
+ *  - Device-side status words live in that array and are not reported;
+ *    callers that need saf_device_status use saf_attn_fwd with a workspace. */
+SAF_API int saf_attn_fwd_noalloc(const void* q, const void* k, const void* v,
+                                 const float* a, const float* r, int ld_prior, const uint8_t* frozen,
+                                 int B, int H, int T, int d, saf_dtype_t dt,
+                                 void* o, float* lse, void* stream);
 
 /* Backward pass of the hybrid layer, given dO = dL/dO.
  *

@@ -235,6 +235,7 @@ const char* saf_error_string(int status) {
         case SAF_EWORKSPACE: return "workspace missing or smaller than saf_attn_workspace_bytes";
         case SAF_ETIMEOUT: return "a bounded device wait expired";
         case SAF_ECUDA: return "CUDA runtime error";
+        case SAF_ESCRATCH: return "problem too large for the 8 MiB fixed scratch of saf_attn_fwd_noalloc";
         default: return "unknown status";
     }
 }

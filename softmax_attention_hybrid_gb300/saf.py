@@ -27,10 +27,12 @@ SAF_ELAUNCH = -4
 SAF_EWORKSPACE = -5
 SAF_ETIMEOUT = -6
 SAF_ECUDA = -8
+SAF_ESCRATCH = -9
 
 # Every symbol that include/saf.h declares.
 EXPORTED = ("saf_attn_workspace_bytes", "saf_attn_fwd", "saf_attn_bwd", "saf_device_status",
-            "saf_error_string", "saf_version", "saf_set_trace_events", "saf_launch_count")
+            "saf_error_string", "saf_version", "saf_set_trace_events", "saf_launch_count",
+            "saf_attn_fwd_noalloc")
 
 SAF_KERNEL_NONE = 0
 SAF_KERNEL_LOGNORM = 1
@@ -57,6 +59,8 @@ def _load():
     lib.saf_attn_workspace_bytes.restype = sz
     lib.saf_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, vp, vp, vp, sz, vp]
     lib.saf_attn_fwd.restype = i
+    lib.saf_attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, vp, vp, vp]
+    lib.saf_attn_fwd_noalloc.restype = i
     lib.saf_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, vp, vp, vp, vp, sz, vp]
     lib.saf_attn_bwd.restype = i
     lib.saf_device_status.argtypes = [vp, vp]
@@ -149,6 +153,25 @@ def saf_attn_fwd(q, k, v, a, r, frozen, o=None, lse=None, workspace=None, stream
                            _stream(stream))
     if st != SAF_OK:
         raise SafError(st, "saf_attn_fwd")
+    return o, lse
+
+
+def saf_attn_fwd_noalloc(q, k, v, a, r, frozen, o=None, lse=None, stream=None):
+    """Forward pass without a workspace, for callers that cannot allocate
+    device memory: the library uses its fixed 8 MiB device scratch instead.
+    Same outputs as saf_attn_fwd; raises SafError (SAF_ESCRATCH) when the
+    problem does not fit. Calls on one device share that scratch, so they
+    must be ordered on one stream."""
+    B, H, T, d = v.shape
+    if o is None:
+        o = torch.empty_like(v)
+    if lse is None:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=v.device)
+    ld = a.shape[1] if a is not None else T
+    st = _lib.saf_attn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(r), int(ld), _frozen_bytes(frozen, H),
+                                   B, H, T, d, _dt(v), _ptr(o), _ptr(lse), _stream(stream))
+    if st != SAF_OK:
+        raise SafError(st, "saf_attn_fwd_noalloc")
     return o, lse
 
 
