@@ -1,0 +1,470 @@
+// Fused hybrid forward on the 5th-generation tensor cores (bf16, d = 64).
+//
+// "When Can Attention Heads Be Statically Defined?": ordinary heads run
+// online-softmax attention with FlashAttention-2 tiling (App. A.1 Eqs. 5-7,
+// §3.3); frozen heads rebuild causal tiles of the fixed pattern P-hat of
+// Eq. 3 in registers from a, r and the precomputed normalisers and multiply
+// them with value tiles (§3.3 "Fused computation", App. D.2). One persistent
+// launch runs both kinds of head; a per-item head-state flag picks the path
+// and outputs keep their head order.
+//
+// Work item: (batch b, head h, query-block pair p) = query rows
+// [256p, 256p + 256) as two 128-row tiles that share every K/V tile load.
+// Items are ordered longest first (descending p, ordinary before frozen) and
+// dealt to the persistent CTAs in a snake order.
+//
+// Warp roles (320 threads, one CTA per SM):
+//   warps 0-3 / 4-7 : softmax group g = 0 / 1, thread = one query row of tile g
+//   warp 8          : TMA producer (Q tiles, K/V stages)
+//   warp 9          : tensor-memory owner and single-thread MMA issuer
+// Tensor memory (512 columns), per tile g at column 256g:
+//   [0, 128)   S = Q K^T (fp32)
+//   [128, 192) P or W (bf16 pairs), the A operand of the P V MMA
+//   [192, 256) O accumulator (fp32)
+// Shared memory: Q tiles (2 x 16 KB), kStages K/V stages (32 KB each), and a
+// small staging area per group for the frozen pattern.
+#include <string.h>
+
+#include "saf_internal.h"
+#include "tc_common.cuh"
+
+namespace saf {
+namespace {
+
+using namespace tc;
+
+constexpr int kStages = 3;
+constexpr int kTileBytes = 128 * 64 * 2;  // one 128 x 64 bf16 tile
+constexpr int kThreads = 320;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kScaleLog2 = 0.125f * 1.4426950408889634f;  // log2(e) / sqrt(64)
+constexpr float kRescaleThreshold = 8.0f;                    // lazy rescale: factor 256
+
+struct FwdParams {
+    CUtensorMap tm_q;
+    CUtensorMap tm_k;
+    CUtensorMap tm_v;
+    __nv_bfloat16* o;
+    float* lse;
+    const float* a;
+    const float* r;
+    const float* lz;
+    uint32_t* status;
+    int B, H, T, ld;
+    int nqb, npairs, n_items;
+    int n_ord, n_frz;
+    uint8_t ord_heads[SAF_MAX_HEADS];
+    uint8_t frz_heads[SAF_MAX_HEADS];
+};
+
+struct SmemLayout {
+    static constexpr int q = 0;                                     // 2 tiles
+    static constexpr int kv = q + 2 * kTileBytes;                   // kStages x (K, V)
+    static constexpr int stage_bytes = 2 * kTileBytes;
+    static constexpr int frz = kv + kStages * stage_bytes;          // 2 groups x (a2[128] + band[256]) fp32
+    static constexpr int frz_group_bytes = (128 + 256) * 4;
+    static constexpr int total = frz + 2 * frz_group_bytes;
+};
+
+struct Item {
+    int b, h, pair;
+    bool frozen;
+};
+
+__device__ __forceinline__ Item decode_item(const FwdParams& p, int idx) {
+    Item it;
+    const int per_level = p.B * p.H;
+    const int level = idx / per_level;
+    const int rem = idx - level * per_level;
+    it.pair = p.npairs - 1 - level;
+    const int n_ord_items = p.B * p.n_ord;
+    if (rem < n_ord_items) {
+        it.b = rem / p.n_ord;
+        it.h = p.ord_heads[rem - it.b * p.n_ord];
+        it.frozen = false;
+    } else {
+        const int f = rem - n_ord_items;
+        it.b = f / p.n_frz;
+        it.h = p.frz_heads[f - it.b * p.n_frz];
+        it.frozen = true;
+    }
+    return it;
+}
+
+// The item index handled by CTA `cta` in round `round` (snake order).
+__device__ __forceinline__ int item_index(int round, int cta, int grid) {
+    return round * grid + ((round & 1) ? (grid - 1 - cta) : cta);
+}
+
+// 2^x on the special-function unit (ex2.approx, flushes subnormal results to 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+struct Barriers {
+    uint64_t q_full, q_empty;
+    uint64_t kv_full[kStages], kv_empty[kStages];
+    uint64_t s_full[2], s_empty[2], p_full[2], o_done[2];
+};
+
+__global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ FwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ Barriers bars;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(&bars.q_full, 1);
+        mbar_init(&bars.q_empty, 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bars.kv_full[s], 1);
+            mbar_init(&bars.kv_empty[s], 1);
+        }
+        for (int g = 0; g < 2; ++g) {
+            mbar_init(&bars.s_full[g], 1);
+            mbar_init(&bars.s_empty[g], 4);
+            mbar_init(&bars.p_full[g], 4);
+            mbar_init(&bars.o_done[g], 1);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(&tmem_base_sh, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
+    volatile int* abort = &abort_flag;
+    uint32_t* status = p.status;
+    const int grid = gridDim.x, cta = blockIdx.x;
+
+    if (warp == 8) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&p.tm_q);
+            tma_prefetch_desc(&p.tm_k);
+            tma_prefetch_desc(&p.tm_v);
+            uint32_t q_empty_ph = 1;
+            uint32_t kv_empty_bits = (1u << kStages) - 1;   // phase parity per stage, bit s
+            int stage = 0;
+            bool ok = true;
+            for (int round = 0; ok; ++round) {
+                const int idx = item_index(round, cta, grid);
+                if (idx >= p.n_items) break;
+                const Item it = decode_item(p, idx);
+                const int bh = it.b * p.H + it.h;
+                const int qb0 = 2 * it.pair, qb1 = qb0 + 1;
+                const bool t1 = qb1 < p.nqb;
+                const int nblk = t1 ? qb1 + 1 : qb0 + 1;
+                if (!it.frozen) {
+                    if (!(ok = mbar_wait(&bars.q_empty, q_empty_ph, abort, status, kStatusTimeout))) break;
+                    q_empty_ph ^= 1;
+                    mbar_expect_tx(&bars.q_full, (t1 ? 2 : 1) * kTileBytes);
+                    tma_load_3d(sm + SmemLayout::q, &p.tm_q, &bars.q_full, 0, qb0 * 128, bh);
+                    if (t1) tma_load_3d(sm + SmemLayout::q + kTileBytes, &p.tm_q, &bars.q_full, 0, qb1 * 128, bh);
+                }
+                for (int j = 0; j < nblk; ++j) {
+                    if (!(ok = mbar_wait(&bars.kv_empty[stage], (kv_empty_bits >> stage) & 1u, abort, status,
+                                         kStatusTimeout)))
+                        break;
+                    kv_empty_bits ^= 1u << stage;
+                    uint8_t* st = sm + SmemLayout::kv + stage * SmemLayout::stage_bytes;
+                    mbar_expect_tx(&bars.kv_full[stage], (it.frozen ? 1 : 2) * kTileBytes);
+                    if (!it.frozen) tma_load_3d(st, &p.tm_k, &bars.kv_full[stage], 0, j * 128, bh);
+                    tma_load_3d(st + kTileBytes, &p.tm_v, &bars.kv_full[stage], 0, j * 128, bh);
+                    stage = (stage + 1 == kStages) ? 0 : stage + 1;
+                }
+            }
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);  // S = Q K^T
+            const uint32_t idesc_o = idesc_bf16(128, 64, 0, 1);   // O += P V, V MN-major
+            uint32_t q_full_ph = 0;
+            uint32_t kv_full_bits = 0;           // phase parity per stage, bit s
+            uint32_t s_empty_bits = 3u;          // bit g: parity of s_empty[g]
+            uint32_t p_full_bits = 0;            // bit g: parity of p_full[g]
+            int stage = 0;
+            bool ok = true;
+            const uint32_t sq = smem_u32(sm + SmemLayout::q);
+            for (int round = 0; ok; ++round) {
+                const int idx = item_index(round, cta, grid);
+                if (idx >= p.n_items) break;
+                const Item it = decode_item(p, idx);
+                const int qb0 = 2 * it.pair, qb1 = qb0 + 1;
+                const bool t1 = qb1 < p.nqb;
+                const int n0 = qb0 + 1, n1 = t1 ? qb1 + 1 : 0;
+                const int nblk = t1 ? n1 : n0;
+                if (!it.frozen) {
+                    if (!(ok = mbar_wait(&bars.q_full, q_full_ph, abort, status, kStatusTimeout))) break;
+                    q_full_ph ^= 1;
+                }
+                // stage index of block j is (stage + j) mod kStages
+                auto stage_of = [&](int j) { return (stage + j) % kStages; };
+                auto issue_s = [&](int g, int j) -> bool {
+                    if (!mbar_wait(&bars.s_empty[g], (s_empty_bits >> g) & 1u, abort, status, kStatusTimeout))
+                        return false;
+                    s_empty_bits ^= 1u << g;
+                    tc_fence_after();
+                    const uint32_t sk = smem_u32(sm + SmemLayout::kv + stage_of(j) * SmemLayout::stage_bytes);
+                    const uint32_t sqg = sq + g * kTileBytes;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_ss(tmem + 256 * g, sdesc_sw128(sqg + 32 * k, 16, 1024),
+                               sdesc_sw128(sk + 32 * k, 16, 1024), idesc_s, k > 0);
+                    mma_commit(&bars.s_full[g]);
+                    return true;
+                };
+                auto issue_pv = [&](int g, int j) -> bool {
+                    if (!mbar_wait(&bars.p_full[g], (p_full_bits >> g) & 1u, abort, status, kStatusTimeout))
+                        return false;
+                    p_full_bits ^= 1u << g;
+                    tc_fence_after();
+                    const uint32_t sv =
+                        smem_u32(sm + SmemLayout::kv + stage_of(j) * SmemLayout::stage_bytes + kTileBytes);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        mma_ts(tmem + 256 * g + 192, tmem + 256 * g + 128 + 8 * k,
+                               sdesc_sw128(sv + 2048 * k, 16384, 1024), idesc_o, (j > 0 || k > 0) ? 1u : 0u);
+                    mma_commit(&bars.o_done[g]);
+                    return true;
+                };
+                auto wait_kv = [&](int j) -> bool {
+                    const int s = stage_of(j);
+                    if (!mbar_wait(&bars.kv_full[s], (kv_full_bits >> s) & 1u, abort, status, kStatusTimeout))
+                        return false;
+                    kv_full_bits ^= 1u << s;
+                    return true;
+                };
+                if (!(ok = wait_kv(0))) break;
+                if (!it.frozen) {
+                    ok = issue_s(0, 0);
+                    if (ok && n1 > 0) ok = issue_s(1, 0);
+                }
+                // Per block j: P V of tile 0, then the next block's S of tile 0 (so that
+                // tile 0's softmax overlaps tile 1's MMAs), then the same for tile 1.
+                for (int j = 0; j < nblk && ok; ++j) {
+                    const bool more = j + 1 < nblk;
+                    if (j < n0) ok = issue_pv(0, j);
+                    if (ok && more) ok = wait_kv(j + 1);
+                    if (ok && more && !it.frozen && j + 1 < n0) ok = issue_s(0, j + 1);
+                    if (ok && j < n1) ok = issue_pv(1, j);
+                    if (ok && more && !it.frozen && j + 1 < n1) ok = issue_s(1, j + 1);
+                    if (!ok) break;
+                    mma_commit(&bars.kv_empty[stage_of(j)]);
+                }
+                if (!ok) break;
+                if (!it.frozen) mma_commit(&bars.q_empty);
+                stage = stage_of(nblk);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ softmax groups
+        const int g = warp >> 2;               // 0 or 1
+        const int r = threadIdx.x & 127;       // row within the tile = TMEM lane
+        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16) + 256 * g;
+        float* a2s = reinterpret_cast<float*>(sm + SmemLayout::frz + g * SmemLayout::frz_group_bytes);
+        float* band = a2s + 128;
+        uint32_t s_full_ph = 0, o_done_ph = 0;
+        bool ok = true;
+        for (int round = 0; ok; ++round) {
+            const int idx = item_index(round, cta, grid);
+            if (idx >= p.n_items) break;
+            const Item it = decode_item(p, idx);
+            const int qb = 2 * it.pair + g;
+            if (qb >= p.nqb) continue;
+            const int bh = it.b * p.H + it.h;
+            const int row = qb * 128 + r;
+            const int nblk = qb + 1;
+            float m_used = -INFINITY, l = 0.f;
+            float lz2 = INFINITY;
+            const float* ah = p.a + (size_t)it.h * p.ld;
+            const float* rh = p.r + (size_t)it.h * p.ld;
+            if (it.frozen && row < p.T) lz2 = p.lz[(size_t)it.h * p.T + row] * kLog2e;
+            for (int j = 0; j < nblk && ok; ++j) {
+                if (!it.frozen) {
+                    if (!(ok = mbar_wait(&bars.s_full[g], s_full_ph, abort, status, kStatusTimeout))) break;
+                    s_full_ph ^= 1;
+                    tc_fence_after();
+                    uint32_t sr[128];   // this row of S, then of log2-scaled scores
+#pragma unroll
+                    for (int c0 = 0; c0 < 128; c0 += 32) tmem_ld32(lane_base + c0, sr + c0);
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars.s_empty[g]);
+                    const bool diag = (j == qb);
+                    float mx = -INFINITY;
+#pragma unroll
+                    for (int c = 0; c < 128; ++c) {
+                        float x = __uint_as_float(sr[c]) * kScaleLog2;
+                        if (diag && c > r) x = -INFINITY;   // causal mask on the diagonal tile
+                        sr[c] = __float_as_uint(x);
+                        mx = fmaxf(mx, x);
+                    }
+                    if (j > 0) {   // P V of the previous block done: P is free, O is stable
+                        if (!(ok = mbar_wait(&bars.o_done[g], o_done_ph, abort, status, kStatusTimeout))) break;
+                        o_done_ph ^= 1;
+                        tc_fence_after();
+                    }
+                    const float m_new = fmaxf(m_used, mx);
+                    const bool need = m_new > m_used + kRescaleThreshold;
+                    if (j > 0 && __any_sync(0xffffffffu, need)) {
+                        const float f = need ? fast_exp2(m_used - m_new) : 1.f;
+                        uint32_t ov[16];
+#pragma unroll
+                        for (int c0 = 0; c0 < 64; c0 += 16) {
+                            tmem_ld16(lane_base + 192 + c0, ov);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int c = 0; c < 16; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * f);
+                            tmem_st16(lane_base + 192 + c0, ov);
+                        }
+                    }
+                    if (need) {
+                        l *= fast_exp2(m_used - m_new);
+                        m_used = m_new;
+                    }
+                    float ls = 0.f;
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        uint32_t pk[32];   // packed bf16 pairs of 64 columns of P
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            const float p0 = fast_exp2(__uint_as_float(sr[64 * h2 + 2 * c]) - m_used);
+                            const float p1 = fast_exp2(__uint_as_float(sr[64 * h2 + 2 * c + 1]) - m_used);
+                            ls += p0 + p1;
+                            pk[c] = pack_bf16(p0, p1);
+                        }
+                        tmem_st32(lane_base + 128 + 32 * h2, pk);
+                    }
+                    l += ls;
+                } else {
+                    // Frozen tile: W(i, k) = exp(a[k] + r[i - k] - log Z(i)) (Eq. 3), built from
+                    // the key block's a values and the tile's band of r values in shared memory.
+                    named_bar_sync(1 + g, 128);   // previous block's staging fully read
+                    const int key = j * 128 + r;
+                    a2s[r] = key < p.T ? ah[key] * kLog2e : -INFINITY;
+                    const int d0 = (qb - j) * 128 - 127;  // offset of band[0]
+                    for (int u = r; u < 255; u += 128) {
+                        const int dl = d0 + u;
+                        band[u] = (dl >= 0 && dl < p.T) ? rh[dl] * kLog2e : -INFINITY;
+                    }
+                    named_bar_sync(1 + g, 128);
+                    if (j > 0) {
+                        if (!(ok = mbar_wait(&bars.o_done[g], o_done_ph, abort, status, kStatusTimeout))) break;
+                        o_done_ph ^= 1;
+                        tc_fence_after();
+                    }
+                    const float* bnd = band + r + 127;   // bnd[-c] = r2[i - k]
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        uint32_t pk[32];
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            const int cc = 64 * h2 + 2 * c;
+                            const float w0 = fast_exp2(a2s[cc] + bnd[-cc] - lz2);
+                            const float w1 = fast_exp2(a2s[cc + 1] + bnd[-cc - 1] - lz2);
+                            pk[c] = pack_bf16(w0, w1);
+                        }
+                        tmem_st32(lane_base + 128 + 32 * h2, pk);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars.p_full[g]);
+            }
+            if (!ok) break;
+            // epilogue: O = acc / l (ordinary) or acc (frozen: W rows sum to one)
+            if (!(ok = mbar_wait(&bars.o_done[g], o_done_ph, abort, status, kStatusTimeout))) break;
+            o_done_ph ^= 1;
+            tc_fence_after();
+            uint32_t ov[64];
+            tmem_ld32(lane_base + 192, ov);
+            tmem_ld32(lane_base + 224, ov + 32);
+            tmem_ld_wait();
+            tc_fence_before();
+            if (row < p.T) {
+                const float inv = it.frozen ? 1.f : 1.f / l;
+                uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)bh * p.T + row) * 64);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 w;
+                    w.x = pack_bf16(__uint_as_float(ov[8 * c + 0]) * inv, __uint_as_float(ov[8 * c + 1]) * inv);
+                    w.y = pack_bf16(__uint_as_float(ov[8 * c + 2]) * inv, __uint_as_float(ov[8 * c + 3]) * inv);
+                    w.z = pack_bf16(__uint_as_float(ov[8 * c + 4]) * inv, __uint_as_float(ov[8 * c + 5]) * inv);
+                    w.w = pack_bf16(__uint_as_float(ov[8 * c + 6]) * inv, __uint_as_float(ov[8 * c + 7]) * inv);
+                    dst[c] = w;
+                }
+                p.lse[(size_t)bh * p.T + row] = it.frozen ? lz2 / kLog2e : (m_used + log2f(l)) / kLog2e;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_tc_fwd(const LayerArgs& a, cudaStream_t s) {
+    FwdParams p;
+    memset(&p, 0, sizeof(p));
+    const int BH = a.B * a.H;
+    const void* vbase = a.v;
+    const void* qbase = a.q ? a.q : vbase;
+    const void* kbase = a.k ? a.k : vbase;
+    if (!make_tmap_bf16_3d(&p.tm_q, qbase, 64, a.T, BH, 64, 128) ||
+        !make_tmap_bf16_3d(&p.tm_k, kbase, 64, a.T, BH, 64, 128) ||
+        !make_tmap_bf16_3d(&p.tm_v, vbase, 64, a.T, BH, 64, 128))
+        return cudaErrorInvalidValue;
+    p.o = (__nv_bfloat16*)a.out;
+    p.lse = a.lse_out;
+    p.a = a.a;
+    p.r = a.r;
+    p.lz = a.lz;
+    p.status = a.status;
+    p.B = a.B;
+    p.H = a.H;
+    p.T = a.T;
+    p.ld = a.ld_prior;
+    p.nqb = (a.T + 127) / 128;
+    p.npairs = (p.nqb + 1) / 2;
+    p.n_items = a.B * a.H * p.npairs;
+    for (int h = 0; h < a.H; ++h) {
+        if (head_frozen(a.mask, h))
+            p.frz_heads[p.n_frz++] = (uint8_t)h;
+        else
+            p.ord_heads[p.n_ord++] = (uint8_t)h;
+    }
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int smem = SmemLayout::total + 1024;
+    cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int grid = p.n_items < sms ? p.n_items : sms;
+    before_launch(SAF_KERNEL_FWD, s);
+    fwd_tc_kernel<<<grid, kThreads, smem, s>>>(p);
+    after_launch(SAF_KERNEL_FWD, s);
+    return cudaGetLastError();
+}
+
+}  // namespace saf

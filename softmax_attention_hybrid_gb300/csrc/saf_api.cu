@@ -181,7 +181,7 @@ int saf_attn_fwd(const void* q, const void* k, const void* v, const float* a, co
     p.lse_out = lse;
     const bool bf16 = dt == SAF_BF16;
     cudaError_t e = begin_call(p, c, s);
-    if (e == cudaSuccess) e = launch_simt_fwd(p, bf16, s);
+    if (e == cudaSuccess) e = bf16 ? launch_tc_fwd(p, s) : launch_simt_fwd(p, false, s);
     return launch_status(e);
 }
 

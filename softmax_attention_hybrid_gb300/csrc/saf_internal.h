@@ -82,6 +82,9 @@ void after_launch(int kernel, cudaStream_t s);
 cudaError_t launch_lognorm(const LayerArgs& p, cudaStream_t s);
 cudaError_t launch_bwd_delta(const LayerArgs& p, bool bf16, cudaStream_t s);
 
+// fwd_tc.cu: tensor-core forward (bf16)
+cudaError_t launch_tc_fwd(const LayerArgs& p, cudaStream_t s);
+
 // simt.cu: fp32-arithmetic path (any dtype), used for SAF_FP32
 cudaError_t launch_simt_fwd(const LayerArgs& p, bool bf16, cudaStream_t s);
 cudaError_t launch_simt_bwd(const LayerArgs& p, bool bf16, cudaStream_t s);
