@@ -227,11 +227,16 @@ KERNEL_FLOP_UNITS = {
     "bwd_kv": (4, 1),     # S recompute, dV, dP, dK | dV
     "bwd_q": (1, 0),      # dQ (its S and dP recomputes are not counted)
     "bwd": (5, 1),
+    "dq_finish": (0, 0),
+    "bwd_delta": (0, 0),
+    "lognorm": (0, 0),
 }
 
 
-# what bounds each kernel: the fp32 CUDA-core kernels are FMA-bound ("alu")
-KERNEL_BOUND = {"fwd": "alu", "bwd_kv": "alu", "bwd_q": "alu", "bwd": "tensor"}
+# what bounds each kernel: the bf16 kernels are tensor-core contractions,
+# the fp32 CUDA-core kernels are FMA-bound ("alu")
+def kernel_bound(name, dtype):
+    return "tensor" if dtype == "bf16" and name in ("fwd", "bwd") else "alu"
 
 
 def run_ours(args, w):
@@ -260,7 +265,9 @@ def run_ours(args, w):
 
     kernels = {"fwd": saf.SAF_KERNEL_FWD}
     if not w.fwd_only:
-        kernels.update({"bwd_kv": saf.SAF_KERNEL_BWD_KV, "bwd_q": saf.SAF_KERNEL_BWD_Q, "bwd": saf.SAF_KERNEL_BWD})
+        kernels.update({"bwd_kv": saf.SAF_KERNEL_BWD_KV, "bwd_q": saf.SAF_KERNEL_BWD_Q, "bwd": saf.SAF_KERNEL_BWD,
+                        "dq_finish": saf.SAF_KERNEL_DQ_FINISH, "bwd_delta": saf.SAF_KERNEL_BWD_DELTA,
+                        "lognorm": saf.SAF_KERNEL_LOGNORM})
 
     def new_event():
         # torch creates the CUDA event on first record; record once so that
@@ -378,7 +385,7 @@ def run_ours(args, w):
         c = 2 * F.pairs(T) * d
         kflops = B * ((H - w.F) * units_o + w.F * units_f) * c
         achieved = kflops / (kms[name] * 1e-3) / 1e12
-        if KERNEL_BOUND.get(name) == "tensor":
+        if kernel_bound(name, w.dtype) == "tensor":
             peak = peaks["bf16_tflops"]
             bound, note = "tensor", f"bf16 dense, burst, {peak_src}"
         else:

@@ -167,7 +167,8 @@ typedef enum {
     SAF_KERNEL_BWD_DELTA = 3,   /* D_i = sum_c dO_ic O_ic                       */
     SAF_KERNEL_BWD_KV = 4,      /* backward key-block pass (dV, dK)            */
     SAF_KERNEL_BWD_Q = 5,       /* backward query-block pass (dQ)              */
-    SAF_KERNEL_BWD = 6          /* fused backward (dQ, dK, dV in one launch)   */
+    SAF_KERNEL_BWD = 6,         /* fused backward (dQ, dK, dV in one launch)   */
+    SAF_KERNEL_DQ_FINISH = 7    /* dQ accumulator -> dq (scale, dtype, zeros)  */
 } saf_kernel_t;
 
 /* From the next call on, record `start` (a cudaEvent_t as void*) on the

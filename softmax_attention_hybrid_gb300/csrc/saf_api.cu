@@ -8,7 +8,7 @@ namespace saf {
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-WorkspaceLayout workspace_layout(int B, int H, int T, int backward) {
+WorkspaceLayout workspace_layout(int B, int H, int T, int backward, int bf16) {
     WorkspaceLayout L;
     size_t off = 0;
     L.status = off;
@@ -20,13 +20,17 @@ WorkspaceLayout workspace_layout(int B, int H, int T, int backward) {
     if (backward) {
         L.delta = off;
         off = align_up(off + (size_t)B * H * T * sizeof(float), 256);
+        if (bf16) {
+            L.dq_acc = off;
+            off = align_up(off + (size_t)B * H * T * kHeadDim * sizeof(float), 256);
+        }
     }
     L.total = off;
     return L;
 }
 
 namespace {
-constexpr int kNumKernelIds = SAF_KERNEL_BWD + 1;
+constexpr int kNumKernelIds = SAF_KERNEL_DQ_FINISH + 1;
 cudaEvent_t g_trace_start[kNumKernelIds] = {};
 cudaEvent_t g_trace_stop[kNumKernelIds] = {};
 unsigned long long g_launches = 0;
@@ -92,15 +96,15 @@ int validate(const void* q, const void* k, const void* v, const float* a, const 
     if ((a && ((uintptr_t)a & 3u)) || (r && ((uintptr_t)r & 3u))) return SAF_EALIGN;
     if (!workspace) return SAF_EWORKSPACE;
     if (((uintptr_t)workspace & 255u) != 0) return SAF_EALIGN;
-    if (ws_bytes < workspace_layout(B, H, T, backward).total) return SAF_EWORKSPACE;
+    if (ws_bytes < workspace_layout(B, H, T, backward, dt == SAF_BF16).total) return SAF_EWORKSPACE;
     return SAF_OK;
 }
 
 LayerArgs make_args(const void* q, const void* k, const void* v, const float* a, const float* r, int ld_prior,
-                    int B, int H, int T, const Common& c, void* workspace, int backward) {
+                    int B, int H, int T, const Common& c, void* workspace, int backward, int bf16) {
     LayerArgs p;
     memset(&p, 0, sizeof(p));
-    const WorkspaceLayout L = workspace_layout(B, H, T, backward);
+    const WorkspaceLayout L = workspace_layout(B, H, T, backward, bf16);
     char* ws = (char*)workspace;
     p.q = q;
     p.k = k;
@@ -116,6 +120,7 @@ LayerArgs make_args(const void* q, const void* k, const void* v, const float* a,
     p.lz = (float*)(ws + L.lz);
     p.hflag = (uint32_t*)(ws + L.hflag);
     p.delta = backward ? (float*)(ws + L.delta) : nullptr;
+    p.dq_acc = (backward && bf16) ? (float*)(ws + L.dq_acc) : nullptr;
     return p;
 }
 
@@ -127,7 +132,7 @@ int launch_status(cudaError_t e) {
 
 // Clear the error words and per-head flags, then compute log Z of the frozen heads.
 cudaError_t begin_call(const LayerArgs& p, const Common& c, cudaStream_t s) {
-    const WorkspaceLayout L = workspace_layout(p.B, p.H, p.T, 0);
+    const WorkspaceLayout L = workspace_layout(p.B, p.H, p.T, 0, 0);
     cudaError_t e = cudaMemsetAsync(p.status, 0, kStatusBytes, s);
     if (e != cudaSuccess) return e;
     e = cudaMemsetAsync(p.hflag, 0, L.total - L.hflag, s);
@@ -146,7 +151,7 @@ extern "C" {
 int saf_version(void) { return 100; }
 
 int saf_set_trace_events(int kernel, void* start, void* stop) {
-    if (kernel < SAF_KERNEL_NONE || kernel > SAF_KERNEL_BWD) return SAF_EINVAL;
+    if (kernel < SAF_KERNEL_NONE || kernel >= kNumKernelIds) return SAF_EINVAL;
     if (kernel == SAF_KERNEL_NONE) {
         for (int i = 0; i < kNumKernelIds; ++i) g_trace_start[i] = g_trace_stop[i] = nullptr;
         return SAF_OK;
@@ -162,7 +167,7 @@ unsigned long long saf_launch_count(void) { return g_launches; }
 size_t saf_attn_workspace_bytes(int B, int H, int T, int d, saf_dtype_t dt, int backward) {
     if (B < 0 || H <= 0 || T < 0 || H > SAF_MAX_HEADS || d != kHeadDim) return 0;
     if (dt != SAF_BF16 && dt != SAF_FP32) return 0;
-    return workspace_layout(B, H, T, backward ? 1 : 0).total;
+    return workspace_layout(B, H, T, backward ? 1 : 0, dt == SAF_BF16).total;
 }
 
 int saf_attn_fwd(const void* q, const void* k, const void* v, const float* a, const float* r, int ld_prior,
@@ -176,7 +181,7 @@ int saf_attn_fwd(const void* q, const void* k, const void* v, const float* a, co
     if (!aligned16(o) || !aligned16(lse)) return SAF_EALIGN;
     if ((st = check_device()) != SAF_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
-    LayerArgs p = make_args(q, k, v, a, r, ld_prior, B, H, T, c, workspace, 0);
+    LayerArgs p = make_args(q, k, v, a, r, ld_prior, B, H, T, c, workspace, 0, dt == SAF_BF16);
     p.out = o;
     p.lse_out = lse;
     const bool bf16 = dt == SAF_BF16;
@@ -198,7 +203,7 @@ int saf_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
         return SAF_EALIGN;
     if ((st = check_device()) != SAF_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
-    LayerArgs p = make_args(q, k, v, a, r, ld_prior, B, H, T, c, workspace, 1);
+    LayerArgs p = make_args(q, k, v, a, r, ld_prior, B, H, T, c, workspace, 1, dt == SAF_BF16);
     p.o = o;
     p.dO = dO;
     p.lse = lse;
@@ -208,7 +213,7 @@ int saf_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
     const bool bf16 = dt == SAF_BF16;
     cudaError_t e = begin_call(p, c, s);
     if (e == cudaSuccess && c.nfrozen < H) e = launch_bwd_delta(p, bf16, s);
-    if (e == cudaSuccess) e = launch_simt_bwd(p, bf16, s);
+    if (e == cudaSuccess) e = bf16 ? launch_tc_bwd(p, s) : launch_simt_bwd(p, false, s);
     return launch_status(e);
 }
 

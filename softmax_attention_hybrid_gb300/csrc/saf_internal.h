@@ -45,9 +45,10 @@ struct WorkspaceLayout {
     size_t lz = 0;       // fp32 [H, T]   log Z of frozen heads (batch independent)
     size_t hflag = 0;    // uint32 [H]    per-head flags raised by the normaliser prep
     size_t delta = 0;    // fp32 [B, H, T] D_i = sum_c dO_ic O_ic (backward only)
+    size_t dq_acc = 0;   // fp32 [B, H, T, 64] dQ accumulator of the tensor-core backward (bf16 only)
     size_t total = 0;
 };
-WorkspaceLayout workspace_layout(int B, int H, int T, int backward);
+WorkspaceLayout workspace_layout(int B, int H, int T, int backward, int bf16);
 
 // Everything a kernel needs about one call. Pointers are device pointers.
 struct LayerArgs {
@@ -67,6 +68,7 @@ struct LayerArgs {
     float* lz;           // workspace: log Z [H, T]
     uint32_t* hflag;     // workspace: per-head flags [H]
     float* delta;        // workspace: D [B, H, T]
+    float* dq_acc;       // workspace: fp32 dQ accumulator [B, H, T, 64]
     uint32_t* status;    // workspace: error words
     int B, H, T, ld_prior;
     HeadMask mask;
@@ -84,6 +86,9 @@ cudaError_t launch_bwd_delta(const LayerArgs& p, bool bf16, cudaStream_t s);
 
 // fwd_tc.cu: tensor-core forward (bf16)
 cudaError_t launch_tc_fwd(const LayerArgs& p, cudaStream_t s);
+
+// bwd_tc.cu: tensor-core backward (bf16), including the dQ finishing kernel
+cudaError_t launch_tc_bwd(const LayerArgs& p, cudaStream_t s);
 
 // simt.cu: fp32-arithmetic path (any dtype), used for SAF_FP32
 cudaError_t launch_simt_fwd(const LayerArgs& p, bool bf16, cudaStream_t s);

@@ -41,6 +41,7 @@ SAF_KERNEL_BWD_DELTA = 3
 SAF_KERNEL_BWD_KV = 4
 SAF_KERNEL_BWD_Q = 5
 SAF_KERNEL_BWD = 6
+SAF_KERNEL_DQ_FINISH = 7
 
 
 class SafError(RuntimeError):
