@@ -230,6 +230,7 @@ KERNEL_FLOP_UNITS = {
     "dq_finish": (0, 0),
     "bwd_delta": (0, 0),
     "lognorm": (0, 0),
+    "pattern_prep": (0, 0),
 }
 
 
@@ -267,7 +268,7 @@ def run_ours(args, w):
     if not w.fwd_only:
         kernels.update({"bwd_kv": saf.SAF_KERNEL_BWD_KV, "bwd_q": saf.SAF_KERNEL_BWD_Q, "bwd": saf.SAF_KERNEL_BWD,
                         "dq_finish": saf.SAF_KERNEL_DQ_FINISH, "bwd_delta": saf.SAF_KERNEL_BWD_DELTA,
-                        "lognorm": saf.SAF_KERNEL_LOGNORM})
+                        "lognorm": saf.SAF_KERNEL_LOGNORM, "pattern_prep": saf.SAF_KERNEL_PATTERN_PREP})
 
     def new_event():
         # torch creates the CUDA event on first record; record once so that

@@ -168,7 +168,8 @@ typedef enum {
     SAF_KERNEL_BWD_KV = 4,      /* backward key-block pass (dV, dK)            */
     SAF_KERNEL_BWD_Q = 5,       /* backward query-block pass (dQ)              */
     SAF_KERNEL_BWD = 6,         /* fused backward (dQ, dK, dV in one launch)   */
-    SAF_KERNEL_DQ_FINISH = 7    /* dQ accumulator -> dq (scale, dtype, zeros)  */
+    SAF_KERNEL_DQ_FINISH = 7,   /* dQ accumulator -> dq (scale, dtype, zeros)  */
+    SAF_KERNEL_PATTERN_PREP = 8 /* padded a, r slices of the frozen heads      */
 } saf_kernel_t;
 
 /* From the next call on, record `start` (a cudaEvent_t as void*) on the

@@ -3,8 +3,13 @@
 //  * lognorm: the row normalisers log Z(i) of every frozen head
 //    ("When Can Attention Heads Be Statically Defined?", §3.2 Eq. 3; §3.3
 //    "precomputed normalisers"). They do not depend on the batch.
-//  * bwd_delta: D_i = sum_c dO_ic O_ic for the ordinary-head backward
-//    (the softmax Jacobian term of Eqs. 5-7 differentiated; App. D.2).
+//  * pattern_prep: a and r of the frozen heads scaled by log2(e) and padded
+//    with -inf, laid out so that every tile of the tensor-core kernels reads
+//    its slice with one aligned bulk copy.
+//  * bwd_delta / bwd_rowvec: D_i = sum_c dO_ic O_ic for the ordinary-head
+//    backward (the softmax Jacobian term of Eqs. 5-7 differentiated; App. D.2),
+//    the latter together with lse * log2(e) in the per-tile layout of the
+//    tensor-core backward.
 #include <math.h>
 
 #include "saf_internal.h"
@@ -13,6 +18,7 @@ namespace saf {
 namespace {
 
 constexpr int kPrepThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ float block_max(float x, float* red) {
     for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
@@ -36,8 +42,7 @@ __device__ float block_max(float x, float* red) {
 // a causal convolution that needs no exp per term. Every factor lies in
 // (0, 1]. If the shifted sum falls below 1e-28, terms that matter may have
 // left the normal fp32 range; that row is recomputed exactly by a running
-// log-sum-exp and the head is flagged (kStatusRange) for the fast kernels,
-// which rely on the factorised form.
+// log-sum-exp and the head is flagged (kStatusRange, informational).
 //
 // Grid: (ceil(T / 256), H); one thread per row i of head h.
 __global__ void __launch_bounds__(kPrepThreads)
@@ -104,6 +109,22 @@ lognorm_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all,
     lz[(size_t)h * T + i] = out;
 }
 
+// a2p[h][j] = a[h][j] log2(e) for j < T, -inf for T <= j < Tp;
+// r2p[h][u] = r[h][u - 127] log2(e) for 0 <= u - 127 < T, -inf otherwise,
+// u < Tp + 256. Frozen heads only. Grid (ceil((Tp + 256) / 256), H).
+__global__ void __launch_bounds__(kPrepThreads)
+pattern_prep_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all, int ld, HeadMask mask,
+                    int T, int Tp, float* __restrict__ a2p, float* __restrict__ r2p) {
+    const int h = blockIdx.y;
+    if (!head_frozen(mask, h)) return;
+    const int u = blockIdx.x * kPrepThreads + threadIdx.x;
+    if (u < Tp) a2p[(size_t)h * Tp + u] = u < T ? a_all[(size_t)h * ld + u] * kLog2e : -INFINITY;
+    if (u < Tp + 256) {
+        const int dl = u - 127;
+        r2p[(size_t)h * (Tp + 256) + u] = (dl >= 0 && dl < T) ? r_all[(size_t)h * ld + dl] * kLog2e : -INFINITY;
+    }
+}
+
 // D_i = sum_c dO_ic * O_ic, one warp per row (d = 64: two elements per lane).
 template <typename E>
 __global__ void __launch_bounds__(256)
@@ -119,6 +140,34 @@ bwd_delta_kernel(const E* __restrict__ o, const E* __restrict__ dO, float* __res
     if (lane == 0) delta[row] = x;
 }
 
+// Per-tile row vectors of the tensor-core backward: for slice bh and query
+// block qb, rowvec[(bh * nqb + qb) * 256 + u] holds lse * log2(e) of query
+// qb*128 + u (u < 128; +inf past T) and, at u + 128, D of that query (0 past
+// T; frozen heads skip the dot product). One warp per padded row; grid
+// (ceil(Tp / 8), B*H).
+__global__ void __launch_bounds__(256)
+bwd_rowvec_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dO,
+                  const float* __restrict__ lse, HeadMask mask, int H, int T, int nqb, float* __restrict__ rowvec) {
+    const int bh = blockIdx.y;
+    const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (i >= nqb * 128) return;
+    const bool frozen = head_frozen(mask, bh % H);
+    float d = 0.f;
+    if (i < T && !frozen) {
+        const size_t row = (size_t)bh * T + i;
+        const __nv_bfloat162 x = reinterpret_cast<const __nv_bfloat162*>(o + row * kHeadDim)[lane];
+        const __nv_bfloat162 y = reinterpret_cast<const __nv_bfloat162*>(dO + row * kHeadDim)[lane];
+        d = __bfloat162float(x.x) * __bfloat162float(y.x) + __bfloat162float(x.y) * __bfloat162float(y.y);
+        for (int s = 16; s > 0; s >>= 1) d += __shfl_xor_sync(0xffffffffu, d, s);
+    }
+    if (lane == 0) {
+        float* v = rowvec + ((size_t)bh * nqb + (i >> 7)) * 256;
+        v[i & 127] = i < T ? lse[(size_t)bh * T + i] * kLog2e : INFINITY;
+        v[128 + (i & 127)] = d;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_lognorm(const LayerArgs& p, cudaStream_t s) {
@@ -126,6 +175,15 @@ cudaError_t launch_lognorm(const LayerArgs& p, cudaStream_t s) {
     before_launch(SAF_KERNEL_LOGNORM, s);
     lognorm_kernel<<<grid, kPrepThreads, 0, s>>>(p.a, p.r, p.ld_prior, p.mask, p.T, p.lz, p.hflag, p.status);
     after_launch(SAF_KERNEL_LOGNORM, s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pattern_prep(const LayerArgs& p, cudaStream_t s) {
+    const int Tp = (p.T + 127) / 128 * 128;
+    dim3 grid((Tp + 256 + kPrepThreads - 1) / kPrepThreads, p.H);
+    before_launch(SAF_KERNEL_PATTERN_PREP, s);
+    pattern_prep_kernel<<<grid, kPrepThreads, 0, s>>>(p.a, p.r, p.ld_prior, p.mask, p.T, Tp, p.a2p, p.r2p);
+    after_launch(SAF_KERNEL_PATTERN_PREP, s);
     return cudaGetLastError();
 }
 
@@ -138,6 +196,16 @@ cudaError_t launch_bwd_delta(const LayerArgs& p, bool bf16, cudaStream_t s) {
             (const __nv_bfloat16*)p.o, (const __nv_bfloat16*)p.dO, p.delta, rows);
     else
         bwd_delta_kernel<float><<<blocks, 256, 0, s>>>((const float*)p.o, (const float*)p.dO, p.delta, rows);
+    after_launch(SAF_KERNEL_BWD_DELTA, s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_rowvec(const LayerArgs& p, cudaStream_t s) {
+    const int nqb = (p.T + 127) / 128;
+    dim3 grid((unsigned)(nqb * 128 / 8), p.B * p.H);
+    before_launch(SAF_KERNEL_BWD_DELTA, s);
+    bwd_rowvec_kernel<<<grid, 256, 0, s>>>((const __nv_bfloat16*)p.o, (const __nv_bfloat16*)p.dO, p.lse, p.mask, p.H,
+                                           p.T, nqb, p.rowvec);
     after_launch(SAF_KERNEL_BWD_DELTA, s);
     return cudaGetLastError();
 }

@@ -10,6 +10,7 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 WorkspaceLayout workspace_layout(int B, int H, int T, int backward, int bf16) {
     WorkspaceLayout L;
+    const size_t Tp = (size_t)(T + 127) / 128 * 128;
     size_t off = 0;
     L.status = off;
     off += kStatusBytes;
@@ -17,12 +18,21 @@ WorkspaceLayout workspace_layout(int B, int H, int T, int backward, int bf16) {
     off = align_up(off + (size_t)H * T * sizeof(float), 256);
     L.hflag = off;
     off = align_up(off + (size_t)H * sizeof(uint32_t), 256);
+    if (bf16) {
+        L.a2p = off;
+        off = align_up(off + (size_t)H * Tp * sizeof(float), 256);
+        L.r2p = off;
+        off = align_up(off + (size_t)H * (Tp + 256) * sizeof(float), 256);
+    }
     if (backward) {
-        L.delta = off;
-        off = align_up(off + (size_t)B * H * T * sizeof(float), 256);
         if (bf16) {
+            L.rowvec = off;
+            off = align_up(off + (size_t)B * H * (Tp / 128) * 256 * sizeof(float), 256);
             L.dq_acc = off;
             off = align_up(off + (size_t)B * H * T * kHeadDim * sizeof(float), 256);
+        } else {
+            L.delta = off;
+            off = align_up(off + (size_t)B * H * T * sizeof(float), 256);
         }
     }
     L.total = off;
@@ -30,7 +40,7 @@ WorkspaceLayout workspace_layout(int B, int H, int T, int backward, int bf16) {
 }
 
 namespace {
-constexpr int kNumKernelIds = SAF_KERNEL_DQ_FINISH + 1;
+constexpr int kNumKernelIds = SAF_KERNEL_PATTERN_PREP + 1;
 cudaEvent_t g_trace_start[kNumKernelIds] = {};
 cudaEvent_t g_trace_stop[kNumKernelIds] = {};
 unsigned long long g_launches = 0;
@@ -119,8 +129,11 @@ LayerArgs make_args(const void* q, const void* k, const void* v, const float* a,
     p.status = (uint32_t*)(ws + L.status);
     p.lz = (float*)(ws + L.lz);
     p.hflag = (uint32_t*)(ws + L.hflag);
-    p.delta = backward ? (float*)(ws + L.delta) : nullptr;
+    p.delta = (backward && !bf16) ? (float*)(ws + L.delta) : nullptr;
     p.dq_acc = (backward && bf16) ? (float*)(ws + L.dq_acc) : nullptr;
+    p.rowvec = (backward && bf16) ? (float*)(ws + L.rowvec) : nullptr;
+    p.a2p = bf16 ? (float*)(ws + L.a2p) : nullptr;
+    p.r2p = bf16 ? (float*)(ws + L.r2p) : nullptr;
     return p;
 }
 
@@ -130,14 +143,20 @@ int launch_status(cudaError_t e) {
     return SAF_ELAUNCH;
 }
 
-// Clear the error words and per-head flags, then compute log Z of the frozen heads.
-cudaError_t begin_call(const LayerArgs& p, const Common& c, cudaStream_t s) {
-    const WorkspaceLayout L = workspace_layout(p.B, p.H, p.T, 0, 0);
+// Clear the error words, work counters and per-head flags; then, for the
+// frozen heads, compute log Z (forward only: the backward reads it from lse)
+// and the padded a, r slices of the tensor-core path.
+cudaError_t begin_call(const LayerArgs& p, const Common& c, bool backward, bool bf16, cudaStream_t s) {
     cudaError_t e = cudaMemsetAsync(p.status, 0, kStatusBytes, s);
     if (e != cudaSuccess) return e;
-    e = cudaMemsetAsync(p.hflag, 0, L.total - L.hflag, s);
+    e = cudaMemsetAsync(p.hflag, 0, (size_t)p.H * sizeof(uint32_t), s);
     if (e != cudaSuccess) return e;
-    if (c.nfrozen > 0) return launch_lognorm(p, s);
+    if (c.nfrozen == 0) return cudaSuccess;
+    if (!backward || !bf16) {
+        e = launch_lognorm(p, s);
+        if (e != cudaSuccess) return e;
+    }
+    if (bf16) return launch_pattern_prep(p, s);
     return cudaSuccess;
 }
 
@@ -185,7 +204,7 @@ int saf_attn_fwd(const void* q, const void* k, const void* v, const float* a, co
     p.out = o;
     p.lse_out = lse;
     const bool bf16 = dt == SAF_BF16;
-    cudaError_t e = begin_call(p, c, s);
+    cudaError_t e = begin_call(p, c, false, bf16, s);
     if (e == cudaSuccess) e = bf16 ? launch_tc_fwd(p, s) : launch_simt_fwd(p, false, s);
     return launch_status(e);
 }
@@ -211,9 +230,14 @@ int saf_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
     p.dk = dk;
     p.dv = dv;
     const bool bf16 = dt == SAF_BF16;
-    cudaError_t e = begin_call(p, c, s);
-    if (e == cudaSuccess && c.nfrozen < H) e = launch_bwd_delta(p, bf16, s);
-    if (e == cudaSuccess) e = bf16 ? launch_tc_bwd(p, s) : launch_simt_bwd(p, false, s);
+    cudaError_t e = begin_call(p, c, true, bf16, s);
+    if (bf16) {
+        if (e == cudaSuccess) e = launch_bwd_rowvec(p, s);
+        if (e == cudaSuccess) e = launch_tc_bwd(p, s);
+    } else {
+        if (e == cudaSuccess && c.nfrozen < H) e = launch_bwd_delta(p, false, s);
+        if (e == cudaSuccess) e = launch_simt_bwd(p, false, s);
+    }
     return launch_status(e);
 }
 

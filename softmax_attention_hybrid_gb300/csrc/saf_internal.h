@@ -29,23 +29,31 @@ __host__ __device__ inline bool head_frozen(const HeadMask& m, int h) {
     return (m.w[h >> 6] >> (h & 63)) & 1ull;
 }
 
-// Error word layout at the start of every workspace (256 bytes reserved).
+// Error word layout at the start of every workspace (256 bytes reserved,
+// cleared at the start of every call).
 //   status[0]: bitwise OR of kStatus* flags raised by kernels of the last call
-//   status[1]: first work item whose bounded wait expired (diagnostic)
+//   status[8]: work-item counter of the tensor-core backward
+//   status[9]: work-item counter of the tensor-core forward
 enum : uint32_t {
     kStatusRange = 1u << 0,     // info: a frozen head left the factorised form's range and
                                 // is computed in the exact exp form (not an error)
     kStatusTimeout = 1u << 1,   // a bounded mbarrier wait expired
 };
 constexpr size_t kStatusBytes = 256;
+constexpr int kCounterBwd = 8;
+constexpr int kCounterFwd = 9;
 
 // Byte offsets of the workspace regions for one call.
+// Tp = T rounded up to a multiple of 128 (query and key blocks).
 struct WorkspaceLayout {
     size_t status = 0;   // uint32[64]
     size_t lz = 0;       // fp32 [H, T]   log Z of frozen heads (batch independent)
     size_t hflag = 0;    // uint32 [H]    per-head flags raised by the normaliser prep
-    size_t delta = 0;    // fp32 [B, H, T] D_i = sum_c dO_ic O_ic (backward only)
-    size_t dq_acc = 0;   // fp32 [B, H, T, 64] dQ accumulator of the tensor-core backward (bf16 only)
+    size_t a2p = 0;      // fp32 [H, Tp]  a * log2(e), -inf padded (bf16 path)
+    size_t r2p = 0;      // fp32 [H, Tp + 256]  r * log2(e) shifted by 127, -inf padded (bf16 path)
+    size_t delta = 0;    // fp32 [B, H, T] D_i = sum_c dO_ic O_ic (fp32 backward)
+    size_t rowvec = 0;   // fp32 [B, H, Tp / 128, 256] lse * log2(e) and D per query block (bf16 backward)
+    size_t dq_acc = 0;   // fp32 [B, H, T, 64] dQ accumulator (bf16 backward)
     size_t total = 0;
 };
 WorkspaceLayout workspace_layout(int B, int H, int T, int backward, int bf16);
@@ -69,6 +77,9 @@ struct LayerArgs {
     uint32_t* hflag;     // workspace: per-head flags [H]
     float* delta;        // workspace: D [B, H, T]
     float* dq_acc;       // workspace: fp32 dQ accumulator [B, H, T, 64]
+    float* a2p;          // workspace: padded a * log2(e) [H, Tp]
+    float* r2p;          // workspace: padded r * log2(e) [H, Tp + 256]
+    float* rowvec;       // workspace: per-block row vectors [B, H, Tp / 128, 256]
     uint32_t* status;    // workspace: error words
     int B, H, T, ld_prior;
     HeadMask mask;
@@ -83,6 +94,8 @@ void after_launch(int kernel, cudaStream_t s);
 // prep.cu
 cudaError_t launch_lognorm(const LayerArgs& p, cudaStream_t s);
 cudaError_t launch_bwd_delta(const LayerArgs& p, bool bf16, cudaStream_t s);
+cudaError_t launch_pattern_prep(const LayerArgs& p, cudaStream_t s);
+cudaError_t launch_bwd_rowvec(const LayerArgs& p, cudaStream_t s);
 
 // fwd_tc.cu: tensor-core forward (bf16)
 cudaError_t launch_tc_fwd(const LayerArgs& p, cudaStream_t s);

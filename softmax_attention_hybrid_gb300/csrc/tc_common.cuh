@@ -88,6 +88,16 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
+// Untiled bulk copy global -> shared (both 16-byte aligned, size a multiple
+// of 16), completion signalled on `bar` through its transaction count.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Make generic-proxy writes to shared memory visible to the async proxy
 // (tcgen05.mma operands written by threads).
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -42,6 +42,7 @@ SAF_KERNEL_BWD_KV = 4
 SAF_KERNEL_BWD_Q = 5
 SAF_KERNEL_BWD = 6
 SAF_KERNEL_DQ_FINISH = 7
+SAF_KERNEL_PATTERN_PREP = 8
 
 
 class SafError(RuntimeError):
