@@ -22,13 +22,15 @@
 //   dP^T = V dO^T         (tcgen05, TMEM)      dS  = P o (dP - D)
 //   dV  += P^T dO         (A = P^T from TMEM)
 //   dK  += dS^T Q         (A = dS in shared memory, K-major view)
-//   dQ   = dS K           (A = dS in shared memory, MN-major view) -> red.add
+//   dQ   = dS K           (A = dS in shared memory, MN-major view), then added
+//                         into the fp32 accumulator by a bulk tensor reduce-add
 //
 // Warp roles (320 threads, one CTA per SM):
 //   warps 0-7 : pattern warps; warp w handles key rows 32(w%4)..+31 and query
 //               columns 64(w/4)..+63 of each tile (P^T, dS or W^T), then drains
-//               dQ rows 32(w%4)..+31, d-columns 32(w/4)..+31 to the accumulator,
-//               and at the end of an item writes its half of the dV, dK rows
+//               dQ rows 32(w%4)..+31, d-columns 32(w/4)..+31 through shared
+//               memory into the accumulator, and at the end of an item writes
+//               its half of the dV, dK rows
 //   warp 8    : producer: takes items from the counter and publishes them,
 //               TMA of K, V per item and of Q, dO and the row vectors per tile
 //   warp 9    : tensor-memory owner and single-thread MMA issuer
@@ -46,7 +48,7 @@ using namespace tc;
 
 constexpr int kTileBytes = 128 * 64 * 2;
 constexpr int kThreads = 320;
-constexpr int kStages = 3;
+constexpr int kStages = 2;
 constexpr int kRing = 4;
 constexpr int kSliceGroup = 8;
 constexpr float kScaleLog2 = 0.125f * 1.4426950408889634f;
@@ -59,6 +61,7 @@ struct BwdParams {
     CUtensorMap tm_k;
     CUtensorMap tm_v;
     CUtensorMap tm_do;
+    CUtensorMap tm_dq;     // fp32 dQ accumulator [BH, T, 64], box {32, 128}
     __nv_bfloat16* dk;
     __nv_bfloat16* dv;
     float* dq_acc;
@@ -80,7 +83,8 @@ struct Smem {
     static constexpr int st_vec = 2 * kTileBytes;     // offset of the 512 fp32 row vectors in a stage
     static constexpr int st_bytes = 2 * kTileBytes + 3 * 1024;   // 1024-aligned
     static constexpr int ds = st + kStages * st_bytes;            // dS, 128 x 128 bf16
-    static constexpr int total = ds + 2 * kTileBytes;
+    static constexpr int dqs = ds + 2 * kTileBytes;               // dQ staging, 2 halves x (128 x 32 fp32)
+    static constexpr int total = dqs + 2 * 16384;
 };
 
 struct Item {
@@ -119,9 +123,8 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
 struct Barriers {
@@ -353,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 }
             }
         }
-    } else {
+    } else if (warp < 8) {
         // ---------------------------------------------------------------- pattern warps
         const int quarter = warp & 3, half = warp >> 2;
         const int j = quarter * 32 + lane;                   // key row of the block = TMEM lane
@@ -364,8 +367,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         bool ok = true;
         uint8_t* dsp = sm + Smem::ds + half * 16384;          // my 64-query half of dS (MN-major atom)
 
-        // Drain dQ of tile (bh, qb) to the fp32 accumulator: rows 32*quarter + lane,
-        // d-columns 32*half .. +31.
+        uint8_t* dqs = sm + Smem::dqs + half * 16384;         // staging of my 32 dQ columns (SW128 rows)
+        const bool dq_issuer = quarter == 0 && lane == 0;     // issues the bulk reduce of this half
+
+        // Drain dQ of tile (bh, qb) into the fp32 accumulator with a bulk tensor
+        // reduce-add: rows 32*quarter + lane, d-columns 32*half .. +31.
         auto drain_dq = [&](int bh, int qb) -> bool {
             if (!mbar_wait(&bars.dq_full, dq_full_ph, abort, status, kStatusTimeout)) return false;
             dq_full_ph ^= 1;
@@ -376,13 +382,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars.dq_free);
-            const int q = qb * 128 + j;
-            if (q < p.T) {
-                float* dst = p.dq_acc + ((size_t)bh * p.T + q) * 64 + 32 * half;
+            if (dq_issuer) bulk_wait_read_all();   // the previous reduce has read the staging buffer
+            named_bar_sync(1 + half, 128);
 #pragma unroll
-                for (int c = 0; c < 32; c += 4)
-                    red_add_v4(dst + c, __uint_as_float(v[c]), __uint_as_float(v[c + 1]), __uint_as_float(v[c + 2]),
-                               __uint_as_float(v[c + 3]));
+            for (int t = 0; t < 8; ++t)
+                *reinterpret_cast<uint4*>(dqs + sw128_offset(j, 16 * t)) =
+                    make_uint4(v[4 * t], v[4 * t + 1], v[4 * t + 2], v[4 * t + 3]);
+            fence_proxy_async_smem();
+            named_bar_sync(1 + half, 128);
+            if (dq_issuer) {
+                tma_reduce_add_3d(&p.tm_dq, dqs, 32 * half, qb * 128, bh);
+                bulk_commit_group();
             }
             return true;
         };
@@ -412,57 +422,81 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 st_full_bits ^= 1u << stage;
                 const float* vec =
                     reinterpret_cast<const float*>(sm + Smem::st + stage * Smem::st_bytes + Smem::st_vec);
-                uint32_t pk[32];   // my 64 query columns of P^T (or W^T), packed bf16 pairs
                 if (!it.frozen) {
                     if (!(ok = mbar_wait(&bars.s_full, s_full_ph, abort, status, kStatusTimeout))) break;
                     s_full_ph ^= 1;
                     tc_fence_after();
-                    uint32_t sv[64], dp[64];
-                    tmem_ld32(lane_base + kColS + 64 * half, sv);
-                    tmem_ld32(lane_base + kColS + 64 * half + 32, sv + 32);
+                    // P^T first: S^T row (64 columns) -> P (bf16 pairs); then dP^T row -> dS.
+                    uint32_t pk[32];
+                    {
+                        uint32_t sv[64];
+                        tmem_ld32(lane_base + kColS + 64 * half, sv);
+                        tmem_ld32(lane_base + kColS + 64 * half + 32, sv + 32);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 64; e += 2) {
+                            const int q0 = 64 * half + e;
+                            float p0 = fast_exp2(fmaf(__uint_as_float(sv[e]), kScaleLog2, -vec[q0]));
+                            float p1 = fast_exp2(fmaf(__uint_as_float(sv[e + 1]), kScaleLog2, -vec[q0 + 1]));
+                            if (diag && j > q0) p0 = 0.f;
+                            if (diag && j > q0 + 1) p1 = 0.f;
+                            pk[e >> 1] = pack_bf16(p0, p1);
+                        }
+                    }
+                    uint32_t dp[64];
                     tmem_ld32(lane_base + kColDP + 64 * half, dp);
                     tmem_ld32(lane_base + kColDP + 64 * half + 32, dp + 32);
                     tmem_ld_wait();
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars.s_consumed);
-                    uint32_t dk[32];
-#pragma unroll
-                    for (int e = 0; e < 64; e += 2) {
-                        const int q0 = 64 * half + e;
-                        float p0 = fast_exp2(fmaf(__uint_as_float(sv[e]), kScaleLog2, -vec[q0]));
-                        float p1 = fast_exp2(fmaf(__uint_as_float(sv[e + 1]), kScaleLog2, -vec[q0 + 1]));
-                        if (diag && j > q0) p0 = 0.f;
-                        if (diag && j > q0 + 1) p1 = 0.f;
-                        const float d0 = p0 * (__uint_as_float(dp[e]) - vec[128 + q0]);
-                        const float d1 = p1 * (__uint_as_float(dp[e + 1]) - vec[128 + q0 + 1]);
-                        pk[e >> 1] = pack_bf16(p0, p1);
-                        dk[e >> 1] = pack_bf16(d0, d1);
-                    }
-                    // dS row j, my 64 queries: MN-major atom `half`, K-row j, 8 chunks of 16 bytes
+                    // P^T may be overwritten once the previous tile's dV MMA has read it, and
+                    // dS once the previous tile's dK and dQ MMAs have
+                    if (!(ok = mbar_wait(&bars.p_free, p_free_ph, abort, status, kStatusTimeout))) break;
+                    p_free_ph ^= 1;
                     if (!(ok = mbar_wait(&bars.ds_free, ds_free_ph, abort, status, kStatusTimeout))) break;
                     ds_free_ph ^= 1;
+                    tc_fence_after();
+                    tmem_st32(lane_base + kColP + 32 * half, pk);
 #pragma unroll
-                    for (int t = 0; t < 8; ++t)
-                        *reinterpret_cast<uint4*>(dsp + sw128_offset(j, 16 * t)) =
-                            make_uint4(dk[4 * t], dk[4 * t + 1], dk[4 * t + 2], dk[4 * t + 3]);
+                    for (int g2 = 0; g2 < 2; ++g2) {
+                        uint32_t dk[16];
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            const int c = 32 * g2 + e;
+                            const int q0 = 64 * half + c;
+                            // dS = P o (dP - D) with P as rounded to bf16 for the MMAs
+                            const float p0 = __uint_as_float(pk[c >> 1] << 16);
+                            const float p1 = __uint_as_float(pk[c >> 1] & 0xffff0000u);
+                            const float d0 = p0 * (__uint_as_float(dp[c]) - vec[128 + q0]);
+                            const float d1 = p1 * (__uint_as_float(dp[c + 1]) - vec[128 + q0 + 1]);
+                            dk[e >> 1] = pack_bf16(d0, d1);
+                        }
+#pragma unroll
+                        for (int t = 0; t < 4; ++t)
+                            *reinterpret_cast<uint4*>(dsp + sw128_offset(j, 16 * (4 * g2 + t))) =
+                                make_uint4(dk[4 * t], dk[4 * t + 1], dk[4 * t + 2], dk[4 * t + 3]);
+                    }
                 } else {
+                    if (!(ok = mbar_wait(&bars.p_free, p_free_ph, abort, status, kStatusTimeout))) break;
+                    p_free_ph ^= 1;
+                    tc_fence_after();
                     // W^T(j, q) = W(q, j) = exp(a[j] + r[q - j] - log Z(q)) (Eq. 3);
                     // vec[256 + u] holds r * log2(e) at offset (qb - kb) * 128 + u - 127
                     const float* band = vec + 256 + 127 - j;
 #pragma unroll
-                    for (int e = 0; e < 64; e += 2) {
-                        const int q0 = 64 * half + e;
-                        const float w0 = fast_exp2(a2j + band[q0] - vec[q0]);
-                        const float w1 = fast_exp2(a2j + band[q0 + 1] - vec[q0 + 1]);
-                        pk[e >> 1] = pack_bf16(w0, w1);
+                    for (int g2 = 0; g2 < 2; ++g2) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            const int q0 = 64 * half + 32 * g2 + e;
+                            const float w0 = fast_exp2(a2j + band[q0] - vec[q0]);
+                            const float w1 = fast_exp2(a2j + band[q0 + 1] - vec[q0 + 1]);
+                            pk[e >> 1] = pack_bf16(w0, w1);
+                        }
+                        tmem_st16(lane_base + kColP + 32 * half + 16 * g2, pk);
                     }
                 }
-                // P^T may be overwritten once the previous tile's dV MMA has read it
-                if (!(ok = mbar_wait(&bars.p_free, p_free_ph, abort, status, kStatusTimeout))) break;
-                p_free_ph ^= 1;
-                tc_fence_after();
-                tmem_st32(lane_base + kColP + 32 * half, pk);
                 tmem_st_wait();
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -511,6 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         }
     }
 
+    if (warp < 8 && (warp & 3) == 0 && lane == 0) bulk_wait_all();   // dQ reduces complete
     tc_fence_before();
     __syncthreads();
     if (warp == 9) {
@@ -552,7 +587,8 @@ cudaError_t launch_tc_bwd(const LayerArgs& a, cudaStream_t s) {
     if (!make_tmap_bf16_3d(&p.tm_q, qbase, 64, a.T, BH, 64, 128) ||
         !make_tmap_bf16_3d(&p.tm_k, kbase, 64, a.T, BH, 64, 128) ||
         !make_tmap_bf16_3d(&p.tm_v, vbase, 64, a.T, BH, 64, 128) ||
-        !make_tmap_bf16_3d(&p.tm_do, a.dO, 64, a.T, BH, 64, 128))
+        !make_tmap_bf16_3d(&p.tm_do, a.dO, 64, a.T, BH, 64, 128) ||
+        !make_tmap_f32_3d(&p.tm_dq, a.dq_acc, 64, a.T, BH, 32, 128))
         return cudaErrorInvalidValue;
     p.dk = (__nv_bfloat16*)a.dk;
     p.dv = (__nv_bfloat16*)a.dv;

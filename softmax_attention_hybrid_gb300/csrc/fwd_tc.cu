@@ -46,24 +46,26 @@ struct FwdParams {
     CUtensorMap tm_v;
     __nv_bfloat16* o;
     float* lse;
-    const float* a;
-    const float* r;
     const float* lz;
+    const float* a2p;     // [H, Tp]: a * log2(e), -inf padded
+    const float* r2p;     // [H, Tp + 256]: r * log2(e) at offset + 127, -inf padded
     uint32_t* status;
-    int B, H, T, ld;
+    int B, H, T, ld, Tp;
     int nqb, npairs, n_items;
     int n_ord, n_frz;
     uint8_t ord_heads[SAF_MAX_HEADS];
     uint8_t frz_heads[SAF_MAX_HEADS];
 };
 
+// A stage holds K and V of one key block; for frozen items the K slot holds
+// instead a * log2(e) of the block's keys (128 fp32 at byte 0) and the band of
+// r * log2(e) both tiles need (384 fp32 at byte 1024).
 struct SmemLayout {
     static constexpr int q = 0;                                     // 2 tiles
     static constexpr int kv = q + 2 * kTileBytes;                   // kStages x (K, V)
     static constexpr int stage_bytes = 2 * kTileBytes;
-    static constexpr int frz = kv + kStages * stage_bytes;          // 2 groups x (a2[128] + band[256]) fp32
-    static constexpr int frz_group_bytes = (128 + 256) * 4;
-    static constexpr int total = frz + 2 * frz_group_bytes;
+    static constexpr int frz_band = 1024;
+    static constexpr int total = kv + kStages * stage_bytes;
 };
 
 struct Item {
@@ -101,10 +103,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
 struct Barriers {
@@ -180,8 +178,16 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         break;
                     kv_empty_bits ^= 1u << stage;
                     uint8_t* st = sm + SmemLayout::kv + stage * SmemLayout::stage_bytes;
-                    mbar_expect_tx(&bars.kv_full[stage], (it.frozen ? 1 : 2) * kTileBytes);
-                    if (!it.frozen) tma_load_3d(st, &p.tm_k, &bars.kv_full[stage], 0, j * 128, bh);
+                    if (!it.frozen) {
+                        mbar_expect_tx(&bars.kv_full[stage], 2 * kTileBytes);
+                        tma_load_3d(st, &p.tm_k, &bars.kv_full[stage], 0, j * 128, bh);
+                    } else {
+                        mbar_expect_tx(&bars.kv_full[stage], kTileBytes + 512 + 1536);
+                        bulk_load(st, p.a2p + (size_t)it.h * p.Tp + (size_t)j * 128, 512, &bars.kv_full[stage]);
+                        bulk_load(st + SmemLayout::frz_band,
+                                  p.r2p + (size_t)it.h * (p.Tp + 256) + (size_t)(qb0 - j) * 128, 1536,
+                                  &bars.kv_full[stage]);
+                    }
                     tma_load_3d(st + kTileBytes, &p.tm_v, &bars.kv_full[stage], 0, j * 128, bh);
                     stage = (stage + 1 == kStages) ? 0 : stage + 1;
                 }
@@ -241,27 +247,31 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     mma_commit(&bars.o_done[g]);
                     return true;
                 };
-                auto wait_kv = [&](int j) -> bool {
-                    const int s = stage_of(j);
-                    if (!mbar_wait(&bars.kv_full[s], (kv_full_bits >> s) & 1u, abort, status, kStatusTimeout))
-                        return false;
-                    kv_full_bits ^= 1u << s;
+                int kv_ready = 0;   // blocks of this item whose K/V stage has been waited for
+                auto ensure_kv = [&](int j) -> bool {
+                    while (kv_ready <= j) {
+                        const int s = stage_of(kv_ready);
+                        if (!mbar_wait(&bars.kv_full[s], (kv_full_bits >> s) & 1u, abort, status, kStatusTimeout))
+                            return false;
+                        kv_full_bits ^= 1u << s;
+                        ++kv_ready;
+                    }
                     return true;
                 };
-                if (!(ok = wait_kv(0))) break;
+                if (!(ok = ensure_kv(0))) break;
                 if (!it.frozen) {
                     ok = issue_s(0, 0);
                     if (ok && n1 > 0) ok = issue_s(1, 0);
                 }
-                // Per block j: P V of tile 0, then the next block's S of tile 0 (so that
-                // tile 0's softmax overlaps tile 1's MMAs), then the same for tile 1.
+                // Per block j and tile g: the next block's S (as soon as the softmax group
+                // has read this block's S, so it runs under the softmax), then P V.
                 for (int j = 0; j < nblk && ok; ++j) {
                     const bool more = j + 1 < nblk;
-                    if (j < n0) ok = issue_pv(0, j);
-                    if (ok && more) ok = wait_kv(j + 1);
-                    if (ok && more && !it.frozen && j + 1 < n0) ok = issue_s(0, j + 1);
+                    if (!(ok = ensure_kv(j))) break;
+                    if (more && !it.frozen && j + 1 < n0) ok = ensure_kv(j + 1) && issue_s(0, j + 1);
+                    if (ok && j < n0) ok = issue_pv(0, j);
+                    if (ok && more && !it.frozen && j + 1 < n1) ok = ensure_kv(j + 1) && issue_s(1, j + 1);
                     if (ok && j < n1) ok = issue_pv(1, j);
-                    if (ok && more && !it.frozen && j + 1 < n1) ok = issue_s(1, j + 1);
                     if (!ok) break;
                     mma_commit(&bars.kv_empty[stage_of(j)]);
                 }
@@ -275,14 +285,16 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         const int g = warp >> 2;               // 0 or 1
         const int r = threadIdx.x & 127;       // row within the tile = TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16) + 256 * g;
-        float* a2s = reinterpret_cast<float*>(sm + SmemLayout::frz + g * SmemLayout::frz_group_bytes);
-        float* band = a2s + 128;
         uint32_t s_full_ph = 0, o_done_ph = 0;
+        int gblk = 0;   // key blocks of all previous items of this CTA (stage = gblk % kStages)
         bool ok = true;
         for (int round = 0; ok; ++round) {
             const int idx = item_index(round, cta, grid);
             if (idx >= p.n_items) break;
             const Item it = decode_item(p, idx);
+            const int item_blocks = (2 * it.pair + 1 < p.nqb) ? 2 * it.pair + 2 : 2 * it.pair + 1;
+            const int gblk0 = gblk;
+            gblk += item_blocks;
             const int qb = 2 * it.pair + g;
             if (qb >= p.nqb) continue;
             const int bh = it.b * p.H + it.h;
@@ -290,8 +302,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             const int nblk = qb + 1;
             float m_used = -INFINITY, l = 0.f;
             float lz2 = INFINITY;
-            const float* ah = p.a + (size_t)it.h * p.ld;
-            const float* rh = p.r + (size_t)it.h * p.ld;
             if (it.frozen && row < p.T) lz2 = p.lz[(size_t)it.h * p.T + row] * kLog2e;
             for (int j = 0; j < nblk && ok; ++j) {
                 if (!it.frozen) {
@@ -339,47 +349,47 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     }
                     float ls = 0.f;
 #pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        uint32_t pk[32];   // packed bf16 pairs of 64 columns of P
+                    for (int h4 = 0; h4 < 4; ++h4) {
+                        uint32_t pk[16];   // packed bf16 pairs of 32 columns of P
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) {
-                            const float p0 = fast_exp2(__uint_as_float(sr[64 * h2 + 2 * c]) - m_used);
-                            const float p1 = fast_exp2(__uint_as_float(sr[64 * h2 + 2 * c + 1]) - m_used);
+                        for (int c = 0; c < 16; ++c) {
+                            const float p0 = fast_exp2(__uint_as_float(sr[32 * h4 + 2 * c]) - m_used);
+                            const float p1 = fast_exp2(__uint_as_float(sr[32 * h4 + 2 * c + 1]) - m_used);
                             ls += p0 + p1;
                             pk[c] = pack_bf16(p0, p1);
                         }
-                        tmem_st32(lane_base + 128 + 32 * h2, pk);
+                        tmem_st16(lane_base + 128 + 16 * h4, pk);
                     }
                     l += ls;
                 } else {
-                    // Frozen tile: W(i, k) = exp(a[k] + r[i - k] - log Z(i)) (Eq. 3), built from
-                    // the key block's a values and the tile's band of r values in shared memory.
-                    named_bar_sync(1 + g, 128);   // previous block's staging fully read
-                    const int key = j * 128 + r;
-                    a2s[r] = key < p.T ? ah[key] * kLog2e : -INFINITY;
-                    const int d0 = (qb - j) * 128 - 127;  // offset of band[0]
-                    for (int u = r; u < 255; u += 128) {
-                        const int dl = d0 + u;
-                        band[u] = (dl >= 0 && dl < p.T) ? rh[dl] * kLog2e : -INFINITY;
-                    }
-                    named_bar_sync(1 + g, 128);
+                    // Frozen tile: W(i, k) = exp(a[k] + r[i - k] - log Z(i)) (Eq. 3), from the key
+                    // block's a values and the band of r values the producer staged in the K slot.
+                    const int G = gblk0 + j;
+                    const int st = G % kStages;
+                    if (!(ok = mbar_wait(&bars.kv_full[st], (uint32_t)(G / kStages) & 1u, abort, status,
+                                         kStatusTimeout)))
+                        break;
                     if (j > 0) {
                         if (!(ok = mbar_wait(&bars.o_done[g], o_done_ph, abort, status, kStatusTimeout))) break;
                         o_done_ph ^= 1;
                         tc_fence_after();
                     }
-                    const float* bnd = band + r + 127;   // bnd[-c] = r2[i - k]
+                    const float* a2s = reinterpret_cast<const float*>(sm + SmemLayout::kv + st * SmemLayout::stage_bytes);
+                    // bnd[-c] = r * log2(e) at offset i - k = (qb - j) * 128 + r - c
+                    const float* bnd = reinterpret_cast<const float*>(sm + SmemLayout::kv + st * SmemLayout::stage_bytes +
+                                                                      SmemLayout::frz_band) +
+                                       128 * g + r + 127;
 #pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        uint32_t pk[32];
+                    for (int h4 = 0; h4 < 4; ++h4) {
+                        uint32_t pk[16];
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) {
-                            const int cc = 64 * h2 + 2 * c;
+                        for (int c = 0; c < 16; ++c) {
+                            const int cc = 32 * h4 + 2 * c;
                             const float w0 = fast_exp2(a2s[cc] + bnd[-cc] - lz2);
                             const float w1 = fast_exp2(a2s[cc + 1] + bnd[-cc - 1] - lz2);
                             pk[c] = pack_bf16(w0, w1);
                         }
-                        tmem_st32(lane_base + 128 + 32 * h2, pk);
+                        tmem_st16(lane_base + 128 + 16 * h4, pk);
                     }
                 }
                 tmem_st_wait();
@@ -437,15 +447,16 @@ cudaError_t launch_tc_fwd(const LayerArgs& a, cudaStream_t s) {
         return cudaErrorInvalidValue;
     p.o = (__nv_bfloat16*)a.out;
     p.lse = a.lse_out;
-    p.a = a.a;
-    p.r = a.r;
     p.lz = a.lz;
+    p.a2p = a.a2p;
+    p.r2p = a.r2p;
     p.status = a.status;
     p.B = a.B;
     p.H = a.H;
     p.T = a.T;
     p.ld = a.ld_prior;
     p.nqb = (a.T + 127) / 128;
+    p.Tp = p.nqb * 128;
     p.npairs = (p.nqb + 1) / 2;
     p.n_items = a.B * a.H * p.npairs;
     for (int h = 0; h < a.H; ++h) {
