@@ -66,8 +66,12 @@ struct BwdParams {
     __nv_bfloat16* dv;
     float* dq_acc;
     const float* rowvec;   // [BH, nqb, 256]: lse * log2(e) | D
-    const float* a2p;      // [H, Tp]
-    const float* r2p;      // [H, Tp + 256]
+    const float* a2p;      // [H, Tp]: a * log2(e)                (exact form)
+    const float* r2p;      // [H, Tp + 256]: r * log2(e), + 127   (exact form)
+    const float* eap;      // [H, Tp]: exp(a - max a)             (factorised form)
+    const float* erp;      // [H, Tp + 256]: exp(r - max r), + 127
+    const float* invz;     // [H, Tp]: 1 / Z'
+    const uint32_t* hflag; // per head: bit 1 = use the exact form
     uint32_t* status;
     int B, H, T, Tp;
     int nqb, n_items, n_ord_items;
@@ -235,10 +239,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                         tma_load_3d(st + kTileBytes, &p.tm_do, &bars.st_full[stage], 0, qb * 128, bh);
                         bulk_load(vec, rv, 1024, &bars.st_full[stage]);
                     } else {
-                        const float* band = p.r2p + (size_t)it.h * (p.Tp + 256) + (size_t)(qb - it.kb) * 128;
-                        mbar_expect_tx(&bars.st_full[stage], kTileBytes + 2048);
+                        // exact form: vec[0..128) lse * log2(e) (= log2 Z), vec[256..512) r * log2(e);
+                        // factorised form: vec[0..128) 1 / Z', vec[256..512) exp(r - R)
+                        const bool exact = (p.hflag[it.h] & 2u) != 0;
+                        const float* band = (exact ? p.r2p : p.erp) + (size_t)it.h * (p.Tp + 256) +
+                                            (size_t)(qb - it.kb) * 128;
+                        mbar_expect_tx(&bars.st_full[stage], kTileBytes + 1024 + 512);
                         tma_load_3d(st + kTileBytes, &p.tm_do, &bars.st_full[stage], 0, qb * 128, bh);
-                        bulk_load(vec, rv, 1024, &bars.st_full[stage]);
+                        if (exact)
+                            bulk_load(vec, rv, 512, &bars.st_full[stage]);
+                        else
+                            bulk_load(vec, p.invz + (size_t)it.h * p.Tp + (size_t)qb * 128, 512, &bars.st_full[stage]);
                         bulk_load(vec + 256, band, 1024, &bars.st_full[stage]);
                     }
                     stage = (stage + 1) % kStages;
@@ -411,8 +422,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             const int bh = it.b * p.H + it.h;
             const int key = it.kb * 128 + j;
             const int n = nqb - it.kb;
-            float a2j = -INFINITY;
-            if (it.frozen) a2j = p.a2p[(size_t)it.h * p.Tp + key];
+            float a2j = -INFINITY;   // exact form: a * log2(e) of my key
+            float eaj = 0.f;         // factorised form: exp(a - A) of my key, applied to dV
+            bool exact = false;
+            if (it.frozen) {
+                exact = (p.hflag[it.h] & 2u) != 0;
+                a2j = p.a2p[(size_t)it.h * p.Tp + key];
+                eaj = p.eap[(size_t)it.h * p.Tp + key];
+            }
             for (int i = 0; i < n && ok; ++i) {
                 const int qb = it.kb + i;
                 const bool diag = i == 0;
@@ -481,18 +498,27 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                     if (!(ok = mbar_wait(&bars.p_free, p_free_ph, abort, status, kStatusTimeout))) break;
                     p_free_ph ^= 1;
                     tc_fence_after();
-                    // W^T(j, q) = W(q, j) = exp(a[j] + r[q - j] - log Z(q)) (Eq. 3);
-                    // vec[256 + u] holds r * log2(e) at offset (qb - kb) * 128 + u - 127
+                    // W^T(j, q) = W(q, j) (Eq. 3); band[q] is r at offset q - j = (qb - kb) * 128 +
+                    // q - j. Factorised: W(q, j) / exp(a[j] - A) = exp(r[q-j] - R) / Z'(q), no exp per
+                    // element (exp(a[j] - A) is applied to dV). Exact: exp(a[j] + r[q-j] - log Z(q)).
                     const float* band = vec + 256 + 127 - j;
 #pragma unroll
                     for (int g2 = 0; g2 < 2; ++g2) {
                         uint32_t pk[16];
+                        if (!exact) {
 #pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            const int q0 = 64 * half + 32 * g2 + e;
-                            const float w0 = fast_exp2(a2j + band[q0] - vec[q0]);
-                            const float w1 = fast_exp2(a2j + band[q0 + 1] - vec[q0 + 1]);
-                            pk[e >> 1] = pack_bf16(w0, w1);
+                            for (int e = 0; e < 32; e += 2) {
+                                const int q0 = 64 * half + 32 * g2 + e;
+                                pk[e >> 1] = pack_bf16(band[q0] * vec[q0], band[q0 + 1] * vec[q0 + 1]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; e += 2) {
+                                const int q0 = 64 * half + 32 * g2 + e;
+                                const float w0 = fast_exp2(a2j + band[q0] - vec[q0]);
+                                const float w1 = fast_exp2(a2j + band[q0 + 1] - vec[q0 + 1]);
+                                pk[e >> 1] = pack_bf16(w0, w1);
+                            }
                         }
                         tmem_st16(lane_base + kColP + 32 * half + 16 * g2, pk);
                     }
@@ -520,13 +546,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             if (key < p.T) {
                 uint4* pv = reinterpret_cast<uint4*>(p.dv + ((size_t)bh * p.T + key) * 64 + 32 * half);
                 uint4* pk2 = reinterpret_cast<uint4*>(p.dk + ((size_t)bh * p.T + key) * 64 + 32 * half);
+                const float fv = (it.frozen && !exact) ? eaj : 1.f;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const uint32_t* x = dv + 8 * c;
-                    pv[c] = make_uint4(pack_bf16(__uint_as_float(x[0]), __uint_as_float(x[1])),
-                                       pack_bf16(__uint_as_float(x[2]), __uint_as_float(x[3])),
-                                       pack_bf16(__uint_as_float(x[4]), __uint_as_float(x[5])),
-                                       pack_bf16(__uint_as_float(x[6]), __uint_as_float(x[7])));
+                    pv[c] = make_uint4(pack_bf16(__uint_as_float(x[0]) * fv, __uint_as_float(x[1]) * fv),
+                                       pack_bf16(__uint_as_float(x[2]) * fv, __uint_as_float(x[3]) * fv),
+                                       pack_bf16(__uint_as_float(x[4]) * fv, __uint_as_float(x[5]) * fv),
+                                       pack_bf16(__uint_as_float(x[6]) * fv, __uint_as_float(x[7]) * fv));
                 }
                 if (it.frozen) {
 #pragma unroll
@@ -596,6 +623,10 @@ cudaError_t launch_tc_bwd(const LayerArgs& a, cudaStream_t s) {
     p.rowvec = a.rowvec;
     p.a2p = a.a2p;
     p.r2p = a.r2p;
+    p.eap = a.eap;
+    p.erp = a.erp;
+    p.invz = a.invz;
+    p.hflag = a.hflag;
     p.status = a.status;
     p.B = a.B;
     p.H = a.H;

@@ -47,8 +47,12 @@ struct FwdParams {
     __nv_bfloat16* o;
     float* lse;
     const float* lz;
-    const float* a2p;     // [H, Tp]: a * log2(e), -inf padded
-    const float* r2p;     // [H, Tp + 256]: r * log2(e) at offset + 127, -inf padded
+    const float* a2p;     // [H, Tp]: a * log2(e), -inf padded          (exact form)
+    const float* r2p;     // [H, Tp + 256]: r * log2(e) at offset + 127  (exact form)
+    const float* eap;     // [H, Tp]: exp(a - max a), 0 padded          (factorised form)
+    const float* erp;     // [H, Tp + 256]: exp(r - max r) at offset + 127
+    const float* invz;    // [H, Tp]: 1 / Z' of the factorised form
+    const uint32_t* hflag;   // per head: bit 1 = use the exact form
     uint32_t* status;
     int B, H, T, ld, Tp;
     int nqb, npairs, n_items;
@@ -58,8 +62,9 @@ struct FwdParams {
 };
 
 // A stage holds K and V of one key block; for frozen items the K slot holds
-// instead a * log2(e) of the block's keys (128 fp32 at byte 0) and the band of
-// r * log2(e) both tiles need (384 fp32 at byte 1024).
+// instead the block's slice of a (128 fp32 at byte 0) and the band of r both
+// tiles need (384 fp32 at byte 1024), in the factorised form (exp(a - A),
+// exp(r - R)) or, for flagged heads, in the exact form (log2 domain).
 struct SmemLayout {
     static constexpr int q = 0;                                     // 2 tiles
     static constexpr int kv = q + 2 * kTileBytes;                   // kStages x (K, V)
@@ -182,10 +187,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         mbar_expect_tx(&bars.kv_full[stage], 2 * kTileBytes);
                         tma_load_3d(st, &p.tm_k, &bars.kv_full[stage], 0, j * 128, bh);
                     } else {
+                        const bool exact = (p.hflag[it.h] & 2u) != 0;
+                        const float* as = exact ? p.a2p : p.eap;
+                        const float* rs = exact ? p.r2p : p.erp;
                         mbar_expect_tx(&bars.kv_full[stage], kTileBytes + 512 + 1536);
-                        bulk_load(st, p.a2p + (size_t)it.h * p.Tp + (size_t)j * 128, 512, &bars.kv_full[stage]);
+                        bulk_load(st, as + (size_t)it.h * p.Tp + (size_t)j * 128, 512, &bars.kv_full[stage]);
                         bulk_load(st + SmemLayout::frz_band,
-                                  p.r2p + (size_t)it.h * (p.Tp + 256) + (size_t)(qb0 - j) * 128, 1536,
+                                  rs + (size_t)it.h * (p.Tp + 256) + (size_t)(qb0 - j) * 128, 1536,
                                   &bars.kv_full[stage]);
                     }
                     tma_load_3d(st + kTileBytes, &p.tm_v, &bars.kv_full[stage], 0, j * 128, bh);
@@ -301,8 +309,16 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             const int row = qb * 128 + r;
             const int nblk = qb + 1;
             float m_used = -INFINITY, l = 0.f;
-            float lz2 = INFINITY;
-            if (it.frozen && row < p.T) lz2 = p.lz[(size_t)it.h * p.T + row] * kLog2e;
+            float lz2 = INFINITY;   // exact form: log2 Z(i)
+            float iz = 0.f;         // factorised form: 1 / Z'(i)
+            bool exact = false;
+            if (it.frozen) {
+                exact = (p.hflag[it.h] & 2u) != 0;
+                if (row < p.T) {
+                    lz2 = p.lz[(size_t)it.h * p.T + row] * kLog2e;
+                    iz = p.invz[(size_t)it.h * p.Tp + row];
+                }
+            }
             for (int j = 0; j < nblk && ok; ++j) {
                 if (!it.frozen) {
                     if (!(ok = mbar_wait(&bars.s_full[g], s_full_ph, abort, status, kStatusTimeout))) break;
@@ -362,8 +378,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     }
                     l += ls;
                 } else {
-                    // Frozen tile: W(i, k) = exp(a[k] + r[i - k] - log Z(i)) (Eq. 3), from the key
-                    // block's a values and the band of r values the producer staged in the K slot.
+                    // Frozen tile of Eq. 3 from the key block's a values and the band of r values
+                    // the producer staged in the K slot. Factorised form: W(i, k) Z'(i) =
+                    // exp(r[i-k] - R) exp(a[k] - A), no exp per element (1 / Z' is applied to O).
+                    // Exact form: W(i, k) = exp(a[k] + r[i - k] - log Z(i)).
                     const int G = gblk0 + j;
                     const int st = G % kStages;
                     if (!(ok = mbar_wait(&bars.kv_full[st], (uint32_t)(G / kStages) & 1u, abort, status,
@@ -379,17 +397,30 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     const float* bnd = reinterpret_cast<const float*>(sm + SmemLayout::kv + st * SmemLayout::stage_bytes +
                                                                       SmemLayout::frz_band) +
                                        128 * g + r + 127;
+                    if (!exact) {
 #pragma unroll
-                    for (int h4 = 0; h4 < 4; ++h4) {
-                        uint32_t pk[16];
+                        for (int h4 = 0; h4 < 4; ++h4) {
+                            uint32_t pk[16];
 #pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            const int cc = 32 * h4 + 2 * c;
-                            const float w0 = fast_exp2(a2s[cc] + bnd[-cc] - lz2);
-                            const float w1 = fast_exp2(a2s[cc + 1] + bnd[-cc - 1] - lz2);
-                            pk[c] = pack_bf16(w0, w1);
+                            for (int c = 0; c < 16; ++c) {
+                                const int cc = 32 * h4 + 2 * c;
+                                pk[c] = pack_bf16(bnd[-cc] * a2s[cc], bnd[-cc - 1] * a2s[cc + 1]);
+                            }
+                            tmem_st16(lane_base + 128 + 16 * h4, pk);
                         }
-                        tmem_st16(lane_base + 128 + 16 * h4, pk);
+                    } else {
+#pragma unroll
+                        for (int h4 = 0; h4 < 4; ++h4) {
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int c = 0; c < 16; ++c) {
+                                const int cc = 32 * h4 + 2 * c;
+                                const float w0 = fast_exp2(a2s[cc] + bnd[-cc] - lz2);
+                                const float w1 = fast_exp2(a2s[cc + 1] + bnd[-cc - 1] - lz2);
+                                pk[c] = pack_bf16(w0, w1);
+                            }
+                            tmem_st16(lane_base + 128 + 16 * h4, pk);
+                        }
                     }
                 }
                 tmem_st_wait();
@@ -408,7 +439,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             tmem_ld_wait();
             tc_fence_before();
             if (row < p.T) {
-                const float inv = it.frozen ? 1.f : 1.f / l;
+                // ordinary: 1 / l; frozen: W rows sum to one in the exact form, and
+                // carry the factor Z'(i) in the factorised form
+                const float inv = it.frozen ? (exact ? 1.f : iz) : 1.f / l;
                 uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)bh * p.T + row) * 64);
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
@@ -450,6 +483,10 @@ cudaError_t launch_tc_fwd(const LayerArgs& a, cudaStream_t s) {
     p.lz = a.lz;
     p.a2p = a.a2p;
     p.r2p = a.r2p;
+    p.eap = a.eap;
+    p.erp = a.erp;
+    p.invz = a.invz;
+    p.hflag = a.hflag;
     p.status = a.status;
     p.B = a.B;
     p.H = a.H;

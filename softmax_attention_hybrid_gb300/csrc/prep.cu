@@ -3,9 +3,9 @@
 //  * lognorm: the row normalisers log Z(i) of every frozen head
 //    ("When Can Attention Heads Be Statically Defined?", §3.2 Eq. 3; §3.3
 //    "precomputed normalisers"). They do not depend on the batch.
-//  * pattern_prep: a and r of the frozen heads scaled by log2(e) and padded
-//    with -inf, laid out so that every tile of the tensor-core kernels reads
-//    its slice with one aligned bulk copy.
+//  * frozen_prep: per frozen head, a and r in the exact (log2) and the
+//    factorised form of Eq. 3, padded so that every tile of the tensor-core
+//    kernels reads its slice with one aligned bulk copy.
 //  * bwd_delta / bwd_rowvec: D_i = sum_c dO_ic O_ic for the ordinary-head
 //    backward (the softmax Jacobian term of Eqs. 5-7 differentiated; App. D.2),
 //    the latter together with lse * log2(e) in the per-tile layout of the
@@ -109,20 +109,59 @@ lognorm_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all,
     lz[(size_t)h * T + i] = out;
 }
 
-// a2p[h][j] = a[h][j] log2(e) for j < T, -inf for T <= j < Tp;
-// r2p[h][u] = r[h][u - 127] log2(e) for 0 <= u - 127 < T, -inf otherwise,
-// u < Tp + 256. Frozen heads only. Grid (ceil((Tp + 256) / 256), H).
-__global__ void __launch_bounds__(kPrepThreads)
-pattern_prep_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all, int ld, HeadMask mask,
-                    int T, int Tp, float* __restrict__ a2p, float* __restrict__ r2p) {
-    const int h = blockIdx.y;
+// Per frozen head, the slices that the tensor-core kernels read with aligned
+// bulk copies, in two forms of Eq. 3:
+//  exact form (log2 domain, -inf padded):
+//    a2p[j] = a[j] log2(e) (j < T),   r2p[u] = r[u - 127] log2(e) (0 <= u - 127 < T)
+//  factorised form, W(i, k) = er[i - k] ea[k] / Z'(i) with A = max a, R = max r:
+//    eap[j] = exp(a[j] - A) (j < T, else 0),  erp[u] = exp(r[u - 127] - R) (else 0),
+//    invz[i] = 1 / Z'(i) = exp(A + R - log Z(i)) (i < T, else 0).
+// The factorised form is exact up to rounding while every row keeps a term
+// within the normal fp32 range; a head with some log Z(i) - A - R < -64
+// (Z' < 1.6e-28) is flagged (hflag bit 1) and the kernels use the exact form.
+// log Z comes from lz_src (row stride lz_stride): the lognorm output in the
+// forward pass, the frozen rows of lse (batch entry 0) in the backward pass.
+// Grid (H); 512 threads; padded lengths Tp (a, invz) and Tp + 256 (r).
+__global__ void __launch_bounds__(512)
+frozen_prep_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all, int ld, HeadMask mask, int T,
+                   int Tp, const float* __restrict__ lz_src, long long lz_stride, float* __restrict__ a2p,
+                   float* __restrict__ r2p, float* __restrict__ eap, float* __restrict__ erp,
+                   float* __restrict__ invz, uint32_t* __restrict__ hflag) {
+    const int h = blockIdx.x;
     if (!head_frozen(mask, h)) return;
-    const int u = blockIdx.x * kPrepThreads + threadIdx.x;
-    if (u < Tp) a2p[(size_t)h * Tp + u] = u < T ? a_all[(size_t)h * ld + u] * kLog2e : -INFINITY;
-    if (u < Tp + 256) {
-        const int dl = u - 127;
-        r2p[(size_t)h * (Tp + 256) + u] = (dl >= 0 && dl < T) ? r_all[(size_t)h * ld + dl] * kLog2e : -INFINITY;
+    const float* a = a_all + (size_t)h * ld;
+    const float* r = r_all + (size_t)h * ld;
+    const float* lz = lz_src + (size_t)h * lz_stride;
+    __shared__ float red[32];
+    __shared__ int bad;
+    if (threadIdx.x == 0) bad = 0;
+    float ma = -INFINITY, mr = -INFINITY;
+    for (int j = threadIdx.x; j < T; j += blockDim.x) {
+        ma = fmaxf(ma, a[j]);
+        mr = fmaxf(mr, r[j]);
     }
+    const float A = block_max(ma, red);
+    const float R = block_max(mr, red);
+    const size_t ra = (size_t)h * Tp, rr = (size_t)h * (Tp + 256);
+    for (int u = threadIdx.x; u < Tp + 256; u += blockDim.x) {
+        const int dl = u - 127;
+        const bool in = dl >= 0 && dl < T;
+        r2p[rr + u] = in ? r[dl] * kLog2e : -INFINITY;
+        erp[rr + u] = in ? expf(r[dl] - R) : 0.f;
+        if (u < Tp) {
+            a2p[ra + u] = u < T ? a[u] * kLog2e : -INFINITY;
+            eap[ra + u] = u < T ? expf(a[u] - A) : 0.f;
+            float iz = 0.f;
+            if (u < T) {
+                const float sh = lz[u] - A - R;   // log Z'(u)
+                if (!(sh >= -64.f)) bad = 1;
+                iz = expf(fminf(-sh, 80.f));
+            }
+            invz[ra + u] = iz;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && bad) atomicOr(hflag + h, 2u);
 }
 
 // D_i = sum_c dO_ic * O_ic, one warp per row (d = 64: two elements per lane).
@@ -178,11 +217,11 @@ cudaError_t launch_lognorm(const LayerArgs& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_pattern_prep(const LayerArgs& p, cudaStream_t s) {
+cudaError_t launch_pattern_prep(const LayerArgs& p, const float* lz_src, long long lz_stride, cudaStream_t s) {
     const int Tp = (p.T + 127) / 128 * 128;
-    dim3 grid((Tp + 256 + kPrepThreads - 1) / kPrepThreads, p.H);
     before_launch(SAF_KERNEL_PATTERN_PREP, s);
-    pattern_prep_kernel<<<grid, kPrepThreads, 0, s>>>(p.a, p.r, p.ld_prior, p.mask, p.T, Tp, p.a2p, p.r2p);
+    frozen_prep_kernel<<<p.H, 512, 0, s>>>(p.a, p.r, p.ld_prior, p.mask, p.T, Tp, lz_src, lz_stride, p.a2p, p.r2p,
+                                           p.eap, p.erp, p.invz, p.hflag);
     after_launch(SAF_KERNEL_PATTERN_PREP, s);
     return cudaGetLastError();
 }

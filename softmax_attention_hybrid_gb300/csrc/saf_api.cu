@@ -23,6 +23,12 @@ WorkspaceLayout workspace_layout(int B, int H, int T, int backward, int bf16) {
         off = align_up(off + (size_t)H * Tp * sizeof(float), 256);
         L.r2p = off;
         off = align_up(off + (size_t)H * (Tp + 256) * sizeof(float), 256);
+        L.eap = off;
+        off = align_up(off + (size_t)H * Tp * sizeof(float), 256);
+        L.erp = off;
+        off = align_up(off + (size_t)H * (Tp + 256) * sizeof(float), 256);
+        L.invz = off;
+        off = align_up(off + (size_t)H * Tp * sizeof(float), 256);
     }
     if (backward) {
         if (bf16) {
@@ -134,6 +140,9 @@ LayerArgs make_args(const void* q, const void* k, const void* v, const float* a,
     p.rowvec = (backward && bf16) ? (float*)(ws + L.rowvec) : nullptr;
     p.a2p = bf16 ? (float*)(ws + L.a2p) : nullptr;
     p.r2p = bf16 ? (float*)(ws + L.r2p) : nullptr;
+    p.eap = bf16 ? (float*)(ws + L.eap) : nullptr;
+    p.erp = bf16 ? (float*)(ws + L.erp) : nullptr;
+    p.invz = bf16 ? (float*)(ws + L.invz) : nullptr;
     return p;
 }
 
@@ -156,8 +165,11 @@ cudaError_t begin_call(const LayerArgs& p, const Common& c, bool backward, bool 
         e = launch_lognorm(p, s);
         if (e != cudaSuccess) return e;
     }
-    if (bf16) return launch_pattern_prep(p, s);
-    return cudaSuccess;
+    if (!bf16) return cudaSuccess;
+    // log Z per row: the forward computed it above; the backward reads it from
+    // the frozen rows of lse (batch entry 0, identical for every batch entry)
+    if (backward) return launch_pattern_prep(p, p.lse, (long long)p.T, s);
+    return launch_pattern_prep(p, p.lz, (long long)p.T, s);
 }
 
 }  // namespace

@@ -37,6 +37,8 @@ __host__ __device__ inline bool head_frozen(const HeadMask& m, int h) {
 enum : uint32_t {
     kStatusRange = 1u << 0,     // info: a frozen head left the factorised form's range and
                                 // is computed in the exact exp form (not an error)
+// per-head flags (hflag[h]): bit 0 the normaliser prep needed its exact
+// fallback, bit 1 the tensor-core kernels must use the exact form
     kStatusTimeout = 1u << 1,   // a bounded mbarrier wait expired
 };
 constexpr size_t kStatusBytes = 256;
@@ -51,6 +53,9 @@ struct WorkspaceLayout {
     size_t hflag = 0;    // uint32 [H]    per-head flags raised by the normaliser prep
     size_t a2p = 0;      // fp32 [H, Tp]  a * log2(e), -inf padded (bf16 path)
     size_t r2p = 0;      // fp32 [H, Tp + 256]  r * log2(e) shifted by 127, -inf padded (bf16 path)
+    size_t eap = 0;      // fp32 [H, Tp]  exp(a - max a), 0 padded (bf16 path)
+    size_t erp = 0;      // fp32 [H, Tp + 256]  exp(r - max r) shifted by 127, 0 padded (bf16 path)
+    size_t invz = 0;     // fp32 [H, Tp]  1 / Z' of the factorised form, 0 padded (bf16 path)
     size_t delta = 0;    // fp32 [B, H, T] D_i = sum_c dO_ic O_ic (fp32 backward)
     size_t rowvec = 0;   // fp32 [B, H, Tp / 128, 256] lse * log2(e) and D per query block (bf16 backward)
     size_t dq_acc = 0;   // fp32 [B, H, T, 64] dQ accumulator (bf16 backward)
@@ -79,6 +84,9 @@ struct LayerArgs {
     float* dq_acc;       // workspace: fp32 dQ accumulator [B, H, T, 64]
     float* a2p;          // workspace: padded a * log2(e) [H, Tp]
     float* r2p;          // workspace: padded r * log2(e) [H, Tp + 256]
+    float* eap;          // workspace: exp(a - max a) [H, Tp]
+    float* erp;          // workspace: exp(r - max r), shifted by 127 [H, Tp + 256]
+    float* invz;         // workspace: 1 / Z' [H, Tp]
     float* rowvec;       // workspace: per-block row vectors [B, H, Tp / 128, 256]
     uint32_t* status;    // workspace: error words
     int B, H, T, ld_prior;
@@ -94,7 +102,7 @@ void after_launch(int kernel, cudaStream_t s);
 // prep.cu
 cudaError_t launch_lognorm(const LayerArgs& p, cudaStream_t s);
 cudaError_t launch_bwd_delta(const LayerArgs& p, bool bf16, cudaStream_t s);
-cudaError_t launch_pattern_prep(const LayerArgs& p, cudaStream_t s);
+cudaError_t launch_pattern_prep(const LayerArgs& p, const float* lz_src, long long lz_stride, cudaStream_t s);
 cudaError_t launch_bwd_rowvec(const LayerArgs& p, cudaStream_t s);
 
 // fwd_tc.cu: tensor-core forward (bf16)

@@ -213,3 +213,37 @@ def test_full_size_sampled(saf, name):
         assert torch.all(out["dq"][:, fzh] == 0) and torch.all(out["dk"][:, fzh] == 0)
     for h in fzh:
         assert torch.equal(out["lse"][0, h], out["lse"][-1, h])
+
+
+def test_stiff_pattern_uses_exact_form(saf):
+    # a huge attention sink at key 0 and a steep distance penalty: rows far from
+    # the sink have Z' = Z / exp(max a + max r) far below 1e-28, so the
+    # factorised form would underflow; the kernels must switch to the exact form
+    w = custom_workload(2, 3, 600, frozen=(0, 2), slope=0.0)
+    x = make_inputs(w, seed=21)
+    x["a"][:, 0] = 100.0
+    x["r"][:] = -1.0 * torch.arange(600, dtype=torch.float32)
+    out = _run(saf, x)
+    q, k, v, do = (x[n].double().numpy() for n in ("q", "k", "v", "do"))
+    a, r = x["a"].double().numpy(), x["r"].double().numpy()
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, a, r, x["frozen"])
+    dq, dk, dv = oracle.attn_bwd(q, k, v, do, a, r, x["frozen"])
+    assert np.max(np.abs(_np(out["o"]) - o_ref)) <= 1e-2
+    assert np.max(np.abs(_np(out["lse"]) - lse_ref)) <= 1e-2
+    for nm, ref in (("dq", dq), ("dk", dk), ("dv", dv)):
+        assert np.max(np.abs(_np(out[nm]) - ref)) <= 2e-2, nm
+
+
+def test_mixed_flagged_and_factorised_heads(saf):
+    # one frozen head needs the exact form, the other uses the factorised form
+    w = custom_workload(1, 4, 700, frozen=(1, 2), slope=0.02)
+    x = make_inputs(w, seed=22)
+    x["a"][1, 0] = 100.0
+    x["r"][1] = -1.0 * torch.arange(700, dtype=torch.float32)
+    out = _run(saf, x)
+    q, k, v, do = (x[n].double().numpy() for n in ("q", "k", "v", "do"))
+    a, r = x["a"].double().numpy(), x["r"].double().numpy()
+    o_ref, _ = oracle.attn_fwd(q, k, v, a, r, x["frozen"])
+    dq, dk, dv = oracle.attn_bwd(q, k, v, do, a, r, x["frozen"])
+    assert np.max(np.abs(_np(out["o"]) - o_ref)) <= 1e-2
+    assert np.max(np.abs(_np(out["dv"]) - dv)) <= 2e-2
