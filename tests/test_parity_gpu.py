@@ -223,6 +223,8 @@ def test_stiff_pattern_uses_exact_form(saf):
     x = make_inputs(w, seed=21)
     x["a"][:, 0] = 100.0
     x["r"][:] = -1.0 * torch.arange(600, dtype=torch.float32)
+    # the sink collects about 100 rows of dO into dV of key 0; keep dV of order one
+    x["do"] = (x["do"].float() * 0.1).to(x["do"].dtype)
     out = _run(saf, x)
     q, k, v, do = (x[n].double().numpy() for n in ("q", "k", "v", "do"))
     a, r = x["a"].double().numpy(), x["r"].double().numpy()
