@@ -48,7 +48,7 @@ using namespace tc;
 
 constexpr int kTileBytes = 128 * 64 * 2;
 constexpr int kThreads = 320;
-constexpr int kStages = 2;
+constexpr int kStages = 3;
 constexpr int kRing = 4;
 constexpr int kSliceGroup = 8;
 constexpr float kScaleLog2 = 0.125f * 1.4426950408889634f;
@@ -81,9 +81,9 @@ struct BwdParams {
 };
 
 struct Smem {
-    static constexpr int kv = 0;                      // 2 buffers x (K, V)
+    static constexpr int kv = 0;                      // K, V of the current item
     static constexpr int kv_bytes = 2 * kTileBytes;
-    static constexpr int st = kv + 2 * kv_bytes;      // kStages x (Q, dO, row vectors)
+    static constexpr int st = kv + kv_bytes;          // kStages x (Q, dO, row vectors)
     static constexpr int st_vec = 2 * kTileBytes;     // offset of the 512 fp32 row vectors in a stage
     static constexpr int st_bytes = 2 * kTileBytes + 3 * 1024;   // 1024-aligned
     static constexpr int ds = st + kStages * st_bytes;            // dS, 128 x 128 bf16
@@ -133,15 +133,14 @@ __device__ __forceinline__ void named_bar_sync(int id, int n) {
 
 struct Barriers {
     uint64_t item_full[kRing], item_empty[kRing];
-    uint64_t kv_full[2], kv_empty[2];
+    uint64_t kv_full, kv_empty;
     uint64_t st_full[kStages], st_empty[kStages];
     uint64_t s_full;        // S^T and dP^T of the current tile are in TMEM
     uint64_t s_consumed;    // pattern warps have read S^T and dP^T (8 arrivals)
     uint64_t p_ready;       // P^T in TMEM and dS in shared memory (256 arrivals)
-    uint64_t p_free;        // the dV MMA has read P^T
-    uint64_t ds_free;       // the dK and dQ MMAs have read dS
-    uint64_t dq_full, dq_free;
-    uint64_t dkv_full, dkv_free;
+    uint64_t tile_done;     // every MMA of the previous tile has completed
+    uint64_t dq_free;       // dQ of the previous tile has been read out (8 arrivals)
+    uint64_t dkv_free;      // dV, dK of the previous item have been read out (8 arrivals)
 };
 
 __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_constant__ BwdParams p) {
@@ -159,10 +158,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             mbar_init(&bars.item_full[i], 1);
             mbar_init(&bars.item_empty[i], 9);   // MMA warp + 8 pattern warps
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars.kv_full[i], 1);
-            mbar_init(&bars.kv_empty[i], 1);
-        }
+        mbar_init(&bars.kv_full, 1);
+        mbar_init(&bars.kv_empty, 1);
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&bars.st_full[i], 1);
             mbar_init(&bars.st_empty[i], 1);
@@ -170,11 +167,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         mbar_init(&bars.s_full, 1);
         mbar_init(&bars.s_consumed, 8);
         mbar_init(&bars.p_ready, 256);
-        mbar_init(&bars.p_free, 1);
-        mbar_init(&bars.ds_free, 1);
-        mbar_init(&bars.dq_full, 1);
+        mbar_init(&bars.tile_done, 1);
         mbar_init(&bars.dq_free, 8);
-        mbar_init(&bars.dkv_full, 1);
         mbar_init(&bars.dkv_free, 8);
         fence_mbar_init();
     }
@@ -197,9 +191,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             tma_prefetch_desc(&p.tm_k);
             tma_prefetch_desc(&p.tm_v);
             tma_prefetch_desc(&p.tm_do);
-            uint32_t ring_empty_bits = (1u << kRing) - 1, kv_empty_bits = 3u;
+            uint32_t ring_empty_bits = (1u << kRing) - 1, kv_empty_ph = 1;
             uint32_t st_empty_bits = (1u << kStages) - 1;
-            int slot = 0, kvbuf = 0, stage = 0;
+            int slot = 0, stage = 0;
             bool ok = true;
             while (ok) {
                 if (!(ok = mbar_wait(&bars.item_empty[slot], (ring_empty_bits >> slot) & 1u, abort, status,
@@ -215,15 +209,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 const Item it = decode_item(p, idx);
                 const int bh = it.b * p.H + it.h;
                 if (!it.frozen) {
-                    if (!(ok = mbar_wait(&bars.kv_empty[kvbuf], (kv_empty_bits >> kvbuf) & 1u, abort, status,
-                                         kStatusTimeout)))
-                        break;
-                    kv_empty_bits ^= 1u << kvbuf;
-                    uint8_t* kv = sm + Smem::kv + kvbuf * Smem::kv_bytes;
-                    mbar_expect_tx(&bars.kv_full[kvbuf], 2 * kTileBytes);
-                    tma_load_3d(kv, &p.tm_k, &bars.kv_full[kvbuf], 0, it.kb * 128, bh);
-                    tma_load_3d(kv + kTileBytes, &p.tm_v, &bars.kv_full[kvbuf], 0, it.kb * 128, bh);
-                    kvbuf ^= 1;
+                    if (!(ok = mbar_wait(&bars.kv_empty, kv_empty_ph, abort, status, kStatusTimeout))) break;
+                    kv_empty_ph ^= 1;
+                    uint8_t* kv = sm + Smem::kv;
+                    mbar_expect_tx(&bars.kv_full, 2 * kTileBytes);
+                    tma_load_3d(kv, &p.tm_k, &bars.kv_full, 0, it.kb * 128, bh);
+                    tma_load_3d(kv + kTileBytes, &p.tm_v, &bars.kv_full, 0, it.kb * 128, bh);
                 }
                 for (int qb = it.kb; qb < nqb; ++qb) {
                     if (!(ok = mbar_wait(&bars.st_empty[stage], (st_empty_bits >> stage) & 1u, abort, status,
@@ -263,11 +254,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             const uint32_t id_dv = idesc_bf16(128, 64, 0, 1);   // dV += P^T dO (dO MN-major)
             const uint32_t id_dk = idesc_bf16(128, 64, 0, 1);   // dK += dS^T Q (A K-major view, Q MN-major)
             const uint32_t id_dq = idesc_bf16(128, 64, 1, 1);   // dQ = dS K (A MN-major, K MN-major)
-            uint32_t ring_full_bits = 0, kv_full_bits = 0, st_full_bits = 0;
+            uint32_t ring_full_bits = 0, kv_full_ph = 0, st_full_bits = 0;
             uint32_t s_consumed_ph = 0, p_ready_ph = 0, dq_free_ph = 1, dkv_free_ph = 1;
-            int slot = 0, kvbuf = 0, stage = 0;
+            int slot = 0, stage = 0;
             bool ok = true;
             const uint32_t sds = smem_u32(sm + Smem::ds);
+            const uint32_t skv = smem_u32(sm + Smem::kv);
             auto st_addr = [&](int s) { return smem_u32(sm + Smem::st + s * Smem::st_bytes); };
             auto wait_st = [&](int s) -> bool {
                 if (!mbar_wait(&bars.st_full[s], (st_full_bits >> s) & 1u, abort, status, kStatusTimeout))
@@ -275,6 +267,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 st_full_bits ^= 1u << s;
                 tc_fence_after();
                 return true;
+            };
+            auto issue_s_dp = [&](int s) {
+                const uint32_t sq = st_addr(s), sdo = sq + kTileBytes;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_ss(tmem + kColS, sdesc_sw128(skv + 32 * k, 16, 1024), sdesc_sw128(sq + 32 * k, 16, 1024),
+                           id_s, k > 0);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_ss(tmem + kColDP, sdesc_sw128(skv + kTileBytes + 32 * k, 16, 1024),
+                           sdesc_sw128(sdo + 32 * k, 16, 1024), id_s, k > 0);
+                mma_commit(&bars.s_full);
             };
             while (ok) {
                 if (!(ok = mbar_wait(&bars.item_full[slot], (ring_full_bits >> slot) & 1u, abort, status,
@@ -287,24 +291,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 if (idx < 0) break;
                 const Item it = decode_item(p, idx);
                 const int n = nqb - it.kb;
-                const uint32_t skv = smem_u32(sm + Smem::kv + kvbuf * Smem::kv_bytes);
-                auto issue_s_dp = [&](int s) {
-                    const uint32_t sq = st_addr(s), sdo = sq + kTileBytes;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_ss(tmem + kColS, sdesc_sw128(skv + 32 * k, 16, 1024), sdesc_sw128(sq + 32 * k, 16, 1024),
-                               id_s, k > 0);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_ss(tmem + kColDP, sdesc_sw128(skv + kTileBytes + 32 * k, 16, 1024),
-                               sdesc_sw128(sdo + 32 * k, 16, 1024), id_s, k > 0);
-                    mma_commit(&bars.s_full);
-                };
                 if (!it.frozen) {
-                    if (!(ok = mbar_wait(&bars.kv_full[kvbuf], (kv_full_bits >> kvbuf) & 1u, abort, status,
-                                         kStatusTimeout)))
-                        break;
-                    kv_full_bits ^= 1u << kvbuf;
+                    if (!(ok = mbar_wait(&bars.kv_full, kv_full_ph, abort, status, kStatusTimeout))) break;
+                    kv_full_ph ^= 1;
                     if (!(ok = wait_st(stage))) break;
                     issue_s_dp(stage);
                 }
@@ -338,13 +327,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                     for (int k = 0; k < 8; ++k)
                         mma_ts(tmem + kColDV, tmem + kColP + 8 * k, sdesc_sw128(sdo + 2048 * k, 16384, 1024), id_dv,
                                (i > 0 || k > 0) ? 1u : 0u);
-                    mma_commit(&bars.p_free);
                     if (!it.frozen) {
                         // dK += dS^T Q: dS viewed K-major (keys x queries, two 64-query halves)
 #pragma unroll
                         for (int k = 0; k < 8; ++k)
                             mma_ss(tmem + kColDK, sdesc_sw128(sds + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
                                    sdesc_sw128(sq + 2048 * k, 16384, 1024), id_dk, (i > 0 || k > 0) ? 1u : 0u);
+                        // dQ may be overwritten once the previous tile's dQ has been read out
                         if (!(ok = mbar_wait(&bars.dq_free, dq_free_ph, abort, status, kStatusTimeout))) break;
                         dq_free_ph ^= 1;
                         tc_fence_after();
@@ -353,40 +342,42 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                         for (int k = 0; k < 8; ++k)
                             mma_ss(tmem + kColDQ, sdesc_sw128(sds + 2048 * k, 16384, 1024),
                                    sdesc_sw128(skv + 2048 * k, 16384, 1024), id_dq, k > 0);
-                        mma_commit(&bars.dq_full);
-                        mma_commit(&bars.ds_free);
                     }
+                    mma_commit(&bars.tile_done);
                     mma_commit(&bars.st_empty[s]);
                     stage = s_next;
                 }
                 if (!ok) break;
-                mma_commit(&bars.dkv_full);
-                if (!it.frozen) {
-                    mma_commit(&bars.kv_empty[kvbuf]);
-                    kvbuf ^= 1;
-                }
+                if (!it.frozen) mma_commit(&bars.kv_empty);
             }
         }
-    } else if (warp < 8) {
+    } else {
         // ---------------------------------------------------------------- pattern warps
         const int quarter = warp & 3, half = warp >> 2;
         const int j = quarter * 32 + lane;                   // key row of the block = TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         uint32_t ring_full_bits = 0, st_full_bits = 0;
-        uint32_t s_full_ph = 0, p_free_ph = 1, ds_free_ph = 1, dq_full_ph = 0, dkv_full_ph = 0;
+        uint32_t s_full_ph = 0, tile_done_ph = 0;
+        bool pending = false;   // a tile_done commit is outstanding for the last tile we handed over
         int slot = 0, stage = 0;
         bool ok = true;
         uint8_t* dsp = sm + Smem::ds + half * 16384;          // my 64-query half of dS (MN-major atom)
-
         uint8_t* dqs = sm + Smem::dqs + half * 16384;         // staging of my 32 dQ columns (SW128 rows)
         const bool dq_issuer = quarter == 0 && lane == 0;     // issues the bulk reduce of this half
 
+        // The previous tile's MMAs have all completed: P^T, dS may be overwritten
+        // and its dQ (ordinary tiles) can be read out.
+        auto wait_tile_done = [&]() -> bool {
+            if (!pending) return true;
+            if (!mbar_wait(&bars.tile_done, tile_done_ph, abort, status, kStatusTimeout)) return false;
+            tile_done_ph ^= 1;
+            pending = false;
+            tc_fence_after();
+            return true;
+        };
         // Drain dQ of tile (bh, qb) into the fp32 accumulator with a bulk tensor
         // reduce-add: rows 32*quarter + lane, d-columns 32*half .. +31.
-        auto drain_dq = [&](int bh, int qb) -> bool {
-            if (!mbar_wait(&bars.dq_full, dq_full_ph, abort, status, kStatusTimeout)) return false;
-            dq_full_ph ^= 1;
-            tc_fence_after();
+        auto drain_dq = [&](int bh, int qb) {
             uint32_t v[32];
             tmem_ld32(lane_base + kColDQ + 32 * half, v);
             tmem_ld_wait();
@@ -405,7 +396,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 tma_reduce_add_3d(&p.tm_dq, dqs, 32 * half, qb * 128, bh);
                 bulk_commit_group();
             }
-            return true;
         };
 
         while (ok) {
@@ -460,6 +450,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                             pk[e >> 1] = pack_bf16(p0, p1);
                         }
                     }
+                    // the previous tile's MMAs are done: its dQ (same item) goes out first,
+                    // then P^T and dS of this tile overwrite the previous ones
+                    if (!(ok = wait_tile_done())) break;
+                    if (i > 0) drain_dq(bh, qb - 1);
                     uint32_t dp[64];
                     tmem_ld32(lane_base + kColDP + 64 * half, dp);
                     tmem_ld32(lane_base + kColDP + 64 * half + 32, dp + 32);
@@ -467,13 +461,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars.s_consumed);
-                    // P^T may be overwritten once the previous tile's dV MMA has read it, and
-                    // dS once the previous tile's dK and dQ MMAs have
-                    if (!(ok = mbar_wait(&bars.p_free, p_free_ph, abort, status, kStatusTimeout))) break;
-                    p_free_ph ^= 1;
-                    if (!(ok = mbar_wait(&bars.ds_free, ds_free_ph, abort, status, kStatusTimeout))) break;
-                    ds_free_ph ^= 1;
-                    tc_fence_after();
                     tmem_st32(lane_base + kColP + 32 * half, pk);
 #pragma unroll
                     for (int g2 = 0; g2 < 2; ++g2) {
@@ -489,53 +476,47 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                             const float d1 = p1 * (__uint_as_float(dp[c + 1]) - vec[128 + q0 + 1]);
                             dk[e >> 1] = pack_bf16(d0, d1);
                         }
+                        // dS row j, queries 64*half + 32*g2 .. +31: MN-major atom `half`, K-row j
 #pragma unroll
                         for (int t = 0; t < 4; ++t)
                             *reinterpret_cast<uint4*>(dsp + sw128_offset(j, 16 * (4 * g2 + t))) =
                                 make_uint4(dk[4 * t], dk[4 * t + 1], dk[4 * t + 2], dk[4 * t + 3]);
                     }
                 } else {
-                    if (!(ok = mbar_wait(&bars.p_free, p_free_ph, abort, status, kStatusTimeout))) break;
-                    p_free_ph ^= 1;
-                    tc_fence_after();
                     // W^T(j, q) = W(q, j) (Eq. 3); band[q] is r at offset q - j = (qb - kb) * 128 +
                     // q - j. Factorised: W(q, j) / exp(a[j] - A) = exp(r[q-j] - R) / Z'(q), no exp per
                     // element (exp(a[j] - A) is applied to dV). Exact: exp(a[j] + r[q-j] - log Z(q)).
                     const float* band = vec + 256 + 127 - j;
+                    uint32_t pk[32];
+                    if (!exact) {
 #pragma unroll
-                    for (int g2 = 0; g2 < 2; ++g2) {
-                        uint32_t pk[16];
-                        if (!exact) {
-#pragma unroll
-                            for (int e = 0; e < 32; e += 2) {
-                                const int q0 = 64 * half + 32 * g2 + e;
-                                pk[e >> 1] = pack_bf16(band[q0] * vec[q0], band[q0 + 1] * vec[q0 + 1]);
-                            }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 32; e += 2) {
-                                const int q0 = 64 * half + 32 * g2 + e;
-                                const float w0 = fast_exp2(a2j + band[q0] - vec[q0]);
-                                const float w1 = fast_exp2(a2j + band[q0 + 1] - vec[q0 + 1]);
-                                pk[e >> 1] = pack_bf16(w0, w1);
-                            }
+                        for (int e = 0; e < 64; e += 2) {
+                            const int q0 = 64 * half + e;
+                            pk[e >> 1] = pack_bf16(band[q0] * vec[q0], band[q0 + 1] * vec[q0 + 1]);
                         }
-                        tmem_st16(lane_base + kColP + 32 * half + 16 * g2, pk);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 64; e += 2) {
+                            const int q0 = 64 * half + e;
+                            const float w0 = fast_exp2(a2j + band[q0] - vec[q0]);
+                            const float w1 = fast_exp2(a2j + band[q0 + 1] - vec[q0 + 1]);
+                            pk[e >> 1] = pack_bf16(w0, w1);
+                        }
                     }
+                    if (!(ok = wait_tile_done())) break;
+                    tmem_st32(lane_base + kColP + 32 * half, pk);
                 }
                 tmem_st_wait();
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(&bars.p_ready);
+                pending = true;
                 stage = (stage + 1) % kStages;
-                if (!it.frozen && i > 0 && !(ok = drain_dq(bh, qb - 1))) break;
             }
             if (!ok) break;
-            if (!it.frozen && !(ok = drain_dq(bh, nqb - 1))) break;
-            // dV and dK rows of this key block: my 32 d-columns
-            if (!(ok = mbar_wait(&bars.dkv_full, dkv_full_ph, abort, status, kStatusTimeout))) break;
-            dkv_full_ph ^= 1;
-            tc_fence_after();
+            // all MMAs of this item done: the last dQ, then the dV and dK rows (my 32 d-columns)
+            if (!(ok = wait_tile_done())) break;
+            if (!it.frozen) drain_dq(bh, nqb - 1);
             uint32_t dv[32], dk[32];
             tmem_ld32(lane_base + kColDV + 32 * half, dv);
             if (!it.frozen) tmem_ld32(lane_base + kColDK + 32 * half, dk);
