@@ -127,6 +127,33 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// Two fp32 lanes per instruction (f32x2 arithmetic of sm_100 and later).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 neg2(float2 a) { return make_float2(-a.x, -a.y); }
+
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -135,8 +162,10 @@ struct Barriers {
     uint64_t item_full[kRing], item_empty[kRing];
     uint64_t kv_full, kv_empty;
     uint64_t st_full[kStages], st_empty[kStages];
-    uint64_t s_full;        // S^T and dP^T of the current tile are in TMEM
-    uint64_t s_consumed;    // pattern warps have read S^T and dP^T (8 arrivals)
+    uint64_t s_full;        // S^T of the current tile is in TMEM
+    uint64_t dp_full;       // dP^T of the current tile is in TMEM
+    uint64_t s_consumed;    // pattern warps have read S^T (8 arrivals)
+    uint64_t dp_consumed;   // pattern warps have read dP^T (8 arrivals)
     uint64_t p_ready;       // P^T in TMEM and dS in shared memory (256 arrivals)
     uint64_t tile_done;     // every MMA of the previous tile has completed
     uint64_t dq_free;       // dQ of the previous tile has been read out (8 arrivals)
@@ -165,7 +194,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             mbar_init(&bars.st_empty[i], 1);
         }
         mbar_init(&bars.s_full, 1);
+        mbar_init(&bars.dp_full, 1);
         mbar_init(&bars.s_consumed, 8);
+        mbar_init(&bars.dp_consumed, 8);
         mbar_init(&bars.p_ready, 256);
         mbar_init(&bars.tile_done, 1);
         mbar_init(&bars.dq_free, 8);
@@ -255,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             const uint32_t id_dk = idesc_bf16(128, 64, 0, 1);   // dK += dS^T Q (A K-major view, Q MN-major)
             const uint32_t id_dq = idesc_bf16(128, 64, 1, 1);   // dQ = dS K (A MN-major, K MN-major)
             uint32_t ring_full_bits = 0, kv_full_ph = 0, st_full_bits = 0;
-            uint32_t s_consumed_ph = 0, p_ready_ph = 0, dq_free_ph = 1, dkv_free_ph = 1;
+            uint32_t s_consumed_ph = 0, dp_consumed_ph = 0, p_ready_ph = 0, dq_free_ph = 1, dkv_free_ph = 1;
             int slot = 0, stage = 0;
             bool ok = true;
             const uint32_t sds = smem_u32(sm + Smem::ds);
@@ -268,17 +299,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 tc_fence_after();
                 return true;
             };
-            auto issue_s_dp = [&](int s) {
-                const uint32_t sq = st_addr(s), sdo = sq + kTileBytes;
+            auto issue_s = [&](int s) {   // S^T = K Q^T
+                const uint32_t sq = st_addr(s);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     mma_ss(tmem + kColS, sdesc_sw128(skv + 32 * k, 16, 1024), sdesc_sw128(sq + 32 * k, 16, 1024),
                            id_s, k > 0);
+                mma_commit(&bars.s_full);
+            };
+            auto issue_dp = [&](int s) {  // dP^T = V dO^T
+                const uint32_t sdo = st_addr(s) + kTileBytes;
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     mma_ss(tmem + kColDP, sdesc_sw128(skv + kTileBytes + 32 * k, 16, 1024),
                            sdesc_sw128(sdo + 32 * k, 16, 1024), id_s, k > 0);
-                mma_commit(&bars.s_full);
+                mma_commit(&bars.dp_full);
             };
             while (ok) {
                 if (!(ok = mbar_wait(&bars.item_full[slot], (ring_full_bits >> slot) & 1u, abort, status,
@@ -295,20 +330,25 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                     if (!(ok = mbar_wait(&bars.kv_full, kv_full_ph, abort, status, kStatusTimeout))) break;
                     kv_full_ph ^= 1;
                     if (!(ok = wait_st(stage))) break;
-                    issue_s_dp(stage);
+                    issue_s(stage);
+                    issue_dp(stage);
                 }
                 for (int i = 0; i < n && ok; ++i) {
                     const int s = stage;
                     const int s_next = (stage + 1) % kStages;
                     if (!it.frozen) {
-                        // S^T, dP^T of the next tile may overwrite TMEM once this tile's are read
+                        // S^T and dP^T of the next tile may overwrite TMEM once this tile's are read
                         if (!(ok = mbar_wait(&bars.s_consumed, s_consumed_ph, abort, status, kStatusTimeout))) break;
                         s_consumed_ph ^= 1;
                         tc_fence_after();
                         if (i + 1 < n) {
                             if (!(ok = wait_st(s_next))) break;
-                            issue_s_dp(s_next);
+                            issue_s(s_next);
                         }
+                        if (!(ok = mbar_wait(&bars.dp_consumed, dp_consumed_ph, abort, status, kStatusTimeout))) break;
+                        dp_consumed_ph ^= 1;
+                        tc_fence_after();
+                        if (i + 1 < n) issue_dp(s_next);
                     } else {
                         if (!(ok = wait_st(s))) break;
                     }
@@ -357,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         const int j = quarter * 32 + lane;                   // key row of the block = TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         uint32_t ring_full_bits = 0, st_full_bits = 0;
-        uint32_t s_full_ph = 0, tile_done_ph = 0;
+        uint32_t s_full_ph = 0, dp_full_ph = 0, tile_done_ph = 0;
         bool pending = false;   // a tile_done commit is outstanding for the last tile we handed over
         int slot = 0, stage = 0;
         bool ok = true;
@@ -440,11 +480,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                         tmem_ld32(lane_base + kColS + 64 * half, sv);
                         tmem_ld32(lane_base + kColS + 64 * half + 32, sv + 32);
                         tmem_ld_wait();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bars.s_consumed);   // S^T of the next tile may land
+                        const float2* lse2 = reinterpret_cast<const float2*>(vec + 64 * half);
 #pragma unroll
                         for (int e = 0; e < 64; e += 2) {
                             const int q0 = 64 * half + e;
-                            float p0 = fast_exp2(fmaf(__uint_as_float(sv[e]), kScaleLog2, -vec[q0]));
-                            float p1 = fast_exp2(fmaf(__uint_as_float(sv[e + 1]), kScaleLog2, -vec[q0 + 1]));
+                            // x = S * log2(e) / sqrt(d) - lse * log2(e), two columns per instruction
+                            const float2 x = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
+                                                   make_float2(kScaleLog2, kScaleLog2), neg2(lse2[e >> 1]));
+                            float p0 = fast_exp2(x.x);
+                            float p1 = fast_exp2(x.y);
                             if (diag && j > q0) p0 = 0.f;
                             if (diag && j > q0 + 1) p1 = 0.f;
                             pk[e >> 1] = pack_bf16(p0, p1);
@@ -454,14 +501,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                     // then P^T and dS of this tile overwrite the previous ones
                     if (!(ok = wait_tile_done())) break;
                     if (i > 0) drain_dq(bh, qb - 1);
+                    if (!(ok = mbar_wait(&bars.dp_full, dp_full_ph, abort, status, kStatusTimeout))) break;
+                    dp_full_ph ^= 1;
+                    tc_fence_after();
                     uint32_t dp[64];
                     tmem_ld32(lane_base + kColDP + 64 * half, dp);
                     tmem_ld32(lane_base + kColDP + 64 * half + 32, dp + 32);
                     tmem_ld_wait();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars.s_consumed);
+                    if (lane == 0) mbar_arrive(&bars.dp_consumed);   // dP^T of the next tile may land
                     tmem_st32(lane_base + kColP + 32 * half, pk);
+                    const float2* dvec = reinterpret_cast<const float2*>(vec + 128 + 64 * half);
 #pragma unroll
                     for (int g2 = 0; g2 < 2; ++g2) {
                         uint32_t dk[16];
@@ -470,11 +521,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                             const int c = 32 * g2 + e;
                             const int q0 = 64 * half + c;
                             // dS = P o (dP - D) with P as rounded to bf16 for the MMAs
-                            const float p0 = __uint_as_float(pk[c >> 1] << 16);
-                            const float p1 = __uint_as_float(pk[c >> 1] & 0xffff0000u);
-                            const float d0 = p0 * (__uint_as_float(dp[c]) - vec[128 + q0]);
-                            const float d1 = p1 * (__uint_as_float(dp[c + 1]) - vec[128 + q0 + 1]);
-                            dk[e >> 1] = pack_bf16(d0, d1);
+                            const float2 pp = make_float2(__uint_as_float(pk[c >> 1] << 16),
+                                                          __uint_as_float(pk[c >> 1] & 0xffff0000u));
+                            const float2 dd = fmul2(pp, fsub2(make_float2(__uint_as_float(dp[c]),
+                                                                          __uint_as_float(dp[c + 1])),
+                                                              dvec[c >> 1]));
+                            dk[e >> 1] = pack_bf16(dd.x, dd.y);
+                            (void)q0;
                         }
                         // dS row j, queries 64*half + 32*g2 .. +31: MN-major atom `half`, K-row j
 #pragma unroll
