@@ -396,6 +396,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                         for (int k = 0; k < 8; ++k)
                             mma_ss(tmem + kColDQ, sdesc_sw128(sds + 2048 * k, 16384, 1024),
                                    sdesc_sw128(skv + 2048 * k, 16384, 1024), id_dq, k > 0);
+                    } else {
+                        // frozen tile: the dS warps have taken the previous tile_done phase
+                        // (no barrier may run two phases ahead of a waiter)
+                        if (!(ok = wait(&bars.ds_ready, ds_ready_ph))) break;
                     }
                     mma_commit(&bars.tile_done);
                     mma_commit(&bars.st_empty[s]);
@@ -573,9 +577,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 p_written_ph ^= 1;
                 tc_fence_after();
                 if (it.frozen) {
+                    // nothing to compute; take the previous tile_done phase before releasing P^T
+                    // and signalling this tile, so that no barrier runs two phases ahead
+                    if (!(ok = wait_tile_done())) break;
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars.p_free);
-                    if (!(ok = wait_tile_done())) break;
+                    mbar_arrive(&bars.ds_ready);
                     pending = true;
                     stage = (stage + 1) % kStages;
                     continue;
