@@ -380,9 +380,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                                (i > 0 || k > 0) ? 1u : 0u);
                     mma_commit(&bars.p_free);
                     if (!it.frozen) {
-                        // dP^T of the next tile may land once the dS warps have read this one
-                        if (!(ok = wait(&bars.dp_consumed, dp_consumed_ph))) break;
-                        if (more) issue_dp(s_next);
                         if (!(ok = wait(&bars.ds_ready, ds_ready_ph))) break;
                         // dK += dS^T Q: dS viewed K-major (keys x queries, two 64-query halves)
 #pragma unroll
@@ -396,12 +393,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                         for (int k = 0; k < 8; ++k)
                             mma_ss(tmem + kColDQ, sdesc_sw128(sds + 2048 * k, 16384, 1024),
                                    sdesc_sw128(skv + 2048 * k, 16384, 1024), id_dq, k > 0);
+                        mma_commit(&bars.tile_done);
+                        // dP^T of the next tile (the dS warps have read this one), queued after
+                        // dK and dQ so that tile_done is not held up by it
+                        if (!(ok = wait(&bars.dp_consumed, dp_consumed_ph))) break;
+                        if (more) issue_dp(s_next);
                     } else {
                         // frozen tile: the dS warps have taken the previous tile_done phase
                         // (no barrier may run two phases ahead of a waiter)
                         if (!(ok = wait(&bars.ds_ready, ds_ready_ph))) break;
+                        mma_commit(&bars.tile_done);
                     }
-                    mma_commit(&bars.tile_done);
                     mma_commit(&bars.st_empty[s]);
                     stage = s_next;
                 }
@@ -595,28 +597,36 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 if (!(ok = mbar_wait(&bars.dp_full, dp_full_ph, abort, status, kStatusTimeout))) break;
                 dp_full_ph ^= 1;
                 tc_fence_after();
+                // 8 chunks of 16 queries; the loads of chunk c+1 are in flight while chunk c is computed
+                uint32_t dpa[16], pwa[8], dpb[16], pwb[8];
+                tmem_ld16(lane_base + kColDP, dpa);
+                tmem_ld8(lane_base + kColP, pwa);
+                tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {   // queries 32c .. 32c+31
-                    uint32_t dp[32], pw[16];
-                    tmem_ld32(lane_base + kColDP + 32 * c, dp);
-                    tmem_ld16(lane_base + kColP + 16 * c, pw);
-                    tmem_ld_wait();
-                    uint32_t dk[16];
+                for (int c = 0; c < 8; ++c) {   // queries 16c .. 16c+15
+                    uint32_t* dp = (c & 1) ? dpb : dpa;
+                    uint32_t* pw = (c & 1) ? pwb : pwa;
+                    if (c + 1 < 8) {
+                        tmem_ld16(lane_base + kColDP + 16 * (c + 1), (c & 1) ? dpa : dpb);
+                        tmem_ld8(lane_base + kColP + 8 * (c + 1), (c & 1) ? pwa : pwb);
+                    }
+                    uint32_t dk[8];
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
+                    for (int e = 0; e < 16; e += 2) {
                         // dS = P o (dP - D) with P as rounded to bf16 for the MMAs
                         const float2 pp = make_float2(__uint_as_float(pw[e >> 1] << 16),
                                                       __uint_as_float(pw[e >> 1] & 0xffff0000u));
                         const float2 dd = fmul2(pp, fsub2(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])),
-                                                          *reinterpret_cast<const float2*>(dvec + 32 * c + e)));
+                                                          *reinterpret_cast<const float2*>(dvec + 16 * c + e)));
                         dk[e >> 1] = pack_bf16(dd.x, dd.y);
                     }
-                    // dS row j, queries 32c .. 32c+31: MN-major atom c/2, K-row j
-                    uint8_t* rowp = dsbuf + (c >> 1) * 16384;
-#pragma unroll
-                    for (int t = 0; t < 4; ++t)
-                        *reinterpret_cast<uint4*>(rowp + sw128_offset(j, 16 * (4 * (c & 1) + t))) =
-                            make_uint4(dk[4 * t], dk[4 * t + 1], dk[4 * t + 2], dk[4 * t + 3]);
+                    // dS row j, queries 16c .. 16c+15: MN-major atom c/4, K-row j, chunks 2(c%4), 2(c%4)+1
+                    uint8_t* rowp = dsbuf + (c >> 2) * 16384;
+                    *reinterpret_cast<uint4*>(rowp + sw128_offset(j, 16 * (2 * (c & 3)))) =
+                        make_uint4(dk[0], dk[1], dk[2], dk[3]);
+                    *reinterpret_cast<uint4*>(rowp + sw128_offset(j, 16 * (2 * (c & 3) + 1))) =
+                        make_uint4(dk[4], dk[5], dk[6], dk[7]);
+                    if (c + 1 < 8) tmem_ld_wait();
                 }
                 tc_fence_before();
                 __syncwarp();
