@@ -47,9 +47,9 @@ namespace {
 using namespace tc;
 
 constexpr int kTileBytes = 128 * 64 * 2;
-constexpr int kThreads = 512;   // 8 P warps, 4 dS warps, producer, MMA issuer, 2 idle
-constexpr int kWarpProducer = 12;
-constexpr int kWarpMma = 13;
+constexpr int kThreads = 576;   // 8 P warps, 8 dS warps, producer, MMA issuer
+constexpr int kWarpProducer = 16;
+constexpr int kWarpMma = 17;
 constexpr int kStages = 3;
 constexpr int kRing = 4;
 constexpr int kSliceGroup = 8;
@@ -167,13 +167,13 @@ struct Barriers {
     uint64_t s_full;        // S^T of the current tile is in TMEM
     uint64_t s_consumed;    // P warps have read S^T (8 arrivals)
     uint64_t p_written;     // P^T (or W^T) of the current tile is in TMEM (8 arrivals)
-    uint64_t p_free;        // dV MMA and dS warps are done with P^T (1 commit + 4 arrivals)
+    uint64_t p_free;        // dV MMA and dS warps are done with P^T (1 commit + 8 arrivals)
     uint64_t dp_full;       // dP^T of the current tile is in TMEM
-    uint64_t dp_consumed;   // dS warps have read dP^T (4 arrivals)
-    uint64_t ds_ready;      // dS of the current tile is in shared memory (128 arrivals)
+    uint64_t dp_consumed;   // dS warps have read dP^T (8 arrivals)
+    uint64_t ds_ready;      // dS of the current tile is in shared memory (256 arrivals)
     uint64_t tile_done;     // every MMA of a tile has completed
-    uint64_t dq_free;       // dQ of the previous tile has been read out (4 arrivals)
-    uint64_t dkv_free;      // dV, dK of the previous item have been read out (4 arrivals)
+    uint64_t dq_free;       // dQ of the previous tile has been read out (8 arrivals)
+    uint64_t dkv_free;      // dV, dK of the previous item have been read out (8 arrivals)
 };
 
 __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_constant__ BwdParams p) {
@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         abort_flag = 0;
         for (int i = 0; i < kRing; ++i) {
             mbar_init(&bars.item_full[i], 1);
-            mbar_init(&bars.item_empty[i], 13);   // MMA warp + 8 P warps + 4 dS warps
+            mbar_init(&bars.item_empty[i], 17);   // MMA warp + 8 P warps + 8 dS warps
         }
         mbar_init(&bars.kv_full, 1);
         mbar_init(&bars.kv_empty, 1);
@@ -200,13 +200,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         mbar_init(&bars.s_full, 1);
         mbar_init(&bars.s_consumed, 8);
         mbar_init(&bars.p_written, 8);
-        mbar_init(&bars.p_free, 1 + 4);
+        mbar_init(&bars.p_free, 1 + 8);
         mbar_init(&bars.dp_full, 1);
-        mbar_init(&bars.dp_consumed, 4);
-        mbar_init(&bars.ds_ready, 128);
+        mbar_init(&bars.dp_consumed, 8);
+        mbar_init(&bars.ds_ready, 256);
         mbar_init(&bars.tile_done, 1);
-        mbar_init(&bars.dq_free, 4);
-        mbar_init(&bars.dkv_free, 4);
+        mbar_init(&bars.dq_free, 8);
+        mbar_init(&bars.dkv_free, 8);
         fence_mbar_init();
     }
     if (warp == kWarpMma) {
@@ -441,7 +441,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 st_full_bits ^= 1u << stage;
                 const float* vec =
                     reinterpret_cast<const float*>(sm + Smem::st + stage * Smem::st_bytes + Smem::st_vec);
-                uint32_t pk[32];   // my 64 query columns of P^T (or W^T), packed bf16 pairs
                 if (!it.frozen) {
                     if (!(ok = mbar_wait(&bars.s_full, s_full_ph, abort, status, kStatusTimeout))) break;
                     s_full_ph ^= 1;
@@ -454,44 +453,57 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars.s_consumed);   // S^T of the next tile may land
                     const float2* lse2 = reinterpret_cast<const float2*>(vec + 64 * half);
+                    // P^T may be overwritten once the previous tile's dV MMA and the dS warps are done
+                    if (!(ok = mbar_wait(&bars.p_free, p_free_ph, abort, status, kStatusTimeout))) break;
+                    p_free_ph ^= 1;
+                    tc_fence_after();
 #pragma unroll
-                    for (int e = 0; e < 64; e += 2) {
-                        const int q0 = 64 * half + e;
-                        // x = S * log2(e) / sqrt(d) - lse * log2(e), two columns per instruction
-                        const float2 x = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
-                                               make_float2(kScaleLog2, kScaleLog2), neg2(lse2[e >> 1]));
-                        float p0 = fast_exp2(x.x);
-                        float p1 = fast_exp2(x.y);
-                        if (diag && j > q0) p0 = 0.f;
-                        if (diag && j > q0 + 1) p1 = 0.f;
-                        pk[e >> 1] = pack_bf16(p0, p1);
+                    for (int g2 = 0; g2 < 2; ++g2) {
+                        uint32_t pk[16];   // packed bf16 pairs of 32 columns of P^T
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            const int c = 32 * g2 + e;
+                            const int q0 = 64 * half + c;
+                            // x = S * log2(e) / sqrt(d) - lse * log2(e), two columns per instruction
+                            const float2 x = ffma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
+                                                   make_float2(kScaleLog2, kScaleLog2), neg2(lse2[c >> 1]));
+                            float p0 = fast_exp2(x.x);
+                            float p1 = fast_exp2(x.y);
+                            if (diag && j > q0) p0 = 0.f;
+                            if (diag && j > q0 + 1) p1 = 0.f;
+                            pk[e >> 1] = pack_bf16(p0, p1);
+                        }
+                        tmem_st16(lane_base + kColP + 32 * half + 16 * g2, pk);
                     }
                 } else {
                     // W^T(j, q) = W(q, j) (Eq. 3); band[q] is r at offset q - j = (qb - kb) * 128 +
                     // q - j. Factorised: W(q, j) / exp(a[j] - A) = exp(r[q-j] - R) / Z'(q), no exp per
                     // element (exp(a[j] - A) is applied to dV). Exact: exp(a[j] + r[q-j] - log Z(q)).
                     const float* band = vec + 256 + 127 - j;
-                    if (!exact) {
+                    if (!(ok = mbar_wait(&bars.p_free, p_free_ph, abort, status, kStatusTimeout))) break;
+                    p_free_ph ^= 1;
+                    tc_fence_after();
 #pragma unroll
-                        for (int e = 0; e < 64; e += 2) {
-                            const int q0 = 64 * half + e;
-                            pk[e >> 1] = pack_bf16(band[q0] * vec[q0], band[q0 + 1] * vec[q0 + 1]);
-                        }
-                    } else {
+                    for (int g2 = 0; g2 < 2; ++g2) {
+                        uint32_t pk[16];
+                        if (!exact) {
 #pragma unroll
-                        for (int e = 0; e < 64; e += 2) {
-                            const int q0 = 64 * half + e;
-                            const float w0 = fast_exp2(a2j + band[q0] - vec[q0]);
-                            const float w1 = fast_exp2(a2j + band[q0 + 1] - vec[q0 + 1]);
-                            pk[e >> 1] = pack_bf16(w0, w1);
+                            for (int e = 0; e < 32; e += 2) {
+                                const int q0 = 64 * half + 32 * g2 + e;
+                                pk[e >> 1] = pack_bf16(band[q0] * vec[q0], band[q0 + 1] * vec[q0 + 1]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; e += 2) {
+                                const int q0 = 64 * half + 32 * g2 + e;
+                                const float w0 = fast_exp2(a2j + band[q0] - vec[q0]);
+                                const float w1 = fast_exp2(a2j + band[q0 + 1] - vec[q0 + 1]);
+                                pk[e >> 1] = pack_bf16(w0, w1);
+                            }
                         }
+                        tmem_st16(lane_base + kColP + 32 * half + 16 * g2, pk);
                     }
                 }
-                // P^T may be overwritten once the previous tile's dV MMA and the dS warps are done with it
-                if (!(ok = mbar_wait(&bars.p_free, p_free_ph, abort, status, kStatusTimeout))) break;
-                p_free_ph ^= 1;
-                tc_fence_after();
-                tmem_st32(lane_base + kColP + 32 * half, pk);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -499,10 +511,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 stage = (stage + 1) % kStages;
             }
         }
-    } else if (warp < 12) {
+    } else if (warp < 16) {
         // ---------------------------------------------------------------- dS warps
-        // warp 8 + q: key rows 32q..+31 (TMEM lane quarter q), all 128 query columns
-        const int quarter = warp & 3;
+        // warp 8 + 4h + q: key rows 32q..+31 (TMEM lane quarter q), query columns 64h..+63
+        const int quarter = warp & 3, half = (warp - 8) >> 2;
         const int j = quarter * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         uint32_t ring_full_bits = 0, st_full_bits = 0;
@@ -510,9 +522,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         bool pending = false;   // a tile_done commit is outstanding for the last tile handed over
         int slot = 0, stage = 0;
         bool ok = true;
-        uint8_t* dsbuf = sm + Smem::ds;
-        uint8_t* dqs = sm + Smem::dqs;                      // dQ staging: 2 halves x (128 rows x 32 fp32)
-        const bool dq_issuer = quarter == 0 && lane == 0;   // issues the bulk reduces
+        uint8_t* dsp = sm + Smem::ds + half * 16384;        // my 64-query half of dS (MN-major atom)
+        uint8_t* dqs = sm + Smem::dqs + half * 16384;       // staging of my 32 dQ columns (SW128 rows)
+        const bool dq_issuer = quarter == 0 && lane == 0;   // issues the bulk reduce of this half
 
         auto wait_tile_done = [&]() -> bool {
             if (!pending) return true;
@@ -522,30 +534,25 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             tc_fence_after();
             return true;
         };
-        // Drain dQ of tile (bh, qb) (rows 32*quarter + lane, all 64 d-columns) into the
-        // fp32 accumulator with two bulk tensor reduce-adds of 32 columns each.
+        // Drain dQ of tile (bh, qb) into the fp32 accumulator with a bulk tensor
+        // reduce-add: rows 32*quarter + lane, d-columns 32*half .. +31.
         auto drain_dq = [&](int bh, int qb) {
-            if (dq_issuer) bulk_wait_read_all();   // the previous reduces have read the staging buffer
-            named_bar_sync(1, 128);
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                uint32_t v[32];
-                tmem_ld32(lane_base + kColDQ + 32 * h2, v);
-                tmem_ld_wait();
-                uint8_t* dst = dqs + h2 * 16384;
-#pragma unroll
-                for (int t = 0; t < 8; ++t)
-                    *reinterpret_cast<uint4*>(dst + sw128_offset(j, 16 * t)) =
-                        make_uint4(v[4 * t], v[4 * t + 1], v[4 * t + 2], v[4 * t + 3]);
-            }
+            uint32_t v[32];
+            tmem_ld32(lane_base + kColDQ + 32 * half, v);
+            tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars.dq_free);
+            if (dq_issuer) bulk_wait_read_all();   // the previous reduce has read the staging buffer
+            named_bar_sync(1 + half, 128);
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+                *reinterpret_cast<uint4*>(dqs + sw128_offset(j, 16 * t)) =
+                    make_uint4(v[4 * t], v[4 * t + 1], v[4 * t + 2], v[4 * t + 3]);
             fence_proxy_async_smem();
-            named_bar_sync(1, 128);
+            named_bar_sync(1 + half, 128);
             if (dq_issuer) {
-                tma_reduce_add_3d(&p.tm_dq, dqs, 0, qb * 128, bh);
-                tma_reduce_add_3d(&p.tm_dq, dqs + 16384, 32, qb * 128, bh);
+                tma_reduce_add_3d(&p.tm_dq, dqs, 32 * half, qb * 128, bh);
                 bulk_commit_group();
             }
         };
@@ -597,18 +604,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 if (!(ok = mbar_wait(&bars.dp_full, dp_full_ph, abort, status, kStatusTimeout))) break;
                 dp_full_ph ^= 1;
                 tc_fence_after();
-                // 8 chunks of 16 queries; the loads of chunk c+1 are in flight while chunk c is computed
+                // my 64 queries in 4 chunks of 16; the loads of chunk c+1 are in flight while
+                // chunk c is computed
                 uint32_t dpa[16], pwa[8], dpb[16], pwb[8];
-                tmem_ld16(lane_base + kColDP, dpa);
-                tmem_ld8(lane_base + kColP, pwa);
+                tmem_ld16(lane_base + kColDP + 64 * half, dpa);
+                tmem_ld8(lane_base + kColP + 32 * half, pwa);
                 tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {   // queries 16c .. 16c+15
+                for (int c = 0; c < 4; ++c) {   // queries 64*half + 16c .. +15
                     uint32_t* dp = (c & 1) ? dpb : dpa;
                     uint32_t* pw = (c & 1) ? pwb : pwa;
-                    if (c + 1 < 8) {
-                        tmem_ld16(lane_base + kColDP + 16 * (c + 1), (c & 1) ? dpa : dpb);
-                        tmem_ld8(lane_base + kColP + 8 * (c + 1), (c & 1) ? pwa : pwb);
+                    if (c + 1 < 4) {
+                        tmem_ld16(lane_base + kColDP + 64 * half + 16 * (c + 1), (c & 1) ? dpa : dpb);
+                        tmem_ld8(lane_base + kColP + 32 * half + 8 * (c + 1), (c & 1) ? pwa : pwb);
                     }
                     uint32_t dk[8];
 #pragma unroll
@@ -617,16 +625,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                         const float2 pp = make_float2(__uint_as_float(pw[e >> 1] << 16),
                                                       __uint_as_float(pw[e >> 1] & 0xffff0000u));
                         const float2 dd = fmul2(pp, fsub2(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])),
-                                                          *reinterpret_cast<const float2*>(dvec + 16 * c + e)));
+                                                          *reinterpret_cast<const float2*>(dvec + 64 * half + 16 * c + e)));
                         dk[e >> 1] = pack_bf16(dd.x, dd.y);
                     }
-                    // dS row j, queries 16c .. 16c+15: MN-major atom c/4, K-row j, chunks 2(c%4), 2(c%4)+1
-                    uint8_t* rowp = dsbuf + (c >> 2) * 16384;
-                    *reinterpret_cast<uint4*>(rowp + sw128_offset(j, 16 * (2 * (c & 3)))) =
+                    // dS row j, queries 64*half + 16c .. +15: MN-major atom `half`, K-row j, chunks 2c, 2c+1
+                    *reinterpret_cast<uint4*>(dsp + sw128_offset(j, 16 * (2 * c))) =
                         make_uint4(dk[0], dk[1], dk[2], dk[3]);
-                    *reinterpret_cast<uint4*>(rowp + sw128_offset(j, 16 * (2 * (c & 3) + 1))) =
+                    *reinterpret_cast<uint4*>(dsp + sw128_offset(j, 16 * (2 * c + 1))) =
                         make_uint4(dk[4], dk[5], dk[6], dk[7]);
-                    if (c + 1 < 8) tmem_ld_wait();
+                    if (c + 1 < 4) tmem_ld_wait();
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -644,8 +651,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             if (!(ok = wait_tile_done())) break;
             if (!it.frozen) drain_dq(bh, nqb - 1);
             const float fv = (it.frozen && !exact) ? eaj : 1.f;
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
+            {
+                const int h2 = half;   // my 32 d-columns of dV and dK
                 uint32_t dv[32], dk[32];
                 tmem_ld32(lane_base + kColDV + 32 * h2, dv);
                 if (!it.frozen) tmem_ld32(lane_base + kColDK + 32 * h2, dk);
