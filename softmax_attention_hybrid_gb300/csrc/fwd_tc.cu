@@ -324,22 +324,27 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     if (!(ok = mbar_wait(&bars.s_full[g], s_full_ph, abort, status, kStatusTimeout))) break;
                     s_full_ph ^= 1;
                     tc_fence_after();
-                    uint32_t sr[128];   // this row of S, then of log2-scaled scores
+                    uint32_t sr[128];   // this row of S (raw scores)
 #pragma unroll
                     for (int c0 = 0; c0 < 128; c0 += 32) tmem_ld32(lane_base + c0, sr + c0);
                     tmem_ld_wait();
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars.s_empty[g]);
-                    const bool diag = (j == qb);
-                    float mx = -INFINITY;
+                    if (j == qb) {
+                        // causal mask on the diagonal tile: keys c > r are dropped
 #pragma unroll
-                    for (int c = 0; c < 128; ++c) {
-                        float x = __uint_as_float(sr[c]) * kScaleLog2;
-                        if (diag && c > r) x = -INFINITY;   // causal mask on the diagonal tile
-                        sr[c] = __float_as_uint(x);
-                        mx = fmaxf(mx, x);
+                        for (int c = 0; c < 128; ++c)
+                            if (c > r) sr[c] = __float_as_uint(-INFINITY);
                     }
+                    // row max of the raw scores (the scale is positive): two chains of 3-input max
+                    float ma = -INFINITY, mb = -INFINITY;
+#pragma unroll
+                    for (int c = 0; c < 128; c += 4) {
+                        ma = fmax3(ma, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+                        mb = fmax3(mb, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+                    }
+                    const float mx = fmaxf(ma, mb) * kScaleLog2;
                     if (j > 0) {   // P V of the previous block done: P is free, O is stable
                         if (!(ok = mbar_wait(&bars.o_done[g], o_done_ph, abort, status, kStatusTimeout))) break;
                         o_done_ph ^= 1;
@@ -363,20 +368,28 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         l *= fast_exp2(m_used - m_new);
                         m_used = m_new;
                     }
-                    float ls = 0.f;
+                    // P = 2^(S log2(e) / sqrt(d) - m): two columns per FFMA and per FADD
+                    const float2 sc2 = make_float2(kScaleLog2, kScaleLog2);
+                    const float2 nm2 = make_float2(-m_used, -m_used);
+                    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
                     for (int h4 = 0; h4 < 4; ++h4) {
                         uint32_t pk[16];   // packed bf16 pairs of 32 columns of P
 #pragma unroll
                         for (int c = 0; c < 16; ++c) {
-                            const float p0 = fast_exp2(__uint_as_float(sr[32 * h4 + 2 * c]) - m_used);
-                            const float p1 = fast_exp2(__uint_as_float(sr[32 * h4 + 2 * c + 1]) - m_used);
-                            ls += p0 + p1;
-                            pk[c] = pack_bf16(p0, p1);
+                            const int cc = 32 * h4 + 2 * c;
+                            const float2 x =
+                                ffma2(make_float2(__uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1])), sc2, nm2);
+                            const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                            if (c & 1)
+                                acc1 = fadd2(acc1, e);
+                            else
+                                acc0 = fadd2(acc0, e);
+                            pk[c] = pack_bf16(e.x, e.y);
                         }
                         tmem_st16(lane_base + 128 + 16 * h4, pk);
                     }
-                    l += ls;
+                    l += (acc0.x + acc1.x) + (acc0.y + acc1.y);
                 } else {
                     // Frozen tile of Eq. 3 from the key block's a values and the band of r values
                     // the producer staged in the K slot. Factorised form: W(i, k) Z'(i) =

@@ -17,7 +17,6 @@
 namespace saf {
 namespace {
 
-constexpr int kPrepThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ float block_max(float x, float* red) {
@@ -44,8 +43,12 @@ __device__ float block_max(float x, float* red) {
 // left the normal fp32 range; that row is recomputed exactly by a running
 // log-sum-exp and the head is flagged (kStatusRange, informational).
 //
-// Grid: (ceil(T / 256), H); one thread per row i of head h.
-__global__ void __launch_bounds__(kPrepThreads)
+// Grid: (ceil(T / 128), H); 1024 threads, 8 per row (each sums every 8th
+// key). Keys are taken in chunks of kLzChunk: ea of the chunk and er of the
+// offsets that the block's rows need against it are staged in shared memory.
+constexpr int kLzRows = 128, kLzSplit = 8, kLzThreads = kLzRows * kLzSplit, kLzChunk = 2048;
+
+__global__ void __launch_bounds__(kLzThreads)
 lognorm_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all, int ld, HeadMask mask,
                int T, float* __restrict__ lz, uint32_t* __restrict__ hflag, uint32_t* __restrict__ status) {
     const int h = blockIdx.y;
@@ -53,8 +56,8 @@ lognorm_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all,
     const float* a = a_all + (size_t)h * ld;
     const float* r = r_all + (size_t)h * ld;
     __shared__ float red[32];
-    __shared__ float ea_s[kPrepThreads];
-    __shared__ float er_s[2 * kPrepThreads];
+    __shared__ float ea_s[kLzChunk];
+    __shared__ float er_s[kLzChunk + kLzRows];
 
     float ma = -INFINITY, mr = -INFINITY;
     for (int j = threadIdx.x; j < T; j += blockDim.x) {
@@ -64,29 +67,32 @@ lognorm_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all,
     const float A = block_max(ma, red);
     const float R = block_max(mr, red);
 
-    const int i0 = blockIdx.x * kPrepThreads;
-    const int i = i0 + threadIdx.x;
-    const int imax = min(i0 + kPrepThreads - 1, T - 1);
+    const int i0 = blockIdx.x * kLzRows;
+    const int imax = min(i0 + kLzRows, T) - 1;
+    const int i = i0 + (threadIdx.x >> 3), sp = threadIdx.x & 7;
     float z = 0.f;
-    for (int j0 = 0; j0 <= imax; j0 += kPrepThreads) {
-        const int jt = j0 + threadIdx.x;
-        ea_s[threadIdx.x] = (jt <= imax) ? expf(a[jt] - A) : 0.f;
-        // offsets needed by rows i0..i0+255 against keys j0..j0+255
-        const int base = i0 - j0 - (kPrepThreads - 1);
-        for (int t = threadIdx.x; t < 2 * kPrepThreads; t += blockDim.x) {
-            const int dlt = base + t;
-            er_s[t] = (dlt >= 0 && dlt < T) ? expf(r[dlt] - R) : 0.f;
+    for (int j0 = 0; j0 <= imax; j0 += kLzChunk) {
+        // er_s[t] = er at offset i0 - j0 - kLzChunk + 1 + t (0 outside [0, T))
+        const int base = i0 - j0 - kLzChunk + 1;
+        for (int t = threadIdx.x; t < kLzChunk + kLzRows; t += blockDim.x) {
+            if (t < kLzChunk) ea_s[t] = (j0 + t <= imax) ? expf(a[j0 + t] - A) : 0.f;
+            const int dl = base + t;
+            er_s[t] = (dl >= 0 && dl < T) ? expf(r[dl] - R) : 0.f;
         }
         __syncthreads();
         if (i < T) {
-            // er_s[(i - j) - base] with j = j0 + jj; keys j > i meet er_s = 0 (negative offset).
-            const float* e = er_s + (i - i0) + (kPrepThreads - 1);
-#pragma unroll 8
-            for (int jj = 0; jj < kPrepThreads; ++jj) z = fmaf(ea_s[jj], e[-jj], z);
+            // key j = j0 + jj meets offset i - j, i.e. er_s[(i - i0) + kLzChunk - 1 - jj]
+            const float* e = er_s + (i - i0) + kLzChunk - 1;
+            const int jend = min(kLzChunk - 1, i - j0);
+#pragma unroll 4
+            for (int jj = sp; jj <= jend; jj += kLzSplit) z = fmaf(ea_s[jj], e[-jj], z);
         }
         __syncthreads();
     }
-    if (i >= T) return;
+    z += __shfl_xor_sync(0xffffffffu, z, 1);
+    z += __shfl_xor_sync(0xffffffffu, z, 2);
+    z += __shfl_xor_sync(0xffffffffu, z, 4);
+    if (i >= T || sp != 0) return;
     float out;
     if (z >= 1e-28f) {
         out = logf(z) + A + R;
@@ -182,25 +188,33 @@ bwd_delta_kernel(const E* __restrict__ o, const E* __restrict__ dO, float* __res
 // Per-tile row vectors of the tensor-core backward: for slice bh and query
 // block qb, rowvec[(bh * nqb + qb) * 256 + u] holds lse * log2(e) of query
 // qb*128 + u (u < 128; +inf past T) and, at u + 128, D of that query (0 past
-// T; frozen heads skip the dot product). One warp per padded row; grid
-// (ceil(Tp / 8), B*H).
+// T; frozen heads skip the dot product). Four threads per padded row, each
+// reading 32 contiguous bytes of O and dO (a warp reads 1 KB of each);
+// grid (nqb * 128 / 64, B*H), 256 threads.
 __global__ void __launch_bounds__(256)
 bwd_rowvec_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dO,
                   const float* __restrict__ lse, HeadMask mask, int H, int T, int nqb, float* __restrict__ rowvec) {
     const int bh = blockIdx.y;
-    const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (i >= nqb * 128) return;
+    const int i = blockIdx.x * 64 + (threadIdx.x >> 2);
+    const int part = threadIdx.x & 3;
     const bool frozen = head_frozen(mask, bh % H);
     float d = 0.f;
     if (i < T && !frozen) {
         const size_t row = (size_t)bh * T + i;
-        const __nv_bfloat162 x = reinterpret_cast<const __nv_bfloat162*>(o + row * kHeadDim)[lane];
-        const __nv_bfloat162 y = reinterpret_cast<const __nv_bfloat162*>(dO + row * kHeadDim)[lane];
-        d = __bfloat162float(x.x) * __bfloat162float(y.x) + __bfloat162float(x.y) * __bfloat162float(y.y);
-        for (int s = 16; s > 0; s >>= 1) d += __shfl_xor_sync(0xffffffffu, d, s);
+        const uint4* po = reinterpret_cast<const uint4*>(o + row * kHeadDim) + 2 * part;
+        const uint4* pd = reinterpret_cast<const uint4*>(dO + row * kHeadDim) + 2 * part;
+        const uint4 x0 = __ldg(po), x1 = __ldg(po + 1), y0 = __ldg(pd), y1 = __ldg(pd + 1);
+        const uint32_t xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        const uint32_t ys[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            d = fmaf(__uint_as_float(xs[e] << 16), __uint_as_float(ys[e] << 16), d);
+            d = fmaf(__uint_as_float(xs[e] & 0xffff0000u), __uint_as_float(ys[e] & 0xffff0000u), d);
+        }
     }
-    if (lane == 0) {
+    d += __shfl_xor_sync(0xffffffffu, d, 1);
+    d += __shfl_xor_sync(0xffffffffu, d, 2);
+    if (part == 0 && i < nqb * 128) {
         float* v = rowvec + ((size_t)bh * nqb + (i >> 7)) * 256;
         v[i & 127] = i < T ? lse[(size_t)bh * T + i] * kLog2e : INFINITY;
         v[128 + (i & 127)] = d;
@@ -210,9 +224,9 @@ bwd_rowvec_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __re
 }  // namespace
 
 cudaError_t launch_lognorm(const LayerArgs& p, cudaStream_t s) {
-    dim3 grid((p.T + kPrepThreads - 1) / kPrepThreads, p.H);
+    dim3 grid((p.T + kLzRows - 1) / kLzRows, p.H);
     before_launch(SAF_KERNEL_LOGNORM, s);
-    lognorm_kernel<<<grid, kPrepThreads, 0, s>>>(p.a, p.r, p.ld_prior, p.mask, p.T, p.lz, p.hflag, p.status);
+    lognorm_kernel<<<grid, kLzThreads, 0, s>>>(p.a, p.r, p.ld_prior, p.mask, p.T, p.lz, p.hflag, p.status);
     after_launch(SAF_KERNEL_LOGNORM, s);
     return cudaGetLastError();
 }
@@ -241,7 +255,7 @@ cudaError_t launch_bwd_delta(const LayerArgs& p, bool bf16, cudaStream_t s) {
 
 cudaError_t launch_bwd_rowvec(const LayerArgs& p, cudaStream_t s) {
     const int nqb = (p.T + 127) / 128;
-    dim3 grid((unsigned)(nqb * 128 / 8), p.B * p.H);
+    dim3 grid((unsigned)(nqb * 128 / 64), p.B * p.H);
     before_launch(SAF_KERNEL_BWD_DELTA, s);
     bwd_rowvec_kernel<<<grid, 256, 0, s>>>((const __nv_bfloat16*)p.o, (const __nv_bfloat16*)p.dO, p.lse, p.mask, p.H,
                                            p.T, nqb, p.rowvec);
