@@ -13,10 +13,12 @@
 // Items are ordered longest first (descending p, ordinary before frozen) and
 // dealt to the persistent CTAs in a snake order.
 //
-// Warp roles (320 threads, one CTA per SM):
+// Warp roles (352 threads, one CTA per SM):
 //   warps 0-3 / 4-7 : softmax group g = 0 / 1, thread = one query row of tile g
 //   warp 8          : TMA producer (Q tiles, K/V stages)
-//   warp 9          : tensor-memory owner and single-thread MMA issuer
+//   warps 9 / 10    : MMA issuers of tile 0 / 1 (one thread each; one thread
+//                     alone cannot issue tcgen05.mma fast enough to keep the
+//                     tensor core busy at N = 64); warp 9 owns tensor memory
 // Tensor memory (512 columns), per tile g at column 256g:
 //   [0, 128)   S = Q K^T (fp32)
 //   [128, 192) P or W (bf16 pairs), the A operand of the P V MMA
@@ -35,7 +37,7 @@ using namespace tc;
 
 constexpr int kStages = 3;
 constexpr int kTileBytes = 128 * 64 * 2;  // one 128 x 64 bf16 tile
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kScaleLog2 = 0.125f * 1.4426950408889634f;  // log2(e) / sqrt(64)
 constexpr float kRescaleThreshold = 8.0f;                    // lazy rescale: factor 256
@@ -127,10 +129,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     if (threadIdx.x == 0) {
         abort_flag = 0;
         mbar_init(&bars.q_full, 1);
-        mbar_init(&bars.q_empty, 1);
+        mbar_init(&bars.q_empty, 2);   // one commit per issuer
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&bars.kv_full[s], 1);
-            mbar_init(&bars.kv_empty[s], 1);
+            mbar_init(&bars.kv_empty[s], 2);
         }
         for (int g = 0; g < 2; ++g) {
             mbar_init(&bars.s_full[g], 1);
@@ -201,57 +203,55 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 }
             }
         }
-    } else if (warp == 9) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 9 || warp == 10) {
+        // ------------------------------------------------------------ MMA issuer of tile g
         if (lane == 0) {
+            const int g = warp - 9;
             const uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);  // S = Q K^T
             const uint32_t idesc_o = idesc_bf16(128, 64, 0, 1);   // O += P V, V MN-major
             uint32_t q_full_ph = 0;
-            uint32_t kv_full_bits = 0;           // phase parity per stage, bit s
-            uint32_t s_empty_bits = 3u;          // bit g: parity of s_empty[g]
-            uint32_t p_full_bits = 0;            // bit g: parity of p_full[g]
+            uint32_t kv_full_bits = 0;   // phase parity per stage, bit s
+            uint32_t s_empty_ph = 1, p_full_ph = 0;
             int stage = 0;
             bool ok = true;
-            const uint32_t sq = smem_u32(sm + SmemLayout::q);
+            const uint32_t sqg = smem_u32(sm + SmemLayout::q) + g * kTileBytes;
+            const uint32_t d_s = tmem + 256 * g, d_p = d_s + 128, d_o = d_s + 192;
             for (int round = 0; ok; ++round) {
                 const int idx = item_index(round, cta, grid);
                 if (idx >= p.n_items) break;
                 const Item it = decode_item(p, idx);
                 const int qb0 = 2 * it.pair, qb1 = qb0 + 1;
                 const bool t1 = qb1 < p.nqb;
-                const int n0 = qb0 + 1, n1 = t1 ? qb1 + 1 : 0;
-                const int nblk = t1 ? n1 : n0;
+                const int ng = g == 0 ? qb0 + 1 : (t1 ? qb1 + 1 : 0);   // key blocks of my tile
+                const int nblk = t1 ? qb1 + 1 : qb0 + 1;                 // key blocks of the item
                 if (!it.frozen) {
                     if (!(ok = mbar_wait(&bars.q_full, q_full_ph, abort, status, kStatusTimeout))) break;
                     q_full_ph ^= 1;
                 }
                 // stage index of block j is (stage + j) mod kStages
                 auto stage_of = [&](int j) { return (stage + j) % kStages; };
-                auto issue_s = [&](int g, int j) -> bool {
-                    if (!mbar_wait(&bars.s_empty[g], (s_empty_bits >> g) & 1u, abort, status, kStatusTimeout))
-                        return false;
-                    s_empty_bits ^= 1u << g;
+                auto issue_s = [&](int j) -> bool {
+                    if (!mbar_wait(&bars.s_empty[g], s_empty_ph, abort, status, kStatusTimeout)) return false;
+                    s_empty_ph ^= 1;
                     tc_fence_after();
                     const uint32_t sk = smem_u32(sm + SmemLayout::kv + stage_of(j) * SmemLayout::stage_bytes);
-                    const uint32_t sqg = sq + g * kTileBytes;
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        mma_ss(tmem + 256 * g, sdesc_sw128(sqg + 32 * k, 16, 1024),
-                               sdesc_sw128(sk + 32 * k, 16, 1024), idesc_s, k > 0);
+                        mma_ss(d_s, sdesc_sw128(sqg + 32 * k, 16, 1024), sdesc_sw128(sk + 32 * k, 16, 1024), idesc_s,
+                               k > 0);
                     mma_commit(&bars.s_full[g]);
                     return true;
                 };
-                auto issue_pv = [&](int g, int j) -> bool {
-                    if (!mbar_wait(&bars.p_full[g], (p_full_bits >> g) & 1u, abort, status, kStatusTimeout))
-                        return false;
-                    p_full_bits ^= 1u << g;
+                auto issue_pv = [&](int j) -> bool {
+                    if (!mbar_wait(&bars.p_full[g], p_full_ph, abort, status, kStatusTimeout)) return false;
+                    p_full_ph ^= 1;
                     tc_fence_after();
                     const uint32_t sv =
                         smem_u32(sm + SmemLayout::kv + stage_of(j) * SmemLayout::stage_bytes + kTileBytes);
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        mma_ts(tmem + 256 * g + 192, tmem + 256 * g + 128 + 8 * k,
-                               sdesc_sw128(sv + 2048 * k, 16384, 1024), idesc_o, (j > 0 || k > 0) ? 1u : 0u);
+                        mma_ts(d_o, d_p + 8 * k, sdesc_sw128(sv + 2048 * k, 16384, 1024), idesc_o,
+                               (j > 0 || k > 0) ? 1u : 0u);
                     mma_commit(&bars.o_done[g]);
                     return true;
                 };
@@ -266,20 +266,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     }
                     return true;
                 };
-                if (!(ok = ensure_kv(0))) break;
-                if (!it.frozen) {
-                    ok = issue_s(0, 0);
-                    if (ok && n1 > 0) ok = issue_s(1, 0);
-                }
-                // Per block j and tile g: the next block's S (as soon as the softmax group
-                // has read this block's S, so it runs under the softmax), then P V.
+                if (!it.frozen && ng > 0) ok = ensure_kv(0) && issue_s(0);
+                // Per block j: the next block's S (as soon as the softmax group has read this
+                // block's S, so that it runs under the softmax), then P V. Every issuer waits
+                // for and releases every stage of the item, used or not.
                 for (int j = 0; j < nblk && ok; ++j) {
-                    const bool more = j + 1 < nblk;
                     if (!(ok = ensure_kv(j))) break;
-                    if (more && !it.frozen && j + 1 < n0) ok = ensure_kv(j + 1) && issue_s(0, j + 1);
-                    if (ok && j < n0) ok = issue_pv(0, j);
-                    if (ok && more && !it.frozen && j + 1 < n1) ok = ensure_kv(j + 1) && issue_s(1, j + 1);
-                    if (ok && j < n1) ok = issue_pv(1, j);
+                    if (!it.frozen && j + 1 < ng) ok = ensure_kv(j + 1) && issue_s(j + 1);
+                    if (ok && j < ng) ok = issue_pv(j);
                     if (!ok) break;
                     mma_commit(&bars.kv_empty[stage_of(j)]);
                 }
