@@ -47,9 +47,7 @@ namespace {
 using namespace tc;
 
 constexpr int kTileBytes = 128 * 64 * 2;
-constexpr int kThreads = 576;   // 8 P warps, 8 dS warps, producer, MMA issuer
-constexpr int kWarpProducer = 16;
-constexpr int kWarpMma = 17;
+constexpr int kThreads = 320;
 constexpr int kStages = 3;
 constexpr int kRing = 4;
 constexpr int kSliceGroup = 8;
@@ -138,13 +136,11 @@ struct Barriers {
     uint64_t kv_full, kv_empty;
     uint64_t st_full[kStages], st_empty[kStages];
     uint64_t s_full;        // S^T of the current tile is in TMEM
-    uint64_t s_consumed;    // P warps have read S^T (8 arrivals)
-    uint64_t p_written;     // P^T (or W^T) of the current tile is in TMEM (8 arrivals)
-    uint64_t p_free;        // dV MMA and dS warps are done with P^T (1 commit + 8 arrivals)
     uint64_t dp_full;       // dP^T of the current tile is in TMEM
-    uint64_t dp_consumed;   // dS warps have read dP^T (8 arrivals)
-    uint64_t ds_ready;      // dS of the current tile is in shared memory (256 arrivals)
-    uint64_t tile_done;     // every MMA of a tile has completed
+    uint64_t s_consumed;    // pattern warps have read S^T (8 arrivals)
+    uint64_t dp_consumed;   // pattern warps have read dP^T (8 arrivals)
+    uint64_t p_ready;       // P^T in TMEM and dS in shared memory (256 arrivals)
+    uint64_t tile_done;     // every MMA of the previous tile has completed
     uint64_t dq_free;       // dQ of the previous tile has been read out (8 arrivals)
     uint64_t dkv_free;      // dV, dK of the previous item have been read out (8 arrivals)
 };
@@ -162,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         abort_flag = 0;
         for (int i = 0; i < kRing; ++i) {
             mbar_init(&bars.item_full[i], 1);
-            mbar_init(&bars.item_empty[i], 17);   // MMA warp + 8 P warps + 8 dS warps
+            mbar_init(&bars.item_empty[i], 9);   // MMA warp + 8 pattern warps
         }
         mbar_init(&bars.kv_full, 1);
         mbar_init(&bars.kv_empty, 1);
@@ -171,18 +167,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             mbar_init(&bars.st_empty[i], 1);
         }
         mbar_init(&bars.s_full, 1);
-        mbar_init(&bars.s_consumed, 8);
-        mbar_init(&bars.p_written, 8);
-        mbar_init(&bars.p_free, 1 + 8);
         mbar_init(&bars.dp_full, 1);
+        mbar_init(&bars.s_consumed, 8);
         mbar_init(&bars.dp_consumed, 8);
-        mbar_init(&bars.ds_ready, 256);
+        mbar_init(&bars.p_ready, 256);
         mbar_init(&bars.tile_done, 1);
         mbar_init(&bars.dq_free, 8);
         mbar_init(&bars.dkv_free, 8);
         fence_mbar_init();
     }
-    if (warp == kWarpMma) {
+    if (warp == 9) {
         tmem_alloc(&tmem_base_sh, 512);
         tmem_relinquish();
     }
@@ -194,22 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     uint32_t* status = p.status;
     const int nqb = p.nqb;
 
-    // Every consumer takes the same sequence of items from the ring.
-    auto next_item = [&](int& slot, uint32_t& bits, bool arrive_warp) -> int {
-        if (!mbar_wait(&bars.item_full[slot], (bits >> slot) & 1u, abort, status, kStatusTimeout)) return -2;
-        bits ^= 1u << slot;
-        const int idx = item_ring[slot];
-        if (arrive_warp) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars.item_empty[slot]);
-        } else {
-            mbar_arrive(&bars.item_empty[slot]);
-        }
-        slot = (slot + 1) % kRing;
-        return idx;
-    };
-
-    if (warp == kWarpProducer) {
+    if (warp == 8) {
         // ---------------------------------------------------------------- producer
         if (lane == 0) {
             tma_prefetch_desc(&p.tm_q);
@@ -272,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 }
             }
         }
-    } else if (warp == kWarpMma) {
+    } else if (warp == 9) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t id_s = idesc_bf16(128, 128, 0, 0);   // S^T = K Q^T, dP^T = V dO^T
@@ -280,19 +259,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             const uint32_t id_dk = idesc_bf16(128, 64, 0, 1);   // dK += dS^T Q (A K-major view, Q MN-major)
             const uint32_t id_dq = idesc_bf16(128, 64, 1, 1);   // dQ = dS K (A MN-major, K MN-major)
             uint32_t ring_full_bits = 0, kv_full_ph = 0, st_full_bits = 0;
-            uint32_t s_consumed_ph = 0, p_written_ph = 0, dp_consumed_ph = 0, ds_ready_ph = 0;
-            uint32_t dq_free_ph = 1, dkv_free_ph = 1;
+            uint32_t s_consumed_ph = 0, dp_consumed_ph = 0, p_ready_ph = 0, dq_free_ph = 1, dkv_free_ph = 1;
             int slot = 0, stage = 0;
             bool ok = true;
             const uint32_t sds = smem_u32(sm + Smem::ds);
             const uint32_t skv = smem_u32(sm + Smem::kv);
             auto st_addr = [&](int s) { return smem_u32(sm + Smem::st + s * Smem::st_bytes); };
-            auto wait = [&](uint64_t* bar, uint32_t& ph) -> bool {
-                if (!mbar_wait(bar, ph, abort, status, kStatusTimeout)) return false;
-                ph ^= 1;
-                tc_fence_after();
-                return true;
-            };
             auto wait_st = [&](int s) -> bool {
                 if (!mbar_wait(&bars.st_full[s], (st_full_bits >> s) & 1u, abort, status, kStatusTimeout))
                     return false;
@@ -317,8 +289,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 mma_commit(&bars.dp_full);
             };
             while (ok) {
-                const int idx = next_item(slot, ring_full_bits, false);
-                if (idx == -2) break;
+                if (!(ok = mbar_wait(&bars.item_full[slot], (ring_full_bits >> slot) & 1u, abort, status,
+                                     kStatusTimeout)))
+                    break;
+                ring_full_bits ^= 1u << slot;
+                const int idx = item_ring[slot];
+                mbar_arrive(&bars.item_empty[slot]);
+                slot = (slot + 1) % kRing;
                 if (idx < 0) break;
                 const Item it = decode_item(p, idx);
                 const int n = nqb - it.kb;
@@ -332,51 +309,54 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 for (int i = 0; i < n && ok; ++i) {
                     const int s = stage;
                     const int s_next = (stage + 1) % kStages;
-                    const bool more = i + 1 < n;
-                    const uint32_t sq = st_addr(s), sdo = sq + kTileBytes;
                     if (!it.frozen) {
-                        // S^T of the next tile may land once the P warps have read this one
-                        if (!(ok = wait(&bars.s_consumed, s_consumed_ph))) break;
-                        if (more) {
+                        // S^T and dP^T of the next tile may overwrite TMEM once this tile's are read
+                        if (!(ok = mbar_wait(&bars.s_consumed, s_consumed_ph, abort, status, kStatusTimeout))) break;
+                        s_consumed_ph ^= 1;
+                        tc_fence_after();
+                        if (i + 1 < n) {
                             if (!(ok = wait_st(s_next))) break;
                             issue_s(s_next);
                         }
+                        if (!(ok = mbar_wait(&bars.dp_consumed, dp_consumed_ph, abort, status, kStatusTimeout))) break;
+                        dp_consumed_ph ^= 1;
+                        tc_fence_after();
+                        if (i + 1 < n) issue_dp(s_next);
                     } else {
                         if (!(ok = wait_st(s))) break;
                     }
-                    // dV += P^T dO as soon as P^T is written
-                    if (!(ok = wait(&bars.p_written, p_written_ph))) break;
-                    if (i == 0 && !(ok = wait(&bars.dkv_free, dkv_free_ph))) break;   // accumulators read out
+                    if (!(ok = mbar_wait(&bars.p_ready, p_ready_ph, abort, status, kStatusTimeout))) break;
+                    p_ready_ph ^= 1;
+                    if (i == 0) {
+                        // the first dV / dK MMA of this item overwrites the accumulators:
+                        // the previous item's dV and dK must have been read out
+                        if (!(ok = mbar_wait(&bars.dkv_free, dkv_free_ph, abort, status, kStatusTimeout))) break;
+                        dkv_free_ph ^= 1;
+                    }
+                    tc_fence_after();
+                    const uint32_t sq = st_addr(s), sdo = sq + kTileBytes;
+                    // dV += P^T dO
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
                         mma_ts(tmem + kColDV, tmem + kColP + 8 * k, sdesc_sw128(sdo + 2048 * k, 16384, 1024), id_dv,
                                (i > 0 || k > 0) ? 1u : 0u);
-                    mma_commit(&bars.p_free);
                     if (!it.frozen) {
-                        if (!(ok = wait(&bars.ds_ready, ds_ready_ph))) break;
                         // dK += dS^T Q: dS viewed K-major (keys x queries, two 64-query halves)
 #pragma unroll
                         for (int k = 0; k < 8; ++k)
                             mma_ss(tmem + kColDK, sdesc_sw128(sds + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
                                    sdesc_sw128(sq + 2048 * k, 16384, 1024), id_dk, (i > 0 || k > 0) ? 1u : 0u);
                         // dQ may be overwritten once the previous tile's dQ has been read out
-                        if (!(ok = wait(&bars.dq_free, dq_free_ph))) break;
+                        if (!(ok = mbar_wait(&bars.dq_free, dq_free_ph, abort, status, kStatusTimeout))) break;
+                        dq_free_ph ^= 1;
+                        tc_fence_after();
                         // dQ = dS K: dS viewed MN-major (queries x keys)
 #pragma unroll
                         for (int k = 0; k < 8; ++k)
                             mma_ss(tmem + kColDQ, sdesc_sw128(sds + 2048 * k, 16384, 1024),
                                    sdesc_sw128(skv + 2048 * k, 16384, 1024), id_dq, k > 0);
-                        mma_commit(&bars.tile_done);
-                        // dP^T of the next tile (the dS warps have read this one), queued after
-                        // dK and dQ so that tile_done is not held up by it
-                        if (!(ok = wait(&bars.dp_consumed, dp_consumed_ph))) break;
-                        if (more) issue_dp(s_next);
-                    } else {
-                        // frozen tile: the dS warps have taken the previous tile_done phase
-                        // (no barrier may run two phases ahead of a waiter)
-                        if (!(ok = wait(&bars.ds_ready, ds_ready_ph))) break;
-                        mma_commit(&bars.tile_done);
                     }
+                    mma_commit(&bars.tile_done);
                     mma_commit(&bars.st_empty[s]);
                     stage = s_next;
                 }
@@ -384,121 +364,22 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 if (!it.frozen) mma_commit(&bars.kv_empty);
             }
         }
-    } else if (warp < 8) {
-        // ---------------------------------------------------------------- P warps
-        // warp w: key rows 32(w%4)..+31, query columns 64(w/4)..+63 of each tile
+    } else {
+        // ---------------------------------------------------------------- pattern warps
         const int quarter = warp & 3, half = warp >> 2;
         const int j = quarter * 32 + lane;                   // key row of the block = TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         uint32_t ring_full_bits = 0, st_full_bits = 0;
-        uint32_t s_full_ph = 0, p_free_ph = 1;
+        uint32_t s_full_ph = 0, dp_full_ph = 0, tile_done_ph = 0;
+        bool pending = false;   // a tile_done commit is outstanding for the last tile we handed over
         int slot = 0, stage = 0;
         bool ok = true;
-        while (ok) {
-            const int idx = next_item(slot, ring_full_bits, true);
-            if (idx < 0) break;
-            const Item it = decode_item(p, idx);
-            const int key = it.kb * 128 + j;
-            const int n = nqb - it.kb;
-            float a2j = -INFINITY;   // exact form: a * log2(e) of my key
-            bool exact = false;
-            if (it.frozen) {
-                exact = (p.hflag[it.h] & 2u) != 0;
-                a2j = p.a2p[(size_t)it.h * p.Tp + key];
-            }
-            for (int i = 0; i < n && ok; ++i) {
-                const bool diag = i == 0;
-                if (!(ok = mbar_wait(&bars.st_full[stage], (st_full_bits >> stage) & 1u, abort, status,
-                                     kStatusTimeout)))
-                    break;
-                st_full_bits ^= 1u << stage;
-                const float* vec =
-                    reinterpret_cast<const float*>(sm + Smem::st + stage * Smem::st_bytes + Smem::st_vec);
-                if (!it.frozen) {
-                    if (!(ok = mbar_wait(&bars.s_full, s_full_ph, abort, status, kStatusTimeout))) break;
-                    s_full_ph ^= 1;
-                    tc_fence_after();
-                    uint32_t sv[64];
-                    tmem_ld32(lane_base + kColS + 64 * half, sv);
-                    tmem_ld32(lane_base + kColS + 64 * half + 32, sv + 32);
-                    tmem_ld_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars.s_consumed);   // S^T of the next tile may land
-                    const float2* lse2 = reinterpret_cast<const float2*>(vec + 64 * half);
-                    // P^T may be overwritten once the previous tile's dV MMA and the dS warps are done
-                    if (!(ok = mbar_wait(&bars.p_free, p_free_ph, abort, status, kStatusTimeout))) break;
-                    p_free_ph ^= 1;
-                    tc_fence_after();
-#pragma unroll
-                    for (int g2 = 0; g2 < 2; ++g2) {
-                        uint32_t pk[16];   // packed bf16 pairs of 32 columns of P^T
-#pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            const int c = 32 * g2 + e;
-                            const int q0 = 64 * half + c;
-                            // x = S * log2(e) / sqrt(d) - lse * log2(e), two columns per instruction
-                            const float2 x = ffma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
-                                                   make_float2(kScaleLog2, kScaleLog2), neg2(lse2[c >> 1]));
-                            float p0 = fast_exp2(x.x);
-                            float p1 = fast_exp2(x.y);
-                            if (diag && j > q0) p0 = 0.f;
-                            if (diag && j > q0 + 1) p1 = 0.f;
-                            pk[e >> 1] = pack_bf16(p0, p1);
-                        }
-                        tmem_st16(lane_base + kColP + 32 * half + 16 * g2, pk);
-                    }
-                } else {
-                    // W^T(j, q) = W(q, j) (Eq. 3); band[q] is r at offset q - j = (qb - kb) * 128 +
-                    // q - j. Factorised: W(q, j) / exp(a[j] - A) = exp(r[q-j] - R) / Z'(q), no exp per
-                    // element (exp(a[j] - A) is applied to dV). Exact: exp(a[j] + r[q-j] - log Z(q)).
-                    const float* band = vec + 256 + 127 - j;
-                    if (!(ok = mbar_wait(&bars.p_free, p_free_ph, abort, status, kStatusTimeout))) break;
-                    p_free_ph ^= 1;
-                    tc_fence_after();
-#pragma unroll
-                    for (int g2 = 0; g2 < 2; ++g2) {
-                        uint32_t pk[16];
-                        if (!exact) {
-#pragma unroll
-                            for (int e = 0; e < 32; e += 2) {
-                                const int q0 = 64 * half + 32 * g2 + e;
-                                pk[e >> 1] = pack_bf16(band[q0] * vec[q0], band[q0 + 1] * vec[q0 + 1]);
-                            }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 32; e += 2) {
-                                const int q0 = 64 * half + 32 * g2 + e;
-                                const float w0 = fast_exp2(a2j + band[q0] - vec[q0]);
-                                const float w1 = fast_exp2(a2j + band[q0 + 1] - vec[q0 + 1]);
-                                pk[e >> 1] = pack_bf16(w0, w1);
-                            }
-                        }
-                        tmem_st16(lane_base + kColP + 32 * half + 16 * g2, pk);
-                    }
-                }
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars.p_written);
-                stage = (stage + 1) % kStages;
-            }
-        }
-    } else if (warp < 16) {
-        // ---------------------------------------------------------------- dS warps
-        // warp 8 + 4h + q: key rows 32q..+31 (TMEM lane quarter q), query columns 64h..+63
-        const int quarter = warp & 3, half = (warp - 8) >> 2;
-        const int j = quarter * 32 + lane;
-        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-        uint32_t ring_full_bits = 0, st_full_bits = 0;
-        uint32_t p_written_ph = 0, dp_full_ph = 0, tile_done_ph = 0;
-        bool pending = false;   // a tile_done commit is outstanding for the last tile handed over
-        int slot = 0, stage = 0;
-        bool ok = true;
-        uint8_t* dsp = sm + Smem::ds + half * 16384;        // my 64-query half of dS (MN-major atom)
-        uint8_t* dqs = sm + Smem::dqs + half * 16384;       // staging of my 32 dQ columns (SW128 rows)
-        const bool dq_issuer = quarter == 0 && lane == 0;   // issues the bulk reduce of this half
+        uint8_t* dsp = sm + Smem::ds + half * 16384;          // my 64-query half of dS (MN-major atom)
+        uint8_t* dqs = sm + Smem::dqs + half * 16384;         // staging of my 32 dQ columns (SW128 rows)
+        const bool dq_issuer = quarter == 0 && lane == 0;     // issues the bulk reduce of this half
 
+        // The previous tile's MMAs have all completed: P^T, dS may be overwritten
+        // and its dQ (ordinary tiles) can be read out.
         auto wait_tile_done = [&]() -> bool {
             if (!pending) return true;
             if (!mbar_wait(&bars.tile_done, tile_done_ph, abort, status, kStatusTimeout)) return false;
@@ -531,141 +412,177 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         };
 
         while (ok) {
-            const int idx = next_item(slot, ring_full_bits, true);
+            if (!(ok = mbar_wait(&bars.item_full[slot], (ring_full_bits >> slot) & 1u, abort, status,
+                                 kStatusTimeout)))
+                break;
+            ring_full_bits ^= 1u << slot;
+            const int idx = item_ring[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.item_empty[slot]);
+            slot = (slot + 1) % kRing;
             if (idx < 0) break;
             const Item it = decode_item(p, idx);
             const int bh = it.b * p.H + it.h;
             const int key = it.kb * 128 + j;
             const int n = nqb - it.kb;
+            float a2j = -INFINITY;   // exact form: a * log2(e) of my key
+            float eaj = 0.f;         // factorised form: exp(a - A) of my key, applied to dV
             bool exact = false;
-            float eaj = 0.f;   // factorised form: exp(a - A) of my key, applied to dV
             if (it.frozen) {
                 exact = (p.hflag[it.h] & 2u) != 0;
+                a2j = p.a2p[(size_t)it.h * p.Tp + key];
                 eaj = p.eap[(size_t)it.h * p.Tp + key];
             }
             for (int i = 0; i < n && ok; ++i) {
                 const int qb = it.kb + i;
-                // the row vectors (D) of this tile; frozen tiles need none, but their phase of
-                // the stage barrier is counted (it completes before this stage is loaded again,
-                // since the producer refills a stage only after all MMAs of its tile are done)
-                if (!it.frozen) {
-                    if (!(ok = mbar_wait(&bars.st_full[stage], (st_full_bits >> stage) & 1u, abort, status,
-                                         kStatusTimeout)))
-                        break;
-                }
+                const bool diag = i == 0;
+                if (!(ok = mbar_wait(&bars.st_full[stage], (st_full_bits >> stage) & 1u, abort, status,
+                                     kStatusTimeout)))
+                    break;
                 st_full_bits ^= 1u << stage;
-                // P^T of this tile is written (for frozen tiles: keeps the p_free phases in step)
-                if (!(ok = mbar_wait(&bars.p_written, p_written_ph, abort, status, kStatusTimeout))) break;
-                p_written_ph ^= 1;
-                tc_fence_after();
-                if (it.frozen) {
-                    // nothing to compute; take the previous tile_done phase before releasing P^T
-                    // and signalling this tile, so that no barrier runs two phases ahead
+                const float* vec =
+                    reinterpret_cast<const float*>(sm + Smem::st + stage * Smem::st_bytes + Smem::st_vec);
+                if (!it.frozen) {
+                    if (!(ok = mbar_wait(&bars.s_full, s_full_ph, abort, status, kStatusTimeout))) break;
+                    s_full_ph ^= 1;
+                    tc_fence_after();
+                    // P^T first: S^T row (64 columns) -> P (bf16 pairs); then dP^T row -> dS.
+                    uint32_t pk[32];
+                    {
+                        uint32_t sv[64];
+                        tmem_ld32(lane_base + kColS + 64 * half, sv);
+                        tmem_ld32(lane_base + kColS + 64 * half + 32, sv + 32);
+                        tmem_ld_wait();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bars.s_consumed);   // S^T of the next tile may land
+                        const float2* lse2 = reinterpret_cast<const float2*>(vec + 64 * half);
+#pragma unroll
+                        for (int e = 0; e < 64; e += 2) {
+                            const int q0 = 64 * half + e;
+                            // x = S * log2(e) / sqrt(d) - lse * log2(e), two columns per instruction
+                            const float2 x = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
+                                                   make_float2(kScaleLog2, kScaleLog2), neg2(lse2[e >> 1]));
+                            float p0 = fast_exp2(x.x);
+                            float p1 = fast_exp2(x.y);
+                            if (diag && j > q0) p0 = 0.f;
+                            if (diag && j > q0 + 1) p1 = 0.f;
+                            pk[e >> 1] = pack_bf16(p0, p1);
+                        }
+                    }
+                    // the previous tile's MMAs are done: its dQ (same item) goes out first,
+                    // then P^T and dS of this tile overwrite the previous ones
                     if (!(ok = wait_tile_done())) break;
+                    if (!(ok = mbar_wait(&bars.dp_full, dp_full_ph, abort, status, kStatusTimeout))) break;
+                    dp_full_ph ^= 1;
+                    tc_fence_after();
+                    uint32_t dp[64];
+                    tmem_ld32(lane_base + kColDP + 64 * half, dp);
+                    tmem_ld32(lane_base + kColDP + 64 * half + 32, dp + 32);
+                    tmem_ld_wait();
+                    tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars.p_free);
-                    mbar_arrive(&bars.ds_ready);
-                    pending = true;
-                    stage = (stage + 1) % kStages;
-                    continue;
-                }
-                const float* dvec =
-                    reinterpret_cast<const float*>(sm + Smem::st + stage * Smem::st_bytes + Smem::st_vec) + 128;
-                // the previous tile's MMAs are done: its dQ goes out, and dS may be overwritten
-                if (!(ok = wait_tile_done())) break;
-                if (i > 0) drain_dq(bh, qb - 1);
-                if (!(ok = mbar_wait(&bars.dp_full, dp_full_ph, abort, status, kStatusTimeout))) break;
-                dp_full_ph ^= 1;
-                tc_fence_after();
-                // my 64 queries in 4 chunks of 16; the loads of chunk c+1 are in flight while
-                // chunk c is computed
-                uint32_t dpa[16], pwa[8], dpb[16], pwb[8];
-                tmem_ld16(lane_base + kColDP + 64 * half, dpa);
-                tmem_ld8(lane_base + kColP + 32 * half, pwa);
-                tmem_ld_wait();
+                    if (lane == 0) mbar_arrive(&bars.dp_consumed);   // dP^T of the next tile may land
+                    tmem_st32(lane_base + kColP + 32 * half, pk);
+                    const float2* dvec = reinterpret_cast<const float2*>(vec + 128 + 64 * half);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {   // queries 64*half + 16c .. +15
-                    uint32_t* dp = (c & 1) ? dpb : dpa;
-                    uint32_t* pw = (c & 1) ? pwb : pwa;
-                    if (c + 1 < 4) {
-                        tmem_ld16(lane_base + kColDP + 64 * half + 16 * (c + 1), (c & 1) ? dpa : dpb);
-                        tmem_ld8(lane_base + kColP + 32 * half + 8 * (c + 1), (c & 1) ? pwa : pwb);
-                    }
-                    uint32_t dk[8];
+                    for (int g2 = 0; g2 < 2; ++g2) {
+                        uint32_t dk[16];
 #pragma unroll
-                    for (int e = 0; e < 16; e += 2) {
-                        // dS = P o (dP - D) with P as rounded to bf16 for the MMAs
-                        const float2 pp = make_float2(__uint_as_float(pw[e >> 1] << 16),
-                                                      __uint_as_float(pw[e >> 1] & 0xffff0000u));
-                        const float2 dd = fmul2(pp, fsub2(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])),
-                                                          *reinterpret_cast<const float2*>(dvec + 64 * half + 16 * c + e)));
-                        dk[e >> 1] = pack_bf16(dd.x, dd.y);
+                        for (int e = 0; e < 32; e += 2) {
+                            const int c = 32 * g2 + e;
+                            const int q0 = 64 * half + c;
+                            // dS = P o (dP - D) with P as rounded to bf16 for the MMAs
+                            const float2 pp = make_float2(__uint_as_float(pk[c >> 1] << 16),
+                                                          __uint_as_float(pk[c >> 1] & 0xffff0000u));
+                            const float2 dd = fmul2(pp, fsub2(make_float2(__uint_as_float(dp[c]),
+                                                                          __uint_as_float(dp[c + 1])),
+                                                              dvec[c >> 1]));
+                            dk[e >> 1] = pack_bf16(dd.x, dd.y);
+                            (void)q0;
+                        }
+                        // dS row j, queries 64*half + 32*g2 .. +31: MN-major atom `half`, K-row j
+#pragma unroll
+                        for (int t = 0; t < 4; ++t)
+                            *reinterpret_cast<uint4*>(dsp + sw128_offset(j, 16 * (4 * g2 + t))) =
+                                make_uint4(dk[4 * t], dk[4 * t + 1], dk[4 * t + 2], dk[4 * t + 3]);
                     }
-                    // dS row j, queries 64*half + 16c .. +15: MN-major atom `half`, K-row j, chunks 2c, 2c+1
-                    *reinterpret_cast<uint4*>(dsp + sw128_offset(j, 16 * (2 * c))) =
-                        make_uint4(dk[0], dk[1], dk[2], dk[3]);
-                    *reinterpret_cast<uint4*>(dsp + sw128_offset(j, 16 * (2 * c + 1))) =
-                        make_uint4(dk[4], dk[5], dk[6], dk[7]);
-                    if (c + 1 < 4) tmem_ld_wait();
+                } else {
+                    // W^T(j, q) = W(q, j) (Eq. 3); band[q] is r at offset q - j = (qb - kb) * 128 +
+                    // q - j. Factorised: W(q, j) / exp(a[j] - A) = exp(r[q-j] - R) / Z'(q), no exp per
+                    // element (exp(a[j] - A) is applied to dV). Exact: exp(a[j] + r[q-j] - log Z(q)).
+                    const float* band = vec + 256 + 127 - j;
+                    uint32_t pk[32];
+                    if (!exact) {
+#pragma unroll
+                        for (int e = 0; e < 64; e += 2) {
+                            const int q0 = 64 * half + e;
+                            pk[e >> 1] = pack_bf16(band[q0] * vec[q0], band[q0 + 1] * vec[q0 + 1]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 64; e += 2) {
+                            const int q0 = 64 * half + e;
+                            const float w0 = fast_exp2(a2j + band[q0] - vec[q0]);
+                            const float w1 = fast_exp2(a2j + band[q0 + 1] - vec[q0 + 1]);
+                            pk[e >> 1] = pack_bf16(w0, w1);
+                        }
+                    }
+                    if (!(ok = wait_tile_done())) break;
+                    tmem_st32(lane_base + kColP + 32 * half, pk);
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&bars.dp_consumed);   // dP^T of the next tile may land
-                    mbar_arrive(&bars.p_free);        // done with P^T
-                }
+                tmem_st_wait();
                 fence_proxy_async_smem();
-                mbar_arrive(&bars.ds_ready);
+                tc_fence_before();
+                mbar_arrive(&bars.p_ready);
+                if (!it.frozen && i > 0) drain_dq(bh, qb - 1);
                 pending = true;
                 stage = (stage + 1) % kStages;
             }
             if (!ok) break;
-            // all MMAs of this item done: the last dQ, then the dV and dK rows
+            // all MMAs of this item done: the last dQ, then the dV and dK rows (my 32 d-columns)
             if (!(ok = wait_tile_done())) break;
             if (!it.frozen) drain_dq(bh, nqb - 1);
-            const float fv = (it.frozen && !exact) ? eaj : 1.f;
-            {
-                const int h2 = half;   // my 32 d-columns of dV and dK
-                uint32_t dv[32], dk[32];
-                tmem_ld32(lane_base + kColDV + 32 * h2, dv);
-                if (!it.frozen) tmem_ld32(lane_base + kColDK + 32 * h2, dk);
-                tmem_ld_wait();
-                if (key < p.T) {
-                    uint4* pv = reinterpret_cast<uint4*>(p.dv + ((size_t)bh * p.T + key) * 64 + 32 * h2);
-                    uint4* pk2 = reinterpret_cast<uint4*>(p.dk + ((size_t)bh * p.T + key) * 64 + 32 * h2);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const uint32_t* x = dv + 8 * c;
-                        pv[c] = make_uint4(pack_bf16(__uint_as_float(x[0]) * fv, __uint_as_float(x[1]) * fv),
-                                           pack_bf16(__uint_as_float(x[2]) * fv, __uint_as_float(x[3]) * fv),
-                                           pack_bf16(__uint_as_float(x[4]) * fv, __uint_as_float(x[5]) * fv),
-                                           pack_bf16(__uint_as_float(x[6]) * fv, __uint_as_float(x[7]) * fv));
-                    }
-                    if (it.frozen) {
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) pk2[c] = make_uint4(0, 0, 0, 0);
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const uint32_t* x = dk + 8 * c;
-                            pk2[c] = make_uint4(pack_bf16(__uint_as_float(x[0]) * kScale, __uint_as_float(x[1]) * kScale),
-                                                pack_bf16(__uint_as_float(x[2]) * kScale, __uint_as_float(x[3]) * kScale),
-                                                pack_bf16(__uint_as_float(x[4]) * kScale, __uint_as_float(x[5]) * kScale),
-                                                pack_bf16(__uint_as_float(x[6]) * kScale, __uint_as_float(x[7]) * kScale));
-                        }
-                    }
-                }
-            }
+            uint32_t dv[32], dk[32];
+            tmem_ld32(lane_base + kColDV + 32 * half, dv);
+            if (!it.frozen) tmem_ld32(lane_base + kColDK + 32 * half, dk);
+            tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars.dkv_free);
+            if (key < p.T) {
+                uint4* pv = reinterpret_cast<uint4*>(p.dv + ((size_t)bh * p.T + key) * 64 + 32 * half);
+                uint4* pk2 = reinterpret_cast<uint4*>(p.dk + ((size_t)bh * p.T + key) * 64 + 32 * half);
+                const float fv = (it.frozen && !exact) ? eaj : 1.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t* x = dv + 8 * c;
+                    pv[c] = make_uint4(pack_bf16(__uint_as_float(x[0]) * fv, __uint_as_float(x[1]) * fv),
+                                       pack_bf16(__uint_as_float(x[2]) * fv, __uint_as_float(x[3]) * fv),
+                                       pack_bf16(__uint_as_float(x[4]) * fv, __uint_as_float(x[5]) * fv),
+                                       pack_bf16(__uint_as_float(x[6]) * fv, __uint_as_float(x[7]) * fv));
+                }
+                if (it.frozen) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) pk2[c] = make_uint4(0, 0, 0, 0);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t* x = dk + 8 * c;
+                        pk2[c] = make_uint4(pack_bf16(__uint_as_float(x[0]) * kScale, __uint_as_float(x[1]) * kScale),
+                                            pack_bf16(__uint_as_float(x[2]) * kScale, __uint_as_float(x[3]) * kScale),
+                                            pack_bf16(__uint_as_float(x[4]) * kScale, __uint_as_float(x[5]) * kScale),
+                                            pack_bf16(__uint_as_float(x[6]) * kScale, __uint_as_float(x[7]) * kScale));
+                    }
+                }
+            }
         }
-        if (dq_issuer) bulk_wait_all();   // dQ reduces complete before the kernel ends
     }
 
+    if (warp < 8 && (warp & 3) == 0 && lane == 0) bulk_wait_all();   // dQ reduces complete
     tc_fence_before();
     __syncthreads();
-    if (warp == kWarpMma) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
