@@ -120,7 +120,9 @@ struct Barriers {
 
 __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ FwdParams p) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base (swizzled tiles), derived from the shared array itself so that
+    // every access through it stays a shared-memory access
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     __shared__ Barriers bars;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
