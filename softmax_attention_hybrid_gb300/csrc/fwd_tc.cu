@@ -116,6 +116,8 @@ struct Barriers {
     uint64_t q_full, q_empty;
     uint64_t kv_full[kStages], kv_empty[kStages];
     uint64_t s_full[2], s_empty[2], p_full[2], o_done[2];
+    uint64_t w_full[2][2];   // frozen items: W buffer b of tile g is written (4 arrivals)
+    uint64_t w_done[2][2];   // frozen items: P V of tile g that read W buffer b has completed
 };
 
 __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ FwdParams p) {
@@ -141,6 +143,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             mbar_init(&bars.s_empty[g], 4);
             mbar_init(&bars.p_full[g], 4);
             mbar_init(&bars.o_done[g], 1);
+            mbar_init(&bars.w_done[g][0], 1);
+            mbar_init(&bars.w_done[g][1], 1);
+            mbar_init(&bars.w_full[g][0], 4);
+            mbar_init(&bars.w_full[g][1], 4);
         }
         fence_mbar_init();
     }
@@ -213,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             const uint32_t idesc_o = idesc_bf16(128, 64, 0, 1);   // O += P V, V MN-major
             uint32_t q_full_ph = 0;
             uint32_t kv_full_bits = 0;   // phase parity per stage, bit s
-            uint32_t s_empty_ph = 1, p_full_ph = 0;
+            uint32_t s_empty_ph = 1, p_full_ph = 0, w_full_bits = 0;
             int stage = 0;
             bool ok = true;
             const uint32_t sqg = smem_u32(sm + SmemLayout::q) + g * kTileBytes;
@@ -244,17 +250,27 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     mma_commit(&bars.s_full[g]);
                     return true;
                 };
+                // frozen items alternate W between the P columns and the (unused) S columns
+                const bool frz = it.frozen;
                 auto issue_pv = [&](int j) -> bool {
-                    if (!mbar_wait(&bars.p_full[g], p_full_ph, abort, status, kStatusTimeout)) return false;
-                    p_full_ph ^= 1;
+                    if (frz) {   // one barrier per W buffer: the softmax group may be a block ahead
+                        const int b = j & 1;
+                        if (!mbar_wait(&bars.w_full[g][b], (w_full_bits >> b) & 1u, abort, status, kStatusTimeout))
+                            return false;
+                        w_full_bits ^= 1u << b;
+                    } else {
+                        if (!mbar_wait(&bars.p_full[g], p_full_ph, abort, status, kStatusTimeout)) return false;
+                        p_full_ph ^= 1;
+                    }
                     tc_fence_after();
                     const uint32_t sv =
                         smem_u32(sm + SmemLayout::kv + stage_of(j) * SmemLayout::stage_bytes + kTileBytes);
+                    const uint32_t a = (frz && (j & 1)) ? d_s : d_p;
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        mma_ts(d_o, d_p + 8 * k, sdesc_sw128(sv + 2048 * k, 16384, 1024), idesc_o,
+                        mma_ts(d_o, a + 8 * k, sdesc_sw128(sv + 2048 * k, 16384, 1024), idesc_o,
                                (j > 0 || k > 0) ? 1u : 0u);
-                    mma_commit(&bars.o_done[g]);
+                    mma_commit(frz ? &bars.w_done[g][j & 1] : &bars.o_done[g]);
                     return true;
                 };
                 int kv_ready = 0;   // blocks of this item whose K/V stage has been waited for
@@ -275,6 +291,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 for (int j = 0; j < nblk && ok; ++j) {
                     if (!(ok = ensure_kv(j))) break;
                     if (!it.frozen && j + 1 < ng) ok = ensure_kv(j + 1) && issue_s(j + 1);
+                    // A frozen item's W also sits in the S columns. The softmax group arrives on
+                    // s_empty once the item's last P V is done, and the next S waits for that
+                    // phase; its predecessor phase is taken here, before that last P V is issued,
+                    // so that s_empty never runs two phases ahead of this thread.
+                    if (ok && it.frozen && j + 1 == ng) {
+                        ok = mbar_wait(&bars.s_empty[g], s_empty_ph, abort, status, kStatusTimeout);
+                        s_empty_ph ^= 1;
+                    }
                     if (ok && j < ng) ok = issue_pv(j);
                     if (!ok) break;
                     mma_commit(&bars.kv_empty[stage_of(j)]);
@@ -290,6 +314,16 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         const int r = threadIdx.x & 127;       // row within the tile = TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16) + 256 * g;
         uint32_t s_full_ph = 0, o_done_ph = 0;
+        uint32_t w_done_ph[2] = {0, 0};
+        bool w_pend[2] = {false, false};   // a P V that read W buffer b may not have been waited for
+        auto wait_w = [&](int b) -> bool {
+            if (!w_pend[b]) return true;
+            if (!mbar_wait(&bars.w_done[g][b], w_done_ph[b], abort, status, kStatusTimeout)) return false;
+            w_done_ph[b] ^= 1;
+            w_pend[b] = false;
+            tc_fence_after();
+            return true;
+        };
         int gblk = 0;   // key blocks of all previous items of this CTA (stage = gblk % kStages)
         bool ok = true;
         for (int round = 0; ok; ++round) {
@@ -396,11 +430,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     if (!(ok = mbar_wait(&bars.kv_full[st], (uint32_t)(G / kStages) & 1u, abort, status,
                                          kStatusTimeout)))
                         break;
-                    if (j > 0) {
-                        if (!(ok = mbar_wait(&bars.o_done[g], o_done_ph, abort, status, kStatusTimeout))) break;
-                        o_done_ph ^= 1;
-                        tc_fence_after();
-                    }
+                    // W buffer j & 1 (P columns, or the S columns frozen items leave unused) is
+                    // free once the P V of block j - 2 has read it
+                    const int wb = j & 1;
+                    if (!(ok = wait_w(wb))) break;
+                    const uint32_t wcol = wb ? 0u : 128u;
                     const float* a2s = reinterpret_cast<const float*>(sm + SmemLayout::kv + st * SmemLayout::stage_bytes);
                     // bnd[-c] = r * log2(e) at offset i - k = (qb - j) * 128 + r - c
                     const float* bnd = reinterpret_cast<const float*>(sm + SmemLayout::kv + st * SmemLayout::stage_bytes +
@@ -415,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                                 const int cc = 32 * h4 + 2 * c;
                                 pk[c] = pack_bf16(bnd[-cc] * a2s[cc], bnd[-cc - 1] * a2s[cc + 1]);
                             }
-                            tmem_st16(lane_base + 128 + 16 * h4, pk);
+                            tmem_st16(lane_base + wcol + 16 * h4, pk);
                         }
                     } else {
 #pragma unroll
@@ -428,20 +462,29 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                                 const float w1 = fast_exp2(a2s[cc + 1] + bnd[-cc - 1] - lz2);
                                 pk[c] = pack_bf16(w0, w1);
                             }
-                            tmem_st16(lane_base + 128 + 16 * h4, pk);
+                            tmem_st16(lane_base + wcol + 16 * h4, pk);
                         }
                     }
                 }
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars.p_full[g]);
+                if (lane == 0) mbar_arrive(it.frozen ? &bars.w_full[g][j & 1] : &bars.p_full[g]);
+                if (it.frozen) w_pend[j & 1] = true;
             }
             if (!ok) break;
             // epilogue: O = acc / l (ordinary) or acc (frozen: W rows sum to one)
-            if (!(ok = mbar_wait(&bars.o_done[g], o_done_ph, abort, status, kStatusTimeout))) break;
-            o_done_ph ^= 1;
-            tc_fence_after();
+            if (it.frozen) {
+                // the last P V (and, completing in order, every earlier one) is done; the next
+                // item's S may now overwrite the W columns
+                if (!(ok = wait_w((nblk - 1) & 1))) break;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars.s_empty[g]);
+            } else {
+                if (!(ok = mbar_wait(&bars.o_done[g], o_done_ph, abort, status, kStatusTimeout))) break;
+                o_done_ph ^= 1;
+                tc_fence_after();
+            }
             uint32_t ov[64];
             tmem_ld32(lane_base + 192, ov);
             tmem_ld32(lane_base + 224, ov + 32);
