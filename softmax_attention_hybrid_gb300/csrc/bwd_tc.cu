@@ -222,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                     tma_load_3d(kv, &p.tm_k, &bars.kv_full, 0, it.kb * 128, bh);
                     tma_load_3d(kv + kTileBytes, &p.tm_v, &bars.kv_full, 0, it.kb * 128, bh);
                 }
+                const bool exact = it.frozen && (p.hflag[it.h] & 2u) != 0;
                 for (int qb = it.kb; qb < nqb; ++qb) {
                     if (!(ok = mbar_wait(&bars.st_empty[stage], (st_empty_bits >> stage) & 1u, abort, status,
                                          kStatusTimeout)))
@@ -238,7 +239,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                     } else {
                         // exact form: vec[0..128) lse * log2(e) (= log2 Z), vec[256..512) r * log2(e);
                         // factorised form: vec[0..128) 1 / Z', vec[256..512) exp(r - R)
-                        const bool exact = (p.hflag[it.h] & 2u) != 0;
                         const float* band = (exact ? p.r2p : p.erp) + (size_t)it.h * (p.Tp + 256) +
                                             (size_t)(qb - it.kb) * 128;
                         mbar_expect_tx(&bars.st_full[stage], kTileBytes + 1024 + 512);

@@ -35,7 +35,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kStages = 3;
+constexpr int kStages = 5;
 constexpr int kTileBytes = 128 * 64 * 2;  // one 128 x 64 bf16 tile
 constexpr int kThreads = 352;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -180,6 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 const int qb0 = 2 * it.pair, qb1 = qb0 + 1;
                 const bool t1 = qb1 < p.nqb;
                 const int nblk = t1 ? qb1 + 1 : qb0 + 1;
+                const bool exact = it.frozen && (p.hflag[it.h] & 2u) != 0;
                 if (!it.frozen) {
                     if (!(ok = mbar_wait(&bars.q_empty, q_empty_ph, abort, status, kStatusTimeout))) break;
                     q_empty_ph ^= 1;
@@ -197,7 +198,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         mbar_expect_tx(&bars.kv_full[stage], 2 * kTileBytes);
                         tma_load_3d(st, &p.tm_k, &bars.kv_full[stage], 0, j * 128, bh);
                     } else {
-                        const bool exact = (p.hflag[it.h] & 2u) != 0;
                         const float* as = exact ? p.a2p : p.eap;
                         const float* rs = exact ? p.r2p : p.erp;
                         mbar_expect_tx(&bars.kv_full[stage], kTileBytes + 512 + 1536);
