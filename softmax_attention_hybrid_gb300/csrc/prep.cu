@@ -127,13 +127,14 @@ lognorm_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all,
 // (Z' < 1.6e-28) is flagged (hflag bit 1) and the kernels use the exact form.
 // log Z comes from lz_src (row stride lz_stride): the lognorm output in the
 // forward pass, the frozen rows of lse (batch entry 0) in the backward pass.
-// Grid (H); 512 threads; padded lengths Tp (a, invz) and Tp + 256 (r).
+// Grid (ceil((Tp + 256) / 512), H): every block reduces A and R over the
+// head, then writes its 512 entries; padded lengths Tp (a, invz) and Tp + 256 (r).
 __global__ void __launch_bounds__(512)
 frozen_prep_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all, int ld, HeadMask mask, int T,
                    int Tp, const float* __restrict__ lz_src, long long lz_stride, float* __restrict__ a2p,
                    float* __restrict__ r2p, float* __restrict__ eap, float* __restrict__ erp,
                    float* __restrict__ invz, uint32_t* __restrict__ hflag) {
-    const int h = blockIdx.x;
+    const int h = blockIdx.y;
     if (!head_frozen(mask, h)) return;
     const float* a = a_all + (size_t)h * ld;
     const float* r = r_all + (size_t)h * ld;
@@ -149,7 +150,7 @@ frozen_prep_kernel(const float* __restrict__ a_all, const float* __restrict__ r_
     const float A = block_max(ma, red);
     const float R = block_max(mr, red);
     const size_t ra = (size_t)h * Tp, rr = (size_t)h * (Tp + 256);
-    for (int u = threadIdx.x; u < Tp + 256; u += blockDim.x) {
+    for (int u = blockIdx.x * blockDim.x + threadIdx.x; u < Tp + 256; u += gridDim.x * blockDim.x) {
         const int dl = u - 127;
         const bool in = dl >= 0 && dl < T;
         r2p[rr + u] = in ? r[dl] * kLog2e : -INFINITY;
@@ -234,7 +235,8 @@ cudaError_t launch_lognorm(const LayerArgs& p, cudaStream_t s) {
 cudaError_t launch_pattern_prep(const LayerArgs& p, const float* lz_src, long long lz_stride, cudaStream_t s) {
     const int Tp = (p.T + 127) / 128 * 128;
     before_launch(SAF_KERNEL_PATTERN_PREP, s);
-    frozen_prep_kernel<<<p.H, 512, 0, s>>>(p.a, p.r, p.ld_prior, p.mask, p.T, Tp, lz_src, lz_stride, p.a2p, p.r2p,
+    const dim3 grid((unsigned)((Tp + 256 + 511) / 512), (unsigned)p.H);
+    frozen_prep_kernel<<<grid, 512, 0, s>>>(p.a, p.r, p.ld_prior, p.mask, p.T, Tp, lz_src, lz_stride, p.a2p, p.r2p,
                                            p.eap, p.erp, p.invz, p.hflag);
     after_launch(SAF_KERNEL_PATTERN_PREP, s);
     return cudaGetLastError();
