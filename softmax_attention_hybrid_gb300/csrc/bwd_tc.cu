@@ -139,7 +139,7 @@ struct Barriers {
     uint64_t dp_full;       // dP^T of the current tile is in TMEM
     uint64_t s_consumed;    // pattern warps have read S^T (8 arrivals)
     uint64_t dp_consumed;   // pattern warps have read dP^T (8 arrivals)
-    uint64_t p_ready;       // P^T in TMEM and dS in shared memory (256 arrivals)
+    uint64_t p_ready;       // P^T in TMEM and dS in shared memory (8 warp arrivals)
     uint64_t tile_done;     // every MMA of the previous tile has completed
     uint64_t dq_free;       // dQ of the previous tile has been read out (8 arrivals)
     uint64_t dkv_free;      // dV, dK of the previous item have been read out (8 arrivals)
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         mbar_init(&bars.dp_full, 1);
         mbar_init(&bars.s_consumed, 8);
         mbar_init(&bars.dp_consumed, 8);
-        mbar_init(&bars.p_ready, 256);
+        mbar_init(&bars.p_ready, 8);
         mbar_init(&bars.tile_done, 1);
         mbar_init(&bars.dq_free, 8);
         mbar_init(&bars.dkv_free, 8);
@@ -533,10 +533,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                     if (!(ok = wait_tile_done())) break;
                     tmem_st32(lane_base + kColP + 32 * half, pk);
                 }
+                // every thread's P^T stores are complete and its dS stores visible to the
+                // tensor cores; the warp then hands the tile over with one arrival
                 tmem_st_wait();
                 fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(&bars.p_ready);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars.p_ready);
                 if (!it.frozen && i > 0) drain_dq(bh, qb - 1);
                 pending = true;
                 stage = (stage + 1) % kStages;
