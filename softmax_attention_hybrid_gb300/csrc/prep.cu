@@ -35,6 +35,30 @@ __device__ float block_max(float x, float* red) {
     return x;
 }
 
+// max a and max r of every frozen head (the A and R of the factorised form).
+// Grid (H), 1024 threads.
+__global__ void __launch_bounds__(1024)
+frozen_max_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all, int ld, HeadMask mask, int T,
+                  int H, float* __restrict__ amax) {
+    const int h = blockIdx.x;
+    if (!head_frozen(mask, h)) return;
+    const float* a = a_all + (size_t)h * ld;
+    const float* r = r_all + (size_t)h * ld;
+    __shared__ float red[32];
+    float ma = -INFINITY, mr = -INFINITY;
+#pragma unroll 4
+    for (int j = threadIdx.x; j < T; j += blockDim.x) {   // unrolled: the loads go out together
+        ma = fmaxf(ma, a[j]);
+        mr = fmaxf(mr, r[j]);
+    }
+    const float A = block_max(ma, red);
+    const float R = block_max(mr, red);
+    if (threadIdx.x == 0) {
+        amax[h] = A;
+        amax[H + h] = R;
+    }
+}
+
 // Eq. 3 factorises: exp(a[j] + r[i-j]) = e^{A+R} * ea[j] * er[i-j] with
 // ea = exp(a - A), er = exp(r - R), A = max a, R = max r. So
 //     Z(i) = e^{A+R} * sum_{j<=i} ea[j] er[i-j],
@@ -43,72 +67,120 @@ __device__ float block_max(float x, float* red) {
 // left the normal fp32 range; that row is recomputed exactly by a running
 // log-sum-exp and the head is flagged (kStatusRange, informational).
 //
-// Grid: (ceil(T / 128), H); 1024 threads, 8 per row (each sums every 8th
-// key). Keys are taken in chunks of kLzChunk: ea of the chunk and er of the
-// offsets that the block's rows need against it are staged in shared memory.
-constexpr int kLzRows = 128, kLzSplit = 8, kLzThreads = kLzRows * kLzSplit, kLzChunk = 2048;
+// lognorm_part_kernel: grid (ceil(T / 256) * kLzSplit, H), 256 threads. CTA
+// (row block rb, split s) takes its share of the chunks of kLzChunk keys that
+// rows 256 rb .. +255 need, so that the long row blocks are spread over
+// kLzSplit CTAs. Thread (warp w, lane l) sums rows i0 = 256 rb + 8 l .. +7
+// over key run w of each chunk (8 runs of kLzRun keys), eight keys per step:
+// the 15 er values that a step's 8 x 8 products need slide along the band in
+// registers, so a step costs 8 er and 8 ea shared loads for 64 FMAs. The er
+// staging is padded (one word every 8) so that the lanes' rows, 8 apart, hit
+// distinct banks. The 8 runs meet in shared memory; the split's partial sums
+// go to lzp[s][h][i].
+constexpr int kLzRows = 256, kLzThreads = 256, kLzRun = 128, kLzChunk = 8 * kLzRun;
+constexpr int kLzBand = kLzChunk + kLzRows;                 // er offsets a chunk needs
+__device__ __forceinline__ int lz_pad(int x) { return x + (x >> 3); }
 
 __global__ void __launch_bounds__(kLzThreads)
-lognorm_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all, int ld, HeadMask mask,
-               int T, float* __restrict__ lz, uint32_t* __restrict__ hflag, uint32_t* __restrict__ status) {
+lognorm_part_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all, int ld, HeadMask mask,
+                    int T, int H, int Tp, const float* __restrict__ amax, float* __restrict__ lzp) {
     const int h = blockIdx.y;
     if (!head_frozen(mask, h)) return;
     const float* a = a_all + (size_t)h * ld;
     const float* r = r_all + (size_t)h * ld;
-    __shared__ float red[32];
-    __shared__ float ea_s[kLzChunk];
-    __shared__ float er_s[kLzChunk + kLzRows];
+    __shared__ __align__(16) float ea_s[kLzChunk];
+    __shared__ float er_s[kLzBand + kLzBand / 8 + 8];
+    __shared__ float part[8][kLzRows];
+    const float A = amax[h], R = amax[H + h];
 
-    float ma = -INFINITY, mr = -INFINITY;
-    for (int j = threadIdx.x; j < T; j += blockDim.x) {
-        ma = fmaxf(ma, a[j]);
-        mr = fmaxf(mr, r[j]);
-    }
-    const float A = block_max(ma, red);
-    const float R = block_max(mr, red);
-
-    const int i0 = blockIdx.x * kLzRows;
-    const int imax = min(i0 + kLzRows, T) - 1;
-    const int i = i0 + (threadIdx.x >> 3), sp = threadIdx.x & 7;
-    float z = 0.f;
-    for (int j0 = 0; j0 <= imax; j0 += kLzChunk) {
-        // er_s[t] = er at offset i0 - j0 - kLzChunk + 1 + t (0 outside [0, T))
-        const int base = i0 - j0 - kLzChunk + 1;
-        for (int t = threadIdx.x; t < kLzChunk + kLzRows; t += blockDim.x) {
+    const int rb = blockIdx.x / kLzSplit, sp = blockIdx.x - rb * kLzSplit;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int I0 = rb * kLzRows;
+    const int imax = min(I0 + kLzRows, T) - 1;
+    const int nch = imax / kLzChunk + 1;   // chunks of keys 0 .. imax
+    const int c_beg = sp * nch / kLzSplit, c_end = (sp + 1) * nch / kLzSplit;
+    const int i0 = I0 + 8 * lane;   // my 8 rows
+    float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int c = c_beg; c < c_end; ++c) {
+        const int j0 = c * kLzChunk;
+        // er_s[pad(x - base)] = er at offset x, base = I0 - j0 - kLzChunk + 1 (0 outside [0, T))
+        const int base = I0 - j0 - kLzChunk + 1;
+#pragma unroll
+        for (int t = threadIdx.x; t < kLzBand; t += kLzThreads) {
             if (t < kLzChunk) ea_s[t] = (j0 + t <= imax) ? expf(a[j0 + t] - A) : 0.f;
             const int dl = base + t;
-            er_s[t] = (dl >= 0 && dl < T) ? expf(r[dl] - R) : 0.f;
+            er_s[lz_pad(t)] = (dl >= 0 && dl < T) ? expf(r[dl] - R) : 0.f;
         }
         __syncthreads();
-        if (i < T) {
-            // key j = j0 + jj meets offset i - j, i.e. er_s[(i - i0) + kLzChunk - 1 - jj]
-            const float* e = er_s + (i - i0) + kLzChunk - 1;
-            const int jend = min(kLzChunk - 1, i - j0);
-#pragma unroll 4
-            for (int jj = sp; jj <= jend; jj += kLzSplit) z = fmaf(ea_s[jj], e[-jj], z);
+        const int js = j0 + warp * kLzRun;   // my key run js .. js + kLzRun - 1
+        if (js <= i0 + 7 && js <= imax) {
+            // step at key j: W[t] = er[i0 - j - 7 + t], t = 0..14; row r, key j + m uses W[r - m + 7]
+            const int x0 = i0 - js - 7 - base;   // staging index of W[0] at the first step
+            float W[15];
+#pragma unroll
+            for (int t = 0; t < 15; ++t) W[t] = er_s[lz_pad(x0 + t)];
+            const int nsteps = (min(kLzRun, i0 + 8 - js) + 7) >> 3;
+            for (int st = 0; st < nsteps; ++st) {
+                const int jj = js - j0 + 8 * st;
+                const float4 e0 = *reinterpret_cast<const float4*>(ea_s + jj);
+                const float4 e1 = *reinterpret_cast<const float4*>(ea_s + jj + 4);
+                const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+#pragma unroll
+                for (int m = 0; m < 8; ++m)
+#pragma unroll
+                    for (int rr = 0; rr < 8; ++rr) z[rr] = fmaf(ev[m], W[rr - m + 7], z[rr]);
+                // slide the window 8 keys on: W[8..14] = W[0..6], W[0..7] = the next 8 offsets down
+#pragma unroll
+                for (int t = 14; t >= 8; --t) W[t] = W[t - 8];
+                const int xn = x0 - 8 * (st + 1);
+#pragma unroll
+                for (int t = 0; t < 8; ++t) W[t] = (xn + t >= 0) ? er_s[lz_pad(xn + t)] : 0.f;
+            }
         }
         __syncthreads();
     }
-    z += __shfl_xor_sync(0xffffffffu, z, 1);
-    z += __shfl_xor_sync(0xffffffffu, z, 2);
-    z += __shfl_xor_sync(0xffffffffu, z, 4);
-    if (i >= T || sp != 0) return;
+#pragma unroll
+    for (int rr = 0; rr < 8; ++rr) part[warp][8 * lane + rr] = z[rr];
+    __syncthreads();
+    const int i = I0 + threadIdx.x;
+    if (i >= T) return;
+    float zs = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) zs += part[w][threadIdx.x];
+    lzp[((size_t)sp * H + h) * Tp + i] = zs;
+}
+
+// log Z(i) = log(sum of the kLzSplit partial sums, in split order) + A + R,
+// or the exact running log-sum-exp where that sum underflows (see above).
+// Grid (ceil(T / 256), H), 256 threads.
+__global__ void __launch_bounds__(256)
+lognorm_finish_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all, int ld, HeadMask mask,
+                      int T, int H, int Tp, const float* __restrict__ amax, const float* __restrict__ lzp,
+                      float* __restrict__ lz, uint32_t* __restrict__ hflag, uint32_t* __restrict__ status) {
+    const int h = blockIdx.y;
+    if (!head_frozen(mask, h)) return;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= T) return;
+    float zs = 0.f;
+#pragma unroll
+    for (int sp = 0; sp < kLzSplit; ++sp) zs += lzp[((size_t)sp * H + h) * Tp + i];
     float out;
-    if (z >= 1e-28f) {
-        out = logf(z) + A + R;
+    if (zs >= 1e-28f) {
+        out = logf(zs) + amax[h] + amax[H + h];
     } else {
-        // exact running log-sum-exp over j <= i
-        float m = -INFINITY, s = 0.f;
+        const float* a = a_all + (size_t)h * ld;
+        const float* r = r_all + (size_t)h * ld;
+        float m = -INFINITY, sacc = 0.f;
         for (int j = 0; j <= i; ++j) {
             const float x = a[j] + r[i - j];
             if (x > m) {
-                s = s * expf(m - x) + 1.f;
+                sacc = sacc * expf(m - x) + 1.f;
                 m = x;
             } else {
-                s += expf(x - m);
+                sacc += expf(x - m);
             }
         }
-        out = m + logf(s);
+        out = m + logf(sacc);
         atomicOr(hflag + h, 1u);
         atomicOr(status, kStatusRange);
     }
@@ -127,28 +199,22 @@ lognorm_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all,
 // (Z' < 1.6e-28) is flagged (hflag bit 1) and the kernels use the exact form.
 // log Z comes from lz_src (row stride lz_stride): the lognorm output in the
 // forward pass, the frozen rows of lse (batch entry 0) in the backward pass.
-// Grid (ceil((Tp + 256) / 512), H): every block reduces A and R over the
-// head, then writes its 512 entries; padded lengths Tp (a, invz) and Tp + 256 (r).
+// A and R come from frozen_max_kernel. Grid (ceil((Tp + 256) / 512), H), 512
+// threads, one entry each; padded lengths Tp (a, invz) and Tp + 256 (r).
 __global__ void __launch_bounds__(512)
 frozen_prep_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all, int ld, HeadMask mask, int T,
                    int Tp, const float* __restrict__ lz_src, long long lz_stride, float* __restrict__ a2p,
                    float* __restrict__ r2p, float* __restrict__ eap, float* __restrict__ erp,
-                   float* __restrict__ invz, uint32_t* __restrict__ hflag) {
+                   float* __restrict__ invz, uint32_t* __restrict__ hflag, const float* __restrict__ amax, int H) {
     const int h = blockIdx.y;
     if (!head_frozen(mask, h)) return;
     const float* a = a_all + (size_t)h * ld;
     const float* r = r_all + (size_t)h * ld;
     const float* lz = lz_src + (size_t)h * lz_stride;
-    __shared__ float red[32];
     __shared__ int bad;
     if (threadIdx.x == 0) bad = 0;
-    float ma = -INFINITY, mr = -INFINITY;
-    for (int j = threadIdx.x; j < T; j += blockDim.x) {
-        ma = fmaxf(ma, a[j]);
-        mr = fmaxf(mr, r[j]);
-    }
-    const float A = block_max(ma, red);
-    const float R = block_max(mr, red);
+    __syncthreads();
+    const float A = amax[h], R = amax[H + h];
     const size_t ra = (size_t)h * Tp, rr = (size_t)h * (Tp + 256);
     for (int u = blockIdx.x * blockDim.x + threadIdx.x; u < Tp + 256; u += gridDim.x * blockDim.x) {
         const int dl = u - 127;
@@ -224,11 +290,20 @@ bwd_rowvec_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __re
 
 }  // namespace
 
+cudaError_t launch_frozen_max(const LayerArgs& p, cudaStream_t s) {
+    frozen_max_kernel<<<p.H, 1024, 0, s>>>(p.a, p.r, p.ld_prior, p.mask, p.T, p.H, p.amax);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_lognorm(const LayerArgs& p, cudaStream_t s) {
-    dim3 grid((p.T + kLzRows - 1) / kLzRows, p.H);
-    before_launch(SAF_KERNEL_LOGNORM, s);
-    lognorm_kernel<<<grid, kLzThreads, 0, s>>>(p.a, p.r, p.ld_prior, p.mask, p.T, p.lz, p.hflag, p.status);
-    after_launch(SAF_KERNEL_LOGNORM, s);
+    const int Tp = (p.T + 127) / 128 * 128;
+    const int nrb = (p.T + kLzRows - 1) / kLzRows;
+    note_launch();
+    lognorm_part_kernel<<<dim3((unsigned)(nrb * kLzSplit), (unsigned)p.H), kLzThreads, 0, s>>>(
+        p.a, p.r, p.ld_prior, p.mask, p.T, p.H, Tp, p.amax, p.lzp);
+    note_launch();
+    lognorm_finish_kernel<<<dim3((unsigned)((p.T + 255) / 256), (unsigned)p.H), 256, 0, s>>>(
+        p.a, p.r, p.ld_prior, p.mask, p.T, p.H, Tp, p.amax, p.lzp, p.lz, p.hflag, p.status);
     return cudaGetLastError();
 }
 
@@ -237,7 +312,7 @@ cudaError_t launch_pattern_prep(const LayerArgs& p, const float* lz_src, long lo
     before_launch(SAF_KERNEL_PATTERN_PREP, s);
     const dim3 grid((unsigned)((Tp + 256 + 511) / 512), (unsigned)p.H);
     frozen_prep_kernel<<<grid, 512, 0, s>>>(p.a, p.r, p.ld_prior, p.mask, p.T, Tp, lz_src, lz_stride, p.a2p, p.r2p,
-                                           p.eap, p.erp, p.invz, p.hflag);
+                                           p.eap, p.erp, p.invz, p.hflag, p.amax, p.H);
     after_launch(SAF_KERNEL_PATTERN_PREP, s);
     return cudaGetLastError();
 }

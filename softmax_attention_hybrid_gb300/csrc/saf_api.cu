@@ -18,6 +18,8 @@ WorkspaceLayout workspace_layout(int B, int H, int T, int backward, int bf16) {
     off = align_up(off + (size_t)H * T * sizeof(float), 256);
     L.hflag = off;
     off = align_up(off + (size_t)H * sizeof(uint32_t), 256);
+    L.amax = off;
+    off = align_up(off + (size_t)2 * H * sizeof(float), 256);
     if (bf16) {
         L.a2p = off;
         off = align_up(off + (size_t)H * Tp * sizeof(float), 256);
@@ -29,6 +31,15 @@ WorkspaceLayout workspace_layout(int B, int H, int T, int backward, int bf16) {
         off = align_up(off + (size_t)H * (Tp + 256) * sizeof(float), 256);
         L.invz = off;
         off = align_up(off + (size_t)H * Tp * sizeof(float), 256);
+    }
+    // normaliser partial sums, wherever log Z is computed (forward, fp32 backward): the
+    // bf16 forward borrows the a2p, r2p, eap, erp region (contiguous, at least 4 H Tp
+    // floats), which is written only afterwards
+    if (!backward && bf16) {
+        L.lzp = L.a2p;
+    } else if (!bf16) {
+        L.lzp = off;
+        off = align_up(off + (size_t)kLzSplit * H * Tp * sizeof(float), 256);
     }
     if (backward) {
         if (bf16) {
@@ -56,6 +67,8 @@ void before_launch(int kernel, cudaStream_t s) {
     ++g_launches;
     if (g_trace_start[kernel]) cudaEventRecord(g_trace_start[kernel], s);
 }
+
+void note_launch() { ++g_launches; }
 
 void after_launch(int kernel, cudaStream_t s) {
     if (g_trace_stop[kernel]) cudaEventRecord(g_trace_stop[kernel], s);
@@ -135,6 +148,8 @@ LayerArgs make_args(const void* q, const void* k, const void* v, const float* a,
     p.status = (uint32_t*)(ws + L.status);
     p.lz = (float*)(ws + L.lz);
     p.hflag = (uint32_t*)(ws + L.hflag);
+    p.amax = (float*)(ws + L.amax);
+    p.lzp = (!backward || !bf16) ? (float*)(ws + L.lzp) : nullptr;
     p.delta = (backward && !bf16) ? (float*)(ws + L.delta) : nullptr;
     p.dq_acc = (backward && bf16) ? (float*)(ws + L.dq_acc) : nullptr;
     p.rowvec = (backward && bf16) ? (float*)(ws + L.rowvec) : nullptr;
@@ -162,7 +177,16 @@ cudaError_t begin_call(const LayerArgs& p, const Common& c, bool backward, bool 
     if (e != cudaSuccess) return e;
     if (c.nfrozen == 0) return cudaSuccess;
     if (!backward || !bf16) {
-        e = launch_lognorm(p, s);
+        // max a, max r, then log Z (bracketed together for the trace events)
+        before_launch(SAF_KERNEL_LOGNORM, s);
+        e = launch_frozen_max(p, s);
+        if (e == cudaSuccess) e = launch_lognorm(p, s);
+        after_launch(SAF_KERNEL_LOGNORM, s);
+        if (e != cudaSuccess) return e;
+    } else {
+        before_launch(SAF_KERNEL_PATTERN_PREP, s);
+        e = launch_frozen_max(p, s);
+        after_launch(SAF_KERNEL_PATTERN_PREP, s);
         if (e != cudaSuccess) return e;
     }
     if (!bf16) return cudaSuccess;

@@ -42,6 +42,9 @@ enum : uint32_t {
     kStatusTimeout = 1u << 1,   // a bounded mbarrier wait expired
 };
 constexpr size_t kStatusBytes = 256;
+// Key splits of the normaliser convolution (a1): the keys of a row block are
+// summed by kLzSplit CTAs, whose partial sums are added in a fixed order.
+constexpr int kLzSplit = 4;
 constexpr int kCounterBwd = 8;
 constexpr int kCounterFwd = 9;
 
@@ -51,6 +54,9 @@ struct WorkspaceLayout {
     size_t status = 0;   // uint32[64]
     size_t lz = 0;       // fp32 [H, T]   log Z of frozen heads (batch independent)
     size_t hflag = 0;    // uint32 [H]    per-head flags raised by the normaliser prep
+    size_t amax = 0;     // fp32 [2, H]   max a, max r of frozen heads
+    size_t lzp = 0;      // fp32 [kLzSplit, H, Tp]  partial sums of the normaliser convolution
+                         //               (forward; in the bf16 path the a2p.. region, written later)
     size_t a2p = 0;      // fp32 [H, Tp]  a * log2(e), -inf padded (bf16 path)
     size_t r2p = 0;      // fp32 [H, Tp + 256]  r * log2(e) shifted by 127, -inf padded (bf16 path)
     size_t eap = 0;      // fp32 [H, Tp]  exp(a - max a), 0 padded (bf16 path)
@@ -80,6 +86,8 @@ struct LayerArgs {
     void* dv;
     float* lz;           // workspace: log Z [H, T]
     uint32_t* hflag;     // workspace: per-head flags [H]
+    float* amax;         // workspace: max a [H], max r [H]
+    float* lzp;          // workspace: normaliser partial sums [kLzSplit, H, Tp] (forward)
     float* delta;        // workspace: D [B, H, T]
     float* dq_acc;       // workspace: fp32 dQ accumulator [B, H, T, 64]
     float* a2p;          // workspace: padded a * log2(e) [H, Tp]
@@ -97,10 +105,13 @@ struct LayerArgs {
 // right before a launch and after_launch(...) right after it; they count
 // the launch and record the trace events of saf_set_trace_events.
 void before_launch(int kernel, cudaStream_t s);
+// a further launch inside a group bracketed by before_launch / after_launch
+void note_launch();
 void after_launch(int kernel, cudaStream_t s);
 
 // prep.cu
-cudaError_t launch_lognorm(const LayerArgs& p, cudaStream_t s);
+cudaError_t launch_frozen_max(const LayerArgs& p, cudaStream_t s);   // counted by the caller's before_launch
+cudaError_t launch_lognorm(const LayerArgs& p, cudaStream_t s);      // 2 launches, counted with note_launch
 cudaError_t launch_bwd_delta(const LayerArgs& p, bool bf16, cudaStream_t s);
 cudaError_t launch_pattern_prep(const LayerArgs& p, const float* lz_src, long long lz_stride, cudaStream_t s);
 cudaError_t launch_bwd_rowvec(const LayerArgs& p, cudaStream_t s);
