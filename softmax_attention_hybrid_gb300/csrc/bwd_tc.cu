@@ -4,7 +4,7 @@
 // programs accumulate value gradients for every head and key gradients for
 // ordinary heads. Here one persistent launch runs every key-block program of
 // both kinds of head; the query gradients of ordinary heads are produced in
-// the same programs (dQ = dS K per tile pair, added into an fp32 accumulator
+// the same programs (dQ = dS K per tile, added into an fp32 accumulator
 // in the workspace) instead of by a separate query-block pass that would
 // recompute S and dP. Frozen heads compute only dV = W^T dO (§3.3), with W
 // rebuilt from a, r and log Z; their dK rows are written as zeros here and

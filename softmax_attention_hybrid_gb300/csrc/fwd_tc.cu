@@ -20,11 +20,14 @@
 //                     alone cannot issue tcgen05.mma fast enough to keep the
 //                     tensor core busy at N = 64); warp 9 owns tensor memory
 // Tensor memory (512 columns), per tile g at column 256g:
-//   [0, 128)   S = Q K^T (fp32)
-//   [128, 192) P or W (bf16 pairs), the A operand of the P V MMA
+//   [0, 128)   S = Q K^T (fp32); frozen items: W of odd key blocks (bf16 pairs)
+//   [128, 192) P, or W of even key blocks (bf16 pairs), the A operand of P V
 //   [192, 256) O accumulator (fp32)
-// Shared memory: Q tiles (2 x 16 KB), kStages K/V stages (32 KB each), and a
-// small staging area per group for the frozen pattern.
+// Frozen items have no S, so their W alternates between the two buffers and
+// the next block's W is built while the current P V runs.
+// Shared memory: Q tiles (2 x 16 KB) and kStages K/V stages (32 KB each); for
+// frozen items the K slot of a stage holds the key block's slice of a and the
+// band of r that the tiles' diagonals need.
 #include <string.h>
 
 #include "saf_internal.h"
