@@ -331,11 +331,13 @@ def run_ours(args, w):
     if args.all_ordinary and w.F > 0:
         for _ in range(max(1, args.warmup // 2)):
             step([0] * H)
-        ms0, _, _ = timed([0] * H, args.steps, False)
+        # traced like the hybrid run, so that both carry the same event overhead
+        ms0, kms0, _ = timed([0] * H, args.steps, True)
         ao_ms = max_over_ranks(sum(ms0) / len(ms0), world, dev)
         allord = {"ms_per_step": ao_ms, "speedup": ao_ms / step_ms,
                   "ideal_speedup": F.layer_flops(B, H, 0, T, d, not w.fwd_only) /
-                  F.layer_flops(B, H, w.F, T, d, not w.fwd_only)}
+                  F.layer_flops(B, H, w.F, T, d, not w.fwd_only),
+                  "kernel_ms": kms0}
 
     # end to end: host buffers in, host buffers out, through the same C ABI
     e2e = None

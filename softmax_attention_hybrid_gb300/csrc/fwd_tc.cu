@@ -444,15 +444,36 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                                                                       SmemLayout::frz_band) +
                                        128 * g + r + 127;
                     if (!exact) {
+                        // W is Toeplitz up to the column factor exp(a[k] - A). In the 16x128b
+                        // shape a thread holds rows 32 wq + rho + 8 m (m = 0..3) at packed
+                        // columns 4 j + q, keys k = 8 j + 2 q + {0, 1} (j = 0..15): the band
+                        // value of (row, k) depends on m - j alone, so 38 band loads serve
+                        // the thread's 128 products (one per product in the row-per-thread
+                        // shape).
+                        const int wq = warp & 3, rho = lane >> 2, q = lane & 3;
+                        const float* b0 = bnd - r + 32 * wq + rho - 2 * q;   // b0[8 (m - j) - v]
+                        float e0[19], e1[19];   // index m - j + 15
 #pragma unroll
-                        for (int h4 = 0; h4 < 4; ++h4) {
-                            uint32_t pk[16];
+                        for (int d = -15; d <= 3; ++d) {
+                            e0[d + 15] = b0[8 * d];
+                            e1[d + 15] = b0[8 * d - 1];
+                        }
+                        float2 ea[16];
 #pragma unroll
-                            for (int c = 0; c < 16; ++c) {
-                                const int cc = 32 * h4 + 2 * c;
-                                pk[c] = pack_bf16(bnd[-cc] * a2s[cc], bnd[-cc - 1] * a2s[cc + 1]);
+                        for (int j2 = 0; j2 < 16; ++j2) ea[j2] = *reinterpret_cast<const float2*>(a2s + 8 * j2 + 2 * q);
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            uint32_t pk[32];
+#pragma unroll
+                            for (int j2 = 0; j2 < 16; ++j2) {
+#pragma unroll
+                                for (int s2 = 0; s2 < 2; ++s2) {
+                                    const int d = 2 * hh + s2 - j2 + 15;
+                                    const float2 w = fmul2(make_float2(e0[d], e1[d]), ea[j2]);
+                                    pk[2 * j2 + s2] = pack_bf16(w.x, w.y);
+                                }
                             }
-                            tmem_st16(lane_base + wcol + 16 * h4, pk);
+                            tmem_st_16x128b_x16(lane_base + ((uint32_t)(16 * hh) << 16) + wcol, pk);
                         }
                     } else {
 #pragma unroll
