@@ -240,6 +240,22 @@ def kernel_bound(name, dtype):
     return "tensor" if dtype == "bf16" and name in ("fwd", "bwd") else "alu"
 
 
+def e2e_chunk_sizes(B, spec=""):
+    """Batch entries per chunk of the end-to-end step: four equal chunks when the
+    batch allows (fewer, smaller chunks leave the kernels short of work), else halves."""
+    if spec:
+        sizes = [int(x) for x in spec.split(",")]
+    elif B % 4 == 0 and B >= 8:
+        sizes = [B // 4] * 4
+    elif B % 2 == 0:
+        sizes = [B // 2] * 2
+    else:
+        sizes = [B]
+    if sum(sizes) != B or min(sizes) < 1:
+        raise ValueError(f"e2e chunks {sizes} do not partition the batch {B}")
+    return sizes
+
+
 def run_ours(args, w):
     rank, world, local = dist_info()
     torch.cuda.set_device(local)
@@ -357,8 +373,9 @@ def run_ours(args, w):
         # that the host-to-device copy of chunk c + 1 and the device-to-host copy of
         # chunk c - 1 run on their own streams while chunk c computes. Every byte of the
         # step's inputs and results still crosses in the timed region.
-        nch = 4 if B % 4 == 0 and B >= 8 else (2 if B % 2 == 0 else 1)
-        bs = B // nch
+        sizes = e2e_chunk_sizes(B, args.e2e_chunks)
+        nch = len(sizes)
+        bounds = [sum(sizes[:c]) for c in range(nch + 1)]
         s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
         per_batch = ("q", "k", "v", "do")
 
@@ -370,7 +387,7 @@ def run_ours(args, w):
                     if n in in_names:
                         g[n].copy_(host_in[n], non_blocking=True)
                 for c in range(nch):
-                    sl = slice(c * bs, (c + 1) * bs)
+                    sl = slice(bounds[c], bounds[c + 1])
                     for n in in_names:
                         if n in per_batch:
                             g[n][sl].copy_(host_in[n][sl], non_blocking=True)
@@ -378,7 +395,7 @@ def run_ours(args, w):
                     e.record(s_in)
                     ev_in.append(e)
             for c in range(nch):
-                sl = slice(c * bs, (c + 1) * bs)
+                sl = slice(bounds[c], bounds[c + 1])
                 stream.wait_event(ev_in[c])
                 saf.saf_attn_fwd(g["q"][sl], g["k"][sl], g["v"][sl], g["a"], g["r"], frozen, o=o[sl], lse=lse[sl],
                                  workspace=ws)
@@ -407,7 +424,7 @@ def run_ours(args, w):
         torch.cuda.synchronize()
         e_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in evs) / K, world, dev)
         e2e = {"value": total_flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "chunks": nch}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "chunks": sizes}
 
     if rank != 0:
         return 0
@@ -483,6 +500,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-all-ordinary", dest="all_ordinary", action="store_false")
+    ap.add_argument("--e2e-chunks", default="",
+                    help="batch entries per chunk of the end-to-end step, e.g. 2,2,2,2 (default: by batch size)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     w = WORKLOADS[args.workload]

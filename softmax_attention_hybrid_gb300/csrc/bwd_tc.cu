@@ -458,18 +458,25 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&bars.s_consumed);   // S^T of the next tile may land
-                        const float2* lse2 = reinterpret_cast<const float2*>(vec + 64 * half);
+                        // lse * log2(e) of four query columns per (broadcast) shared-memory load
+                        const float4* lse4 = reinterpret_cast<const float4*>(vec + 64 * half);
 #pragma unroll
-                        for (int e = 0; e < 64; e += 2) {
-                            const int q0 = 64 * half + e;
-                            // x = S * log2(e) / sqrt(d) - lse * log2(e), two columns per instruction
-                            const float2 x = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
-                                                   make_float2(kScaleLog2, kScaleLog2), neg2(lse2[e >> 1]));
-                            float p0 = fast_exp2(x.x);
-                            float p1 = fast_exp2(x.y);
-                            if (diag && j > q0) p0 = 0.f;
-                            if (diag && j > q0 + 1) p1 = 0.f;
-                            pk[e >> 1] = pack_bf16(p0, p1);
+                        for (int e = 0; e < 64; e += 4) {
+                            const float4 l4 = lse4[e >> 2];
+#pragma unroll
+                            for (int u = 0; u < 4; u += 2) {
+                                const int q0 = 64 * half + e + u;
+                                // x = S * log2(e) / sqrt(d) - lse * log2(e), two columns per instruction
+                                const float2 x = ffma2(
+                                    make_float2(__uint_as_float(sv[e + u]), __uint_as_float(sv[e + u + 1])),
+                                    make_float2(kScaleLog2, kScaleLog2),
+                                    u == 0 ? make_float2(-l4.x, -l4.y) : make_float2(-l4.z, -l4.w));
+                                float p0 = fast_exp2(x.x);
+                                float p1 = fast_exp2(x.y);
+                                if (diag && j > q0) p0 = 0.f;
+                                if (diag && j > q0 + 1) p1 = 0.f;
+                                pk[(e + u) >> 1] = pack_bf16(p0, p1);
+                            }
                         }
                     }
                     // the previous tile's MMAs are done: its dQ (same item) goes out first,
@@ -486,22 +493,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars.dp_consumed);   // dP^T of the next tile may land
                     tmem_st32(lane_base + kColP + 32 * half, pk);
-                    const float2* dvec = reinterpret_cast<const float2*>(vec + 128 + 64 * half);
+                    const float4* dvec4 = reinterpret_cast<const float4*>(vec + 128 + 64 * half);
 #pragma unroll
                     for (int g2 = 0; g2 < 2; ++g2) {
                         uint32_t dk[16];
 #pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            const int c = 32 * g2 + e;
-                            const int q0 = 64 * half + c;
-                            // dS = P o (dP - D) with P as rounded to bf16 for the MMAs
-                            const float2 pp = make_float2(__uint_as_float(pk[c >> 1] << 16),
-                                                          __uint_as_float(pk[c >> 1] & 0xffff0000u));
-                            const float2 dd = fmul2(pp, fsub2(make_float2(__uint_as_float(dp[c]),
-                                                                          __uint_as_float(dp[c + 1])),
-                                                              dvec[c >> 1]));
-                            dk[e >> 1] = pack_bf16(dd.x, dd.y);
-                            (void)q0;
+                        for (int e = 0; e < 32; e += 4) {
+                            const float4 d4 = dvec4[(32 * g2 + e) >> 2];   // D of four query columns
+#pragma unroll
+                            for (int u = 0; u < 4; u += 2) {
+                                const int c = 32 * g2 + e + u;
+                                // dS = P o (dP - D) with P as rounded to bf16 for the MMAs
+                                const float2 pp = make_float2(__uint_as_float(pk[c >> 1] << 16),
+                                                              __uint_as_float(pk[c >> 1] & 0xffff0000u));
+                                const float2 dd = fmul2(
+                                    pp, fsub2(make_float2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])),
+                                              u == 0 ? make_float2(d4.x, d4.y) : make_float2(d4.z, d4.w)));
+                                dk[(e + u) >> 1] = pack_bf16(dd.x, dd.y);
+                            }
                         }
                         // dS row j, queries 64*half + 32*g2 .. +31: MN-major atom `half`, K-row j
 #pragma unroll
@@ -513,15 +522,32 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                     // W^T(j, q) = W(q, j) (Eq. 3); band[q] is r at offset q - j = (qb - kb) * 128 +
                     // q - j. Factorised: W(q, j) / exp(a[j] - A) = exp(r[q-j] - R) / Z'(q), no exp per
                     // element (exp(a[j] - A) is applied to dV). Exact: exp(a[j] + r[q-j] - log Z(q)).
-                    const float* band = vec + 256 + 127 - j;
                     uint32_t pk[32];
                     if (!exact) {
+                        // W^T is Toeplitz up to the column factor 1 / Z'(q). In the 16x128b shape
+                        // a thread holds key rows 32 quarter + rho + 8 m (m = 0..3) at packed
+                        // columns 4 jr + qq, queries q = 64 half + 8 jr + 2 qq + {0, 1}
+                        // (jr = 0..7): the band value of (row, q) depends on jr - m alone, so 22
+                        // band loads serve the thread's 64 products.
+                        const int rho = lane >> 2, qq = lane & 3;
+                        const float* b1 = vec + 256 + 127 + 64 * half + 2 * qq - 32 * quarter - rho;
+                        float e0[11], e1[11];   // index jr - m + 3
 #pragma unroll
-                        for (int e = 0; e < 64; e += 2) {
-                            const int q0 = 64 * half + e;
-                            pk[e >> 1] = pack_bf16(band[q0] * vec[q0], band[q0 + 1] * vec[q0 + 1]);
+                        for (int d = -3; d <= 7; ++d) {
+                            e0[d + 3] = b1[8 * d];
+                            e1[d + 3] = b1[8 * d + 1];
+                        }
+#pragma unroll
+                        for (int jr = 0; jr < 8; ++jr) {
+                            const float2 iz = *reinterpret_cast<const float2*>(vec + 64 * half + 8 * jr + 2 * qq);
+#pragma unroll
+                            for (int m = 0; m < 4; ++m) {
+                                const float2 w = fmul2(make_float2(e0[jr - m + 3], e1[jr - m + 3]), iz);
+                                pk[16 * (m >> 1) + 2 * jr + (m & 1)] = pack_bf16(w.x, w.y);
+                            }
                         }
                     } else {
+                        const float* band = vec + 256 + 127 - j;
 #pragma unroll
                         for (int e = 0; e < 64; e += 2) {
                             const int q0 = 64 * half + e;
@@ -531,7 +557,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                         }
                     }
                     if (!(ok = wait_tile_done())) break;
-                    tmem_st32(lane_base + kColP + 32 * half, pk);
+                    if (!exact) {
+                        tmem_st_16x128b_x8(lane_base + kColP + 32 * half, pk);
+                        tmem_st_16x128b_x8(lane_base + (16u << 16) + kColP + 32 * half, pk + 16);
+                    } else {
+                        tmem_st32(lane_base + kColP + 32 * half, pk);
+                    }
                 }
                 // every thread's P^T stores are complete and its dS stores visible to the
                 // tensor cores; the warp then hands the tile over with one arrival
