@@ -266,6 +266,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             bool ok = true;
             const uint32_t sds = smem_u32(sm + Smem::ds);
             const uint32_t skv = smem_u32(sm + Smem::kv);
+            // descriptors of the fixed operands; per-stage ones are formed once per tile and
+            // every K step advances a descriptor by a constant
+            const uint64_t d_k = sdesc_sw128(skv, 16, 1024);                  // K, K-major (S^T)
+            const uint64_t d_v = sdesc_sw128(skv + kTileBytes, 16, 1024);     // V, K-major (dP^T)
+            const uint64_t d_kmn = sdesc_sw128(skv, 16384, 1024);             // K, MN-major (dQ)
+            const uint64_t d_ds = sdesc_sw128(sds, 16, 1024);                 // dS, K-major view (dK)
+            const uint64_t d_dsmn = sdesc_sw128(sds, 16384, 1024);            // dS, MN-major view (dQ)
             auto st_addr = [&](int s) { return smem_u32(sm + Smem::st + s * Smem::st_bytes); };
             auto wait_st = [&](int s) -> bool {
                 if (!mbar_wait(&bars.st_full[s], (st_full_bits >> s) & 1u, abort, status, kStatusTimeout))
@@ -275,19 +282,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 return true;
             };
             auto issue_s = [&](int s) {   // S^T = K Q^T
-                const uint32_t sq = st_addr(s);
+                const uint64_t d_q = sdesc_sw128(st_addr(s), 16, 1024);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma_ss(tmem + kColS, sdesc_sw128(skv + 32 * k, 16, 1024), sdesc_sw128(sq + 32 * k, 16, 1024),
-                           id_s, k > 0);
+                    mma_ss(tmem + kColS, sdesc_advance(d_k, 32 * k), sdesc_advance(d_q, 32 * k), id_s, k > 0);
                 mma_commit(&bars.s_full);
             };
             auto issue_dp = [&](int s) {  // dP^T = V dO^T
-                const uint32_t sdo = st_addr(s) + kTileBytes;
+                const uint64_t d_do = sdesc_sw128(st_addr(s) + kTileBytes, 16, 1024);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma_ss(tmem + kColDP, sdesc_sw128(skv + kTileBytes + 32 * k, 16, 1024),
-                           sdesc_sw128(sdo + 32 * k, 16, 1024), id_s, k > 0);
+                    mma_ss(tmem + kColDP, sdesc_advance(d_v, 32 * k), sdesc_advance(d_do, 32 * k), id_s, k > 0);
                 mma_commit(&bars.dp_full);
             };
             while (ok) {
@@ -336,18 +341,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                         dkv_free_ph ^= 1;
                     }
                     tc_fence_after();
-                    const uint32_t sq = st_addr(s), sdo = sq + kTileBytes;
+                    const uint32_t sq = st_addr(s);
+                    const uint64_t d_qmn = sdesc_sw128(sq, 16384, 1024);                // Q, MN-major (dK)
+                    const uint64_t d_domn = sdesc_sw128(sq + kTileBytes, 16384, 1024);  // dO, MN-major (dV)
                     // dV += P^T dO
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        mma_ts(tmem + kColDV, tmem + kColP + 8 * k, sdesc_sw128(sdo + 2048 * k, 16384, 1024), id_dv,
+                        mma_ts(tmem + kColDV, tmem + kColP + 8 * k, sdesc_advance(d_domn, 2048 * k), id_dv,
                                (i > 0 || k > 0) ? 1u : 0u);
                     if (!it.frozen) {
                         // dK += dS^T Q: dS viewed K-major (keys x queries, two 64-query halves)
 #pragma unroll
                         for (int k = 0; k < 8; ++k)
-                            mma_ss(tmem + kColDK, sdesc_sw128(sds + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
-                                   sdesc_sw128(sq + 2048 * k, 16384, 1024), id_dk, (i > 0 || k > 0) ? 1u : 0u);
+                            mma_ss(tmem + kColDK, sdesc_advance(d_ds, (k >> 2) * 16384 + (k & 3) * 32),
+                                   sdesc_advance(d_qmn, 2048 * k), id_dk, (i > 0 || k > 0) ? 1u : 0u);
                         // dQ may be overwritten once the previous tile's dQ has been read out
                         if (!(ok = mbar_wait(&bars.dq_free, dq_free_ph, abort, status, kStatusTimeout))) break;
                         dq_free_ph ^= 1;
@@ -355,8 +362,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                         // dQ = dS K: dS viewed MN-major (queries x keys)
 #pragma unroll
                         for (int k = 0; k < 8; ++k)
-                            mma_ss(tmem + kColDQ, sdesc_sw128(sds + 2048 * k, 16384, 1024),
-                                   sdesc_sw128(skv + 2048 * k, 16384, 1024), id_dq, k > 0);
+                            mma_ss(tmem + kColDQ, sdesc_advance(d_dsmn, 2048 * k), sdesc_advance(d_kmn, 2048 * k), id_dq,
+                                   k > 0);
                     }
                     mma_commit(&bars.tile_done);
                     mma_commit(&bars.st_empty[s]);

@@ -226,6 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             int stage = 0;
             bool ok = true;
             const uint32_t sqg = smem_u32(sm + SmemLayout::q) + g * kTileBytes;
+            const uint64_t d_q = sdesc_sw128(sqg, 16, 1024);   // this tile's Q, K-major
             const uint32_t d_s = tmem + 256 * g, d_p = d_s + 128, d_o = d_s + 192;
             for (int round = 0; ok; ++round) {
                 const int idx = item_index(round, cta, grid);
@@ -245,11 +246,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     if (!mbar_wait(&bars.s_empty[g], s_empty_ph, abort, status, kStatusTimeout)) return false;
                     s_empty_ph ^= 1;
                     tc_fence_after();
-                    const uint32_t sk = smem_u32(sm + SmemLayout::kv + stage_of(j) * SmemLayout::stage_bytes);
+                    const uint64_t d_k =
+                        sdesc_sw128(smem_u32(sm + SmemLayout::kv + stage_of(j) * SmemLayout::stage_bytes), 16, 1024);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        mma_ss(d_s, sdesc_sw128(sqg + 32 * k, 16, 1024), sdesc_sw128(sk + 32 * k, 16, 1024), idesc_s,
-                               k > 0);
+                        mma_ss(d_s, sdesc_advance(d_q, 32 * k), sdesc_advance(d_k, 32 * k), idesc_s, k > 0);
                     mma_commit(&bars.s_full[g]);
                     return true;
                 };
@@ -266,12 +267,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         p_full_ph ^= 1;
                     }
                     tc_fence_after();
-                    const uint32_t sv =
-                        smem_u32(sm + SmemLayout::kv + stage_of(j) * SmemLayout::stage_bytes + kTileBytes);
+                    const uint64_t d_v = sdesc_sw128(
+                        smem_u32(sm + SmemLayout::kv + stage_of(j) * SmemLayout::stage_bytes + kTileBytes), 16384, 1024);
                     const uint32_t a = (frz && (j & 1)) ? d_s : d_p;
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        mma_ts(d_o, a + 8 * k, sdesc_sw128(sv + 2048 * k, 16384, 1024), idesc_o,
+                        mma_ts(d_o, a + 8 * k, sdesc_advance(d_v, 2048 * k), idesc_o,
                                (j > 0 || k > 0) ? 1u : 0u);
                     mma_commit(frz ? &bars.w_done[g][j & 1] : &bars.o_done[g]);
                     return true;
