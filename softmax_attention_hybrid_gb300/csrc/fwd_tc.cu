@@ -10,8 +10,10 @@
 //
 // Work item: (batch b, head h, query-block pair p) = query rows
 // [256p, 256p + 256) as two 128-row tiles that share every K/V tile load.
-// Items are ordered longest first (descending p, ordinary before frozen) and
-// dealt to the persistent CTAs in a snake order.
+// Items are numbered longest first (descending p, ordinary before frozen); the
+// producer of each persistent CTA takes the next number from a global counter
+// when its CTA is ready for more work and publishes it to the CTA's other warps
+// through a small ring in shared memory.
 //
 // Warp roles (352 threads, one CTA per SM):
 //   warps 0-3 / 4-7 : softmax group g = 0 / 1, thread = one query row of tile g
@@ -39,6 +41,7 @@ namespace {
 using namespace tc;
 
 constexpr int kStages = 5;
+constexpr int kRing = 4;   // work items published ahead by the producer
 constexpr int kTileBytes = 128 * 64 * 2;  // one 128 x 64 bf16 tile
 constexpr int kThreads = 352;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -103,11 +106,6 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, int idx) {
     return it;
 }
 
-// The item index handled by CTA `cta` in round `round` (snake order).
-__device__ __forceinline__ int item_index(int round, int cta, int grid) {
-    return round * grid + ((round & 1) ? (grid - 1 - cta) : cta);
-}
-
 // 2^x on the special-function unit (ex2.approx, flushes subnormal results to 0).
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
@@ -121,6 +119,7 @@ struct Barriers {
     uint64_t s_full[2], s_empty[2], p_full[2], o_done[2];
     uint64_t w_full[2][2];   // frozen items: W buffer b of tile g is written (4 arrivals)
     uint64_t w_done[2][2];   // frozen items: P V of tile g that read W buffer b has completed
+    uint64_t item_full[kRing], item_empty[kRing];   // work-item ring (10 consumer warps)
 };
 
 __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ FwdParams p) {
@@ -129,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     // every access through it stays a shared-memory access
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     __shared__ Barriers bars;
+    __shared__ int item_ring[kRing];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
 
@@ -151,6 +151,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             mbar_init(&bars.w_full[g][0], 4);
             mbar_init(&bars.w_full[g][1], 4);
         }
+        for (int i = 0; i < kRing; ++i) {
+            mbar_init(&bars.item_full[i], 1);
+            mbar_init(&bars.item_empty[i], 10);   // 2 MMA issuers + 8 softmax warps
+        }
         fence_mbar_init();
     }
     if (warp == 9) {
@@ -163,7 +167,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     const uint32_t tmem = tmem_base_sh;
     volatile int* abort = &abort_flag;
     uint32_t* status = p.status;
-    const int grid = gridDim.x, cta = blockIdx.x;
 
     if (warp == 8) {
         // ------------------------------------------------------------ producer
@@ -175,9 +178,20 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             uint32_t kv_empty_bits = (1u << kStages) - 1;   // phase parity per stage, bit s
             int stage = 0;
             bool ok = true;
-            for (int round = 0; ok; ++round) {
-                const int idx = item_index(round, cta, grid);
-                if (idx >= p.n_items) break;
+            uint32_t ring_empty_bits = (1u << kRing) - 1;
+            int slot = 0;
+            while (ok) {
+                // next item from the global counter (longest first), published to the ring
+                if (!(ok = mbar_wait(&bars.item_empty[slot], (ring_empty_bits >> slot) & 1u, abort, status,
+                                     kStatusTimeout)))
+                    break;
+                ring_empty_bits ^= 1u << slot;
+                int idx = (int)atomicAdd(status + kCounterFwd, 1u);
+                if (idx >= p.n_items) idx = -1;
+                item_ring[slot] = idx;
+                mbar_arrive(&bars.item_full[slot]);
+                slot = (slot + 1) % kRing;
+                if (idx < 0) break;
                 const Item it = decode_item(p, idx);
                 const int bh = it.b * p.H + it.h;
                 const int qb0 = 2 * it.pair, qb1 = qb0 + 1;
@@ -228,9 +242,17 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             const uint32_t sqg = smem_u32(sm + SmemLayout::q) + g * kTileBytes;
             const uint64_t d_q = sdesc_sw128(sqg, 16, 1024);   // this tile's Q, K-major
             const uint32_t d_s = tmem + 256 * g, d_p = d_s + 128, d_o = d_s + 192;
-            for (int round = 0; ok; ++round) {
-                const int idx = item_index(round, cta, grid);
-                if (idx >= p.n_items) break;
+            uint32_t ring_full_bits = 0;
+            int slot = 0;
+            while (ok) {
+                if (!(ok = mbar_wait(&bars.item_full[slot], (ring_full_bits >> slot) & 1u, abort, status,
+                                     kStatusTimeout)))
+                    break;
+                ring_full_bits ^= 1u << slot;
+                const int idx = item_ring[slot];
+                mbar_arrive(&bars.item_empty[slot]);
+                slot = (slot + 1) % kRing;
+                if (idx < 0) break;
                 const Item it = decode_item(p, idx);
                 const int qb0 = 2 * it.pair, qb1 = qb0 + 1;
                 const bool t1 = qb1 < p.nqb;
@@ -330,9 +352,18 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         };
         int gblk = 0;   // key blocks of all previous items of this CTA (stage = gblk % kStages)
         bool ok = true;
-        for (int round = 0; ok; ++round) {
-            const int idx = item_index(round, cta, grid);
-            if (idx >= p.n_items) break;
+        uint32_t ring_full_bits = 0;
+        int slot = 0;
+        while (ok) {
+            if (!(ok = mbar_wait(&bars.item_full[slot], (ring_full_bits >> slot) & 1u, abort, status,
+                                 kStatusTimeout)))
+                break;
+            ring_full_bits ^= 1u << slot;
+            const int idx = item_ring[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.item_empty[slot]);
+            slot = (slot + 1) % kRing;
+            if (idx < 0) break;
             const Item it = decode_item(p, idx);
             const int item_blocks = (2 * it.pair + 1 < p.nqb) ? 2 * it.pair + 2 : 2 * it.pair + 1;
             const int gblk0 = gblk;
