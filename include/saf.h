@@ -118,7 +118,7 @@ SAF_API int saf_attn_fwd(const void* q, const void* k, const void* v,
  *
  *  - Size limit: saf_attn_workspace_bytes(B, H, T, d, dt, 0) must be at most
  *    8 MiB: about H * T <= 340,000 for SAF_BF16 (for example 12 heads of
- *    16,384 tokens) and H * T <= 400,000 for SAF_FP32, independent of B;
+ *    16,384 tokens) and H * T <= 2,000,000 for SAF_FP32, independent of B;
  *    larger problems return SAF_ESCRATCH and enqueue nothing.
  *  - Set-up: the first call on each device looks up the array's device
  *    address (cudaGetSymbolAddress, with that device current) and caches

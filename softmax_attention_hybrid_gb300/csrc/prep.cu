@@ -46,10 +46,22 @@ frozen_max_kernel(const float* __restrict__ a_all, const float* __restrict__ r_a
     const float* r = r_all + (size_t)h * ld;
     __shared__ float red[32];
     float ma = -INFINITY, mr = -INFINITY;
-#pragma unroll 4
-    for (int j = threadIdx.x; j < T; j += blockDim.x) {   // unrolled: the loads go out together
-        ma = fmaxf(ma, a[j]);
-        mr = fmaxf(mr, r[j]);
+    // 16 loads of a and 16 of r per thread go out before any is used, so that a
+    // row of up to 16 K entries costs one memory latency
+    constexpr int kPer = 16;
+    for (int base = 0; base < T; base += kPer * 1024) {
+        float va[kPer], vr[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int j = base + threadIdx.x + 1024 * k;
+            va[k] = j < T ? a[j] : -INFINITY;
+            vr[k] = j < T ? r[j] : -INFINITY;
+        }
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            ma = fmaxf(ma, va[k]);
+            mr = fmaxf(mr, vr[k]);
+        }
     }
     const float A = block_max(ma, red);
     const float R = block_max(mr, red);
@@ -67,63 +79,118 @@ frozen_max_kernel(const float* __restrict__ a_all, const float* __restrict__ r_a
 // left the normal fp32 range; that row is recomputed exactly by a running
 // log-sum-exp and the head is flagged (kStatusRange, informational).
 //
-// lognorm_part_kernel: grid (ceil(T / 256) * kLzSplit, H), 256 threads. CTA
-// (row block rb, split s) takes its share of the chunks of kLzChunk keys that
-// rows 256 rb .. +255 need, so that the long row blocks are spread over
-// kLzSplit CTAs. Thread (warp w, lane l) sums rows i0 = 256 rb + 8 l .. +7
-// over key run w of each chunk (8 runs of kLzRun keys), eight keys per step:
-// the 15 er values that a step's 8 x 8 products need slide along the band in
+// lognorm_kernel: one CTA per (frozen head, 128-row tile), numbered so that
+// the tiles with the most keys come first: the block scheduler then hands the
+// long tiles out early and fills in with short ones. 256 threads. Thread
+// (warp w, lane l) sums rows i0 = 128 t + 8 (l % 16) .. +7 over key run
+// 2 w + l / 16 of each chunk (16 runs of kLnRun keys), eight keys per step: the
+// 15 er values that a step's 8 x 8 products need slide along the band in
 // registers, so a step costs 8 er and 8 ea shared loads for 64 FMAs. The er
-// staging is padded (one word every 8) so that the lanes' rows, 8 apart, hit
-// distinct banks. The 8 runs meet in shared memory; the split's partial sums
-// go to lzp[s][h][i].
-constexpr int kLzRows = 256, kLzThreads = 256, kLzRun = 128, kLzChunk = 8 * kLzRun;
-constexpr int kLzBand = kLzChunk + kLzRows;                 // er offsets a chunk needs
+// staging is padded (one word every 8): a half-warp's rows, 8 apart, and the two
+// half-warps' runs, kLnRun apart, then fall on 32 distinct banks. The 16 runs
+// meet in shared memory and are added in a fixed order, so the result does not
+// depend on scheduling; a row whose sum underflows is recomputed by a running
+// log-sum-exp in the exact domain and its head is flagged.
+// kPre: ea and er come precomputed (eap, erp of the tensor-core path) and are
+// copied into shared memory asynchronously, the next chunk while the current
+// one is summed; otherwise every chunk stages exp(a - A), exp(r - R) itself.
+constexpr int kLnRows = 128, kLnThreads = 256, kLnRuns = 16, kLnRun = 128, kLnChunk = kLnRuns * kLnRun;
+constexpr int kLnBand = kLnChunk + kLnRows;   // er offsets a chunk needs
+constexpr int kLnBandPad = kLnBand + kLnBand / 8 + 8;
 __device__ __forceinline__ int lz_pad(int x) { return x + (x >> 3); }
 
-__global__ void __launch_bounds__(kLzThreads)
-lognorm_part_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all, int ld, HeadMask mask,
-                    int T, int H, int Tp, const float* __restrict__ amax, float* __restrict__ lzp) {
-    const int h = blockIdx.y;
-    if (!head_frozen(mask, h)) return;
+__device__ __forceinline__ uint32_t shared_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(shared_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(shared_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+template <bool kPre>
+__global__ void __launch_bounds__(kLnThreads)
+lognorm_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all, int ld, HeadMask mask, int T, int H,
+               int F, int nrt, int Tp, const float* __restrict__ eap, const float* __restrict__ erp,
+               const float* __restrict__ amax, float* __restrict__ lz, uint32_t* __restrict__ hflag,
+               uint32_t* __restrict__ status) {
+    // unit u: row tile nrt - 1 - u / F (longest first), f-th frozen head
+    const int u = blockIdx.x;
+    const int rt = nrt - 1 - u / F;
+    const int f = u - (u / F) * F;
+    int h = 0;
+    for (int c = -1; h < H; ++h)
+        if (head_frozen(mask, h) && ++c == f) break;
+    if (h >= H) return;
     const float* a = a_all + (size_t)h * ld;
     const float* r = r_all + (size_t)h * ld;
-    __shared__ __align__(16) float ea_s[kLzChunk];
-    __shared__ float er_s[kLzBand + kLzBand / 8 + 8];
-    __shared__ float part[8][kLzRows];
+    __shared__ __align__(16) float ea_s[2][kLnChunk];
+    __shared__ float er_s[2][kLnBandPad];
+    __shared__ float part[kLnRuns][kLnRows];
     const float A = amax[h], R = amax[H + h];
-
-    const int rb = blockIdx.x / kLzSplit, sp = blockIdx.x - rb * kLzSplit;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int I0 = rb * kLzRows;
-    const int imax = min(I0 + kLzRows, T) - 1;
-    const int nch = imax / kLzChunk + 1;   // chunks of keys 0 .. imax
-    const int c_beg = sp * nch / kLzSplit, c_end = (sp + 1) * nch / kLzSplit;
-    const int i0 = I0 + 8 * lane;   // my 8 rows
-    float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int c = c_beg; c < c_end; ++c) {
-        const int j0 = c * kLzChunk;
-        // er_s[pad(x - base)] = er at offset x, base = I0 - j0 - kLzChunk + 1 (0 outside [0, T))
-        const int base = I0 - j0 - kLzChunk + 1;
-#pragma unroll
-        for (int t = threadIdx.x; t < kLzBand; t += kLzThreads) {
-            if (t < kLzChunk) ea_s[t] = (j0 + t <= imax) ? expf(a[j0 + t] - A) : 0.f;
-            const int dl = base + t;
-            er_s[lz_pad(t)] = (dl >= 0 && dl < T) ? expf(r[dl] - R) : 0.f;
+    const int I0 = rt * kLnRows;
+    const int imax = min(I0 + kLnRows, T) - 1;
+    const int nch = imax / kLnChunk + 1;   // chunks of keys 0 .. imax
+    // er_s[b][pad(x)] = er at offset base(c) + x, base(c) = I0 - j0 - kLnChunk + 1 (0 outside [0, T));
+    // ea_s[b][t] = ea of key j0 + t (keys past imax meet only zero er: their value is not used)
+    auto stage = [&](int c, int b) {
+        const int j0 = c * kLnChunk;
+        const int base = I0 - j0 - kLnChunk + 1;
+        if (kPre) {
+            const float* eah = eap + (size_t)h * Tp;
+            const float* erh = erp + (size_t)h * (Tp + 256) + 127;   // erh[d], d in [-127, Tp + 129)
+            for (int q = threadIdx.x; q < kLnChunk / 4; q += kLnThreads) {
+                if (j0 + 4 * q < Tp)
+                    cp_async16(&ea_s[b][4 * q], eah + j0 + 4 * q);
+                else
+                    *reinterpret_cast<float4*>(&ea_s[b][4 * q]) = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            for (int t = threadIdx.x; t < kLnBand; t += kLnThreads) {
+                const int dl = base + t;
+                if (dl >= -127 && dl < Tp + 129)
+                    cp_async4(&er_s[b][lz_pad(t)], erh + dl);
+                else
+                    er_s[b][lz_pad(t)] = 0.f;
+            }
+        } else {
+            for (int t = threadIdx.x; t < kLnBand; t += kLnThreads) {
+                if (t < kLnChunk) ea_s[b][t] = (j0 + t <= imax) ? expf(a[j0 + t] - A) : 0.f;
+                const int dl = base + t;
+                er_s[b][lz_pad(t)] = (dl >= 0 && dl < T) ? expf(r[dl] - R) : 0.f;
+            }
         }
+    };
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int run = 2 * warp + (lane >> 4);
+    const int i0 = I0 + 8 * (lane & 15);   // my 8 rows
+    float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    stage(0, 0);
+    cp_async_commit();
+    for (int c = 0; c < nch; ++c) {
+        const int b = c & 1;
+        if (c + 1 < nch) stage(c + 1, b ^ 1);
+        cp_async_commit();       // (an empty group on the last chunk keeps the count)
+        cp_async_wait_prev();    // chunk c has landed
         __syncthreads();
-        const int js = j0 + warp * kLzRun;   // my key run js .. js + kLzRun - 1
+        const int j0 = c * kLnChunk;
+        const int base = I0 - j0 - kLnChunk + 1;
+        const float* eb = ea_s[b];
+        const float* rb = er_s[b];
+        const int js = j0 + run * kLnRun;   // my key run js .. js + kLnRun - 1
         if (js <= i0 + 7 && js <= imax) {
             // step at key j: W[t] = er[i0 - j - 7 + t], t = 0..14; row r, key j + m uses W[r - m + 7]
             const int x0 = i0 - js - 7 - base;   // staging index of W[0] at the first step
             float W[15];
 #pragma unroll
-            for (int t = 0; t < 15; ++t) W[t] = er_s[lz_pad(x0 + t)];
-            const int nsteps = (min(kLzRun, i0 + 8 - js) + 7) >> 3;
+            for (int t = 0; t < 15; ++t) W[t] = rb[lz_pad(x0 + t)];
+            const int nsteps = (min(kLnRun, i0 + 8 - js) + 7) >> 3;
             for (int st = 0; st < nsteps; ++st) {
                 const int jj = js - j0 + 8 * st;
-                const float4 e0 = *reinterpret_cast<const float4*>(ea_s + jj);
-                const float4 e1 = *reinterpret_cast<const float4*>(ea_s + jj + 4);
+                const float4 e0 = *reinterpret_cast<const float4*>(eb + jj);
+                const float4 e1 = *reinterpret_cast<const float4*>(eb + jj + 4);
                 const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
 #pragma unroll
                 for (int m = 0; m < 8; ++m)
@@ -134,42 +201,24 @@ lognorm_part_kernel(const float* __restrict__ a_all, const float* __restrict__ r
                 for (int t = 14; t >= 8; --t) W[t] = W[t - 8];
                 const int xn = x0 - 8 * (st + 1);
 #pragma unroll
-                for (int t = 0; t < 8; ++t) W[t] = (xn + t >= 0) ? er_s[lz_pad(xn + t)] : 0.f;
+                for (int t = 0; t < 8; ++t) W[t] = (xn + t >= 0) ? rb[lz_pad(xn + t)] : 0.f;
             }
         }
-        __syncthreads();
+        __syncthreads();         // buffer b is free for chunk c + 2
     }
 #pragma unroll
-    for (int rr = 0; rr < 8; ++rr) part[warp][8 * lane + rr] = z[rr];
+    for (int rr = 0; rr < 8; ++rr) part[run][8 * (lane & 15) + rr] = z[rr];
     __syncthreads();
+    if (threadIdx.x >= kLnRows) return;
     const int i = I0 + threadIdx.x;
     if (i >= T) return;
     float zs = 0.f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) zs += part[w][threadIdx.x];
-    lzp[((size_t)sp * H + h) * Tp + i] = zs;
-}
-
-// log Z(i) = log(sum of the kLzSplit partial sums, in split order) + A + R,
-// or the exact running log-sum-exp where that sum underflows (see above).
-// Grid (ceil(T / 256), H), 256 threads.
-__global__ void __launch_bounds__(256)
-lognorm_finish_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all, int ld, HeadMask mask,
-                      int T, int H, int Tp, const float* __restrict__ amax, const float* __restrict__ lzp,
-                      float* __restrict__ lz, uint32_t* __restrict__ hflag, uint32_t* __restrict__ status) {
-    const int h = blockIdx.y;
-    if (!head_frozen(mask, h)) return;
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= T) return;
-    float zs = 0.f;
-#pragma unroll
-    for (int sp = 0; sp < kLzSplit; ++sp) zs += lzp[((size_t)sp * H + h) * Tp + i];
+    for (int w = 0; w < kLnRuns; ++w) zs += part[w][threadIdx.x];
     float out;
     if (zs >= 1e-28f) {
-        out = logf(zs) + amax[h] + amax[H + h];
+        out = logf(zs) + A + R;
     } else {
-        const float* a = a_all + (size_t)h * ld;
-        const float* r = r_all + (size_t)h * ld;
         float m = -INFINITY, sacc = 0.f;
         for (int j = 0; j <= i; ++j) {
             const float x = a[j] + r[i - j];
@@ -201,6 +250,10 @@ lognorm_finish_kernel(const float* __restrict__ a_all, const float* __restrict__
 // forward pass, the frozen rows of lse (batch entry 0) in the backward pass.
 // A and R come from frozen_max_kernel. Grid (ceil((Tp + 256) / 512), H), 512
 // threads, one entry each; padded lengths Tp (a, invz) and Tp + 256 (r).
+// kParts: kPrepPad writes a2p, r2p, eap, erp (needs A, R only); kPrepInvz
+// writes invz and the hflag bit (needs log Z).
+constexpr int kPrepPad = 1, kPrepInvz = 2;
+template <int kParts>
 __global__ void __launch_bounds__(512)
 frozen_prep_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all, int ld, HeadMask mask, int T,
                    int Tp, const float* __restrict__ lz_src, long long lz_stride, float* __restrict__ a2p,
@@ -219,11 +272,15 @@ frozen_prep_kernel(const float* __restrict__ a_all, const float* __restrict__ r_
     for (int u = blockIdx.x * blockDim.x + threadIdx.x; u < Tp + 256; u += gridDim.x * blockDim.x) {
         const int dl = u - 127;
         const bool in = dl >= 0 && dl < T;
-        r2p[rr + u] = in ? r[dl] * kLog2e : -INFINITY;
-        erp[rr + u] = in ? expf(r[dl] - R) : 0.f;
-        if (u < Tp) {
+        if (kParts & kPrepPad) {
+            r2p[rr + u] = in ? r[dl] * kLog2e : -INFINITY;
+            erp[rr + u] = in ? expf(r[dl] - R) : 0.f;
+        }
+        if (u < Tp && (kParts & kPrepPad)) {
             a2p[ra + u] = u < T ? a[u] * kLog2e : -INFINITY;
             eap[ra + u] = u < T ? expf(a[u] - A) : 0.f;
+        }
+        if (u < Tp && (kParts & kPrepInvz)) {
             float iz = 0.f;
             if (u < T) {
                 const float sh = lz[u] - A - R;   // log Z'(u)
@@ -295,24 +352,43 @@ cudaError_t launch_frozen_max(const LayerArgs& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_lognorm(const LayerArgs& p, cudaStream_t s) {
+cudaError_t launch_lognorm(const LayerArgs& p, bool pre, cudaStream_t s) {
+    int F = 0;
+    for (int h = 0; h < p.H; ++h) F += head_frozen(p.mask, h) ? 1 : 0;
+    if (F == 0) return cudaSuccess;
     const int Tp = (p.T + 127) / 128 * 128;
-    const int nrb = (p.T + kLzRows - 1) / kLzRows;
+    const int nrt = (p.T + kLnRows - 1) / kLnRows;
     note_launch();
-    lognorm_part_kernel<<<dim3((unsigned)(nrb * kLzSplit), (unsigned)p.H), kLzThreads, 0, s>>>(
-        p.a, p.r, p.ld_prior, p.mask, p.T, p.H, Tp, p.amax, p.lzp);
-    note_launch();
-    lognorm_finish_kernel<<<dim3((unsigned)((p.T + 255) / 256), (unsigned)p.H), 256, 0, s>>>(
-        p.a, p.r, p.ld_prior, p.mask, p.T, p.H, Tp, p.amax, p.lzp, p.lz, p.hflag, p.status);
+    if (pre)
+        lognorm_kernel<true><<<(unsigned)(nrt * F), kLnThreads, 0, s>>>(
+            p.a, p.r, p.ld_prior, p.mask, p.T, p.H, F, nrt, Tp, p.eap, p.erp, p.amax, p.lz, p.hflag, p.status);
+    else
+        lognorm_kernel<false><<<(unsigned)(nrt * F), kLnThreads, 0, s>>>(
+            p.a, p.r, p.ld_prior, p.mask, p.T, p.H, F, nrt, Tp, nullptr, nullptr, p.amax, p.lz, p.hflag, p.status);
     return cudaGetLastError();
 }
 
-cudaError_t launch_pattern_prep(const LayerArgs& p, const float* lz_src, long long lz_stride, cudaStream_t s) {
+cudaError_t launch_frozen_pad(const LayerArgs& p, cudaStream_t s) {
+    const int Tp = (p.T + 127) / 128 * 128;
+    note_launch();
+    const dim3 grid((unsigned)((Tp + 256 + 511) / 512), (unsigned)p.H);
+    frozen_prep_kernel<kPrepPad><<<grid, 512, 0, s>>>(p.a, p.r, p.ld_prior, p.mask, p.T, Tp, nullptr, 0, p.a2p, p.r2p,
+                                                       p.eap, p.erp, p.invz, p.hflag, p.amax, p.H);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pattern_prep(const LayerArgs& p, const float* lz_src, long long lz_stride, bool pad,
+                                cudaStream_t s) {
     const int Tp = (p.T + 127) / 128 * 128;
     before_launch(SAF_KERNEL_PATTERN_PREP, s);
     const dim3 grid((unsigned)((Tp + 256 + 511) / 512), (unsigned)p.H);
-    frozen_prep_kernel<<<grid, 512, 0, s>>>(p.a, p.r, p.ld_prior, p.mask, p.T, Tp, lz_src, lz_stride, p.a2p, p.r2p,
-                                           p.eap, p.erp, p.invz, p.hflag, p.amax, p.H);
+    if (pad)
+        frozen_prep_kernel<kPrepPad | kPrepInvz><<<grid, 512, 0, s>>>(p.a, p.r, p.ld_prior, p.mask, p.T, Tp, lz_src,
+                                                                      lz_stride, p.a2p, p.r2p, p.eap, p.erp, p.invz,
+                                                                      p.hflag, p.amax, p.H);
+    else
+        frozen_prep_kernel<kPrepInvz><<<grid, 512, 0, s>>>(p.a, p.r, p.ld_prior, p.mask, p.T, Tp, lz_src, lz_stride,
+                                                           p.a2p, p.r2p, p.eap, p.erp, p.invz, p.hflag, p.amax, p.H);
     after_launch(SAF_KERNEL_PATTERN_PREP, s);
     return cudaGetLastError();
 }

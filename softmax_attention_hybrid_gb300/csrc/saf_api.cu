@@ -32,15 +32,6 @@ WorkspaceLayout workspace_layout(int B, int H, int T, int backward, int bf16) {
         L.invz = off;
         off = align_up(off + (size_t)H * Tp * sizeof(float), 256);
     }
-    // normaliser partial sums, wherever log Z is computed (forward, fp32 backward): the
-    // bf16 forward borrows the a2p, r2p, eap, erp region (contiguous, at least 4 H Tp
-    // floats), which is written only afterwards
-    if (!backward && bf16) {
-        L.lzp = L.a2p;
-    } else if (!bf16) {
-        L.lzp = off;
-        off = align_up(off + (size_t)kLzSplit * H * Tp * sizeof(float), 256);
-    }
     if (backward) {
         if (bf16) {
             L.rowvec = off;
@@ -149,7 +140,6 @@ LayerArgs make_args(const void* q, const void* k, const void* v, const float* a,
     p.lz = (float*)(ws + L.lz);
     p.hflag = (uint32_t*)(ws + L.hflag);
     p.amax = (float*)(ws + L.amax);
-    p.lzp = (!backward || !bf16) ? (float*)(ws + L.lzp) : nullptr;
     p.delta = (backward && !bf16) ? (float*)(ws + L.delta) : nullptr;
     p.dq_acc = (backward && bf16) ? (float*)(ws + L.dq_acc) : nullptr;
     p.rowvec = (backward && bf16) ? (float*)(ws + L.rowvec) : nullptr;
@@ -177,10 +167,13 @@ cudaError_t begin_call(const LayerArgs& p, const Common& c, bool backward, bool 
     if (e != cudaSuccess) return e;
     if (c.nfrozen == 0) return cudaSuccess;
     if (!backward || !bf16) {
-        // max a, max r, then log Z (bracketed together for the trace events)
+        // max a, max r, then log Z (bracketed together for the trace events); the
+        // tensor-core forward writes the padded exp(a - A), exp(r - R) slices first
+        // and sums those
         before_launch(SAF_KERNEL_LOGNORM, s);
         e = launch_frozen_max(p, s);
-        if (e == cudaSuccess) e = launch_lognorm(p, s);
+        if (e == cudaSuccess && bf16) e = launch_frozen_pad(p, s);
+        if (e == cudaSuccess) e = launch_lognorm(p, bf16, s);
         after_launch(SAF_KERNEL_LOGNORM, s);
         if (e != cudaSuccess) return e;
     } else {
@@ -192,8 +185,8 @@ cudaError_t begin_call(const LayerArgs& p, const Common& c, bool backward, bool 
     if (!bf16) return cudaSuccess;
     // log Z per row: the forward computed it above; the backward reads it from
     // the frozen rows of lse (batch entry 0, identical for every batch entry)
-    if (backward) return launch_pattern_prep(p, p.lse, (long long)p.T, s);
-    return launch_pattern_prep(p, p.lz, (long long)p.T, s);
+    if (backward) return launch_pattern_prep(p, p.lse, (long long)p.T, true, s);
+    return launch_pattern_prep(p, p.lz, (long long)p.T, false, s);
 }
 
 }  // namespace

@@ -42,9 +42,6 @@ enum : uint32_t {
     kStatusTimeout = 1u << 1,   // a bounded mbarrier wait expired
 };
 constexpr size_t kStatusBytes = 256;
-// Key splits of the normaliser convolution (a1): the keys of a row block are
-// summed by kLzSplit CTAs, whose partial sums are added in a fixed order.
-constexpr int kLzSplit = 4;
 constexpr int kCounterBwd = 8;
 constexpr int kCounterFwd = 9;
 
@@ -55,8 +52,6 @@ struct WorkspaceLayout {
     size_t lz = 0;       // fp32 [H, T]   log Z of frozen heads (batch independent)
     size_t hflag = 0;    // uint32 [H]    per-head flags raised by the normaliser prep
     size_t amax = 0;     // fp32 [2, H]   max a, max r of frozen heads
-    size_t lzp = 0;      // fp32 [kLzSplit, H, Tp]  partial sums of the normaliser convolution
-                         //               (forward; in the bf16 path the a2p.. region, written later)
     size_t a2p = 0;      // fp32 [H, Tp]  a * log2(e), -inf padded (bf16 path)
     size_t r2p = 0;      // fp32 [H, Tp + 256]  r * log2(e) shifted by 127, -inf padded (bf16 path)
     size_t eap = 0;      // fp32 [H, Tp]  exp(a - max a), 0 padded (bf16 path)
@@ -87,7 +82,6 @@ struct LayerArgs {
     float* lz;           // workspace: log Z [H, T]
     uint32_t* hflag;     // workspace: per-head flags [H]
     float* amax;         // workspace: max a [H], max r [H]
-    float* lzp;          // workspace: normaliser partial sums [kLzSplit, H, Tp] (forward)
     float* delta;        // workspace: D [B, H, T]
     float* dq_acc;       // workspace: fp32 dQ accumulator [B, H, T, 64]
     float* a2p;          // workspace: padded a * log2(e) [H, Tp]
@@ -111,9 +105,13 @@ void after_launch(int kernel, cudaStream_t s);
 
 // prep.cu
 cudaError_t launch_frozen_max(const LayerArgs& p, cudaStream_t s);   // counted by the caller's before_launch
-cudaError_t launch_lognorm(const LayerArgs& p, cudaStream_t s);      // 2 launches, counted with note_launch
+// log Z of the frozen heads; pre: from the eap, erp slices written by launch_frozen_pad
+cudaError_t launch_lognorm(const LayerArgs& p, bool pre, cudaStream_t s);   // 1 launch, counted with note_launch
+cudaError_t launch_frozen_pad(const LayerArgs& p, cudaStream_t s);          // 1 launch, counted with note_launch
 cudaError_t launch_bwd_delta(const LayerArgs& p, bool bf16, cudaStream_t s);
-cudaError_t launch_pattern_prep(const LayerArgs& p, const float* lz_src, long long lz_stride, cudaStream_t s);
+// 1 / Z' and the exact-form flag from log Z; pad: also the padded a, r slices
+cudaError_t launch_pattern_prep(const LayerArgs& p, const float* lz_src, long long lz_stride, bool pad,
+                                cudaStream_t s);
 cudaError_t launch_bwd_rowvec(const LayerArgs& p, cudaStream_t s);
 
 // fwd_tc.cu: tensor-core forward (bf16)
