@@ -40,7 +40,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kStages = 3;   // more stages measured slower: the larger shared-memory carve-out leaves less L1
+constexpr int kStages = 3;   // 4 and 5 measured slower (likely: a larger shared-memory carve-out leaves less L1)
 constexpr int kRing = 4;   // work items published ahead by the producer
 constexpr int kTileBytes = 128 * 64 * 2;  // one 128 x 64 bf16 tile
 constexpr int kThreads = 352;
