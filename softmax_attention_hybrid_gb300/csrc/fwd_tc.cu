@@ -417,20 +417,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     }
                     const float m_new = fmaxf(m_used, mx);
                     const bool need = m_new > m_used + kRescaleThreshold;
-                    if (j > 0 && __any_sync(0xffffffffu, need)) {
-                        const float f = need ? fast_exp2(m_used - m_new) : 1.f;
-                        uint32_t ov[16];
-#pragma unroll
-                        for (int c0 = 0; c0 < 64; c0 += 16) {
-                            tmem_ld16(lane_base + 192 + c0, ov);
-                            tmem_ld_wait();
-#pragma unroll
-                            for (int c = 0; c < 16; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * f);
-                            tmem_st16(lane_base + 192 + c0, ov);
-                        }
-                    }
+                    const float f = need ? fast_exp2(m_used - m_new) : 1.f;   // O and l rescale factor
                     if (need) {
-                        l *= fast_exp2(m_used - m_new);
+                        l *= f;
                         m_used = m_new;
                     }
                     // P = 2^(S log2(e) / sqrt(d) - m): two columns per FFMA and per FADD
@@ -455,6 +444,19 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         tmem_st16(lane_base + 128 + 16 * h4, pk);
                     }
                     l += (acc0.x + acc1.x) + (acc0.y + acc1.y);
+                    // rescale O (stable: the previous P V is done) before this block's P V adds
+                    // to it; done after the exp loop, when the row's scores no longer hold registers
+                    if (j > 0 && __any_sync(0xffffffffu, need)) {
+                        uint32_t ov[16];
+#pragma unroll
+                        for (int c0 = 0; c0 < 64; c0 += 16) {
+                            tmem_ld16(lane_base + 192 + c0, ov);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int c = 0; c < 16; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * f);
+                            tmem_st16(lane_base + 192 + c0, ov);
+                        }
+                    }
                 } else {
                     // Frozen tile of Eq. 3 from the key block's a values and the band of r values
                     // the producer staged in the K slot. Factorised form: W(i, k) Z'(i) =
