@@ -350,6 +350,27 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             tc_fence_after();
             return true;
         };
+        // epilogue of a row: O (tensor memory) times inv, rounded to bf16, and the row's lse
+        auto store_o = [&](int bh, int row, float inv, float lse_row) {
+            uint32_t ov[64];
+            tmem_ld32(lane_base + 192, ov);
+            tmem_ld32(lane_base + 224, ov + 32);
+            tmem_ld_wait();
+            tc_fence_before();
+            if (row < p.T) {
+                uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)bh * p.T + row) * 64);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 w;
+                    w.x = pack_bf16(__uint_as_float(ov[8 * c + 0]) * inv, __uint_as_float(ov[8 * c + 1]) * inv);
+                    w.y = pack_bf16(__uint_as_float(ov[8 * c + 2]) * inv, __uint_as_float(ov[8 * c + 3]) * inv);
+                    w.z = pack_bf16(__uint_as_float(ov[8 * c + 4]) * inv, __uint_as_float(ov[8 * c + 5]) * inv);
+                    w.w = pack_bf16(__uint_as_float(ov[8 * c + 6]) * inv, __uint_as_float(ov[8 * c + 7]) * inv);
+                    dst[c] = w;
+                }
+                p.lse[(size_t)bh * p.T + row] = lse_row;
+            }
+        };
         int gblk = 0;   // key blocks of all previous items of this CTA (stage = gblk % kStages)
         bool ok = true;
         uint32_t ring_full_bits = 0;
@@ -373,19 +394,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             const int bh = it.b * p.H + it.h;
             const int row = qb * 128 + r;
             const int nblk = qb + 1;
-            float m_used = -INFINITY, l = 0.f;
-            float lz2 = INFINITY;   // exact form: log2 Z(i)
-            float iz = 0.f;         // factorised form: 1 / Z'(i)
-            bool exact = false;
-            if (it.frozen) {
-                exact = (p.hflag[it.h] & 2u) != 0;
-                if (row < p.T) {
-                    lz2 = p.lz[(size_t)it.h * p.T + row] * kLog2e;
-                    iz = p.invz[(size_t)it.h * p.Tp + row];
-                }
-            }
-            for (int j = 0; j < nblk && ok; ++j) {
-                if (!it.frozen) {
+            if (!it.frozen) {
+                float m_used = -INFINITY, l = 0.f;
+                for (int j = 0; j < nblk && ok; ++j) {
                     if (!(ok = mbar_wait(&bars.s_full[g], s_full_ph, abort, status, kStatusTimeout))) break;
                     s_full_ph ^= 1;
                     tc_fence_after();
@@ -457,7 +468,22 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                             tmem_st16(lane_base + 192 + c0, ov);
                         }
                     }
-                } else {
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars.p_full[g]);
+                }
+                if (!ok) break;
+                // epilogue: O = acc / l
+                if (!(ok = mbar_wait(&bars.o_done[g], o_done_ph, abort, status, kStatusTimeout))) break;
+                o_done_ph ^= 1;
+                tc_fence_after();
+                store_o(bh, row, 1.f / l, (m_used + log2f(l)) / kLog2e);
+            } else {
+                // frozen item: the exact or the factorised form of Eq. 3 (per-head flag)
+                const bool exact = (p.hflag[it.h] & 2u) != 0;
+                const float lz2 = row < p.T ? p.lz[(size_t)it.h * p.T + row] * kLog2e : INFINITY;   // log2 Z(i)
+                for (int j = 0; j < nblk && ok; ++j) {
                     // Frozen tile of Eq. 3 from the key block's a values and the band of r values
                     // the producer staged in the K slot. Factorised form: W(i, k) Z'(i) =
                     // exp(r[i-k] - R) exp(a[k] - A), no exp per element (1 / Z' is applied to O).
@@ -523,46 +549,22 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                             tmem_st16(lane_base + wcol + 16 * h4, pk);
                         }
                     }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars.w_full[g][j & 1]);
+                    w_pend[j & 1] = true;
                 }
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(it.frozen ? &bars.w_full[g][j & 1] : &bars.p_full[g]);
-                if (it.frozen) w_pend[j & 1] = true;
-            }
-            if (!ok) break;
-            // epilogue: O = acc / l (ordinary) or acc (frozen: W rows sum to one)
-            if (it.frozen) {
+                if (!ok) break;
                 // the last P V (and, completing in order, every earlier one) is done; the next
                 // item's S may now overwrite the W columns
                 if (!(ok = wait_w((nblk - 1) & 1))) break;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars.s_empty[g]);
-            } else {
-                if (!(ok = mbar_wait(&bars.o_done[g], o_done_ph, abort, status, kStatusTimeout))) break;
-                o_done_ph ^= 1;
-                tc_fence_after();
-            }
-            uint32_t ov[64];
-            tmem_ld32(lane_base + 192, ov);
-            tmem_ld32(lane_base + 224, ov + 32);
-            tmem_ld_wait();
-            tc_fence_before();
-            if (row < p.T) {
-                // ordinary: 1 / l; frozen: W rows sum to one in the exact form, and
-                // carry the factor Z'(i) in the factorised form
-                const float inv = it.frozen ? (exact ? 1.f : iz) : 1.f / l;
-                uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)bh * p.T + row) * 64);
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint4 w;
-                    w.x = pack_bf16(__uint_as_float(ov[8 * c + 0]) * inv, __uint_as_float(ov[8 * c + 1]) * inv);
-                    w.y = pack_bf16(__uint_as_float(ov[8 * c + 2]) * inv, __uint_as_float(ov[8 * c + 3]) * inv);
-                    w.z = pack_bf16(__uint_as_float(ov[8 * c + 4]) * inv, __uint_as_float(ov[8 * c + 5]) * inv);
-                    w.w = pack_bf16(__uint_as_float(ov[8 * c + 6]) * inv, __uint_as_float(ov[8 * c + 7]) * inv);
-                    dst[c] = w;
-                }
-                p.lse[(size_t)bh * p.T + row] = it.frozen ? lz2 / kLog2e : (m_used + log2f(l)) / kLog2e;
+                // epilogue: W rows sum to one in the exact form and carry the factor Z'(i) in
+                // the factorised form
+                const float inv = (exact || row >= p.T) ? 1.f : p.invz[(size_t)it.h * p.Tp + row];
+                store_o(bh, row, inv, lz2 / kLog2e);
             }
         }
     }
