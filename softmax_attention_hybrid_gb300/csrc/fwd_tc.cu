@@ -15,7 +15,7 @@
 // when its CTA is ready for more work and publishes it to the CTA's other warps
 // through a small ring in shared memory.
 //
-// Warp roles (352 threads, one CTA per SM):
+// Warp roles (384 threads, one CTA per SM; warp 11 idles):
 //   warps 0-3 / 4-7 : softmax group g = 0 / 1, thread = one query row of tile g
 //   warp 8          : TMA producer (Q tiles, K/V stages)
 //   warps 9 / 10    : MMA issuers of tile 0 / 1 (one thread each; one thread
@@ -43,7 +43,13 @@ using namespace tc;
 constexpr int kStages = 3;   // 4 and 5 measured slower (likely: a larger shared-memory carve-out leaves less L1)
 constexpr int kRing = 4;   // work items published ahead by the producer
 constexpr int kTileBytes = 128 * 64 * 2;  // one 128 x 64 bf16 tile
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;   // 3 warpgroups: 2 softmax, 1 producer / issuers / idle
+// Register split (setmaxnreg): warpgroup 2 drops to kRegsOther registers per thread and
+// the softmax warpgroups rise to kRegsSoftmax. The launch gives every thread
+// kRegsLaunch (checked on the host); the split must not exceed that total:
+// 2 x 128 x kRegsSoftmax + 128 x kRegsOther <= 384 x kRegsLaunch.
+constexpr int kRegsLaunch = 168, kRegsSoftmax = 216, kRegsOther = 64;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther <= kThreads * kRegsLaunch, "register split too large");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kScaleLog2 = 0.125f * 1.4426950408889634f;  // log2(e) / sqrt(64)
 constexpr float kRescaleThreshold = 8.0f;                    // lazy rescale: factor 256
@@ -168,6 +174,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     volatile int* abort = &abort_flag;
     uint32_t* status = p.status;
 
+    // warpgroup 2 (warps 8-11) gives up registers in one instruction for the whole
+    // warpgroup; the softmax warpgroups take them
+    if (warp >= 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
     if (warp == 8) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
@@ -334,8 +344,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 stage = stage_of(nblk);
             }
         }
+    }   // warp 11: idle
     } else {
         // ------------------------------------------------------------ softmax groups
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
         const int g = warp >> 2;               // 0 or 1
         const int r = threadIdx.x & 127;       // row within the tile = TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16) + 256 * g;
@@ -620,6 +632,13 @@ cudaError_t launch_tc_fwd(const LayerArgs& a, cudaStream_t s) {
     const int smem = SmemLayout::total + 1024;
     cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    // The register split inside the kernel draws on the registers the launch hands out: a
+    // build that launches with fewer than kRegsLaunch per thread is refused here, since the
+    // softmax warpgroups could then never obtain theirs.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, fwd_tc_kernel);
+    if (e != cudaSuccess) return e;
+    if (2 * 128 * kRegsSoftmax + 128 * kRegsOther > kThreads * fa.numRegs) return cudaErrorInvalidConfiguration;
     const int grid = p.n_items < sms ? p.n_items : sms;
     before_launch(SAF_KERNEL_FWD, s);
     fwd_tc_kernel<<<grid, kThreads, smem, s>>>(p);
