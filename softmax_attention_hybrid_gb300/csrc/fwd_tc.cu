@@ -27,7 +27,8 @@
 //   [192, 256) O accumulator (fp32)
 // Frozen items have no S, so their W alternates between the two buffers and
 // the next block's W is built while the current P V runs.
-// Shared memory: Q tiles (2 x 16 KB) and kStages K/V stages (32 KB each); for
+// Shared memory: two Q slots of 2 tiles (16 KB each; alternate ordinary items, so
+// the next item's Q loads while this one runs) and kStages K/V stages (32 KB each); for
 // frozen items the K slot of a stage holds the key block's slice of a and the
 // band of r that the tiles' diagonals need.
 #include <string.h>
@@ -80,8 +81,9 @@ struct FwdParams {
 // tiles need (384 fp32 at byte 1024), in the factorised form (exp(a - A),
 // exp(r - R)) or, for flagged heads, in the exact form (log2 domain).
 struct SmemLayout {
-    static constexpr int q = 0;                                     // 2 tiles
-    static constexpr int kv = q + 2 * kTileBytes;                   // kStages x (K, V)
+    static constexpr int q = 0;                                     // 2 slots x 2 tiles
+    static constexpr int q_slot_bytes = 2 * kTileBytes;
+    static constexpr int kv = q + 2 * q_slot_bytes;                 // kStages x (K, V)
     static constexpr int stage_bytes = 2 * kTileBytes;
     static constexpr int frz_band = 1024;
     static constexpr int total = kv + kStages * stage_bytes;
@@ -120,7 +122,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 struct Barriers {
-    uint64_t q_full, q_empty;
+    uint64_t q_full[2], q_empty[2];   // Q slot of alternate ordinary items
     uint64_t kv_full[kStages], kv_empty[kStages];
     uint64_t s_full[2], s_empty[2], p_full[2], o_done[2];
     uint64_t w_full[2][2];   // frozen items: W buffer b of tile g is written (4 arrivals)
@@ -141,8 +143,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        mbar_init(&bars.q_full, 1);
-        mbar_init(&bars.q_empty, 2);   // one commit per issuer
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars.q_full[i], 1);
+            mbar_init(&bars.q_empty[i], 2);   // one commit per issuer
+        }
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&bars.kv_full[s], 1);
             mbar_init(&bars.kv_empty[s], 2);
@@ -184,7 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             tma_prefetch_desc(&p.tm_q);
             tma_prefetch_desc(&p.tm_k);
             tma_prefetch_desc(&p.tm_v);
-            uint32_t q_empty_ph = 1;
+            uint32_t q_empty_bits = 3;   // phase parity per Q slot
+            int nord = 0;                // ordinary items so far: Q slot nord & 1
             uint32_t kv_empty_bits = (1u << kStages) - 1;   // phase parity per stage, bit s
             int stage = 0;
             bool ok = true;
@@ -209,11 +214,17 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 const int nblk = t1 ? qb1 + 1 : qb0 + 1;
                 const bool exact = it.frozen && (p.hflag[it.h] & 2u) != 0;
                 if (!it.frozen) {
-                    if (!(ok = mbar_wait(&bars.q_empty, q_empty_ph, abort, status, kStatusTimeout))) break;
-                    q_empty_ph ^= 1;
-                    mbar_expect_tx(&bars.q_full, (t1 ? 2 : 1) * kTileBytes);
-                    tma_load_3d(sm + SmemLayout::q, &p.tm_q, &bars.q_full, 0, qb0 * 128, bh);
-                    if (t1) tma_load_3d(sm + SmemLayout::q + kTileBytes, &p.tm_q, &bars.q_full, 0, qb1 * 128, bh);
+                    // the next item's Q goes to the other slot while this CTA may still work
+                    // on the previous item
+                    const int qs = nord++ & 1;
+                    if (!(ok = mbar_wait(&bars.q_empty[qs], (q_empty_bits >> qs) & 1u, abort, status,
+                                         kStatusTimeout)))
+                        break;
+                    q_empty_bits ^= 1u << qs;
+                    uint8_t* sq = sm + SmemLayout::q + qs * SmemLayout::q_slot_bytes;
+                    mbar_expect_tx(&bars.q_full[qs], (t1 ? 2 : 1) * kTileBytes);
+                    tma_load_3d(sq, &p.tm_q, &bars.q_full[qs], 0, qb0 * 128, bh);
+                    if (t1) tma_load_3d(sq + kTileBytes, &p.tm_q, &bars.q_full[qs], 0, qb1 * 128, bh);
                 }
                 for (int j = 0; j < nblk; ++j) {
                     if (!(ok = mbar_wait(&bars.kv_empty[stage], (kv_empty_bits >> stage) & 1u, abort, status,
@@ -244,13 +255,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             const int g = warp - 9;
             const uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);  // S = Q K^T
             const uint32_t idesc_o = idesc_bf16(128, 64, 0, 1);   // O += P V, V MN-major
-            uint32_t q_full_ph = 0;
+            uint32_t q_full_bits = 0;    // phase parity per Q slot
+            int nord = 0;                // ordinary items so far: Q slot nord & 1
             uint32_t kv_full_bits = 0;   // phase parity per stage, bit s
             uint32_t s_empty_ph = 1, p_full_ph = 0, w_full_bits = 0;
             int stage = 0;
             bool ok = true;
-            const uint32_t sqg = smem_u32(sm + SmemLayout::q) + g * kTileBytes;
-            const uint64_t d_q = sdesc_sw128(sqg, 16, 1024);   // this tile's Q, K-major
+            uint64_t d_q = 0;   // this tile's Q (slot of the current item), K-major
+            int qs = 0;
             const uint32_t d_s = tmem + 256 * g, d_p = d_s + 128, d_o = d_s + 192;
             uint32_t ring_full_bits = 0;
             int slot = 0;
@@ -269,8 +281,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 const int ng = g == 0 ? qb0 + 1 : (t1 ? qb1 + 1 : 0);   // key blocks of my tile
                 const int nblk = t1 ? qb1 + 1 : qb0 + 1;                 // key blocks of the item
                 if (!it.frozen) {
-                    if (!(ok = mbar_wait(&bars.q_full, q_full_ph, abort, status, kStatusTimeout))) break;
-                    q_full_ph ^= 1;
+                    qs = nord++ & 1;
+                    if (!(ok = mbar_wait(&bars.q_full[qs], (q_full_bits >> qs) & 1u, abort, status, kStatusTimeout)))
+                        break;
+                    q_full_bits ^= 1u << qs;
+                    d_q = sdesc_sw128(smem_u32(sm + SmemLayout::q + qs * SmemLayout::q_slot_bytes) + g * kTileBytes, 16,
+                                      1024);
                 }
                 // stage index of block j is (stage + j) mod kStages
                 auto stage_of = [&](int j) { return (stage + j) % kStages; };
@@ -340,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     mma_commit(&bars.kv_empty[stage_of(j)]);
                 }
                 if (!ok) break;
-                if (!it.frozen) mma_commit(&bars.q_empty);
+                if (!it.frozen) mma_commit(&bars.q_empty[qs]);
                 stage = stage_of(nblk);
             }
         }
