@@ -135,8 +135,7 @@ struct Barriers {
     uint64_t item_full[kRing], item_empty[kRing];
     uint64_t kv_full, kv_empty;
     uint64_t st_full[kStages], st_empty[kStages];
-    uint64_t s_full;        // S^T of the current tile is in TMEM
-    uint64_t dp_full;       // dP^T of the current tile is in TMEM
+    uint64_t sdp_full;      // S^T and dP^T of the current tile are in TMEM (one commit after both)
     uint64_t s_consumed;    // pattern warps have read S^T (8 arrivals)
     uint64_t dp_consumed;   // pattern warps have read dP^T (8 arrivals)
     uint64_t p_ready;       // P^T in TMEM and dS in shared memory (8 warp arrivals)
@@ -168,8 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             mbar_init(&bars.st_full[i], 1);
             mbar_init(&bars.st_empty[i], 1);
         }
-        mbar_init(&bars.s_full, 1);
-        mbar_init(&bars.dp_full, 1);
+        mbar_init(&bars.sdp_full, 1);
         mbar_init(&bars.s_consumed, 8);
         mbar_init(&bars.dp_consumed, 8);
         mbar_init(&bars.p_ready, 8);
@@ -286,14 +284,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     mma_ss(tmem + kColS, sdesc_advance(d_k, 32 * k), sdesc_advance(d_q, 32 * k), id_s, k > 0);
-                mma_commit(&bars.s_full);
             };
             auto issue_dp = [&](int s) {  // dP^T = V dO^T
                 const uint64_t d_do = sdesc_sw128(st_addr(s) + kTileBytes, 16, 1024);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     mma_ss(tmem + kColDP, sdesc_advance(d_v, 32 * k), sdesc_advance(d_do, 32 * k), id_s, k > 0);
-                mma_commit(&bars.dp_full);
+                mma_commit(&bars.sdp_full);   // S^T (issued just before) and dP^T
             };
             while (ok) {
                 if (!(ok = mbar_wait(&bars.item_full[slot], (ring_full_bits >> slot) & 1u, abort, status,
@@ -379,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         const int j = quarter * 32 + lane;                   // key row of the block = TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         uint32_t ring_full_bits = 0, st_full_bits = 0;
-        uint32_t s_full_ph = 0, dp_full_ph = 0, tile_done_ph = 0;
+        uint32_t sdp_full_ph = 0, tile_done_ph = 0;
         bool pending = false;   // a tile_done commit is outstanding for the last tile we handed over
         int slot = 0, stage = 0;
         bool ok = true;
@@ -452,8 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 const float* vec =
                     reinterpret_cast<const float*>(sm + Smem::st + stage * Smem::st_bytes + Smem::st_vec);
                 if (!it.frozen) {
-                    if (!(ok = mbar_wait(&bars.s_full, s_full_ph, abort, status, kStatusTimeout))) break;
-                    s_full_ph ^= 1;
+                    if (!(ok = mbar_wait(&bars.sdp_full, sdp_full_ph, abort, status, kStatusTimeout))) break;
+                    sdp_full_ph ^= 1;
                     tc_fence_after();
                     // P^T first: S^T row (64 columns) -> P (bf16 pairs); then dP^T row -> dS.
                     uint32_t pk[32];
@@ -489,9 +486,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                     // the previous tile's MMAs are done: its dQ (same item) goes out first,
                     // then P^T and dS of this tile overwrite the previous ones
                     if (!(ok = wait_tile_done())) break;
-                    if (!(ok = mbar_wait(&bars.dp_full, dp_full_ph, abort, status, kStatusTimeout))) break;
-                    dp_full_ph ^= 1;
-                    tc_fence_after();
                     uint32_t dp[64];
                     tmem_ld32(lane_base + kColDP + 64 * half, dp);
                     tmem_ld32(lane_base + kColDP + 64 * half + 32, dp + 32);
