@@ -139,7 +139,8 @@ struct Barriers {
     uint64_t s_consumed;    // pattern warps have read S^T (8 arrivals)
     uint64_t dp_consumed;   // pattern warps have read dP^T (8 arrivals)
     uint64_t p_ready;       // P^T in TMEM and dS in shared memory (8 warp arrivals)
-    uint64_t tile_done;     // every MMA of the previous tile has completed
+    // (a tile's MMAs have all completed when the st_empty commit of its stage arrives: the
+    // pattern warps wait on that barrier too)
     uint64_t dq_free;       // dQ of the previous tile has been read out (8 arrivals)
     uint64_t dkv_free;      // dV, dK of the previous item have been read out (8 arrivals)
 };
@@ -171,7 +172,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         mbar_init(&bars.s_consumed, 8);
         mbar_init(&bars.dp_consumed, 8);
         mbar_init(&bars.p_ready, 8);
-        mbar_init(&bars.tile_done, 1);
         mbar_init(&bars.dq_free, 8);
         mbar_init(&bars.dkv_free, 8);
         fence_mbar_init();
@@ -362,7 +362,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                             mma_ss(tmem + kColDQ, sdesc_advance(d_dsmn, 2048 * k), sdesc_advance(d_kmn, 2048 * k), id_dq,
                                    k > 0);
                     }
-                    mma_commit(&bars.tile_done);
                     mma_commit(&bars.st_empty[s]);
                     stage = s_next;
                 }
@@ -376,8 +375,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         const int j = quarter * 32 + lane;                   // key row of the block = TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         uint32_t ring_full_bits = 0, st_full_bits = 0;
-        uint32_t sdp_full_ph = 0, tile_done_ph = 0;
-        bool pending = false;   // a tile_done commit is outstanding for the last tile we handed over
+        uint32_t sdp_full_ph = 0;
+        uint32_t done_bits = 0;   // per stage: parity of the st_empty phase that ends its next tile
+        int pending = -1;         // stage of the last tile handed over whose MMAs were not waited for
         int slot = 0, stage = 0;
         bool ok = true;
         uint8_t* dsp = sm + Smem::ds + half * 16384;          // my 64-query half of dS (MN-major atom)
@@ -387,10 +387,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         // The previous tile's MMAs have all completed: P^T, dS may be overwritten
         // and its dQ (ordinary tiles) can be read out.
         auto wait_tile_done = [&]() -> bool {
-            if (!pending) return true;
-            if (!mbar_wait(&bars.tile_done, tile_done_ph, abort, status, kStatusTimeout)) return false;
-            tile_done_ph ^= 1;
-            pending = false;
+            if (pending < 0) return true;
+            if (!mbar_wait(&bars.st_empty[pending], (done_bits >> pending) & 1u, abort, status, kStatusTimeout))
+                return false;
+            done_bits ^= 1u << pending;
+            pending = -1;
             tc_fence_after();
             return true;
         };
@@ -573,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars.p_ready);
                 if (!it.frozen && i > 0) drain_dq(bh, qb - 1);
-                pending = true;
+                pending = stage;
                 stage = (stage + 1) % kStages;
             }
             if (!ok) break;
