@@ -86,9 +86,13 @@ struct Smem {
     static constexpr int st = kv + kv_bytes;          // kStages x (Q, dO, row vectors)
     static constexpr int st_vec = 2 * kTileBytes;     // offset of the 512 fp32 row vectors in a stage
     static constexpr int st_bytes = 2 * kTileBytes + 3 * 1024;   // 1024-aligned
-    static constexpr int ds = st + kStages * st_bytes;            // dS, 128 x 128 bf16
-    static constexpr int dqs = ds + 2 * kTileBytes;               // dQ staging, 2 halves x (128 x 32 fp32)
-    static constexpr int total = dqs + 2 * 16384;
+    // Two 32 KB buffers R[0], R[1]: ordinary tile t writes its dS (128 x 128 bf16) into
+    // R[t & 1]; once the tile's MMAs are done the same buffer stages its dQ for the bulk
+    // reduce (2 halves x 128 x 32 fp32), and tile t + 2's dS goes there after that reduce
+    // has read it. So dS can be stored before the previous tile's MMAs have finished.
+    static constexpr int ds = st + kStages * st_bytes;
+    static constexpr int ds_bytes = 2 * kTileBytes;
+    static constexpr int total = ds + 2 * ds_bytes;
 };
 
 struct Item {
@@ -262,15 +266,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             uint32_t s_consumed_ph = 0, dp_consumed_ph = 0, p_ready_ph = 0, dq_free_ph = 1, dkv_free_ph = 1;
             int slot = 0, stage = 0;
             bool ok = true;
-            const uint32_t sds = smem_u32(sm + Smem::ds);
+            int gto = 0;   // ordinary tiles so far: dS buffer gto & 1
             const uint32_t skv = smem_u32(sm + Smem::kv);
             // descriptors of the fixed operands; per-stage ones are formed once per tile and
             // every K step advances a descriptor by a constant
             const uint64_t d_k = sdesc_sw128(skv, 16, 1024);                  // K, K-major (S^T)
             const uint64_t d_v = sdesc_sw128(skv + kTileBytes, 16, 1024);     // V, K-major (dP^T)
             const uint64_t d_kmn = sdesc_sw128(skv, 16384, 1024);             // K, MN-major (dQ)
-            const uint64_t d_ds = sdesc_sw128(sds, 16, 1024);                 // dS, K-major view (dK)
-            const uint64_t d_dsmn = sdesc_sw128(sds, 16384, 1024);            // dS, MN-major view (dQ)
+
             auto st_addr = [&](int s) { return smem_u32(sm + Smem::st + s * Smem::st_bytes); };
             auto wait_st = [&](int s) -> bool {
                 if (!mbar_wait(&bars.st_full[s], (st_full_bits >> s) & 1u, abort, status, kStatusTimeout))
@@ -347,6 +350,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                         mma_ts(tmem + kColDV, tmem + kColP + 8 * k, sdesc_advance(d_domn, 2048 * k), id_dv,
                                (i > 0 || k > 0) ? 1u : 0u);
                     if (!it.frozen) {
+                        const uint32_t sds = smem_u32(sm + Smem::ds + (gto++ & 1) * Smem::ds_bytes);
+                        const uint64_t d_ds = sdesc_sw128(sds, 16, 1024);       // dS, K-major view (dK)
+                        const uint64_t d_dsmn = sdesc_sw128(sds, 16384, 1024);  // dS, MN-major view (dQ)
                         // dK += dS^T Q: dS viewed K-major (keys x queries, two 64-query halves)
 #pragma unroll
                         for (int k = 0; k < 8; ++k)
@@ -380,8 +386,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         int pending = -1;         // stage of the last tile handed over whose MMAs were not waited for
         int slot = 0, stage = 0;
         bool ok = true;
-        uint8_t* dsp = sm + Smem::ds + half * 16384;          // my 64-query half of dS (MN-major atom)
-        uint8_t* dqs = sm + Smem::dqs + half * 16384;         // staging of my 32 dQ columns (SW128 rows)
+        int gto = 0;   // ordinary tiles so far: dS buffer gto & 1
+        // my half of buffer b: 64 queries of dS (MN-major atom), or 32 columns of dQ staging
+        auto dsbuf = [&](int b) { return sm + Smem::ds + b * Smem::ds_bytes + half * 16384; };
         const bool dq_issuer = quarter == 0 && lane == 0;     // issues the bulk reduce of this half
 
         // The previous tile's MMAs have all completed: P^T, dS may be overwritten
@@ -397,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         };
         // Drain dQ of tile (bh, qb) into the fp32 accumulator with a bulk tensor
         // reduce-add: rows 32*quarter + lane, d-columns 32*half .. +31.
-        auto drain_dq = [&](int bh, int qb) {
+        auto drain_dq = [&](int bh, int qb, uint8_t* dqs) {
             uint32_t v[32];
             tmem_ld32(lane_base + kColDQ + 32 * half, v);
             tmem_ld_wait();
@@ -484,9 +491,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                             }
                         }
                     }
-                    // the previous tile's MMAs are done: its dQ (same item) goes out first,
-                    // then P^T and dS of this tile overwrite the previous ones
-                    if (!(ok = wait_tile_done())) break;
                     uint32_t dp[64];
                     tmem_ld32(lane_base + kColDP + 64 * half, dp);
                     tmem_ld32(lane_base + kColDP + 64 * half + 32, dp + 32);
@@ -494,7 +498,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars.dp_consumed);   // dP^T of the next tile may land
-                    tmem_st32(lane_base + kColP + 32 * half, pk);
+                    // dS goes to buffer gto & 1 while the previous tile's MMAs may still run: that
+                    // buffer last staged the dQ of tile gto - 2, whose reduce must have read it
+                    uint8_t* dsp = dsbuf(gto & 1);
+                    if (dq_issuer) bulk_wait_read_all();
+                    named_bar_sync(1 + half, 128);
                     const float4* dvec4 = reinterpret_cast<const float4*>(vec + 128 + 64 * half);
 #pragma unroll
                     for (int g2 = 0; g2 < 2; ++g2) {
@@ -520,6 +528,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                             *reinterpret_cast<uint4*>(dsp + sw128_offset(j, 16 * (4 * g2 + t))) =
                                 make_uint4(dk[4 * t], dk[4 * t + 1], dk[4 * t + 2], dk[4 * t + 3]);
                     }
+                    // the previous tile's MMAs are done: P^T of this tile overwrites the previous one
+                    if (!(ok = wait_tile_done())) break;
+                    tmem_st32(lane_base + kColP + 32 * half, pk);
+                    ++gto;
                 } else {
                     // W^T(j, q) = W(q, j) (Eq. 3); band[q] is r at offset q - j = (qb - kb) * 128 +
                     // q - j. Factorised: W(q, j) / exp(a[j] - A) = exp(r[q-j] - R) / Z'(q), no exp per
@@ -573,14 +585,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars.p_ready);
-                if (!it.frozen && i > 0) drain_dq(bh, qb - 1);
+                // dQ of the previous tile, staged in the buffer that held its dS
+                if (!it.frozen && i > 0) drain_dq(bh, qb - 1, dsbuf(gto & 1));
                 pending = stage;
                 stage = (stage + 1) % kStages;
             }
             if (!ok) break;
             // all MMAs of this item done: the last dQ, then the dV and dK rows (my 32 d-columns)
             if (!(ok = wait_tile_done())) break;
-            if (!it.frozen) drain_dq(bh, nqb - 1);
+            if (!it.frozen) drain_dq(bh, nqb - 1, dsbuf((gto - 1) & 1));
             uint32_t dv[32], dk[32];
             tmem_ld32(lane_base + kColDV + 32 * half, dv);
             if (!it.frozen) tmem_ld32(lane_base + kColDK + 32 * half, dk);
