@@ -159,6 +159,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
 
+    // the preparation kernels before this one on the stream have completed
+    grid_dep_wait();
+    grid_dep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -643,6 +646,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
 // Grid (ceil(T * 8 / 256), B*H); one thread per 8 elements of a slice.
 __global__ void __launch_bounds__(256) dq_finish_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq,
                                                         HeadMask mask, int H, int T) {
+    grid_dep_wait();   // the backward kernel has completed
+    grid_dep_launch();
     const long long per_bh8 = (long long)T * 8;
     const long long i8 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i8 >= per_bh8) return;
@@ -700,11 +705,8 @@ cudaError_t launch_tc_bwd(const LayerArgs& a, cudaStream_t s) {
     p.n_ord_items = a.B * p.n_ord * p.nqb;
     p.n_items = a.B * a.H * p.nqb;
 
+    // (the dQ accumulator of the ordinary heads was zeroed by bwd_prep_kernel)
     cudaError_t e;
-    if (p.n_ord > 0) {
-        e = cudaMemsetAsync(a.dq_acc, 0, (size_t)BH * a.T * 64 * sizeof(float), s);
-        if (e != cudaSuccess) return e;
-    }
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -713,15 +715,15 @@ cudaError_t launch_tc_bwd(const LayerArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const int grid = p.n_items < sms ? p.n_items : sms;
     before_launch(SAF_KERNEL_BWD, s);
-    bwd_tc_kernel<<<grid, kThreads, smem, s>>>(p);
+    e = launch_ex(bwd_tc_kernel, dim3(grid), dim3(kThreads), smem, s, true, 1, p);
     after_launch(SAF_KERNEL_BWD, s);
-    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     dim3 g2((unsigned)(((long long)a.T * 8 + 255) / 256), BH);
     before_launch(SAF_KERNEL_DQ_FINISH, s);
-    dq_finish_kernel<<<g2, 256, 0, s>>>(a.dq_acc, (__nv_bfloat16*)a.dq, a.mask, a.H, a.T);
+    e = launch_ex(dq_finish_kernel, g2, dim3(256), 0, s, true, 1, (const float*)a.dq_acc, (__nv_bfloat16*)a.dq,
+                  a.mask, a.H, a.T);
     after_launch(SAF_KERNEL_DQ_FINISH, s);
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace saf

@@ -140,6 +140,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
 
+    // the preparation kernels before this one on the stream have completed
+    grid_dep_wait();
+    grid_dep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -657,8 +660,9 @@ cudaError_t launch_tc_fwd(const LayerArgs& a, cudaStream_t s) {
     if (2 * 128 * kRegsSoftmax + 128 * kRegsOther > kThreads * fa.numRegs) return cudaErrorInvalidConfiguration;
     const int grid = p.n_items < sms ? p.n_items : sms;
     before_launch(SAF_KERNEL_FWD, s);
-    fwd_tc_kernel<<<grid, kThreads, smem, s>>>(p);
+    e = launch_ex(fwd_tc_kernel, dim3(grid), dim3(kThreads), smem, s, true, 1, p);
     after_launch(SAF_KERNEL_FWD, s);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

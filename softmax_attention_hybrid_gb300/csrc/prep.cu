@@ -1,15 +1,16 @@
 // Per-call preparation kernels of the hybrid attention layer.
 //
+//  * call_init: clears the call's status words and flags; per frozen head,
+//    max a and max r, and the padded a, r slices in the exact (log2) and the
+//    factorised form of Eq. 3, so that every tile of the tensor-core kernels
+//    reads its slice with one aligned bulk copy.
 //  * lognorm: the row normalisers log Z(i) of every frozen head
 //    ("When Can Attention Heads Be Statically Defined?", §3.2 Eq. 3; §3.3
 //    "precomputed normalisers"). They do not depend on the batch.
-//  * frozen_prep: per frozen head, a and r in the exact (log2) and the
-//    factorised form of Eq. 3, padded so that every tile of the tensor-core
-//    kernels reads its slice with one aligned bulk copy.
-//  * bwd_delta / bwd_rowvec: D_i = sum_c dO_ic O_ic for the ordinary-head
-//    backward (the softmax Jacobian term of Eqs. 5-7 differentiated; App. D.2),
-//    the latter together with lse * log2(e) in the per-tile layout of the
-//    tensor-core backward.
+//  * bwd_prep / bwd_delta: D_i = sum_c dO_ic O_ic for the ordinary-head
+//    backward (the softmax Jacobian term of Eqs. 5-7 differentiated; App. D.2);
+//    bwd_prep also lays out lse * log2(e) per tile, zeroes the dQ accumulator
+//    and forms 1 / Z' for the tensor-core backward.
 #include <math.h>
 
 #include "saf_internal.h"
@@ -35,12 +36,35 @@ __device__ float block_max(float x, float* red) {
     return x;
 }
 
-// max a and max r of every frozen head (the A and R of the factorised form).
-// Grid (H), 1024 threads.
+// Per frozen head, the slices that the tensor-core kernels read with aligned
+// bulk copies, in two forms of Eq. 3 (A = max a, R = max r):
+//  exact form (log2 domain, -inf padded):
+//    a2p[j] = a[j] log2(e) (j < T),   r2p[u] = r[u - 127] log2(e) (0 <= u - 127 < T)
+//  factorised form, W(i, k) = er[i - k] ea[k] / Z'(i):
+//    eap[j] = exp(a[j] - A) (j < T, else 0),  erp[u] = exp(r[u - 127] - R) (else 0),
+//    invz[i] = 1 / Z'(i) = exp(A + R - log Z(i)) (i < T, else 0).
+// The factorised form is exact up to rounding while every row keeps a term
+// within the normal fp32 range; a head with some log Z(i) - A - R < -64
+// (Z' < 1.6e-28) is flagged (hflag bit 1) and the kernels use the exact form.
+
+// call_init_kernel: the first kernel of every call. Block (0, 0) clears the
+// status words, block (0, h) the flags of head h (later kernels of the call
+// raise them). For a frozen head every block finds max a and max r (the same
+// exact values in every block), block (0, h) stores them, and with pad each
+// block writes its 1024 entries of the padded slices above.
+// Grid (npart, H), 1024 threads; npart = ceil((Tp + 256) / 1024) with pad, else 1.
 __global__ void __launch_bounds__(1024)
-frozen_max_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all, int ld, HeadMask mask, int T,
-                  int H, float* __restrict__ amax) {
-    const int h = blockIdx.x;
+call_init_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all, int ld, HeadMask mask, int T,
+                 int H, int Tp, float* __restrict__ amax, uint32_t* __restrict__ status,
+                 uint32_t* __restrict__ hflag, float* __restrict__ a2p, float* __restrict__ r2p,
+                 float* __restrict__ eap, float* __restrict__ erp) {
+    grid_dep_wait();
+    grid_dep_launch();
+    const int h = blockIdx.y;
+    if (blockIdx.x == 0) {
+        if (h == 0 && threadIdx.x < kStatusBytes / sizeof(uint32_t)) status[threadIdx.x] = 0;
+        if (threadIdx.x == 0) hflag[h] = 0;
+    }
     if (!head_frozen(mask, h)) return;
     const float* a = a_all + (size_t)h * ld;
     const float* r = r_all + (size_t)h * ld;
@@ -65,10 +89,42 @@ frozen_max_kernel(const float* __restrict__ a_all, const float* __restrict__ r_a
     }
     const float A = block_max(ma, red);
     const float R = block_max(mr, red);
-    if (threadIdx.x == 0) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
         amax[h] = A;
         amax[H + h] = R;
     }
+    if (!eap) return;
+    const int u = blockIdx.x * 1024 + threadIdx.x;
+    if (u >= Tp + 256) return;
+    const size_t ra = (size_t)h * Tp, rr = (size_t)h * (Tp + 256);
+    const int dl = u - 127;
+    const bool in = dl >= 0 && dl < T;
+    r2p[rr + u] = in ? r[dl] * kLog2e : -INFINITY;
+    erp[rr + u] = in ? expf(r[dl] - R) : 0.f;
+    if (u < Tp) {
+        a2p[ra + u] = u < T ? a[u] * kLog2e : -INFINITY;
+        eap[ra + u] = u < T ? expf(a[u] - A) : 0.f;
+    }
+}
+
+// Thread-block cluster primitives (PTX): rank of this CTA in its cluster, a
+// barrier over the cluster's CTAs (release / acquire: shared-memory writes
+// before it are visible to every CTA of the cluster after it), and a load
+// from another CTA's shared memory.
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_barrier() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_cluster_f32(const float* p, uint32_t rank) {
+    uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(p)), remote;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
 }
 
 // Eq. 3 factorises: exp(a[j] + r[i-j]) = e^{A+R} * ea[j] * er[i-j] with
@@ -79,25 +135,29 @@ frozen_max_kernel(const float* __restrict__ a_all, const float* __restrict__ r_a
 // left the normal fp32 range; that row is recomputed exactly by a running
 // log-sum-exp and the head is flagged (kStatusRange, informational).
 //
-// lognorm_kernel: one CTA per (frozen head, 128-row tile), numbered so that
-// the tiles with the most keys come first: the block scheduler then hands the
-// long tiles out early and fills in with short ones. 256 threads. Thread
-// (warp w, lane l) sums rows i0 = 128 t + 8 (l % 16) .. +7 over key run
-// 2 w + l / 16 of each chunk (16 runs of kLnRun keys), eight keys per step: the
-// 15 er values that a step's 8 x 8 products need slide along the band in
-// registers, so a step costs 8 er and 8 ea shared loads for 64 FMAs. The er
-// staging is padded (one word every 8): a half-warp's rows, 8 apart, and the two
-// half-warps' runs, kLnRun apart, then fall on 32 distinct banks. The 16 runs
-// meet in shared memory and are added in a fixed order, so the result does not
-// depend on scheduling; a row whose sum underflows is recomputed by a running
-// log-sum-exp in the exact domain and its head is flagged.
-// kPre: ea and er come precomputed (eap, erp of the tensor-core path) and are
-// copied into shared memory asynchronously, the next chunk while the current
-// one is summed; otherwise every chunk stages exp(a - A), exp(r - R) itself.
+// lognorm_kernel: one cluster of S CTAs (S = 1..4) per (frozen head, 128-row
+// tile), numbered so that the tiles with the most keys come first. The keys
+// 0 .. imax of a tile are cut into chunks of kLnChunk; CTA s of the cluster
+// sums chunks s, s + S, ... and the S partial sums meet in CTA 0's registers
+// through distributed shared memory, added in rank order, so the result does
+// not depend on scheduling. 256 threads: thread (warp w, lane l) sums rows
+// i0 = 128 t + 8 (l % 16) .. +7 over key run 2 w + l / 16 of each chunk (16
+// runs of kLnRun keys), eight keys per step. A step's 8 x 8 products need 15
+// er values: the 8 of the step's own aligned group and 7 of the group the
+// previous step loaded, so each step loads one group of 8 er and 8 ea (four
+// 16-byte shared loads) for 64 FMAs, and the two register groups swap roles
+// from step to step. The er staging puts four padding words after every group
+// of 8: the 16-byte loads of the 8 lanes of a quarter-warp (rows 8 apart, so
+// groups 1 apart, 12 words) then cover all 32 banks once.
+// kPre (tensor-core path): ea and er come from the padded eap, erp slices of
+// call_init_kernel, copied into shared memory asynchronously (the next chunk
+// while the current one is summed), and CTA 0 also writes 1 / Z' and the
+// exact-form flag. Otherwise every chunk stages exp(a - A), exp(r - R) itself.
 constexpr int kLnRows = 128, kLnThreads = 256, kLnRuns = 16, kLnRun = 128, kLnChunk = kLnRuns * kLnRun;
-constexpr int kLnBand = kLnChunk + kLnRows;   // er offsets a chunk needs
-constexpr int kLnBandPad = kLnBand + kLnBand / 8 + 8;
-__device__ __forceinline__ int lz_pad(int x) { return x + (x >> 3); }
+constexpr int kLnBand = kLnChunk + kLnRows;   // er offsets a chunk needs (272 groups of 8)
+constexpr int kLnBandPad = kLnBand / 8 * 12;
+constexpr int kLnSplitMax = 4;
+__device__ __forceinline__ int lz_pad(int x) { return x + 4 * (x >> 3); }
 
 __device__ __forceinline__ uint32_t shared_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -105,35 +165,54 @@ __device__ __forceinline__ uint32_t shared_addr(const void* p) {
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(shared_addr(dst)), "l"(src) : "memory");
 }
-__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(shared_addr(dst)), "l"(src) : "memory");
-}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// z[rr] += sum_m ev[m] * er[i0 + rr - (j + m)]: W[t] = er of staging index x + t,
+// lo = W[0..7], hi = W[8..15] (W[15] unused), row rr and key j + m use W[rr - m + 7]
+__device__ __forceinline__ void ln_step(float (&z)[8], const float* ep, const float4& l0, const float4& l1,
+                                        const float4& h0, const float4& h1) {
+    const float4 e0 = *reinterpret_cast<const float4*>(ep);
+    const float4 e1 = *reinterpret_cast<const float4*>(ep + 4);
+    const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+    const float W[16] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w,
+                         h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr) z[rr] = fmaf(ev[m], W[rr - m + 7], z[rr]);
+}
 
 template <bool kPre>
 __global__ void __launch_bounds__(kLnThreads)
 lognorm_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all, int ld, HeadMask mask, int T, int H,
                int F, int nrt, int Tp, const float* __restrict__ eap, const float* __restrict__ erp,
-               const float* __restrict__ amax, float* __restrict__ lz, uint32_t* __restrict__ hflag,
-               uint32_t* __restrict__ status) {
-    // unit u: row tile nrt - 1 - u / F (longest first), f-th frozen head
-    const int u = blockIdx.x;
+               const float* __restrict__ amax, float* __restrict__ lz, float* __restrict__ invz,
+               uint32_t* __restrict__ hflag, uint32_t* __restrict__ status) {
+    grid_dep_wait();
+    grid_dep_launch();
+    // cluster u: row tile nrt - 1 - u / F (longest first), f-th frozen head
+    const int S = (int)(gridDim.x / (unsigned)(nrt * F));
+    const int rank = (int)cluster_rank();
+    const int u = blockIdx.x / S;
     const int rt = nrt - 1 - u / F;
     const int f = u - (u / F) * F;
     int h = 0;
     for (int c = -1; h < H; ++h)
         if (head_frozen(mask, h) && ++c == f) break;
-    if (h >= H) return;
-    const float* a = a_all + (size_t)h * ld;
-    const float* r = r_all + (size_t)h * ld;
+    const bool valid = h < H;   // always, for a mask with F frozen heads
+    const float* a = a_all + (size_t)(valid ? h : 0) * ld;
+    const float* r = r_all + (size_t)(valid ? h : 0) * ld;
     __shared__ __align__(16) float ea_s[2][kLnChunk];
-    __shared__ float er_s[2][kLnBandPad];
-    __shared__ float part[kLnRuns][kLnRows];
-    const float A = amax[h], R = amax[H + h];
+    __shared__ __align__(16) float er_s[2][kLnBandPad];
+    __shared__ float tot[kLnRows];
+    // the runs' partial sums reuse the first ea buffer once every chunk is summed
+    static_assert(kLnRuns * kLnRows <= kLnChunk, "partial sums must fit an ea buffer");
+    float(*part)[kLnRows] = reinterpret_cast<float(*)[kLnRows]>(&ea_s[0][0]);
+    const float A = valid ? amax[h] : 0.f, R = valid ? amax[H + h] : 0.f;
     const int I0 = rt * kLnRows;
     const int imax = min(I0 + kLnRows, T) - 1;
-    const int nch = imax / kLnChunk + 1;   // chunks of keys 0 .. imax
+    const int nch = valid ? imax / kLnChunk + 1 : 0;   // chunks of keys 0 .. imax
     // er_s[b][pad(x)] = er at offset base(c) + x, base(c) = I0 - j0 - kLnChunk + 1 (0 outside [0, T));
     // ea_s[b][t] = ea of key j0 + t (keys past imax meet only zero er: their value is not used)
     auto stage = [&](int c, int b) {
@@ -141,19 +220,23 @@ lognorm_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all,
         const int base = I0 - j0 - kLnChunk + 1;
         if (kPre) {
             const float* eah = eap + (size_t)h * Tp;
-            const float* erh = erp + (size_t)h * (Tp + 256) + 127;   // erh[d], d in [-127, Tp + 129)
+            // erh[d] = er at offset d for d in [-127, Tp + 129); base + 4 q + 127 is a
+            // multiple of 4, so every 4-entry group is 16-byte aligned and lies wholly
+            // inside or wholly outside the padded row
+            const float* erh = erp + (size_t)h * (Tp + 256) + 127;
             for (int q = threadIdx.x; q < kLnChunk / 4; q += kLnThreads) {
                 if (j0 + 4 * q < Tp)
                     cp_async16(&ea_s[b][4 * q], eah + j0 + 4 * q);
                 else
                     *reinterpret_cast<float4*>(&ea_s[b][4 * q]) = make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            for (int t = threadIdx.x; t < kLnBand; t += kLnThreads) {
-                const int dl = base + t;
+            for (int q = threadIdx.x; q < kLnBand / 4; q += kLnThreads) {
+                const int dl = base + 4 * q;
+                float* dst = &er_s[b][lz_pad(4 * q)];
                 if (dl >= -127 && dl < Tp + 129)
-                    cp_async4(&er_s[b][lz_pad(t)], erh + dl);
+                    cp_async16(dst, erh + dl);
                 else
-                    er_s[b][lz_pad(t)] = 0.f;
+                    *reinterpret_cast<float4*>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         } else {
             for (int t = threadIdx.x; t < kLnBand; t += kLnThreads) {
@@ -167,11 +250,10 @@ lognorm_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all,
     const int run = 2 * warp + (lane >> 4);
     const int i0 = I0 + 8 * (lane & 15);   // my 8 rows
     float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    stage(0, 0);
+    if (rank < nch) stage(rank, 0);
     cp_async_commit();
-    for (int c = 0; c < nch; ++c) {
-        const int b = c & 1;
-        if (c + 1 < nch) stage(c + 1, b ^ 1);
+    for (int c = rank, b = 0; c < nch; c += S, b ^= 1) {
+        if (c + S < nch) stage(c + S, b ^ 1);
         cp_async_commit();       // (an empty group on the last chunk keeps the count)
         cp_async_wait_prev();    // chunk c has landed
         __syncthreads();
@@ -181,117 +263,78 @@ lognorm_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all,
         const float* rb = er_s[b];
         const int js = j0 + run * kLnRun;   // my key run js .. js + kLnRun - 1
         if (js <= i0 + 7 && js <= imax) {
-            // step at key j: W[t] = er[i0 - j - 7 + t], t = 0..14; row r, key j + m uses W[r - m + 7]
-            const int x0 = i0 - js - 7 - base;   // staging index of W[0] at the first step
-            float W[15];
-#pragma unroll
-            for (int t = 0; t < 15; ++t) W[t] = rb[lz_pad(x0 + t)];
+            // step st covers keys js + 8 st .. +7; its window starts at staging index
+            // x0 - 8 st, x0 = i0 - js - 7 - base = 8 (l % 16) - 128 run + 2040 (a multiple
+            // of 8, >= 8 st for every step taken; x0 + 15 < kLnBand)
+            const int g0 = (i0 - js - 7 - base) >> 3;
             const int nsteps = (min(kLnRun, i0 + 8 - js) + 7) >> 3;
-            for (int st = 0; st < nsteps; ++st) {
-                const int jj = js - j0 + 8 * st;
-                const float4 e0 = *reinterpret_cast<const float4*>(eb + jj);
-                const float4 e1 = *reinterpret_cast<const float4*>(eb + jj + 4);
-                const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
-#pragma unroll
-                for (int m = 0; m < 8; ++m)
-#pragma unroll
-                    for (int rr = 0; rr < 8; ++rr) z[rr] = fmaf(ev[m], W[rr - m + 7], z[rr]);
-                // slide the window 8 keys on: W[8..14] = W[0..6], W[0..7] = the next 8 offsets down
-#pragma unroll
-                for (int t = 14; t >= 8; --t) W[t] = W[t - 8];
-                const int xn = x0 - 8 * (st + 1);
-#pragma unroll
-                for (int t = 0; t < 8; ++t) W[t] = (xn + t >= 0) ? rb[lz_pad(xn + t)] : 0.f;
+            const float* ep = eb + (js - j0);
+            auto group = [&](int g, float4& v0, float4& v1) {
+                const float* q = rb + 12 * g;
+                v0 = *reinterpret_cast<const float4*>(q);
+                v1 = *reinterpret_cast<const float4*>(q + 4);
+            };
+            float4 l0, l1, h0, h1;
+            group(g0, l0, l1);
+            group(g0 + 1, h0, h1);
+            for (int st = 0;;) {
+                ln_step(z, ep + 8 * st, l0, l1, h0, h1);
+                if (++st >= nsteps) break;
+                group(g0 - st, h0, h1);
+                ln_step(z, ep + 8 * st, h0, h1, l0, l1);
+                if (++st >= nsteps) break;
+                group(g0 - st, l0, l1);
             }
         }
-        __syncthreads();         // buffer b is free for chunk c + 2
+        __syncthreads();         // buffer b is free for chunk c + 2 S
     }
+    // (every copy has landed: the last group committed in the loop is empty)
 #pragma unroll
     for (int rr = 0; rr < 8; ++rr) part[run][8 * (lane & 15) + rr] = z[rr];
     __syncthreads();
-    if (threadIdx.x >= kLnRows) return;
-    const int i = I0 + threadIdx.x;
-    if (i >= T) return;
-    float zs = 0.f;
+    if (threadIdx.x < kLnRows) {
+        float zs = 0.f;
 #pragma unroll
-    for (int w = 0; w < kLnRuns; ++w) zs += part[w][threadIdx.x];
-    float out;
-    if (zs >= 1e-28f) {
-        out = logf(zs) + A + R;
-    } else {
-        float m = -INFINITY, sacc = 0.f;
-        for (int j = 0; j <= i; ++j) {
-            const float x = a[j] + r[i - j];
-            if (x > m) {
-                sacc = sacc * expf(m - x) + 1.f;
-                m = x;
-            } else {
-                sacc += expf(x - m);
-            }
-        }
-        out = m + logf(sacc);
-        atomicOr(hflag + h, 1u);
-        atomicOr(status, kStatusRange);
+        for (int w = 0; w < kLnRuns; ++w) zs += part[w][threadIdx.x];
+        tot[threadIdx.x] = zs;
     }
-    lz[(size_t)h * T + i] = out;
-}
-
-// Per frozen head, the slices that the tensor-core kernels read with aligned
-// bulk copies, in two forms of Eq. 3:
-//  exact form (log2 domain, -inf padded):
-//    a2p[j] = a[j] log2(e) (j < T),   r2p[u] = r[u - 127] log2(e) (0 <= u - 127 < T)
-//  factorised form, W(i, k) = er[i - k] ea[k] / Z'(i) with A = max a, R = max r:
-//    eap[j] = exp(a[j] - A) (j < T, else 0),  erp[u] = exp(r[u - 127] - R) (else 0),
-//    invz[i] = 1 / Z'(i) = exp(A + R - log Z(i)) (i < T, else 0).
-// The factorised form is exact up to rounding while every row keeps a term
-// within the normal fp32 range; a head with some log Z(i) - A - R < -64
-// (Z' < 1.6e-28) is flagged (hflag bit 1) and the kernels use the exact form.
-// log Z comes from lz_src (row stride lz_stride): the lognorm output in the
-// forward pass, the frozen rows of lse (batch entry 0) in the backward pass.
-// A and R come from frozen_max_kernel. Grid (ceil((Tp + 256) / 512), H), 512
-// threads, one entry each; padded lengths Tp (a, invz) and Tp + 256 (r).
-// kParts: kPrepPad writes a2p, r2p, eap, erp (needs A, R only); kPrepInvz
-// writes invz and the hflag bit (needs log Z).
-constexpr int kPrepPad = 1, kPrepInvz = 2;
-template <int kParts>
-__global__ void __launch_bounds__(512)
-frozen_prep_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all, int ld, HeadMask mask, int T,
-                   int Tp, const float* __restrict__ lz_src, long long lz_stride, float* __restrict__ a2p,
-                   float* __restrict__ r2p, float* __restrict__ eap, float* __restrict__ erp,
-                   float* __restrict__ invz, uint32_t* __restrict__ hflag, const float* __restrict__ amax, int H) {
-    const int h = blockIdx.y;
-    if (!head_frozen(mask, h)) return;
-    const float* a = a_all + (size_t)h * ld;
-    const float* r = r_all + (size_t)h * ld;
-    const float* lz = lz_src + (size_t)h * lz_stride;
-    __shared__ int bad;
-    if (threadIdx.x == 0) bad = 0;
-    __syncthreads();
-    const float A = amax[h], R = amax[H + h];
-    const size_t ra = (size_t)h * Tp, rr = (size_t)h * (Tp + 256);
-    for (int u = blockIdx.x * blockDim.x + threadIdx.x; u < Tp + 256; u += gridDim.x * blockDim.x) {
-        const int dl = u - 127;
-        const bool in = dl >= 0 && dl < T;
-        if (kParts & kPrepPad) {
-            r2p[rr + u] = in ? r[dl] * kLog2e : -INFINITY;
-            erp[rr + u] = in ? expf(r[dl] - R) : 0.f;
+    cluster_barrier();   // every CTA's tot is written
+    const int i = I0 + threadIdx.x;
+    if (rank == 0 && valid && threadIdx.x < kLnRows && i < Tp) {
+        float out = 0.f;
+        if (i < T) {
+            float zs = 0.f;
+            for (int q = 0; q < S; ++q) zs += ld_cluster_f32(&tot[threadIdx.x], (uint32_t)q);
+            if (zs >= 1e-28f) {
+                out = logf(zs) + A + R;
+            } else {
+                float m = -INFINITY, sacc = 0.f;
+                for (int j = 0; j <= i; ++j) {
+                    const float x = a[j] + r[i - j];
+                    if (x > m) {
+                        sacc = sacc * expf(m - x) + 1.f;
+                        m = x;
+                    } else {
+                        sacc += expf(x - m);
+                    }
+                }
+                out = m + logf(sacc);
+                atomicOr(hflag + h, 1u);
+                atomicOr(status, kStatusRange);
+            }
+            lz[(size_t)h * T + i] = out;
         }
-        if (u < Tp && (kParts & kPrepPad)) {
-            a2p[ra + u] = u < T ? a[u] * kLog2e : -INFINITY;
-            eap[ra + u] = u < T ? expf(a[u] - A) : 0.f;
-        }
-        if (u < Tp && (kParts & kPrepInvz)) {
+        if (kPre) {
             float iz = 0.f;
-            if (u < T) {
-                const float sh = lz[u] - A - R;   // log Z'(u)
-                if (!(sh >= -64.f)) bad = 1;
+            if (i < T) {
+                const float sh = out - A - R;   // log Z'(i)
+                if (!(sh >= -64.f)) atomicOr(hflag + h, 2u);
                 iz = expf(fminf(-sh, 80.f));
             }
-            invz[ra + u] = iz;
+            invz[(size_t)h * Tp + i] = iz;
         }
     }
-    __syncthreads();
-    if (threadIdx.x == 0 && bad) atomicOr(hflag + h, 2u);
+    cluster_barrier();   // CTA 0 has read every tot: the other CTAs may exit
 }
 
 // D_i = sum_c dO_ic * O_ic, one warp per row (d = 64: two elements per lane).
@@ -309,88 +352,113 @@ bwd_delta_kernel(const E* __restrict__ o, const E* __restrict__ dO, float* __res
     if (lane == 0) delta[row] = x;
 }
 
-// Per-tile row vectors of the tensor-core backward: for slice bh and query
-// block qb, rowvec[(bh * nqb + qb) * 256 + u] holds lse * log2(e) of query
-// qb*128 + u (u < 128; +inf past T) and, at u + 128, D of that query (0 past
-// T; frozen heads skip the dot product). Four threads per padded row, each
-// reading 32 contiguous bytes of O and dO (a warp reads 1 KB of each);
-// grid (nqb * 128 / 64, B*H), 256 threads.
+// bwd_prep_kernel: the per-call preparation of the tensor-core backward, one
+// launch (after call_init_kernel, which wrote max a, max r and the padded
+// slices of the frozen heads).
+//  * Blocks [0, BH * 2 nqb): 64 query rows of slice bh each. For query block qb,
+//    rowvec[(bh * nqb + qb) * 256 + u] holds lse * log2(e) of query qb*128 + u
+//    (u < 128; +inf past T) and, at u + 128, D of that query (0 past T; frozen
+//    heads skip the dot product). Four threads per padded row, each reading 32
+//    contiguous bytes of O and dO (a warp reads 1 KB of each). For an ordinary
+//    head the block also zeroes the block's rows of the fp32 dQ accumulator
+//    that the backward reduce-adds into.
+//  * Then ceil(Tp / 256) blocks per frozen head: 1 / Z'(i) from log Z(i), read
+//    back from the frozen rows of lse (batch entry 0; identical for every
+//    batch entry), and the exact-form flag (hflag bit 1).
+// 256 threads.
 __global__ void __launch_bounds__(256)
-bwd_rowvec_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dO,
-                  const float* __restrict__ lse, HeadMask mask, int H, int T, int nqb, float* __restrict__ rowvec) {
-    const int bh = blockIdx.y;
-    const int i = blockIdx.x * 64 + (threadIdx.x >> 2);
-    const int part = threadIdx.x & 3;
-    const bool frozen = head_frozen(mask, bh % H);
-    float d = 0.f;
-    if (i < T && !frozen) {
-        const size_t row = (size_t)bh * T + i;
-        const uint4* po = reinterpret_cast<const uint4*>(o + row * kHeadDim) + 2 * part;
-        const uint4* pd = reinterpret_cast<const uint4*>(dO + row * kHeadDim) + 2 * part;
-        const uint4 x0 = __ldg(po), x1 = __ldg(po + 1), y0 = __ldg(pd), y1 = __ldg(pd + 1);
-        const uint32_t xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-        const uint32_t ys[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dO,
+                const float* __restrict__ lse, HeadMask mask, int H, int T, int nqb, int BH,
+                float* __restrict__ rowvec, float* __restrict__ dq_acc, int Tp, const float* __restrict__ amax,
+                float* __restrict__ invz, uint32_t* __restrict__ hflag) {
+    grid_dep_wait();
+    grid_dep_launch();
+    const int per_bh = 2 * nqb;
+    const long long nrv = (long long)BH * per_bh;
+    if ((long long)blockIdx.x < nrv) {
+        const int bh = (int)(blockIdx.x / (unsigned)per_bh);
+        const int bx = (int)(blockIdx.x - (unsigned)(bh * per_bh));
+        const int i = bx * 64 + (threadIdx.x >> 2);
+        const int part = threadIdx.x & 3;
+        const bool frozen = head_frozen(mask, bh % H);
+        float d = 0.f;
+        if (i < T && !frozen) {
+            const size_t row = (size_t)bh * T + i;
+            const uint4* po = reinterpret_cast<const uint4*>(o + row * kHeadDim) + 2 * part;
+            const uint4* pd = reinterpret_cast<const uint4*>(dO + row * kHeadDim) + 2 * part;
+            const uint4 x0 = __ldg(po), x1 = __ldg(po + 1), y0 = __ldg(pd), y1 = __ldg(pd + 1);
+            const uint32_t xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            const uint32_t ys[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            d = fmaf(__uint_as_float(xs[e] << 16), __uint_as_float(ys[e] << 16), d);
-            d = fmaf(__uint_as_float(xs[e] & 0xffff0000u), __uint_as_float(ys[e] & 0xffff0000u), d);
+            for (int e = 0; e < 8; ++e) {
+                d = fmaf(__uint_as_float(xs[e] << 16), __uint_as_float(ys[e] << 16), d);
+                d = fmaf(__uint_as_float(xs[e] & 0xffff0000u), __uint_as_float(ys[e] & 0xffff0000u), d);
+            }
         }
+        d += __shfl_xor_sync(0xffffffffu, d, 1);
+        d += __shfl_xor_sync(0xffffffffu, d, 2);
+        if (part == 0 && i < nqb * 128) {
+            float* v = rowvec + ((size_t)bh * nqb + (i >> 7)) * 256;
+            v[i & 127] = i < T ? lse[(size_t)bh * T + i] * kLog2e : INFINITY;
+            v[128 + (i & 127)] = d;
+        }
+        if (!frozen) {
+            const int rows = min(64, T - bx * 64);
+            float4* acc = reinterpret_cast<float4*>(dq_acc + ((size_t)bh * T + (size_t)bx * 64) * kHeadDim);
+            for (int q = threadIdx.x; q < rows * (kHeadDim / 4); q += 256) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        return;
     }
-    d += __shfl_xor_sync(0xffffffffu, d, 1);
-    d += __shfl_xor_sync(0xffffffffu, d, 2);
-    if (part == 0 && i < nqb * 128) {
-        float* v = rowvec + ((size_t)bh * nqb + (i >> 7)) * 256;
-        v[i & 127] = i < T ? lse[(size_t)bh * T + i] * kLog2e : INFINITY;
-        v[128 + (i & 127)] = d;
+    const int nzb = (Tp + 255) / 256;
+    const int v = (int)((long long)blockIdx.x - nrv);
+    const int f = v / nzb;
+    int h = 0;
+    for (int c = -1; h < H; ++h)
+        if (head_frozen(mask, h) && ++c == f) break;
+    const int u = (v - f * nzb) * 256 + threadIdx.x;
+    if (h >= H || u >= Tp) return;
+    float iz = 0.f;
+    if (u < T) {
+        const float sh = lse[(size_t)h * T + u] - amax[h] - amax[H + h];   // log Z'(u)
+        if (!(sh >= -64.f)) atomicOr(hflag + h, 2u);
+        iz = expf(fminf(-sh, 80.f));
     }
+    invz[(size_t)h * Tp + u] = iz;
 }
 
 }  // namespace
 
-cudaError_t launch_frozen_max(const LayerArgs& p, cudaStream_t s) {
-    frozen_max_kernel<<<p.H, 1024, 0, s>>>(p.a, p.r, p.ld_prior, p.mask, p.T, p.H, p.amax);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_lognorm(const LayerArgs& p, bool pre, cudaStream_t s) {
+static int count_frozen(const LayerArgs& p) {
     int F = 0;
     for (int h = 0; h < p.H; ++h) F += head_frozen(p.mask, h) ? 1 : 0;
+    return F;
+}
+
+cudaError_t launch_call_init(const LayerArgs& p, bool pad, bool pdl, cudaStream_t s) {
+    const int Tp = (p.T + 127) / 128 * 128;
+    const int npart = (pad && count_frozen(p) > 0) ? (Tp + 256 + 1023) / 1024 : 1;
+    note_launch();
+    return launch_ex(call_init_kernel, dim3((unsigned)npart, (unsigned)p.H), dim3(1024), 0, s, pdl, 1, p.a, p.r,
+                     p.ld_prior, p.mask, p.T, p.H, Tp, p.amax, p.status, p.hflag, pad ? p.a2p : nullptr,
+                     pad ? p.r2p : nullptr, pad ? p.eap : nullptr, pad ? p.erp : nullptr);
+}
+
+cudaError_t launch_lognorm(const LayerArgs& p, bool pre, bool pdl, cudaStream_t s) {
+    const int F = count_frozen(p);
     if (F == 0) return cudaSuccess;
     const int Tp = (p.T + 127) / 128 * 128;
     const int nrt = (p.T + kLnRows - 1) / kLnRows;
+    const int nch = (p.T - 1) / kLnChunk + 1;   // chunks of the longest tile
+    const int S = nch < kLnSplitMax ? nch : kLnSplitMax;
+    const dim3 grid((unsigned)(nrt * F * S));
     note_launch();
     if (pre)
-        lognorm_kernel<true><<<(unsigned)(nrt * F), kLnThreads, 0, s>>>(
-            p.a, p.r, p.ld_prior, p.mask, p.T, p.H, F, nrt, Tp, p.eap, p.erp, p.amax, p.lz, p.hflag, p.status);
-    else
-        lognorm_kernel<false><<<(unsigned)(nrt * F), kLnThreads, 0, s>>>(
-            p.a, p.r, p.ld_prior, p.mask, p.T, p.H, F, nrt, Tp, nullptr, nullptr, p.amax, p.lz, p.hflag, p.status);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_frozen_pad(const LayerArgs& p, cudaStream_t s) {
-    const int Tp = (p.T + 127) / 128 * 128;
-    note_launch();
-    const dim3 grid((unsigned)((Tp + 256 + 511) / 512), (unsigned)p.H);
-    frozen_prep_kernel<kPrepPad><<<grid, 512, 0, s>>>(p.a, p.r, p.ld_prior, p.mask, p.T, Tp, nullptr, 0, p.a2p, p.r2p,
-                                                       p.eap, p.erp, p.invz, p.hflag, p.amax, p.H);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_pattern_prep(const LayerArgs& p, const float* lz_src, long long lz_stride, bool pad,
-                                cudaStream_t s) {
-    const int Tp = (p.T + 127) / 128 * 128;
-    before_launch(SAF_KERNEL_PATTERN_PREP, s);
-    const dim3 grid((unsigned)((Tp + 256 + 511) / 512), (unsigned)p.H);
-    if (pad)
-        frozen_prep_kernel<kPrepPad | kPrepInvz><<<grid, 512, 0, s>>>(p.a, p.r, p.ld_prior, p.mask, p.T, Tp, lz_src,
-                                                                      lz_stride, p.a2p, p.r2p, p.eap, p.erp, p.invz,
-                                                                      p.hflag, p.amax, p.H);
-    else
-        frozen_prep_kernel<kPrepInvz><<<grid, 512, 0, s>>>(p.a, p.r, p.ld_prior, p.mask, p.T, Tp, lz_src, lz_stride,
-                                                           p.a2p, p.r2p, p.eap, p.erp, p.invz, p.hflag, p.amax, p.H);
-    after_launch(SAF_KERNEL_PATTERN_PREP, s);
-    return cudaGetLastError();
+        return launch_ex(lognorm_kernel<true>, grid, dim3(kLnThreads), 0, s, pdl, S, p.a, p.r, p.ld_prior, p.mask,
+                         p.T, p.H, F, nrt, Tp, (const float*)p.eap, (const float*)p.erp, (const float*)p.amax,
+                         p.lz, p.invz, p.hflag, p.status);
+    return launch_ex(lognorm_kernel<false>, grid, dim3(kLnThreads), 0, s, pdl, S, p.a, p.r, p.ld_prior, p.mask, p.T,
+                     p.H, F, nrt, Tp, (const float*)nullptr, (const float*)nullptr, (const float*)p.amax, p.lz,
+                     (float*)nullptr, p.hflag, p.status);
 }
 
 cudaError_t launch_bwd_delta(const LayerArgs& p, bool bf16, cudaStream_t s) {
@@ -406,14 +474,17 @@ cudaError_t launch_bwd_delta(const LayerArgs& p, bool bf16, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_rowvec(const LayerArgs& p, cudaStream_t s) {
+cudaError_t launch_bwd_prep(const LayerArgs& p, cudaStream_t s) {
     const int nqb = (p.T + 127) / 128;
-    dim3 grid((unsigned)(nqb * 128 / 64), p.B * p.H);
+    const int Tp = nqb * 128;
+    const int BH = p.B * p.H;
+    const long long blocks = (long long)BH * 2 * nqb + (long long)count_frozen(p) * ((Tp + 255) / 256);
     before_launch(SAF_KERNEL_BWD_DELTA, s);
-    bwd_rowvec_kernel<<<grid, 256, 0, s>>>((const __nv_bfloat16*)p.o, (const __nv_bfloat16*)p.dO, p.lse, p.mask, p.H,
-                                           p.T, nqb, p.rowvec);
+    const cudaError_t e = launch_ex(bwd_prep_kernel, dim3((unsigned)blocks), dim3(256), 0, s, true, 1,
+                                    (const __nv_bfloat16*)p.o, (const __nv_bfloat16*)p.dO, p.lse, p.mask, p.H, p.T,
+                                    nqb, BH, p.rowvec, p.dq_acc, Tp, (const float*)p.amax, p.invz, p.hflag);
     after_launch(SAF_KERNEL_BWD_DELTA, s);
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace saf

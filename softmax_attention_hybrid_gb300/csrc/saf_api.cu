@@ -54,9 +54,13 @@ cudaEvent_t g_trace_stop[kNumKernelIds] = {};
 unsigned long long g_launches = 0;
 }  // namespace
 
+void trace_begin(int kernel, cudaStream_t s) {
+    if (g_trace_start[kernel]) cudaEventRecord(g_trace_start[kernel], s);
+}
+
 void before_launch(int kernel, cudaStream_t s) {
     ++g_launches;
-    if (g_trace_start[kernel]) cudaEventRecord(g_trace_start[kernel], s);
+    trace_begin(kernel, s);
 }
 
 void note_launch() { ++g_launches; }
@@ -157,36 +161,20 @@ int launch_status(cudaError_t e) {
     return SAF_ELAUNCH;
 }
 
-// Clear the error words, work counters and per-head flags; then, for the
-// frozen heads, compute log Z (forward only: the backward reads it from lse)
-// and the padded a, r slices of the tensor-core path.
+// The kernels that run before the main kernel of a pass. The first one
+// (call_init) clears the error words, work counters and per-head flags and,
+// for the frozen heads, finds max a, max r and (tensor-core path) writes the
+// padded a, r slices. The forward then computes log Z (and on the tensor-core
+// path 1 / Z'); the tensor-core backward reads log Z back from lse in its prep
+// kernel (launched by saf_attn_bwd), the fp32 backward recomputes it. The
+// tensor-core path launches every kernel with programmatic dependent launch.
 cudaError_t begin_call(const LayerArgs& p, const Common& c, bool backward, bool bf16, cudaStream_t s) {
-    cudaError_t e = cudaMemsetAsync(p.status, 0, kStatusBytes, s);
-    if (e != cudaSuccess) return e;
-    e = cudaMemsetAsync(p.hflag, 0, (size_t)p.H * sizeof(uint32_t), s);
-    if (e != cudaSuccess) return e;
-    if (c.nfrozen == 0) return cudaSuccess;
-    if (!backward || !bf16) {
-        // max a, max r, then log Z (bracketed together for the trace events); the
-        // tensor-core forward writes the padded exp(a - A), exp(r - R) slices first
-        // and sums those
-        before_launch(SAF_KERNEL_LOGNORM, s);
-        e = launch_frozen_max(p, s);
-        if (e == cudaSuccess && bf16) e = launch_frozen_pad(p, s);
-        if (e == cudaSuccess) e = launch_lognorm(p, bf16, s);
-        after_launch(SAF_KERNEL_LOGNORM, s);
-        if (e != cudaSuccess) return e;
-    } else {
-        before_launch(SAF_KERNEL_PATTERN_PREP, s);
-        e = launch_frozen_max(p, s);
-        after_launch(SAF_KERNEL_PATTERN_PREP, s);
-        if (e != cudaSuccess) return e;
-    }
-    if (!bf16) return cudaSuccess;
-    // log Z per row: the forward computed it above; the backward reads it from
-    // the frozen rows of lse (batch entry 0, identical for every batch entry)
-    if (backward) return launch_pattern_prep(p, p.lse, (long long)p.T, true, s);
-    return launch_pattern_prep(p, p.lz, (long long)p.T, false, s);
+    const int kid = backward ? SAF_KERNEL_PATTERN_PREP : SAF_KERNEL_LOGNORM;
+    trace_begin(kid, s);
+    cudaError_t e = launch_call_init(p, bf16, bf16, s);
+    if (e == cudaSuccess && c.nfrozen > 0 && !(backward && bf16)) e = launch_lognorm(p, bf16, bf16, s);
+    after_launch(kid, s);
+    return e;
 }
 
 }  // namespace
@@ -261,7 +249,7 @@ int saf_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
     const bool bf16 = dt == SAF_BF16;
     cudaError_t e = begin_call(p, c, true, bf16, s);
     if (bf16) {
-        if (e == cudaSuccess) e = launch_bwd_rowvec(p, s);
+        if (e == cudaSuccess) e = launch_bwd_prep(p, s);
         if (e == cudaSuccess) e = launch_tc_bwd(p, s);
     } else {
         if (e == cudaSuccess && c.nfrozen < H) e = launch_bwd_delta(p, false, s);

@@ -29,8 +29,51 @@ __host__ __device__ inline bool head_frozen(const HeadMask& m, int h) {
     return (m.w[h >> 6] >> (h & 63)) & 1ull;
 }
 
+// Programmatic dependent launch. Every kernel of the tensor-core path starts
+// with grid_dep_wait(): it returns once the kernels before it on the stream
+// have completed and their memory is visible (at once when the kernel was
+// launched without the attribute), so a kernel that was scheduled early never
+// touches data that is still being written. Every CTA runs it, early exits
+// included, so that a kernel's completion implies its predecessors'.
+// grid_dep_launch() then lets the next kernel on the stream be scheduled while
+// this one runs; that kernel's own grid_dep_wait() holds it back until this
+// one has completed.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch with cudaLaunchKernelEx: pdl allows programmatic dependent launch
+// after the previous kernel on the stream (the kernel must call
+// grid_dep_wait() first); cluster > 1 groups consecutive CTAs of the x
+// dimension into thread-block clusters of that size.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                      int cluster, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[2];
+    unsigned n = 0;
+    if (pdl) {
+        at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster > 1) {
+        at[n].id = cudaLaunchAttributeClusterDimension;
+        at[n].val.clusterDim.x = (unsigned)cluster;
+        at[n].val.clusterDim.y = 1;
+        at[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = at;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Error word layout at the start of every workspace (256 bytes reserved,
-// cleared at the start of every call).
+// cleared by the first kernel of every call).
 //   status[0]: bitwise OR of kStatus* flags raised by kernels of the last call
 //   status[8]: work-item counter of the tensor-core backward
 //   status[9]: work-item counter of the tensor-core forward
@@ -99,20 +142,25 @@ struct LayerArgs {
 // right before a launch and after_launch(...) right after it; they count
 // the launch and record the trace events of saf_set_trace_events.
 void before_launch(int kernel, cudaStream_t s);
+// the start event only (launches counted separately with note_launch)
+void trace_begin(int kernel, cudaStream_t s);
 // a further launch inside a group bracketed by before_launch / after_launch
 void note_launch();
 void after_launch(int kernel, cudaStream_t s);
 
 // prep.cu
-cudaError_t launch_frozen_max(const LayerArgs& p, cudaStream_t s);   // counted by the caller's before_launch
-// log Z of the frozen heads; pre: from the eap, erp slices written by launch_frozen_pad
-cudaError_t launch_lognorm(const LayerArgs& p, bool pre, cudaStream_t s);   // 1 launch, counted with note_launch
-cudaError_t launch_frozen_pad(const LayerArgs& p, cudaStream_t s);          // 1 launch, counted with note_launch
+// First kernel of every call: clears the status words and per-head flags; for
+// the frozen heads, max a and max r, and with pad (tensor-core path) the
+// padded a, r slices in both forms of Eq. 3. 1 launch, counted.
+cudaError_t launch_call_init(const LayerArgs& p, bool pad, bool pdl, cudaStream_t s);
+// log Z of the frozen heads (and with pre, tensor-core path: from the padded
+// exp slices of launch_call_init, also 1 / Z' and the exact-form flag).
+// 1 launch, counted.
+cudaError_t launch_lognorm(const LayerArgs& p, bool pre, bool pdl, cudaStream_t s);
+// Tensor-core backward prep: per-tile lse and D rows, the zeroed dQ
+// accumulator of ordinary heads, and 1 / Z' of frozen heads from lse.
+cudaError_t launch_bwd_prep(const LayerArgs& p, cudaStream_t s);
 cudaError_t launch_bwd_delta(const LayerArgs& p, bool bf16, cudaStream_t s);
-// 1 / Z' and the exact-form flag from log Z; pad: also the padded a, r slices
-cudaError_t launch_pattern_prep(const LayerArgs& p, const float* lz_src, long long lz_stride, bool pad,
-                                cudaStream_t s);
-cudaError_t launch_bwd_rowvec(const LayerArgs& p, cudaStream_t s);
 
 // fwd_tc.cu: tensor-core forward (bf16)
 cudaError_t launch_tc_fwd(const LayerArgs& p, cudaStream_t s);
