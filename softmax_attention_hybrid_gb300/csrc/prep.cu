@@ -20,20 +20,26 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-__device__ float block_max(float x, float* red) {
-    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+// max over the block of x and of y (red: 64 floats of shared memory)
+__device__ float2 block_max2(float x, float y, float* red) {
+    for (int o = 16; o > 0; o >>= 1) {
+        x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+        y = fmaxf(y, __shfl_xor_sync(0xffffffffu, y, o));
+    }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (lane == 0) red[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-        x = lane < (int)(blockDim.x >> 5) ? red[lane] : -INFINITY;
-        for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-        if (lane == 0) red[0] = x;
+    if (lane == 0) {
+        red[warp] = x;
+        red[32 + warp] = y;
     }
     __syncthreads();
-    x = red[0];
-    __syncthreads();
-    return x;
+    const bool in = lane < (int)(blockDim.x >> 5);
+    x = in ? red[lane] : -INFINITY;
+    y = in ? red[32 + lane] : -INFINITY;
+    for (int o = 16; o > 0; o >>= 1) {
+        x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+        y = fmaxf(y, __shfl_xor_sync(0xffffffffu, y, o));
+    }
+    return make_float2(x, y);
 }
 
 // Per frozen head, the slices that the tensor-core kernels read with aligned
@@ -68,7 +74,7 @@ call_init_kernel(const float* __restrict__ a_all, const float* __restrict__ r_al
     if (!head_frozen(mask, h)) return;
     const float* a = a_all + (size_t)h * ld;
     const float* r = r_all + (size_t)h * ld;
-    __shared__ float red[32];
+    __shared__ float red[64];
     float ma = -INFINITY, mr = -INFINITY;
     // 16 loads of a and 16 of r per thread go out before any is used, so that a
     // row of up to 16 K entries costs one memory latency
@@ -87,8 +93,8 @@ call_init_kernel(const float* __restrict__ a_all, const float* __restrict__ r_al
             mr = fmaxf(mr, vr[k]);
         }
     }
-    const float A = block_max(ma, red);
-    const float R = block_max(mr, red);
+    const float2 m = block_max2(ma, mr, red);
+    const float A = m.x, R = m.y;
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         amax[h] = A;
         amax[H + h] = R;
@@ -135,28 +141,30 @@ __device__ __forceinline__ float ld_cluster_f32(const float* p, uint32_t rank) {
 // left the normal fp32 range; that row is recomputed exactly by a running
 // log-sum-exp and the head is flagged (kStatusRange, informational).
 //
-// lognorm_kernel: one cluster of S CTAs (S = 1..4) per (frozen head, 128-row
-// tile), numbered so that the tiles with the most keys come first. The keys
-// 0 .. imax of a tile are cut into chunks of kLnChunk; CTA s of the cluster
-// sums chunks s, s + S, ... and the S partial sums meet in CTA 0's registers
-// through distributed shared memory, added in rank order, so the result does
+// lognorm_kernel: one cluster of kLnSplit CTAs per (frozen head, 128-row
+// tile), numbered so that the tiles with the most keys come first. A tile's
+// keys 0 .. I0 + 127 form units of 128; CTA s of the cluster takes an even,
+// contiguous share of the units (so the CTAs of a cluster finish together),
+// in chunks of up to 16 units. The partial sums meet in CTA 0 through
+// distributed shared memory and are added in rank order, so the result does
 // not depend on scheduling. 256 threads: thread (warp w, lane l) sums rows
 // i0 = 128 t + 8 (l % 16) .. +7 over key run 2 w + l / 16 of each chunk (16
-// runs of kLnRun keys), eight keys per step. A step's 8 x 8 products need 15
-// er values: the 8 of the step's own aligned group and 7 of the group the
-// previous step loaded, so each step loads one group of 8 er and 8 ea (four
-// 16-byte shared loads) for 64 FMAs, and the two register groups swap roles
-// from step to step. The er staging puts four padding words after every group
-// of 8: the 16-byte loads of the 8 lanes of a quarter-warp (rows 8 apart, so
-// groups 1 apart, 12 words) then cover all 32 banks once.
+// runs of 8 keys per unit in the chunk), eight keys per step. A step's 8 x 8
+// products need 15 er values: the 8 of the step's own aligned group and 7 of
+// the group the previous step loaded, so each step loads one group of 8 er and
+// 8 ea (four 16-byte shared loads) for 64 FMAs, and the two register groups
+// swap roles from step to step. The er staging puts four padding words after
+// every group of 8: the 16-byte loads of the 8 lanes of a quarter-warp (rows 8
+// apart, so groups 1 apart, 12 words) then cover all 32 banks once.
 // kPre (tensor-core path): ea and er come from the padded eap, erp slices of
 // call_init_kernel, copied into shared memory asynchronously (the next chunk
 // while the current one is summed), and CTA 0 also writes 1 / Z' and the
 // exact-form flag. Otherwise every chunk stages exp(a - A), exp(r - R) itself.
-constexpr int kLnRows = 128, kLnThreads = 256, kLnRuns = 16, kLnRun = 128, kLnChunk = kLnRuns * kLnRun;
-constexpr int kLnBand = kLnChunk + kLnRows;   // er offsets a chunk needs (272 groups of 8)
+constexpr int kLnRows = 128, kLnThreads = 256, kLnRuns = 16, kLnUnit = 128, kLnChunkUnits = 16;
+constexpr int kLnChunk = kLnChunkUnits * kLnUnit;   // keys per chunk at most (runs of up to 128)
+constexpr int kLnBand = kLnChunk + kLnRows;         // er offsets a chunk needs at most (272 groups of 8)
 constexpr int kLnBandPad = kLnBand / 8 * 12;
-constexpr int kLnSplitMax = 4;
+constexpr int kLnSplit = 4;
 __device__ __forceinline__ int lz_pad(int x) { return x + 4 * (x >> 3); }
 
 __device__ __forceinline__ uint32_t shared_addr(const void* p) {
@@ -212,25 +220,28 @@ lognorm_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all,
     const float A = valid ? amax[h] : 0.f, R = valid ? amax[H + h] : 0.f;
     const int I0 = rt * kLnRows;
     const int imax = min(I0 + kLnRows, T) - 1;
-    const int nch = valid ? imax / kLnChunk + 1 : 0;   // chunks of keys 0 .. imax
-    // er_s[b][pad(x)] = er at offset base(c) + x, base(c) = I0 - j0 - kLnChunk + 1 (0 outside [0, T));
-    // ea_s[b][t] = ea of key j0 + t (keys past imax meet only zero er: their value is not used)
-    auto stage = [&](int c, int b) {
-        const int j0 = c * kLnChunk;
-        const int base = I0 - j0 - kLnChunk + 1;
+    // the tile's keys 0 .. I0 + 127 in units of kLnUnit keys; this CTA takes units
+    // [ub0, ub1), an even share, in chunks of up to kLnChunk / kLnUnit units
+    const int nu = valid ? rt + 1 : 0;
+    const int ub0 = rank * nu / S, ub1 = (rank + 1) * nu / S;
+    const int nck = (ub1 - ub0 + kLnChunkUnits - 1) / kLnChunkUnits;
+    // chunk k: keys j0 .. j0 + L - 1, L = 128 nuc; runs of 8 nuc keys; er offsets
+    // base .. base + L + 127, base = I0 - j0 - L + 1, at staging index x = offset - base
+    // er_s[b][pad(x)] = er (0 outside [0, T)); ea_s[b][t] = ea of key j0 + t (keys past
+    // imax meet only zero er: their value does not matter)
+    auto stage = [&](int k, int b) {
+        const int ub = ub0 + k * kLnChunkUnits;
+        const int nuc = min(kLnChunkUnits, ub1 - ub);
+        const int j0 = ub * kLnUnit, L = nuc * kLnUnit;
+        const int base = I0 - j0 - L + 1;
         if (kPre) {
             const float* eah = eap + (size_t)h * Tp;
             // erh[d] = er at offset d for d in [-127, Tp + 129); base + 4 q + 127 is a
             // multiple of 4, so every 4-entry group is 16-byte aligned and lies wholly
-            // inside or wholly outside the padded row
+            // inside or wholly outside the padded row (keys j0 + 4 q < I0 + 128 <= Tp)
             const float* erh = erp + (size_t)h * (Tp + 256) + 127;
-            for (int q = threadIdx.x; q < kLnChunk / 4; q += kLnThreads) {
-                if (j0 + 4 * q < Tp)
-                    cp_async16(&ea_s[b][4 * q], eah + j0 + 4 * q);
-                else
-                    *reinterpret_cast<float4*>(&ea_s[b][4 * q]) = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-            for (int q = threadIdx.x; q < kLnBand / 4; q += kLnThreads) {
+            for (int q = threadIdx.x; q < L / 4; q += kLnThreads) cp_async16(&ea_s[b][4 * q], eah + j0 + 4 * q);
+            for (int q = threadIdx.x; q < (L + kLnRows) / 4; q += kLnThreads) {
                 const int dl = base + 4 * q;
                 float* dst = &er_s[b][lz_pad(4 * q)];
                 if (dl >= -127 && dl < Tp + 129)
@@ -239,8 +250,8 @@ lognorm_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all,
                     *reinterpret_cast<float4*>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         } else {
-            for (int t = threadIdx.x; t < kLnBand; t += kLnThreads) {
-                if (t < kLnChunk) ea_s[b][t] = (j0 + t <= imax) ? expf(a[j0 + t] - A) : 0.f;
+            for (int t = threadIdx.x; t < L + kLnRows; t += kLnThreads) {
+                if (t < L) ea_s[b][t] = (j0 + t <= imax) ? expf(a[j0 + t] - A) : 0.f;
                 const int dl = base + t;
                 er_s[b][lz_pad(t)] = (dl >= 0 && dl < T) ? expf(r[dl] - R) : 0.f;
             }
@@ -250,25 +261,27 @@ lognorm_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all,
     const int run = 2 * warp + (lane >> 4);
     const int i0 = I0 + 8 * (lane & 15);   // my 8 rows
     float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (rank < nch) stage(rank, 0);
+    if (nck > 0) stage(0, 0);
     cp_async_commit();
-    for (int c = rank, b = 0; c < nch; c += S, b ^= 1) {
-        if (c + S < nch) stage(c + S, b ^ 1);
+    for (int k = 0, b = 0; k < nck; ++k, b ^= 1) {
+        if (k + 1 < nck) stage(k + 1, b ^ 1);
         cp_async_commit();       // (an empty group on the last chunk keeps the count)
-        cp_async_wait_prev();    // chunk c has landed
+        cp_async_wait_prev();    // chunk k has landed
         __syncthreads();
-        const int j0 = c * kLnChunk;
-        const int base = I0 - j0 - kLnChunk + 1;
+        const int ub = ub0 + k * kLnChunkUnits;
+        const int nuc = min(kLnChunkUnits, ub1 - ub);
+        const int j0 = ub * kLnUnit, L = nuc * kLnUnit, rl = 8 * nuc;   // rl: keys per run
+        const int base = I0 - j0 - L + 1;
         const float* eb = ea_s[b];
         const float* rb = er_s[b];
-        const int js = j0 + run * kLnRun;   // my key run js .. js + kLnRun - 1
+        const int js = j0 + run * rl;   // my key run js .. js + rl - 1
         if (js <= i0 + 7 && js <= imax) {
             // step st covers keys js + 8 st .. +7; its window starts at staging index
-            // x0 - 8 st, x0 = i0 - js - 7 - base = 8 (l % 16) - 128 run + 2040 (a multiple
-            // of 8, >= 8 st for every step taken; x0 + 15 < kLnBand)
+            // x0 - 8 st, x0 = i0 - js - 7 - base = 8 (l % 16) + rl (16 - run) - 8 (a
+            // multiple of 8, >= 8 st for every step taken; x0 + 15 < L + 128)
             const int g0 = (i0 - js - 7 - base) >> 3;
-            const int nsteps = (min(kLnRun, i0 + 8 - js) + 7) >> 3;
-            const float* ep = eb + (js - j0);
+            const int nsteps = (min(rl, i0 + 8 - js) + 7) >> 3;
+            const float* ep = eb + run * rl;
             auto group = [&](int g, float4& v0, float4& v1) {
                 const float* q = rb + 12 * g;
                 v0 = *reinterpret_cast<const float4*>(q);
@@ -286,7 +299,7 @@ lognorm_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all,
                 group(g0 - st, l0, l1);
             }
         }
-        __syncthreads();         // buffer b is free for chunk c + 2 S
+        __syncthreads();         // buffer b is free for chunk k + 2
     }
     // (every copy has landed: the last group committed in the loop is empty)
 #pragma unroll
@@ -448,8 +461,7 @@ cudaError_t launch_lognorm(const LayerArgs& p, bool pre, bool pdl, cudaStream_t 
     if (F == 0) return cudaSuccess;
     const int Tp = (p.T + 127) / 128 * 128;
     const int nrt = (p.T + kLnRows - 1) / kLnRows;
-    const int nch = (p.T - 1) / kLnChunk + 1;   // chunks of the longest tile
-    const int S = nch < kLnSplitMax ? nch : kLnSplitMax;
+    const int S = kLnSplit;
     const dim3 grid((unsigned)(nrt * F * S));
     note_launch();
     if (pre)
