@@ -124,8 +124,8 @@ SAF_API int saf_attn_fwd(const void* q, const void* k, const void* v,
  *    address (cudaGetSymbolAddress, with that device current) and caches
  *    it. Make that first call before any stream capture begins.
  *  - Sharing: every call on a device uses the same array, which keeps the
- *    contents the last call left. Each call clears the parts that must
- *    start at zero before its kernels run. Calls whose work overlaps on the
+ *    contents the last call left. Each call's first kernel clears the parts
+ *    that must start at zero before anything reads them. Calls whose work overlaps on the
  *    GPU (two streams, or two host threads) race on the array: order them
  *    on one stream.
  *  - Device-side status words live in that array and are not reported;
@@ -163,19 +163,21 @@ SAF_API int saf_version(void);
  * Kernel identifiers for saf_set_trace_events. */
 typedef enum {
     SAF_KERNEL_NONE = 0,
-    SAF_KERNEL_LOGNORM = 1,     /* log Z of the frozen heads                    */
+    SAF_KERNEL_LOGNORM = 1,     /* forward: init kernel, log Z of frozen heads  */
     SAF_KERNEL_FWD = 2,         /* fused forward (both kinds of head)           */
-    SAF_KERNEL_BWD_DELTA = 3,   /* D_i = sum_c dO_ic O_ic                       */
+    SAF_KERNEL_BWD_DELTA = 3,   /* D_i = sum_c dO_ic O_ic (bf16: also the row   *
+                                 * vectors, dQ accumulator zeroing and 1 / Z')  */
     SAF_KERNEL_BWD_KV = 4,      /* backward key-block pass (dV, dK)            */
     SAF_KERNEL_BWD_Q = 5,       /* backward query-block pass (dQ)              */
     SAF_KERNEL_BWD = 6,         /* fused backward (dQ, dK, dV in one launch)   */
     SAF_KERNEL_DQ_FINISH = 7,   /* dQ accumulator -> dq (scale, dtype, zeros)  */
-    SAF_KERNEL_PATTERN_PREP = 8 /* padded a, r slices of the frozen heads      */
+    SAF_KERNEL_PATTERN_PREP = 8 /* backward: init kernel (clears the status    *
+                                 * words; maxima and padded a, r slices)        */
 } saf_kernel_t;
 
 /* From the next call on, record `start` (a cudaEvent_t as void*) on the
- * call's stream right before every launch of `kernel`, and `stop` right
- * after it. Each kernel id has its own pair; NULL events switch that id
+ * call's stream right before the launches that `kernel` names, and `stop`
+ * right after them. Each kernel id has its own pair; NULL events switch that id
  * off, SAF_KERNEL_NONE switches every id off. The hook is process-wide and
  * not thread-safe; it is meant for benchmarks. Returns SAF_OK or
  * SAF_EINVAL for an unknown id. */

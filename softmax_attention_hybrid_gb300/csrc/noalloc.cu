@@ -65,8 +65,8 @@ extern "C" int saf_attn_fwd_noalloc(const void* q, const void* k, const void* v,
     void* ws = nullptr;
     const int st = scratch_address(&ws);
     if (st != SAF_OK) return st;
-    // The forward pass clears the status words and per-head flags it uses
-    // (cudaMemsetAsync on `stream`) before its kernels run, so stale contents
+    // The forward pass clears the status words and per-head flags it uses (its
+    // first kernel, on `stream`) before anything reads them, so stale contents
     // left by an earlier call do not leak into this one.
     return saf_attn_fwd(q, k, v, a, r, ld_prior, frozen, B, H, T, d, dt, o, lse, ws, kNoallocScratchBytes, stream);
 }
