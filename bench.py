@@ -47,15 +47,24 @@ def _peaks():
         "fallback"
 
 
-def _src_hash():
+# the sources that decide a kernel's DRAM traffic: its own file, the shared
+# device helpers, and the launch sequence with the kernels around it
+KERNEL_SOURCES = {"bwd": ("bwd_tc.cu", "tc_common.cuh", "saf_internal.h", "prep.cu", "saf_api.cu"),
+                  "fwd": ("fwd_tc.cu", "tc_common.cuh", "saf_internal.h", "prep.cu", "saf_api.cu")}
+
+
+def _src_hash(kernel=None):
+    """Hash of the library sources (all of them, or those of one kernel)."""
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "softmax_attention_hybrid_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    names = KERNEL_SOURCES.get(kernel) if kernel else None
+    for name in sorted(names or os.listdir(csrc)):
         if name.endswith((".cu", ".h", ".cuh")):
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + f.read())
-    with open(os.path.join(ROOT, "include", "saf.h"), "rb") as f:
-        h.update(f.read())
+    if not names:
+        with open(os.path.join(ROOT, "include", "saf.h"), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:12]
 
 
@@ -458,7 +467,7 @@ def run_ours(args, w):
         if os.path.exists(tpath):
             with open(tpath) as f:
                 tt = json.load(f)
-            ent = tt.get(f"{name}|{w.name}|{_src_hash()}")
+            ent = tt.get(f"{name}|{w.name}|{_src_hash(name)}")
             traffic = ent if ent is not None else None
         roofline = {"kernel": name, "bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": achieved / peak, "traffic": traffic, "peak_source": note,
