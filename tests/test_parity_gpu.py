@@ -158,6 +158,38 @@ def test_repeated_calls_are_deterministic(saf):
         assert torch.equal(a[n], b[n]), n
 
 
+def test_back_to_back_calls_on_one_stream(saf):
+    # Forward and backward calls of different shapes and frozen sets, queued on one
+    # stream with one shared workspace and no host synchronisation in between: each
+    # kernel may be scheduled before the one ahead of it has finished (programmatic
+    # dependent launch) and must still see all of its results. Outputs equal those of
+    # the same calls run one at a time (dq up to the order of its fp32 reduce-adds).
+    # A kernel that read data its predecessor was still writing would be far off.
+    cases = [custom_workload(2, 4, 700, frozen=(1, 3), slope=0.02),
+             custom_workload(1, 2, 300, frozen=()),
+             custom_workload(1, 3, 1100, frozen=(0,), slope=0.01),
+             custom_workload(2, 2, 200, frozen=(0, 1))]
+    xs = [make_inputs(w, seed=30 + i) for i, w in enumerate(cases)]
+    serial = [_run(saf, x) for x in xs]
+    dev = torch.device("cuda:0")
+    ws = max((saf.alloc_workspace(w.B, w.H, w.T, 64, torch.bfloat16, True) for w in cases), key=lambda t: t.numel())
+    gs = [{n: x[n].to(dev) for n in ("q", "k", "v", "do", "a", "r")} for x in xs]
+    torch.cuda.synchronize()
+    queued = []
+    for x, g in zip(xs, gs):
+        o, lse = saf.saf_attn_fwd(g["q"], g["k"], g["v"], g["a"], g["r"], x["frozen"], workspace=ws)
+        dq, dk, dv = saf.saf_attn_bwd(g["q"], g["k"], g["v"], o, g["do"], lse, g["a"], g["r"], x["frozen"],
+                                      workspace=ws)
+        queued.append({"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv})
+    torch.cuda.synchronize()
+    assert saf.saf_device_status(ws) == saf.SAF_OK
+    for a, b in zip(serial, queued):
+        for n in ("o", "lse", "dk", "dv"):
+            assert torch.equal(a[n], b[n]), n
+        # (a different summation order can move a bf16 result by one unit in the last place)
+        assert (a["dq"].float() - b["dq"].float()).abs().max().item() <= TOL["bf16"][1]
+
+
 def test_device_status_ok(saf):
     w = custom_workload(1, 2, 100, frozen=(1,))
     x = make_inputs(w, seed=16)
