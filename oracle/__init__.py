@@ -15,4 +15,6 @@ from .saf_oracle import (  # noqa: F401
     head_bwd,
     attn_fwd,
     attn_bwd,
+    pattern_grad,
+    attn_pattern_grad,
 )

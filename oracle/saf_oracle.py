@@ -32,6 +32,13 @@ m_i + log sum_j exp(S_ij - m_i); for frozen rows log Z(i).
 Row blocking: every quantity except dV and dK is local to one query row, so
 the functions below process query rows in blocks to bound memory at large T.
 dV and dK sum over query rows; blocking only changes the order of that sum.
+
+Trainable patterns (App. C.3.2: the trainable variant "computes pattern
+gradients and refreshes the normalisers after each update"): Eq. 3 is a row
+softmax of the logits L(i, j) = alpha(j) + rho(i - j), so the gradient of the
+loss with respect to those logits is the softmax Jacobian applied to
+G = dZ V^T, dL(i, j) = P(i, j) (G(i, j) - D_i) with D_i = sum_j P(i, j) G(i, j),
+and alpha(j) collects column j, rho(delta) the diagonal i - j = delta.
 """
 from __future__ import annotations
 
@@ -185,6 +192,32 @@ def head_bwd(q, k, v, do, a, r, frozen, block=1024):
     return dq, dk, dv
 
 
+def pattern_grad(v, do, a, r, block=1024):
+    """Gradients of the loss with respect to a and r of one frozen head on one
+    sequence, given the output gradient dO (trainable patterns, App. C.3.2).
+
+    With P from Eq. 3, G = dO V^T and D_i = sum_j P_ij G_ij, the logit gradient
+    is dL_ij = P_ij (G_ij - D_i); a[j] appears in every logit of key column j and
+    r[delta] in every logit of the diagonal i - j = delta, so
+        da[j] = sum_{i >= j} dL_ij,   dr[delta] = sum_{i >= delta} dL_{i, i - delta}.
+    Returns (da [T], dr [T]).
+    """
+    v = _as64(v)
+    do = _as64(do)
+    T = v.shape[0]
+    da = np.zeros(T)
+    dr = np.zeros(T)
+    for blk in _blocks(np.arange(T), block):
+        P = frozen_pattern(a, r, T, blk)                    # Eq. 3
+        G = do[blk] @ v.T                                   # dL/dP = dO V^T
+        D = np.sum(P * G, axis=1, keepdims=True)            # D_i = sum_j P_ij G_ij
+        dL = P * (G - D)                                    # row-softmax Jacobian
+        da += np.sum(dL, axis=0)                            # column sums
+        for t, i in enumerate(blk):
+            dr[:i + 1] += dL[t, i::-1]                      # entry (i, j) -> delta = i - j
+    return da, dr
+
+
 # ---------------------------------------------------------------------------
 # Whole layer [B, H, T, d]
 # ---------------------------------------------------------------------------
@@ -239,3 +272,24 @@ def attn_bwd(q, k, v, do, a, r, frozen, threads=1):
 
     _map(one, [(b, h) for b in range(B) for h in range(H)], threads)
     return dq, dk, dv
+
+
+def attn_pattern_grad(v, do, a, r, frozen, threads=1):
+    """Gradients of a and r for every frozen head, summed over the batch (the
+    pattern of a head is shared by all batch entries, §3.2). v, do [B, H, T, d];
+    a, r [H, >= T]. Returns da, dr [H, T] in fp64; rows of ordinary heads are 0.
+    """
+    v = _as64(v)
+    do = _as64(do)
+    B, H, T, d = v.shape
+    a = _as64(a)
+    r = _as64(r)
+    da = np.zeros((H, T))
+    dr = np.zeros((H, T))
+    heads = [h for h in range(H) if frozen[h]]
+    parts = _map(lambda bh: pattern_grad(v[bh[0], bh[1]], do[bh[0], bh[1]], a[bh[1]], r[bh[1]]),
+                 [(b, h) for h in heads for b in range(B)], threads)
+    for (b, h), (ga, gr) in zip([(b, h) for h in heads for b in range(B)], parts):
+        da[h] += ga
+        dr[h] += gr
+    return da, dr

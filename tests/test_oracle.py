@@ -318,6 +318,84 @@ def test_gradient_invariants(frozen):
         assert np.max(np.abs(dk.sum(0))) < 1e-11
 
 
+# ---------------------------------------------------------------------------
+# Trainable patterns (App. C.3.2): gradients of alpha and rho
+# ---------------------------------------------------------------------------
+
+def test_pattern_grad_finite_differences():
+    # central differences of L = sum(O * G) through Eq. 3, with a stored prior
+    # longer than T (only its first T entries may receive gradient)
+    T, d, Tp = 11, 3, 15
+    g = _rng(60)
+    v, G = (g.normal(size=(T, d)) for _ in range(2))
+    a = g.normal(size=Tp)
+    r = -0.1 * np.arange(Tp) + 0.5 * g.normal(size=Tp)
+
+    def loss(aa, rr):
+        o, _ = oracle.head_fwd(None, None, v, aa, rr, True)
+        return float(np.sum(o * G))
+
+    da, dr = oracle.pattern_grad(v, G, a, r)
+    assert da.shape == (T,) and dr.shape == (T,)
+    na = _fd_grad(lambda x: loss(x, r), a)
+    nr = _fd_grad(lambda x: loss(a, x), r)
+    assert not np.any(na[T:]) and not np.any(nr[T:])
+    assert np.max(np.abs(da - na[:T])) / np.max(np.abs(na)) < 1e-6
+    assert np.max(np.abs(dr - nr[:T])) / np.max(np.abs(nr)) < 1e-6
+
+
+def test_pattern_grad_matches_torch_autograd():
+    # an independent construction of Eq. 3 in torch (masked logits, softmax), fp64
+    T, d = 37, 5
+    gen = torch.Generator().manual_seed(7)
+    v, do = (torch.randn(T, d, generator=gen, dtype=torch.float64) for _ in range(2))
+    a = torch.randn(T, generator=gen, dtype=torch.float64).requires_grad_(True)
+    r = (-0.05 * torch.arange(T, dtype=torch.float64)
+         + 0.5 * torch.randn(T, generator=gen, dtype=torch.float64)).requires_grad_(True)
+    i = torch.arange(T)[:, None]
+    j = torch.arange(T)[None, :]
+    L = (a[None, :] + r[(i - j).clamp(min=0)]).masked_fill(j > i, float("-inf"))
+    (torch.softmax(L, dim=-1) @ v).backward(do)
+    da, dr = oracle.pattern_grad(v.numpy(), do.numpy(), a.detach().numpy(), r.detach().numpy())
+    assert np.max(np.abs(da - a.grad.numpy())) < 1e-12
+    assert np.max(np.abs(dr - r.grad.numpy())) < 1e-12
+
+
+def test_pattern_grad_invariants():
+    # adding one constant to every a (or to every r) shifts all logits of every row
+    # alike and leaves Eq. 3 unchanged, so both gradients sum to zero; the first key
+    # only ever meets offsets 0..T-1 and the last offset only the pair (T-1, 0)
+    T, d = 50, 4
+    g = _rng(61)
+    v, do = (g.normal(size=(T, d)) for _ in range(2))
+    a, r, _ = _frozen_case(T=T, seed=62)
+    da, dr = oracle.pattern_grad(v, do, a, r)
+    assert abs(da.sum()) < 1e-10 and abs(dr.sum()) < 1e-10
+    P = oracle.frozen_pattern(a, r, T)
+    G = do @ v.T
+    # dr[T-1] comes from the single entry (i, j) = (T-1, 0) of the softmax Jacobian
+    row = T - 1
+    expect = P[row, 0] * (G[row, 0] - np.dot(P[row], G[row]))
+    assert abs(dr[T - 1] - expect) < 1e-12
+
+
+def test_attn_pattern_grad_sums_over_batch():
+    # the pattern is shared by the batch: a layer's gradient is the sum over batch
+    # entries, and ordinary heads get none
+    B, H, T, d = 3, 3, 20, 4
+    g = _rng(63)
+    v, do = (g.normal(size=(B, H, T, d)) for _ in range(2))
+    a = g.normal(size=(H, T))
+    r = -0.1 * np.arange(T) + 0.3 * g.normal(size=(H, T))
+    frozen = [1, 0, 1]
+    da, dr = oracle.attn_pattern_grad(v, do, a, r, frozen)
+    assert not np.any(da[1]) and not np.any(dr[1])
+    for h in (0, 2):
+        parts = [oracle.pattern_grad(v[b, h], do[b, h], a[h], r[h]) for b in range(B)]
+        assert np.max(np.abs(da[h] - sum(p[0] for p in parts))) < 1e-12
+        assert np.max(np.abs(dr[h] - sum(p[1] for p in parts))) < 1e-12
+
+
 def test_frozen_head_ignores_nan_qk():
     B, H, T, d = 1, 2, 12, 4
     g = _rng(50)

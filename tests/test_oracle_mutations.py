@@ -33,6 +33,12 @@ MUTATIONS = {
     "dK_transposed": ("dk += (dS.T @ q[blk]) * scale", "dk += (dS.T @ k[blk]) * scale"),
     # backward: frozen dV with the pattern untransposed
     "frozen_dV_untransposed": ("dv += P.T @ do[blk]", "dv[:len(blk)] += P[:, :len(blk)] @ do[blk]"),
+    # pattern gradient: softmax Jacobian without the row term D
+    "pattern_no_D": ("dL = P * (G - D)", "dL = P * G"),
+    # pattern gradient: diagonal read the wrong way (delta = j instead of i - j)
+    "pattern_diag_reversed": ("dr[:i + 1] += dL[t, i::-1]", "dr[:i + 1] += dL[t, :i + 1]"),
+    # pattern gradient: dL/dP with V and dO swapped
+    "pattern_G_swapped": ("G = do[blk] @ v.T", "G = v[blk] @ do.T"),
     # lse: forgot the max shift
     "lse_no_max": ("return m + np.log(np.sum(np.exp(L - m[:, None]), axis=1))",
                    "return np.log(np.sum(np.exp(L - m[:, None]), axis=1))"),
