@@ -17,4 +17,13 @@ from .saf_oracle import (  # noqa: F401
     attn_bwd,
     pattern_grad,
     attn_pattern_grad,
+    FIT_STEPS,
+    FIT_LR,
+    FIT_TOL,
+    floor_and_normalise,
+    target_marginals,
+    fit_loss,
+    fit_grad,
+    fit_compact,
+    fit_kl,
 )

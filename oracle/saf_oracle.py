@@ -293,3 +293,83 @@ def attn_pattern_grad(v, do, a, r, frozen, threads=1):
         da[h] += ga
         dr[h] += gr
     return da, dr
+
+
+# ---------------------------------------------------------------------------
+# Compact fitting (§3.2 "Fitting", Eq. 4; App. D.1, Eq. 20; the selection
+# algorithm's fitting steps; settings of App. C.1)
+# ---------------------------------------------------------------------------
+
+FIT_STEPS = 400        # J, Adam steps without early stopping
+FIT_LR = 0.05          # gamma
+FIT_TOL = 0.2          # epsilon_fit, nats per row
+FIT_FLOOR = 1e-9       # floor of causal entries before row normalisation
+
+
+def floor_and_normalise(A):
+    """Target pattern from a measured mean attention matrix: causal entries
+    floored at 1e-9, then every row normalised (the algorithm's step before the
+    marginals). Entries above the diagonal are 0."""
+    A = _as64(A)
+    T = A.shape[0]
+    causal = np.tril(np.ones((T, T), dtype=bool))
+    P = np.where(causal, np.maximum(A, FIT_FLOOR), 0.0)
+    return P / np.sum(P, axis=1, keepdims=True)
+
+
+def target_marginals(P):
+    """eta_abs(j) = sum_{i >= j} P(i, j) and eta_rel(delta) = sum_{i - j = delta} P(i, j)
+    of a causal target P (Eq. 4): its key-column sums and its diagonal sums."""
+    P = np.tril(_as64(P))
+    T = P.shape[0]
+    eta_abs = np.sum(P, axis=0)
+    eta_rel = np.array([np.trace(P, offset=-delta) for delta in range(T)])
+    return eta_abs, eta_rel
+
+
+def fit_loss(a, r, eta_abs, eta_rel):
+    """Eq. 4: (1/T) [sum_i log Z(i) - sum_j eta_abs(j) a(j) - sum_delta eta_rel(delta) r(delta)]."""
+    T = len(eta_abs)
+    a = _as64(a)[:T]
+    r = _as64(r)[:T]
+    return (np.sum(log_normaliser(a, r, T)) - np.dot(eta_abs, a) - np.dot(eta_rel, r)) / T
+
+
+def fit_grad(a, r, eta_abs, eta_rel):
+    """Eq. 20 and its analogue for r: the fitted prior's marginals minus the
+    target's, over T."""
+    T = len(eta_abs)
+    fa, fr = target_marginals(frozen_pattern(a, r, T))
+    return (fa - eta_abs) / T, (fr - eta_rel) / T
+
+
+def fit_compact(eta_abs, eta_rel, steps=FIT_STEPS, lr=FIT_LR, betas=(0.9, 0.999), eps=1e-8):
+    """Fit (a, r) of Eq. 3 to the target marginals: a = 0 and
+    r(delta) = log max(eta_rel(delta) / (T - delta), 1e-9) to start, then `steps`
+    Adam steps (Kingma and Ba, bias-corrected moments) on Eq. 4."""
+    eta_abs = _as64(eta_abs)
+    eta_rel = _as64(eta_rel)
+    T = len(eta_abs)
+    a = np.zeros(T)
+    r = np.log(np.maximum(eta_rel / (T - np.arange(T)), FIT_FLOOR))
+    b1, b2 = betas
+    m = [np.zeros(T), np.zeros(T)]
+    v = [np.zeros(T), np.zeros(T)]
+    for t in range(1, steps + 1):
+        g = fit_grad(a, r, eta_abs, eta_rel)
+        for k, x in enumerate((a, r)):
+            m[k] = b1 * m[k] + (1 - b1) * g[k]
+            v[k] = b2 * v[k] + (1 - b2) * g[k] ** 2
+            mh = m[k] / (1 - b1 ** t)
+            vh = v[k] / (1 - b2 ** t)
+            x -= lr * mh / (np.sqrt(vh) + eps)
+    return a, r
+
+
+def fit_kl(P, a, r):
+    """kappa = (1/T) sum_i KL(P(i, 0..i) || P-hat(i, 0..i)), P-hat from Eq. 3."""
+    P = _as64(P)
+    T = P.shape[0]
+    Ph = frozen_pattern(a, r, T)
+    causal = np.tril(np.ones((T, T), dtype=bool)) & (P > 0)
+    return float(np.sum(P[causal] * (np.log(P[causal]) - np.log(Ph[causal])))) / T

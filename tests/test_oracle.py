@@ -396,6 +396,104 @@ def test_attn_pattern_grad_sums_over_batch():
         assert np.max(np.abs(dr[h] - sum(p[1] for p in parts))) < 1e-12
 
 
+# ---------------------------------------------------------------------------
+# Compact fitting (Eq. 4, Eq. 20, the fitting steps of the selection algorithm)
+# ---------------------------------------------------------------------------
+
+def _family_target(T, seed):
+    g = _rng(seed)
+    a = g.normal(size=T)
+    r = -0.1 * np.arange(T) + 0.5 * g.normal(size=T)
+    return a, r, oracle.frozen_pattern(a, r, T)
+
+
+def test_fit_marginals_bruteforce():
+    T = 7
+    g = _rng(70)
+    P = oracle.floor_and_normalise(g.random((T, T)))
+    ea, er = oracle.target_marginals(P)
+    for j in range(T):
+        assert abs(ea[j] - sum(P[i, j] for i in range(j, T))) < 1e-15
+    for delta in range(T):
+        assert abs(er[delta] - sum(P[i, i - delta] for i in range(delta, T))) < 1e-15
+    # each row is a distribution, so both marginals carry T units of mass
+    assert abs(ea.sum() - T) < 1e-12 and abs(er.sum() - T) < 1e-12
+
+
+def test_floor_and_normalise():
+    A = np.array([[0.0, 5.0, 5.0], [2.0, 0.0, 7.0], [1.0, 1.0, 2.0]])
+    P = oracle.floor_and_normalise(A)
+    assert np.allclose(P.sum(axis=1), 1.0) and not np.any(np.triu(P, 1))
+    assert P[0, 0] == 1.0                       # a floored lone entry becomes the whole row
+    assert abs(P[1, 1] - 1e-9 / (2.0 + 1e-9)) < 1e-24
+    assert np.allclose(P[2], [0.25, 0.25, 0.5])
+
+
+def test_fit_grad_finite_differences():
+    T = 10
+    _, _, P = _family_target(T, 71)
+    ea, er = oracle.target_marginals(P)
+    g = _rng(72)
+    a, r = g.normal(size=T), g.normal(size=T)
+    ga, gr = oracle.fit_grad(a, r, ea, er)
+    na = _fd_grad(lambda x: oracle.fit_loss(x, r, ea, er), a)
+    nr = _fd_grad(lambda x: oracle.fit_loss(a, x, ea, er), r)
+    assert np.max(np.abs(ga - na)) < 1e-8 and np.max(np.abs(gr - nr)) < 1e-8
+
+
+def test_fit_loss_minus_optimum_is_kl():
+    # for a target inside the family of Eq. 3, Eq. 4 is the row-averaged cross
+    # entropy, so its excess over the generating parameters is exactly the kappa KL
+    T = 24
+    a0, r0, P = _family_target(T, 73)
+    ea, er = oracle.target_marginals(P)
+    g = _rng(74)
+    for _ in range(3):
+        a, r = g.normal(size=T), g.normal(size=T)
+        excess = oracle.fit_loss(a, r, ea, er) - oracle.fit_loss(a0, r0, ea, er)
+        assert abs(excess - oracle.fit_kl(P, a, r)) < 1e-12
+    assert abs(oracle.fit_kl(P, a0, r0)) < 1e-14
+
+
+def test_fit_loss_shift_invariant_and_convex():
+    T = 16
+    _, _, P = _family_target(T, 75)
+    ea, er = oracle.target_marginals(P)
+    g = _rng(76)
+    a, r = g.normal(size=T), g.normal(size=T)
+    f = oracle.fit_loss(a, r, ea, er)
+    assert abs(oracle.fit_loss(a + 3.0, r, ea, er) - f) < 1e-12
+    assert abs(oracle.fit_loss(a, r - 2.0, ea, er) - f) < 1e-12
+    a2, r2 = g.normal(size=T), g.normal(size=T)
+    mid = oracle.fit_loss((a + a2) / 2, (r + r2) / 2, ea, er)
+    assert mid <= (f + oracle.fit_loss(a2, r2, ea, er)) / 2 + 1e-12
+
+
+def test_fit_recovers_target_from_the_family():
+    # the paper's settings (400 Adam steps at 0.05 from its initialisation) fit a
+    # target generated by Eq. 3: the marginals match (Eq. 20 at the optimum) and
+    # kappa is far below the 0.2-nat acceptance threshold
+    T = 48
+    _, _, P = _family_target(T, 77)
+    ea, er = oracle.target_marginals(P)
+    a, r = oracle.fit_compact(ea, er)
+    fa, fr = oracle.target_marginals(oracle.frozen_pattern(a, r, T))
+    assert np.max(np.abs(fa - ea)) < 1e-3 and np.max(np.abs(fr - er)) < 1e-3
+    assert oracle.fit_kl(P, a, r) < 1e-6 < oracle.FIT_TOL
+
+
+def test_fit_rejects_a_pattern_outside_the_family():
+    # a target that attends only to key i // 2 cannot be written as Eq. 3 with a
+    # small KL: neither key position nor distance alone decides the weight
+    T = 32
+    A = np.zeros((T, T))
+    A[np.arange(T), np.arange(T) // 2] = 1.0
+    P = oracle.floor_and_normalise(A)
+    ea, er = oracle.target_marginals(P)
+    a, r = oracle.fit_compact(ea, er)
+    assert oracle.fit_kl(P, a, r) > oracle.FIT_TOL
+
+
 def test_frozen_head_ignores_nan_qk():
     B, H, T, d = 1, 2, 12, 4
     g = _rng(50)

@@ -39,6 +39,12 @@ MUTATIONS = {
     "pattern_diag_reversed": ("dr[:i + 1] += dL[t, i::-1]", "dr[:i + 1] += dL[t, :i + 1]"),
     # pattern gradient: dL/dP with V and dO swapped
     "pattern_G_swapped": ("G = do[blk] @ v.T", "G = v[blk] @ do.T"),
+    # fitting: relative marginal from the wrong side of the diagonal
+    "fit_eta_rel_side": ("np.trace(P, offset=-delta)", "np.trace(P, offset=delta)"),
+    # fitting: Eq. 20 without the 1/T
+    "fit_grad_no_T": ("return (fa - eta_abs) / T, (fr - eta_rel) / T", "return (fa - eta_abs), (fr - eta_rel) / T"),
+    # fitting: Eq. 4 with the relative term's sign flipped
+    "fit_loss_sign": ("- np.dot(eta_rel, r)) / T", "+ np.dot(eta_rel, r)) / T"),
     # lse: forgot the max shift
     "lse_no_max": ("return m + np.log(np.sum(np.exp(L - m[:, None]), axis=1))",
                    "return np.log(np.sum(np.exp(L - m[:, None]), axis=1))"),
