@@ -159,6 +159,31 @@ SAF_API const char* saf_error_string(int status);
 /* ABI version of this library (major * 100 + minor). */
 SAF_API int saf_version(void);
 
+/* ---- Compact fitting of a frozen pattern -----------------------------------
+ * Fits a, r of Eq. 3 to a target pattern P, given only P's sufficient
+ * statistics (§3.2 "Fitting", Eq. 4; App. D.1, Eq. 20):
+ *   eta_abs(j)   = sum_{i >= j} P(i, j)          (key-column sums)
+ *   eta_rel(d)   = sum_{i - d >= 0} P(i, i - d)  (diagonal sums)
+ * It starts from a = 0, r(d) = log max(eta_rel(d) / (T - d), 1e-9) and takes
+ * `steps` Adam steps (moment decays 0.9 and 0.999, epsilon 1e-8, bias-corrected)
+ * at learning rate `lr` on
+ *   L(a, r) = (1/T) [sum_i log Z(i) - sum_j eta_abs(j) a(j) - sum_d eta_rel(d) r(d)],
+ * whose gradient is the fitted pattern's marginals minus the target's, over T.
+ * The paper's settings are steps = 400, lr = 0.05 (App. C.1).
+ *
+ * In:  eta_abs, eta_rel: DEVICE fp32 [H, T] (row h: head h); H <= SAF_MAX_HEADS.
+ * Out: a, r: DEVICE fp32 [H, T], the fitted parameters (row stride T, ready to
+ *      pass to saf_attn_fwd with ld_prior = T); loss: DEVICE fp32 [H], L at the
+ *      result. The paper's acceptance statistic kappa (mean KL per row of the
+ *      target from the fit) is loss[h] + (1/T) sum P log P of the target, a
+ *      number the caller has from the target; a fit passes when kappa <= 0.2.
+ * workspace: DEVICE scratch of saf_fit_workspace_bytes(H, T) bytes, 256-byte
+ * aligned. fp32 pointers must be 4-byte aligned. Work is enqueued on `stream`;
+ * errors in the arguments return before any work is enqueued. */
+SAF_API size_t saf_fit_workspace_bytes(int H, int T);
+SAF_API int saf_fit_compact(const float* eta_abs, const float* eta_rel, int H, int T, int steps, float lr,
+                            float* a, float* r, float* loss, void* workspace, size_t ws_bytes, void* stream);
+
 /* ---- Profiling hooks (not part of the layer's arithmetic) ----------------
  * Kernel identifiers for saf_set_trace_events. */
 typedef enum {

@@ -1,0 +1,235 @@
+// Compact fitting of a frozen pattern on the GPU ("When Can Attention Heads Be
+// Statically Defined?", §3.2 "Fitting", Eq. 4; App. D.1, Eq. 20; the fitting
+// steps of the selection algorithm; settings in App. C.1).
+//
+// Given a target's sufficient statistics, the key-column sums eta_abs(j) and
+// the diagonal sums eta_rel(delta), the fitter minimises Eq. 4,
+//     L(a, r) = (1/T) [sum_i log Z(i) - sum_j eta_abs(j) a(j) - sum_d eta_rel(d) r(d)],
+// whose gradient (Eq. 20 and its analogue for r) is the fitted pattern's
+// marginals minus the target's, over T. Every Adam step therefore needs log Z
+// of the current (a, r), which the normaliser kernels of the attention layer
+// compute (call_init_kernel for the maxima, lognorm_kernel for the causal
+// convolution), and the fitted marginals
+//     fa(j) = sum_{i >= j} W(i, j),   fr(d) = sum_{i >= d} W(i, i - d),
+// W(i, j) = exp(a(j) + r(i - j) - log Z(i)) from Eq. 3. Each term is a
+// probability (at most 1), so the sums are formed in the exact exp form.
+#include <math.h>
+#include <string.h>
+
+#include "saf_internal.h"
+
+namespace saf {
+namespace {
+
+constexpr float kFitFloor = 1e-9f;
+
+// a = 0, r(d) = log max(eta_rel(d) / (T - d), 1e-9), Adam moments 0.
+// Grid (ceil(T / 256), H), 256 threads.
+__global__ void __launch_bounds__(256)
+fit_init_kernel(const float* __restrict__ eta_rel, int T, int H, float* __restrict__ a, float* __restrict__ r,
+                float* __restrict__ mom) {
+    const int h = blockIdx.y;
+    const int j = blockIdx.x * 256 + threadIdx.x;
+    if (j >= T) return;
+    const size_t o = (size_t)h * T + j;
+    a[o] = 0.f;
+    r[o] = logf(fmaxf(eta_rel[o] / (float)(T - j), kFitFloor));
+    const size_t n = (size_t)H * T;
+    for (int k = 0; k < 4; ++k) mom[k * n + o] = 0.f;
+}
+
+// out(x) = sum_{i >= x} exp(c(x) + u(i - x) - lz(i)): with (c, u) = (a, r) the
+// key-column marginal fa, with (c, u) = (r, a) the diagonal marginal fr.
+// Grid (ceil(T / 128), H, 2) (z = 0: fa, z = 1: fr), 128 threads: thread t of
+// block x sums output x = 128 bx + t over i in chunks of 128, with lz of the
+// chunk and the 255 values of u the chunk meets staged in shared memory.
+__global__ void __launch_bounds__(128)
+fit_marginals_kernel(const float* __restrict__ a, const float* __restrict__ r, const float* __restrict__ lz, int T,
+                     float* __restrict__ fa, float* __restrict__ fr) {
+    const int h = blockIdx.y;
+    const bool rel = blockIdx.z != 0;
+    const size_t row = (size_t)h * T;
+    const float* c = (rel ? r : a) + row;
+    const float* u = (rel ? a : r) + row;
+    const float* l = lz + row;
+    __shared__ float ls[128];
+    __shared__ float us[256];
+    const int x0 = blockIdx.x * 128;
+    const int x = x0 + threadIdx.x;
+    const float cx = x < T ? c[x] : 0.f;
+    float acc = 0.f;
+    for (int i0 = x0; i0 < T; i0 += 128) {
+        // ls[t] = lz(i0 + t); us[k] = u(i0 - x0 - 127 + k), the offsets i - x of this chunk
+        ls[threadIdx.x] = (i0 + (int)threadIdx.x < T) ? l[i0 + threadIdx.x] : INFINITY;
+        for (int k = threadIdx.x; k < 255; k += 128) {
+            const int d = i0 - x0 - 127 + k;
+            us[k] = (d >= 0 && d < T) ? u[d] : -INFINITY;
+        }
+        __syncthreads();
+        if (x < T) {
+#pragma unroll 4
+            for (int t = 0; t < 128; ++t) {
+                const int i = i0 + t;
+                if (i >= x && i < T) acc += expf(cx + us[t - (int)threadIdx.x + 127] - ls[t]);
+            }
+        }
+        __syncthreads();
+    }
+    if (x < T) (rel ? fr : fa)[row + x] = acc;
+}
+
+// One Adam step (Kingma and Ba, bias-corrected moments) on a and r with the
+// gradient of Eq. 4: (fa - eta_abs) / T and (fr - eta_rel) / T.
+// mom: [4][H][T] = m_a, v_a, m_r, v_r. c1 = 1 - b1^t, c2 = 1 - b2^t.
+__global__ void __launch_bounds__(256)
+fit_adam_kernel(const float* __restrict__ eta_abs, const float* __restrict__ eta_rel, const float* __restrict__ fa,
+                const float* __restrict__ fr, int T, int H, float lr, float b1, float b2, float eps, float c1,
+                float c2, float* __restrict__ a, float* __restrict__ r, float* __restrict__ mom) {
+    const int h = blockIdx.y;
+    const int j = blockIdx.x * 256 + threadIdx.x;
+    if (j >= T) return;
+    const size_t o = (size_t)h * T + j;
+    const size_t n = (size_t)H * T;
+    const float inv_t = 1.f / (float)T;
+    const float g[2] = {(fa[o] - eta_abs[o]) * inv_t, (fr[o] - eta_rel[o]) * inv_t};
+    float* p[2] = {a, r};
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        float& m = mom[(2 * k) * n + o];
+        float& v = mom[(2 * k + 1) * n + o];
+        m = b1 * m + (1.f - b1) * g[k];
+        v = b2 * v + (1.f - b2) * g[k] * g[k];
+        p[k][o] -= lr * (m / c1) / (sqrtf(v / c2) + eps);
+    }
+}
+
+// loss[h] = Eq. 4 at the current (a, r), from log Z. One block per head,
+// 256 threads; the per-thread strided sums meet in a fixed-order tree.
+__global__ void __launch_bounds__(256)
+fit_loss_kernel(const float* __restrict__ lz, const float* __restrict__ eta_abs, const float* __restrict__ eta_rel,
+                const float* __restrict__ a, const float* __restrict__ r, int T, float* __restrict__ loss) {
+    const int h = blockIdx.x;
+    const size_t row = (size_t)h * T;
+    float s = 0.f;
+    for (int i = threadIdx.x; i < T; i += 256)
+        s += lz[row + i] - eta_abs[row + i] * a[row + i] - eta_rel[row + i] * r[row + i];
+    __shared__ float red[256];
+    red[threadIdx.x] = s;
+    __syncthreads();
+    for (int w = 128; w > 0; w >>= 1) {
+        if ((int)threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) loss[h] = red[0] / (float)T;
+}
+
+struct FitLayout {
+    size_t status, hflag, amax, lz, fa, fr, mom, total;
+};
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+FitLayout fit_layout(int H, int T) {
+    FitLayout L;
+    const size_t n = (size_t)H * T * sizeof(float);
+    size_t off = 0;
+    L.status = off;
+    off = align256(off + kStatusBytes);
+    L.hflag = off;
+    off = align256(off + (size_t)H * sizeof(uint32_t));
+    L.amax = off;
+    off = align256(off + 2 * (size_t)H * sizeof(float));
+    L.lz = off;
+    off = align256(off + n);
+    L.fa = off;
+    off = align256(off + n);
+    L.fr = off;
+    off = align256(off + n);
+    L.mom = off;
+    off = align256(off + 4 * n);
+    L.total = off;
+    return L;
+}
+
+}  // namespace
+}  // namespace saf
+
+using namespace saf;
+
+extern "C" size_t saf_fit_workspace_bytes(int H, int T) {
+    if (H <= 0 || H > SAF_MAX_HEADS || T <= 0) return 0;
+    return fit_layout(H, T).total;
+}
+
+extern "C" int saf_fit_compact(const float* eta_abs, const float* eta_rel, int H, int T, int steps, float lr,
+                               float* a, float* r, float* loss, void* workspace, size_t ws_bytes, void* stream) {
+    if (H <= 0 || H > SAF_MAX_HEADS || T <= 0 || steps < 0 || !(lr > 0.f) || !isfinite(lr)) return SAF_EINVAL;
+    if (!eta_abs || !eta_rel || !a || !r || !loss) return SAF_EINVAL;
+    const uintptr_t any = (uintptr_t)eta_abs | (uintptr_t)eta_rel | (uintptr_t)a | (uintptr_t)r | (uintptr_t)loss;
+    if (any & 3u) return SAF_EALIGN;
+    if (!workspace) return SAF_EWORKSPACE;
+    if (((uintptr_t)workspace & 255u) != 0) return SAF_EALIGN;
+    const FitLayout L = fit_layout(H, T);
+    if (ws_bytes < L.total) return SAF_EWORKSPACE;
+    int dev = 0;
+    cudaDeviceProp prop;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SAF_ECUDA;
+    }
+    if (!(prop.major == 10 && prop.minor == 3)) return SAF_EUNSUPPORTED;
+    cudaStream_t s = (cudaStream_t)stream;
+    char* ws = (char*)workspace;
+    float* lz = (float*)(ws + L.lz);
+    float* fa = (float*)(ws + L.fa);
+    float* fr = (float*)(ws + L.fr);
+    float* mom = (float*)(ws + L.mom);
+
+    // the normaliser kernels of the layer see every head as frozen, with the
+    // current parameters as their a and r (row stride T)
+    LayerArgs p;
+    memset(&p, 0, sizeof(p));
+    p.a = a;
+    p.r = r;
+    p.ld_prior = T;
+    p.B = 1;
+    p.H = H;
+    p.T = T;
+    for (int h = 0; h < H; ++h) p.mask.w[h >> 6] |= 1ull << (h & 63);
+    p.status = (uint32_t*)(ws + L.status);
+    p.hflag = (uint32_t*)(ws + L.hflag);
+    p.amax = (float*)(ws + L.amax);
+    p.lz = lz;
+
+    const dim3 g256((unsigned)((T + 255) / 256), (unsigned)H);
+    const dim3 gm((unsigned)((T + 127) / 128), (unsigned)H, 2);
+    const float b1 = 0.9f, b2 = 0.999f, eps = 1e-8f;
+    cudaError_t e;
+    note_launch();
+    fit_init_kernel<<<g256, 256, 0, s>>>(eta_rel, T, H, a, r, mom);
+    e = cudaGetLastError();
+    double p1 = 1.0, p2 = 1.0;
+    for (int t = 1; t <= steps && e == cudaSuccess; ++t) {
+        e = launch_call_init(p, false, false, s);
+        if (e == cudaSuccess) e = launch_lognorm(p, false, false, s);
+        if (e != cudaSuccess) break;
+        note_launch();
+        fit_marginals_kernel<<<gm, 128, 0, s>>>(a, r, lz, T, fa, fr);
+        p1 *= b1;
+        p2 *= b2;
+        note_launch();
+        fit_adam_kernel<<<g256, 256, 0, s>>>(eta_abs, eta_rel, fa, fr, T, H, lr, b1, b2, eps, (float)(1.0 - p1),
+                                             (float)(1.0 - p2), a, r, mom);
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) e = launch_call_init(p, false, false, s);
+    if (e == cudaSuccess) e = launch_lognorm(p, false, false, s);
+    if (e == cudaSuccess) {
+        note_launch();
+        fit_loss_kernel<<<H, 256, 0, s>>>(lz, eta_abs, eta_rel, a, r, T, loss);
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) return SAF_OK;
+    cudaGetLastError();
+    return SAF_ELAUNCH;
+}

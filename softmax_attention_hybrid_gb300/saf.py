@@ -32,7 +32,7 @@ SAF_ESCRATCH = -9
 # Every symbol that include/saf.h declares.
 EXPORTED = ("saf_attn_workspace_bytes", "saf_attn_fwd", "saf_attn_bwd", "saf_device_status",
             "saf_error_string", "saf_version", "saf_set_trace_events", "saf_launch_count",
-            "saf_attn_fwd_noalloc")
+            "saf_attn_fwd_noalloc", "saf_fit_workspace_bytes", "saf_fit_compact")
 
 SAF_KERNEL_NONE = 0
 SAF_KERNEL_LOGNORM = 1
@@ -75,6 +75,10 @@ def _load():
     lib.saf_set_trace_events.restype = i
     lib.saf_launch_count.argtypes = []
     lib.saf_launch_count.restype = ctypes.c_ulonglong
+    lib.saf_fit_workspace_bytes.argtypes = [i, i]
+    lib.saf_fit_workspace_bytes.restype = sz
+    lib.saf_fit_compact.argtypes = [vp, vp, i, i, i, ctypes.c_float, vp, vp, vp, vp, sz, vp]
+    lib.saf_fit_compact.restype = i
     return lib
 
 
@@ -210,3 +214,24 @@ def saf_launch_count() -> int:
 
 def saf_device_status(workspace, stream=None) -> int:
     return int(_lib.saf_device_status(_ptr(workspace), _stream(stream)))
+
+
+def saf_fit_workspace_bytes(H, T) -> int:
+    return int(_lib.saf_fit_workspace_bytes(int(H), int(T)))
+
+
+def saf_fit_compact(eta_abs, eta_rel, steps=400, lr=0.05, a=None, r=None, loss=None, workspace=None, stream=None):
+    """Fit a, r of Eq. 3 to target marginals eta_abs, eta_rel (fp32 CUDA tensors
+    [H, T]); returns (a, r, loss) as fp32 CUDA tensors [H, T], [H, T], [H]."""
+    H, T = eta_abs.shape
+    dev = eta_abs.device
+    a = torch.empty((H, T), dtype=torch.float32, device=dev) if a is None else a
+    r = torch.empty((H, T), dtype=torch.float32, device=dev) if r is None else r
+    loss = torch.empty((H,), dtype=torch.float32, device=dev) if loss is None else loss
+    if workspace is None:
+        workspace = torch.empty(max(saf_fit_workspace_bytes(H, T), 256), dtype=torch.uint8, device=dev)
+    st = _lib.saf_fit_compact(_ptr(eta_abs), _ptr(eta_rel), H, T, int(steps), float(lr), _ptr(a), _ptr(r),
+                              _ptr(loss), _ptr(workspace), workspace.numel(), _stream(stream))
+    if st != SAF_OK:
+        raise SafError(st, "saf_fit_compact")
+    return a, r, loss
