@@ -40,42 +40,73 @@ fit_init_kernel(const float* __restrict__ eta_rel, int T, int H, float* __restri
 
 // out(x) = sum_{i >= x} exp(c(x) + u(i - x) - lz(i)): with (c, u) = (a, r) the
 // key-column marginal fa, with (c, u) = (r, a) the diagonal marginal fr.
+// Eq. 3 factorises as in the layer's kernels: with C = max c, U = max u,
+//     exp(c(x) + u(i - x) - lz(i)) = exp(c(x) - C) * exp(u(i - x) - U) * exp(C + U - lz(i)),
+// so a term costs one multiply-add once the factors are staged. Rows with
+// lz(i) - C - U < -64 would push the last factor past e^64; their terms are
+// formed in the exact exp form instead (the choice is per row i, so every
+// thread of the block takes the same branch). Elsewhere a term lost to
+// underflow of the first two factors is below e^-23 of its row's total.
 // Grid (ceil(T / 128), H, 2) (z = 0: fa, z = 1: fr), 128 threads: thread t of
-// block x sums output x = 128 bx + t over i in chunks of 128, with lz of the
-// chunk and the 255 values of u the chunk meets staged in shared memory.
+// block x sums output x = 128 bx + t over i in chunks of 128; the chunk's
+// factors and the 255 values of u it meets are staged in shared memory.
 __global__ void __launch_bounds__(128)
-fit_marginals_kernel(const float* __restrict__ a, const float* __restrict__ r, const float* __restrict__ lz, int T,
-                     float* __restrict__ fa, float* __restrict__ fr) {
+fit_marginals_kernel(const float* __restrict__ a, const float* __restrict__ r, const float* __restrict__ lz,
+                     const float* __restrict__ amax, int T, int H, float* __restrict__ fa, float* __restrict__ fr) {
     const int h = blockIdx.y;
     const bool rel = blockIdx.z != 0;
     const size_t row = (size_t)h * T;
     const float* c = (rel ? r : a) + row;
     const float* u = (rel ? a : r) + row;
     const float* l = lz + row;
-    __shared__ float ls[128];
-    __shared__ float us[256];
+    const float C = amax[rel ? H + h : h], U = amax[rel ? h : H + h];
+    __shared__ float ls[128], izs[128];
+    __shared__ float us[256], eus[256];
+    __shared__ int exact_any;
     const int x0 = blockIdx.x * 128;
     const int x = x0 + threadIdx.x;
     const float cx = x < T ? c[x] : 0.f;
-    float acc = 0.f;
+    float acc_f = 0.f, acc_x = 0.f;   // factorised terms (without exp(c(x) - C)), exact terms
     for (int i0 = x0; i0 < T; i0 += 128) {
-        // ls[t] = lz(i0 + t); us[k] = u(i0 - x0 - 127 + k), the offsets i - x of this chunk
-        ls[threadIdx.x] = (i0 + (int)threadIdx.x < T) ? l[i0 + threadIdx.x] : INFINITY;
+        if (threadIdx.x == 0) exact_any = 0;
+        __syncthreads();
+        {
+            const int i = i0 + threadIdx.x;
+            const float li = i < T ? l[i] : INFINITY;
+            const float sh = li - C - U;
+            const bool ex = i < T && !(sh >= -64.f);
+            ls[threadIdx.x] = li;
+            izs[threadIdx.x] = (i < T && !ex) ? expf(-sh) : 0.f;
+            if (ex) exact_any = 1;
+        }
         for (int k = threadIdx.x; k < 255; k += 128) {
             const int d = i0 - x0 - 127 + k;
-            us[k] = (d >= 0 && d < T) ? u[d] : -INFINITY;
+            const bool in = d >= 0 && d < T;
+            us[k] = in ? u[d] : -INFINITY;
+            eus[k] = in ? expf(u[d] - U) : 0.f;
         }
         __syncthreads();
         if (x < T) {
-#pragma unroll 4
-            for (int t = 0; t < 128; ++t) {
-                const int i = i0 + t;
-                if (i >= x && i < T) acc += expf(cx + us[t - (int)threadIdx.x + 127] - ls[t]);
+            const float* ep = eus + 127 - (int)threadIdx.x;
+            if (!exact_any) {
+#pragma unroll 8
+                for (int t = 0; t < 128; ++t)
+                    if (i0 + t >= x) acc_f = fmaf(ep[t], izs[t], acc_f);
+            } else {
+                const float* up = us + 127 - (int)threadIdx.x;
+                for (int t = 0; t < 128; ++t) {
+                    const int i = i0 + t;
+                    if (i < x || i >= T) continue;
+                    if (izs[t] != 0.f)
+                        acc_f = fmaf(ep[t], izs[t], acc_f);
+                    else
+                        acc_x += expf(cx + up[t] - ls[t]);
+                }
             }
         }
         __syncthreads();
     }
-    if (x < T) (rel ? fr : fa)[row + x] = acc;
+    if (x < T) (rel ? fr : fa)[row + x] = expf(cx - C) * acc_f + acc_x;
 }
 
 // One Adam step (Kingma and Ba, bias-corrected moments) on a and r with the
@@ -214,7 +245,7 @@ extern "C" int saf_fit_compact(const float* eta_abs, const float* eta_rel, int H
         if (e == cudaSuccess) e = launch_lognorm(p, false, false, s);
         if (e != cudaSuccess) break;
         note_launch();
-        fit_marginals_kernel<<<gm, 128, 0, s>>>(a, r, lz, T, fa, fr);
+        fit_marginals_kernel<<<gm, 128, 0, s>>>(a, r, lz, p.amax, T, H, fa, fr);
         p1 *= b1;
         p2 *= b2;
         note_launch();
