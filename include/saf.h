@@ -184,6 +184,24 @@ SAF_API size_t saf_fit_workspace_bytes(int H, int T);
 SAF_API int saf_fit_compact(const float* eta_abs, const float* eta_rel, int H, int T, int steps, float lr,
                             float* a, float* r, float* loss, void* workspace, size_t ws_bytes, void* stream);
 
+/* ---- Gradients of trainable patterns ---------------------------------------
+ * For the variant whose patterns keep training (App. C.3.2): the gradients of
+ * the loss with respect to a and r of every frozen head, given the forward
+ * output and the output gradient. Eq. 3 is a row softmax of the logits
+ * a(j) + r(i - j); with G(i, j) = dO_i . V_j and D_i = dO_i . O_i,
+ *   dL(i, j) = W(i, j) (G(i, j) - D_i),
+ *   da(j) = sum_b sum_{i >= j} dL(i, j),   dr(d) = sum_b sum_{i >= d} dL(i, i - d).
+ *
+ * In:  v, dO, o [B, H, T, d] (dt), lse [B, H, T] as saf_attn_fwd wrote it (the
+ *      frozen rows hold log Z), a, r, ld_prior, frozen as for saf_attn_fwd.
+ * Out: da, dr: DEVICE fp32 [H, T]; rows of ordinary heads are zero. They are
+ *      overwritten (cleared on `stream` first).
+ * fp32 arithmetic on CUDA cores; the additions into da and dr are atomic, so
+ * their last bits vary from run to run. No workspace. */
+SAF_API int saf_pattern_grad(const void* v, const void* dO, const void* o, const float* lse, const float* a,
+                             const float* r, int ld_prior, const uint8_t* frozen, int B, int H, int T, int d,
+                             saf_dtype_t dt, float* da, float* dr, void* stream);
+
 /* ---- Profiling hooks (not part of the layer's arithmetic) ----------------
  * Kernel identifiers for saf_set_trace_events. */
 typedef enum {

@@ -32,7 +32,8 @@ SAF_ESCRATCH = -9
 # Every symbol that include/saf.h declares.
 EXPORTED = ("saf_attn_workspace_bytes", "saf_attn_fwd", "saf_attn_bwd", "saf_device_status",
             "saf_error_string", "saf_version", "saf_set_trace_events", "saf_launch_count",
-            "saf_attn_fwd_noalloc", "saf_fit_workspace_bytes", "saf_fit_compact")
+            "saf_attn_fwd_noalloc", "saf_fit_workspace_bytes", "saf_fit_compact",
+            "saf_pattern_grad")
 
 SAF_KERNEL_NONE = 0
 SAF_KERNEL_LOGNORM = 1
@@ -79,6 +80,8 @@ def _load():
     lib.saf_fit_workspace_bytes.restype = sz
     lib.saf_fit_compact.argtypes = [vp, vp, i, i, i, ctypes.c_float, vp, vp, vp, vp, sz, vp]
     lib.saf_fit_compact.restype = i
+    lib.saf_pattern_grad.argtypes = [vp, vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, vp, vp, vp]
+    lib.saf_pattern_grad.restype = i
     return lib
 
 
@@ -235,3 +238,15 @@ def saf_fit_compact(eta_abs, eta_rel, steps=400, lr=0.05, a=None, r=None, loss=N
     if st != SAF_OK:
         raise SafError(st, "saf_fit_compact")
     return a, r, loss
+
+
+def saf_pattern_grad(v, do, o, lse, a, r, frozen, da=None, dr=None, stream=None):
+    """Gradients of a and r of the frozen heads (fp32 CUDA tensors [H, T])."""
+    B, H, T, d = v.shape
+    da = torch.empty((H, T), dtype=torch.float32, device=v.device) if da is None else da
+    dr = torch.empty((H, T), dtype=torch.float32, device=v.device) if dr is None else dr
+    st = _lib.saf_pattern_grad(_ptr(v), _ptr(do), _ptr(o), _ptr(lse), _ptr(a), _ptr(r), a.shape[-1],
+                               _frozen_bytes(frozen, H), B, H, T, d, _dt(v), _ptr(da), _ptr(dr), _stream(stream))
+    if st != SAF_OK:
+        raise SafError(st, "saf_pattern_grad")
+    return da, dr
