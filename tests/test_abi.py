@@ -123,3 +123,45 @@ def test_no_device_is_reported_not_faked(saf):
         pytest.skip("a GPU is present")
     # every argument valid: the call reaches the device check and must fail there
     assert _fwd(saf.library()) in (saf.SAF_ECUDA, saf.SAF_EUNSUPPORTED)
+
+
+def test_fit_argument_errors(saf):
+    lib = saf.library()
+    F = FAKE
+    assert saf.saf_fit_workspace_bytes(3, 4096) > 0 and saf.saf_fit_workspace_bytes(3, 4096) % 256 == 0
+    assert saf.saf_fit_workspace_bytes(0, 16) == 0 and saf.saf_fit_workspace_bytes(2, 0) == 0
+
+    def fit(**kw):
+        a = dict(ea=F, er=F, H=2, T=64, steps=400, lr=0.05, a=F, r=F, loss=F, ws=F, wsb=1 << 30)
+        a.update(kw)
+        return lib.saf_fit_compact(a["ea"], a["er"], a["H"], a["T"], a["steps"], a["lr"], a["a"], a["r"],
+                                   a["loss"], a["ws"], a["wsb"], None)
+
+    assert fit(H=0) == saf.SAF_EINVAL
+    assert fit(T=0) == saf.SAF_EINVAL
+    assert fit(steps=-1) == saf.SAF_EINVAL
+    assert fit(lr=0.0) == saf.SAF_EINVAL
+    assert fit(lr=float("nan")) == saf.SAF_EINVAL
+    assert fit(ea=None) == saf.SAF_EINVAL
+    assert fit(a=F + 2) == saf.SAF_EALIGN
+    assert fit(ws=None) == saf.SAF_EWORKSPACE
+    assert fit(ws=F + 64) == saf.SAF_EALIGN
+    assert fit(wsb=256) == saf.SAF_EWORKSPACE
+
+
+def test_pattern_grad_argument_errors(saf):
+    lib = saf.library()
+    F = FAKE
+
+    def pg(**kw):
+        a = dict(v=F, do=F, o=F, lse=F, a=F, r=F, ld=256, B=1, H=4, T=256, d=64, dt=0, da=F, dr=F)
+        a.update(kw)
+        return lib.saf_pattern_grad(a["v"], a["do"], a["o"], a["lse"], a["a"], a["r"], a["ld"], None, a["B"],
+                                    a["H"], a["T"], a["d"], a["dt"], a["da"], a["dr"], None)
+
+    assert pg(H=0) == saf.SAF_EINVAL
+    assert pg(d=96) == saf.SAF_EUNSUPPORTED
+    assert pg(dt=5) == saf.SAF_EINVAL
+    assert pg(da=None) == saf.SAF_EINVAL
+    assert pg(dr=F + 1) == saf.SAF_EALIGN
+    assert pg(T=0) == saf.SAF_OK
