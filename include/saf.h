@@ -22,6 +22,8 @@
  * ---------------------------------------
  *  - Tensors q, k, v, o, dO, dq, dk, dv have layout [B, H, T, d], contiguous,
  *    element type `dt` (bf16 or fp32). lse and the normalisers are fp32.
+ *    d = 64 for SAF_BF16 (tensor-core kernels); d = 64, 96 or 128 for
+ *    SAF_FP32 (CUDA-core kernels). Other values return SAF_EUNSUPPORTED.
  *    Every tensor pointer must be 16-byte aligned (SAF_EALIGN otherwise).
  *  - a, r: fp32 [H, ld_prior] device arrays, ld_prior >= T; row h holds the
  *    absolute-key preference a and the relative-distance preference r of

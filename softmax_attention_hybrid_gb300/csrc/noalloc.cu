@@ -60,7 +60,7 @@ extern "C" int saf_attn_fwd_noalloc(const void* q, const void* k, const void* v,
                                     saf_dtype_t dt, void* o, float* lse, void* stream) {
     using namespace saf;
     const size_t need = saf_attn_workspace_bytes(B, H, T, d, dt, 0);
-    if (need == 0) return (d != kHeadDim) ? SAF_EUNSUPPORTED : SAF_EINVAL;
+    if (need == 0) return (dt == SAF_BF16 || dt == SAF_FP32) && !head_dim_supported(d, dt) ? SAF_EUNSUPPORTED : SAF_EINVAL;
     if (need > kNoallocScratchBytes) return SAF_ESCRATCH;
     void* ws = nullptr;
     const int st = scratch_address(&ws);

@@ -350,17 +350,18 @@ lognorm_kernel(const float* __restrict__ a_all, const float* __restrict__ r_all,
     cluster_barrier();   // CTA 0 has read every tot: the other CTAs may exit
 }
 
-// D_i = sum_c dO_ic * O_ic, one warp per row (d = 64: two elements per lane).
+// D_i = sum_c dO_ic * O_ic, one warp per row (head dimension d: d / 32 elements per lane).
 template <typename E>
 __global__ void __launch_bounds__(256)
-bwd_delta_kernel(const E* __restrict__ o, const E* __restrict__ dO, float* __restrict__ delta, long long rows) {
+bwd_delta_kernel(const E* __restrict__ o, const E* __restrict__ dO, float* __restrict__ delta, long long rows,
+                 int d) {
     const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (row >= rows) return;
     const int lane = threadIdx.x & 31;
-    const E* po = o + row * kHeadDim;
-    const E* pd = dO + row * kHeadDim;
+    const E* po = o + row * d;
+    const E* pd = dO + row * d;
     float x = 0.f;
-    for (int c = lane; c < kHeadDim; c += 32) x = fmaf(to_f(po[c]), to_f(pd[c]), x);
+    for (int c = lane; c < d; c += 32) x = fmaf(to_f(po[c]), to_f(pd[c]), x);
     for (int s = 16; s > 0; s >>= 1) x += __shfl_xor_sync(0xffffffffu, x, s);
     if (lane == 0) delta[row] = x;
 }
@@ -479,9 +480,9 @@ cudaError_t launch_bwd_delta(const LayerArgs& p, bool bf16, cudaStream_t s) {
     before_launch(SAF_KERNEL_BWD_DELTA, s);
     if (bf16)
         bwd_delta_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
-            (const __nv_bfloat16*)p.o, (const __nv_bfloat16*)p.dO, p.delta, rows);
+            (const __nv_bfloat16*)p.o, (const __nv_bfloat16*)p.dO, p.delta, rows, p.d);
     else
-        bwd_delta_kernel<float><<<blocks, 256, 0, s>>>((const float*)p.o, (const float*)p.dO, p.delta, rows);
+        bwd_delta_kernel<float><<<blocks, 256, 0, s>>>((const float*)p.o, (const float*)p.dO, p.delta, rows, p.d);
     after_launch(SAF_KERNEL_BWD_DELTA, s);
     return cudaGetLastError();
 }

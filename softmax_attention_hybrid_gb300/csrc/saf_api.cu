@@ -103,7 +103,7 @@ int validate(const void* q, const void* k, const void* v, const float* a, const 
     if (B < 0 || H <= 0 || T < 0) return SAF_EINVAL;
     if (H > SAF_MAX_HEADS) return SAF_EINVAL;
     if (dt != SAF_BF16 && dt != SAF_FP32) return SAF_EINVAL;
-    if (d != kHeadDim) return SAF_EUNSUPPORTED;
+    if (!head_dim_supported(d, dt)) return SAF_EUNSUPPORTED;
     if ((long long)B * H * T * d > (1ll << 40)) return SAF_EINVAL;
     memset(c, 0, sizeof(*c));
     for (int h = 0; h < H; ++h) {
@@ -201,8 +201,9 @@ int saf_set_trace_events(int kernel, void* start, void* stop) {
 unsigned long long saf_launch_count(void) { return g_launches; }
 
 size_t saf_attn_workspace_bytes(int B, int H, int T, int d, saf_dtype_t dt, int backward) {
-    if (B < 0 || H <= 0 || T < 0 || H > SAF_MAX_HEADS || d != kHeadDim) return 0;
+    if (B < 0 || H <= 0 || T < 0 || H > SAF_MAX_HEADS) return 0;
     if (dt != SAF_BF16 && dt != SAF_FP32) return 0;
+    if (!head_dim_supported(d, dt)) return 0;
     return workspace_layout(B, H, T, backward ? 1 : 0, dt == SAF_BF16).total;
 }
 
@@ -218,6 +219,7 @@ int saf_attn_fwd(const void* q, const void* k, const void* v, const float* a, co
     if ((st = check_device()) != SAF_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     LayerArgs p = make_args(q, k, v, a, r, ld_prior, B, H, T, c, workspace, 0, dt == SAF_BF16);
+    p.d = d;
     p.out = o;
     p.lse_out = lse;
     const bool bf16 = dt == SAF_BF16;
@@ -240,6 +242,7 @@ int saf_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
     if ((st = check_device()) != SAF_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     LayerArgs p = make_args(q, k, v, a, r, ld_prior, B, H, T, c, workspace, 1, dt == SAF_BF16);
+    p.d = d;
     p.o = o;
     p.dO = dO;
     p.lse = lse;

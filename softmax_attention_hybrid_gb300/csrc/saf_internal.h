@@ -11,8 +11,12 @@
 
 namespace saf {
 
-// Head dimension of every kernel in this library.
+// Head dimension of the tensor-core kernels (bf16). The fp32 CUDA-core path
+// also takes 96 and 128.
 constexpr int kHeadDim = 64;
+inline bool head_dim_supported(int d, saf_dtype_t dt) {
+    return d == kHeadDim || (dt == SAF_FP32 && (d == 96 || d == 128));
+}
 
 // Per-head frozen flags as a bitmask, passed by value to every kernel so that
 // no host-to-device copy is needed per call (H <= SAF_MAX_HEADS).
@@ -135,6 +139,7 @@ struct LayerArgs {
     float* rowvec;       // workspace: per-block row vectors [B, H, Tp / 128, 256]
     uint32_t* status;    // workspace: error words
     int B, H, T, ld_prior;
+    int d;               // head dimension
     HeadMask mask;
 };
 

@@ -12,9 +12,10 @@
 //              and a query-block pass (dQ for ordinary heads), as App. D.2
 //              describes; frozen heads get dV = W^T dO and exact-zero dQ, dK.
 //
-// Tile: 64 query rows x 64 keys, d = 64, 256 threads. Thread (ty, tx),
-// ty = tid / 16, tx = tid % 16, owns rows 4*ty .. 4*ty+3 and the columns
-// tx, tx+16, tx+32, tx+48 of the key (or head-dimension) axis.
+// Tile: 64 query rows x 64 keys, head dimension D = 64, 96 or 128, 256
+// threads. Thread (ty, tx), ty = tid / 16, tx = tid % 16, owns rows
+// 4*ty .. 4*ty+3 and the columns tx, tx+16, ... of the key axis (4 of them)
+// or of the head-dimension axis (D / 16 of them).
 #include <math.h>
 
 #include "saf_internal.h"
@@ -23,16 +24,19 @@ namespace saf {
 namespace {
 
 constexpr int kB = 64;          // rows per tile (queries and keys)
-constexpr int kLd = kB + 1;     // padded fp32 row stride in shared memory
-constexpr int kTile = kB * kLd; // floats per tile
+constexpr int kLd = kB + 1;     // padded fp32 row stride of a (key x query) tile
 constexpr int kThreads = 256;
+// floats per tile slot: every tile, (rows x D) or (key x query), fits one slot
+template <int D>
+__host__ __device__ constexpr int tile_floats() { return kB * ((D > kB ? D : kB) + 1); }
 
-template <typename E>
+// rows r0 .. r0 + 63 of a [T, D] slice into shared memory, row stride D + 1
+template <int D, typename E>
 __device__ __forceinline__ void load_tile(float* s, const E* g, int r0, int T) {
-    for (int e = threadIdx.x; e < kB * kHeadDim; e += kThreads) {
-        const int rr = e >> 6, c = e & 63;
+    for (int e = threadIdx.x; e < kB * D; e += kThreads) {
+        const int rr = e / D, c = e - rr * D;
         const int row = r0 + rr;
-        s[rr * kLd + c] = row < T ? to_f(g[(size_t)row * kHeadDim + c]) : 0.f;
+        s[rr * (D + 1) + c] = row < T ? to_f(g[(size_t)row * D + c]) : 0.f;
     }
 }
 
@@ -48,18 +52,19 @@ __device__ __forceinline__ float quad16_sum(float x) {
 // ---------------------------------------------------------------------------
 // Forward. Grid (ceil(T/64), B*H).
 // ---------------------------------------------------------------------------
-template <typename E>
+template <typename E, int D>
 __global__ void __launch_bounds__(kThreads) fwd_kernel(LayerArgs p) {
     extern __shared__ float sm[];
     float* Qs = sm;
-    float* Ks = Qs + kTile;
-    float* Vs = Ks + kTile;
-    float* Ps = Vs + kTile;
+    constexpr int LdD = D + 1, NC = D / 16, kT = tile_floats<D>();
+    float* Ks = Qs + kT;
+    float* Vs = Ks + kT;
+    float* Ps = Vs + kT;
 
     const int T = p.T;
     const int qb = blockIdx.x, bh = blockIdx.y, h = bh % p.H;
     const bool frozen = head_frozen(p.mask, h);
-    const size_t base = (size_t)bh * T * kHeadDim;
+    const size_t base = (size_t)bh * T * D;
     const E* q = (const E*)p.q + base;
     const E* k = (const E*)p.k + base;
     const E* v = (const E*)p.v + base;
@@ -67,10 +72,10 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(LayerArgs p) {
     const float* r = p.r + (size_t)h * p.ld_prior;
     const int q0 = qb * kB;
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-    const float scale = 0.125f;  // 1 / sqrt(64)
+    const float scale = 1.f / sqrtf((float)D);
 
-    if (!frozen) load_tile(Qs, q, q0, T);
-    float m[4], l[4], lzr[4], acc[4][4];
+    if (!frozen) load_tile<D>(Qs, q, q0, T);
+    float m[4], l[4], lzr[4], acc[4][NC];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int row = q0 + ty * 4 + i;
@@ -78,13 +83,13 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(LayerArgs p) {
         l[i] = 0.f;
         lzr[i] = (frozen && row < T) ? p.lz[(size_t)h * T + row] : 0.f;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) acc[i][c] = 0.f;
+        for (int c = 0; c < NC; ++c) acc[i][c] = 0.f;
     }
 
     for (int kb = 0; kb <= qb; ++kb) {
         __syncthreads();
-        if (!frozen) load_tile(Ks, k, kb * kB, T);
-        load_tile(Vs, v, kb * kB, T);
+        if (!frozen) load_tile<D>(Ks, k, kb * kB, T);
+        load_tile<D>(Vs, v, kb * kB, T);
         __syncthreads();
         float s[4][4];
 #pragma unroll
@@ -99,10 +104,10 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(LayerArgs p) {
                     s[i][c] = ok ? expf(a[key] + r[row - key] - lzr[i]) : 0.f;
                 } else {
                     float dot = 0.f;
-                    const float* qr = Qs + (ty * 4 + i) * kLd;
-                    const float* kr = Ks + (tx + 16 * c) * kLd;
+                    const float* qr = Qs + (ty * 4 + i) * LdD;
+                    const float* kr = Ks + (tx + 16 * c) * LdD;
 #pragma unroll 16
-                    for (int e = 0; e < kHeadDim; ++e) dot = fmaf(qr[e], kr[e], dot);
+                    for (int e = 0; e < D; ++e) dot = fmaf(qr[e], kr[e], dot);
                     s[i][c] = (key <= row && key < T) ? dot * scale : -INFINITY;
                 }
             }
@@ -122,7 +127,7 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(LayerArgs p) {
                 l[i] = l[i] * corr + quad16_sum(ls);
                 m[i] = mnew;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) acc[i][c] *= corr;
+                for (int c = 0; c < NC; ++c) acc[i][c] *= corr;
             }
         }
 #pragma unroll
@@ -132,14 +137,14 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(LayerArgs p) {
         __syncthreads();
 #pragma unroll 4
         for (int j = 0; j < kB; ++j) {
-            float vv[4];
+            float vv[NC];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) vv[c] = Vs[j * kLd + tx + 16 * c];
+            for (int c = 0; c < NC; ++c) vv[c] = Vs[j * LdD + tx + 16 * c];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float pij = Ps[(ty * 4 + i) * kLd + j];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) acc[i][c] = fmaf(pij, vv[c], acc[i][c]);
+                for (int c = 0; c < NC; ++c) acc[i][c] = fmaf(pij, vv[c], acc[i][c]);
             }
         }
     }
@@ -151,7 +156,7 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(LayerArgs p) {
         if (row >= T) continue;
         const float inv = frozen ? 1.f : 1.f / l[i];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) from_f(o + (size_t)row * kHeadDim + tx + 16 * c, acc[i][c] * inv);
+        for (int c = 0; c < NC; ++c) from_f(o + (size_t)row * D + tx + 16 * c, acc[i][c] * inv);
         if (tx == 0) p.lse_out[(size_t)bh * T + row] = frozen ? lzr[i] : m[i] + logf(l[i]);
     }
 }
@@ -160,22 +165,23 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(LayerArgs p) {
 // Backward, key-block pass. Grid (ceil(T/64), B*H). Program owns keys
 // k0..k0+63; loops over query blocks qb >= kb. Thread rows = keys.
 // ---------------------------------------------------------------------------
-template <typename E>
+template <typename E, int D>
 __global__ void __launch_bounds__(kThreads) bwd_kv_kernel(LayerArgs p) {
     extern __shared__ float sm[];
+    constexpr int LdD = D + 1, NC = D / 16, kT = tile_floats<D>();
     float* Ks = sm;
-    float* Vs = Ks + kTile;
-    float* Qs = Vs + kTile;
-    float* dOs = Qs + kTile;
-    float* Pt = dOs + kTile;    // P^T  [key][query]
-    float* dSt = Pt + kTile;    // dS^T [key][query]
+    float* Vs = Ks + kT;
+    float* Qs = Vs + kT;
+    float* dOs = Qs + kT;
+    float* Pt = dOs + kT;    // P^T  [key][query]
+    float* dSt = Pt + kT;    // dS^T [key][query]
     __shared__ float rowstat[kB];  // lse (ordinary) or log Z (frozen) per query
     __shared__ float rowD[kB];
 
     const int T = p.T;
     const int kb = blockIdx.x, bh = blockIdx.y, h = bh % p.H;
     const bool frozen = head_frozen(p.mask, h);
-    const size_t base = (size_t)bh * T * kHeadDim;
+    const size_t base = (size_t)bh * T * D;
     const E* q = (const E*)p.q + base;
     const E* k = (const E*)p.k + base;
     const E* v = (const E*)p.v + base;
@@ -184,22 +190,22 @@ __global__ void __launch_bounds__(kThreads) bwd_kv_kernel(LayerArgs p) {
     const float* r = p.r + (size_t)h * p.ld_prior;
     const int k0 = kb * kB;
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-    const float scale = 0.125f;
+    const float scale = 1.f / sqrtf((float)D);
 
-    if (!frozen) load_tile(Ks, k, k0, T);
-    load_tile(Vs, v, k0, T);
-    float dv[4][4], dk[4][4];
+    if (!frozen) load_tile<D>(Ks, k, k0, T);
+    load_tile<D>(Vs, v, k0, T);
+    float dv[4][NC], dk[4][NC];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) dv[i][c] = dk[i][c] = 0.f;
+        for (int c = 0; c < NC; ++c) dv[i][c] = dk[i][c] = 0.f;
 
     const int nqb = (T + kB - 1) / kB;
     for (int qb = kb; qb < nqb; ++qb) {
         const int q0 = qb * kB;
         __syncthreads();
-        if (!frozen) load_tile(Qs, q, q0, T);
-        load_tile(dOs, dO, q0, T);
+        if (!frozen) load_tile<D>(Qs, q, q0, T);
+        load_tile<D>(dOs, dO, q0, T);
         if (tid < kB) {
             const int qi = q0 + tid;
             if (frozen) {
@@ -223,12 +229,12 @@ __global__ void __launch_bounds__(kThreads) bwd_kv_kernel(LayerArgs p) {
                     pt = ok ? expf(a[key] + r[qi - key] - rowstat[qq]) : 0.f;
                 } else {
                     float dot = 0.f, dpt = 0.f;
-                    const float* kr = Ks + (ty * 4 + i) * kLd;
-                    const float* qr = Qs + qq * kLd;
-                    const float* vr = Vs + (ty * 4 + i) * kLd;
-                    const float* gr = dOs + qq * kLd;
+                    const float* kr = Ks + (ty * 4 + i) * LdD;
+                    const float* qr = Qs + qq * LdD;
+                    const float* vr = Vs + (ty * 4 + i) * LdD;
+                    const float* gr = dOs + qq * LdD;
 #pragma unroll 16
-                    for (int e = 0; e < kHeadDim; ++e) {
+                    for (int e = 0; e < D; ++e) {
                         dot = fmaf(kr[e], qr[e], dot);
                         dpt = fmaf(vr[e], gr[e], dpt);
                     }
@@ -242,18 +248,18 @@ __global__ void __launch_bounds__(kThreads) bwd_kv_kernel(LayerArgs p) {
         __syncthreads();
 #pragma unroll 4
         for (int qq = 0; qq < kB; ++qq) {
-            float g[4], x[4];
+            float g[NC], x[NC];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                g[c] = dOs[qq * kLd + tx + 16 * c];
-                x[c] = frozen ? 0.f : Qs[qq * kLd + tx + 16 * c];
+            for (int c = 0; c < NC; ++c) {
+                g[c] = dOs[qq * LdD + tx + 16 * c];
+                x[c] = frozen ? 0.f : Qs[qq * LdD + tx + 16 * c];
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float pt = Pt[(ty * 4 + i) * kLd + qq];
                 const float ds = dSt[(ty * 4 + i) * kLd + qq];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < NC; ++c) {
                     dv[i][c] = fmaf(pt, g[c], dv[i][c]);
                     dk[i][c] = fmaf(ds, x[c], dk[i][c]);
                 }
@@ -268,9 +274,9 @@ __global__ void __launch_bounds__(kThreads) bwd_kv_kernel(LayerArgs p) {
         const int key = k0 + ty * 4 + i;
         if (key >= T) continue;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            from_f(dvp + (size_t)key * kHeadDim + tx + 16 * c, dv[i][c]);
-            from_f(dkp + (size_t)key * kHeadDim + tx + 16 * c, frozen ? 0.f : dk[i][c] * scale);
+        for (int c = 0; c < NC; ++c) {
+            from_f(dvp + (size_t)key * D + tx + 16 * c, dv[i][c]);
+            from_f(dkp + (size_t)key * D + tx + 16 * c, frozen ? 0.f : dk[i][c] * scale);
         }
     }
 }
@@ -279,26 +285,27 @@ __global__ void __launch_bounds__(kThreads) bwd_kv_kernel(LayerArgs p) {
 // Backward, query-block pass (dQ). Grid (ceil(T/64), B*H). Frozen heads
 // write zeros.
 // ---------------------------------------------------------------------------
-template <typename E>
+template <typename E, int D>
 __global__ void __launch_bounds__(kThreads) bwd_q_kernel(LayerArgs p) {
     extern __shared__ float sm[];
+    constexpr int LdD = D + 1, NC = D / 16, kT = tile_floats<D>();
     float* Qs = sm;
-    float* dOs = Qs + kTile;
-    float* Ks = dOs + kTile;
-    float* Vs = Ks + kTile;
-    float* dSs = Vs + kTile;
+    float* dOs = Qs + kT;
+    float* Ks = dOs + kT;
+    float* Vs = Ks + kT;
+    float* dSs = Vs + kT;
 
     const int T = p.T;
     const int qb = blockIdx.x, bh = blockIdx.y, h = bh % p.H;
     const bool frozen = head_frozen(p.mask, h);
-    const size_t base = (size_t)bh * T * kHeadDim;
+    const size_t base = (size_t)bh * T * D;
     E* dq = (E*)p.dq + base;
     const int q0 = qb * kB;
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
     if (frozen) {
-        for (int e = tid; e < kB * kHeadDim; e += kThreads) {
-            const int row = q0 + (e >> 6);
-            if (row < T) from_f(dq + (size_t)row * kHeadDim + (e & 63), 0.f);
+        for (int e = tid; e < kB * D; e += kThreads) {
+            const int row = q0 + e / D;
+            if (row < T) from_f(dq + (size_t)row * D + e % D, 0.f);
         }
         return;
     }
@@ -306,23 +313,23 @@ __global__ void __launch_bounds__(kThreads) bwd_q_kernel(LayerArgs p) {
     const E* k = (const E*)p.k + base;
     const E* v = (const E*)p.v + base;
     const E* dO = (const E*)p.dO + base;
-    const float scale = 0.125f;
+    const float scale = 1.f / sqrtf((float)D);
 
-    load_tile(Qs, q, q0, T);
-    load_tile(dOs, dO, q0, T);
-    float lse[4], Dr[4], acc[4][4];
+    load_tile<D>(Qs, q, q0, T);
+    load_tile<D>(dOs, dO, q0, T);
+    float lse[4], Dr[4], acc[4][NC];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int row = q0 + ty * 4 + i;
         lse[i] = row < T ? p.lse[(size_t)bh * T + row] : 0.f;
         Dr[i] = row < T ? p.delta[(size_t)bh * T + row] : 0.f;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) acc[i][c] = 0.f;
+        for (int c = 0; c < NC; ++c) acc[i][c] = 0.f;
     }
     for (int kb = 0; kb <= qb; ++kb) {
         __syncthreads();
-        load_tile(Ks, k, kb * kB, T);
-        load_tile(Vs, v, kb * kB, T);
+        load_tile<D>(Ks, k, kb * kB, T);
+        load_tile<D>(Vs, v, kb * kB, T);
         __syncthreads();
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -331,12 +338,12 @@ __global__ void __launch_bounds__(kThreads) bwd_q_kernel(LayerArgs p) {
             for (int c = 0; c < 4; ++c) {
                 const int key = kb * kB + tx + 16 * c;
                 float dot = 0.f, dp = 0.f;
-                const float* qr = Qs + (ty * 4 + i) * kLd;
-                const float* kr = Ks + (tx + 16 * c) * kLd;
-                const float* gr = dOs + (ty * 4 + i) * kLd;
-                const float* vr = Vs + (tx + 16 * c) * kLd;
+                const float* qr = Qs + (ty * 4 + i) * LdD;
+                const float* kr = Ks + (tx + 16 * c) * LdD;
+                const float* gr = dOs + (ty * 4 + i) * LdD;
+                const float* vr = Vs + (tx + 16 * c) * LdD;
 #pragma unroll 16
-                for (int e = 0; e < kHeadDim; ++e) {
+                for (int e = 0; e < D; ++e) {
                     dot = fmaf(qr[e], kr[e], dot);
                     dp = fmaf(gr[e], vr[e], dp);
                 }
@@ -348,14 +355,14 @@ __global__ void __launch_bounds__(kThreads) bwd_q_kernel(LayerArgs p) {
         __syncthreads();
 #pragma unroll 4
         for (int j = 0; j < kB; ++j) {
-            float kk[4];
+            float kk[NC];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) kk[c] = Ks[j * kLd + tx + 16 * c];
+            for (int c = 0; c < NC; ++c) kk[c] = Ks[j * LdD + tx + 16 * c];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float ds = dSs[(ty * 4 + i) * kLd + j];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) acc[i][c] = fmaf(ds, kk[c], acc[i][c]);
+                for (int c = 0; c < NC; ++c) acc[i][c] = fmaf(ds, kk[c], acc[i][c]);
             }
         }
     }
@@ -364,13 +371,13 @@ __global__ void __launch_bounds__(kThreads) bwd_q_kernel(LayerArgs p) {
         const int row = q0 + ty * 4 + i;
         if (row >= T) continue;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) from_f(dq + (size_t)row * kHeadDim + tx + 16 * c, acc[i][c] * scale);
+        for (int c = 0; c < NC; ++c) from_f(dq + (size_t)row * D + tx + 16 * c, acc[i][c] * scale);
     }
 }
 
-template <typename K>
+template <int D, typename K>
 cudaError_t launch(K kernel, int id, int tiles, const LayerArgs& p, cudaStream_t s) {
-    const int smem = tiles * kTile * (int)sizeof(float);
+    const int smem = tiles * tile_floats<D>() * (int)sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid((p.T + kB - 1) / kB, p.B * p.H);
@@ -380,19 +387,36 @@ cudaError_t launch(K kernel, int id, int tiles, const LayerArgs& p, cudaStream_t
     return cudaGetLastError();
 }
 
+template <typename E, int D>
+cudaError_t fwd_d(const LayerArgs& p, cudaStream_t s) {
+    return launch<D>(fwd_kernel<E, D>, SAF_KERNEL_FWD, 4, p, s);
+}
+
+template <typename E, int D>
+cudaError_t bwd_d(const LayerArgs& p, cudaStream_t s) {
+    cudaError_t e = launch<D>(bwd_kv_kernel<E, D>, SAF_KERNEL_BWD_KV, 6, p, s);
+    if (e != cudaSuccess) return e;
+    return launch<D>(bwd_q_kernel<E, D>, SAF_KERNEL_BWD_Q, 5, p, s);
+}
+
 }  // namespace
 
 cudaError_t launch_simt_fwd(const LayerArgs& p, bool bf16, cudaStream_t s) {
-    return bf16 ? launch(fwd_kernel<__nv_bfloat16>, SAF_KERNEL_FWD, 4, p, s)
-                : launch(fwd_kernel<float>, SAF_KERNEL_FWD, 4, p, s);
+    if (bf16) return fwd_d<__nv_bfloat16, 64>(p, s);
+    switch (p.d) {
+        case 96: return fwd_d<float, 96>(p, s);
+        case 128: return fwd_d<float, 128>(p, s);
+        default: return fwd_d<float, 64>(p, s);
+    }
 }
 
 cudaError_t launch_simt_bwd(const LayerArgs& p, bool bf16, cudaStream_t s) {
-    cudaError_t e = bf16 ? launch(bwd_kv_kernel<__nv_bfloat16>, SAF_KERNEL_BWD_KV, 6, p, s)
-                         : launch(bwd_kv_kernel<float>, SAF_KERNEL_BWD_KV, 6, p, s);
-    if (e != cudaSuccess) return e;
-    return bf16 ? launch(bwd_q_kernel<__nv_bfloat16>, SAF_KERNEL_BWD_Q, 5, p, s)
-                : launch(bwd_q_kernel<float>, SAF_KERNEL_BWD_Q, 5, p, s);
+    if (bf16) return bwd_d<__nv_bfloat16, 64>(p, s);
+    switch (p.d) {
+        case 96: return bwd_d<float, 96>(p, s);
+        case 128: return bwd_d<float, 128>(p, s);
+        default: return bwd_d<float, 64>(p, s);
+    }
 }
 
 }  // namespace saf

@@ -52,6 +52,8 @@ def test_workspace_bytes(saf):
     assert f(8, 12, 4096, 64, "bf16", 1) > f(8, 12, 4096, 64, "bf16", 0)
     assert f(8, 12, 4096, 64, "bf16", 1) % 256 == 0
     assert f(1, 4, 256, 32, "bf16", 0) == 0        # unsupported d
+    assert f(1, 4, 256, 96, "bf16", 0) == 0        # the tensor-core path takes d = 64 only
+    assert f(1, 4, 256, 96, "fp32", 1) > 0 and f(1, 4, 256, 128, "fp32", 0) > 0
     assert f(1, 0, 256, 64, "bf16", 0) == 0        # no heads
     assert f(1, 300, 256, 64, "bf16", 0) == 0      # more than SAF_MAX_HEADS
     assert f(0, 4, 0, 64, "fp32", 1) > 0           # empty call still has the status words

@@ -81,6 +81,14 @@ def test_ragged_lengths(saf, T, dtype):
     _check_full(saf, w, seed=T)
 
 
+@pytest.mark.parametrize("d", [96, 128])
+def test_fp32_head_dims(saf, d):
+    # the fp32 CUDA-core path also takes head dimensions 96 and 128 (the paper's
+    # 1B layer has d 96; the bf16 tensor-core path takes 64)
+    w = custom_workload(2, 3, 150, d=d, dtype="fp32", frozen=(1,), slope=0.05)
+    _check_full(saf, w, seed=60 + d)
+
+
 @pytest.mark.parametrize("frozen", [(), (0, 1, 2, 3), (0,), (2, 3), (1, 3)])
 def test_head_sets(saf, frozen):
     # empty, full and partial replaced sets (App. D.2 suite)
