@@ -26,4 +26,6 @@ from .saf_oracle import (  # noqa: F401
     fit_grad,
     fit_compact,
     fit_kl,
+    gqa_fwd,
+    gqa_bwd,
 )

@@ -373,3 +373,66 @@ def fit_kl(P, a, r):
     Ph = frozen_pattern(a, r, T)
     causal = np.tril(np.ones((T, T), dtype=bool)) & (P > 0)
     return float(np.sum(P[causal] * (np.log(P[causal]) - np.log(Ph[causal])))) / T
+
+
+# ---------------------------------------------------------------------------
+# Grouped-query layout (§3.3: the grouped-query path drops the replaced heads'
+# query projections and keeps the shared key and value projections; App. C.6:
+# 32 query heads share 8 key/value heads)
+# ---------------------------------------------------------------------------
+
+def gqa_fwd(q, k, v, a, r, frozen, threads=1):
+    """Layer forward with H query heads over Hkv shared key/value heads: query
+    head h reads key/value head h // (H / Hkv). q [B, H, T, d]; k, v
+    [B, Hkv, T, d]; a, r [H, >= T]; frozen: H flags (a frozen head reads only
+    the values of its group). Returns o [B, H, T, d], lse [B, H, T]."""
+    q = _as64(q)
+    k = _as64(k)
+    v = _as64(v)
+    B, H, T, d = q.shape
+    Hkv = k.shape[1]
+    assert H % Hkv == 0, "the query heads must split evenly over the key/value heads"
+    g = H // Hkv
+    a = _as64(a)
+    r = _as64(r)
+    o = np.empty((B, H, T, d))
+    lse = np.empty((B, H, T))
+
+    def one(bh):
+        b, h = bh
+        o[b, h], lse[b, h] = head_fwd(q[b, h], k[b, h // g], v[b, h // g], a[h], r[h], bool(frozen[h]))
+
+    _map(one, [(b, h) for b in range(B) for h in range(H)], threads)
+    return o, lse
+
+
+def gqa_bwd(q, k, v, do, a, r, frozen, threads=1):
+    """Layer backward of gqa_fwd. Returns dq [B, H, T, d] (zero for frozen
+    heads) and dk, dv [B, Hkv, T, d]: a shared head's gradient is the sum of
+    what each query head of its group sends it (frozen heads send dV only)."""
+    q = _as64(q)
+    k = _as64(k)
+    v = _as64(v)
+    do = _as64(do)
+    B, H, T, d = q.shape
+    Hkv = k.shape[1]
+    assert H % Hkv == 0, "the query heads must split evenly over the key/value heads"
+    g = H // Hkv
+    a = _as64(a)
+    r = _as64(r)
+    dq = np.empty((B, H, T, d))
+    parts = [[None] * H for _ in range(B)]
+
+    def one(bh):
+        b, h = bh
+        dq[b, h], dkh, dvh = head_bwd(q[b, h], k[b, h // g], v[b, h // g], do[b, h], a[h], r[h], bool(frozen[h]))
+        parts[b][h] = (dkh, dvh)
+
+    _map(one, [(b, h) for b in range(B) for h in range(H)], threads)
+    dk = np.zeros((B, Hkv, T, d))
+    dv = np.zeros((B, Hkv, T, d))
+    for b in range(B):
+        for h in range(H):
+            dk[b, h // g] += parts[b][h][0]
+            dv[b, h // g] += parts[b][h][1]
+    return dq, dk, dv

@@ -494,6 +494,53 @@ def test_fit_rejects_a_pattern_outside_the_family():
     assert oracle.fit_kl(P, a, r) > oracle.FIT_TOL
 
 
+# ---------------------------------------------------------------------------
+# Grouped-query layout
+# ---------------------------------------------------------------------------
+
+def _gqa_case(B, H, Hkv, T, d, seed):
+    g = _rng(seed)
+    q = g.normal(size=(B, H, T, d))
+    k, v = (g.normal(size=(B, Hkv, T, d)) for _ in range(2))
+    do = g.normal(size=(B, H, T, d))
+    a = g.normal(size=(H, T))
+    r = -0.1 * np.arange(T) + 0.3 * g.normal(size=(H, T))
+    return q, k, v, do, a, r
+
+
+def test_gqa_equals_mha_on_repeated_heads():
+    # grouped-query attention is multi-head attention whose key/value heads are
+    # repeated over each group; shared-head gradients are the group sums
+    B, H, Hkv, T, d = 2, 6, 2, 19, 4
+    q, k, v, do, a, r = _gqa_case(B, H, Hkv, T, d, 80)
+    frozen = [0, 1, 0, 0, 1, 1]
+    rep = lambda x: np.repeat(x, H // Hkv, axis=1)   # noqa: E731
+    o, lse = oracle.gqa_fwd(q, k, v, a, r, frozen)
+    o_m, lse_m = oracle.attn_fwd(q, rep(k), rep(v), a, r, frozen)
+    assert np.array_equal(o, o_m) and np.array_equal(lse, lse_m)
+    dq, dk, dv = oracle.gqa_bwd(q, k, v, do, a, r, frozen)
+    dq_m, dk_m, dv_m = oracle.attn_bwd(q, rep(k), rep(v), do, a, r, frozen)
+    assert np.array_equal(dq, dq_m)
+    grp = lambda x: x.reshape(B, Hkv, H // Hkv, T, d).sum(axis=2)   # noqa: E731
+    assert np.max(np.abs(dk - grp(dk_m))) < 1e-12 and np.max(np.abs(dv - grp(dv_m))) < 1e-12
+
+
+def test_gqa_finite_differences():
+    B, H, Hkv, T, d = 1, 4, 2, 7, 3
+    q, k, v, G, a, r = _gqa_case(B, H, Hkv, T, d, 81)
+    frozen = [0, 1, 1, 0]
+
+    def loss(kk, vv):
+        o, _ = oracle.gqa_fwd(q, kk, vv, a, r, frozen)
+        return float(np.sum(o * G))
+
+    _, dk, dv = oracle.gqa_bwd(q, k, v, G, a, r, frozen)
+    nk = _fd_grad(lambda x: loss(x, v), k)
+    nv = _fd_grad(lambda x: loss(k, x), v)
+    assert np.max(np.abs(dk - nk)) / np.max(np.abs(nk)) < 1e-6
+    assert np.max(np.abs(dv - nv)) / np.max(np.abs(nv)) < 1e-6
+
+
 def test_frozen_head_ignores_nan_qk():
     B, H, T, d = 1, 2, 12, 4
     g = _rng(50)

@@ -45,6 +45,9 @@ MUTATIONS = {
     "fit_grad_no_T": ("return (fa - eta_abs) / T, (fr - eta_rel) / T", "return (fa - eta_abs), (fr - eta_rel) / T"),
     # fitting: Eq. 4 with the relative term's sign flipped
     "fit_loss_sign": ("- np.dot(eta_rel, r)) / T", "+ np.dot(eta_rel, r)) / T"),
+    # grouped-query layout: query head mapped to its key/value head by h % g instead of h // g
+    "gqa_head_map": ("head_fwd(q[b, h], k[b, h // g], v[b, h // g], a[h], r[h], bool(frozen[h]))",
+                     "head_fwd(q[b, h], k[b, h % Hkv], v[b, h % Hkv], a[h], r[h], bool(frozen[h]))"),
     # lse: forgot the max shift
     "lse_no_max": ("return m + np.log(np.sum(np.exp(L - m[:, None]), axis=1))",
                    "return np.log(np.sum(np.exp(L - m[:, None]), axis=1))"),
