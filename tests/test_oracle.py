@@ -494,6 +494,55 @@ def test_fit_rejects_a_pattern_outside_the_family():
     assert oracle.fit_kl(P, a, r) > oracle.FIT_TOL
 
 
+def test_fit_start_point_closed_form():
+    # App. C.1 starts the fit at a = 0 and r(delta) = log(eta_rel(delta) / (T - delta)):
+    # the mean weight on diagonal delta, which holds T - delta entries. For the
+    # uniform causal target P(i, j) = 1 / (i + 1), diagonal delta holds
+    # 1 / (delta + 1), ..., 1 / T, so eta_rel(delta) = H_T - H_delta (harmonic
+    # numbers) and column j sums to H_T - H_j as well; both are computed here in
+    # exact rationals, without the oracle's marginals
+    T = 20
+    harm = [Fraction(0)]
+    for n in range(1, T + 1):
+        harm.append(harm[-1] + Fraction(1, n))
+    eta = np.array([float(harm[T] - harm[t]) for t in range(T)])
+    r_want = np.array([math.log(float((harm[T] - harm[t]) / (T - t))) for t in range(T)])
+    a, r = oracle.fit_compact(eta, eta, steps=0)
+    assert np.all(a == 0.0)
+    assert np.max(np.abs(r - r_want)) < 1e-12
+    # a diagonal with no mass starts at the 1e-9 floor instead of log 0
+    eta0 = eta.copy()
+    eta0[T - 1] = 0.0
+    _, r0 = oracle.fit_compact(eta, eta0, steps=0)
+    assert r0[T - 1] == math.log(1e-9) and np.array_equal(r0[:T - 1], r[:T - 1])
+
+
+def test_fit_first_adam_steps():
+    # Adam with bias-corrected moments (Kingma and Ba; beta = 0.9, 0.999, eps 1e-8):
+    # after one step m_hat = g and v_hat = g^2, so every coordinate moves by
+    # lr |g| / (|g| + eps), about lr, against the sign of its gradient; the second
+    # step is lr m2 / (sqrt(v2) + eps) with m2 = (0.09 g1 + 0.1 g2) / (1 - 0.9^2) and
+    # v2 = (0.000999 g1^2 + 0.001 g2^2) / (1 - 0.999^2), the moments written out by hand
+    T = 12
+    _, _, P = _family_target(T, 78)
+    ea, er = oracle.target_marginals(P)
+    lr, eps = 0.05, 1e-8
+    x0 = oracle.fit_compact(ea, er, steps=0)
+    x1 = oracle.fit_compact(ea, er, steps=1)
+    x2 = oracle.fit_compact(ea, er, steps=2)
+    g1 = oracle.fit_grad(x0[0], x0[1], ea, er)
+    g2 = oracle.fit_grad(x1[0], x1[1], ea, er)
+    for k in range(2):
+        step1 = x1[k] - x0[k]
+        assert np.max(np.abs(step1 + lr * g1[k] / (np.abs(g1[k]) + eps))) < 1e-13
+        moved = np.abs(g1[k]) > 1e-5
+        assert moved.sum() >= T // 2
+        assert np.max(np.abs(np.abs(step1[moved]) - lr)) < 1e-3 * lr
+        m2 = (0.9 * 0.1 * g1[k] + 0.1 * g2[k]) / (1 - 0.9 ** 2)
+        v2 = (0.999 * 0.001 * g1[k] ** 2 + 0.001 * g2[k] ** 2) / (1 - 0.999 ** 2)
+        assert np.max(np.abs((x2[k] - x1[k]) + lr * m2 / (np.sqrt(v2) + eps))) < 1e-13
+
+
 # ---------------------------------------------------------------------------
 # Grouped-query layout
 # ---------------------------------------------------------------------------
