@@ -97,8 +97,8 @@ SAF_API size_t saf_attn_workspace_bytes(int B, int H, int T, int d, saf_dtype_t 
  *      frozen rows log Z(i). saf_attn_bwd consumes lse.
  * The normalisers log Z of the frozen heads are computed here ("precomputed
  * normalisers", §3.3), once per head, independent of the batch.
- * Supported: d == 64; dt SAF_BF16 (tensor cores, fp32 accumulation) or
- * SAF_FP32 (fp32 arithmetic throughout). */
+ * Supported: d == 64 for SAF_BF16 (tensor cores, fp32 accumulation);
+ * d in {64, 96, 128} for SAF_FP32 (fp32 arithmetic throughout, CUDA cores). */
 SAF_API int saf_attn_fwd(const void* q, const void* k, const void* v,
                  const float* a, const float* r, int ld_prior, const uint8_t* frozen,
                  int B, int H, int T, int d, saf_dtype_t dt,
@@ -124,7 +124,11 @@ SAF_API int saf_attn_fwd(const void* q, const void* k, const void* v,
  *    larger problems return SAF_ESCRATCH and enqueue nothing.
  *  - Set-up: the first call on each device looks up the array's device
  *    address (cudaGetSymbolAddress, with that device current) and caches
- *    it. Make that first call before any stream capture begins.
+ *    it. Make that first call before any stream capture begins. The cached
+ *    address belongs to the device's primary context: after
+ *    cudaDeviceReset (or anything else that ends that context) it is stale,
+ *    so a process that resets a device must not call this entry point on
+ *    that device again.
  *  - Sharing: every call on a device uses the same array, which keeps the
  *    contents the last call left. Each call's first kernel clears the parts
  *    that must start at zero before anything reads them. Calls whose work overlaps on the
@@ -143,7 +147,8 @@ SAF_API int saf_attn_fwd_noalloc(const void* q, const void* k, const void* v,
  *      same inputs; a, r, frozen as in saf_attn_fwd.
  * Out: dq, dk, dv [B,H,T,d] (dt). Ordinary heads: the gradient of Eqs. 5-7.
  *      Frozen heads: dv = W^T dO; dq and dk are written as exact zeros
- *      (§3.3, App. D.2). */
+ *      (§3.3, App. D.2).
+ * Supported: d == 64 for SAF_BF16; d in {64, 96, 128} for SAF_FP32. */
 SAF_API int saf_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
                  const float* lse, const float* a, const float* r, int ld_prior,
                  const uint8_t* frozen, int B, int H, int T, int d, saf_dtype_t dt,

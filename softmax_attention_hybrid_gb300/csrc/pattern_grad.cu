@@ -145,15 +145,13 @@ extern "C" int saf_pattern_grad(const void* v, const void* dO, const void* o, co
         }
     cudaStream_t s = (cudaStream_t)stream;
     if (T == 0) return SAF_OK;
-    if (cudaMemsetAsync(da, 0, (size_t)H * T * sizeof(float), s) != cudaSuccess ||
-        cudaMemsetAsync(dr, 0, (size_t)H * T * sizeof(float), s) != cudaSuccess) {
-        cudaGetLastError();
-        return SAF_ELAUNCH;
+    // every argument and the device are checked before the first work is enqueued
+    const bool work = B > 0 && F > 0;
+    if (work) {
+        if (!v || !dO || !o || !lse || !a || !r || ld_prior < T) return SAF_EINVAL;
+        if (((uintptr_t)v | (uintptr_t)dO | (uintptr_t)o | (uintptr_t)lse) & 15u) return SAF_EALIGN;
+        if (((uintptr_t)a | (uintptr_t)r) & 3u) return SAF_EALIGN;
     }
-    if (B == 0 || F == 0) return SAF_OK;
-    if (!v || !dO || !o || !lse || !a || !r || ld_prior < T) return SAF_EINVAL;
-    if (((uintptr_t)v | (uintptr_t)dO | (uintptr_t)o | (uintptr_t)lse) & 15u) return SAF_EALIGN;
-    if (((uintptr_t)a | (uintptr_t)r) & 3u) return SAF_EALIGN;
     int dev = 0;
     cudaDeviceProp prop;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
@@ -161,6 +159,12 @@ extern "C" int saf_pattern_grad(const void* v, const void* dO, const void* o, co
         return SAF_ECUDA;
     }
     if (!(prop.major == 10 && prop.minor == 3)) return SAF_EUNSUPPORTED;
+    if (cudaMemsetAsync(da, 0, (size_t)H * T * sizeof(float), s) != cudaSuccess ||
+        cudaMemsetAsync(dr, 0, (size_t)H * T * sizeof(float), s) != cudaSuccess) {
+        cudaGetLastError();
+        return SAF_ELAUNCH;
+    }
+    if (!work) return SAF_OK;
     const int ntq = (T + kPgTile - 1) / kPgTile;
     const dim3 grid((unsigned)(ntq * (ntq + 1) / 2), (unsigned)F, (unsigned)B);
     note_launch();

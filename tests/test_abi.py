@@ -156,9 +156,11 @@ def test_pattern_grad_argument_errors(saf):
     F = FAKE
 
     def pg(**kw):
-        a = dict(v=F, do=F, o=F, lse=F, a=F, r=F, ld=256, B=1, H=4, T=256, d=64, dt=0, da=F, dr=F)
+        a = dict(v=F, do=F, o=F, lse=F, a=F, r=F, ld=256, B=1, H=4, T=256, d=64, dt=0, da=F, dr=F, frozen=None)
         a.update(kw)
-        return lib.saf_pattern_grad(a["v"], a["do"], a["o"], a["lse"], a["a"], a["r"], a["ld"], None, a["B"],
+        fz = a["frozen"]
+        fzp = (ctypes.c_uint8 * len(fz))(*fz) if fz is not None else None
+        return lib.saf_pattern_grad(a["v"], a["do"], a["o"], a["lse"], a["a"], a["r"], a["ld"], fzp, a["B"],
                                     a["H"], a["T"], a["d"], a["dt"], a["da"], a["dr"], None)
 
     assert pg(H=0) == saf.SAF_EINVAL
@@ -167,3 +169,11 @@ def test_pattern_grad_argument_errors(saf):
     assert pg(da=None) == saf.SAF_EINVAL
     assert pg(dr=F + 1) == saf.SAF_EALIGN
     assert pg(T=0) == saf.SAF_OK
+    # with a frozen head there is work to do: the remaining arguments are checked
+    # before anything is enqueued (da and dr are cleared on the stream only after
+    # every check), so these return their own error, not a device error
+    fz = [0, 1, 0, 0]
+    assert pg(frozen=fz, v=None) == saf.SAF_EINVAL
+    assert pg(frozen=fz, ld=255) == saf.SAF_EINVAL
+    assert pg(frozen=fz, lse=F + 4) == saf.SAF_EALIGN
+    assert pg(frozen=fz, a=F + 2) == saf.SAF_EALIGN
