@@ -10,6 +10,19 @@ heads frozen (B=8, H=12 with heads 3, 7, 11 frozen, T=4096, d=64, bf16).
 Prints one JSON line (rank 0). Under torchrun each rank runs its own batch of
 the same workload (weak scaling, no collective on the data path); the time
 is the max over ranks and the value the work of all ranks over that time.
+`--gpus N` without torchrun starts the N ranks itself (torchrun on 127.0.0.1).
+
+Besides the headline workload, the line carries `other_workloads`: the other
+bench workloads of the same layer (50% frozen, the 1B-shaped layer at 8K, the
+16K prefill), each timed in the same run with its all-ordinary comparison.
+
+    python bench.py --workload W --record-traffic ncu.csv
+
+stores the DRAM bytes per launch of fwd_tc_kernel / bwd_tc_kernel from an ncu
+capture (`--metrics dram__bytes_read.sum,dram__bytes_write.sum --csv`) in
+profiles/traffic.json, keyed by the hash of the kernel's sources at the time
+of recording; the bench line reports `roofline.traffic` only for a key that
+matches the sources it runs.
 """
 from __future__ import annotations
 
@@ -34,6 +47,8 @@ from softmax_attention_hybrid_gb300.inputs import WORKLOADS, make_inputs, Worklo
 
 METRIC = "hybrid attention fwd+bwd TFLOP/s and tokens/s at 1 GB300; % of bf16 tensor peak"
 DEFAULT_WORKLOAD = "gpt2_124m_25"
+# timed after the headline workload in the same run, each with its all-ordinary run
+OTHER_WORKLOADS = ("gpt2_124m_50", "1b_25", "prefill_16k")
 L2_FLUSH_BYTES = 256 << 20  # larger than the 129 MB L2
 
 
@@ -265,36 +280,41 @@ def e2e_chunk_sizes(B, spec=""):
     return sizes
 
 
-def run_ours(args, w):
-    rank, world, local = dist_info()
-    torch.cuda.set_device(local)
-    dist_init(world, "nccl")
-    dev = torch.device("cuda", local)
-    from softmax_attention_hybrid_gb300 import saf
+class Layer:
+    """Device buffers of one workload and one step of the layer through the C ABI."""
 
-    x = make_inputs(w, seed=rank)
-    frozen = x["frozen"]
-    g = {n: x[n].to(dev) for n in ("q", "k", "v", "do", "a", "r")}
-    B, H, T, d = w.B, w.H, w.T, w.d
-    o = torch.empty_like(g["v"])
-    lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
-    dq, dk, dv = (torch.empty_like(g["v"]) for _ in range(3))
-    ws = saf.alloc_workspace(B, H, T, d, g["v"].dtype, True, dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream()
-
-    def step(mask):
-        saf.saf_attn_fwd(g["q"], g["k"], g["v"], g["a"], g["r"], mask, o=o, lse=lse, workspace=ws)
+    def __init__(self, saf, w: Workload, seed, dev):
+        self.saf, self.w = saf, w
+        self.x = make_inputs(w, seed=seed)
+        self.frozen = self.x["frozen"]
+        self.g = {n: self.x[n].to(dev) for n in ("q", "k", "v", "do", "a", "r")}
+        B, H, T, d = w.B, w.H, w.T, w.d
+        self.o = torch.empty_like(self.g["v"])
+        self.lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+        self.dq, self.dk, self.dv = (torch.empty_like(self.g["v"]) for _ in range(3))
+        self.ws = saf.alloc_workspace(B, H, T, d, self.g["v"].dtype, not w.fwd_only, dev)
+        self.kernels = {"fwd": saf.SAF_KERNEL_FWD, "lognorm": saf.SAF_KERNEL_LOGNORM,
+                        "pattern_prep": saf.SAF_KERNEL_PATTERN_PREP}
         if not w.fwd_only:
-            saf.saf_attn_bwd(g["q"], g["k"], g["v"], o, g["do"], lse, g["a"], g["r"], mask, dq=dq, dk=dk, dv=dv,
-                             workspace=ws)
+            self.kernels.update({"bwd_kv": saf.SAF_KERNEL_BWD_KV, "bwd_q": saf.SAF_KERNEL_BWD_Q,
+                                 "bwd": saf.SAF_KERNEL_BWD, "dq_finish": saf.SAF_KERNEL_DQ_FINISH,
+                                 "bwd_delta": saf.SAF_KERNEL_BWD_DELTA})
 
-    kernels = {"fwd": saf.SAF_KERNEL_FWD, "lognorm": saf.SAF_KERNEL_LOGNORM,
-               "pattern_prep": saf.SAF_KERNEL_PATTERN_PREP}
-    if not w.fwd_only:
-        kernels.update({"bwd_kv": saf.SAF_KERNEL_BWD_KV, "bwd_q": saf.SAF_KERNEL_BWD_Q, "bwd": saf.SAF_KERNEL_BWD,
-                        "dq_finish": saf.SAF_KERNEL_DQ_FINISH, "bwd_delta": saf.SAF_KERNEL_BWD_DELTA})
+    def step(self, mask):
+        saf, g = self.saf, self.g
+        saf.saf_attn_fwd(g["q"], g["k"], g["v"], g["a"], g["r"], mask, o=self.o, lse=self.lse, workspace=self.ws)
+        if not self.w.fwd_only:
+            saf.saf_attn_bwd(g["q"], g["k"], g["v"], self.o, g["do"], self.lse, g["a"], g["r"], mask, dq=self.dq,
+                             dk=self.dk, dv=self.dv, workspace=self.ws)
 
+
+def timed(saf, lay, mask, K, trace, flush, stream, world):
+    """K steps, each after an L2 flush, bracketed by CUDA events on the launching
+    stream. trace: the kernel brackets that get their own events. Events between
+    two launches cost a little time and stop the next launch from starting early,
+    so the headline run brackets the dominant kernel alone and a separate run
+    brackets every kernel for the per-kernel breakdown.
+    Returns (per-step ms, per-kernel mean ms, launches)."""
     def new_event():
         # torch creates the CUDA event on first record; record once so that
         # the handle handed to the library is a real event
@@ -302,55 +322,129 @@ def run_ours(args, w):
         ev.record(stream)
         return ev
 
-    def timed(mask, K, trace):
-        # trace: the kernel brackets that get CUDA events; the events between two
-        # launches cost a little time and stop the next launch from starting early,
-        # so the timed region brackets the dominant kernel alone and a separate run
-        # brackets every kernel for the per-kernel breakdown
-        evs = [(new_event(), new_event()) for _ in range(K)]
-        kev = {nm: [(new_event(), new_event()) for _ in range(K)] for nm in trace}
-        barrier(world)
-        torch.cuda.synchronize()
-        n0 = saf.saf_launch_count()
-        for i in range(K):
-            flush.fill_(float(i))
-            for nm in trace:
-                saf.saf_set_trace_events(kernels[nm], kev[nm][i][0], kev[nm][i][1])
-            evs[i][0].record(stream)
-            step(mask)
-            evs[i][1].record(stream)
-        torch.cuda.synchronize()
-        barrier(world)
-        saf.saf_set_trace_events(saf.SAF_KERNEL_NONE)
-        launches = saf.saf_launch_count() - n0
-        ms = [s.elapsed_time(e) for s, e in evs]
-        kms = {}
+    evs = [(new_event(), new_event()) for _ in range(K)]
+    kev = {nm: [(new_event(), new_event()) for _ in range(K)] for nm in trace}
+    barrier(world)
+    torch.cuda.synchronize()
+    n0 = saf.saf_launch_count()
+    for i in range(K):
+        flush.fill_(float(i))
         for nm in trace:
-            # a kernel this path never launches keeps the events' creation
-            # records, which precede the step's start event
-            if evs[0][0].elapsed_time(kev[nm][0][0]) < 0:
-                continue
-            vals = [s.elapsed_time(e) for s, e in kev[nm]]
-            kms[nm] = sum(vals) / len(vals)
-        return ms, kms, launches
+            saf.saf_set_trace_events(lay.kernels[nm], kev[nm][i][0], kev[nm][i][1])
+        evs[i][0].record(stream)
+        lay.step(mask)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    saf.saf_set_trace_events(saf.SAF_KERNEL_NONE)
+    launches = saf.saf_launch_count() - n0
+    ms = [s.elapsed_time(e) for s, e in evs]
+    kms = {}
+    for nm in trace:
+        # a kernel this path never launches keeps the events' creation
+        # records, which precede the step's start event
+        if evs[0][0].elapsed_time(kev[nm][0][0]) < 0:
+            continue
+        vals = [s.elapsed_time(e) for s, e in kev[nm]]
+        kms[nm] = sum(vals) / len(vals)
+    return ms, kms, launches
+
+
+def spread(ms):
+    return {"min": min(ms), "median": statistics.median(ms), "max": max(ms),
+            "stdev": statistics.pstdev(ms) if len(ms) > 1 else 0.0}
+
+
+def kernel_roofline(name, kms, w, peaks, peak_src):
+    """Achieved rate of kernel `name` (counted FLOP per launch / its mean launch time)."""
+    units_o, units_f = KERNEL_FLOP_UNITS[name]
+    c = 2 * F.pairs(w.T) * w.d
+    kflops = w.B * ((w.H - w.F) * units_o + w.F * units_f) * c
+    achieved = kflops / (kms[name] * 1e-3) / 1e12
+    if kernel_bound(name, w.dtype) == "tensor":
+        peak = peaks["bf16_tflops"]
+        bound, note = "tensor", f"bf16 dense, burst, {peak_src}"
+    else:
+        # fp32 FMA pipes: 152 SMs x 128 FMA/clk x 2 FLOP at the max SM clock
+        peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        bound, note = "alu", "fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x max SM clock (derived)"
+    return {"kernel": name, "bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "peak_source": note, "flops_per_launch": kflops, "ms_per_launch": kms[name]}
+
+
+def measure_workload(saf, w, args, dev, world, rank, stream, flush, peaks, peak_src):
+    """Hybrid and all-ordinary step times of one more workload (no end-to-end leg)."""
+    lay = Layer(saf, w, rank, dev)
+    for _ in range(args.warmup):
+        lay.step(lay.frozen)
+    torch.cuda.synchronize()
+    if saf.saf_device_status(lay.ws) != saf.SAF_OK:
+        raise RuntimeError(f"device status after warm-up ({w.name}) is not ok")
+    _, kms, _ = timed(saf, lay, lay.frozen, args.steps, list(lay.kernels), flush, stream, world)
+    dom = max(kms, key=kms.get)
+    ms, kms_dom, _ = timed(saf, lay, lay.frozen, args.steps, [dom], flush, stream, world)
+    step_ms = max_over_ranks(sum(ms) / len(ms), world, dev)
+    flops = F.layer_flops(w.B, w.H, w.F, w.T, w.d, backward=not w.fwd_only) * world
+    out = {"ms_per_step": step_ms, "ms_spread": spread(ms), "value": flops / (step_ms * 1e-3) / 1e12,
+           "unit": "TFLOP/s", "frac_of_bf16_peak": flops / world / (step_ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+           "tokens_per_s": w.B * w.T * world / (step_ms * 1e-3),
+           "config": {"B": w.B, "H": w.H, "F": w.F, "T": w.T, "d": w.d, "dtype": w.dtype,
+                      "fwd_only": w.fwd_only},
+           "roofline": kernel_roofline(dom, kms_dom, w, peaks, peak_src), "kernel_ms": kms}
+    if w.F > 0:
+        zero = [0] * w.H
+        for _ in range(max(1, args.warmup // 2)):
+            lay.step(zero)
+        ms0, _, _ = timed(saf, lay, zero, args.steps, [dom], flush, stream, world)
+        ao = max_over_ranks(sum(ms0) / len(ms0), world, dev)
+        out["all_ordinary"] = {"ms_per_step": ao, "speedup": ao / step_ms,
+                               "ideal_speedup": F.layer_flops(w.B, w.H, 0, w.T, w.d, not w.fwd_only) /
+                               F.layer_flops(w.B, w.H, w.F, w.T, w.d, not w.fwd_only)}
+    del lay
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args, w):
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    dist_init(world, "nccl")
+    dev = torch.device("cuda", local)
+    from softmax_attention_hybrid_gb300 import saf
+
+    lay = Layer(saf, w, rank, dev)
+    x, frozen, g = lay.x, lay.frozen, lay.g
+    B, H, T, d = w.B, w.H, w.T, w.d
+    o, lse, dq, dk, dv, ws = lay.o, lay.lse, lay.dq, lay.dk, lay.dv, lay.ws
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    peaks, peak_src = _peaks()
 
     for _ in range(args.warmup):
-        step(frozen)
+        lay.step(frozen)
     torch.cuda.synchronize()
     status = saf.saf_device_status(ws)
     if status != saf.SAF_OK:
         raise RuntimeError(f"device status after warm-up: {saf.saf_error_string(status)}")
 
     # per-kernel breakdown (every bracket traced), which also names the dominant kernel
-    _, kms, _ = timed(frozen, args.steps, list(kernels))
+    _, kms, _ = timed(saf, lay, frozen, args.steps, list(lay.kernels), flush, stream, world)
     dom = max(kms, key=kms.get)
 
+    # the clock sampler runs through a soak of the same step (about 1 s, so that it
+    # collects samples under load) and then through the timed region
     clocks = ClockSampler(local)
     clocks.start()
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < args.soak_s:
+        for _ in range(20):
+            lay.step(frozen)
+        torch.cuda.synchronize()
     t_wall0 = time.perf_counter()
-    ms, kms_dom, launches = timed(frozen, args.steps, [dom])
+    ms, kms_dom, launches = timed(saf, lay, frozen, args.steps, [dom], flush, stream, world)
     t_wall = time.perf_counter() - t_wall0
     clk = clocks.stop()
+    clk["window"] = f"{args.soak_s:.1f} s soak of the same step, then the timed region"
 
     step_ms = max_over_ranks(sum(ms) / len(ms), world, dev)
     total_flops = F.layer_flops(B, H, w.F, T, d, backward=not w.fwd_only) * world
@@ -361,10 +455,10 @@ def run_ours(args, w):
     allord = None
     if args.all_ordinary and w.F > 0:
         for _ in range(max(1, args.warmup // 2)):
-            step([0] * H)
+            lay.step([0] * H)
         # traced like the hybrid run, so that both carry the same event overhead
-        ms0, _, _ = timed([0] * H, args.steps, [dom])
-        _, kms0, _ = timed([0] * H, args.steps, list(kernels))
+        ms0, _, _ = timed(saf, lay, [0] * H, args.steps, [dom], flush, stream, world)
+        _, kms0, _ = timed(saf, lay, [0] * H, args.steps, list(lay.kernels), flush, stream, world)
         ao_ms = max_over_ranks(sum(ms0) / len(ms0), world, dev)
         allord = {"ms_per_step": ao_ms, "speedup": ao_ms / step_ms,
                   "ideal_speedup": F.layer_flops(B, H, 0, T, d, not w.fwd_only) /
@@ -442,37 +536,27 @@ def run_ours(args, w):
         e2e = {"value": total_flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "chunks": sizes}
 
+    # the other workloads of the same layer, timed in the same run (not the headline)
+    others = None
+    if args.other_workloads:
+        del lay, g, o, lse, dq, dk, dv, ws
+        torch.cuda.empty_cache()
+        others = {}
+        for name in OTHER_WORKLOADS:
+            if name != w.name:
+                others[name] = measure_workload(saf, WORKLOADS[name], args, dev, world, rank, stream, flush,
+                                                peaks, peak_src)
+
     if rank != 0:
         return 0
 
-    peaks, peak_src = _peaks()
     # dominant kernel: the longest kernel of the step, timed by its own events
     # inside the timed region
     roofline = None
     if dom in kms_dom:
-        name = dom
-        units_o, units_f = KERNEL_FLOP_UNITS[name]
-        c = 2 * F.pairs(T) * d
-        kflops = B * ((H - w.F) * units_o + w.F * units_f) * c
-        achieved = kflops / (kms_dom[name] * 1e-3) / 1e12
-        if kernel_bound(name, w.dtype) == "tensor":
-            peak = peaks["bf16_tflops"]
-            bound, note = "tensor", f"bf16 dense, burst, {peak_src}"
-        else:
-            # fp32 FMA pipes: 152 SMs x 128 FMA/clk x 2 FLOP at the max SM clock
-            peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
-            bound, note = "alu", "fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x max SM clock (derived)"
-        traffic = None
-        tpath = os.path.join(ROOT, "profiles", "traffic.json")
-        if os.path.exists(tpath):
-            with open(tpath) as f:
-                tt = json.load(f)
-            ent = tt.get(f"{name}|{w.name}|{_src_hash(name)}")
-            traffic = ent if ent is not None else None
-        roofline = {"kernel": name, "bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "traffic": traffic, "peak_source": note,
-                    "flops_per_launch": kflops, "ms_per_launch": kms_dom[name],
-                    "kernel_ms": kms}
+        roofline = kernel_roofline(dom, kms_dom, w, peaks, peak_src)
+        roofline["traffic"] = traffic_for(dom, w.name)
+        roofline["kernel_ms"] = kms
 
     cpu = None
     if args.cpu_baseline and world == 1:
@@ -493,10 +577,12 @@ def run_ours(args, w):
                    "parallelism": f"replicas x{world}, one batch per GPU"},
         "tokens_per_s": tokens,
         "frac_of_bf16_peak": value / world / peaks["bf16_tflops"],
+        "ms_spread": spread(ms),
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "all_ordinary": allord,
+        "other_workloads": others,
         "gpu_launches": launches,
         "clocks": clk,
         "wall_s_timed_region": t_wall,
@@ -505,6 +591,72 @@ def run_ours(args, w):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+# ---------------------------------------------------------------------------
+# DRAM traffic of the dominant kernels, from an ncu capture
+# ---------------------------------------------------------------------------
+
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
+NCU_KERNELS = {"fwd_tc_kernel": "fwd", "bwd_tc_kernel": "bwd"}
+
+
+def traffic_for(kernel, workload):
+    """DRAM bytes per launch of `kernel` at `workload`, if a capture was taken on
+    the current sources of that kernel (else None)."""
+    if not os.path.exists(TRAFFIC_PATH):
+        return None
+    with open(TRAFFIC_PATH) as f:
+        tt = json.load(f)
+    return tt.get(f"{kernel}|{workload}|{_src_hash(kernel)}")
+
+
+def record_traffic(csv_path, workload, out_path):
+    """Read an ncu CSV with dram__bytes_read.sum and dram__bytes_write.sum per
+    launch and store read + write bytes per launch of each tensor-core kernel,
+    keyed by kernel, workload and the hash of the kernel's sources as they are
+    now (run this where and when the capture ran, on the same sources)."""
+    import csv
+    scale = {"byte": 1.0, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9, "kibyte": 1024.0, "mibyte": 1024.0 ** 2,
+             "gibyte": 1024.0 ** 3}
+    with open(csv_path) as f:
+        lines = [ln for ln in f if ln.startswith('"')]
+    per = {}
+    for row in csv.DictReader(lines):
+        kname = row.get("Kernel Name", "")
+        short = next((v for k, v in NCU_KERNELS.items() if k in kname), None)
+        metric = row.get("Metric Name", "")
+        if short is None or metric not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        val = float(row["Metric Value"].replace(",", "")) * scale[row.get("Metric Unit", "byte").lower()]
+        per.setdefault(short, {}).setdefault(row["ID"], 0.0)
+        per[short][row["ID"]] += val
+    tt = {}
+    if os.path.exists(out_path):
+        with open(out_path) as f:
+            tt = json.load(f)
+    # drop entries of sources that no longer exist
+    tt = {k: v for k, v in tt.items() if k.rsplit("|", 1)[-1] == _src_hash(k.split("|", 1)[0])}
+    for short, launches in per.items():
+        vals = list(launches.values())
+        tt[f"{short}|{workload}|{_src_hash(short)}"] = sum(vals) / len(vals)
+    os.makedirs(os.path.dirname(out_path), exist_ok=True)
+    with open(out_path, "w") as f:
+        json.dump(tt, f, indent=1, sort_keys=True)
+    print(json.dumps({"recorded": {s: len(v) for s, v in per.items()}, "workload": workload, "out": out_path}))
+    return 0 if per else 1
+
+
+def spawn_ranks(args):
+    """`--gpus N` without a torchrun environment: start N local ranks the way the
+    driver does (torchrun, one process per GPU, rendezvous on 127.0.0.1)."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+           "--master-addr=127.0.0.1", f"--master-port={port}", os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.call(cmd)
 
 
 def main():
@@ -519,9 +671,24 @@ def main():
     ap.add_argument("--no-all-ordinary", dest="all_ordinary", action="store_false")
     ap.add_argument("--e2e-chunks", default="",
                     help="batch entries per chunk of the end-to-end step, e.g. 2,2,2,2 (default: by batch size)")
+    ap.add_argument("--no-other-workloads", dest="other_workloads", action="store_false",
+                    help="time only the named workload (by default the other bench workloads are timed too)")
+    ap.add_argument("--soak-s", type=float, default=1.0,
+                    help="seconds of untimed steps under the clock sampler before the timed region")
+    ap.add_argument("--record-traffic", metavar="NCU_CSV",
+                    help="store the DRAM bytes of an ncu capture (--csv, dram__bytes_read/write.sum) of --workload")
+    ap.add_argument("--traffic-out", default=TRAFFIC_PATH)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     w = WORKLOADS[args.workload]
+    if args.record_traffic:
+        return record_traffic(args.record_traffic, w.name, args.traffic_out)
+    rank, world, _ = dist_info()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        return spawn_ranks(args)
+    if "WORLD_SIZE" in os.environ and world != args.gpus:
+        print(json.dumps({"error": f"--gpus {args.gpus} but WORLD_SIZE={world}"}), flush=True)
+        return 2
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

@@ -7,12 +7,16 @@ Frozen heads must give bitwise-zero dq and dk ("When Can Attention Heads Be
 Statically Defined?", §3.3 and App. D.2), and their lse rows (log Z) are the
 same for every batch entry.
 """
+import concurrent.futures as cf
+import os
+
 import numpy as np
 import pytest
 import torch
 
 import oracle
 from softmax_attention_hybrid_gb300.inputs import WORKLOADS, custom_workload, make_inputs
+from tests import _parity_log
 
 pytestmark = pytest.mark.gpu
 
@@ -43,7 +47,24 @@ def _np(x):
     return x.double().cpu().numpy()
 
 
-def _check_full(saf, w, seed=0, T_prior=None, poison=False, backward=True):
+def _floor(ref, dtype):
+    """Half a unit in the last place of the largest |ref| in the output dtype: the
+    error of the correctly rounded result."""
+    m = float(np.max(np.abs(ref))) if np.size(ref) else 0.0
+    if m == 0.0:
+        return 0.0
+    return 2.0 ** (np.floor(np.log2(m)) - (8 if dtype == "bf16" else 24))
+
+
+def _threads():
+    try:
+        n = len(os.sched_getaffinity(0))
+    except Exception:
+        n = os.cpu_count() or 1
+    return max(1, min(12, n))
+
+
+def _check_full(saf, w, seed=0, T_prior=None, poison=False, backward=True, case=None):
     x = make_inputs(w, seed=seed, T_prior=T_prior)
     fz = [h for h in range(w.H) if x["frozen"][h]]
     if poison and fz:
@@ -53,32 +74,41 @@ def _check_full(saf, w, seed=0, T_prior=None, poison=False, backward=True):
     q, k, v, do = (x[n].double().numpy() for n in ("q", "k", "v", "do"))
     a, r = x["a"].double().numpy(), x["r"].double().numpy()
     tol_o, tol_g = TOL[w.dtype]
-    o_ref, lse_ref = oracle.attn_fwd(q, k, v, a, r, x["frozen"], threads=8)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, a, r, x["frozen"], threads=_threads())
     err = {"o": np.max(np.abs(_np(out["o"]) - o_ref)), "lse": np.max(np.abs(_np(out["lse"]) - lse_ref))}
-    assert err["o"] <= tol_o and err["lse"] <= tol_o, err
+    tols = {"o": tol_o, "lse": tol_o}
+    floors = {"o": _floor(o_ref, w.dtype)}
     if backward:
-        dq, dk, dv = oracle.attn_bwd(q, k, v, do, a, r, x["frozen"], threads=8)
+        dq, dk, dv = oracle.attn_bwd(q, k, v, do, a, r, x["frozen"], threads=_threads())
         for name, ref in (("dq", dq), ("dk", dk), ("dv", dv)):
             got = _np(out[name])
             assert np.all(np.isfinite(got)), name
             err[name] = np.max(np.abs(got - ref))
+            tols[name] = tol_g
+            floors[name] = _floor(ref, w.dtype)
+    if case:
+        _parity_log.record(case, err, tols, floors)
+    assert err["o"] <= tol_o and err["lse"] <= tol_o, err
+    for name in ("dq", "dk", "dv"):
+        if name in err:
             assert err[name] <= tol_g, (name, err)
+    if backward:
         for h in fz:
             assert torch.all(out["dq"][:, h] == 0) and torch.all(out["dk"][:, h] == 0)
     for h in fz:
         assert torch.equal(out["lse"][0, h], out["lse"][-1, h])
-    return err
+    return err, out, x
 
 
 def test_tiny_layer_fp32(saf):
-    _check_full(saf, WORKLOADS["tiny"])
+    _check_full(saf, WORKLOADS["tiny"], case="tiny (B1 H4 T256 fp32)")
 
 
 @pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 127, 128, 129, 255, 300])
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 def test_ragged_lengths(saf, T, dtype):
     w = custom_workload(2, 4, T, dtype=dtype, frozen=(1, 3), scale=0.5 if dtype == "bf16" else 1.0, slope=0.05)
-    _check_full(saf, w, seed=T)
+    _check_full(saf, w, seed=T, case=f"ragged T={T} {dtype}" if T in (1, 65, 129, 300) else None)
 
 
 @pytest.mark.parametrize("d", [96, 128])
@@ -209,25 +239,40 @@ def test_device_status_ok(saf):
 
 
 # ---------------------------------------------------------------------------
-# Full-size workloads, in the launch configuration the benchmark times:
-# every output of a few sampled (batch, head) slices against the oracle, and
-# properties of the whole output.
+# Full-size workloads, in the launch configuration the benchmark times.
+# The 124M-shaped layer at 25% frozen (fwd + bwd) and the 16K prefill (fwd)
+# are compared element by element on every (batch, head) slice. The 50% and
+# 1B-shaped layers share their kernels and launch sequence with the first;
+# there eight slices of every kind are compared element by element (the
+# whole-layer oracle would take several more minutes of host time), and the
+# whole output is checked for finiteness, exact frozen zeros and batch-
+# independent log Z.
 # ---------------------------------------------------------------------------
 
-def _sample_slices(w, frozen):
+@pytest.mark.parametrize("name", ["gpt2_124m_25", "prefill_16k"])
+def test_full_size_complete(saf, name):
+    w = WORKLOADS[name]
+    _check_full(saf, w, seed=0, backward=not w.fwd_only, case=f"{name} (every slice)")
+
+
+def _sample_slices(w, frozen, n_each=4):
     fz = [h for h in range(w.H) if frozen[h]]
     od = [h for h in range(w.H) if not frozen[h]]
     picks = []
-    if fz:
-        picks.append((0, fz[0]))
-        picks.append((w.B - 1, fz[-1]))
-    if od:
-        picks.append((w.B // 2, od[len(od) // 2]))
-        picks.append((w.B - 1, od[-1]))
+    rng = np.random.default_rng(w.B * 1000 + w.H)
+    for heads in (fz, od):
+        if heads:
+            cand = [(b, h) for b in range(w.B) for h in heads]
+            idx = rng.choice(len(cand), size=min(n_each, len(cand)), replace=False)
+            picks += [cand[i] for i in sorted(idx)]
+    # the first and the last slice of the layer always
+    for bh in ((0, 0), (w.B - 1, w.H - 1)):
+        if bh not in picks:
+            picks.append(bh)
     return picks
 
 
-@pytest.mark.parametrize("name", ["gpt2_124m_25", "gpt2_124m_50", "1b_25", "prefill_16k"])
+@pytest.mark.parametrize("name", ["gpt2_124m_50", "1b_25"])
 def test_full_size_sampled(saf, name):
     w = WORKLOADS[name]
     x = make_inputs(w, seed=0)
@@ -235,17 +280,26 @@ def test_full_size_sampled(saf, name):
     out = _run(saf, x, backward)
     tol_o, tol_g = TOL[w.dtype]
     a, r = x["a"].double().numpy(), x["r"].double().numpy()
-    for (b, h) in _sample_slices(w, x["frozen"]):
+    picks = _sample_slices(w, x["frozen"])
+
+    def one(bh):
+        b, h = bh
         fz = bool(x["frozen"][h])
         q, k, v, do = (x[n][b, h].double().numpy() for n in ("q", "k", "v", "do"))
-        o_ref, lse_ref = oracle.head_fwd(q, k, v, a[h], r[h], fz)
-        assert np.max(np.abs(_np(out["o"][b, h]) - o_ref)) <= tol_o, (b, h)
-        assert np.max(np.abs(_np(out["lse"][b, h]) - lse_ref)) <= tol_o, (b, h)
+        ref = dict(zip(("o", "lse"), oracle.head_fwd(q, k, v, a[h], r[h], fz)))
         if backward:
-            dq, dk, dv = oracle.head_bwd(q, k, v, do, a[h], r[h], fz)
-            for nm, ref in (("dq", dq), ("dk", dk), ("dv", dv)):
-                e = np.max(np.abs(_np(out[nm][b, h]) - ref))
-                assert e <= tol_g, (nm, b, h, e)
+            ref.update(zip(("dq", "dk", "dv"), oracle.head_bwd(q, k, v, do, a[h], r[h], fz)))
+        return bh, ref
+
+    err = {}
+    with cf.ThreadPoolExecutor(_threads()) as ex:
+        for (b, h), ref in ex.map(one, picks):
+            for nm, rv in ref.items():
+                e = float(np.max(np.abs(_np(out[nm][b, h]) - rv)))
+                err[nm] = max(err.get(nm, 0.0), e)
+                assert e <= (tol_o if nm in ("o", "lse") else tol_g), (nm, b, h, e)
+    _parity_log.record(f"{name} ({len(picks)} slices)", err,
+                       {nm: (tol_o if nm in ("o", "lse") else tol_g) for nm in err})
     for nm, t in out.items():
         assert torch.isfinite(t).all(), nm
     fzh = [h for h in range(w.H) if x["frozen"][h]]
