@@ -10,17 +10,19 @@
 //
 // Work item: (batch b, head h, query-block pair p) = query rows
 // [256p, 256p + 256) as two 128-row tiles that share every K/V tile load.
-// Items are numbered longest first (descending p, ordinary before frozen); the
-// producer of each persistent CTA takes the next number from a global counter
-// when its CTA is ready for more work and publishes it to the CTA's other warps
-// through a small ring in shared memory.
+// Items are numbered in groups of (batch, head) slices (ordinary slices before
+// frozen ones), longest first inside a group, so that a group's key and value
+// tiles stay in L2 while its query pairs re-read them; the producer of each
+// persistent CTA takes the next number from a global counter when its CTA is
+// ready for more work and publishes it to the CTA's other warps through a small
+// ring in shared memory.
 //
 // Warp roles (384 threads, one CTA per SM; warp 11 idles):
 //   warps 0-3 / 4-7 : softmax group g = 0 / 1, thread = one query row of tile g
 //   warp 8          : TMA producer (Q tiles, K/V stages)
-//   warps 9 / 10    : MMA issuers of tile 0 / 1 (one thread each; one thread
-//                     alone cannot issue tcgen05.mma fast enough to keep the
-//                     tensor core busy at N = 64); warp 9 owns tensor memory
+//   warps 9 / 10    : MMA issuers of tile 0 / 1 (the whole warp runs the issue
+//                     loop, one elected lane issues; two issuers keep the
+//                     tensor core fed at N = 64); warp 9 owns tensor memory
 // Tensor memory (512 columns), per tile g at column 256g:
 //   [0, 128)   S = Q K^T (fp32); frozen items: W of odd key blocks (bf16 pairs)
 //   [128, 192) P, or W of even key blocks (bf16 pairs), the A operand of P V
@@ -43,13 +45,18 @@ using namespace tc;
 
 constexpr int kStages = 3;   // 4 and 5 measured slower (likely: a larger shared-memory carve-out leaves less L1)
 constexpr int kRing = 4;   // work items published ahead by the producer
+// Items run in groups of slices whose key/value tiles stay in L2 together
+// (launch_tc_fwd picks the group size: all slices when their K and V fit in
+// kL2GroupBytes, else kSliceGroup slices).
+constexpr int kSliceGroup = 8;
+constexpr size_t kL2GroupBytes = 64ull << 20;
 constexpr int kTileBytes = 128 * 64 * 2;  // one 128 x 64 bf16 tile
 constexpr int kThreads = 384;   // 3 warpgroups: 2 softmax, 1 producer / issuers / idle
 // Register split (setmaxnreg): warpgroup 2 drops to kRegsOther registers per thread and
 // the softmax warpgroups rise to kRegsSoftmax. The launch gives every thread
 // kRegsLaunch (checked on the host); the split must not exceed that total:
 // 2 x 128 x kRegsSoftmax + 128 x kRegsOther <= 384 x kRegsLaunch.
-constexpr int kRegsLaunch = 168, kRegsSoftmax = 216, kRegsOther = 64;
+constexpr int kRegsLaunch = 168, kRegsSoftmax = 216, kRegsOther = 72;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther <= kThreads * kRegsLaunch, "register split too large");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kScaleLog2 = 0.125f * 1.4426950408889634f;  // log2(e) / sqrt(64)
@@ -71,6 +78,7 @@ struct FwdParams {
     uint32_t* status;
     int B, H, T, ld, Tp;
     int nqb, npairs, n_items;
+    int slice_group;   // (batch, head) slices per item group
     int n_ord, n_frz;
     uint8_t ord_heads[SAF_MAX_HEADS];
     uint8_t frz_heads[SAF_MAX_HEADS];
@@ -94,19 +102,30 @@ struct Item {
     bool frozen;
 };
 
+// Items are numbered group by group: the (batch, head) slices, ordinary before
+// frozen, form groups of p.slice_group consecutive slices, and inside a group the
+// query-block pairs go longest first, all slices of the group at one level before
+// the next. A group's key and value tiles are re-read by each of its pairs, and
+// they stay in L2 while the group runs. (With one group for all slices this is
+// longest first over the whole launch.)
 __device__ __forceinline__ Item decode_item(const FwdParams& p, int idx) {
     Item it;
-    const int per_level = p.B * p.H;
-    const int level = idx / per_level;
-    const int rem = idx - level * per_level;
+    const int n_slices = p.B * p.H;
+    const int G = p.slice_group;
+    const int per_group = G * p.npairs;
+    const int grp = idx / per_group;
+    const int gsize = min(G, n_slices - grp * G);
+    const int within = idx - grp * per_group;
+    const int level = within / gsize;
+    const int slice = grp * G + (within - level * gsize);
     it.pair = p.npairs - 1 - level;
     const int n_ord_items = p.B * p.n_ord;
-    if (rem < n_ord_items) {
-        it.b = rem / p.n_ord;
-        it.h = p.ord_heads[rem - it.b * p.n_ord];
+    if (slice < n_ord_items) {
+        it.b = slice / p.n_ord;
+        it.h = p.ord_heads[slice - it.b * p.n_ord];
         it.frozen = false;
     } else {
-        const int f = rem - n_ord_items;
+        const int f = slice - n_ord_items;
         it.b = f / p.n_frz;
         it.h = p.frz_heads[f - it.b * p.n_frz];
         it.frozen = true;
@@ -254,7 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         }
     } else if (warp == 9 || warp == 10) {
         // ------------------------------------------------------------ MMA issuer of tile g
-        if (lane == 0) {
+        // The whole warp runs the issue loop (warp-uniform descriptors); one elected lane
+        // issues each MMA and commit, lane 0 waits on barriers and arrives.
+        {
             const int g = warp - 9;
             const uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);  // S = Q K^T
             const uint32_t idesc_o = idesc_bf16(128, 64, 0, 1);   // O += P V, V MN-major
@@ -270,12 +291,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             uint32_t ring_full_bits = 0;
             int slot = 0;
             while (ok) {
-                if (!(ok = mbar_wait(&bars.item_full[slot], (ring_full_bits >> slot) & 1u, abort, status,
+                if (!(ok = mbar_wait_warp(&bars.item_full[slot], (ring_full_bits >> slot) & 1u, abort, status,
                                      kStatusTimeout)))
                     break;
                 ring_full_bits ^= 1u << slot;
                 const int idx = item_ring[slot];
-                mbar_arrive(&bars.item_empty[slot]);
+                if (lane == 0) mbar_arrive(&bars.item_empty[slot]);
                 slot = (slot + 1) % kRing;
                 if (idx < 0) break;
                 const Item it = decode_item(p, idx);
@@ -285,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 const int nblk = t1 ? qb1 + 1 : qb0 + 1;                 // key blocks of the item
                 if (!it.frozen) {
                     qs = nord++ & 1;
-                    if (!(ok = mbar_wait(&bars.q_full[qs], (q_full_bits >> qs) & 1u, abort, status, kStatusTimeout)))
+                    if (!(ok = mbar_wait_warp(&bars.q_full[qs], (q_full_bits >> qs) & 1u, abort, status, kStatusTimeout)))
                         break;
                     q_full_bits ^= 1u << qs;
                     d_q = sdesc_sw128(smem_u32(sm + SmemLayout::q + qs * SmemLayout::q_slot_bytes) + g * kTileBytes, 16,
@@ -294,15 +315,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 // stage index of block j is (stage + j) mod kStages
                 auto stage_of = [&](int j) { return (stage + j) % kStages; };
                 auto issue_s = [&](int j) -> bool {
-                    if (!mbar_wait(&bars.s_empty[g], s_empty_ph, abort, status, kStatusTimeout)) return false;
+                    if (!mbar_wait_warp(&bars.s_empty[g], s_empty_ph, abort, status, kStatusTimeout)) return false;
                     s_empty_ph ^= 1;
                     tc_fence_after();
                     const uint64_t d_k =
                         sdesc_sw128(smem_u32(sm + SmemLayout::kv + stage_of(j) * SmemLayout::stage_bytes), 16, 1024);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        mma_ss(d_s, sdesc_advance(d_q, 32 * k), sdesc_advance(d_k, 32 * k), idesc_s, k > 0);
-                    mma_commit(&bars.s_full[g]);
+                        mma_ss_warp(d_s, sdesc_advance(d_q, 32 * k), sdesc_advance(d_k, 32 * k), idesc_s, k > 0);
+                    mma_commit_warp(&bars.s_full[g]);
                     return true;
                 };
                 // frozen items alternate W between the P columns and the (unused) S columns
@@ -310,11 +331,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 auto issue_pv = [&](int j) -> bool {
                     if (frz) {   // one barrier per W buffer: the softmax group may be a block ahead
                         const int b = j & 1;
-                        if (!mbar_wait(&bars.w_full[g][b], (w_full_bits >> b) & 1u, abort, status, kStatusTimeout))
+                        if (!mbar_wait_warp(&bars.w_full[g][b], (w_full_bits >> b) & 1u, abort, status, kStatusTimeout))
                             return false;
                         w_full_bits ^= 1u << b;
                     } else {
-                        if (!mbar_wait(&bars.p_full[g], p_full_ph, abort, status, kStatusTimeout)) return false;
+                        if (!mbar_wait_warp(&bars.p_full[g], p_full_ph, abort, status, kStatusTimeout)) return false;
                         p_full_ph ^= 1;
                     }
                     tc_fence_after();
@@ -323,16 +344,16 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     const uint32_t a = (frz && (j & 1)) ? d_s : d_p;
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        mma_ts(d_o, a + 8 * k, sdesc_advance(d_v, 2048 * k), idesc_o,
+                        mma_ts_warp(d_o, a + 8 * k, sdesc_advance(d_v, 2048 * k), idesc_o,
                                (j > 0 || k > 0) ? 1u : 0u);
-                    mma_commit(frz ? &bars.w_done[g][j & 1] : &bars.o_done[g]);
+                    mma_commit_warp(frz ? &bars.w_done[g][j & 1] : &bars.o_done[g]);
                     return true;
                 };
                 int kv_ready = 0;   // blocks of this item whose K/V stage has been waited for
                 auto ensure_kv = [&](int j) -> bool {
                     while (kv_ready <= j) {
                         const int s = stage_of(kv_ready);
-                        if (!mbar_wait(&bars.kv_full[s], (kv_full_bits >> s) & 1u, abort, status, kStatusTimeout))
+                        if (!mbar_wait_warp(&bars.kv_full[s], (kv_full_bits >> s) & 1u, abort, status, kStatusTimeout))
                             return false;
                         kv_full_bits ^= 1u << s;
                         ++kv_ready;
@@ -351,15 +372,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     // phase; its predecessor phase is taken here, before that last P V is issued,
                     // so that s_empty never runs two phases ahead of this thread.
                     if (ok && it.frozen && j + 1 == ng) {
-                        ok = mbar_wait(&bars.s_empty[g], s_empty_ph, abort, status, kStatusTimeout);
+                        ok = mbar_wait_warp(&bars.s_empty[g], s_empty_ph, abort, status, kStatusTimeout);
                         s_empty_ph ^= 1;
                     }
                     if (ok && j < ng) ok = issue_pv(j);
                     if (!ok) break;
-                    mma_commit(&bars.kv_empty[stage_of(j)]);
+                    mma_commit_warp(&bars.kv_empty[stage_of(j)]);
                 }
                 if (!ok) break;
-                if (!it.frozen) mma_commit(&bars.q_empty[qs]);
+                if (!it.frozen) mma_commit_warp(&bars.q_empty[qs]);
                 stage = stage_of(nblk);
             }
         }
@@ -452,11 +473,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         mb = fmax3(mb, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
                     }
                     const float mx = fmaxf(ma, mb) * kScaleLog2;
-                    if (j > 0) {   // P V of the previous block done: P is free, O is stable
-                        if (!(ok = mbar_wait(&bars.o_done[g], o_done_ph, abort, status, kStatusTimeout))) break;
-                        o_done_ph ^= 1;
-                        tc_fence_after();
-                    }
                     const float m_new = fmaxf(m_used, mx);
                     const bool need = m_new > m_used + kRescaleThreshold;
                     const float f = need ? fast_exp2(m_used - m_new) : 1.f;   // O and l rescale factor
@@ -464,27 +480,30 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         l *= f;
                         m_used = m_new;
                     }
-                    // P = 2^(S log2(e) / sqrt(d) - m): two columns per FFMA and per FADD
+                    // P = 2^(S log2(e) / sqrt(d) - m), two columns per FFMA and per FADD, packed
+                    // into registers while the previous block's P V may still run
                     const float2 sc2 = make_float2(kScaleLog2, kScaleLog2);
                     const float2 nm2 = make_float2(-m_used, -m_used);
                     float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+                    uint32_t pk[64];   // packed bf16 pairs of the row's 128 columns of P
 #pragma unroll
-                    for (int h4 = 0; h4 < 4; ++h4) {
-                        uint32_t pk[16];   // packed bf16 pairs of 32 columns of P
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            const int cc = 32 * h4 + 2 * c;
-                            const float2 x =
-                                ffma2(make_float2(__uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1])), sc2, nm2);
-                            const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-                            if (c & 1)
-                                acc1 = fadd2(acc1, e);
-                            else
-                                acc0 = fadd2(acc0, e);
-                            pk[c] = pack_bf16(e.x, e.y);
-                        }
-                        tmem_st16(lane_base + 128 + 16 * h4, pk);
+                    for (int c = 0; c < 64; ++c) {
+                        const float2 x =
+                            ffma2(make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sc2, nm2);
+                        const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                        if (c & 1)
+                            acc1 = fadd2(acc1, e);
+                        else
+                            acc0 = fadd2(acc0, e);
+                        pk[c] = pack_bf16(e.x, e.y);
                     }
+                    if (j > 0) {   // P V of the previous block done: P is free, O is stable
+                        if (!(ok = mbar_wait(&bars.o_done[g], o_done_ph, abort, status, kStatusTimeout))) break;
+                        o_done_ph ^= 1;
+                        tc_fence_after();
+                    }
+                    tmem_st32(lane_base + 128, pk);
+                    tmem_st32(lane_base + 160, pk + 32);
                     l += (acc0.x + acc1.x) + (acc0.y + acc1.y);
                     // rescale O (stable: the previous P V is done) before this block's P V adds
                     // to it; done after the exp loop, when the row's scores no longer hold registers
@@ -639,6 +658,12 @@ cudaError_t launch_tc_fwd(const LayerArgs& a, cudaStream_t s) {
     p.Tp = p.nqb * 128;
     p.npairs = (p.nqb + 1) / 2;
     p.n_items = a.B * a.H * p.npairs;
+    // K and V of every slice: 2 x T x 64 bf16 each. When all of them fit in part of
+    // the L2 one group keeps the launch longest first (best balance); otherwise
+    // groups of kSliceGroup slices keep each group's K and V in L2 while its
+    // query pairs re-read them.
+    const size_t kv_all = (size_t)a.B * a.H * 2 * (size_t)a.T * 64 * 2;
+    p.slice_group = kv_all <= kL2GroupBytes ? a.B * a.H : kSliceGroup;
     for (int h = 0; h < a.H; ++h) {
         if (head_frozen(a.mask, h))
             p.frz_heads[p.n_frz++] = (uint8_t)h;

@@ -211,6 +211,48 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                  : "memory");
 }
 
+// Warp-wide forms of the three calls above, for an issuing warp whose 32 lanes
+// run the same code: every lane computes the (warp-uniform) descriptors and one
+// elected lane issues the instruction. Issuing from a warp that stays converged
+// lets back-to-back MMAs leave at the tensor core's own rate; issued from a
+// single-lane branch, an M128 x N64 MMA with A in tensor memory takes about 47
+// cycles to issue against 32 cycles to execute (measured on GB300).
+__device__ __forceinline__ void mma_ss_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit_warp(uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+// mbar_wait for a converged warp: lane 0 waits and the whole warp gets its
+// answer, so every lane leaves with the same result (an expired wait cannot
+// split the warp). Lane 0 is also the lane elect.sync picks in a converged
+// warp, so the lane that issues the next asynchronous operation is the one that
+// observed the phase.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                               uint32_t* status, uint32_t timeout_bit) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, status, timeout_bit) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 // ---------------------------------------------------------------------------
 // tcgen05.ld / st, shape 32x32b: thread t of warp w reads lane 32*(w%4)+t,
 // N consecutive 32-bit columns starting at the address's column.
