@@ -147,6 +147,7 @@ struct Barriers {
     // pattern warps wait on that barrier too)
     uint64_t dq_free;       // dQ of the previous tile has been read out (8 arrivals)
     uint64_t dkv_free;      // dV, dK of the previous item have been read out (8 arrivals)
+    uint64_t mma_idle;      // every MMA this CTA issued has completed (commit before TMEM is freed)
 };
 
 __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_constant__ BwdParams p) {
@@ -181,6 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         mbar_init(&bars.p_ready, 8);
         mbar_init(&bars.dq_free, 8);
         mbar_init(&bars.dkv_free, 8);
+        mbar_init(&bars.mma_idle, 1);
         fence_mbar_init();
     }
     if (warp == 9) {
@@ -377,6 +379,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 if (!ok) break;
                 if (!it.frozen) mma_commit(&bars.kv_empty);
             }
+            // Tensor memory is freed below: every MMA issued here must have completed (on
+            // the normal path the pattern warps have already seen it; after an abort the
+            // last MMAs may still run), with a bounded wait of its own.
+            mma_commit(&bars.mma_idle);
+            mbar_wait_bounded(&bars.mma_idle, 0, kWaitLimitNs);
         }
     } else {
         // ---------------------------------------------------------------- pattern warps

@@ -147,6 +147,7 @@ struct Barriers {
     uint64_t w_full[2][2];   // frozen items: W buffer b of tile g is written (4 arrivals)
     uint64_t w_done[2][2];   // frozen items: P V of tile g that read W buffer b has completed
     uint64_t item_full[kRing], item_empty[kRing];   // work-item ring (10 consumer warps)
+    uint64_t mma_idle[2];   // every MMA issuer g issued has completed (before TMEM is freed)
 };
 
 __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ FwdParams p) {
@@ -187,6 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             mbar_init(&bars.item_full[i], 1);
             mbar_init(&bars.item_empty[i], 10);   // 2 MMA issuers + 8 softmax warps
         }
+        mbar_init(&bars.mma_idle[0], 1);
+        mbar_init(&bars.mma_idle[1], 1);
         fence_mbar_init();
     }
     if (warp == 9) {
@@ -383,6 +386,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 if (!it.frozen) mma_commit_warp(&bars.q_empty[qs]);
                 stage = stage_of(nblk);
             }
+            // Tensor memory is freed at the end: every MMA issued here must have completed
+            // (after an abort the last ones may still run), with a bounded wait of its own.
+            mma_commit_warp(&bars.mma_idle[g]);
+            if (lane == 0) mbar_wait_bounded(&bars.mma_idle[g], 0, kWaitLimitNs);
+            __syncwarp();
         }
     }   // warp 11: idle
     } else {

@@ -87,6 +87,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// Wait for phase `parity` of `bar` for at most `limit_ns`, whatever the abort
+// flag says (used on the way out, after an abort, to let operations already
+// issued finish). Returns whether the phase completed.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 <= limit_ns)
+        if (mbar_try_wait_suspend(bar, parity)) return true;
+    return false;
+}
+
 // ---------------------------------------------------------------------------
 // TMA
 // ---------------------------------------------------------------------------
