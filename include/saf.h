@@ -155,6 +155,44 @@ SAF_API int saf_attn_bwd(const void* q, const void* k, const void* v, const void
                  void* dq, void* dk, void* dv,
                  void* workspace, size_t ws_bytes, void* stream);
 
+/* Grouped-query forward pass (§3.3: the grouped-query path keeps the shared
+ * key and value projections and drops the replaced heads' query projections;
+ * App. C.6: Qwen3-4B shares 8 key/value heads among 32 query heads; App. D.2:
+ * each ordinary query head is mapped to its retained key/value group).
+ *
+ * Same as saf_attn_fwd, except that k and v have Hkv heads:
+ * In:  q [B,H,T,d], k, v [B,Hkv,T,d] (dt), H a multiple of Hkv; query head h
+ *      reads key/value head h / (H / Hkv). a, r, frozen are per query head
+ *      ([H, ld_prior], H bytes): a frozen query head applies its own Eq. 3
+ *      pattern to the values of its group and reads no q or k.
+ * Out: o [B,H,T,d], lse [B,H,T] as for saf_attn_fwd.
+ * Workspace: saf_attn_workspace_bytes(B, H, T, d, dt, 0) (query heads).
+ * Errors: as saf_attn_fwd; SAF_EINVAL also for Hkv <= 0 or H % Hkv != 0.
+ * saf_attn_fwd(...) equals saf_attn_fwd_gqa(..., Hkv = H, ...). */
+SAF_API int saf_attn_fwd_gqa(const void* q, const void* k, const void* v,
+                     const float* a, const float* r, int ld_prior, const uint8_t* frozen,
+                     int B, int H, int Hkv, int T, int d, saf_dtype_t dt,
+                     void* o, float* lse,
+                     void* workspace, size_t ws_bytes, void* stream);
+
+/* Grouped-query backward pass (§3.3, App. C.6, App. D.2), given dO.
+ *
+ * In:  q, o, dO [B,H,T,d]; k, v [B,Hkv,T,d]; lse [B,H,T] from
+ *      saf_attn_fwd_gqa with the same inputs; a, r, frozen per query head.
+ * Out: dq [B,H,T,d]: the gradient of Eqs. 5-7 for ordinary query heads,
+ *      exact zeros for frozen ones. dk, dv [B,Hkv,T,d]: the gradient of a
+ *      shared head is the sum over the query heads of its group; frozen query
+ *      heads add W^T dO to dv only, so a group with no ordinary query head
+ *      gets dk = 0 exactly.
+ * Workspace: saf_attn_workspace_bytes(B, H, T, d, dt, 1).
+ * Errors: as saf_attn_bwd; SAF_EINVAL also for Hkv <= 0 or H % Hkv != 0.
+ * saf_attn_bwd(...) equals saf_attn_bwd_gqa(..., Hkv = H, ...). */
+SAF_API int saf_attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                     const float* lse, const float* a, const float* r, int ld_prior,
+                     const uint8_t* frozen, int B, int H, int Hkv, int T, int d, saf_dtype_t dt,
+                     void* dq, void* dk, void* dv,
+                     void* workspace, size_t ws_bytes, void* stream);
+
 /* Waits for `stream`, then reads the error word that the kernels of the last
  * call on `workspace` left there. Returns SAF_OK, SAF_ETIMEOUT, or
  * SAF_ECUDA if the stream reported a CUDA error. */

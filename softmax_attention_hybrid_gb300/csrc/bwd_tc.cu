@@ -10,12 +10,18 @@
 // rebuilt from a, r and log Z; their dK rows are written as zeros here and
 // their dQ rows by the finishing kernel.
 //
-// Work item: (batch b, head h, key block kb) = key rows [128 kb, 128 kb + 128);
-// it loops over query blocks qb = kb .. nqb-1 (causal). Items are taken from
-// a global counter, in this order: ordinary items in groups of kSliceGroup
-// (batch, head) slices, each group by ascending kb (longest first, and the
-// group's dQ accumulator rows stay in L2), then all frozen items by
-// ascending kb.
+// Key and value heads may be shared (grouped-query layout, §3.3 and App. C.6:
+// query head h reads key/value head h / G, G = H / Hkv; with G = 1 this is the
+// multi-head layer). The gradient of a shared head is the sum over its group,
+// so one work item covers a whole group: (batch b, key/value head hk, key
+// block kb) = key rows [128 kb, 128 kb + 128); it loops over the group's query
+// heads, ordinary ones first, and for each over query blocks qb = kb .. nqb-1
+// (causal), accumulating dV (every head) and dK (ordinary heads) in tensor
+// memory without atomics. Items are taken from a global counter, in this
+// order: items of key/value heads that have an ordinary query head, in groups
+// of kSliceGroup (batch, key/value head) slices, each group by ascending kb
+// (longest first, and the group's dQ accumulator rows stay in L2), then the
+// items whose query heads are all frozen, by ascending kb.
 //
 // Per (kb, qb) tile of an ordinary head (key row j of the block):
 //   S^T  = K Q^T          (tcgen05, TMEM)      P^T = exp(S^T / sqrt(d) - lse)
@@ -62,8 +68,8 @@ struct BwdParams {
     CUtensorMap tm_v;
     CUtensorMap tm_do;
     CUtensorMap tm_dq;     // fp32 dQ accumulator [BH, T, 64], box {32, 128}
-    __nv_bfloat16* dk;
-    __nv_bfloat16* dv;
+    __nv_bfloat16* dk;     // [B, Hkv, T, 64]
+    __nv_bfloat16* dv;     // [B, Hkv, T, 64]
     float* dq_acc;
     const float* rowvec;   // [BH, nqb, 256]: lse * log2(e) | D
     const float* a2p;      // [H, Tp]: a * log2(e)                (exact form)
@@ -73,11 +79,13 @@ struct BwdParams {
     const float* invz;     // [H, Tp]: 1 / Z'
     const uint32_t* hflag; // per head: bit 1 = use the exact form
     uint32_t* status;
-    int B, H, T, Tp;
-    int nqb, n_items, n_ord_items;
-    int n_ord, n_frz;
-    uint8_t ord_heads[SAF_MAX_HEADS];
-    uint8_t frz_heads[SAF_MAX_HEADS];
+    int B, H, Hkv, G, T, Tp;
+    int nqb, n_items, n_act_items;
+    int n_act, n_pas;                  // key/value heads with / without an ordinary query head
+    uint8_t act_kv[SAF_MAX_HEADS];     // the former
+    uint8_t pas_kv[SAF_MAX_HEADS];     // the latter
+    uint8_t gheads[SAF_MAX_HEADS];     // query heads of key/value head hk at [hk G, hk G + G), ordinary first
+    uint8_t gord[SAF_MAX_HEADS];       // ordinary query heads of key/value head hk
 };
 
 struct Smem {
@@ -96,32 +104,31 @@ struct Smem {
 };
 
 struct Item {
-    int b, h, kb;
-    bool frozen;
+    int b, hk, kb;
+    int nord;   // ordinary query heads of the group (their tiles come first); 0: no K, V, dK
 };
 
 __device__ __forceinline__ Item decode_item(const BwdParams& p, int idx) {
     Item it;
-    if (idx < p.n_ord_items) {
-        const int n_slices = p.B * p.n_ord;
+    if (idx < p.n_act_items) {
+        const int n_slices = p.B * p.n_act;
         const int per_group = kSliceGroup * p.nqb;
         const int g = idx / per_group;
         const int gsize = min(kSliceGroup, n_slices - g * kSliceGroup);
         const int within = idx - g * per_group;
         it.kb = within / gsize;
         const int slice = g * kSliceGroup + (within - it.kb * gsize);
-        it.b = slice / p.n_ord;
-        it.h = p.ord_heads[slice - it.b * p.n_ord];
-        it.frozen = false;
+        it.b = slice / p.n_act;
+        it.hk = p.act_kv[slice - it.b * p.n_act];
     } else {
-        const int f = idx - p.n_ord_items;
-        const int per = p.B * p.n_frz;
+        const int f = idx - p.n_act_items;
+        const int per = p.B * p.n_pas;
         it.kb = f / per;
         const int rem = f - it.kb * per;
-        it.b = rem / p.n_frz;
-        it.h = p.frz_heads[rem - it.b * p.n_frz];
-        it.frozen = true;
+        it.b = rem / p.n_pas;
+        it.hk = p.pas_kv[rem - it.b * p.n_pas];
     }
+    it.nord = p.gord[it.hk];
     return it;
 }
 
@@ -150,6 +157,9 @@ struct Barriers {
     uint64_t mma_idle;      // every MMA this CTA issued has completed (commit before TMEM is freed)
 };
 
+// kGrouped = false compiles the multi-head layer (one query head per key/value
+// head) with the group size fixed at 1, so that its loops keep their simple form.
+template <bool kGrouped>
 __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_constant__ BwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base (swizzled tiles), derived from the shared array itself so that
@@ -196,6 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     volatile int* abort = &abort_flag;
     uint32_t* status = p.status;
     const int nqb = p.nqb;
+    const int G = kGrouped ? p.G : 1;   // query heads per key/value head
 
     if (warp == 8) {
         // ---------------------------------------------------------------- producer
@@ -220,43 +231,50 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 slot = (slot + 1) % kRing;
                 if (idx < 0) break;
                 const Item it = decode_item(p, idx);
-                const int bh = it.b * p.H + it.h;
-                if (!it.frozen) {
+                if (it.nord > 0) {
                     if (!(ok = mbar_wait(&bars.kv_empty, kv_empty_ph, abort, status, kStatusTimeout))) break;
                     kv_empty_ph ^= 1;
                     uint8_t* kv = sm + Smem::kv;
+                    const int bkv = it.b * p.Hkv + it.hk;
                     mbar_expect_tx(&bars.kv_full, 2 * kTileBytes);
-                    tma_load_3d(kv, &p.tm_k, &bars.kv_full, 0, it.kb * 128, bh);
-                    tma_load_3d(kv + kTileBytes, &p.tm_v, &bars.kv_full, 0, it.kb * 128, bh);
+                    tma_load_3d(kv, &p.tm_k, &bars.kv_full, 0, it.kb * 128, bkv);
+                    tma_load_3d(kv + kTileBytes, &p.tm_v, &bars.kv_full, 0, it.kb * 128, bkv);
                 }
-                const bool exact = it.frozen && (p.hflag[it.h] & 2u) != 0;
-                for (int qb = it.kb; qb < nqb; ++qb) {
-                    if (!(ok = mbar_wait(&bars.st_empty[stage], (st_empty_bits >> stage) & 1u, abort, status,
-                                         kStatusTimeout)))
-                        break;
-                    st_empty_bits ^= 1u << stage;
-                    uint8_t* st = sm + Smem::st + stage * Smem::st_bytes;
-                    float* vec = reinterpret_cast<float*>(st + Smem::st_vec);
-                    const float* rv = p.rowvec + ((size_t)bh * nqb + qb) * 256;
-                    if (!it.frozen) {
-                        mbar_expect_tx(&bars.st_full[stage], 2 * kTileBytes + 1024);
-                        tma_load_3d(st, &p.tm_q, &bars.st_full[stage], 0, qb * 128, bh);
-                        tma_load_3d(st + kTileBytes, &p.tm_do, &bars.st_full[stage], 0, qb * 128, bh);
-                        bulk_load(vec, rv, 1024, &bars.st_full[stage]);
-                    } else {
-                        // exact form: vec[0..128) lse * log2(e) (= log2 Z), vec[256..512) r * log2(e);
-                        // factorised form: vec[0..128) 1 / Z', vec[256..512) exp(r - R)
-                        const float* band = (exact ? p.r2p : p.erp) + (size_t)it.h * (p.Tp + 256) +
-                                            (size_t)(qb - it.kb) * 128;
-                        mbar_expect_tx(&bars.st_full[stage], kTileBytes + 1024 + 512);
-                        tma_load_3d(st + kTileBytes, &p.tm_do, &bars.st_full[stage], 0, qb * 128, bh);
-                        if (exact)
-                            bulk_load(vec, rv, 512, &bars.st_full[stage]);
-                        else
-                            bulk_load(vec, p.invz + (size_t)it.h * p.Tp + (size_t)qb * 128, 512, &bars.st_full[stage]);
-                        bulk_load(vec + 256, band, 1024, &bars.st_full[stage]);
+                // the group's query heads, ordinary first, each over query blocks kb .. nqb-1
+                for (int gi = 0; gi < G && ok; ++gi) {
+                    const int h = p.gheads[it.hk * G + gi];
+                    const int bh = it.b * p.H + h;
+                    const bool frz = gi >= it.nord;
+                    const bool exact = frz && (p.hflag[h] & 2u) != 0;
+                    for (int qb = it.kb; qb < nqb; ++qb) {
+                        if (!(ok = mbar_wait(&bars.st_empty[stage], (st_empty_bits >> stage) & 1u, abort, status,
+                                             kStatusTimeout)))
+                            break;
+                        st_empty_bits ^= 1u << stage;
+                        uint8_t* st = sm + Smem::st + stage * Smem::st_bytes;
+                        float* vec = reinterpret_cast<float*>(st + Smem::st_vec);
+                        const float* rv = p.rowvec + ((size_t)bh * nqb + qb) * 256;
+                        if (!frz) {
+                            mbar_expect_tx(&bars.st_full[stage], 2 * kTileBytes + 1024);
+                            tma_load_3d(st, &p.tm_q, &bars.st_full[stage], 0, qb * 128, bh);
+                            tma_load_3d(st + kTileBytes, &p.tm_do, &bars.st_full[stage], 0, qb * 128, bh);
+                            bulk_load(vec, rv, 1024, &bars.st_full[stage]);
+                        } else {
+                            // exact form: vec[0..128) lse * log2(e) (= log2 Z), vec[256..512) r * log2(e);
+                            // factorised form: vec[0..128) 1 / Z', vec[256..512) exp(r - R)
+                            const float* band = (exact ? p.r2p : p.erp) + (size_t)h * (p.Tp + 256) +
+                                                (size_t)(qb - it.kb) * 128;
+                            mbar_expect_tx(&bars.st_full[stage], kTileBytes + 1024 + 512);
+                            tma_load_3d(st + kTileBytes, &p.tm_do, &bars.st_full[stage], 0, qb * 128, bh);
+                            if (exact)
+                                bulk_load(vec, rv, 512, &bars.st_full[stage]);
+                            else
+                                bulk_load(vec, p.invz + (size_t)h * p.Tp + (size_t)qb * 128, 512,
+                                          &bars.st_full[stage]);
+                            bulk_load(vec + 256, band, 1024, &bars.st_full[stage]);
+                        }
+                        stage = (stage + 1) % kStages;
                     }
-                    stage = (stage + 1) % kStages;
                 }
             }
         }
@@ -310,8 +328,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 slot = (slot + 1) % kRing;
                 if (idx < 0) break;
                 const Item it = decode_item(p, idx);
-                const int n = nqb - it.kb;
-                if (!it.frozen) {
+                const int n = G * (nqb - it.kb);        // tiles of the item
+                const int n_ord = it.nord * (nqb - it.kb);   // its ordinary tiles come first
+                if (n_ord > 0) {
                     if (!(ok = mbar_wait(&bars.kv_full, kv_full_ph, abort, status, kStatusTimeout))) break;
                     kv_full_ph ^= 1;
                     if (!(ok = wait_st(stage))) break;
@@ -321,19 +340,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 for (int i = 0; i < n && ok; ++i) {
                     const int s = stage;
                     const int s_next = (stage + 1) % kStages;
-                    if (!it.frozen) {
+                    const bool ord = i < n_ord;
+                    if (ord) {
                         // S^T and dP^T of the next tile may overwrite TMEM once this tile's are read
                         if (!(ok = mbar_wait(&bars.s_consumed, s_consumed_ph, abort, status, kStatusTimeout))) break;
                         s_consumed_ph ^= 1;
                         tc_fence_after();
-                        if (i + 1 < n) {
+                        if (i + 1 < n_ord) {
                             if (!(ok = wait_st(s_next))) break;
                             issue_s(s_next);
                         }
                         if (!(ok = mbar_wait(&bars.dp_consumed, dp_consumed_ph, abort, status, kStatusTimeout))) break;
                         dp_consumed_ph ^= 1;
                         tc_fence_after();
-                        if (i + 1 < n) issue_dp(s_next);
+                        if (i + 1 < n_ord) issue_dp(s_next);
                     } else {
                         if (!(ok = wait_st(s))) break;
                     }
@@ -354,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                     for (int k = 0; k < 8; ++k)
                         mma_ts(tmem + kColDV, tmem + kColP + 8 * k, sdesc_advance(d_domn, 2048 * k), id_dv,
                                (i > 0 || k > 0) ? 1u : 0u);
-                    if (!it.frozen) {
+                    if (ord) {
                         const uint32_t sds = smem_u32(sm + Smem::ds + (gto++ & 1) * Smem::ds_bytes);
                         const uint64_t d_ds = sdesc_sw128(sds, 16, 1024);       // dS, K-major view (dK)
                         const uint64_t d_dsmn = sdesc_sw128(sds, 16384, 1024);  // dS, MN-major view (dQ)
@@ -377,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                     stage = s_next;
                 }
                 if (!ok) break;
-                if (!it.frozen) mma_commit(&bars.kv_empty);
+                if (n_ord > 0) mma_commit(&bars.kv_empty);
             }
             // Tensor memory is freed below: every MMA issued here must have completed (on
             // the normal path the pattern warps have already seen it; after an abort the
@@ -446,27 +466,33 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             slot = (slot + 1) % kRing;
             if (idx < 0) break;
             const Item it = decode_item(p, idx);
-            const int bh = it.b * p.H + it.h;
+            const int bkv = it.b * p.Hkv + it.hk;   // the key/value slice whose dK, dV this item writes
             const int key = it.kb * 128 + j;
-            const int n = nqb - it.kb;
-            float a2j = -INFINITY;   // exact form: a * log2(e) of my key
-            float eaj = 0.f;         // factorised form: exp(a - A) of my key, applied to dV
-            bool exact = false;
-            if (it.frozen) {
-                exact = (p.hflag[it.h] & 2u) != 0;
-                a2j = p.a2p[(size_t)it.h * p.Tp + key];
-                eaj = p.eap[(size_t)it.h * p.Tp + key];
-            }
+            const int n = G * (nqb - it.kb);
+            // tile i: query head gheads[hk G + gi] (ordinary for gi < nord), query block qb
+            int gi = 0, qb = it.kb;
+            const int n_ord = it.nord * (nqb - it.kb);   // the ordinary tiles come first
+            // In the multi-head layer a frozen item's tiles all belong to one head: the factor
+            // exp(a[j] - A) of its key rows stays out of W^T and is applied to dV at the end.
+            // A group of query heads puts it into each W^T tile instead.
+            const bool ea_at_end = !kGrouped && it.nord == 0;
+            // exact-form flag of the current query head (read when the head changes)
+            bool exact = it.nord == 0 && (p.hflag[p.gheads[it.hk * G]] & 2u) != 0;
+            // the multi-head layer has one query head per item: its slice and kind are fixed
+            const int h_item = p.gheads[it.hk * G];
             for (int i = 0; i < n && ok; ++i) {
-                const int qb = it.kb + i;
-                const bool diag = i == 0;
+                if (!kGrouped) qb = it.kb + i;
+                const bool diag = qb == it.kb;
+                const int h = kGrouped ? p.gheads[it.hk * G + gi] : h_item;
+                const int bh = it.b * p.H + h;
+                const bool frz = kGrouped ? gi >= it.nord : it.nord == 0;
                 if (!(ok = mbar_wait(&bars.st_full[stage], (st_full_bits >> stage) & 1u, abort, status,
                                      kStatusTimeout)))
                     break;
                 st_full_bits ^= 1u << stage;
                 const float* vec =
                     reinterpret_cast<const float*>(sm + Smem::st + stage * Smem::st_bytes + Smem::st_vec);
-                if (!it.frozen) {
+                if (!frz) {
                     if (!(ok = mbar_wait(&bars.sdp_full, sdp_full_ph, abort, status, kStatusTimeout))) break;
                     sdp_full_ph ^= 1;
                     tc_fence_after();
@@ -544,17 +570,26 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                     ++gto;
                 } else {
                     // W^T(j, q) = W(q, j) (Eq. 3); band[q] is r at offset q - j = (qb - kb) * 128 +
-                    // q - j. Factorised: W(q, j) / exp(a[j] - A) = exp(r[q-j] - R) / Z'(q), no exp per
-                    // element (exp(a[j] - A) is applied to dV). Exact: exp(a[j] + r[q-j] - log Z(q)).
+                    // q - j. Factorised: W(q, j) = exp(a[j] - A) exp(r[q-j] - R) / Z'(q), no exp per
+                    // element (exp(a[j] - A) in the tile, or on dV at the end: ea_at_end). Exact:
+                    // exp(a[j] + r[q-j] - log Z(q)).
                     uint32_t pk[32];
                     if (!exact) {
-                        // W^T is Toeplitz up to the column factor 1 / Z'(q). In the 16x128b shape
-                        // a thread holds key rows 32 quarter + rho + 8 m (m = 0..3) at packed
-                        // columns 4 jr + qq, queries q = 64 half + 8 jr + 2 qq + {0, 1}
-                        // (jr = 0..7): the band value of (row, q) depends on jr - m alone, so 22
-                        // band loads serve the thread's 64 products.
+                        // W^T is Toeplitz up to the row factor exp(a[j] - A) and the column
+                        // factor 1 / Z'(q). In the 16x128b shape a thread holds key rows
+                        // 32 quarter + rho + 8 m (m = 0..3) at packed columns 4 jr + qq, queries
+                        // q = 64 half + 8 jr + 2 qq + {0, 1} (jr = 0..7): the band value of
+                        // (row, q) depends on jr - m alone, so 22 band loads serve the thread's
+                        // 64 products.
                         const int rho = lane >> 2, qq = lane & 3;
                         const float* b1 = vec + 256 + 127 + 64 * half + 2 * qq - 32 * quarter - rho;
+                        // exp(a - A) of my four key rows (1 when it is applied to dV at the end)
+                        float ea4[4] = {1.f, 1.f, 1.f, 1.f};
+                        if (kGrouped) {
+                            const float* ea = p.eap + (size_t)h * p.Tp + it.kb * 128 + 32 * quarter + rho;
+#pragma unroll
+                            for (int m = 0; m < 4; ++m) ea4[m] = ea[8 * m];
+                        }
                         float e0[11], e1[11];   // index jr - m + 3
 #pragma unroll
                         for (int d = -3; d <= 7; ++d) {
@@ -566,11 +601,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                             const float2 iz = *reinterpret_cast<const float2*>(vec + 64 * half + 8 * jr + 2 * qq);
 #pragma unroll
                             for (int m = 0; m < 4; ++m) {
-                                const float2 w = fmul2(make_float2(e0[jr - m + 3], e1[jr - m + 3]), iz);
+                                const float2 izm = kGrouped ? fmul2(iz, make_float2(ea4[m], ea4[m])) : iz;
+                                const float2 w = fmul2(make_float2(e0[jr - m + 3], e1[jr - m + 3]), izm);
                                 pk[16 * (m >> 1) + 2 * jr + (m & 1)] = pack_bf16(w.x, w.y);
                             }
                         }
                     } else {
+                        const float a2j = p.a2p[(size_t)h * p.Tp + key];   // a * log2(e) of my key
                         const float* band = vec + 256 + 127 - j;
 #pragma unroll
                         for (int e = 0; e < 64; e += 2) {
@@ -595,26 +632,42 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars.p_ready);
-                // dQ of the previous tile, staged in the buffer that held its dS
-                if (!it.frozen && i > 0) drain_dq(bh, qb - 1, dsbuf(gto & 1));
+                // dQ of the previous ordinary tile (its MMAs are done), staged in the buffer
+                // that held its dS
+                // dQ of the previous tile if it was ordinary (its MMAs are done), staged in the
+                // buffer that held its dS (gto has counted this tile if it is ordinary)
+                if (!kGrouped) {
+                    if (!frz && i > 0) drain_dq(bh, qb - 1, dsbuf(gto & 1));
+                } else if (i > 0 && i - 1 < n_ord) {
+                    const bool first = qb == it.kb;
+                    const int bhp = it.b * p.H + p.gheads[it.hk * G + (first ? gi - 1 : gi)];
+                    drain_dq(bhp, first ? nqb - 1 : qb - 1, dsbuf((frz ? gto - 1 : gto) & 1));
+                }
                 pending = stage;
                 stage = (stage + 1) % kStages;
+                if (kGrouped && ++qb == nqb) {   // next query head of the group
+                    qb = it.kb;
+                    if (++gi >= it.nord && gi < G) exact = (p.hflag[p.gheads[it.hk * G + gi]] & 2u) != 0;
+                }
             }
             if (!ok) break;
             // all MMAs of this item done: the last dQ, then the dV and dK rows (my 32 d-columns)
             if (!(ok = wait_tile_done())) break;
-            if (!it.frozen) drain_dq(bh, nqb - 1, dsbuf((gto - 1) & 1));
+            if (n > 0 && n - 1 < n_ord)   // the last tile was ordinary
+                drain_dq(it.b * p.H + p.gheads[it.hk * G + G - 1], nqb - 1, dsbuf((gto - 1) & 1));
             uint32_t dv[32], dk[32];
             tmem_ld32(lane_base + kColDV + 32 * half, dv);
-            if (!it.frozen) tmem_ld32(lane_base + kColDK + 32 * half, dk);
+            if (it.nord > 0) tmem_ld32(lane_base + kColDK + 32 * half, dk);
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars.dkv_free);
             if (key < p.T) {
-                uint4* pv = reinterpret_cast<uint4*>(p.dv + ((size_t)bh * p.T + key) * 64 + 32 * half);
-                uint4* pk2 = reinterpret_cast<uint4*>(p.dk + ((size_t)bh * p.T + key) * 64 + 32 * half);
-                const float fv = (it.frozen && !exact) ? eaj : 1.f;
+                uint4* pv = reinterpret_cast<uint4*>(p.dv + ((size_t)bkv * p.T + key) * 64 + 32 * half);
+                uint4* pk2 = reinterpret_cast<uint4*>(p.dk + ((size_t)bkv * p.T + key) * 64 + 32 * half);
+                // exp(a[j] - A) of my key, when the item left it out of W^T (factorised form)
+                float fv = 1.f;
+                if (ea_at_end && !exact) fv = p.eap[(size_t)p.gheads[it.hk * G] * p.Tp + key];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const uint32_t* x = dv + 8 * c;
@@ -623,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                                        pack_bf16(__uint_as_float(x[4]) * fv, __uint_as_float(x[5]) * fv),
                                        pack_bf16(__uint_as_float(x[6]) * fv, __uint_as_float(x[7]) * fv));
                 }
-                if (it.frozen) {
+                if (it.nord == 0) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) pk2[c] = make_uint4(0, 0, 0, 0);
                 } else {
@@ -678,12 +731,16 @@ cudaError_t launch_tc_bwd(const LayerArgs& a, cudaStream_t s) {
     BwdParams p;
     memset(&p, 0, sizeof(p));
     const int BH = a.B * a.H;
+    const int Hkv = a.Hkv > 0 ? a.Hkv : a.H;
+    const int BHkv = a.B * Hkv;
     const void* vbase = a.v;
-    const void* qbase = a.q ? a.q : vbase;
     const void* kbase = a.k ? a.k : vbase;
-    if (!make_tmap_bf16_3d(&p.tm_q, qbase, 64, a.T, BH, 64, 128) ||
-        !make_tmap_bf16_3d(&p.tm_k, kbase, 64, a.T, BH, 64, 128) ||
-        !make_tmap_bf16_3d(&p.tm_v, vbase, 64, a.T, BH, 64, 128) ||
+    // q (and k) may be NULL when every head is frozen; the maps then point at v and are never used
+    const void* qbase = a.q ? a.q : vbase;
+    const int BHq = a.q ? BH : BHkv;
+    if (!make_tmap_bf16_3d(&p.tm_q, qbase, 64, a.T, BHq, 64, 128) ||
+        !make_tmap_bf16_3d(&p.tm_k, kbase, 64, a.T, BHkv, 64, 128) ||
+        !make_tmap_bf16_3d(&p.tm_v, vbase, 64, a.T, BHkv, 64, 128) ||
         !make_tmap_bf16_3d(&p.tm_do, a.dO, 64, a.T, BH, 64, 128) ||
         !make_tmap_f32_3d(&p.tm_dq, a.dq_acc, 64, a.T, BH, 32, 128))
         return cudaErrorInvalidValue;
@@ -700,17 +757,29 @@ cudaError_t launch_tc_bwd(const LayerArgs& a, cudaStream_t s) {
     p.status = a.status;
     p.B = a.B;
     p.H = a.H;
+    p.Hkv = Hkv;
+    p.G = a.H / Hkv;
     p.T = a.T;
     p.nqb = (a.T + 127) / 128;
     p.Tp = p.nqb * 128;
-    for (int h = 0; h < a.H; ++h) {
-        if (head_frozen(a.mask, h))
-            p.frz_heads[p.n_frz++] = (uint8_t)h;
+    // per key/value head: its query heads, ordinary first
+    for (int hk = 0; hk < Hkv; ++hk) {
+        int n = 0;
+        for (int pass = 0; pass < 2; ++pass)
+            for (int gi = 0; gi < p.G; ++gi) {
+                const int h = hk * p.G + gi;
+                if (head_frozen(a.mask, h) == (pass == 1)) p.gheads[hk * p.G + n++] = (uint8_t)h;
+            }
+        int nord = 0;
+        for (int gi = 0; gi < p.G; ++gi) nord += head_frozen(a.mask, hk * p.G + gi) ? 0 : 1;
+        p.gord[hk] = (uint8_t)nord;
+        if (nord > 0)
+            p.act_kv[p.n_act++] = (uint8_t)hk;
         else
-            p.ord_heads[p.n_ord++] = (uint8_t)h;
+            p.pas_kv[p.n_pas++] = (uint8_t)hk;
     }
-    p.n_ord_items = a.B * p.n_ord * p.nqb;
-    p.n_items = a.B * a.H * p.nqb;
+    p.n_act_items = a.B * p.n_act * p.nqb;
+    p.n_items = BHkv * p.nqb;
 
     // (the dQ accumulator of the ordinary heads was zeroed by bwd_prep_kernel)
     cudaError_t e;
@@ -718,11 +787,12 @@ cudaError_t launch_tc_bwd(const LayerArgs& a, cudaStream_t s) {
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int smem = Smem::total + 1024;
-    e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    void (*kernel)(BwdParams) = p.G > 1 ? bwd_tc_kernel<true> : bwd_tc_kernel<false>;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int grid = p.n_items < sms ? p.n_items : sms;
     before_launch(SAF_KERNEL_BWD, s);
-    e = launch_ex(bwd_tc_kernel, dim3(grid), dim3(kThreads), smem, s, true, 1, p);
+    e = launch_ex(kernel, dim3(grid), dim3(kThreads), smem, s, true, 1, p);
     after_launch(SAF_KERNEL_BWD, s);
     if (e != cudaSuccess) return e;
     dim3 g2((unsigned)(((long long)a.T * 8 + 255) / 256), BH);

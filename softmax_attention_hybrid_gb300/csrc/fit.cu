@@ -225,6 +225,7 @@ extern "C" int saf_fit_compact(const float* eta_abs, const float* eta_rel, int H
     p.ld_prior = T;
     p.B = 1;
     p.H = H;
+    p.Hkv = H;
     p.T = T;
     for (int h = 0; h < H; ++h) p.mask.w[h >> 6] |= 1ull << (h & 63);
     p.status = (uint32_t*)(ws + L.status);

@@ -77,6 +77,7 @@ struct FwdParams {
     const uint32_t* hflag;   // per head: bit 1 = use the exact form
     uint32_t* status;
     int B, H, T, ld, Tp;
+    int Hkv, G;        // key/value heads; query heads per key/value head (query head h reads h / G)
     int nqb, npairs, n_items;
     int slice_group;   // (batch, head) slices per item group
     int n_ord, n_frz;
@@ -234,6 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 if (idx < 0) break;
                 const Item it = decode_item(p, idx);
                 const int bh = it.b * p.H + it.h;
+                const int bkv = it.b * p.Hkv + it.h / p.G;   // the key/value slice this head reads
                 const int qb0 = 2 * it.pair, qb1 = qb0 + 1;
                 const bool t1 = qb1 < p.nqb;
                 const int nblk = t1 ? qb1 + 1 : qb0 + 1;
@@ -259,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     uint8_t* st = sm + SmemLayout::kv + stage * SmemLayout::stage_bytes;
                     if (!it.frozen) {
                         mbar_expect_tx(&bars.kv_full[stage], 2 * kTileBytes);
-                        tma_load_3d(st, &p.tm_k, &bars.kv_full[stage], 0, j * 128, bh);
+                        tma_load_3d(st, &p.tm_k, &bars.kv_full[stage], 0, j * 128, bkv);
                     } else {
                         const float* as = exact ? p.a2p : p.eap;
                         const float* rs = exact ? p.r2p : p.erp;
@@ -269,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                                   rs + (size_t)it.h * (p.Tp + 256) + (size_t)(qb0 - j) * 128, 1536,
                                   &bars.kv_full[stage]);
                     }
-                    tma_load_3d(st + kTileBytes, &p.tm_v, &bars.kv_full[stage], 0, j * 128, bh);
+                    tma_load_3d(st + kTileBytes, &p.tm_v, &bars.kv_full[stage], 0, j * 128, bkv);
                     stage = (stage + 1 == kStages) ? 0 : stage + 1;
                 }
             }
@@ -641,12 +643,16 @@ cudaError_t launch_tc_fwd(const LayerArgs& a, cudaStream_t s) {
     FwdParams p;
     memset(&p, 0, sizeof(p));
     const int BH = a.B * a.H;
+    const int Hkv = a.Hkv > 0 ? a.Hkv : a.H;
+    const int BHkv = a.B * Hkv;
     const void* vbase = a.v;
-    const void* qbase = a.q ? a.q : vbase;
     const void* kbase = a.k ? a.k : vbase;
-    if (!make_tmap_bf16_3d(&p.tm_q, qbase, 64, a.T, BH, 64, 128) ||
-        !make_tmap_bf16_3d(&p.tm_k, kbase, 64, a.T, BH, 64, 128) ||
-        !make_tmap_bf16_3d(&p.tm_v, vbase, 64, a.T, BH, 64, 128))
+    // q (and k) may be NULL when every head is frozen; the maps then point at v and are never used
+    const void* qbase = a.q ? a.q : vbase;
+    const int BHq = a.q ? BH : BHkv;
+    if (!make_tmap_bf16_3d(&p.tm_q, qbase, 64, a.T, BHq, 64, 128) ||
+        !make_tmap_bf16_3d(&p.tm_k, kbase, 64, a.T, BHkv, 64, 128) ||
+        !make_tmap_bf16_3d(&p.tm_v, vbase, 64, a.T, BHkv, 64, 128))
         return cudaErrorInvalidValue;
     p.o = (__nv_bfloat16*)a.out;
     p.lse = a.lse_out;
@@ -660,6 +666,8 @@ cudaError_t launch_tc_fwd(const LayerArgs& a, cudaStream_t s) {
     p.status = a.status;
     p.B = a.B;
     p.H = a.H;
+    p.Hkv = Hkv;
+    p.G = a.H / Hkv;
     p.T = a.T;
     p.ld = a.ld_prior;
     p.nqb = (a.T + 127) / 128;
@@ -670,7 +678,7 @@ cudaError_t launch_tc_fwd(const LayerArgs& a, cudaStream_t s) {
     // the L2 one group keeps the launch longest first (best balance); otherwise
     // groups of kSliceGroup slices keep each group's K and V in L2 while its
     // query pairs re-read them.
-    const size_t kv_all = (size_t)a.B * a.H * 2 * (size_t)a.T * 64 * 2;
+    const size_t kv_all = (size_t)BHkv * 2 * (size_t)a.T * 64 * 2;
     p.slice_group = kv_all <= kL2GroupBytes ? a.B * a.H : kSliceGroup;
     for (int h = 0; h < a.H; ++h) {
         if (head_frozen(a.mask, h))

@@ -139,6 +139,7 @@ LayerArgs make_args(const void* q, const void* k, const void* v, const float* a,
     p.H = H;
     p.T = T;
     p.ld_prior = ld_prior;
+    p.Hkv = H;
     p.mask = c.mask;
     p.status = (uint32_t*)(ws + L.status);
     p.lz = (float*)(ws + L.lz);
@@ -207,9 +208,10 @@ size_t saf_attn_workspace_bytes(int B, int H, int T, int d, saf_dtype_t dt, int 
     return workspace_layout(B, H, T, backward ? 1 : 0, dt == SAF_BF16).total;
 }
 
-int saf_attn_fwd(const void* q, const void* k, const void* v, const float* a, const float* r, int ld_prior,
-                 const uint8_t* frozen, int B, int H, int T, int d, saf_dtype_t dt, void* o, float* lse,
-                 void* workspace, size_t ws_bytes, void* stream) {
+int saf_attn_fwd_gqa(const void* q, const void* k, const void* v, const float* a, const float* r, int ld_prior,
+                     const uint8_t* frozen, int B, int H, int Hkv, int T, int d, saf_dtype_t dt, void* o, float* lse,
+                     void* workspace, size_t ws_bytes, void* stream) {
+    if (Hkv <= 0 || H <= 0 || H % Hkv != 0) return SAF_EINVAL;
     Common c;
     int st = validate(q, k, v, a, r, ld_prior, frozen, B, H, T, d, dt, workspace, ws_bytes, 0, &c);
     if (st != SAF_OK) return st;
@@ -219,6 +221,7 @@ int saf_attn_fwd(const void* q, const void* k, const void* v, const float* a, co
     if ((st = check_device()) != SAF_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     LayerArgs p = make_args(q, k, v, a, r, ld_prior, B, H, T, c, workspace, 0, dt == SAF_BF16);
+    p.Hkv = Hkv;
     p.d = d;
     p.out = o;
     p.lse_out = lse;
@@ -228,9 +231,17 @@ int saf_attn_fwd(const void* q, const void* k, const void* v, const float* a, co
     return launch_status(e);
 }
 
-int saf_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
-                 const float* a, const float* r, int ld_prior, const uint8_t* frozen, int B, int H, int T, int d,
-                 saf_dtype_t dt, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes, void* stream) {
+int saf_attn_fwd(const void* q, const void* k, const void* v, const float* a, const float* r, int ld_prior,
+                 const uint8_t* frozen, int B, int H, int T, int d, saf_dtype_t dt, void* o, float* lse,
+                 void* workspace, size_t ws_bytes, void* stream) {
+    return saf_attn_fwd_gqa(q, k, v, a, r, ld_prior, frozen, B, H, H, T, d, dt, o, lse, workspace, ws_bytes, stream);
+}
+
+int saf_attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                     const float* a, const float* r, int ld_prior, const uint8_t* frozen, int B, int H, int Hkv, int T,
+                     int d, saf_dtype_t dt, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+                     void* stream) {
+    if (Hkv <= 0 || H <= 0 || H % Hkv != 0) return SAF_EINVAL;
     Common c;
     int st = validate(q, k, v, a, r, ld_prior, frozen, B, H, T, d, dt, workspace, ws_bytes, 1, &c);
     if (st != SAF_OK) return st;
@@ -242,6 +253,7 @@ int saf_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
     if ((st = check_device()) != SAF_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     LayerArgs p = make_args(q, k, v, a, r, ld_prior, B, H, T, c, workspace, 1, dt == SAF_BF16);
+    p.Hkv = Hkv;
     p.d = d;
     p.o = o;
     p.dO = dO;
@@ -259,6 +271,13 @@ int saf_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
         if (e == cudaSuccess) e = launch_simt_bwd(p, false, s);
     }
     return launch_status(e);
+}
+
+int saf_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                 const float* a, const float* r, int ld_prior, const uint8_t* frozen, int B, int H, int T, int d,
+                 saf_dtype_t dt, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes, void* stream) {
+    return saf_attn_bwd_gqa(q, k, v, o, dO, lse, a, r, ld_prior, frozen, B, H, H, T, d, dt, dq, dk, dv, workspace,
+                            ws_bytes, stream);
 }
 
 int saf_device_status(const void* workspace, void* stream) {

@@ -139,6 +139,7 @@ struct LayerArgs {
     float* rowvec;       // workspace: per-block row vectors [B, H, Tp / 128, 256]
     uint32_t* status;    // workspace: error words
     int B, H, T, ld_prior;
+    int Hkv;             // key/value heads: query head h reads key/value head h / (H / Hkv)
     int d;               // head dimension
     HeadMask mask;
 };

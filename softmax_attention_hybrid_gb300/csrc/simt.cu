@@ -65,9 +65,11 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(LayerArgs p) {
     const int qb = blockIdx.x, bh = blockIdx.y, h = bh % p.H;
     const bool frozen = head_frozen(p.mask, h);
     const size_t base = (size_t)bh * T * D;
+    // key/value slice of this query head (grouped-query layout: head h reads h / (H / Hkv))
+    const size_t kvbase = ((size_t)(bh / p.H) * p.Hkv + h / (p.H / p.Hkv)) * T * D;
     const E* q = (const E*)p.q + base;
-    const E* k = (const E*)p.k + base;
-    const E* v = (const E*)p.v + base;
+    const E* k = (const E*)p.k + kvbase;
+    const E* v = (const E*)p.v + kvbase;
     const float* a = p.a + (size_t)h * p.ld_prior;
     const float* r = p.r + (size_t)h * p.ld_prior;
     const int q0 = qb * kB;
@@ -162,8 +164,11 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(LayerArgs p) {
 }
 
 // ---------------------------------------------------------------------------
-// Backward, key-block pass. Grid (ceil(T/64), B*H). Program owns keys
-// k0..k0+63; loops over query blocks qb >= kb. Thread rows = keys.
+// Backward, key-block pass. Grid (ceil(T/64), B*Hkv). Program owns keys
+// k0..k0+63 of one key/value slice; loops over the query heads that share it
+// (grouped-query layout; one head in the multi-head layer) and, for each, over
+// query blocks qb >= kb, so that the slice's dV and dK are group sums formed
+// without atomics. Thread rows = keys.
 // ---------------------------------------------------------------------------
 template <typename E, int D>
 __global__ void __launch_bounds__(kThreads) bwd_kv_kernel(LayerArgs p) {
@@ -179,20 +184,18 @@ __global__ void __launch_bounds__(kThreads) bwd_kv_kernel(LayerArgs p) {
     __shared__ float rowD[kB];
 
     const int T = p.T;
-    const int kb = blockIdx.x, bh = blockIdx.y, h = bh % p.H;
-    const bool frozen = head_frozen(p.mask, h);
-    const size_t base = (size_t)bh * T * D;
-    const E* q = (const E*)p.q + base;
-    const E* k = (const E*)p.k + base;
-    const E* v = (const E*)p.v + base;
-    const E* dO = (const E*)p.dO + base;
-    const float* a = p.a + (size_t)h * p.ld_prior;
-    const float* r = p.r + (size_t)h * p.ld_prior;
+    const int G = p.H / p.Hkv;
+    const int kb = blockIdx.x, bkv = blockIdx.y, b = bkv / p.Hkv, hk = bkv % p.Hkv;
+    const size_t kvbase = (size_t)bkv * T * D;
+    const E* k = (const E*)p.k + kvbase;
+    const E* v = (const E*)p.v + kvbase;
     const int k0 = kb * kB;
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
     const float scale = 1.f / sqrtf((float)D);
+    bool any_ordinary = false;
+    for (int gi = 0; gi < G; ++gi) any_ordinary |= !head_frozen(p.mask, hk * G + gi);
 
-    if (!frozen) load_tile<D>(Ks, k, k0, T);
+    if (any_ordinary) load_tile<D>(Ks, k, k0, T);
     load_tile<D>(Vs, v, k0, T);
     float dv[4][NC], dk[4][NC];
 #pragma unroll
@@ -201,6 +204,14 @@ __global__ void __launch_bounds__(kThreads) bwd_kv_kernel(LayerArgs p) {
         for (int c = 0; c < NC; ++c) dv[i][c] = dk[i][c] = 0.f;
 
     const int nqb = (T + kB - 1) / kB;
+    for (int gi = 0; gi < G; ++gi) {
+    const int h = hk * G + gi, bh = b * p.H + h;
+    const bool frozen = head_frozen(p.mask, h);
+    const size_t base = (size_t)bh * T * D;
+    const E* q = (const E*)p.q + base;
+    const E* dO = (const E*)p.dO + base;
+    const float* a = p.a + (size_t)h * p.ld_prior;
+    const float* r = p.r + (size_t)h * p.ld_prior;
     for (int qb = kb; qb < nqb; ++qb) {
         const int q0 = qb * kB;
         __syncthreads();
@@ -266,9 +277,10 @@ __global__ void __launch_bounds__(kThreads) bwd_kv_kernel(LayerArgs p) {
             }
         }
     }
+    }
 
-    E* dvp = (E*)p.dv + base;
-    E* dkp = (E*)p.dk + base;
+    E* dvp = (E*)p.dv + kvbase;
+    E* dkp = (E*)p.dk + kvbase;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int key = k0 + ty * 4 + i;
@@ -276,7 +288,7 @@ __global__ void __launch_bounds__(kThreads) bwd_kv_kernel(LayerArgs p) {
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
             from_f(dvp + (size_t)key * D + tx + 16 * c, dv[i][c]);
-            from_f(dkp + (size_t)key * D + tx + 16 * c, frozen ? 0.f : dk[i][c] * scale);
+            from_f(dkp + (size_t)key * D + tx + 16 * c, any_ordinary ? dk[i][c] * scale : 0.f);
         }
     }
 }
@@ -309,9 +321,10 @@ __global__ void __launch_bounds__(kThreads) bwd_q_kernel(LayerArgs p) {
         }
         return;
     }
+    const size_t kvbase = ((size_t)(bh / p.H) * p.Hkv + h / (p.H / p.Hkv)) * T * D;
     const E* q = (const E*)p.q + base;
-    const E* k = (const E*)p.k + base;
-    const E* v = (const E*)p.v + base;
+    const E* k = (const E*)p.k + kvbase;
+    const E* v = (const E*)p.v + kvbase;
     const E* dO = (const E*)p.dO + base;
     const float scale = 1.f / sqrtf((float)D);
 
@@ -376,11 +389,11 @@ __global__ void __launch_bounds__(kThreads) bwd_q_kernel(LayerArgs p) {
 }
 
 template <int D, typename K>
-cudaError_t launch(K kernel, int id, int tiles, const LayerArgs& p, cudaStream_t s) {
+cudaError_t launch(K kernel, int id, int tiles, const LayerArgs& p, cudaStream_t s, int slices) {
     const int smem = tiles * tile_floats<D>() * (int)sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((p.T + kB - 1) / kB, p.B * p.H);
+    dim3 grid((p.T + kB - 1) / kB, slices);
     before_launch(id, s);
     kernel<<<grid, kThreads, smem, s>>>(p);
     after_launch(id, s);
@@ -389,14 +402,14 @@ cudaError_t launch(K kernel, int id, int tiles, const LayerArgs& p, cudaStream_t
 
 template <typename E, int D>
 cudaError_t fwd_d(const LayerArgs& p, cudaStream_t s) {
-    return launch<D>(fwd_kernel<E, D>, SAF_KERNEL_FWD, 4, p, s);
+    return launch<D>(fwd_kernel<E, D>, SAF_KERNEL_FWD, 4, p, s, p.B * p.H);
 }
 
 template <typename E, int D>
 cudaError_t bwd_d(const LayerArgs& p, cudaStream_t s) {
-    cudaError_t e = launch<D>(bwd_kv_kernel<E, D>, SAF_KERNEL_BWD_KV, 6, p, s);
+    cudaError_t e = launch<D>(bwd_kv_kernel<E, D>, SAF_KERNEL_BWD_KV, 6, p, s, p.B * p.Hkv);
     if (e != cudaSuccess) return e;
-    return launch<D>(bwd_q_kernel<E, D>, SAF_KERNEL_BWD_Q, 5, p, s);
+    return launch<D>(bwd_q_kernel<E, D>, SAF_KERNEL_BWD_Q, 5, p, s, p.B * p.H);
 }
 
 }  // namespace

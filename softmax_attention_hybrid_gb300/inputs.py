@@ -31,7 +31,7 @@ import dataclasses
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "frozen_mask", "make_inputs", "custom_workload"]
+__all__ = ["Workload", "WORKLOADS", "frozen_mask", "make_inputs", "make_gqa_inputs", "custom_workload"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -113,3 +113,16 @@ def make_inputs(w: Workload, seed: int = 0, T_prior: int | None = None):
     r = -w.slope * delta[None, :] + 0.5 * _normal((H, Tp), seed, 5)
     return {"q": q, "k": k, "v": v, "do": do, "a": a.contiguous(), "r": r.contiguous(),
             "frozen": frozen_mask(w)}
+
+
+def make_gqa_inputs(w: Workload, Hkv: int, seed: int = 0, T_prior: int | None = None):
+    """Inputs of a grouped-query layer with w.H query heads over Hkv shared
+    key/value heads (w.H a multiple of Hkv): the draws of make_inputs, with k
+    and v cut to their first Hkv heads ([B, Hkv, T, d]). q, dO, a, r and the
+    frozen flags stay per query head."""
+    if Hkv <= 0 or w.H % Hkv != 0:
+        raise ValueError("H must be a multiple of Hkv")
+    x = make_inputs(w, seed=seed, T_prior=T_prior)
+    x["k"] = x["k"][:, :Hkv].contiguous()
+    x["v"] = x["v"][:, :Hkv].contiguous()
+    return x

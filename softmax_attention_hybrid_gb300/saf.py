@@ -33,7 +33,7 @@ SAF_ESCRATCH = -9
 EXPORTED = ("saf_attn_workspace_bytes", "saf_attn_fwd", "saf_attn_bwd", "saf_device_status",
             "saf_error_string", "saf_version", "saf_set_trace_events", "saf_launch_count",
             "saf_attn_fwd_noalloc", "saf_fit_workspace_bytes", "saf_fit_compact",
-            "saf_pattern_grad")
+            "saf_pattern_grad", "saf_attn_fwd_gqa", "saf_attn_bwd_gqa")
 
 SAF_KERNEL_NONE = 0
 SAF_KERNEL_LOGNORM = 1
@@ -65,6 +65,10 @@ def _load():
     lib.saf_attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, vp, vp, vp]
     lib.saf_attn_fwd_noalloc.restype = i
     lib.saf_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, vp, vp, vp, vp, sz, vp]
+    lib.saf_attn_fwd_gqa.restype = i
+    lib.saf_attn_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, i, vp, vp, vp, sz, vp]
+    lib.saf_attn_bwd_gqa.restype = i
+    lib.saf_attn_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, i, vp, vp, vp, vp, sz, vp]
     lib.saf_attn_bwd.restype = i
     lib.saf_device_status.argtypes = [vp, vp]
     lib.saf_device_status.restype = i
@@ -198,6 +202,55 @@ def saf_attn_bwd(q, k, v, o, do, lse, a, r, frozen, dq=None, dk=None, dv=None, w
                            _ptr(workspace), workspace.numel(), _stream(stream))
     if st != SAF_OK:
         raise SafError(st, "saf_attn_bwd")
+    return dq, dk, dv
+
+
+def _gqa_shape(q, v, frozen):
+    B, Hkv, T, d = v.shape
+    if q is not None:
+        H = q.shape[1]
+    elif frozen is not None:
+        H = len(frozen)
+    else:
+        raise ValueError("q is needed unless the frozen mask gives H")
+    return B, H, Hkv, T, d
+
+
+def saf_attn_fwd_gqa(q, k, v, a, r, frozen, o=None, lse=None, workspace=None, stream=None):
+    """Grouped-query forward; returns (o, lse). q: [B, H, T, d]; k, v:
+    [B, Hkv, T, d] with H a multiple of Hkv (query head h reads key/value head
+    h // (H // Hkv)); a, r, frozen per query head, as for saf_attn_fwd."""
+    B, H, Hkv, T, d = _gqa_shape(q, v, frozen)
+    if o is None:
+        o = torch.empty((B, H, T, d), dtype=v.dtype, device=v.device)
+    if lse is None:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=v.device)
+    if workspace is None:
+        workspace = alloc_workspace(B, H, T, d, v.dtype, False, v.device)
+    ld = a.shape[1] if a is not None else T
+    st = _lib.saf_attn_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(r), int(ld), _frozen_bytes(frozen, H),
+                               B, H, Hkv, T, d, _dt(v), _ptr(o), _ptr(lse), _ptr(workspace), workspace.numel(),
+                               _stream(stream))
+    if st != SAF_OK:
+        raise SafError(st, "saf_attn_fwd_gqa")
+    return o, lse
+
+
+def saf_attn_bwd_gqa(q, k, v, o, do, lse, a, r, frozen, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Grouped-query backward; returns dq [B, H, T, d] and dk, dv [B, Hkv, T, d]
+    (a shared head's gradient is the sum over its query heads)."""
+    B, H, Hkv, T, d = _gqa_shape(q, v, frozen)
+    dq = torch.empty((B, H, T, d), dtype=v.dtype, device=v.device) if dq is None else dq
+    dk = torch.empty_like(v) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = alloc_workspace(B, H, T, d, v.dtype, True, v.device)
+    ld = a.shape[1] if a is not None else T
+    st = _lib.saf_attn_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(a), _ptr(r), int(ld),
+                               _frozen_bytes(frozen, H), B, H, Hkv, T, d, _dt(v), _ptr(dq), _ptr(dk), _ptr(dv),
+                               _ptr(workspace), workspace.numel(), _stream(stream))
+    if st != SAF_OK:
+        raise SafError(st, "saf_attn_bwd_gqa")
     return dq, dk, dv
 
 

@@ -177,3 +177,31 @@ def test_pattern_grad_argument_errors(saf):
     assert pg(frozen=fz, ld=255) == saf.SAF_EINVAL
     assert pg(frozen=fz, lse=F + 4) == saf.SAF_EALIGN
     assert pg(frozen=fz, a=F + 2) == saf.SAF_EALIGN
+
+
+def test_gqa_argument_errors(saf):
+    lib = saf.library()
+    F = FAKE
+
+    def fwd(**kw):
+        a = dict(H=8, Hkv=2, frozen=None, T=256, ws=F)
+        a.update(kw)
+        fz = a["frozen"]
+        fzp = (ctypes.c_uint8 * len(fz))(*fz) if fz is not None else None
+        return lib.saf_attn_fwd_gqa(F, F, F, F, F, 256, fzp, 1, a["H"], a["Hkv"], a["T"], 64, 0, F, F, a["ws"],
+                                    1 << 30, None)
+
+    def bwd(**kw):
+        a = dict(H=8, Hkv=2, T=256)
+        a.update(kw)
+        return lib.saf_attn_bwd_gqa(F, F, F, F, F, F, F, F, 256, None, 1, a["H"], a["Hkv"], a["T"], 64, 0, F, F, F,
+                                    F, 1 << 30, None)
+
+    assert fwd(Hkv=0) == saf.SAF_EINVAL
+    assert fwd(Hkv=3) == saf.SAF_EINVAL           # 8 query heads do not split over 3
+    assert fwd(Hkv=16) == saf.SAF_EINVAL          # more key/value heads than query heads
+    assert fwd(ws=None) == saf.SAF_EWORKSPACE     # a valid layout reaches the later checks
+    assert fwd(T=0, ws=None) == saf.SAF_OK
+    assert bwd(Hkv=-1) == saf.SAF_EINVAL
+    assert bwd(Hkv=5) == saf.SAF_EINVAL
+    assert bwd(T=0) == saf.SAF_OK
