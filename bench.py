@@ -48,7 +48,7 @@ from softmax_attention_hybrid_gb300.inputs import WORKLOADS, make_inputs, Worklo
 METRIC = "hybrid attention fwd+bwd TFLOP/s and tokens/s at 1 GB300; % of bf16 tensor peak"
 DEFAULT_WORKLOAD = "gpt2_124m_25"
 # timed after the headline workload in the same run, each with its all-ordinary run
-OTHER_WORKLOADS = ("gpt2_124m_50", "1b_25", "prefill_16k")
+OTHER_WORKLOADS = ("gpt2_124m_50", "1b_25", "prefill_16k", "gqa_32q8kv_4k")
 L2_FLUSH_BYTES = 256 << 20  # larger than the 129 MB L2
 
 
@@ -187,7 +187,8 @@ def oracle_sample(w: Workload, x, batches=2):
     import oracle
     nb = min(batches, w.B)
     a, r = x["a"].double().numpy(), x["r"].double().numpy()
-    sl = {(b, h): [x[n][b, h].double().numpy() for n in ("q", "k", "v", "do")]
+    G = w.H // (w.Hkv or w.H)   # query heads per key/value head
+    sl = {(b, h): [x[n][b, h if n in ("q", "do") else h // G].double().numpy() for n in ("q", "k", "v", "do")]
           for b in range(nb) for h in range(w.H)}
     flops = F.layer_flops(nb, w.H, sum(1 for h in range(w.H) if x["frozen"][h]), w.T, w.d,
                           backward=not w.fwd_only)
@@ -289,9 +290,11 @@ class Layer:
         self.frozen = self.x["frozen"]
         self.g = {n: self.x[n].to(dev) for n in ("q", "k", "v", "do", "a", "r")}
         B, H, T, d = w.B, w.H, w.T, w.d
-        self.o = torch.empty_like(self.g["v"])
+        self.gqa = w.Hkv is not None and w.Hkv != H
+        self.o = torch.empty_like(self.g["q"])
         self.lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
-        self.dq, self.dk, self.dv = (torch.empty_like(self.g["v"]) for _ in range(3))
+        self.dq = torch.empty_like(self.g["q"])
+        self.dk, self.dv = torch.empty_like(self.g["v"]), torch.empty_like(self.g["v"])
         self.ws = saf.alloc_workspace(B, H, T, d, self.g["v"].dtype, not w.fwd_only, dev)
         self.kernels = {"fwd": saf.SAF_KERNEL_FWD, "lognorm": saf.SAF_KERNEL_LOGNORM,
                         "pattern_prep": saf.SAF_KERNEL_PATTERN_PREP}
@@ -302,10 +305,12 @@ class Layer:
 
     def step(self, mask):
         saf, g = self.saf, self.g
-        saf.saf_attn_fwd(g["q"], g["k"], g["v"], g["a"], g["r"], mask, o=self.o, lse=self.lse, workspace=self.ws)
+        fwd = saf.saf_attn_fwd_gqa if self.gqa else saf.saf_attn_fwd
+        bwd = saf.saf_attn_bwd_gqa if self.gqa else saf.saf_attn_bwd
+        fwd(g["q"], g["k"], g["v"], g["a"], g["r"], mask, o=self.o, lse=self.lse, workspace=self.ws)
         if not self.w.fwd_only:
-            saf.saf_attn_bwd(g["q"], g["k"], g["v"], self.o, g["do"], self.lse, g["a"], g["r"], mask, dq=self.dq,
-                             dk=self.dk, dv=self.dv, workspace=self.ws)
+            bwd(g["q"], g["k"], g["v"], self.o, g["do"], self.lse, g["a"], g["r"], mask, dq=self.dq, dk=self.dk,
+                dv=self.dv, workspace=self.ws)
 
 
 def timed(saf, lay, mask, K, trace, flush, stream, world):
@@ -388,7 +393,7 @@ def measure_workload(saf, w, args, dev, world, rank, stream, flush, peaks, peak_
     out = {"ms_per_step": step_ms, "ms_spread": spread(ms), "value": flops / (step_ms * 1e-3) / 1e12,
            "unit": "TFLOP/s", "frac_of_bf16_peak": flops / world / (step_ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
            "tokens_per_s": w.B * w.T * world / (step_ms * 1e-3),
-           "config": {"B": w.B, "H": w.H, "F": w.F, "T": w.T, "d": w.d, "dtype": w.dtype,
+           "config": {"B": w.B, "H": w.H, "Hkv": w.Hkv or w.H, "F": w.F, "T": w.T, "d": w.d, "dtype": w.dtype,
                       "fwd_only": w.fwd_only},
            "roofline": kernel_roofline(dom, kms_dom, w, peaks, peak_src), "kernel_ms": kms}
     if w.F > 0:
@@ -507,11 +512,12 @@ def run_ours(args, w):
             for c in range(nch):
                 sl = slice(bounds[c], bounds[c + 1])
                 stream.wait_event(ev_in[c])
-                saf.saf_attn_fwd(g["q"][sl], g["k"][sl], g["v"][sl], g["a"], g["r"], frozen, o=o[sl], lse=lse[sl],
-                                 workspace=ws)
+                fwd = saf.saf_attn_fwd_gqa if lay.gqa else saf.saf_attn_fwd
+                bwd = saf.saf_attn_bwd_gqa if lay.gqa else saf.saf_attn_bwd
+                fwd(g["q"][sl], g["k"][sl], g["v"][sl], g["a"], g["r"], frozen, o=o[sl], lse=lse[sl], workspace=ws)
                 if not w.fwd_only:
-                    saf.saf_attn_bwd(g["q"][sl], g["k"][sl], g["v"][sl], o[sl], g["do"][sl], lse[sl], g["a"], g["r"],
-                                     frozen, dq=dq[sl], dk=dk[sl], dv=dv[sl], workspace=ws)
+                    bwd(g["q"][sl], g["k"][sl], g["v"][sl], o[sl], g["do"][sl], lse[sl], g["a"], g["r"], frozen,
+                        dq=dq[sl], dk=dk[sl], dv=dv[sl], workspace=ws)
                 e = torch.cuda.Event()
                 e.record(stream)
                 s_out.wait_event(e)

@@ -13,6 +13,7 @@ dimension 64 at T=4096, the systems runs use B=8; the 1B study runs T=8192):
     gpt2_124m_50  B=8  H=12 F=6  T=4096  d=64 bf16
     1b_25         B=2  H=32 F=8  T=8192  d=64 bf16
     prefill_16k   B=1  H=12 F=3  T=16384 d=64 bf16, forward only
+    gqa_32q8kv_4k B=4  H=32 (over Hkv=8 key/value heads) F=8 T=4096 d=64 bf16
 
 In every workload a[j] ~ N(0,1) (absolute key preference) and
 r[δ] = -slope*δ + 0.5 N(0,1) (relative distance preference), one row per
@@ -47,6 +48,7 @@ class Workload:
     slope: float        # r[δ] = -slope*δ + 0.5*N(0,1)
     fwd_only: bool = False
     frozen: tuple | None = None   # explicit frozen head list (overrides the F rule)
+    Hkv: int | None = None        # shared key/value heads (grouped-query layout); None: H
 
     @property
     def torch_dtype(self):
@@ -59,6 +61,9 @@ WORKLOADS = {
     "gpt2_124m_50": Workload("gpt2_124m_50", 8, 12, 6, 4096, 64, "bf16", 0.5, 0.02),
     "1b_25": Workload("1b_25", 2, 32, 8, 8192, 64, "bf16", 0.5, 0.01),
     "prefill_16k": Workload("prefill_16k", 1, 12, 3, 16384, 64, "bf16", 0.5, 0.005, fwd_only=True),
+    # 32 query heads over 8 key/value heads (the grouped-query layout of the paper's
+    # Qwen3-4B study, App. C.6) at head dimension 64, one frozen query head per group
+    "gqa_32q8kv_4k": Workload("gqa_32q8kv_4k", 4, 32, 8, 4096, 64, "bf16", 0.5, 0.02, Hkv=8),
 }
 
 
@@ -111,6 +116,10 @@ def make_inputs(w: Workload, seed: int = 0, T_prior: int | None = None):
     a = _normal((H, Tp), seed, 4)
     delta = torch.arange(Tp, dtype=torch.float32)
     r = -w.slope * delta[None, :] + 0.5 * _normal((H, Tp), seed, 5)
+    if w.Hkv is not None and w.Hkv != H:
+        # grouped-query layout: the same draws, k and v cut to their first Hkv heads
+        k = k[:, :w.Hkv].contiguous()
+        v = v[:, :w.Hkv].contiguous()
     return {"q": q, "k": k, "v": v, "do": do, "a": a.contiguous(), "r": r.contiguous(),
             "frozen": frozen_mask(w)}
 

@@ -127,3 +127,46 @@ def test_one_query_head_per_group_is_the_multi_head_layer(saf, dtype):
     # dQ sums its key-block contributions with floating-point reduce-adds, whose order
     # may differ between runs: one unit in the last place at most
     assert (b1[0].float() - b2[0].float()).abs().max().item() <= TOL[dtype][1]
+
+
+def test_full_size_grouped_layer_sampled(saf):
+    # the grouped-query bench workload (B4, 32 query heads over 8 key/value heads,
+    # T 4096, one frozen query head per group) in the launch configuration the
+    # benchmark times; two whole groups are compared element by element (every query
+    # head of the group, and the group sums dK, dV), the rest of the output is checked
+    # for finiteness and exact zeros
+    import concurrent.futures as cf
+    from softmax_attention_hybrid_gb300.inputs import WORKLOADS, make_inputs
+    w = WORKLOADS["gqa_32q8kv_4k"]
+    x = make_inputs(w, seed=0)
+    out = _run(saf, x)
+    G = w.H // w.Hkv
+    a, r = x["a"].double().numpy(), x["r"].double().numpy()
+    tol_o, tol_g = TOL[w.dtype]
+    err = {}
+    for b, hk in ((0, 0), (w.B - 1, w.Hkv - 1)):
+        k, v = (x[n][b, hk].double().numpy() for n in ("k", "v"))
+
+        def one(h):
+            q, do = (x[n][b, h].double().numpy() for n in ("q", "do"))
+            fz = bool(x["frozen"][h])
+            return h, oracle.head_fwd(q, k, v, a[h], r[h], fz), oracle.head_bwd(q, k, v, do, a[h], r[h], fz)
+
+        dk_ref = np.zeros_like(k)
+        dv_ref = np.zeros_like(v)
+        with cf.ThreadPoolExecutor(G) as ex:
+            for h, (o_ref, lse_ref), (dq_ref, dkh, dvh) in ex.map(one, range(hk * G, hk * G + G)):
+                for nm, ref in (("o", o_ref), ("lse", lse_ref), ("dq", dq_ref)):
+                    err[nm] = max(err.get(nm, 0.0), float(np.max(np.abs(_np(out[nm][b, h]) - ref))))
+                dk_ref += dkh
+                dv_ref += dvh
+        for nm, ref in (("dk", dk_ref), ("dv", dv_ref)):
+            err[nm] = max(err.get(nm, 0.0), float(np.max(np.abs(_np(out[nm][b, hk]) - ref))))
+    _parity_log.record("gqa_32q8kv_4k (2 groups)", err,
+                       {nm: (tol_o if nm in ("o", "lse") else tol_g) for nm in err})
+    assert err["o"] <= tol_o and err["lse"] <= tol_o, err
+    assert max(err["dq"], err["dk"], err["dv"]) <= tol_g, err
+    for nm, t in out.items():
+        assert torch.isfinite(t).all(), nm
+    fzh = [h for h in range(w.H) if x["frozen"][h]]
+    assert torch.all(out["dq"][:, fzh] == 0)
