@@ -220,14 +220,47 @@ SAF_API int saf_version(void);
  * Out: a, r: DEVICE fp32 [H, T], the fitted parameters (row stride T, ready to
  *      pass to saf_attn_fwd with ld_prior = T); loss: DEVICE fp32 [H], L at the
  *      result. The paper's acceptance statistic kappa (mean KL per row of the
- *      target from the fit) is loss[h] + (1/T) sum P log P of the target, a
- *      number the caller has from the target; a fit passes when kappa <= 0.2.
+ *      target from the fit) is loss[h] + (1/T) sum P log P of the target
+ *      (saf_fit_target_stats computes that term; saf_fit_from_target runs the
+ *      whole path); a fit passes when kappa <= 0.2.
  * workspace: DEVICE scratch of saf_fit_workspace_bytes(H, T) bytes, 256-byte
  * aligned. fp32 pointers must be 4-byte aligned. Work is enqueued on `stream`;
  * errors in the arguments return before any work is enqueued. */
 SAF_API size_t saf_fit_workspace_bytes(int H, int T);
 SAF_API int saf_fit_compact(const float* eta_abs, const float* eta_rel, int H, int T, int steps, float lr,
                             float* a, float* r, float* loss, void* workspace, size_t ws_bytes, void* stream);
+
+/* ---- From a measured target to accept / reject ------------------------------
+ * The selection algorithm's target steps (§3.2 "Fitting"; App. A.2; App. C.1):
+ * the measured mean attention matrix A of a head has its causal entries
+ * floored at 1e-9 and every row normalised, P = floor-and-normalise(A); Eq. 4
+ * needs only P's key-column sums eta_abs(j) = sum_{i >= j} P(i, j) and diagonal
+ * sums eta_rel(d) = sum_{i >= d} P(i, i - d); a fitted head is accepted when
+ * kappa = (1/T) sum_i KL(P(i, .) || W(i, .)) <= 0.2 nats (App. C.1). Since
+ * kappa = (1/T) sum_i sum_j P log P + L(a, r) with L the Eq. 4 loss, the
+ * target's negative entropy per row, negent = (1/T) sum P log P, completes it.
+ *
+ * saf_fit_target_stats
+ * In:  A: DEVICE fp32 [H, T, T] row-major; entries above the diagonal are not
+ *      read. P is never stored.
+ * Out: eta_abs, eta_rel: DEVICE fp32 [H, T]; negent: DEVICE fp32 [H].
+ * Sums run in a fixed order: results are the same on every run.
+ * workspace: DEVICE scratch of saf_fit_stats_workspace_bytes(H, T) bytes,
+ * 256-byte aligned. Errors: SAF_EINVAL (sizes, NULL), SAF_EALIGN, SAF_EWORKSPACE,
+ * SAF_EUNSUPPORTED (device), all before any work is enqueued.
+ *
+ * saf_fit_from_target: the whole path on the device: the statistics above,
+ * saf_fit_compact's `steps` Adam steps at rate `lr`, then kappa.
+ * Out: a, r: DEVICE fp32 [H, T] (the fitted pattern); kappa: DEVICE fp32 [H];
+ *      accept: DEVICE uint8 [H], 1 when kappa <= tol (the paper: 0.2).
+ * workspace: saf_fit_from_target_workspace_bytes(H, T) bytes, 256-byte aligned.
+ * Errors as above, and SAF_EINVAL for steps < 0, lr <= 0 or tol < 0. */
+SAF_API size_t saf_fit_stats_workspace_bytes(int H, int T);
+SAF_API int saf_fit_target_stats(const float* A, int H, int T, float* eta_abs, float* eta_rel, float* negent,
+                                 void* workspace, size_t ws_bytes, void* stream);
+SAF_API size_t saf_fit_from_target_workspace_bytes(int H, int T);
+SAF_API int saf_fit_from_target(const float* A, int H, int T, int steps, float lr, float tol, float* a, float* r,
+                                float* kappa, uint8_t* accept, void* workspace, size_t ws_bytes, void* stream);
 
 /* ---- Gradients of trainable patterns ---------------------------------------
  * For the variant whose patterns keep training (App. C.3.2): the gradients of

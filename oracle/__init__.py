@@ -22,6 +22,7 @@ from .saf_oracle import (  # noqa: F401
     FIT_TOL,
     floor_and_normalise,
     target_marginals,
+    target_negentropy,
     fit_loss,
     fit_grad,
     fit_compact,

@@ -366,6 +366,17 @@ def fit_compact(eta_abs, eta_rel, steps=FIT_STEPS, lr=FIT_LR, betas=(0.9, 0.999)
     return a, r
 
 
+def target_negentropy(P):
+    """(1/T) sum_i sum_{j <= i} P(i, j) log P(i, j) of a causal target (terms with
+    P = 0 contribute 0): the part of kappa that depends on the target alone, since
+    kappa = (1/T) sum_i KL(P(i, .) || P-hat(i, .)) splits into this and the cross
+    entropy of Eq. 4."""
+    P = np.tril(_as64(P))
+    T = P.shape[0]
+    pos = P > 0
+    return float(np.sum(P[pos] * np.log(P[pos]))) / T
+
+
 def fit_kl(P, a, r):
     """kappa = (1/T) sum_i KL(P(i, 0..i) || P-hat(i, 0..i)), P-hat from Eq. 3."""
     P = _as64(P)

@@ -154,11 +154,109 @@ fit_loss_kernel(const float* __restrict__ lz, const float* __restrict__ eta_abs,
     if (threadIdx.x == 0) loss[h] = red[0] / (float)T;
 }
 
+// ---------------------------------------------------------------------------
+// Target statistics: from a measured mean attention matrix A (dense, [T, T]
+// per head) to the fit's inputs. The selection algorithm floors the causal
+// entries at 1e-9 and normalises every row (P = floor-and-normalise(A)); the
+// fit then needs only the marginals eta_abs(j) = sum_{i >= j} P(i, j) and
+// eta_rel(d) = sum_{i >= d} P(i, i - d) (Eq. 4), and the acceptance test needs
+// (1/T) sum_i sum_j P log P, since
+//     kappa = (1/T) sum_i KL(P(i, .) || W(i, .)) = (1/T) sum P log P + L(a, r)
+// with L the Eq. 4 loss at the fitted (a, r) (the cross term is
+// sum_ij P(i, j) (a(j) + r(i - j)) - sum_i log Z(i) = T (-L)). P is never stored.
+// ---------------------------------------------------------------------------
+
+// One warp per row i of head h: s(i) = sum_{j <= i} f(i, j) with f = max(A, 1e-9),
+// and the row's sum_j P log P = (sum_j f log f) / s - log s.
+// Grid (ceil(T / 8), H), 256 threads.
+__global__ void __launch_bounds__(256)
+target_rows_kernel(const float* __restrict__ A, int T, float* __restrict__ rs, float* __restrict__ rplogp) {
+    const int h = blockIdx.y;
+    const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (i >= T) return;
+    const float* row = A + ((size_t)h * T + i) * T;
+    float sum = 0.f, flf = 0.f;
+    for (int j = lane; j <= i; j += 32) {
+        const float f = fmaxf(row[j], kFitFloor);
+        sum += f;
+        flf = fmaf(f, logf(f), flf);
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        flf += __shfl_xor_sync(0xffffffffu, flf, o);
+    }
+    if (lane == 0) {
+        rs[(size_t)h * T + i] = sum;
+        rplogp[(size_t)h * T + i] = flf / sum - logf(sum);
+    }
+}
+
+// Marginals of P: thread x of block (bx, h, z) sums column x (z = 0, eta_abs) or
+// diagonal x (z = 1, eta_rel) over rows i >= x in a fixed order, so the result
+// is the same on every run. Consecutive threads read consecutive addresses of a
+// row (column x, or i - x). Grid (ceil(T / 256), H, 2), 256 threads.
+__global__ void __launch_bounds__(256)
+target_marginals_kernel(const float* __restrict__ A, const float* __restrict__ rs, int T,
+                        float* __restrict__ eta_abs, float* __restrict__ eta_rel) {
+    const int h = blockIdx.y;
+    const bool rel = blockIdx.z != 0;
+    const int x = blockIdx.x * 256 + threadIdx.x;
+    if (x >= T) return;
+    const float* Ah = A + (size_t)h * T * T;
+    const float* sh = rs + (size_t)h * T;
+    float acc = 0.f;
+    for (int i = x; i < T; ++i) {
+        const float f = fmaxf(Ah[(size_t)i * T + (rel ? i - x : x)], kFitFloor);
+        acc += f / sh[i];
+    }
+    (rel ? eta_rel : eta_abs)[(size_t)h * T + x] = acc;
+}
+
+// negent[h] = (1/T) sum_i rplogp(i); one block per head, fixed-order tree.
+__global__ void __launch_bounds__(256)
+target_negent_kernel(const float* __restrict__ rplogp, int T, float* __restrict__ negent) {
+    const int h = blockIdx.x;
+    float s = 0.f;
+    for (int i = threadIdx.x; i < T; i += 256) s += rplogp[(size_t)h * T + i];
+    __shared__ float red[256];
+    red[threadIdx.x] = s;
+    __syncthreads();
+    for (int w = 128; w > 0; w >>= 1) {
+        if ((int)threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) negent[h] = red[0] / (float)T;
+}
+
+// kappa = negent + L at the fitted parameters; accepted when kappa <= tol.
+__global__ void target_kappa_kernel(const float* __restrict__ negent, const float* __restrict__ loss, int H,
+                                    float tol, float* __restrict__ kappa, uint8_t* __restrict__ accept) {
+    const int h = blockIdx.x * blockDim.x + threadIdx.x;
+    if (h >= H) return;
+    const float k = negent[h] + loss[h];
+    kappa[h] = k;
+    accept[h] = k <= tol ? 1 : 0;
+}
+
+struct StatsLayout {
+    size_t rs, rplogp, total;
+};
+
 struct FitLayout {
     size_t status, hflag, amax, lz, fa, fr, mom, total;
 };
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+StatsLayout stats_layout(int H, int T) {
+    StatsLayout L;
+    const size_t n = (size_t)H * T * sizeof(float);
+    L.rs = 0;
+    L.rplogp = align256(n);
+    L.total = align256(L.rplogp + n);
+    return L;
+}
 
 FitLayout fit_layout(int H, int T) {
     FitLayout L;
@@ -192,25 +290,24 @@ extern "C" size_t saf_fit_workspace_bytes(int H, int T) {
     return fit_layout(H, T).total;
 }
 
-extern "C" int saf_fit_compact(const float* eta_abs, const float* eta_rel, int H, int T, int steps, float lr,
-                               float* a, float* r, float* loss, void* workspace, size_t ws_bytes, void* stream) {
-    if (H <= 0 || H > SAF_MAX_HEADS || T <= 0 || steps < 0 || !(lr > 0.f) || !isfinite(lr)) return SAF_EINVAL;
-    if (!eta_abs || !eta_rel || !a || !r || !loss) return SAF_EINVAL;
-    const uintptr_t any = (uintptr_t)eta_abs | (uintptr_t)eta_rel | (uintptr_t)a | (uintptr_t)r | (uintptr_t)loss;
-    if (any & 3u) return SAF_EALIGN;
-    if (!workspace) return SAF_EWORKSPACE;
-    if (((uintptr_t)workspace & 255u) != 0) return SAF_EALIGN;
-    const FitLayout L = fit_layout(H, T);
-    if (ws_bytes < L.total) return SAF_EWORKSPACE;
+namespace saf {
+namespace {
+
+int check_fit_device() {
     int dev = 0;
     cudaDeviceProp prop;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
         cudaGetLastError();
         return SAF_ECUDA;
     }
-    if (!(prop.major == 10 && prop.minor == 3)) return SAF_EUNSUPPORTED;
-    cudaStream_t s = (cudaStream_t)stream;
-    char* ws = (char*)workspace;
+    return (prop.major == 10 && prop.minor == 3) ? SAF_OK : SAF_EUNSUPPORTED;
+}
+
+// The fit itself, arguments already checked: `steps` Adam steps from the
+// start point, then the Eq. 4 loss at the result.
+int run_fit(const float* eta_abs, const float* eta_rel, int H, int T, int steps, float lr, float* a, float* r,
+            float* loss, char* ws, cudaStream_t s) {
+    const FitLayout L = fit_layout(H, T);
     float* lz = (float*)(ws + L.lz);
     float* fa = (float*)(ws + L.fa);
     float* fr = (float*)(ws + L.fr);
@@ -264,4 +361,113 @@ extern "C" int saf_fit_compact(const float* eta_abs, const float* eta_rel, int H
     if (e == cudaSuccess) return SAF_OK;
     cudaGetLastError();
     return SAF_ELAUNCH;
+}
+
+// Target statistics into eta_abs, eta_rel [H, T] and negent [H].
+int run_stats(const float* A, int H, int T, float* eta_abs, float* eta_rel, float* negent, char* ws,
+              cudaStream_t s) {
+    const StatsLayout L = stats_layout(H, T);
+    float* rs = (float*)(ws + L.rs);
+    float* rplogp = (float*)(ws + L.rplogp);
+    note_launch();
+    target_rows_kernel<<<dim3((unsigned)((T + 7) / 8), (unsigned)H), 256, 0, s>>>(A, T, rs, rplogp);
+    note_launch();
+    target_marginals_kernel<<<dim3((unsigned)((T + 255) / 256), (unsigned)H, 2), 256, 0, s>>>(A, rs, T, eta_abs,
+                                                                                              eta_rel);
+    note_launch();
+    target_negent_kernel<<<H, 256, 0, s>>>(rplogp, T, negent);
+    if (cudaGetLastError() != cudaSuccess) return SAF_ELAUNCH;
+    return SAF_OK;
+}
+
+// Workspace of saf_fit_from_target: statistics, eta_abs, eta_rel, negent, loss, fit.
+struct PipeLayout {
+    size_t stats, eta_abs, eta_rel, negent, loss, fit, total;
+};
+PipeLayout pipe_layout(int H, int T) {
+    PipeLayout L;
+    const size_t n = (size_t)H * T * sizeof(float);
+    size_t off = 0;
+    L.stats = off;
+    off = align256(off + stats_layout(H, T).total);
+    L.eta_abs = off;
+    off = align256(off + n);
+    L.eta_rel = off;
+    off = align256(off + n);
+    L.negent = off;
+    off = align256(off + (size_t)H * sizeof(float));
+    L.loss = off;
+    off = align256(off + (size_t)H * sizeof(float));
+    L.fit = off;
+    off = align256(off + fit_layout(H, T).total);
+    L.total = off;
+    return L;
+}
+
+bool bad_align4(const void* p) { return ((uintptr_t)p & 3u) != 0; }
+
+}  // namespace
+}  // namespace saf
+
+extern "C" int saf_fit_compact(const float* eta_abs, const float* eta_rel, int H, int T, int steps, float lr,
+                               float* a, float* r, float* loss, void* workspace, size_t ws_bytes, void* stream) {
+    if (H <= 0 || H > SAF_MAX_HEADS || T <= 0 || steps < 0 || !(lr > 0.f) || !isfinite(lr)) return SAF_EINVAL;
+    if (!eta_abs || !eta_rel || !a || !r || !loss) return SAF_EINVAL;
+    const uintptr_t any = (uintptr_t)eta_abs | (uintptr_t)eta_rel | (uintptr_t)a | (uintptr_t)r | (uintptr_t)loss;
+    if (any & 3u) return SAF_EALIGN;
+    if (!workspace) return SAF_EWORKSPACE;
+    if (((uintptr_t)workspace & 255u) != 0) return SAF_EALIGN;
+    if (ws_bytes < fit_layout(H, T).total) return SAF_EWORKSPACE;
+    const int st = check_fit_device();
+    if (st != SAF_OK) return st;
+    return run_fit(eta_abs, eta_rel, H, T, steps, lr, a, r, loss, (char*)workspace, (cudaStream_t)stream);
+}
+
+extern "C" size_t saf_fit_stats_workspace_bytes(int H, int T) {
+    if (H <= 0 || H > SAF_MAX_HEADS || T <= 0) return 0;
+    return stats_layout(H, T).total;
+}
+
+extern "C" int saf_fit_target_stats(const float* A, int H, int T, float* eta_abs, float* eta_rel, float* negent,
+                                    void* workspace, size_t ws_bytes, void* stream) {
+    if (H <= 0 || H > SAF_MAX_HEADS || T <= 0) return SAF_EINVAL;
+    if (!A || !eta_abs || !eta_rel || !negent) return SAF_EINVAL;
+    if (bad_align4(A) || bad_align4(eta_abs) || bad_align4(eta_rel) || bad_align4(negent)) return SAF_EALIGN;
+    if (!workspace) return SAF_EWORKSPACE;
+    if (((uintptr_t)workspace & 255u) != 0) return SAF_EALIGN;
+    if (ws_bytes < stats_layout(H, T).total) return SAF_EWORKSPACE;
+    const int st = check_fit_device();
+    if (st != SAF_OK) return st;
+    return run_stats(A, H, T, eta_abs, eta_rel, negent, (char*)workspace, (cudaStream_t)stream);
+}
+
+extern "C" size_t saf_fit_from_target_workspace_bytes(int H, int T) {
+    if (H <= 0 || H > SAF_MAX_HEADS || T <= 0) return 0;
+    return pipe_layout(H, T).total;
+}
+
+extern "C" int saf_fit_from_target(const float* A, int H, int T, int steps, float lr, float tol, float* a, float* r,
+                                   float* kappa, uint8_t* accept, void* workspace, size_t ws_bytes, void* stream) {
+    if (H <= 0 || H > SAF_MAX_HEADS || T <= 0 || steps < 0 || !(lr > 0.f) || !isfinite(lr) || !(tol >= 0.f))
+        return SAF_EINVAL;
+    if (!A || !a || !r || !kappa || !accept) return SAF_EINVAL;
+    if (bad_align4(A) || bad_align4(a) || bad_align4(r) || bad_align4(kappa)) return SAF_EALIGN;
+    if (!workspace) return SAF_EWORKSPACE;
+    if (((uintptr_t)workspace & 255u) != 0) return SAF_EALIGN;
+    const PipeLayout L = pipe_layout(H, T);
+    if (ws_bytes < L.total) return SAF_EWORKSPACE;
+    int st = check_fit_device();
+    if (st != SAF_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    char* ws = (char*)workspace;
+    float* ea = (float*)(ws + L.eta_abs);
+    float* er = (float*)(ws + L.eta_rel);
+    float* ng = (float*)(ws + L.negent);
+    float* ls = (float*)(ws + L.loss);
+    if ((st = run_stats(A, H, T, ea, er, ng, ws + L.stats, s)) != SAF_OK) return st;
+    if ((st = run_fit(ea, er, H, T, steps, lr, a, r, ls, ws + L.fit, s)) != SAF_OK) return st;
+    note_launch();
+    target_kappa_kernel<<<(H + 127) / 128, 128, 0, s>>>(ng, ls, H, tol, kappa, accept);
+    if (cudaGetLastError() != cudaSuccess) return SAF_ELAUNCH;
+    return SAF_OK;
 }

@@ -33,7 +33,8 @@ SAF_ESCRATCH = -9
 EXPORTED = ("saf_attn_workspace_bytes", "saf_attn_fwd", "saf_attn_bwd", "saf_device_status",
             "saf_error_string", "saf_version", "saf_set_trace_events", "saf_launch_count",
             "saf_attn_fwd_noalloc", "saf_fit_workspace_bytes", "saf_fit_compact",
-            "saf_pattern_grad", "saf_attn_fwd_gqa", "saf_attn_bwd_gqa")
+            "saf_pattern_grad", "saf_attn_fwd_gqa", "saf_attn_bwd_gqa", "saf_fit_stats_workspace_bytes",
+            "saf_fit_target_stats", "saf_fit_from_target_workspace_bytes", "saf_fit_from_target")
 
 SAF_KERNEL_NONE = 0
 SAF_KERNEL_LOGNORM = 1
@@ -65,6 +66,14 @@ def _load():
     lib.saf_attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, vp, vp, vp]
     lib.saf_attn_fwd_noalloc.restype = i
     lib.saf_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, vp, vp, vp, vp, sz, vp]
+    lib.saf_fit_stats_workspace_bytes.restype = sz
+    lib.saf_fit_stats_workspace_bytes.argtypes = [i, i]
+    lib.saf_fit_target_stats.restype = i
+    lib.saf_fit_target_stats.argtypes = [vp, i, i, vp, vp, vp, vp, sz, vp]
+    lib.saf_fit_from_target_workspace_bytes.restype = sz
+    lib.saf_fit_from_target_workspace_bytes.argtypes = [i, i]
+    lib.saf_fit_from_target.restype = i
+    lib.saf_fit_from_target.argtypes = [vp, i, i, i, ctypes.c_float, ctypes.c_float, vp, vp, vp, vp, vp, sz, vp]
     lib.saf_attn_fwd_gqa.restype = i
     lib.saf_attn_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, i, vp, vp, vp, sz, vp]
     lib.saf_attn_bwd_gqa.restype = i
@@ -291,6 +300,40 @@ def saf_fit_compact(eta_abs, eta_rel, steps=400, lr=0.05, a=None, r=None, loss=N
     if st != SAF_OK:
         raise SafError(st, "saf_fit_compact")
     return a, r, loss
+
+
+def saf_fit_target_stats(A, stream=None):
+    """eta_abs, eta_rel [H, T] and negent [H] of the floored, row-normalised
+    targets of A (fp32 CUDA tensor [H, T, T])."""
+    H, T, _ = A.shape
+    dev = A.device
+    ea = torch.empty((H, T), dtype=torch.float32, device=dev)
+    er = torch.empty((H, T), dtype=torch.float32, device=dev)
+    ng = torch.empty((H,), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(int(_lib.saf_fit_stats_workspace_bytes(H, T)), 256), dtype=torch.uint8, device=dev)
+    st = _lib.saf_fit_target_stats(_ptr(A), H, T, _ptr(ea), _ptr(er), _ptr(ng), _ptr(ws), ws.numel(),
+                                   _stream(stream))
+    if st != SAF_OK:
+        raise SafError(st, "saf_fit_target_stats")
+    return ea, er, ng
+
+
+def saf_fit_from_target(A, steps=400, lr=0.05, tol=0.2, stream=None):
+    """Fit every head of A (fp32 CUDA tensor [H, T, T]) from its measured
+    pattern to accept / reject on the device; returns a, r [H, T], kappa [H]
+    and accept [H] (uint8)."""
+    H, T, _ = A.shape
+    dev = A.device
+    a = torch.empty((H, T), dtype=torch.float32, device=dev)
+    r = torch.empty((H, T), dtype=torch.float32, device=dev)
+    kappa = torch.empty((H,), dtype=torch.float32, device=dev)
+    accept = torch.empty((H,), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(int(_lib.saf_fit_from_target_workspace_bytes(H, T)), 256), dtype=torch.uint8, device=dev)
+    st = _lib.saf_fit_from_target(_ptr(A), H, T, int(steps), float(lr), float(tol), _ptr(a), _ptr(r), _ptr(kappa),
+                                  _ptr(accept), _ptr(ws), ws.numel(), _stream(stream))
+    if st != SAF_OK:
+        raise SafError(st, "saf_fit_from_target")
+    return a, r, kappa, accept
 
 
 def saf_pattern_grad(v, do, o, lse, a, r, frozen, da=None, dr=None, stream=None):

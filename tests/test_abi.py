@@ -205,3 +205,34 @@ def test_gqa_argument_errors(saf):
     assert bwd(Hkv=-1) == saf.SAF_EINVAL
     assert bwd(Hkv=5) == saf.SAF_EINVAL
     assert bwd(T=0) == saf.SAF_OK
+
+
+def test_fit_target_argument_errors(saf):
+    lib = saf.library()
+    F = FAKE
+    assert lib.saf_fit_stats_workspace_bytes(3, 256) > 0 and lib.saf_fit_stats_workspace_bytes(0, 256) == 0
+    assert lib.saf_fit_from_target_workspace_bytes(3, 256) >= lib.saf_fit_workspace_bytes(3, 256)
+
+    def stats(**kw):
+        a = dict(A=F, H=3, T=64, ea=F, er=F, ng=F, ws=F, wsb=1 << 30)
+        a.update(kw)
+        return lib.saf_fit_target_stats(a["A"], a["H"], a["T"], a["ea"], a["er"], a["ng"], a["ws"], a["wsb"], None)
+
+    def pipe(**kw):
+        a = dict(A=F, H=3, T=64, steps=400, lr=0.05, tol=0.2, a=F, r=F, k=F, acc=F, ws=F, wsb=1 << 30)
+        a.update(kw)
+        return lib.saf_fit_from_target(a["A"], a["H"], a["T"], a["steps"], a["lr"], a["tol"], a["a"], a["r"],
+                                       a["k"], a["acc"], a["ws"], a["wsb"], None)
+
+    assert stats(H=0) == saf.SAF_EINVAL
+    assert stats(A=None) == saf.SAF_EINVAL
+    assert stats(ea=F + 2) == saf.SAF_EALIGN
+    assert stats(ws=None) == saf.SAF_EWORKSPACE
+    assert stats(wsb=16) == saf.SAF_EWORKSPACE
+    assert pipe(steps=-1) == saf.SAF_EINVAL
+    assert pipe(tol=-0.1) == saf.SAF_EINVAL
+    assert pipe(lr=0.0) == saf.SAF_EINVAL
+    assert pipe(acc=None) == saf.SAF_EINVAL
+    assert pipe(k=F + 1) == saf.SAF_EALIGN
+    assert pipe(ws=F + 128) == saf.SAF_EALIGN
+    assert pipe(wsb=4096) == saf.SAF_EWORKSPACE

@@ -68,3 +68,63 @@ def test_fit_compact_zero_steps_is_the_start_point(saf):
     assert np.max(np.abs(a.double().cpu().numpy()[0] - ao)) == 0.0
     assert np.max(np.abs(r.double().cpu().numpy()[0] - ro)) < 1e-5
     assert abs(loss.item() - oracle.fit_loss(ao, ro, ea, er)) < 1e-4
+
+
+# ---------------------------------------------------------------------------
+# From a measured pattern to accept / reject on the device
+# ---------------------------------------------------------------------------
+
+def _measured(T, seed):
+    """Three 'measured' mean attention matrices (dense, with values above the
+    diagonal that must be ignored): a pattern from the family of Eq. 3 with
+    noise, a spiky random one (uniform draws to the 4th power: neither key
+    position nor distance decides its weights), and one that attends to key
+    i // 2 only (zeros elsewhere, which the 1e-9 floor turns into a valid
+    target)."""
+    g = np.random.default_rng(seed)
+    A0 = oracle.frozen_pattern(g.normal(size=T), -0.08 * np.arange(T) + 0.4 * g.normal(size=T), T)
+    A0 = A0 * (1.0 + 0.01 * g.random((T, T))) + np.triu(g.random((T, T)), 1)
+    A1 = g.random((T, T)) ** 4
+    A2 = np.zeros((T, T))
+    A2[np.arange(T), np.arange(T) // 2] = 1.0
+    A2 += np.triu(np.ones((T, T)), 1)
+    return np.stack([A0, A1, A2])
+
+
+@pytest.mark.parametrize("T", [96, 257])
+def test_target_stats_match_oracle(saf, T):
+    A = _measured(T, 60 + T)
+    ea, er, ng = saf.saf_fit_target_stats(_dev(A))
+    ea2, er2, ng2 = saf.saf_fit_target_stats(_dev(A))
+    torch.cuda.synchronize()
+    # fixed summation order: the same bits on every run
+    assert torch.equal(ea, ea2) and torch.equal(er, er2) and torch.equal(ng, ng2)
+    ea, er, ng = (x.double().cpu().numpy() for x in (ea, er, ng))
+    for h in range(A.shape[0]):
+        P = oracle.floor_and_normalise(A[h].astype(np.float32).astype(np.float64))
+        ea_ref, er_ref = oracle.target_marginals(P)
+        assert np.max(np.abs(ea[h] - ea_ref)) <= 1e-4 * max(1.0, np.max(ea_ref)), h
+        assert np.max(np.abs(er[h] - er_ref)) <= 1e-4 * max(1.0, np.max(er_ref)), h
+        assert abs(ng[h] - oracle.target_negentropy(P)) <= 1e-4, (h, ng[h], oracle.target_negentropy(P))
+
+
+def test_fit_from_target_accepts_and_rejects(saf):
+    # the whole selection path on the device: the noisy family pattern passes the
+    # 0.2-nat test, the spiky random pattern and the i // 2 pattern do not; kappa
+    # equals the fp64 KL of each target from the fitted pattern the device returns
+    T = 128
+    A = _measured(T, 64)
+    a, r, kappa, accept = saf.saf_fit_from_target(_dev(A), steps=oracle.FIT_STEPS, lr=oracle.FIT_LR,
+                                                  tol=oracle.FIT_TOL)
+    torch.cuda.synchronize()
+    a, r, kappa = (x.double().cpu().numpy() for x in (a, r, kappa))
+    accept = accept.cpu().numpy()
+    for h in range(3):
+        P = oracle.floor_and_normalise(A[h].astype(np.float32).astype(np.float64))
+        k_ref = oracle.fit_kl(P, a[h], r[h])
+        assert abs(kappa[h] - k_ref) <= 2e-4 + 1e-3 * k_ref, (h, kappa[h], k_ref)
+        assert accept[h] == (1 if kappa[h] <= oracle.FIT_TOL else 0)
+        # and the oracle's own fit of the same target takes the same decision
+        ao, ro = oracle.fit_compact(*oracle.target_marginals(P))
+        assert (oracle.fit_kl(P, ao, ro) <= oracle.FIT_TOL) == bool(accept[h]), h
+    assert accept.tolist() == [1, 0, 0]

@@ -494,6 +494,25 @@ def test_fit_rejects_a_pattern_outside_the_family():
     assert oracle.fit_kl(P, a, r) > oracle.FIT_TOL
 
 
+def test_target_negentropy_closed_form_and_kappa_split():
+    # uniform causal target P(i, j) = 1 / (i + 1): each row has entropy log(i + 1),
+    # so (1/T) sum P log P = -(1/T) sum_i log(i + 1) = -log(T!) / T
+    T = 30
+    P = oracle.floor_and_normalise(np.ones((T, T)))
+    assert abs(oracle.target_negentropy(P) + math.lgamma(T + 1) / T) < 1e-12
+    # a one-hot row contributes 0 (0 log 0 = 0, 1 log 1 = 0)
+    Pid = np.eye(T)
+    assert oracle.target_negentropy(Pid) == 0.0
+    # kappa = negentropy + Eq. 4 loss, for any (a, r) and any causal target
+    g = _rng(79)
+    Pt = oracle.floor_and_normalise(g.random((T, T)))
+    ea, er = oracle.target_marginals(Pt)
+    for _ in range(3):
+        a, r = g.normal(size=T), g.normal(size=T)
+        kl = oracle.fit_kl(Pt, a, r)
+        assert abs(kl - (oracle.target_negentropy(Pt) + oracle.fit_loss(a, r, ea, er))) < 1e-12
+
+
 def test_fit_start_point_closed_form():
     # App. C.1 starts the fit at a = 0 and r(delta) = log(eta_rel(delta) / (T - delta)):
     # the mean weight on diagonal delta, which holds T - delta entries. For the

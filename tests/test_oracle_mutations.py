@@ -53,6 +53,9 @@ MUTATIONS = {
     # fitting: Adam without the bias correction of its moments
     "fit_adam_no_bias_correction": ("mh = m[k] / (1 - b1 ** t)\n            vh = v[k] / (1 - b2 ** t)",
                                     "mh = m[k]\n            vh = v[k]"),
+    # target negentropy: the sum taken over the whole matrix after a flipped log
+    "negentropy_sign": ("return float(np.sum(P[pos] * np.log(P[pos]))) / T",
+                        "return float(np.sum(P[pos] * np.log(1.0 / P[pos]))) / T"),
     # grouped-query layout: query head mapped to its key/value head by h % g instead of h // g
     "gqa_head_map": ("head_fwd(q[b, h], k[b, h // g], v[b, h // g], a[h], r[h], bool(frozen[h]))",
                      "head_fwd(q[b, h], k[b, h % Hkv], v[b, h % Hkv], a[h], r[h], bool(frozen[h]))"),
