@@ -632,8 +632,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars.p_ready);
-                // dQ of the previous ordinary tile (its MMAs are done), staged in the buffer
-                // that held its dS
                 // dQ of the previous tile if it was ordinary (its MMAs are done), staged in the
                 // buffer that held its dS (gto has counted this tile if it is ordinary)
                 if (!kGrouped) {
