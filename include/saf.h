@@ -193,6 +193,29 @@ SAF_API int saf_attn_bwd_gqa(const void* q, const void* k, const void* v, const 
                      void* dq, void* dk, void* dv,
                      void* workspace, size_t ws_bytes, void* stream);
 
+/* Diagnostic forward pass for testing failure detection (the paper has no
+ * counterpart; it exercises this library's bounded waits).
+ *
+ * Every wait inside the tensor-core kernels is bounded: when it expires, the
+ * kernel records SAF_ETIMEOUT in the workspace's error word, its other warps
+ * give up too, it frees its tensor memory and returns, so the CUDA context
+ * stays usable. This entry point makes that happen on purpose, without any
+ * fault: it is saf_attn_fwd (SAF_BF16 only, else SAF_EUNSUPPORTED) with
+ *  - withhold = 1: the forward kernel's producer publishes no work item, so
+ *    every other role's first wait expires (o and lse are not written);
+ *    withhold = 0 runs the normal pass;
+ *  - wait_limit_us: the limit of every bounded wait in the forward kernel,
+ *    in microseconds (0: the default of 2 s). A wait ends at most one
+ *    suspend interval (about 10 ms) after its limit.
+ * The next saf_device_status on `workspace` reports SAF_ETIMEOUT after a
+ * withheld call; the next normal call clears the word. */
+SAF_API int saf_attn_fwd_diag(const void* q, const void* k, const void* v,
+                              const float* a, const float* r, int ld_prior, const uint8_t* frozen,
+                              int B, int H, int T, int d, saf_dtype_t dt,
+                              void* o, float* lse,
+                              void* workspace, size_t ws_bytes, void* stream,
+                              int withhold, unsigned wait_limit_us);
+
 /* Waits for `stream`, then reads the error word that the kernels of the last
  * call on `workspace` left there. Returns SAF_OK, SAF_ETIMEOUT, or
  * SAF_ECUDA if the stream reported a CUDA error. */

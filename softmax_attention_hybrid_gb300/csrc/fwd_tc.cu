@@ -80,6 +80,8 @@ struct FwdParams {
     int Hkv, G;        // key/value heads; query heads per key/value head (query head h reads h / G)
     int nqb, npairs, n_items;
     int slice_group;   // (batch, head) slices per item group
+    unsigned long long wait_ns;   // limit of every bounded wait (kWaitLimitNs unless a diagnostic call sets it)
+    int withhold;      // diagnostic: the producer publishes no work item, so every waiter gives up
     int n_ord, n_frz;
     uint8_t ord_heads[SAF_MAX_HEADS];
     uint8_t frz_heads[SAF_MAX_HEADS];
@@ -221,10 +223,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             bool ok = true;
             uint32_t ring_empty_bits = (1u << kRing) - 1;
             int slot = 0;
+            // diagnostic call: publish nothing and leave; the other roles' first waits expire
+            if (p.withhold) ok = false;
             while (ok) {
                 // next item from the global counter (longest first), published to the ring
                 if (!(ok = mbar_wait(&bars.item_empty[slot], (ring_empty_bits >> slot) & 1u, abort, status,
-                                     kStatusTimeout)))
+                                     kStatusTimeout, p.wait_ns)))
                     break;
                 ring_empty_bits ^= 1u << slot;
                 int idx = (int)atomicAdd(status + kCounterFwd, 1u);
@@ -245,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     // on the previous item
                     const int qs = nord++ & 1;
                     if (!(ok = mbar_wait(&bars.q_empty[qs], (q_empty_bits >> qs) & 1u, abort, status,
-                                         kStatusTimeout)))
+                                         kStatusTimeout, p.wait_ns)))
                         break;
                     q_empty_bits ^= 1u << qs;
                     uint8_t* sq = sm + SmemLayout::q + qs * SmemLayout::q_slot_bytes;
@@ -255,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 }
                 for (int j = 0; j < nblk; ++j) {
                     if (!(ok = mbar_wait(&bars.kv_empty[stage], (kv_empty_bits >> stage) & 1u, abort, status,
-                                         kStatusTimeout)))
+                                         kStatusTimeout, p.wait_ns)))
                         break;
                     kv_empty_bits ^= 1u << stage;
                     uint8_t* st = sm + SmemLayout::kv + stage * SmemLayout::stage_bytes;
@@ -297,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             int slot = 0;
             while (ok) {
                 if (!(ok = mbar_wait_warp(&bars.item_full[slot], (ring_full_bits >> slot) & 1u, abort, status,
-                                     kStatusTimeout)))
+                                     kStatusTimeout, p.wait_ns)))
                     break;
                 ring_full_bits ^= 1u << slot;
                 const int idx = item_ring[slot];
@@ -311,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 const int nblk = t1 ? qb1 + 1 : qb0 + 1;                 // key blocks of the item
                 if (!it.frozen) {
                     qs = nord++ & 1;
-                    if (!(ok = mbar_wait_warp(&bars.q_full[qs], (q_full_bits >> qs) & 1u, abort, status, kStatusTimeout)))
+                    if (!(ok = mbar_wait_warp(&bars.q_full[qs], (q_full_bits >> qs) & 1u, abort, status, kStatusTimeout, p.wait_ns)))
                         break;
                     q_full_bits ^= 1u << qs;
                     d_q = sdesc_sw128(smem_u32(sm + SmemLayout::q + qs * SmemLayout::q_slot_bytes) + g * kTileBytes, 16,
@@ -320,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 // stage index of block j is (stage + j) mod kStages
                 auto stage_of = [&](int j) { return (stage + j) % kStages; };
                 auto issue_s = [&](int j) -> bool {
-                    if (!mbar_wait_warp(&bars.s_empty[g], s_empty_ph, abort, status, kStatusTimeout)) return false;
+                    if (!mbar_wait_warp(&bars.s_empty[g], s_empty_ph, abort, status, kStatusTimeout, p.wait_ns)) return false;
                     s_empty_ph ^= 1;
                     tc_fence_after();
                     const uint64_t d_k =
@@ -336,11 +340,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 auto issue_pv = [&](int j) -> bool {
                     if (frz) {   // one barrier per W buffer: the softmax group may be a block ahead
                         const int b = j & 1;
-                        if (!mbar_wait_warp(&bars.w_full[g][b], (w_full_bits >> b) & 1u, abort, status, kStatusTimeout))
+                        if (!mbar_wait_warp(&bars.w_full[g][b], (w_full_bits >> b) & 1u, abort, status, kStatusTimeout, p.wait_ns))
                             return false;
                         w_full_bits ^= 1u << b;
                     } else {
-                        if (!mbar_wait_warp(&bars.p_full[g], p_full_ph, abort, status, kStatusTimeout)) return false;
+                        if (!mbar_wait_warp(&bars.p_full[g], p_full_ph, abort, status, kStatusTimeout, p.wait_ns)) return false;
                         p_full_ph ^= 1;
                     }
                     tc_fence_after();
@@ -358,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 auto ensure_kv = [&](int j) -> bool {
                     while (kv_ready <= j) {
                         const int s = stage_of(kv_ready);
-                        if (!mbar_wait_warp(&bars.kv_full[s], (kv_full_bits >> s) & 1u, abort, status, kStatusTimeout))
+                        if (!mbar_wait_warp(&bars.kv_full[s], (kv_full_bits >> s) & 1u, abort, status, kStatusTimeout, p.wait_ns))
                             return false;
                         kv_full_bits ^= 1u << s;
                         ++kv_ready;
@@ -377,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     // phase; its predecessor phase is taken here, before that last P V is issued,
                     // so that s_empty never runs two phases ahead of this thread.
                     if (ok && it.frozen && j + 1 == ng) {
-                        ok = mbar_wait_warp(&bars.s_empty[g], s_empty_ph, abort, status, kStatusTimeout);
+                        ok = mbar_wait_warp(&bars.s_empty[g], s_empty_ph, abort, status, kStatusTimeout, p.wait_ns);
                         s_empty_ph ^= 1;
                     }
                     if (ok && j < ng) ok = issue_pv(j);
@@ -406,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         bool w_pend[2] = {false, false};   // a P V that read W buffer b may not have been waited for
         auto wait_w = [&](int b) -> bool {
             if (!w_pend[b]) return true;
-            if (!mbar_wait(&bars.w_done[g][b], w_done_ph[b], abort, status, kStatusTimeout)) return false;
+            if (!mbar_wait(&bars.w_done[g][b], w_done_ph[b], abort, status, kStatusTimeout, p.wait_ns)) return false;
             w_done_ph[b] ^= 1;
             w_pend[b] = false;
             tc_fence_after();
@@ -439,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         int slot = 0;
         while (ok) {
             if (!(ok = mbar_wait(&bars.item_full[slot], (ring_full_bits >> slot) & 1u, abort, status,
-                                 kStatusTimeout)))
+                                 kStatusTimeout, p.wait_ns)))
                 break;
             ring_full_bits ^= 1u << slot;
             const int idx = item_ring[slot];
@@ -459,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             if (!it.frozen) {
                 float m_used = -INFINITY, l = 0.f;
                 for (int j = 0; j < nblk && ok; ++j) {
-                    if (!(ok = mbar_wait(&bars.s_full[g], s_full_ph, abort, status, kStatusTimeout))) break;
+                    if (!(ok = mbar_wait(&bars.s_full[g], s_full_ph, abort, status, kStatusTimeout, p.wait_ns))) break;
                     s_full_ph ^= 1;
                     tc_fence_after();
                     uint32_t sr[128];   // this row of S (raw scores)
@@ -508,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         pk[c] = pack_bf16(e.x, e.y);
                     }
                     if (j > 0) {   // P V of the previous block done: P is free, O is stable
-                        if (!(ok = mbar_wait(&bars.o_done[g], o_done_ph, abort, status, kStatusTimeout))) break;
+                        if (!(ok = mbar_wait(&bars.o_done[g], o_done_ph, abort, status, kStatusTimeout, p.wait_ns))) break;
                         o_done_ph ^= 1;
                         tc_fence_after();
                     }
@@ -535,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 }
                 if (!ok) break;
                 // epilogue: O = acc / l
-                if (!(ok = mbar_wait(&bars.o_done[g], o_done_ph, abort, status, kStatusTimeout))) break;
+                if (!(ok = mbar_wait(&bars.o_done[g], o_done_ph, abort, status, kStatusTimeout, p.wait_ns))) break;
                 o_done_ph ^= 1;
                 tc_fence_after();
                 store_o(bh, row, 1.f / l, (m_used + log2f(l)) / kLog2e);
@@ -551,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     const int G = gblk0 + j;
                     const int st = G % kStages;
                     if (!(ok = mbar_wait(&bars.kv_full[st], (uint32_t)(G / kStages) & 1u, abort, status,
-                                         kStatusTimeout)))
+                                         kStatusTimeout, p.wait_ns)))
                         break;
                     // W buffer j & 1 (P columns, or the S columns frozen items leave unused) is
                     // free once the P V of block j - 2 has read it
@@ -680,6 +684,8 @@ cudaError_t launch_tc_fwd(const LayerArgs& a, cudaStream_t s) {
     // query pairs re-read them.
     const size_t kv_all = (size_t)BHkv * 2 * (size_t)a.T * 64 * 2;
     p.slice_group = kv_all <= kL2GroupBytes ? a.B * a.H : kSliceGroup;
+    p.wait_ns = a.diag_wait_ns ? a.diag_wait_ns : kWaitLimitNs;
+    p.withhold = a.diag_withhold;
     for (int h = 0; h < a.H; ++h) {
         if (head_frozen(a.mask, h))
             p.frz_heads[p.n_frz++] = (uint8_t)h;

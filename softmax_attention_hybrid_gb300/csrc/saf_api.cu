@@ -231,6 +231,30 @@ int saf_attn_fwd_gqa(const void* q, const void* k, const void* v, const float* a
     return launch_status(e);
 }
 
+int saf_attn_fwd_diag(const void* q, const void* k, const void* v, const float* a, const float* r, int ld_prior,
+                      const uint8_t* frozen, int B, int H, int T, int d, saf_dtype_t dt, void* o, float* lse,
+                      void* workspace, size_t ws_bytes, void* stream, int withhold, unsigned wait_limit_us) {
+    if (dt != SAF_BF16) return SAF_EUNSUPPORTED;   // the bounded waits live in the tensor-core kernels
+    if (withhold != 0 && withhold != 1) return SAF_EINVAL;
+    Common c;
+    int st = validate(q, k, v, a, r, ld_prior, frozen, B, H, T, d, dt, workspace, ws_bytes, 0, &c);
+    if (st != SAF_OK) return st;
+    if (B == 0 || T == 0) return SAF_OK;
+    if (!o || !lse) return SAF_EINVAL;
+    if (!aligned16(o) || !aligned16(lse)) return SAF_EALIGN;
+    if ((st = check_device()) != SAF_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    LayerArgs p = make_args(q, k, v, a, r, ld_prior, B, H, T, c, workspace, 0, 1);
+    p.d = d;
+    p.out = o;
+    p.lse_out = lse;
+    p.diag_wait_ns = (unsigned long long)wait_limit_us * 1000ull;
+    p.diag_withhold = withhold;
+    cudaError_t e = begin_call(p, c, false, true, s);
+    if (e == cudaSuccess) e = launch_tc_fwd(p, s);
+    return launch_status(e);
+}
+
 int saf_attn_fwd(const void* q, const void* k, const void* v, const float* a, const float* r, int ld_prior,
                  const uint8_t* frozen, int B, int H, int T, int d, saf_dtype_t dt, void* o, float* lse,
                  void* workspace, size_t ws_bytes, void* stream) {

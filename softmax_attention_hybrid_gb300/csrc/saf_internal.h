@@ -142,6 +142,10 @@ struct LayerArgs {
     int Hkv;             // key/value heads: query head h reads key/value head h / (H / Hkv)
     int d;               // head dimension
     HeadMask mask;
+    // diagnostic forward only (saf_attn_fwd_diag): a shorter limit for every bounded
+    // wait (0: the default), and a producer that withholds every work item
+    unsigned long long diag_wait_ns;
+    int diag_withhold;
 };
 
 // Launch bookkeeping (saf_api.cu): call before_launch(kernel id, stream)

@@ -69,17 +69,19 @@ __device__ __forceinline__ uint32_t mbar_try_wait_suspend(uint64_t* bar, uint32_
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // Wait for phase `parity` of `bar` to complete. Gives up when `abort` (a
-// shared flag) is set by another thread, or after kWaitLimitNs; in the
+// shared flag) is set by another thread, or after limit_ns (kWaitLimitNs unless
+// a diagnostic call shortens it); in the
 // latter case it sets `abort`, ORs `timeout_bit` into *status and returns
 // false. Every wait in the kernels goes through here, so no wait is endless.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          uint32_t* status, uint32_t timeout_bit) {
+                                          uint32_t* status, uint32_t timeout_bit,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait_suspend(bar, parity)) return true;
         if (*abort) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             *abort = 1;
             atomicOr(status, timeout_bit);
             return false;
@@ -258,9 +260,10 @@ __device__ __forceinline__ void mma_commit_warp(uint64_t* bar) {
 // warp, so the lane that issues the next asynchronous operation is the one that
 // observed the phase.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                               uint32_t* status, uint32_t timeout_bit) {
+                                               uint32_t* status, uint32_t timeout_bit,
+                                               uint64_t limit_ns = kWaitLimitNs) {
     int ok = 1;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, status, timeout_bit) ? 1 : 0;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, status, timeout_bit, limit_ns) ? 1 : 0;
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 

@@ -34,7 +34,8 @@ EXPORTED = ("saf_attn_workspace_bytes", "saf_attn_fwd", "saf_attn_bwd", "saf_dev
             "saf_error_string", "saf_version", "saf_set_trace_events", "saf_launch_count",
             "saf_attn_fwd_noalloc", "saf_fit_workspace_bytes", "saf_fit_compact",
             "saf_pattern_grad", "saf_attn_fwd_gqa", "saf_attn_bwd_gqa", "saf_fit_stats_workspace_bytes",
-            "saf_fit_target_stats", "saf_fit_from_target_workspace_bytes", "saf_fit_from_target")
+            "saf_fit_target_stats", "saf_fit_from_target_workspace_bytes", "saf_fit_from_target",
+            "saf_attn_fwd_diag")
 
 SAF_KERNEL_NONE = 0
 SAF_KERNEL_LOGNORM = 1
@@ -74,6 +75,9 @@ def _load():
     lib.saf_fit_from_target_workspace_bytes.argtypes = [i, i]
     lib.saf_fit_from_target.restype = i
     lib.saf_fit_from_target.argtypes = [vp, i, i, i, ctypes.c_float, ctypes.c_float, vp, vp, vp, vp, vp, sz, vp]
+    lib.saf_attn_fwd_diag.restype = i
+    lib.saf_attn_fwd_diag.argtypes = [vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, vp, vp, vp, sz, vp, i,
+                                      ctypes.c_uint]
     lib.saf_attn_fwd_gqa.restype = i
     lib.saf_attn_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, i, vp, vp, vp, sz, vp]
     lib.saf_attn_bwd_gqa.restype = i
@@ -176,6 +180,28 @@ def saf_attn_fwd(q, k, v, a, r, frozen, o=None, lse=None, workspace=None, stream
     if st != SAF_OK:
         raise SafError(st, "saf_attn_fwd")
     return o, lse
+
+
+def saf_attn_fwd_diag(q, k, v, a, r, frozen, withhold, wait_limit_us, o=None, lse=None, workspace=None,
+                      stream=None):
+    """Diagnostic forward for testing failure detection: with withhold=1 the
+    kernel's producer publishes no work item and every bounded wait expires
+    after wait_limit_us; returns (o, lse, workspace). Read the result with
+    saf_device_status(workspace)."""
+    B, H, T, d = v.shape
+    if o is None:
+        o = torch.empty_like(v)
+    if lse is None:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=v.device)
+    if workspace is None:
+        workspace = alloc_workspace(B, H, T, d, v.dtype, False, v.device)
+    ld = a.shape[1] if a is not None else T
+    st = _lib.saf_attn_fwd_diag(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(r), int(ld), _frozen_bytes(frozen, H),
+                                B, H, T, d, _dt(v), _ptr(o), _ptr(lse), _ptr(workspace), workspace.numel(),
+                                _stream(stream), int(withhold), int(wait_limit_us))
+    if st != SAF_OK:
+        raise SafError(st, "saf_attn_fwd_diag")
+    return o, lse, workspace
 
 
 def saf_attn_fwd_noalloc(q, k, v, a, r, frozen, o=None, lse=None, stream=None):

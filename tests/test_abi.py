@@ -236,3 +236,18 @@ def test_fit_target_argument_errors(saf):
     assert pipe(k=F + 1) == saf.SAF_EALIGN
     assert pipe(ws=F + 128) == saf.SAF_EALIGN
     assert pipe(wsb=4096) == saf.SAF_EWORKSPACE
+
+
+def test_diag_argument_errors(saf):
+    lib = saf.library()
+    F = FAKE
+
+    def diag(**kw):
+        a = dict(dt=0, withhold=1, wait=1000, ws=F)
+        a.update(kw)
+        return lib.saf_attn_fwd_diag(F, F, F, F, F, 256, None, 1, 4, 256, 64, a["dt"], F, F, a["ws"], 1 << 30,
+                                     None, a["withhold"], a["wait"])
+
+    assert diag(dt=1) == saf.SAF_EUNSUPPORTED     # the bounded waits live in the tensor-core kernels
+    assert diag(withhold=2) == saf.SAF_EINVAL
+    assert diag(ws=None) == saf.SAF_EWORKSPACE
