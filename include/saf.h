@@ -193,6 +193,43 @@ SAF_API int saf_attn_bwd_gqa(const void* q, const void* k, const void* v, const 
                      void* dq, void* dk, void* dv,
                      void* workspace, size_t ws_bytes, void* stream);
 
+/* ---- Prepared frozen-pattern state -------------------------------------------
+ * A frozen head's pattern depends on a and r alone (§3.2, Eq. 3), so its
+ * normalisers can be computed once and kept: the paper's persistent state per
+ * replaced head is alpha, rho, the normalisers and a small relative-distance
+ * band (§3.3 "precomputed normalisers"; App. D.2). saf_attn_fwd / saf_attn_bwd
+ * recompute them in every call; the calls below take them from a state that
+ * saf_frozen_prepare filled once for fixed (a, r).
+ *
+ * saf_frozen_state_bytes: bytes of DEVICE state for H heads of length T
+ * (0 for invalid sizes). It does not depend on B.
+ *
+ * saf_frozen_prepare: fills `state` (caller-owned, 256-byte aligned) for the
+ * frozen heads of `frozen` from a, r [H, ld_prior]. Enqueued on `stream`.
+ * Prepare again after a or r change (the trainable variant of App. C.3.2
+ * refreshes its normalisers after each update).
+ *
+ * saf_attn_fwd_prepared / saf_attn_bwd_prepared: saf_attn_fwd_gqa /
+ * saf_attn_bwd_gqa (Hkv = H for the multi-head layer) with the frozen-pattern
+ * data read from `state`. a, r, ld_prior and frozen must be the ones the state
+ * was prepared with (the fp32 path still reads a and r). `workspace` is the
+ * per-call workspace of saf_attn_workspace_bytes. Calls may share one state
+ * while nothing prepares it again. Results equal those of the unprepared
+ * calls up to rounding (the forward's exactly). Errors as the unprepared
+ * calls, and SAF_EWORKSPACE for a NULL state. */
+SAF_API size_t saf_frozen_state_bytes(int H, int T, saf_dtype_t dt);
+SAF_API int saf_frozen_prepare(const float* a, const float* r, int ld_prior, const uint8_t* frozen, int H, int T,
+                               saf_dtype_t dt, void* state, size_t state_bytes, void* stream);
+SAF_API int saf_attn_fwd_prepared(const void* q, const void* k, const void* v, const float* a, const float* r,
+                                  int ld_prior, const uint8_t* frozen, const void* state, int B, int H, int Hkv,
+                                  int T, int d, saf_dtype_t dt, void* o, float* lse, void* workspace,
+                                  size_t ws_bytes, void* stream);
+SAF_API int saf_attn_bwd_prepared(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                                  const float* lse, const float* a, const float* r, int ld_prior,
+                                  const uint8_t* frozen, const void* state, int B, int H, int Hkv, int T, int d,
+                                  saf_dtype_t dt, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+                                  void* stream);
+
 /* Diagnostic forward pass for testing failure detection (the paper has no
  * counterpart; it exercises this library's bounded waits).
  *

@@ -487,11 +487,12 @@ cudaError_t launch_bwd_delta(const LayerArgs& p, bool bf16, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_prep(const LayerArgs& p, cudaStream_t s) {
+cudaError_t launch_bwd_prep(const LayerArgs& p, cudaStream_t s, bool frozen_part) {
     const int nqb = (p.T + 127) / 128;
     const int Tp = nqb * 128;
     const int BH = p.B * p.H;
-    const long long blocks = (long long)BH * 2 * nqb + (long long)count_frozen(p) * ((Tp + 255) / 256);
+    const long long blocks =
+        (long long)BH * 2 * nqb + (frozen_part ? (long long)count_frozen(p) * ((Tp + 255) / 256) : 0);
     before_launch(SAF_KERNEL_BWD_DELTA, s);
     const cudaError_t e = launch_ex(bwd_prep_kernel, dim3((unsigned)blocks), dim3(256), 0, s, true, 1,
                                     (const __nv_bfloat16*)p.o, (const __nv_bfloat16*)p.dO, p.lse, p.mask, p.H, p.T,

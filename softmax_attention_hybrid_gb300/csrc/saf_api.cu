@@ -304,6 +304,132 @@ int saf_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
                             ws_bytes, stream);
 }
 
+// ---------------------------------------------------------------------------
+// Prepared frozen-pattern state: the normalisers and padded slices of the frozen
+// heads, computed once for fixed (a, r) and reused by every call.
+// ---------------------------------------------------------------------------
+
+size_t saf_frozen_state_bytes(int H, int T, saf_dtype_t dt) {
+    if (H <= 0 || H > SAF_MAX_HEADS || T <= 0) return 0;
+    if (dt != SAF_BF16 && dt != SAF_FP32) return 0;
+    return workspace_layout(0, H, T, 0, dt == SAF_BF16).total;
+}
+
+int saf_frozen_prepare(const float* a, const float* r, int ld_prior, const uint8_t* frozen, int H, int T,
+                       saf_dtype_t dt, void* state, size_t state_bytes, void* stream) {
+    if (H <= 0 || H > SAF_MAX_HEADS || T <= 0) return SAF_EINVAL;
+    if (dt != SAF_BF16 && dt != SAF_FP32) return SAF_EINVAL;
+    Common c;
+    memset(&c, 0, sizeof(c));
+    for (int h = 0; h < H; ++h)
+        if (frozen && frozen[h]) {
+            c.mask.w[h >> 6] |= 1ull << (h & 63);
+            c.nfrozen++;
+        }
+    if (c.nfrozen > 0 && (!a || !r || ld_prior < T)) return SAF_EINVAL;
+    if ((a && ((uintptr_t)a & 3u)) || (r && ((uintptr_t)r & 3u))) return SAF_EALIGN;
+    if (!state) return SAF_EWORKSPACE;
+    if (((uintptr_t)state & 255u) != 0) return SAF_EALIGN;
+    if (state_bytes < saf_frozen_state_bytes(H, T, dt)) return SAF_EWORKSPACE;
+    int st = check_device();
+    if (st != SAF_OK) return st;
+    const bool bf16 = dt == SAF_BF16;
+    LayerArgs p = make_args(nullptr, nullptr, nullptr, a, r, ld_prior, 0, H, T, c, state, 0, bf16);
+    return launch_status(begin_call(p, c, false, bf16, (cudaStream_t)stream));
+}
+
+namespace saf {
+namespace {
+// The frozen-pattern fields of p point into a prepared state instead of the workspace.
+void use_state(LayerArgs& p, const void* state, int H, int T, bool bf16) {
+    const WorkspaceLayout L = workspace_layout(0, H, T, 0, bf16);
+    char* st = (char*)state;
+    p.lz = (float*)(st + L.lz);
+    p.hflag = (uint32_t*)(st + L.hflag);
+    p.amax = (float*)(st + L.amax);
+    p.a2p = bf16 ? (float*)(st + L.a2p) : nullptr;
+    p.r2p = bf16 ? (float*)(st + L.r2p) : nullptr;
+    p.eap = bf16 ? (float*)(st + L.eap) : nullptr;
+    p.erp = bf16 ? (float*)(st + L.erp) : nullptr;
+    p.invz = bf16 ? (float*)(st + L.invz) : nullptr;
+}
+// First kernel of a prepared call: clears the workspace's status words (error word
+// and work counters) and nothing else: with no frozen head in its mask the init
+// kernel touches no frozen-pattern data, and its per-head flags go to the
+// workspace's own (unused) flag region.
+cudaError_t clear_call(const LayerArgs& ws_view, bool bf16, cudaStream_t s) {
+    LayerArgs q = ws_view;
+    memset(&q.mask, 0, sizeof(q.mask));
+    return launch_call_init(q, false, bf16, s);
+}
+}  // namespace
+}  // namespace saf
+
+int saf_attn_fwd_prepared(const void* q, const void* k, const void* v, const float* a, const float* r,
+                          int ld_prior, const uint8_t* frozen, const void* state, int B, int H, int Hkv, int T, int d,
+                          saf_dtype_t dt, void* o, float* lse, void* workspace, size_t ws_bytes, void* stream) {
+    if (Hkv <= 0 || H <= 0 || H % Hkv != 0) return SAF_EINVAL;
+    Common c;
+    int st = validate(q, k, v, a, r, ld_prior, frozen, B, H, T, d, dt, workspace, ws_bytes, 0, &c);
+    if (st != SAF_OK) return st;
+    if (B == 0 || T == 0) return SAF_OK;
+    if (!o || !lse) return SAF_EINVAL;
+    if (!aligned16(o) || !aligned16(lse)) return SAF_EALIGN;
+    if (!state) return SAF_EWORKSPACE;
+    if (((uintptr_t)state & 255u) != 0) return SAF_EALIGN;
+    if ((st = check_device()) != SAF_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool bf16 = dt == SAF_BF16;
+    LayerArgs p = make_args(q, k, v, a, r, ld_prior, B, H, T, c, workspace, 0, bf16);
+    p.Hkv = Hkv;
+    p.d = d;
+    p.out = o;
+    p.lse_out = lse;
+    cudaError_t e = clear_call(p, bf16, s);
+    use_state(p, state, H, T, bf16);
+    if (e == cudaSuccess) e = bf16 ? launch_tc_fwd(p, s) : launch_simt_fwd(p, false, s);
+    return launch_status(e);
+}
+
+int saf_attn_bwd_prepared(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                          const float* lse, const float* a, const float* r, int ld_prior, const uint8_t* frozen,
+                          const void* state, int B, int H, int Hkv, int T, int d, saf_dtype_t dt, void* dq, void* dk,
+                          void* dv, void* workspace, size_t ws_bytes, void* stream) {
+    if (Hkv <= 0 || H <= 0 || H % Hkv != 0) return SAF_EINVAL;
+    Common c;
+    int st = validate(q, k, v, a, r, ld_prior, frozen, B, H, T, d, dt, workspace, ws_bytes, 1, &c);
+    if (st != SAF_OK) return st;
+    if (B == 0 || T == 0) return SAF_OK;
+    if (!o || !dO || !lse || !dq || !dk || !dv) return SAF_EINVAL;
+    if (!aligned16(o) || !aligned16(dO) || !aligned16(lse) || !aligned16(dq) || !aligned16(dk) ||
+        !aligned16(dv))
+        return SAF_EALIGN;
+    if (!state) return SAF_EWORKSPACE;
+    if (((uintptr_t)state & 255u) != 0) return SAF_EALIGN;
+    if ((st = check_device()) != SAF_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool bf16 = dt == SAF_BF16;
+    LayerArgs p = make_args(q, k, v, a, r, ld_prior, B, H, T, c, workspace, 1, bf16);
+    p.Hkv = Hkv;
+    p.d = d;
+    p.o = o;
+    p.dO = dO;
+    p.lse = lse;
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    cudaError_t e = clear_call(p, bf16, s);
+    use_state(p, state, H, T, bf16);
+    if (bf16) {
+        if (e == cudaSuccess) e = launch_bwd_prep(p, s, false);
+        if (e == cudaSuccess) e = launch_tc_bwd(p, s);
+    } else {
+        if (e == cudaSuccess && c.nfrozen < H) e = launch_bwd_delta(p, false, s);
+        if (e == cudaSuccess) e = launch_simt_bwd(p, false, s);
+    }
+    return launch_status(e);
+}
+
 int saf_device_status(const void* workspace, void* stream) {
     if (!workspace) return SAF_EWORKSPACE;
     cudaStream_t s = (cudaStream_t)stream;

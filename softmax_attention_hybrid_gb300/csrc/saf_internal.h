@@ -169,7 +169,9 @@ cudaError_t launch_call_init(const LayerArgs& p, bool pad, bool pdl, cudaStream_
 cudaError_t launch_lognorm(const LayerArgs& p, bool pre, bool pdl, cudaStream_t s);
 // Tensor-core backward prep: per-tile lse and D rows, the zeroed dQ
 // accumulator of ordinary heads, and 1 / Z' of frozen heads from lse.
-cudaError_t launch_bwd_prep(const LayerArgs& p, cudaStream_t s);
+// frozen_part: also 1 / Z' and the exact-form flags of the frozen heads, from the
+// log Z rows of lse (false when a prepared frozen-pattern state already holds them).
+cudaError_t launch_bwd_prep(const LayerArgs& p, cudaStream_t s, bool frozen_part = true);
 cudaError_t launch_bwd_delta(const LayerArgs& p, bool bf16, cudaStream_t s);
 
 // fwd_tc.cu: tensor-core forward (bf16)

@@ -35,7 +35,8 @@ EXPORTED = ("saf_attn_workspace_bytes", "saf_attn_fwd", "saf_attn_bwd", "saf_dev
             "saf_attn_fwd_noalloc", "saf_fit_workspace_bytes", "saf_fit_compact",
             "saf_pattern_grad", "saf_attn_fwd_gqa", "saf_attn_bwd_gqa", "saf_fit_stats_workspace_bytes",
             "saf_fit_target_stats", "saf_fit_from_target_workspace_bytes", "saf_fit_from_target",
-            "saf_attn_fwd_diag")
+            "saf_attn_fwd_diag", "saf_frozen_state_bytes", "saf_frozen_prepare", "saf_attn_fwd_prepared",
+            "saf_attn_bwd_prepared")
 
 SAF_KERNEL_NONE = 0
 SAF_KERNEL_LOGNORM = 1
@@ -75,6 +76,15 @@ def _load():
     lib.saf_fit_from_target_workspace_bytes.argtypes = [i, i]
     lib.saf_fit_from_target.restype = i
     lib.saf_fit_from_target.argtypes = [vp, i, i, i, ctypes.c_float, ctypes.c_float, vp, vp, vp, vp, vp, sz, vp]
+    lib.saf_frozen_state_bytes.restype = sz
+    lib.saf_frozen_state_bytes.argtypes = [i, i, i]
+    lib.saf_frozen_prepare.restype = i
+    lib.saf_frozen_prepare.argtypes = [vp, vp, i, vp, i, i, i, vp, sz, vp]
+    lib.saf_attn_fwd_prepared.restype = i
+    lib.saf_attn_fwd_prepared.argtypes = [vp, vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, i, vp, vp, vp, sz, vp]
+    lib.saf_attn_bwd_prepared.restype = i
+    lib.saf_attn_bwd_prepared.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, i, vp, vp, vp,
+                                          vp, sz, vp]
     lib.saf_attn_fwd_diag.restype = i
     lib.saf_attn_fwd_diag.argtypes = [vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, vp, vp, vp, sz, vp, i,
                                       ctypes.c_uint]
@@ -286,6 +296,59 @@ def saf_attn_bwd_gqa(q, k, v, o, do, lse, a, r, frozen, dq=None, dk=None, dv=Non
                                _ptr(workspace), workspace.numel(), _stream(stream))
     if st != SAF_OK:
         raise SafError(st, "saf_attn_bwd_gqa")
+    return dq, dk, dv
+
+
+def saf_frozen_prepare(a, r, frozen, T, dtype, state=None, stream=None):
+    """Fill (and return) the prepared frozen-pattern state of a, r ([H, ld_prior]
+    fp32 CUDA tensors) for sequences of length T in `dtype`."""
+    H = a.shape[0]
+    dt = SAF_BF16 if dtype in (torch.bfloat16, SAF_BF16, "bf16") else SAF_FP32
+    n = int(_lib.saf_frozen_state_bytes(H, int(T), dt))
+    if state is None:
+        state = torch.empty(max(n, 256), dtype=torch.uint8, device=a.device)
+    st = _lib.saf_frozen_prepare(_ptr(a), _ptr(r), int(a.shape[1]), _frozen_bytes(frozen, H), H, int(T), dt,
+                                 _ptr(state), state.numel(), _stream(stream))
+    if st != SAF_OK:
+        raise SafError(st, "saf_frozen_prepare")
+    return state
+
+
+def saf_attn_fwd_prepared(q, k, v, a, r, frozen, state, o=None, lse=None, workspace=None, stream=None):
+    """Forward with the frozen-pattern data from a prepared state (grouped-query
+    shapes allowed: k, v [B, Hkv, T, d]); returns (o, lse)."""
+    B, H, Hkv, T, d = _gqa_shape(q, v, frozen)
+    if o is None:
+        o = torch.empty((B, H, T, d), dtype=v.dtype, device=v.device)
+    if lse is None:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=v.device)
+    if workspace is None:
+        workspace = alloc_workspace(B, H, T, d, v.dtype, False, v.device)
+    ld = a.shape[1] if a is not None else T
+    st = _lib.saf_attn_fwd_prepared(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(r), int(ld), _frozen_bytes(frozen, H),
+                                    _ptr(state), B, H, Hkv, T, d, _dt(v), _ptr(o), _ptr(lse), _ptr(workspace),
+                                    workspace.numel(), _stream(stream))
+    if st != SAF_OK:
+        raise SafError(st, "saf_attn_fwd_prepared")
+    return o, lse
+
+
+def saf_attn_bwd_prepared(q, k, v, o, do, lse, a, r, frozen, state, dq=None, dk=None, dv=None, workspace=None,
+                          stream=None):
+    """Backward with the frozen-pattern data from a prepared state; returns (dq, dk, dv)."""
+    B, H, Hkv, T, d = _gqa_shape(q, v, frozen)
+    dq = torch.empty((B, H, T, d), dtype=v.dtype, device=v.device) if dq is None else dq
+    dk = torch.empty_like(v) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = alloc_workspace(B, H, T, d, v.dtype, True, v.device)
+    ld = a.shape[1] if a is not None else T
+    st = _lib.saf_attn_bwd_prepared(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(a), _ptr(r),
+                                    int(ld), _frozen_bytes(frozen, H), _ptr(state), B, H, Hkv, T, d, _dt(v),
+                                    _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(),
+                                    _stream(stream))
+    if st != SAF_OK:
+        raise SafError(st, "saf_attn_bwd_prepared")
     return dq, dk, dv
 
 

@@ -251,3 +251,22 @@ def test_diag_argument_errors(saf):
     assert diag(dt=1) == saf.SAF_EUNSUPPORTED     # the bounded waits live in the tensor-core kernels
     assert diag(withhold=2) == saf.SAF_EINVAL
     assert diag(ws=None) == saf.SAF_EWORKSPACE
+
+
+def test_prepared_state_argument_errors(saf):
+    lib = saf.library()
+    F = FAKE
+    assert lib.saf_frozen_state_bytes(4, 256, 0) > lib.saf_frozen_state_bytes(4, 256, 1) > 0
+    assert lib.saf_frozen_state_bytes(0, 256, 0) == 0 and lib.saf_frozen_state_bytes(4, 256, 7) == 0
+    fz = (ctypes.c_uint8 * 4)(0, 1, 0, 0)
+    prep = lambda **kw: lib.saf_frozen_prepare(kw.get("a", F), F, kw.get("ld", 256), fz, 4, 256, 0,
+                                               kw.get("st", F), kw.get("sb", 1 << 30), None)
+    assert prep(a=None) == saf.SAF_EINVAL
+    assert prep(ld=100) == saf.SAF_EINVAL
+    assert prep(st=None) == saf.SAF_EWORKSPACE
+    assert prep(st=F + 64) == saf.SAF_EALIGN
+    assert prep(sb=1024) == saf.SAF_EWORKSPACE
+    fwd = lambda **kw: lib.saf_attn_fwd_prepared(F, F, F, F, F, 256, fz, kw.get("st", F), 1, 4, kw.get("hkv", 4),
+                                                 256, 64, 0, F, F, F, 1 << 30, None)
+    assert fwd(st=None) == saf.SAF_EWORKSPACE
+    assert fwd(hkv=3) == saf.SAF_EINVAL
