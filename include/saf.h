@@ -340,6 +340,31 @@ SAF_API int saf_pattern_grad(const void* v, const void* dO, const void* o, const
                              const float* r, int ld_prior, const uint8_t* frozen, int B, int H, int T, int d,
                              saf_dtype_t dt, float* da, float* dr, void* stream);
 
+/* The same gradients on the tensor cores (bf16 inputs, d = 64), with sums in a
+ * fixed order: the results have the same bits on every run.
+ * G^T = V dO^T is formed per causal 128 x 128 tile with tcgen05 MMAs (fp32 in
+ * tensor memory); W is rebuilt from a, r and the log Z rows of lse in the form
+ * the layer's backward uses (factorised, or exact when a head's log Z' falls
+ * below -64); tiles are visited band by band (band = query block - key block),
+ * each thread summing its elements of one distance i - j over the band in
+ * registers, and the per-tile key sums and per-band distance sums are written
+ * to the workspace and added up by a last kernel.
+ * In:  v, dO, o [B, H, T, 64] bf16, 16-byte aligned; lse [B, H, T] fp32 as
+ *      saf_attn_fwd wrote it; a, r, ld_prior, frozen as for saf_attn_fwd.
+ * Out: da, dr: DEVICE fp32 [H, T], overwritten; rows of ordinary heads zero.
+ * workspace: DEVICE scratch of saf_pattern_grad_tc_workspace_bytes(B, H, T,
+ * n_frozen) bytes (n_frozen = number of nonzero entries of `frozen`), 256-byte
+ * aligned; clobbered. Its first 256 bytes are the status words that
+ * saf_device_status reads after the call (SAF_ETIMEOUT when a bounded
+ * wait of the kernel expired).
+ * Errors: SAF_EINVAL (sizes, NULL), SAF_EALIGN, SAF_EWORKSPACE,
+ * SAF_EUNSUPPORTED (d != 64, device), all before any work is enqueued;
+ * SAF_ELAUNCH. saf_pattern_grad_tc_workspace_bytes returns 0 for invalid sizes. */
+SAF_API size_t saf_pattern_grad_tc_workspace_bytes(int B, int H, int T, int n_frozen);
+SAF_API int saf_pattern_grad_tc(const void* v, const void* dO, const void* o, const float* lse, const float* a,
+                                const float* r, int ld_prior, const uint8_t* frozen, int B, int H, int T, int d,
+                                float* da, float* dr, void* workspace, size_t ws_bytes, void* stream);
+
 /* ---- Profiling hooks (not part of the layer's arithmetic) ----------------
  * Kernel identifiers for saf_set_trace_events. */
 typedef enum {
@@ -352,8 +377,9 @@ typedef enum {
     SAF_KERNEL_BWD_Q = 5,       /* backward query-block pass (dQ)              */
     SAF_KERNEL_BWD = 6,         /* fused backward (dQ, dK, dV in one launch)   */
     SAF_KERNEL_DQ_FINISH = 7,   /* dQ accumulator -> dq (scale, dtype, zeros)  */
-    SAF_KERNEL_PATTERN_PREP = 8 /* backward: init kernel (clears the status    *
-                                 * words; maxima and padded a, r slices)        */
+    SAF_KERNEL_PATTERN_PREP = 8, /* backward: init kernel (clears the status   *
+                                  * words; maxima and padded a, r slices)       */
+    SAF_KERNEL_PATTERN_GRAD = 9  /* saf_pattern_grad_tc: all of its launches    */
 } saf_kernel_t;
 
 /* From the next call on, record `start` (a cudaEvent_t as void*) on the

@@ -48,7 +48,7 @@ WorkspaceLayout workspace_layout(int B, int H, int T, int backward, int bf16) {
 }
 
 namespace {
-constexpr int kNumKernelIds = SAF_KERNEL_PATTERN_PREP + 1;
+constexpr int kNumKernelIds = SAF_KERNEL_PATTERN_GRAD + 1;
 cudaEvent_t g_trace_start[kNumKernelIds] = {};
 cudaEvent_t g_trace_stop[kNumKernelIds] = {};
 unsigned long long g_launches = 0;

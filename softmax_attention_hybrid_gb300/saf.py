@@ -36,7 +36,7 @@ EXPORTED = ("saf_attn_workspace_bytes", "saf_attn_fwd", "saf_attn_bwd", "saf_dev
             "saf_pattern_grad", "saf_attn_fwd_gqa", "saf_attn_bwd_gqa", "saf_fit_stats_workspace_bytes",
             "saf_fit_target_stats", "saf_fit_from_target_workspace_bytes", "saf_fit_from_target",
             "saf_attn_fwd_diag", "saf_frozen_state_bytes", "saf_frozen_prepare", "saf_attn_fwd_prepared",
-            "saf_attn_bwd_prepared")
+            "saf_attn_bwd_prepared", "saf_pattern_grad_tc_workspace_bytes", "saf_pattern_grad_tc")
 
 SAF_KERNEL_NONE = 0
 SAF_KERNEL_LOGNORM = 1
@@ -47,6 +47,7 @@ SAF_KERNEL_BWD_Q = 5
 SAF_KERNEL_BWD = 6
 SAF_KERNEL_DQ_FINISH = 7
 SAF_KERNEL_PATTERN_PREP = 8
+SAF_KERNEL_PATTERN_GRAD = 9
 
 
 class SafError(RuntimeError):
@@ -109,6 +110,10 @@ def _load():
     lib.saf_fit_compact.restype = i
     lib.saf_pattern_grad.argtypes = [vp, vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, vp, vp, vp]
     lib.saf_pattern_grad.restype = i
+    lib.saf_pattern_grad_tc_workspace_bytes.argtypes = [i, i, i, i]
+    lib.saf_pattern_grad_tc_workspace_bytes.restype = sz
+    lib.saf_pattern_grad_tc.argtypes = [vp, vp, vp, vp, vp, vp, i, vp, i, i, i, i, vp, vp, vp, sz, vp]
+    lib.saf_pattern_grad_tc.restype = i
     return lib
 
 
@@ -434,4 +439,27 @@ def saf_pattern_grad(v, do, o, lse, a, r, frozen, da=None, dr=None, stream=None)
                                _frozen_bytes(frozen, H), B, H, T, d, _dt(v), _ptr(da), _ptr(dr), _stream(stream))
     if st != SAF_OK:
         raise SafError(st, "saf_pattern_grad")
+    return da, dr
+
+
+def saf_pattern_grad_tc_workspace_bytes(B, H, T, n_frozen):
+    return int(_lib.saf_pattern_grad_tc_workspace_bytes(B, H, T, n_frozen))
+
+
+def saf_pattern_grad_tc(v, do, o, lse, a, r, frozen, da=None, dr=None, workspace=None, stream=None):
+    """Gradients of a and r of the frozen heads on the tensor cores (bf16 v, do, o
+    [B, H, T, 64]); fp32 CUDA tensors [H, T], the same bits on every run.
+    `workspace` (uint8 CUDA tensor) is allocated when not given."""
+    B, H, T, d = v.shape
+    fz = _frozen_bytes(frozen, H)
+    nf = sum(fz) if fz is not None else 0
+    da = torch.empty((H, T), dtype=torch.float32, device=v.device) if da is None else da
+    dr = torch.empty((H, T), dtype=torch.float32, device=v.device) if dr is None else dr
+    if workspace is None:
+        n = max(saf_pattern_grad_tc_workspace_bytes(B, H, T, nf), 256)
+        workspace = torch.empty(n, dtype=torch.uint8, device=v.device)
+    st = _lib.saf_pattern_grad_tc(_ptr(v), _ptr(do), _ptr(o), _ptr(lse), _ptr(a), _ptr(r), a.shape[-1], fz, B, H,
+                                  T, d, _ptr(da), _ptr(dr), _ptr(workspace), workspace.numel(), _stream(stream))
+    if st != SAF_OK:
+        raise SafError(st, "saf_pattern_grad_tc")
     return da, dr

@@ -179,6 +179,43 @@ def test_pattern_grad_argument_errors(saf):
     assert pg(frozen=fz, a=F + 2) == saf.SAF_EALIGN
 
 
+def test_pattern_grad_tc_argument_errors(saf):
+    lib = saf.library()
+    F = FAKE
+    need = lib.saf_pattern_grad_tc_workspace_bytes(2, 4, 256, 1)
+    assert need > 0
+    # the workspace grows with the batch and the number of frozen heads
+    assert lib.saf_pattern_grad_tc_workspace_bytes(2, 4, 256, 2) > need
+    assert lib.saf_pattern_grad_tc_workspace_bytes(4, 4, 256, 1) > need
+    for bad in ((-1, 4, 256, 1), (2, 0, 256, 0), (2, 4, -1, 1), (2, 4, 256, 5), (2, 4, 256, -1)):
+        assert lib.saf_pattern_grad_tc_workspace_bytes(*bad) == 0, bad
+
+    def pg(**kw):
+        a = dict(v=F, do=F, o=F, lse=F, a=F, r=F, ld=256, B=2, H=4, T=256, d=64, da=F, dr=F, frozen=None,
+                 ws=F, wsb=need)
+        a.update(kw)
+        fz = a["frozen"]
+        fzp = (ctypes.c_uint8 * len(fz))(*fz) if fz is not None else None
+        return lib.saf_pattern_grad_tc(a["v"], a["do"], a["o"], a["lse"], a["a"], a["r"], a["ld"], fzp, a["B"],
+                                       a["H"], a["T"], a["d"], a["da"], a["dr"], a["ws"], a["wsb"], None)
+
+    assert pg(H=0) == saf.SAF_EINVAL
+    assert pg(B=-1) == saf.SAF_EINVAL
+    assert pg(d=128) == saf.SAF_EUNSUPPORTED
+    assert pg(da=None) == saf.SAF_EINVAL
+    assert pg(dr=F + 1) == saf.SAF_EALIGN
+    assert pg(T=0) == saf.SAF_OK
+    # with a frozen head, every argument and the workspace are checked before any work
+    fz = [0, 1, 0, 0]
+    assert pg(frozen=fz, v=None) == saf.SAF_EINVAL
+    assert pg(frozen=fz, ld=255) == saf.SAF_EINVAL
+    assert pg(frozen=fz, o=F + 8) == saf.SAF_EALIGN
+    assert pg(frozen=fz, r=F + 2) == saf.SAF_EALIGN
+    assert pg(frozen=fz, ws=None) == saf.SAF_EWORKSPACE
+    assert pg(frozen=fz, ws=F + 128) == saf.SAF_EALIGN
+    assert pg(frozen=fz, wsb=need - 1) == saf.SAF_EWORKSPACE
+
+
 def test_gqa_argument_errors(saf):
     lib = saf.library()
     F = FAKE
