@@ -14,7 +14,9 @@ is the max over ranks and the value the work of all ranks over that time.
 
 Besides the headline workload, the line carries `other_workloads`: the other
 bench workloads of the same layer (50% frozen, the 1B-shaped layer at 8K, the
-16K prefill), each timed in the same run with its all-ordinary comparison.
+16K prefill), each timed in the same run with its all-ordinary comparison, and
+`trainable_patterns`: the time of the pattern gradient (saf_pattern_grad_tc) that
+the trainable-pattern variant adds to a step.
 
     python bench.py --workload W --record-traffic ncu.csv
 
@@ -408,6 +410,46 @@ def time_prepared(saf, lay, args, dom, flush, stream, world, dev, flops, ao_ms):
     return out
 
 
+def time_pattern_grad(saf, lay, args, flush, stream, world, dev, step_ms, bwd_ms):
+    """The trainable-pattern variant's extra work (App. C.3.2): da, dr of the frozen
+    heads from the step's V, dO, o and lse through saf_pattern_grad_tc, each call
+    after an L2 flush and bracketed by CUDA events on the launching stream."""
+    w, g = lay.w, lay.g
+    H, T = w.H, w.T
+    nf = sum(lay.frozen)
+    ws = torch.empty(max(saf.saf_pattern_grad_tc_workspace_bytes(w.B, H, T, nf), 256), dtype=torch.uint8,
+                     device=dev)
+    da = torch.empty((H, T), dtype=torch.float32, device=dev)
+    dr = torch.empty((H, T), dtype=torch.float32, device=dev)
+
+    def call():
+        saf.saf_pattern_grad_tc(g["v"], g["do"], lay.o, lay.lse, g["a"], g["r"], lay.frozen, da=da, dr=dr,
+                                workspace=ws)
+
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    if saf.saf_device_status(ws) != saf.SAF_OK:
+        raise RuntimeError("device status after the pattern-gradient warm-up is not ok")
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.fill_(float(i))
+        evs[i][0].record(stream)
+        call()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    pm = max_over_ranks(sum(s.elapsed_time(e) for s, e in evs) / K, world, dev)
+    out = {"ms": pm, "fraction_of_step": pm / step_ms,
+           "note": "saf_pattern_grad_tc (tcgen05, fixed-order sums): gradients of a and r of the frozen heads, "
+                   "timed alone after the step that produced o and lse"}
+    if bwd_ms:
+        out["fraction_of_bwd"] = pm / bwd_ms
+    return out
+
+
 def measure_workload(saf, w, args, dev, world, rank, stream, flush, peaks, peak_src):
     """Hybrid and all-ordinary step times of one more workload (no end-to-end leg)."""
     lay = Layer(saf, w, rank, dev)
@@ -437,6 +479,10 @@ def measure_workload(saf, w, args, dev, world, rank, stream, flush, peaks, peak_
                                "ideal_speedup": F.layer_flops(w.B, w.H, 0, w.T, w.d, not w.fwd_only) /
                                F.layer_flops(w.B, w.H, w.F, w.T, w.d, not w.fwd_only)}
         out["prepared_normalisers"] = time_prepared(saf, lay, args, dom, flush, stream, world, dev, flops, ao)
+        if not w.fwd_only and w.d == 64 and not lay.gqa:
+            lay.step(lay.frozen)
+            out["trainable_patterns"] = time_pattern_grad(saf, lay, args, flush, stream, world, dev, step_ms,
+                                                          kms.get("bwd"))
     del lay
     torch.cuda.empty_cache()
     return out
@@ -503,9 +549,13 @@ def run_ours(args, w):
                   "kernel_ms": kms0}
 
     prepared = None
+    trainable = None
     if w.F > 0:
         prepared = time_prepared(saf, lay, args, dom, flush, stream, world, dev, total_flops,
                                  allord["ms_per_step"] if allord else None)
+        if not w.fwd_only and d == 64 and not lay.gqa:
+            lay.step(frozen)   # o and lse of the frozen-mask step
+            trainable = time_pattern_grad(saf, lay, args, flush, stream, world, dev, step_ms, kms.get("bwd"))
 
     # end to end: host buffers in, host buffers out, through the same C ABI
     e2e = None
@@ -626,6 +676,7 @@ def run_ours(args, w):
         "e2e": e2e,
         "all_ordinary": allord,
         "prepared_normalisers": prepared,
+        "trainable_patterns": trainable,
         "other_workloads": others,
         "gpu_launches": launches,
         "clocks": clk,
