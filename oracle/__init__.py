@@ -17,6 +17,7 @@ from .saf_oracle import (  # noqa: F401
     attn_bwd,
     pattern_grad,
     attn_pattern_grad,
+    attn_pattern_grad_at,
     FIT_STEPS,
     FIT_LR,
     FIT_TOL,

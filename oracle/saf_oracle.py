@@ -295,6 +295,50 @@ def attn_pattern_grad(v, do, a, r, frozen, threads=1):
     return da, dr
 
 
+def attn_pattern_grad_at(v, do, o, a, r, frozen, cols, dists):
+    """Chosen entries of the pattern gradients of every frozen head, summed over
+    the batch, with D_i = dO_i . o_i taken from a given layer output o
+    (trainable patterns, App. C.3.2).
+
+    For o = P V, the output of Eq. 3, D_i = sum_j P_ij G_ij and the entries are
+    those of attn_pattern_grad. A layer output that carries rounding (a bf16 o)
+    gives the gradient that the same formula yields with that D:
+        da[j] = sum_b sum_{i >= j} P_ij (G_ij - D_i),
+        dr[d] = sum_b sum_{i >= d} P_{i,i-d} (G_{i,i-d} - D_i),   G = dO V^T.
+    Each entry is formed on its own from log Z (Eq. 3), one column or diagonal
+    of P and the matching dot products, so full-length sequences stay cheap.
+    v, do, o [B, H, T, d]; a, r [H, >= T]; cols, dists: indices into [0, T).
+    Returns da [H, len(cols)], dr [H, len(dists)] in fp64; ordinary heads 0.
+    """
+    v = _as64(v)
+    do = _as64(do)
+    o = _as64(o)
+    a = _as64(a)
+    r = _as64(r)
+    B, H, T, d = v.shape
+    cols = [int(j) for j in cols]
+    dists = [int(x) for x in dists]
+    da = np.zeros((H, len(cols)))
+    dr = np.zeros((H, len(dists)))
+    for h in range(H):
+        if not frozen[h]:
+            continue
+        lz = log_normaliser(a[h], r[h], T)                   # Eq. 3 normalisers
+        for b in range(B):
+            D = np.sum(do[b, h] * o[b, h], axis=1)           # D_i = dO_i . o_i
+            for n, j in enumerate(cols):
+                i = np.arange(j, T)
+                p = np.exp(a[h, j] + r[h, i - j] - lz[i])    # column j of P
+                g = do[b, h, i] @ v[b, h, j]                 # G(i, j)
+                da[h, n] += np.sum(p * (g - D[i]))
+            for n, x in enumerate(dists):
+                i = np.arange(x, T)
+                p = np.exp(a[h, i - x] + r[h, x] - lz[i])    # diagonal i - j = x of P
+                g = np.sum(do[b, h, i] * v[b, h, i - x], axis=1)
+                dr[h, n] += np.sum(p * (g - D[i]))
+    return da, dr
+
+
 # ---------------------------------------------------------------------------
 # Compact fitting (§3.2 "Fitting", Eq. 4; App. D.1, Eq. 20; the selection
 # algorithm's fitting steps; settings of App. C.1)

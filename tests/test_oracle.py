@@ -379,6 +379,52 @@ def test_pattern_grad_invariants():
     assert abs(dr[T - 1] - expect) < 1e-12
 
 
+def _pattern_layer_case(seed):
+    B, H, T, d = 2, 3, 40, 4
+    g = _rng(seed)
+    q, k, v, do = (g.normal(size=(B, H, T, d)) for _ in range(4))
+    a = g.normal(size=(H, T))
+    r = -0.1 * np.arange(T) + 0.4 * g.normal(size=(H, T))
+    return q, k, v, do, a, r, [1, 0, 1]
+
+
+def test_pattern_grad_at_equals_the_full_gradient_for_the_exact_output():
+    # with the layer's own output (o = P V for a frozen head), D_i = dO_i . o_i is
+    # the D of the softmax Jacobian, so every entry equals attn_pattern_grad's
+    q, k, v, do, a, r, frozen = _pattern_layer_case(64)
+    T = v.shape[2]
+    o, _ = oracle.attn_fwd(q, k, v, a, r, frozen)
+    da, dr = oracle.attn_pattern_grad(v, do, a, r, frozen)
+    sa, sr = oracle.attn_pattern_grad_at(v, do, o, a, r, frozen, range(T), range(T))
+    assert np.max(np.abs(sa - da)) < 1e-12 and np.max(np.abs(sr - dr)) < 1e-12
+    # a subset in any order
+    cols, dists = [T - 1, 0, 17], [3, T - 1, 0]
+    sa2, sr2 = oracle.attn_pattern_grad_at(v, do, o, a, r, frozen, cols, dists)
+    assert np.max(np.abs(sa2 - da[:, cols])) < 1e-12 and np.max(np.abs(sr2 - dr[:, dists])) < 1e-12
+
+
+def test_pattern_grad_at_moves_with_the_given_output():
+    # dL = P (G - D) is linear in D: replacing o by o + E moves da[j] by
+    # -sum_b sum_i P_ij dO_i . E_i and dr[x] by the same sum along diagonal x
+    q, k, v, do, a, r, frozen = _pattern_layer_case(65)
+    B, H, T, _ = v.shape
+    o, _ = oracle.attn_fwd(q, k, v, a, r, frozen)
+    E = 1e-2 * _rng(66).normal(size=o.shape)
+    base = oracle.attn_pattern_grad_at(v, do, o, a, r, frozen, range(T), range(T))
+    moved = oracle.attn_pattern_grad_at(v, do, o + E, a, r, frozen, range(T), range(T))
+    for h in (0, 2):
+        P = oracle.frozen_pattern(a[h], r[h], T)
+        ea = np.zeros(T)
+        er = np.zeros(T)
+        for b in range(B):
+            M = P * np.sum(do[b, h] * E[b, h], axis=1)[:, None]
+            ea -= M.sum(axis=0)
+            er -= np.array([np.trace(M, -x) for x in range(T)])
+        assert np.max(np.abs(moved[0][h] - base[0][h] - ea)) < 1e-12
+        assert np.max(np.abs(moved[1][h] - base[1][h] - er)) < 1e-12
+    assert not np.any(moved[0][1]) and not np.any(moved[1][1])
+
+
 def test_attn_pattern_grad_sums_over_batch():
     # the pattern is shared by the batch: a layer's gradient is the sum over batch
     # entries, and ordinary heads get none

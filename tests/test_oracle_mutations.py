@@ -39,6 +39,12 @@ MUTATIONS = {
     "pattern_diag_reversed": ("dr[:i + 1] += dL[t, i::-1]", "dr[:i + 1] += dL[t, :i + 1]"),
     # pattern gradient: dL/dP with V and dO swapped
     "pattern_G_swapped": ("G = do[blk] @ v.T", "G = v[blk] @ do.T"),
+    # sampled pattern gradient: D from the values instead of the given output
+    "pattern_at_D_from_v": ("D = np.sum(do[b, h] * o[b, h], axis=1)", "D = np.sum(do[b, h] * v[b, h], axis=1)"),
+    # sampled pattern gradient: the diagonal's absolute term indexed by the query
+    "pattern_at_diag_alpha": ("p = np.exp(a[h, i - x] + r[h, x] - lz[i])", "p = np.exp(a[h, i] + r[h, x] - lz[i])"),
+    # sampled pattern gradient: column j's relative term read at the key index
+    "pattern_at_col_rho": ("p = np.exp(a[h, j] + r[h, i - j] - lz[i])", "p = np.exp(a[h, j] + r[h, j] - lz[i])"),
     # fitting: relative marginal from the wrong side of the diagonal
     "fit_eta_rel_side": ("np.trace(P, offset=-delta)", "np.trace(P, offset=delta)"),
     # fitting: Eq. 20 without the 1/T

@@ -162,3 +162,48 @@ def test_pattern_grad_tc_without_frozen_heads_gives_zeros(saf):
     saf.saf_pattern_grad_tc(g["v"], g["do"], o, lse, g["a"], g["r"], x["frozen"], da=da, dr=dr)
     torch.cuda.synchronize()
     assert not torch.any(da) and not torch.any(dr)
+
+
+@pytest.mark.parametrize("name", ["gpt2_124m_25", "gpt2_124m_50"])
+def test_pattern_grad_tc_full_size_sampled(saf, name):
+    # the bench's workloads at full size, in the launch configuration bench.py times
+    # (one call on the layer's own o and lse): sampled entries of da and dr against
+    # the oracle's entry-wise form with the same D = dO . o, within the fp32 rounding
+    # bound of the small cases
+    from softmax_attention_hybrid_gb300.inputs import WORKLOADS
+    w = WORKLOADS[name]
+    x = make_inputs(w, seed=1)
+    g = {n: x[n].to("cuda") for n in ("q", "k", "v", "do", "a", "r")}
+    o, lse = saf.saf_attn_fwd(g["q"], g["k"], g["v"], g["a"], g["r"], x["frozen"])
+    ws = torch.empty(saf.saf_pattern_grad_tc_workspace_bytes(w.B, w.H, w.T, sum(x["frozen"])), dtype=torch.uint8,
+                     device="cuda")
+    da, dr = saf.saf_pattern_grad_tc(g["v"], g["do"], o, lse, g["a"], g["r"], x["frozen"], workspace=ws)
+    assert saf.saf_device_status(ws) == saf.SAF_OK
+    T = w.T
+    rng = np.random.default_rng(5)
+    idx = sorted(set([0, 1, 127, 128, 129, T // 2, T - 129, T - 128, T - 2, T - 1] +
+                     rng.integers(0, T, size=14).tolist()))
+    v, do = (x[n].double().numpy() for n in ("v", "do"))
+    a, r = x["a"].double().numpy(), x["r"].double().numpy()
+    on = o.double().cpu().numpy()
+    ra, rr = oracle.attn_pattern_grad_at(v, do, on, a, r, x["frozen"], idx, idx)
+    da, dr = da.double().cpu().numpy(), dr.double().cpu().numpy()
+    scale = max(1.0, np.max(np.abs(ra)), np.max(np.abs(rr)))
+    for h in range(w.H):
+        if not x["frozen"][h]:
+            assert not np.any(da[h]) and not np.any(dr[h])
+            continue
+        P = oracle.frozen_pattern(a[h], r[h], T)
+        ba, br = np.zeros(len(idx)), np.zeros(len(idx))
+        for b in range(w.B):
+            Dabs = np.sum(np.abs(do[b, h] * on[b, h]), axis=1)
+            for n, j in enumerate(idx):
+                gc = np.abs(do[b, h, j:]) @ np.abs(v[b, h, j])
+                ba[n] += np.sum(P[j:, j] * (gc + Dabs[j:]))
+                ii = np.arange(j, T)
+                gd = np.sum(np.abs(do[b, h, ii]) * np.abs(v[b, h, ii - j]), axis=1)
+                br[n] += np.sum(P[ii, ii - j] * (gd + Dabs[ii]))
+        ta, tr = 2.0 ** -15 * ba + 1e-6 * scale, 2.0 ** -15 * br + 1e-6 * scale
+        ea, er = np.abs(da[h, idx] - ra[h]), np.abs(dr[h, idx] - rr[h])
+        assert np.all(ea <= ta), (name, h, float(np.max(ea)), float(np.max(ta)))
+        assert np.all(er <= tr), (name, h, float(np.max(er)), float(np.max(tr)))
