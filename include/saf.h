@@ -22,8 +22,10 @@
  * ---------------------------------------
  *  - Tensors q, k, v, o, dO, dq, dk, dv have layout [B, H, T, d], contiguous,
  *    element type `dt` (bf16 or fp32). lse and the normalisers are fp32.
- *    d = 64 for SAF_BF16 (tensor-core kernels); d = 64, 96 or 128 for
- *    SAF_FP32 (CUDA-core kernels). Other values return SAF_EUNSUPPORTED.
+ *    d = 64, 96 or 128. SAF_BF16 runs on tensor-core kernels (at 96 and 128
+ *    for the multi-head layout with per-call normalisers: the grouped-query
+ *    and prepared-state calls take d = 64 in bf16); SAF_FP32 on CUDA-core
+ *    kernels. Other values return SAF_EUNSUPPORTED.
  *    Every tensor pointer must be 16-byte aligned (SAF_EALIGN otherwise).
  *  - a, r: fp32 [H, ld_prior] device arrays, ld_prior >= T; row h holds the
  *    absolute-key preference a and the relative-distance preference r of
@@ -97,8 +99,9 @@ SAF_API size_t saf_attn_workspace_bytes(int B, int H, int T, int d, saf_dtype_t 
  *      frozen rows log Z(i). saf_attn_bwd consumes lse.
  * The normalisers log Z of the frozen heads are computed here ("precomputed
  * normalisers", §3.3), once per head, independent of the batch.
- * Supported: d == 64 for SAF_BF16 (tensor cores, fp32 accumulation);
- * d in {64, 96, 128} for SAF_FP32 (fp32 arithmetic throughout, CUDA cores). */
+ * Supported: d in {64, 96, 128}; SAF_BF16 on the tensor cores with fp32
+ * accumulation (App. C.5's 1B model has d_h = 96), SAF_FP32 in fp32 arithmetic
+ * throughout on CUDA cores. */
 SAF_API int saf_attn_fwd(const void* q, const void* k, const void* v,
                  const float* a, const float* r, int ld_prior, const uint8_t* frozen,
                  int B, int H, int T, int d, saf_dtype_t dt,
@@ -148,7 +151,7 @@ SAF_API int saf_attn_fwd_noalloc(const void* q, const void* k, const void* v,
  * Out: dq, dk, dv [B,H,T,d] (dt). Ordinary heads: the gradient of Eqs. 5-7.
  *      Frozen heads: dv = W^T dO; dq and dk are written as exact zeros
  *      (§3.3, App. D.2).
- * Supported: d == 64 for SAF_BF16; d in {64, 96, 128} for SAF_FP32. */
+ * Supported: d in {64, 96, 128} for both types. */
 SAF_API int saf_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
                  const float* lse, const float* a, const float* r, int ld_prior,
                  const uint8_t* frozen, int B, int H, int T, int d, saf_dtype_t dt,

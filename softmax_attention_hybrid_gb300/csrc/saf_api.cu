@@ -215,6 +215,7 @@ int saf_attn_fwd_gqa(const void* q, const void* k, const void* v, const float* a
     Common c;
     int st = validate(q, k, v, a, r, ld_prior, frozen, B, H, T, d, dt, workspace, ws_bytes, 0, &c);
     if (st != SAF_OK) return st;
+    if (dt == SAF_BF16 && d != kHeadDim && Hkv != H) return SAF_EUNSUPPORTED;
     if (B == 0 || T == 0) return SAF_OK;
     if (!o || !lse) return SAF_EINVAL;
     if (!aligned16(o) || !aligned16(lse)) return SAF_EALIGN;
@@ -227,14 +228,15 @@ int saf_attn_fwd_gqa(const void* q, const void* k, const void* v, const float* a
     p.lse_out = lse;
     const bool bf16 = dt == SAF_BF16;
     cudaError_t e = begin_call(p, c, false, bf16, s);
-    if (e == cudaSuccess) e = bf16 ? launch_tc_fwd(p, s) : launch_simt_fwd(p, false, s);
+    if (e == cudaSuccess)
+        e = !bf16 ? launch_simt_fwd(p, false, s) : d == kHeadDim ? launch_tc_fwd(p, s) : launch_dh_fwd(p, s);
     return launch_status(e);
 }
 
 int saf_attn_fwd_diag(const void* q, const void* k, const void* v, const float* a, const float* r, int ld_prior,
                       const uint8_t* frozen, int B, int H, int T, int d, saf_dtype_t dt, void* o, float* lse,
                       void* workspace, size_t ws_bytes, void* stream, int withhold, unsigned wait_limit_us) {
-    if (dt != SAF_BF16) return SAF_EUNSUPPORTED;   // the bounded waits live in the tensor-core kernels
+    if (dt != SAF_BF16 || d != kHeadDim) return SAF_EUNSUPPORTED;   // the forward kernel with the test switches
     if (withhold != 0 && withhold != 1) return SAF_EINVAL;
     Common c;
     int st = validate(q, k, v, a, r, ld_prior, frozen, B, H, T, d, dt, workspace, ws_bytes, 0, &c);
@@ -269,6 +271,7 @@ int saf_attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
     Common c;
     int st = validate(q, k, v, a, r, ld_prior, frozen, B, H, T, d, dt, workspace, ws_bytes, 1, &c);
     if (st != SAF_OK) return st;
+    if (dt == SAF_BF16 && d != kHeadDim && Hkv != H) return SAF_EUNSUPPORTED;
     if (B == 0 || T == 0) return SAF_OK;
     if (!o || !dO || !lse || !dq || !dk || !dv) return SAF_EINVAL;
     if (!aligned16(o) || !aligned16(dO) || !aligned16(lse) || !aligned16(dq) || !aligned16(dk) ||
@@ -287,7 +290,9 @@ int saf_attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
     p.dv = dv;
     const bool bf16 = dt == SAF_BF16;
     cudaError_t e = begin_call(p, c, true, bf16, s);
-    if (bf16) {
+    if (bf16 && d != kHeadDim) {
+        if (e == cudaSuccess) e = launch_dh_bwd(p, s);
+    } else if (bf16) {
         if (e == cudaSuccess) e = launch_bwd_prep(p, s);
         if (e == cudaSuccess) e = launch_tc_bwd(p, s);
     } else {
@@ -372,6 +377,7 @@ int saf_attn_fwd_prepared(const void* q, const void* k, const void* v, const flo
     Common c;
     int st = validate(q, k, v, a, r, ld_prior, frozen, B, H, T, d, dt, workspace, ws_bytes, 0, &c);
     if (st != SAF_OK) return st;
+    if (dt == SAF_BF16 && d != kHeadDim) return SAF_EUNSUPPORTED;
     if (B == 0 || T == 0) return SAF_OK;
     if (!o || !lse) return SAF_EINVAL;
     if (!aligned16(o) || !aligned16(lse)) return SAF_EALIGN;
@@ -399,6 +405,7 @@ int saf_attn_bwd_prepared(const void* q, const void* k, const void* v, const voi
     Common c;
     int st = validate(q, k, v, a, r, ld_prior, frozen, B, H, T, d, dt, workspace, ws_bytes, 1, &c);
     if (st != SAF_OK) return st;
+    if (dt == SAF_BF16 && d != kHeadDim) return SAF_EUNSUPPORTED;
     if (B == 0 || T == 0) return SAF_OK;
     if (!o || !dO || !lse || !dq || !dk || !dv) return SAF_EINVAL;
     if (!aligned16(o) || !aligned16(dO) || !aligned16(lse) || !aligned16(dq) || !aligned16(dk) ||

@@ -11,11 +11,13 @@
 
 namespace saf {
 
-// Head dimension of the tensor-core kernels (bf16). The fp32 CUDA-core path
-// also takes 96 and 128.
+// Head dimension of the main tensor-core kernels (bf16). dh_tc.cu serves bf16
+// at 96 and 128 (multi-head layout, per-call normalisers); the fp32 CUDA-core
+// path takes 64, 96 and 128.
 constexpr int kHeadDim = 64;
 inline bool head_dim_supported(int d, saf_dtype_t dt) {
-    return d == kHeadDim || (dt == SAF_FP32 && (d == 96 || d == 128));
+    (void)dt;
+    return d == kHeadDim || d == 96 || d == 128;
 }
 
 // Per-head frozen flags as a bitmask, passed by value to every kernel so that
@@ -179,6 +181,12 @@ cudaError_t launch_tc_fwd(const LayerArgs& p, cudaStream_t s);
 
 // bwd_tc.cu: tensor-core backward (bf16), including the dQ finishing kernel
 cudaError_t launch_tc_bwd(const LayerArgs& p, cudaStream_t s);
+
+// dh_tc.cu: tensor-core forward and backward (bf16) at head dimensions 96 and 128
+// (one key/value head per query head). The forward needs the layer's call_init
+// and lognorm launches before it; the backward call_init, and launches its own prep.
+cudaError_t launch_dh_fwd(const LayerArgs& p, cudaStream_t s);
+cudaError_t launch_dh_bwd(const LayerArgs& p, cudaStream_t s);
 
 // simt.cu: fp32-arithmetic path (any dtype), used for SAF_FP32
 cudaError_t launch_simt_fwd(const LayerArgs& p, bool bf16, cudaStream_t s);

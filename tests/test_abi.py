@@ -52,7 +52,8 @@ def test_workspace_bytes(saf):
     assert f(8, 12, 4096, 64, "bf16", 1) > f(8, 12, 4096, 64, "bf16", 0)
     assert f(8, 12, 4096, 64, "bf16", 1) % 256 == 0
     assert f(1, 4, 256, 32, "bf16", 0) == 0        # unsupported d
-    assert f(1, 4, 256, 96, "bf16", 0) == 0        # the tensor-core path takes d = 64 only
+    assert f(1, 4, 256, 80, "bf16", 0) == 0        # unsupported d
+    assert f(1, 4, 256, 96, "bf16", 1) > 0 and f(1, 4, 256, 128, "bf16", 0) > 0
     assert f(1, 4, 256, 96, "fp32", 1) > 0 and f(1, 4, 256, 128, "fp32", 0) > 0
     assert f(1, 0, 256, 64, "bf16", 0) == 0        # no heads
     assert f(1, 300, 256, 64, "bf16", 0) == 0      # more than SAF_MAX_HEADS
@@ -78,7 +79,7 @@ def test_argument_errors_return_before_device_work(saf):
     assert _fwd(lib, H=0) == saf.SAF_EINVAL
     assert _fwd(lib, B=-1) == saf.SAF_EINVAL
     assert _fwd(lib, H=257, frozen=None) == saf.SAF_EINVAL
-    assert _fwd(lib, d=128) == saf.SAF_EUNSUPPORTED
+    assert _fwd(lib, d=80) == saf.SAF_EUNSUPPORTED
     assert _fwd(lib, dt=7) == saf.SAF_EINVAL
     assert _fwd(lib, v=None) == saf.SAF_EINVAL
     assert _fwd(lib, q=None) == saf.SAF_EINVAL                           # ordinary heads need q
@@ -113,6 +114,7 @@ def test_bwd_argument_errors(saf):
     assert bwd(do=F + 4) == saf.SAF_EALIGN
     assert bwd(wsb=1024) == saf.SAF_EWORKSPACE
     assert bwd(T=0) == saf.SAF_OK
+    assert bwd(d=80) == saf.SAF_EUNSUPPORTED
 
 
 def test_device_status_rejects_null(saf):
@@ -229,10 +231,10 @@ def test_gqa_argument_errors(saf):
                                     1 << 30, None)
 
     def bwd(**kw):
-        a = dict(H=8, Hkv=2, T=256)
+        a = dict(H=8, Hkv=2, T=256, d=64)
         a.update(kw)
-        return lib.saf_attn_bwd_gqa(F, F, F, F, F, F, F, F, 256, None, 1, a["H"], a["Hkv"], a["T"], 64, 0, F, F, F,
-                                    F, 1 << 30, None)
+        return lib.saf_attn_bwd_gqa(F, F, F, F, F, F, F, F, 256, None, 1, a["H"], a["Hkv"], a["T"], a["d"], 0, F, F,
+                                    F, F, 1 << 30, None)
 
     assert fwd(Hkv=0) == saf.SAF_EINVAL
     assert fwd(Hkv=3) == saf.SAF_EINVAL           # 8 query heads do not split over 3
@@ -242,6 +244,10 @@ def test_gqa_argument_errors(saf):
     assert bwd(Hkv=-1) == saf.SAF_EINVAL
     assert bwd(Hkv=5) == saf.SAF_EINVAL
     assert bwd(T=0) == saf.SAF_OK
+    # bf16 at d = 96 / 128 serves the multi-head layout only
+    assert bwd(d=128) == saf.SAF_EUNSUPPORTED
+    assert lib.saf_attn_fwd_gqa(F, F, F, F, F, 256, None, 1, 8, 2, 256, 96, 0, F, F, F, 1 << 30,
+                                None) == saf.SAF_EUNSUPPORTED
 
 
 def test_fit_target_argument_errors(saf):
@@ -285,7 +291,7 @@ def test_diag_argument_errors(saf):
         return lib.saf_attn_fwd_diag(F, F, F, F, F, 256, None, 1, 4, 256, 64, a["dt"], F, F, a["ws"], 1 << 30,
                                      None, a["withhold"], a["wait"])
 
-    assert diag(dt=1) == saf.SAF_EUNSUPPORTED     # the bounded waits live in the tensor-core kernels
+    assert diag(dt=1) == saf.SAF_EUNSUPPORTED     # the test switches live in the d = 64 tensor-core forward
     assert diag(withhold=2) == saf.SAF_EINVAL
     assert diag(ws=None) == saf.SAF_EWORKSPACE
 
@@ -307,3 +313,6 @@ def test_prepared_state_argument_errors(saf):
                                                  256, 64, 0, F, F, F, 1 << 30, None)
     assert fwd(st=None) == saf.SAF_EWORKSPACE
     assert fwd(hkv=3) == saf.SAF_EINVAL
+    # the prepared calls take d = 64 in bf16
+    assert lib.saf_attn_fwd_prepared(F, F, F, F, F, 256, fz, F, 1, 4, 4, 256, 128, 0, F, F, F, 1 << 30,
+                                     None) == saf.SAF_EUNSUPPORTED

@@ -114,9 +114,62 @@ def test_ragged_lengths(saf, T, dtype):
 @pytest.mark.parametrize("d", [96, 128])
 def test_fp32_head_dims(saf, d):
     # the fp32 CUDA-core path also takes head dimensions 96 and 128 (the paper's
-    # 1B layer has d 96; the bf16 tensor-core path takes 64)
+    # 1B layer has d 96)
     w = custom_workload(2, 3, 150, d=d, dtype="fp32", frozen=(1,), slope=0.05)
     _check_full(saf, w, seed=60 + d)
+
+
+@pytest.mark.parametrize("d", [96, 128])
+@pytest.mark.parametrize("T", [1, 65, 129, 300])
+def test_bf16_head_dims(saf, d, T):
+    # the bf16 tensor-core path at head dimensions 96 (the paper's 1B layer) and 128:
+    # ragged lengths, ordinary and frozen heads together
+    w = custom_workload(2, 4, T, d=d, frozen=(1, 3), slope=0.05)
+    _check_full(saf, w, seed=70 + d + T, case=f"bf16 d={d} T={T}" if T == 300 else None)
+
+
+@pytest.mark.parametrize("d", [96, 128])
+@pytest.mark.parametrize("frozen", [(), (0, 1, 2)])
+def test_bf16_head_dims_head_sets(saf, d, frozen):
+    # all ordinary, and all frozen with q and k never passed
+    w = custom_workload(1, 3, 257, d=d, frozen=frozen, slope=0.03)
+    if frozen:
+        x = make_inputs(w, seed=80 + d)
+        dev = torch.device("cuda:0")
+        g = {n: x[n].to(dev) for n in ("v", "do", "a", "r")}
+        o, lse = saf.saf_attn_fwd(None, None, g["v"], g["a"], g["r"], x["frozen"])
+        dq, dk, dv = saf.saf_attn_bwd(None, None, g["v"], o, g["do"], lse, g["a"], g["r"], x["frozen"])
+        torch.cuda.synchronize()
+        v, do = (x[n].double().numpy() for n in ("v", "do"))
+        a, r = x["a"].double().numpy(), x["r"].double().numpy()
+        o_ref, lse_ref = oracle.attn_fwd(v, v, v, a, r, x["frozen"])
+        _, _, dv_ref = oracle.attn_bwd(v, v, v, do, a, r, x["frozen"])
+        assert np.max(np.abs(_np(o) - o_ref)) <= 1e-2 and np.max(np.abs(_np(lse) - lse_ref)) <= 1e-2
+        assert np.max(np.abs(_np(dv) - dv_ref)) <= 2e-2
+        assert not torch.any(dq) and not torch.any(dk)
+    else:
+        _check_full(saf, w, seed=81 + d)
+
+
+@pytest.mark.parametrize("d", [96, 128])
+def test_bf16_head_dims_deterministic_and_exact_form(saf, d):
+    # a stiff pattern (a sink of e^100 and a steep distance penalty) beside an
+    # ordinary head; two calls give the same bits
+    w = custom_workload(1, 2, 400, d=d, frozen=(0,), slope=0.0)
+    x = make_inputs(w, seed=90 + d)
+    x["a"][0, 0] = 100.0
+    x["r"][0] = -1.0 * torch.arange(400, dtype=torch.float32)
+    x["do"] = (x["do"].float() * 0.1).to(x["do"].dtype)
+    a1, a2 = _run(saf, x), _run(saf, x)
+    for n in a1:
+        assert torch.equal(a1[n], a2[n]), n
+    q, k, v, do = (x[n].double().numpy() for n in ("q", "k", "v", "do"))
+    a, r = x["a"].double().numpy(), x["r"].double().numpy()
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, a, r, x["frozen"])
+    dq, dk, dv = oracle.attn_bwd(q, k, v, do, a, r, x["frozen"])
+    assert np.max(np.abs(_np(a1["o"]) - o_ref)) <= 1e-2 and np.max(np.abs(_np(a1["lse"]) - lse_ref)) <= 1e-2
+    for nm, ref in (("dq", dq), ("dk", dk), ("dv", dv)):
+        assert np.max(np.abs(_np(a1[nm]) - ref)) <= 2e-2, nm
 
 
 @pytest.mark.parametrize("frozen", [(), (0, 1, 2, 3), (0,), (2, 3), (1, 3)])
