@@ -50,7 +50,7 @@ from softmax_attention_hybrid_gb300.inputs import WORKLOADS, make_inputs, Worklo
 METRIC = "hybrid attention fwd+bwd TFLOP/s and tokens/s at 1 GB300; % of bf16 tensor peak"
 DEFAULT_WORKLOAD = "gpt2_124m_25"
 # timed after the headline workload in the same run, each with its all-ordinary run
-OTHER_WORKLOADS = ("gpt2_124m_50", "1b_25", "prefill_16k", "gqa_32q8kv_4k")
+OTHER_WORKLOADS = ("gpt2_124m_50", "1b_25", "prefill_16k", "gqa_32q8kv_4k", "1b_d96")
 L2_FLUSH_BYTES = 256 << 20  # larger than the 129 MB L2
 
 
@@ -264,7 +264,8 @@ KERNEL_FLOP_UNITS = {
 # what bounds each kernel: the bf16 kernels are tensor-core contractions,
 # the fp32 CUDA-core kernels are FMA-bound ("alu")
 def kernel_bound(name, dtype):
-    return "tensor" if dtype == "bf16" and name in ("fwd", "bwd") else "alu"
+    # bf16 runs every main kernel on the tensor cores (bwd_kv / bwd_q: the d = 96, 128 path)
+    return "tensor" if dtype == "bf16" and name in ("fwd", "bwd", "bwd_kv", "bwd_q") else "alu"
 
 
 def e2e_chunk_sizes(B, spec=""):
@@ -478,7 +479,8 @@ def measure_workload(saf, w, args, dev, world, rank, stream, flush, peaks, peak_
         out["all_ordinary"] = {"ms_per_step": ao, "speedup": ao / step_ms,
                                "ideal_speedup": F.layer_flops(w.B, w.H, 0, w.T, w.d, not w.fwd_only) /
                                F.layer_flops(w.B, w.H, w.F, w.T, w.d, not w.fwd_only)}
-        out["prepared_normalisers"] = time_prepared(saf, lay, args, dom, flush, stream, world, dev, flops, ao)
+        if w.d == 64 or w.dtype == "fp32":   # the prepared calls take d = 64 in bf16
+            out["prepared_normalisers"] = time_prepared(saf, lay, args, dom, flush, stream, world, dev, flops, ao)
         if not w.fwd_only and w.d == 64 and not lay.gqa:
             lay.step(lay.frozen)
             out["trainable_patterns"] = time_pattern_grad(saf, lay, args, flush, stream, world, dev, step_ms,
@@ -550,9 +552,10 @@ def run_ours(args, w):
 
     prepared = None
     trainable = None
-    if w.F > 0:
+    if w.F > 0 and (d == 64 or w.dtype == "fp32"):
         prepared = time_prepared(saf, lay, args, dom, flush, stream, world, dev, total_flops,
                                  allord["ms_per_step"] if allord else None)
+    if w.F > 0:
         if not w.fwd_only and d == 64 and not lay.gqa:
             lay.step(frozen)   # o and lse of the frozen-mask step
             trainable = time_pattern_grad(saf, lay, args, flush, stream, world, dev, step_ms, kms.get("bwd"))

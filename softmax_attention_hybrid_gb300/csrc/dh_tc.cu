@@ -58,29 +58,6 @@ __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, 
     tma_load_3d(dst + kAtom, map, bar, 64, y, z);
 }
 
-// Store 64 packed bf16 pairs of a 128-column bf16 row into a K-major [128 x 128]
-// tile at row `row` (two atoms, 128-byte swizzle).
-__device__ __forceinline__ void store_row_kmajor(uint8_t* tile, int row, const uint32_t* pk) {
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-        uint8_t* atom = tile + (c >> 3) * kAtom;
-        *reinterpret_cast<uint4*>(atom + sw128_offset(row, 16 * (c & 7))) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-    }
-}
-
-// Columns 32 c4 .. 32 c4 + 31 (16 packed bf16 pairs) of row `row` of a K-major
-// [128 x 128] bf16 tile.
-__device__ __forceinline__ void store_quarter_kmajor(uint8_t* tile, int row, int c4, const uint32_t* pk) {
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const int c = 4 * c4 + u;   // 16-byte chunk of the row
-        uint8_t* atom = tile + (c >> 3) * kAtom;
-        *reinterpret_cast<uint4*>(atom + sw128_offset(row, 16 * (c & 7))) =
-            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-    }
-}
-
 // Row `row` of a d-column bf16 output from 128 fp32 values (scaled), 16-byte stores.
 __device__ __forceinline__ void store_out_row(__nv_bfloat16* out, int d, const uint32_t* v, float scale) {
     uint4* dst = reinterpret_cast<uint4*>(out);
@@ -118,22 +95,25 @@ struct DhParams {
 };
 
 // ---------------------------------------------------------------------------
-// Forward
+// Forward. Two CTAs share an SM (about 99 KB of shared memory and 256 TMEM
+// columns each), so that one CTA's MMAs run while the other's rows are in the
+// softmax. K and V have a buffer each: K(j + 1) loads while the rows work on
+// S(j), V(j + 1) while they work on S(j + 1).
+// TMEM: S [0, 128) fp32, P written over S[0, 64) as bf16 pairs | O [128, 256).
 // ---------------------------------------------------------------------------
 struct FwdSmem {
     static constexpr int q = 0;
-    static constexpr int st = kTile;                      // 2 stages: K | V | a2 slice [128] | r2 band [256]
-    static constexpr int st_k = 0, st_v = kTile, st_vec = 2 * kTile;
-    static constexpr int st_bytes = 2 * kTile + 2048;
-    static constexpr int total = st + 2 * st_bytes;
+    static constexpr int k = kTile;
+    static constexpr int v = 2 * kTile;
+    static constexpr int vec = 3 * kTile;   // frozen: a2 slice [128] | r2 band [256]
+    static constexpr int total = vec + 2048;
 };
 
 struct FwdBars {
-    uint64_t q_full, kv_full[2], kv_empty[2], s_full, p_ready, o_done, mma_idle;
+    uint64_t q_full, k_full, k_empty, v_full, v_empty, s_full, p_ready, o_done, mma_idle;
 };
 
-// TMEM: S [0, 128) fp32 | P [128, 192) bf16 pairs | O [256, 384) fp32.
-__global__ void __launch_bounds__(kThreads, 1) dh_fwd_kernel(const __grid_constant__ DhParams p) {
+__global__ void __launch_bounds__(kThreads, 2) dh_fwd_kernel(const __grid_constant__ DhParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     __shared__ FwdBars bars;
@@ -150,10 +130,10 @@ __global__ void __launch_bounds__(kThreads, 1) dh_fwd_kernel(const __grid_consta
     if (threadIdx.x == 0) {
         abort_flag = 0;
         mbar_init(&bars.q_full, 1);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars.kv_full[i], 1);
-            mbar_init(&bars.kv_empty[i], 1);
-        }
+        mbar_init(&bars.k_full, 1);
+        mbar_init(&bars.k_empty, 1);
+        mbar_init(&bars.v_full, 1);
+        mbar_init(&bars.v_empty, 1);
         mbar_init(&bars.s_full, 1);
         mbar_init(&bars.p_ready, 4);
         mbar_init(&bars.o_done, 1);
@@ -161,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1) dh_fwd_kernel(const __grid_consta
         fence_mbar_init();
     }
     if (warp == 5) {
-        tmem_alloc(&tmem_base_sh, 512);
+        tmem_alloc(&tmem_base_sh, 256);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -178,21 +158,22 @@ __global__ void __launch_bounds__(kThreads, 1) dh_fwd_kernel(const __grid_consta
                 mbar_expect_tx(&bars.q_full, kTile);
                 load_tile(sm + FwdSmem::q, &p.tm_q, &bars.q_full, qb * 128, bh);
             }
+            float* vec = reinterpret_cast<float*>(sm + FwdSmem::vec);
             for (int j = 0; j < nblk; ++j) {
-                const int s = j & 1;
-                if (!mbar_wait(&bars.kv_empty[s], ((j >> 1) & 1) ^ 1u, abort, status, kStatusTimeout)) break;
-                uint8_t* st = sm + FwdSmem::st + s * FwdSmem::st_bytes;
+                // the K buffer is free once S(j - 1) has been computed, the V buffer
+                // (and the frozen rows' vectors) once P(j - 1) V has
                 if (!frz) {
-                    mbar_expect_tx(&bars.kv_full[s], 2 * kTile);
-                    load_tile(st + FwdSmem::st_k, &p.tm_k, &bars.kv_full[s], j * 128, bh);
-                    load_tile(st + FwdSmem::st_v, &p.tm_v, &bars.kv_full[s], j * 128, bh);
-                } else {
-                    float* vec = reinterpret_cast<float*>(st + FwdSmem::st_vec);
-                    mbar_expect_tx(&bars.kv_full[s], kTile + 512 + 1024);
-                    load_tile(st + FwdSmem::st_v, &p.tm_v, &bars.kv_full[s], j * 128, bh);
-                    bulk_load(vec, p.a2p + (size_t)h * p.Tp + (size_t)j * 128, 512, &bars.kv_full[s]);
+                    if (!mbar_wait(&bars.k_empty, (j & 1) ^ 1u, abort, status, kStatusTimeout)) break;
+                    mbar_expect_tx(&bars.k_full, kTile);
+                    load_tile(sm + FwdSmem::k, &p.tm_k, &bars.k_full, j * 128, bh);
+                }
+                if (!mbar_wait(&bars.v_empty, (j & 1) ^ 1u, abort, status, kStatusTimeout)) break;
+                mbar_expect_tx(&bars.v_full, frz ? kTile + 512 + 1024 : kTile);
+                load_tile(sm + FwdSmem::v, &p.tm_v, &bars.v_full, j * 128, bh);
+                if (frz) {
+                    bulk_load(vec, p.a2p + (size_t)h * p.Tp + (size_t)j * 128, 512, &bars.v_full);
                     bulk_load(vec + 128, p.r2p + (size_t)h * (p.Tp + 256) + (size_t)(qb - j) * 128, 1024,
-                              &bars.kv_full[s]);
+                              &bars.v_full);
                 }
             }
         }
@@ -201,33 +182,32 @@ __global__ void __launch_bounds__(kThreads, 1) dh_fwd_kernel(const __grid_consta
         if (lane == 0) {
             const uint32_t id_s = idesc_bf16(128, 128, 0, 0);   // S = Q K^T
             const uint32_t id_o = idesc_bf16(128, 64, 0, 1);    // O += P V, V MN-major
-            const uint32_t d_s = tmem, d_p = tmem + 128, d_o = tmem + 256;
-            const uint32_t sq = smem_u32(sm + FwdSmem::q);
+            const uint32_t d_s = tmem, d_o = tmem + 128;
+            const uint32_t sq = smem_u32(sm + FwdSmem::q), sk = smem_u32(sm + FwdSmem::k);
+            const uint32_t sv = smem_u32(sm + FwdSmem::v);
             bool ok = true;
             auto issue_s = [&](int j) -> bool {
-                const int s = j & 1;
-                if (!mbar_wait(&bars.kv_full[s], (j >> 1) & 1, abort, status, kStatusTimeout)) return false;
+                if (!mbar_wait(&bars.k_full, j & 1, abort, status, kStatusTimeout)) return false;
                 tc_fence_after();
-                const uint32_t sk = smem_u32(sm + FwdSmem::st + s * FwdSmem::st_bytes + FwdSmem::st_k);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) mma_ss(d_s, kmaj(sq, k), kmaj(sk, k), id_s, k > 0);
                 mma_commit(&bars.s_full);
+                mma_commit(&bars.k_empty);
                 return true;
             };
             if (!frz) ok = mbar_wait(&bars.q_full, 0, abort, status, kStatusTimeout) && issue_s(0);
             for (int j = 0; j < nblk && ok; ++j) {
-                const int s = j & 1;
-                if (frz && !(ok = mbar_wait(&bars.kv_full[s], (j >> 1) & 1, abort, status, kStatusTimeout))) break;
+                if (!(ok = mbar_wait(&bars.v_full, j & 1, abort, status, kStatusTimeout))) break;
                 if (!(ok = mbar_wait(&bars.p_ready, j & 1, abort, status, kStatusTimeout))) break;
                 tc_fence_after();
-                const uint32_t sv = smem_u32(sm + FwdSmem::st + s * FwdSmem::st_bytes + FwdSmem::st_v);
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
 #pragma unroll
                     for (int c = 0; c < 2; ++c)
-                        mma_ts(d_o + 64 * c, d_p + 8 * k, mnmaj(sv, c, k), id_o, (j > 0 || k > 0) ? 1u : 0u);
+                        mma_ts(d_o + 64 * c, d_s + 8 * k, mnmaj(sv, c, k), id_o, (j > 0 || k > 0) ? 1u : 0u);
                 mma_commit(&bars.o_done);
-                mma_commit(&bars.kv_empty[s]);
+                mma_commit(&bars.v_empty);
+                // S(j + 1) overwrites the columns P(j) is read from; MMAs run in issue order
                 if (!frz && j + 1 < nblk) ok = issue_s(j + 1);
             }
             mma_commit(&bars.mma_idle);
@@ -240,6 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1) dh_fwd_kernel(const __grid_consta
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
         float m = -INFINITY, l = 0.f;
         const float lz2 = (frz && row < p.T) ? p.lz[(size_t)h * p.T + row] * kLog2e : INFINITY;
+        const float* vec = reinterpret_cast<const float*>(sm + FwdSmem::vec);
         bool ok = true;
         for (int j = 0; j < nblk; ++j) {
             uint32_t pk[64];
@@ -272,7 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1) dh_fwd_kernel(const __grid_consta
                 }
                 const float corr = fast_exp2(m - mx);   // 0 on the first block (m = -inf)
                 l = l * corr + sum;
-                // P(j-1) V has been added before P is overwritten or O is rescaled
+                // P(j - 1) V has been added before O is rescaled (S(j) was computed after it,
+                // so its columns are free for P(j) already)
                 if (j > 0) {
                     if (!(ok = mbar_wait(&bars.o_done, (j - 1) & 1, abort, status, kStatusTimeout))) break;
                     tc_fence_after();
@@ -282,22 +264,19 @@ __global__ void __launch_bounds__(kThreads, 1) dh_fwd_kernel(const __grid_consta
 #pragma unroll
                         for (int c4 = 0; c4 < 4; ++c4) {
                             uint32_t u[32];
-                            tmem_ld32(lane_base + 256 + 32 * c4, u);
+                            tmem_ld32(lane_base + 128 + 32 * c4, u);
                             tmem_ld_wait();
 #pragma unroll
                             for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * corr);
-                            tmem_st32(lane_base + 256 + 32 * c4, u);
+                            tmem_st32(lane_base + 128 + 32 * c4, u);
                         }
                     }
                 }
                 m = mx;
             } else {
-                const int s = j & 1;
-                if (!(ok = mbar_wait(&bars.kv_full[s], (j >> 1) & 1, abort, status, kStatusTimeout))) break;
+                if (!(ok = mbar_wait(&bars.v_full, j & 1, abort, status, kStatusTimeout))) break;
                 if (j > 0 && !(ok = mbar_wait(&bars.o_done, (j - 1) & 1, abort, status, kStatusTimeout))) break;
                 tc_fence_after();
-                const float* vec = reinterpret_cast<const float*>(sm + FwdSmem::st + s * FwdSmem::st_bytes +
-                                                                  FwdSmem::st_vec);
                 // W(row, key) = exp2(a2[key] + r2[row - key] - log2 Z(row)) (Eq. 3); the band
                 // holds r at distance (qb - j) 128 + t - c at entry 127 + t - c
                 const float* band = vec + 128 + 127 + t;
@@ -308,8 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1) dh_fwd_kernel(const __grid_consta
                     pk[c >> 1] = pack_bf16(w0, w1);
                 }
             }
-            tmem_st32(lane_base + 128, pk);
-            tmem_st32(lane_base + 160, pk + 32);
+            tmem_st32(lane_base, pk);
+            tmem_st32(lane_base + 32, pk + 32);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -320,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1) dh_fwd_kernel(const __grid_consta
             const float inv = frz ? 1.f : 1.f / l;
             uint32_t ov[128];
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(lane_base + 256 + 32 * c4, ov + 32 * c4);
+            for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(lane_base + 128 + 32 * c4, ov + 32 * c4);
             tmem_ld_wait();
             if (row < p.T) {
                 store_out_row(p.o + ((size_t)bh * p.T + row) * p.d, p.d, ov, inv);
@@ -333,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) dh_fwd_kernel(const __grid_consta
     __syncthreads();
     if (warp == 5) {
         tc_fence_after();
-        tmem_dealloc(tmem, 512);
+        tmem_dealloc(tmem, 256);
     }
 }
 
@@ -370,22 +349,30 @@ __global__ void __launch_bounds__(128) dh_rowvec_kernel(const __grid_constant__ 
     v[128 + threadIdx.x] = dd;
 }
 
+// TMEM column of k-step k (16 rows of the contraction) of an operand written in
+// chunks of 32 rows: chunk c holds its 16 packed pairs at [32 c, 32 c + 16) and the
+// second operand's at [32 c + 16, 32 c + 32).
+__device__ __forceinline__ uint32_t chunk_col(int k, int second) {
+    return 32u * (uint32_t)(k >> 1) + 16u * (uint32_t)second + 8u * (uint32_t)(k & 1);
+}
+
 // ---------------------------------------------------------------------------
-// Backward, key-block pass: dV, dK of key block kb of slice bh.
-// TMEM: S^T [0, 128) fp32 (then P^T bf16 pairs at [0, 64)) | dP^T [128, 256) |
-//       dV [256, 384) | dK [384, 512).
+// Backward, key-block pass: dV, dK of key block kb of slice bh. Q, dO and the row
+// vectors of the next query tile load while this one runs (two stages).
+// TMEM: S^T [0, 128) fp32, overwritten chunk by chunk with P^T and dS^T as bf16
+//       pairs (chunk c: P^T at [32 c, +16), dS^T at [32 c + 16, +16)) |
+//       dP^T [128, 256) | dV [256, 384) | dK [384, 512).
 // ---------------------------------------------------------------------------
 struct KvSmem {
     static constexpr int k = 0, v = kTile;
-    static constexpr int st = 2 * kTile;                  // Q | dO | lse2 [128] | D [128] | r2 band [256]
+    static constexpr int st = 2 * kTile;                  // 2 stages: Q | dO | lse2 [128] | D [128] | r2 band [256]
     static constexpr int st_q = 0, st_do = kTile, st_vec = 2 * kTile;
     static constexpr int st_bytes = 2 * kTile + 2048;
-    static constexpr int ds = st + st_bytes;              // dS^T staging, K-major over queries
-    static constexpr int total = ds + kTile;
+    static constexpr int total = st + 2 * st_bytes;
 };
 
 struct KvBars {
-    uint64_t kv_full, st_full, st_empty, sdp_full, pds_ready, tile_done, mma_idle;
+    uint64_t kv_full, st_full[2], st_empty[2], sdp_full, pds_ready, tile_done, mma_idle;
 };
 
 __global__ void __launch_bounds__(kThreads, 1) dh_bwd_kv_kernel(const __grid_constant__ DhParams p) {
@@ -405,8 +392,10 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_kv_kernel(const __grid_con
     if (threadIdx.x == 0) {
         abort_flag = 0;
         mbar_init(&bars.kv_full, 1);
-        mbar_init(&bars.st_full, 1);
-        mbar_init(&bars.st_empty, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars.st_full[i], 1);
+            mbar_init(&bars.st_empty[i], 1);
+        }
         mbar_init(&bars.sdp_full, 1);
         mbar_init(&bars.pds_ready, 4);
         mbar_init(&bars.tile_done, 1);
@@ -430,16 +419,16 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_kv_kernel(const __grid_con
             if (!frz) load_tile(sm + KvSmem::k, &p.tm_k, &bars.kv_full, kb * 128, bh);
             load_tile(sm + KvSmem::v, &p.tm_v, &bars.kv_full, kb * 128, bh);
             for (int i = 0; i < ntiles; ++i) {
-                const int qb = kb + i;
-                if (!mbar_wait(&bars.st_empty, (i & 1) ^ 1u, abort, status, kStatusTimeout)) break;
-                uint8_t* st = sm + KvSmem::st;
+                const int qb = kb + i, s = i & 1;
+                if (!mbar_wait(&bars.st_empty[s], ((i >> 1) & 1) ^ 1u, abort, status, kStatusTimeout)) break;
+                uint8_t* st = sm + KvSmem::st + s * KvSmem::st_bytes;
                 float* vec = reinterpret_cast<float*>(st + KvSmem::st_vec);
-                mbar_expect_tx(&bars.st_full, (frz ? kTile : 2 * kTile) + 1024 + (frz ? 1024 : 0));
-                if (!frz) load_tile(st + KvSmem::st_q, &p.tm_q, &bars.st_full, qb * 128, bh);
-                load_tile(st + KvSmem::st_do, &p.tm_do, &bars.st_full, qb * 128, bh);
-                bulk_load(vec, p.rowvec + ((size_t)bh * p.nqb + qb) * 256, 1024, &bars.st_full);
+                mbar_expect_tx(&bars.st_full[s], (frz ? kTile : 2 * kTile) + 1024 + (frz ? 1024 : 0));
+                if (!frz) load_tile(st + KvSmem::st_q, &p.tm_q, &bars.st_full[s], qb * 128, bh);
+                load_tile(st + KvSmem::st_do, &p.tm_do, &bars.st_full[s], qb * 128, bh);
+                bulk_load(vec, p.rowvec + ((size_t)bh * p.nqb + qb) * 256, 1024, &bars.st_full[s]);
                 if (frz)
-                    bulk_load(vec + 256, p.r2p + (size_t)h * (p.Tp + 256) + (size_t)i * 128, 1024, &bars.st_full);
+                    bulk_load(vec + 256, p.r2p + (size_t)h * (p.Tp + 256) + (size_t)i * 128, 1024, &bars.st_full[s]);
             }
         }
     } else if (warp == 5) {
@@ -447,14 +436,15 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_kv_kernel(const __grid_con
             const uint32_t id_s = idesc_bf16(128, 128, 0, 0);   // S^T = K Q^T, dP^T = V dO^T
             const uint32_t id_n = idesc_bf16(128, 64, 0, 1);    // dV += P^T dO, dK += dS^T Q (B MN-major)
             const uint32_t sk = smem_u32(sm + KvSmem::k), sv = smem_u32(sm + KvSmem::v);
-            const uint32_t sq = smem_u32(sm + KvSmem::st + KvSmem::st_q);
-            const uint32_t sdo = smem_u32(sm + KvSmem::st + KvSmem::st_do);
-            const uint32_t sds = smem_u32(sm + KvSmem::ds);
             bool ok = mbar_wait(&bars.kv_full, 0, abort, status, kStatusTimeout);
             for (int i = 0; i < ntiles && ok; ++i) {
-                if (!(ok = mbar_wait(&bars.st_full, i & 1, abort, status, kStatusTimeout))) break;
+                const int s = i & 1;
+                if (!(ok = mbar_wait(&bars.st_full[s], (i >> 1) & 1, abort, status, kStatusTimeout))) break;
                 tc_fence_after();
+                const uint32_t st = smem_u32(sm + KvSmem::st + s * KvSmem::st_bytes);
+                const uint32_t sq = st + KvSmem::st_q, sdo = st + KvSmem::st_do;
                 if (!frz) {
+                    // after the previous tile's dV and dK MMAs, which read columns [0, 128)
 #pragma unroll
                     for (int k = 0; k < 8; ++k) mma_ss(tmem, kmaj(sk, k), kmaj(sq, k), id_s, k > 0);
 #pragma unroll
@@ -467,16 +457,17 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_kv_kernel(const __grid_con
                 for (int k = 0; k < 8; ++k)
 #pragma unroll
                     for (int c = 0; c < 2; ++c)
-                        mma_ts(tmem + 256 + 64 * c, tmem + 8 * k, mnmaj(sdo, c, k), id_n, (i > 0 || k > 0) ? 1u : 0u);
+                        mma_ts(tmem + 256 + 64 * c, tmem + chunk_col(k, 0), mnmaj(sdo, c, k), id_n,
+                               (i > 0 || k > 0) ? 1u : 0u);
                 if (!frz) {
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
 #pragma unroll
                         for (int c = 0; c < 2; ++c)
-                            mma_ss(tmem + 384 + 64 * c, kmaj(sds, k), mnmaj(sq, c, k), id_n,
+                            mma_ts(tmem + 384 + 64 * c, tmem + chunk_col(k, 1), mnmaj(sq, c, k), id_n,
                                    (i > 0 || k > 0) ? 1u : 0u);
                 }
-                mma_commit(&bars.st_empty);
+                mma_commit(&bars.st_empty[s]);
                 mma_commit(&bars.tile_done);
             }
             mma_commit(&bars.mma_idle);
@@ -487,20 +478,20 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_kv_kernel(const __grid_con
         const int key = kb * 128 + t;
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
         const float a2k = frz ? p.a2p[(size_t)h * p.Tp + key] : 0.f;
-        uint8_t* sds = sm + KvSmem::ds;
         bool ok = true;
         for (int i = 0; i < ntiles; ++i) {
             const bool diag = i == 0;
-            if (!(ok = mbar_wait(&bars.st_full, i & 1, abort, status, kStatusTimeout))) break;
-            const float* vec = reinterpret_cast<const float*>(sm + KvSmem::st + KvSmem::st_vec);
-            uint32_t pk[64];
+            const int s = i & 1;
+            if (!(ok = mbar_wait(&bars.st_full[s], (i >> 1) & 1, abort, status, kStatusTimeout))) break;
+            const float* vec =
+                reinterpret_cast<const float*>(sm + KvSmem::st + s * KvSmem::st_bytes + KvSmem::st_vec);
             if (!frz) {
                 // S^T, dP^T of this tile; their commit also means the previous tile's MMAs are done
                 if (!(ok = mbar_wait(&bars.sdp_full, i & 1, abort, status, kStatusTimeout))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) {
-                    uint32_t su[32], du[32], dk[16];
+                    uint32_t su[32], du[32], pk[16], dk[16];
                     tmem_ld32(lane_base + 32 * c4, su);
                     tmem_ld32(lane_base + 128 + 32 * c4, du);
                     tmem_ld_wait();
@@ -513,27 +504,32 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_kv_kernel(const __grid_con
                         if (diag && q0 + 1 < t) p1 = 0.f;
                         const float d0 = p0 * (__uint_as_float(du[e]) - vec[128 + q0]);
                         const float d1 = p1 * (__uint_as_float(du[e + 1]) - vec[128 + q0 + 1]);
-                        pk[q0 >> 1] = pack_bf16(p0, p1);
+                        pk[e >> 1] = pack_bf16(p0, p1);
                         dk[e >> 1] = pack_bf16(d0, d1);
                     }
-                    store_quarter_kmajor(sds, t, c4, dk);
+                    // chunk c4's own columns, already read
+                    tmem_st16(lane_base + 32 * c4, pk);
+                    tmem_st16(lane_base + 32 * c4 + 16, dk);
                 }
-                fence_proxy_async_smem();
             } else {
                 // W^T(key, q) = exp2(a2[key] + r2[q - key] - log2 Z(q)); the band holds r at
-                // distance i 128 + c - t at entry 127 + c - t
+                // distance i 128 + c - t at entry 127 + c - t. The previous tile's dV MMA has
+                // read its W^T before this one is written.
                 if (i > 0 && !(ok = mbar_wait(&bars.tile_done, (i - 1) & 1, abort, status, kStatusTimeout))) break;
                 tc_fence_after();
                 const float* band = vec + 256 + 127 - t;
 #pragma unroll
-                for (int c = 0; c < 128; c += 2) {
-                    const float w0 = fast_exp2(a2k + band[c] - vec[c]);
-                    const float w1 = fast_exp2(a2k + band[c + 1] - vec[c + 1]);
-                    pk[c >> 1] = pack_bf16(w0, w1);
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const int c = 32 * c4 + e;
+                        pk[e >> 1] = pack_bf16(fast_exp2(a2k + band[c] - vec[c]),
+                                               fast_exp2(a2k + band[c + 1] - vec[c + 1]));
+                    }
+                    tmem_st16(lane_base + 32 * c4, pk);
                 }
             }
-            tmem_st32(lane_base, pk);
-            tmem_st32(lane_base + 32, pk + 32);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -569,19 +565,20 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_kv_kernel(const __grid_con
 
 // ---------------------------------------------------------------------------
 // Backward, query-block pass: dQ of query block qb of an ordinary slice (zeros
-// for frozen slices). TMEM: S [0, 128) | dP [128, 256) | dQ [256, 384).
+// for frozen slices). K and V of the next key block load while this one runs.
+// TMEM: S [0, 128) fp32, overwritten chunk by chunk with dS as bf16 pairs
+//       (chunk c at [32 c, 32 c + 16)) | dP [128, 256) | dQ [256, 384).
 // ---------------------------------------------------------------------------
 struct QSmem {
     static constexpr int q = 0, dO = kTile;
-    static constexpr int st = 2 * kTile;                  // K | V
+    static constexpr int st = 2 * kTile;                  // 2 stages: K | V
     static constexpr int st_k = 0, st_v = kTile;
     static constexpr int st_bytes = 2 * kTile;
-    static constexpr int ds = st + st_bytes;              // dS staging, K-major over keys
-    static constexpr int total = ds + kTile;
+    static constexpr int total = st + 2 * st_bytes;
 };
 
 struct QBars {
-    uint64_t q_full, st_full, st_empty, sdp_full, ds_ready, tile_done, mma_idle;
+    uint64_t q_full, st_full[2], st_empty[2], sdp_full, ds_ready, tile_done, mma_idle;
 };
 
 __global__ void __launch_bounds__(kThreads, 1) dh_bwd_q_kernel(const __grid_constant__ DhParams p) {
@@ -611,8 +608,10 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_q_kernel(const __grid_cons
     if (threadIdx.x == 0) {
         abort_flag = 0;
         mbar_init(&bars.q_full, 1);
-        mbar_init(&bars.st_full, 1);
-        mbar_init(&bars.st_empty, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars.st_full[i], 1);
+            mbar_init(&bars.st_empty[i], 1);
+        }
         mbar_init(&bars.sdp_full, 1);
         mbar_init(&bars.ds_ready, 4);
         mbar_init(&bars.tile_done, 1);
@@ -636,10 +635,12 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_q_kernel(const __grid_cons
             load_tile(sm + QSmem::q, &p.tm_q, &bars.q_full, qb * 128, bh);
             load_tile(sm + QSmem::dO, &p.tm_do, &bars.q_full, qb * 128, bh);
             for (int j = 0; j < nblk; ++j) {
-                if (!mbar_wait(&bars.st_empty, (j & 1) ^ 1u, abort, status, kStatusTimeout)) break;
-                mbar_expect_tx(&bars.st_full, 2 * kTile);
-                load_tile(sm + QSmem::st + QSmem::st_k, &p.tm_k, &bars.st_full, j * 128, bh);
-                load_tile(sm + QSmem::st + QSmem::st_v, &p.tm_v, &bars.st_full, j * 128, bh);
+                const int s = j & 1;
+                if (!mbar_wait(&bars.st_empty[s], ((j >> 1) & 1) ^ 1u, abort, status, kStatusTimeout)) break;
+                uint8_t* st = sm + QSmem::st + s * QSmem::st_bytes;
+                mbar_expect_tx(&bars.st_full[s], 2 * kTile);
+                load_tile(st + QSmem::st_k, &p.tm_k, &bars.st_full[s], j * 128, bh);
+                load_tile(st + QSmem::st_v, &p.tm_v, &bars.st_full[s], j * 128, bh);
             }
         }
     } else if (warp == 5) {
@@ -647,12 +648,14 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_q_kernel(const __grid_cons
             const uint32_t id_s = idesc_bf16(128, 128, 0, 0);   // S = Q K^T, dP = dO V^T
             const uint32_t id_n = idesc_bf16(128, 64, 0, 1);    // dQ += dS K (K MN-major)
             const uint32_t sq = smem_u32(sm + QSmem::q), sdo = smem_u32(sm + QSmem::dO);
-            const uint32_t sk = smem_u32(sm + QSmem::st + QSmem::st_k), sv = smem_u32(sm + QSmem::st + QSmem::st_v);
-            const uint32_t sds = smem_u32(sm + QSmem::ds);
             bool ok = mbar_wait(&bars.q_full, 0, abort, status, kStatusTimeout);
             for (int j = 0; j < nblk && ok; ++j) {
-                if (!(ok = mbar_wait(&bars.st_full, j & 1, abort, status, kStatusTimeout))) break;
+                const int s = j & 1;
+                if (!(ok = mbar_wait(&bars.st_full[s], (j >> 1) & 1, abort, status, kStatusTimeout))) break;
                 tc_fence_after();
+                const uint32_t st = smem_u32(sm + QSmem::st + s * QSmem::st_bytes);
+                const uint32_t sk = st + QSmem::st_k, sv = st + QSmem::st_v;
+                // after the previous block's dQ MMAs, which read dS from columns [0, 128)
 #pragma unroll
                 for (int k = 0; k < 8; ++k) mma_ss(tmem, kmaj(sq, k), kmaj(sk, k), id_s, k > 0);
 #pragma unroll
@@ -664,8 +667,9 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_q_kernel(const __grid_cons
                 for (int k = 0; k < 8; ++k)
 #pragma unroll
                     for (int c = 0; c < 2; ++c)
-                        mma_ss(tmem + 256 + 64 * c, kmaj(sds, k), mnmaj(sk, c, k), id_n, (j > 0 || k > 0) ? 1u : 0u);
-                mma_commit(&bars.st_empty);
+                        mma_ts(tmem + 256 + 64 * c, tmem + chunk_col(k, 0), mnmaj(sk, c, k), id_n,
+                               (j > 0 || k > 0) ? 1u : 0u);
+                mma_commit(&bars.st_empty[s]);
                 mma_commit(&bars.tile_done);
             }
             mma_commit(&bars.mma_idle);
@@ -677,15 +681,13 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_q_kernel(const __grid_cons
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
         const float* rv = p.rowvec + ((size_t)bh * p.nqb + qb) * 256;
         const float l2 = rv[t], dd = rv[128 + t];
-        uint8_t* sds = sm + QSmem::ds;
         bool ok = true;
         for (int j = 0; j < nblk; ++j) {
             if (!(ok = mbar_wait(&bars.sdp_full, j & 1, abort, status, kStatusTimeout))) break;
             tc_fence_after();
-            uint32_t dk[64];
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
-                uint32_t su[32], du[32];
+                uint32_t su[32], du[32], dk[16];
                 tmem_ld32(lane_base + 32 * c4, su);
                 tmem_ld32(lane_base + 128 + 32 * c4, du);
                 tmem_ld_wait();
@@ -696,11 +698,11 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_q_kernel(const __grid_cons
                     float p1 = fast_exp2(__uint_as_float(su[e + 1]) * p.scale_log2 - l2);
                     if (j == qb && k0 > t) p0 = 0.f;
                     if (j == qb && k0 + 1 > t) p1 = 0.f;
-                    dk[k0 >> 1] = pack_bf16(p0 * (__uint_as_float(du[e]) - dd), p1 * (__uint_as_float(du[e + 1]) - dd));
+                    dk[e >> 1] = pack_bf16(p0 * (__uint_as_float(du[e]) - dd), p1 * (__uint_as_float(du[e + 1]) - dd));
                 }
+                tmem_st16(lane_base + 32 * c4, dk);   // chunk c4's own columns, already read
             }
-            store_row_kmajor(sds, t, dk);
-            fence_proxy_async_smem();
+            tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars.ds_ready);

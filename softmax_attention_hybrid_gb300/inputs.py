@@ -64,6 +64,9 @@ WORKLOADS = {
     # 32 query heads over 8 key/value heads (the grouped-query layout of the paper's
     # Qwen3-4B study, App. C.6) at head dimension 64, one frozen query head per group
     "gqa_32q8kv_4k": Workload("gqa_32q8kv_4k", 4, 32, 8, 4096, 64, "bf16", 0.5, 0.02, Hkv=8),
+    # the paper's 1B layer at its own head dimension (App. C.5: 16 heads of d 96),
+    # a quarter of them frozen, at the 8K context of the long-sequence runs
+    "1b_d96": Workload("1b_d96", 2, 16, 4, 8192, 96, "bf16", 0.5, 0.01),
 }
 
 
