@@ -46,10 +46,11 @@ __device__ __forceinline__ float fast_exp2(float x) {
 __device__ __forceinline__ uint64_t kmaj(uint32_t tile, int k) {
     return sdesc_sw128(tile + (uint32_t)(k >> 2) * kAtom + (uint32_t)(k & 3) * 32, 16, 1024);
 }
-// Descriptor of k-step k (16 rows) of atom c (64 columns of d) of a tile read
-// MN-major (d as the N dimension).
-__device__ __forceinline__ uint64_t mnmaj(uint32_t tile, int c, int k) {
-    return sdesc_sw128(tile + (uint32_t)c * kAtom + (uint32_t)k * 2048, 16384, 1024);
+// Descriptor of k-step k (16 rows) of a tile read MN-major (d as the N dimension):
+// the leading-dimension offset steps from the first 64 columns of d (atom 0) to the
+// next (atom 1), so one N = 128 MMA covers the whole padded head dimension.
+__device__ __forceinline__ uint64_t mnmaj(uint32_t tile, int k) {
+    return sdesc_sw128(tile + (uint32_t)k * 2048, kAtom, 1024);
 }
 
 // Load a [128 x 128] tile (two atoms) of tensor map `map` at row y of slice z.
@@ -181,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 2) dh_fwd_kernel(const __grid_consta
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t id_s = idesc_bf16(128, 128, 0, 0);   // S = Q K^T
-            const uint32_t id_o = idesc_bf16(128, 64, 0, 1);    // O += P V, V MN-major
+            const uint32_t id_o = idesc_bf16(128, 128, 0, 1);   // O += P V, V MN-major
             const uint32_t d_s = tmem, d_o = tmem + 128;
             const uint32_t sq = smem_u32(sm + FwdSmem::q), sk = smem_u32(sm + FwdSmem::k);
             const uint32_t sv = smem_u32(sm + FwdSmem::v);
@@ -201,10 +202,7 @@ __global__ void __launch_bounds__(kThreads, 2) dh_fwd_kernel(const __grid_consta
                 if (!(ok = mbar_wait(&bars.p_ready, j & 1, abort, status, kStatusTimeout))) break;
                 tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-#pragma unroll
-                    for (int c = 0; c < 2; ++c)
-                        mma_ts(d_o + 64 * c, d_s + 8 * k, mnmaj(sv, c, k), id_o, (j > 0 || k > 0) ? 1u : 0u);
+                for (int k = 0; k < 8; ++k) mma_ts(d_o, d_s + 8 * k, mnmaj(sv, k), id_o, (j > 0 || k > 0) ? 1u : 0u);
                 mma_commit(&bars.o_done);
                 mma_commit(&bars.v_empty);
                 // S(j + 1) overwrites the columns P(j) is read from; MMAs run in issue order
@@ -434,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_kv_kernel(const __grid_con
     } else if (warp == 5) {
         if (lane == 0) {
             const uint32_t id_s = idesc_bf16(128, 128, 0, 0);   // S^T = K Q^T, dP^T = V dO^T
-            const uint32_t id_n = idesc_bf16(128, 64, 0, 1);    // dV += P^T dO, dK += dS^T Q (B MN-major)
+            const uint32_t id_n = idesc_bf16(128, 128, 0, 1);   // dV += P^T dO, dK += dS^T Q (B MN-major)
             const uint32_t sk = smem_u32(sm + KvSmem::k), sv = smem_u32(sm + KvSmem::v);
             bool ok = mbar_wait(&bars.kv_full, 0, abort, status, kStatusTimeout);
             for (int i = 0; i < ntiles && ok; ++i) {
@@ -455,17 +453,11 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_kv_kernel(const __grid_con
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-#pragma unroll
-                    for (int c = 0; c < 2; ++c)
-                        mma_ts(tmem + 256 + 64 * c, tmem + chunk_col(k, 0), mnmaj(sdo, c, k), id_n,
-                               (i > 0 || k > 0) ? 1u : 0u);
+                    mma_ts(tmem + 256, tmem + chunk_col(k, 0), mnmaj(sdo, k), id_n, (i > 0 || k > 0) ? 1u : 0u);
                 if (!frz) {
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-#pragma unroll
-                        for (int c = 0; c < 2; ++c)
-                            mma_ts(tmem + 384 + 64 * c, tmem + chunk_col(k, 1), mnmaj(sq, c, k), id_n,
-                                   (i > 0 || k > 0) ? 1u : 0u);
+                        mma_ts(tmem + 384, tmem + chunk_col(k, 1), mnmaj(sq, k), id_n, (i > 0 || k > 0) ? 1u : 0u);
                 }
                 mma_commit(&bars.st_empty[s]);
                 mma_commit(&bars.tile_done);
@@ -646,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_q_kernel(const __grid_cons
     } else if (warp == 5) {
         if (lane == 0) {
             const uint32_t id_s = idesc_bf16(128, 128, 0, 0);   // S = Q K^T, dP = dO V^T
-            const uint32_t id_n = idesc_bf16(128, 64, 0, 1);    // dQ += dS K (K MN-major)
+            const uint32_t id_n = idesc_bf16(128, 128, 0, 1);   // dQ += dS K (K MN-major)
             const uint32_t sq = smem_u32(sm + QSmem::q), sdo = smem_u32(sm + QSmem::dO);
             bool ok = mbar_wait(&bars.q_full, 0, abort, status, kStatusTimeout);
             for (int j = 0; j < nblk && ok; ++j) {
@@ -665,10 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_q_kernel(const __grid_cons
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-#pragma unroll
-                    for (int c = 0; c < 2; ++c)
-                        mma_ts(tmem + 256 + 64 * c, tmem + chunk_col(k, 0), mnmaj(sk, c, k), id_n,
-                               (j > 0 || k > 0) ? 1u : 0u);
+                    mma_ts(tmem + 256, tmem + chunk_col(k, 0), mnmaj(sk, k), id_n, (j > 0 || k > 0) ? 1u : 0u);
                 mma_commit(&bars.st_empty[s]);
                 mma_commit(&bars.tile_done);
             }
