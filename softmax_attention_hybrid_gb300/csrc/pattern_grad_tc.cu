@@ -528,6 +528,13 @@ pg_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restr
         const int part = threadIdx.x & 3;
         const int b = slice / p.F, f = slice - b * p.F;
         const int h = p.frz_heads[f];
+        // log Z(i) and the maxima are loaded with o and dO, not after the dot product
+        float lz = 0.f, am = 0.f, rm = 0.f;
+        if (part == 0 && i < p.T) {
+            lz = lse[(size_t)h * p.T + i];
+            am = amax[h];
+            rm = amax[p.H + h];
+        }
         float d = 0.f;
         if (i < p.T) {
             const size_t row = ((size_t)b * p.H + h) * p.T + i;
@@ -545,8 +552,8 @@ pg_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restr
         d += __shfl_xor_sync(0xffffffffu, d, 1);
         d += __shfl_xor_sync(0xffffffffu, d, 2);
         if (part == 0) {
-            float lz, y = 0.f;
-            if (i < p.T) y = -d * pg_invz(lse, amax, hflag, p.H, p.T, h, i, &lz);
+            // 1 / Z'(i) as pg_invz forms it (the head blocks below raise the exact-form flag)
+            const float y = i < p.T ? -d * expf(fminf(-(lz - am - rm), 80.f)) : 0.f;
             const size_t at = (size_t)slice * p.Tp + (i & ~127) + qperm(i & 127);
             p.yx[at] = d;
             p.yf[at] = y;
@@ -576,15 +583,16 @@ pg_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restr
 // that exist (band < nqb - x / 128); dr[h, x] = sum_b of the two bands that hold
 // distance x (band x / 128: entry x mod 128 + 128; band x / 128 + 1: entry
 // x mod 128). Ordinary heads get zeros.
-// Grid (ceil(T / 32), H), 256 threads: 32 keys x 8 groups. Group g = 2 c + half
-// adds, for b = 0.. and then band = c, c + 4, ..., the terms of its column half;
-// group 0 then adds the eight partial sums in group order, and group 1 the dr
+// Grid (ceil(T / 32), H), 512 threads: 32 keys x 16 groups. Group g = 2 c + half
+// adds, for b = 0.. and then band = c, c + 8, ..., the terms of its column half;
+// group 0 then adds the sixteen partial sums in group order, and group 1 the dr
 // terms in batch order. Every result has the same bits on every run.
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(512)
 pg_reduce_kernel(const __grid_constant__ PgParams p, float* __restrict__ da, float* __restrict__ dr) {
     grid_dep_wait();
     grid_dep_launch();
-    __shared__ float part[8][32];
+    constexpr int kGroups = 16, kPhases = kGroups / 2;
+    __shared__ float part[kGroups][32];
     const int h = blockIdx.y;
     const int lane = threadIdx.x & 31, grp = threadIdx.x >> 5;
     const int x = blockIdx.x * 32 + lane;
@@ -612,7 +620,7 @@ pg_reduce_kernel(const __grid_constant__ PgParams p, float* __restrict__ da, flo
             for (int u = 0; u < 8; ++u) {
                 const bool in = b < p.B;
                 v[u] = in ? base[b * stride_b + band * stride_band] : 0.f;
-                if (in && (band += 4) >= nb) {
+                if (in && (band += kPhases) >= nb) {
                     band = grp >> 1;
                     ++b;
                 }
@@ -627,7 +635,7 @@ pg_reduce_kernel(const __grid_constant__ PgParams p, float* __restrict__ da, flo
     if (grp == 0) {
         float t = part[0][lane];
 #pragma unroll
-        for (int g = 1; g < 8; ++g) t += part[g][lane];
+        for (int g = 1; g < kGroups; ++g) t += part[g][lane];
         da[(size_t)h * p.T + x] = t;
     } else if (grp == 1) {
         float sr = 0.f;
@@ -795,7 +803,7 @@ extern "C" int saf_pattern_grad_tc(const void* v, const void* dO, const void* o,
     }
     if (e == cudaSuccess) {
         note_launch();
-        e = launch_ex(pg_reduce_kernel, dim3((unsigned)((T + 31) / 32), (unsigned)H), dim3(256), 0, s, true, 1, p,
+        e = launch_ex(pg_reduce_kernel, dim3((unsigned)((T + 31) / 32), (unsigned)H), dim3(512), 0, s, true, 1, p,
                       da, dr);
     }
     after_launch(SAF_KERNEL_PATTERN_GRAD, s);
