@@ -32,7 +32,8 @@ using namespace tc;
 
 constexpr int kAtom = 128 * 64 * 2;    // 128 rows x 64 bf16, 128-byte swizzle
 constexpr int kTile = 2 * kAtom;       // 128 rows x 128 (d padded to 128)
-constexpr int kThreads = 192;
+constexpr int kThreads = 192;      // forward: 4 row warps, a TMA warp, an MMA warp
+constexpr int kThreadsBwd = 320;   // backward: 8 row warps (a row's columns in two halves), TMA, MMA
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -66,6 +67,23 @@ __device__ __forceinline__ void store_out_row(__nv_bfloat16* out, int d, const u
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
         if (c < n) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                w[e] = pack_bf16(__uint_as_float(v[8 * c + 2 * e]) * scale,
+                                 __uint_as_float(v[8 * c + 2 * e + 1]) * scale);
+            dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
+// Columns c0 .. c0 + n - 1 (n a multiple of 8, at most 64) of a bf16 output row from
+// n fp32 values (scaled), 16-byte stores.
+__device__ __forceinline__ void store_out_cols(__nv_bfloat16* row, int c0, int n, const uint32_t* v, float scale) {
+    uint4* dst = reinterpret_cast<uint4*>(row + c0);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        if (8 * c < n) {
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e)
@@ -373,7 +391,7 @@ struct KvBars {
     uint64_t kv_full, st_full[2], st_empty[2], sdp_full, pds_ready, tile_done, mma_idle;
 };
 
-__global__ void __launch_bounds__(kThreads, 1) dh_bwd_kv_kernel(const __grid_constant__ DhParams p) {
+__global__ void __launch_bounds__(kThreadsBwd, 1) dh_bwd_kv_kernel(const __grid_constant__ DhParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     __shared__ KvBars bars;
@@ -395,12 +413,12 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_kv_kernel(const __grid_con
             mbar_init(&bars.st_empty[i], 1);
         }
         mbar_init(&bars.sdp_full, 1);
-        mbar_init(&bars.pds_ready, 4);
+        mbar_init(&bars.pds_ready, 8);
         mbar_init(&bars.tile_done, 1);
         mbar_init(&bars.mma_idle, 1);
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == 9) {
         tmem_alloc(&tmem_base_sh, 512);
         tmem_relinquish();
     }
@@ -411,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_kv_kernel(const __grid_con
     volatile int* abort = &abort_flag;
     uint32_t* status = p.status;
 
-    if (warp == 4) {
+    if (warp == 8) {
         if (lane == 0) {
             mbar_expect_tx(&bars.kv_full, frz ? kTile : 2 * kTile);
             if (!frz) load_tile(sm + KvSmem::k, &p.tm_k, &bars.kv_full, kb * 128, bh);
@@ -429,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_kv_kernel(const __grid_con
                     bulk_load(vec + 256, p.r2p + (size_t)h * (p.Tp + 256) + (size_t)i * 128, 1024, &bars.st_full[s]);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         if (lane == 0) {
             const uint32_t id_s = idesc_bf16(128, 128, 0, 0);   // S^T = K Q^T, dP^T = V dO^T
             const uint32_t id_n = idesc_bf16(128, 128, 0, 1);   // dV += P^T dO, dK += dS^T Q (B MN-major)
@@ -466,9 +484,11 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_kv_kernel(const __grid_con
             mbar_wait_bounded(&bars.mma_idle, 0, kWaitLimitNs);
         }
     } else {
-        const int t = threadIdx.x;   // key row of the block = TMEM lane
+        // warp w: key rows 32 (w % 4) .. + 31 (its TMEM lanes), query columns 64 (w / 4) .. + 63
+        const int quarter = warp & 3, half = warp >> 2;
+        const int t = quarter * 32 + lane;   // key row of the block = TMEM lane
         const int key = kb * 128 + t;
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         const float a2k = frz ? p.a2p[(size_t)h * p.Tp + key] : 0.f;
         bool ok = true;
         for (int i = 0; i < ntiles; ++i) {
@@ -482,7 +502,8 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_kv_kernel(const __grid_con
                 if (!(ok = mbar_wait(&bars.sdp_full, i & 1, abort, status, kStatusTimeout))) break;
                 tc_fence_after();
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int c4 = 2 * half + cc;   // chunk of 32 queries
                     uint32_t su[32], du[32], pk[16], dk[16];
                     tmem_ld32(lane_base + 32 * c4, su);
                     tmem_ld32(lane_base + 128 + 32 * c4, du);
@@ -511,7 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_kv_kernel(const __grid_con
                 tc_fence_after();
                 const float* band = vec + 256 + 127 - t;
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int c4 = 2 * half + cc;
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
@@ -527,29 +549,31 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_kv_kernel(const __grid_con
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars.pds_ready);
         }
-        // tcgen05.ld is warp-collective: every lane loads, only rows inside T are stored
+        // tcgen05.ld is warp-collective: every lane loads, only rows inside T are stored;
+        // each half of the warps writes its 64 columns of dV and dK (those inside d)
         if (ok && mbar_wait(&bars.tile_done, (ntiles - 1) & 1, abort, status, kStatusTimeout)) {
             tc_fence_after();
-            uint32_t v[128];
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(lane_base + 256 + 32 * c4, v + 32 * c4);
+            const int c0 = 64 * half, n = min(64, p.d - c0);
+            uint32_t v[64];
+            tmem_ld32(lane_base + 256 + c0, v);
+            tmem_ld32(lane_base + 256 + c0 + 32, v + 32);
             tmem_ld_wait();
-            if (key < p.T) store_out_row(p.dv + ((size_t)bh * p.T + key) * p.d, p.d, v, 1.f);
+            if (key < p.T) store_out_cols(p.dv + ((size_t)bh * p.T + key) * p.d, c0, n, v, 1.f);
             if (!frz) {
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(lane_base + 384 + 32 * c4, v + 32 * c4);
+                tmem_ld32(lane_base + 384 + c0, v);
+                tmem_ld32(lane_base + 384 + c0 + 32, v + 32);
                 tmem_ld_wait();
             } else {
 #pragma unroll
-                for (int c = 0; c < 128; ++c) v[c] = 0u;
+                for (int c = 0; c < 64; ++c) v[c] = 0u;
             }
-            if (key < p.T) store_out_row(p.dk + ((size_t)bh * p.T + key) * p.d, p.d, v, p.scale);
+            if (key < p.T) store_out_cols(p.dk + ((size_t)bh * p.T + key) * p.d, c0, n, v, p.scale);
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -573,7 +597,7 @@ struct QBars {
     uint64_t q_full, st_full[2], st_empty[2], sdp_full, ds_ready, tile_done, mma_idle;
 };
 
-__global__ void __launch_bounds__(kThreads, 1) dh_bwd_q_kernel(const __grid_constant__ DhParams p) {
+__global__ void __launch_bounds__(kThreadsBwd, 1) dh_bwd_q_kernel(const __grid_constant__ DhParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     __shared__ QBars bars;
@@ -605,12 +629,12 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_q_kernel(const __grid_cons
             mbar_init(&bars.st_empty[i], 1);
         }
         mbar_init(&bars.sdp_full, 1);
-        mbar_init(&bars.ds_ready, 4);
+        mbar_init(&bars.ds_ready, 8);
         mbar_init(&bars.tile_done, 1);
         mbar_init(&bars.mma_idle, 1);
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == 9) {
         tmem_alloc(&tmem_base_sh, 512);
         tmem_relinquish();
     }
@@ -621,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_q_kernel(const __grid_cons
     volatile int* abort = &abort_flag;
     uint32_t* status = p.status;
 
-    if (warp == 4) {
+    if (warp == 8) {
         if (lane == 0) {
             mbar_expect_tx(&bars.q_full, 2 * kTile);
             load_tile(sm + QSmem::q, &p.tm_q, &bars.q_full, qb * 128, bh);
@@ -635,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_q_kernel(const __grid_cons
                 load_tile(st + QSmem::st_v, &p.tm_v, &bars.st_full[s], j * 128, bh);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         if (lane == 0) {
             const uint32_t id_s = idesc_bf16(128, 128, 0, 0);   // S = Q K^T, dP = dO V^T
             const uint32_t id_n = idesc_bf16(128, 128, 0, 1);   // dQ += dS K (K MN-major)
@@ -665,9 +689,11 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_q_kernel(const __grid_cons
             mbar_wait_bounded(&bars.mma_idle, 0, kWaitLimitNs);
         }
     } else {
-        const int t = threadIdx.x;   // query row of the block = TMEM lane
+        // warp w: query rows 32 (w % 4) .. + 31 (its TMEM lanes), key columns 64 (w / 4) .. + 63
+        const int quarter = warp & 3, half = warp >> 2;
+        const int t = quarter * 32 + lane;   // query row of the block = TMEM lane
         const int row = qb * 128 + t;
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         const float* rv = p.rowvec + ((size_t)bh * p.nqb + qb) * 256;
         const float l2 = rv[t], dd = rv[128 + t];
         bool ok = true;
@@ -675,7 +701,8 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_q_kernel(const __grid_cons
             if (!(ok = mbar_wait(&bars.sdp_full, j & 1, abort, status, kStatusTimeout))) break;
             tc_fence_after();
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c4 = 2 * half + cc;   // chunk of 32 keys
                 uint32_t su[32], du[32], dk[16];
                 tmem_ld32(lane_base + 32 * c4, su);
                 tmem_ld32(lane_base + 128 + 32 * c4, du);
@@ -698,17 +725,18 @@ __global__ void __launch_bounds__(kThreads, 1) dh_bwd_q_kernel(const __grid_cons
         }
         if (ok && mbar_wait(&bars.tile_done, (nblk - 1) & 1, abort, status, kStatusTimeout)) {
             tc_fence_after();
-            uint32_t v[128];
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(lane_base + 256 + 32 * c4, v + 32 * c4);
+            const int c0 = 64 * half, n = min(64, p.d - c0);
+            uint32_t v[64];
+            tmem_ld32(lane_base + 256 + c0, v);
+            tmem_ld32(lane_base + 256 + c0 + 32, v + 32);
             tmem_ld_wait();
-            if (row < p.T) store_out_row(p.dq + ((size_t)bh * p.T + row) * p.d, p.d, v, p.scale);
+            if (row < p.T) store_out_cols(p.dq + ((size_t)bh * p.T + row) * p.d, c0, n, v, p.scale);
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -779,11 +807,11 @@ cudaError_t launch_dh_bwd(const LayerArgs& a, cudaStream_t s) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(dh_bwd_q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_q);
     if (e != cudaSuccess) return e;
     before_launch(SAF_KERNEL_BWD_KV, s);
-    e = launch_ex(dh_bwd_kv_kernel, grid, dim3(kThreads), (size_t)smem_kv, s, true, 1, p);
+    e = launch_ex(dh_bwd_kv_kernel, grid, dim3(kThreadsBwd), (size_t)smem_kv, s, true, 1, p);
     after_launch(SAF_KERNEL_BWD_KV, s);
     if (e != cudaSuccess) return e;
     before_launch(SAF_KERNEL_BWD_Q, s);
-    e = launch_ex(dh_bwd_q_kernel, grid, dim3(kThreads), (size_t)smem_q, s, true, 1, p);
+    e = launch_ex(dh_bwd_q_kernel, grid, dim3(kThreadsBwd), (size_t)smem_q, s, true, 1, p);
     after_launch(SAF_KERNEL_BWD_Q, s);
     return e;
 }
