@@ -142,35 +142,6 @@ __device__ __forceinline__ void named_bar_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-// Element i (0..3) of four 16-byte values, i in a register.
-__device__ __forceinline__ uint4 sel4(const uint4 (&v)[4], int i) {
-    const uint4 lo = (i & 1) ? v[1] : v[0];
-    const uint4 hi = (i & 1) ? v[3] : v[2];
-    return (i & 2) ? hi : lo;
-}
-
-__device__ __forceinline__ uint4 shfl_xor4(const uint4 v, int m) {
-    return make_uint4(__shfl_xor_sync(0xffffffffu, v.x, m), __shfl_xor_sync(0xffffffffu, v.y, m),
-                      __shfl_xor_sync(0xffffffffu, v.z, m), __shfl_xor_sync(0xffffffffu, v.w, m));
-}
-
-// A warp's 32 rows of 64 bytes each (lane l: row l, bytes x[0..3]) to global memory at
-// row0 + l * row_bytes, rows l < nrows only. The four lanes of a group first exchange their
-// 16-byte chunks (a 4 x 4 transpose in three xor rounds), so that each store instruction
-// writes 64 contiguous bytes of each of 8 rows: whole 32-byte sectors instead of 32
-// half sectors.
-__device__ __forceinline__ void store_rows64(uint8_t* row0, size_t row_bytes, int nrows, const uint4 (&x)[4],
-                                             int lane) {
-    const int a = lane & 3, g4 = lane & ~3;
-    uint4 z[4];   // z[k]: chunk a of group row a ^ k
-    z[0] = sel4(x, a);
-#pragma unroll
-    for (int k = 1; k < 4; ++k) z[k] = shfl_xor4(sel4(x, a ^ k), k);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        if (g4 + i < nrows) *reinterpret_cast<uint4*>(row0 + (size_t)(g4 + i) * row_bytes + 16 * a) = sel4(z, i ^ a);
-}
-
 struct Barriers {
     uint64_t item_full[kRing], item_empty[kRing];
     uint64_t kv_full, kv_empty;
@@ -704,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                                       pack_bf16(__uint_as_float(v[4]) * fv, __uint_as_float(v[5]) * fv),
                                       pack_bf16(__uint_as_float(v[6]) * fv, __uint_as_float(v[7]) * fv));
                 }
-                store_rows64(reinterpret_cast<uint8_t*>(p.dv + off), 128, nrows, x, lane);
+                store_rows64(reinterpret_cast<uint8_t*>(p.dv + off), 128, nrows, x);
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const uint32_t* v = dk + 8 * c;
@@ -714,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                                                      pack_bf16(__uint_as_float(v[4]) * kScale, __uint_as_float(v[5]) * kScale),
                                                      pack_bf16(__uint_as_float(v[6]) * kScale, __uint_as_float(v[7]) * kScale));
                 }
-                store_rows64(reinterpret_cast<uint8_t*>(p.dk + off), 128, nrows, x, lane);
+                store_rows64(reinterpret_cast<uint8_t*>(p.dk + off), 128, nrows, x);
             }
         }
     }

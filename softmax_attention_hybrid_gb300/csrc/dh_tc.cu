@@ -60,36 +60,24 @@ __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, 
     tma_load_3d(dst + kAtom, map, bar, 64, y, z);
 }
 
-// Row `row` of a d-column bf16 output from 128 fp32 values (scaled), 16-byte stores.
-__device__ __forceinline__ void store_out_row(__nv_bfloat16* out, int d, const uint32_t* v, float scale) {
-    uint4* dst = reinterpret_cast<uint4*>(out);
-    const int n = d / 8;
+// Columns c0 .. c0 + n - 1 (n a multiple of 32, at most 128, the same in every lane) of a
+// warp's 32 bf16 output rows of d elements: lane l holds row row0 + l as n fp32 values, which
+// are scaled and rounded; rows l < nrows only. Whole 32-byte sectors per store instruction.
+__device__ __forceinline__ void store_rows_cols(__nv_bfloat16* row0, int d, int nrows, int c0, int n,
+                                                const uint32_t* v, float scale) {
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
-        if (c < n) {
-            uint32_t w[4];
+    for (int q = 0; q < 4; ++q) {
+        if (32 * q < n) {
+            uint4 x[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                w[e] = pack_bf16(__uint_as_float(v[8 * c + 2 * e]) * scale,
-                                 __uint_as_float(v[8 * c + 2 * e + 1]) * scale);
-            dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-    }
-}
-
-// Columns c0 .. c0 + n - 1 (n a multiple of 8, at most 64) of a bf16 output row from
-// n fp32 values (scaled), 16-byte stores.
-__device__ __forceinline__ void store_out_cols(__nv_bfloat16* row, int c0, int n, const uint32_t* v, float scale) {
-    uint4* dst = reinterpret_cast<uint4*>(row + c0);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        if (8 * c < n) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                w[e] = pack_bf16(__uint_as_float(v[8 * c + 2 * e]) * scale,
-                                 __uint_as_float(v[8 * c + 2 * e + 1]) * scale);
-            dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t* w = v + 32 * q + 8 * c;
+                x[c] = make_uint4(pack_bf16(__uint_as_float(w[0]) * scale, __uint_as_float(w[1]) * scale),
+                                  pack_bf16(__uint_as_float(w[2]) * scale, __uint_as_float(w[3]) * scale),
+                                  pack_bf16(__uint_as_float(w[4]) * scale, __uint_as_float(w[5]) * scale),
+                                  pack_bf16(__uint_as_float(w[6]) * scale, __uint_as_float(w[7]) * scale));
+            }
+            store_rows64(reinterpret_cast<uint8_t*>(row0 + c0 + 32 * q), 2 * (size_t)d, nrows, x);
         }
     }
 }
@@ -310,17 +298,16 @@ __global__ void __launch_bounds__(kThreads, 2) dh_fwd_kernel(const __grid_consta
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars.p_ready);
         }
-        if (ok && mbar_wait(&bars.o_done, (nblk - 1) & 1, abort, status, kStatusTimeout)) {
+        if (ok && mbar_wait_warp(&bars.o_done, (nblk - 1) & 1, abort, status, kStatusTimeout)) {
             tc_fence_after();
             const float inv = frz ? 1.f : 1.f / l;
             uint32_t ov[128];
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(lane_base + 128 + 32 * c4, ov + 32 * c4);
             tmem_ld_wait();
-            if (row < p.T) {
-                store_out_row(p.o + ((size_t)bh * p.T + row) * p.d, p.d, ov, inv);
-                p.lse[(size_t)bh * p.T + row] = frz ? lz2 * kLn2 : (m + log2f(l)) * kLn2;
-            }
+            const int row0 = row - lane;
+            store_rows_cols(p.o + ((size_t)bh * p.T + row0) * p.d, p.d, p.T - row0, 0, p.d, ov, inv);
+            if (row < p.T) p.lse[(size_t)bh * p.T + row] = frz ? lz2 * kLn2 : (m + log2f(l)) * kLn2;
         }
     }
 
@@ -551,14 +538,15 @@ __global__ void __launch_bounds__(kThreadsBwd, 1) dh_bwd_kv_kernel(const __grid_
         }
         // tcgen05.ld is warp-collective: every lane loads, only rows inside T are stored;
         // each half of the warps writes its 64 columns of dV and dK (those inside d)
-        if (ok && mbar_wait(&bars.tile_done, (ntiles - 1) & 1, abort, status, kStatusTimeout)) {
+        if (ok && mbar_wait_warp(&bars.tile_done, (ntiles - 1) & 1, abort, status, kStatusTimeout)) {
             tc_fence_after();
             const int c0 = 64 * half, n = min(64, p.d - c0);
+            const int key0 = key - lane;
             uint32_t v[64];
             tmem_ld32(lane_base + 256 + c0, v);
             tmem_ld32(lane_base + 256 + c0 + 32, v + 32);
             tmem_ld_wait();
-            if (key < p.T) store_out_cols(p.dv + ((size_t)bh * p.T + key) * p.d, c0, n, v, 1.f);
+            store_rows_cols(p.dv + ((size_t)bh * p.T + key0) * p.d, p.d, p.T - key0, c0, n, v, 1.f);
             if (!frz) {
                 tmem_ld32(lane_base + 384 + c0, v);
                 tmem_ld32(lane_base + 384 + c0 + 32, v + 32);
@@ -567,7 +555,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1) dh_bwd_kv_kernel(const __grid_
 #pragma unroll
                 for (int c = 0; c < 64; ++c) v[c] = 0u;
             }
-            if (key < p.T) store_out_cols(p.dk + ((size_t)bh * p.T + key) * p.d, c0, n, v, p.scale);
+            store_rows_cols(p.dk + ((size_t)bh * p.T + key0) * p.d, p.d, p.T - key0, c0, n, v, p.scale);
         }
     }
 
@@ -723,14 +711,15 @@ __global__ void __launch_bounds__(kThreadsBwd, 1) dh_bwd_q_kernel(const __grid_c
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars.ds_ready);
         }
-        if (ok && mbar_wait(&bars.tile_done, (nblk - 1) & 1, abort, status, kStatusTimeout)) {
+        if (ok && mbar_wait_warp(&bars.tile_done, (nblk - 1) & 1, abort, status, kStatusTimeout)) {
             tc_fence_after();
             const int c0 = 64 * half, n = min(64, p.d - c0);
+            const int row0 = row - lane;
             uint32_t v[64];
             tmem_ld32(lane_base + 256 + c0, v);
             tmem_ld32(lane_base + 256 + c0 + 32, v + 32);
             tmem_ld_wait();
-            if (row < p.T) store_out_cols(p.dq + ((size_t)bh * p.T + row) * p.d, c0, n, v, p.scale);
+            store_rows_cols(p.dq + ((size_t)bh * p.T + row0) * p.d, p.d, p.T - row0, c0, n, v, p.scale);
         }
     }
 

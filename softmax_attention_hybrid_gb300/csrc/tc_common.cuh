@@ -402,6 +402,35 @@ __host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t
     return off ^ ((row & 7u) << 4);
 }
 
+// Element i (0..3) of four 16-byte values, i in a register.
+__device__ __forceinline__ uint4 sel4(const uint4 (&v)[4], int i) {
+    const uint4 lo = (i & 1) ? v[1] : v[0];
+    const uint4 hi = (i & 1) ? v[3] : v[2];
+    return (i & 2) ? hi : lo;
+}
+
+__device__ __forceinline__ uint4 shfl_xor4(const uint4 v, int m) {
+    return make_uint4(__shfl_xor_sync(0xffffffffu, v.x, m), __shfl_xor_sync(0xffffffffu, v.y, m),
+                      __shfl_xor_sync(0xffffffffu, v.z, m), __shfl_xor_sync(0xffffffffu, v.w, m));
+}
+
+// 64 bytes of each of a warp's 32 rows (lane l: row l, bytes x[0..3]) to global memory at
+// row0 + l * row_bytes, rows l < nrows only; the whole warp must call it. The four lanes of
+// a group first exchange their 16-byte chunks (a 4 x 4 transpose in three xor rounds), so
+// that each store instruction writes 64 contiguous bytes of each of 8 rows: whole 32-byte
+// sectors, where a store of each lane's own row writes 16 bytes of each of 32 rows.
+__device__ __forceinline__ void store_rows64(uint8_t* row0, size_t row_bytes, int nrows, const uint4 (&x)[4]) {
+    const int lane = threadIdx.x & 31;
+    const int a = lane & 3, g4 = lane & ~3;
+    uint4 z[4];   // z[k]: chunk a of group row a ^ k
+    z[0] = sel4(x, a);
+#pragma unroll
+    for (int k = 1; k < 4; ++k) z[k] = shfl_xor4(sel4(x, a ^ k), k);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        if (g4 + i < nrows) *reinterpret_cast<uint4*>(row0 + (size_t)(g4 + i) * row_bytes + 16 * a) = sel4(z, i ^ a);
+}
+
 }  // namespace tc
 
 // Host: encode a 3-D TMA descriptor for a bf16 tensor [n2][n1][n0] (n0
