@@ -82,6 +82,13 @@ __device__ __forceinline__ void store_rows_cols(__nv_bfloat16* row0, int d, int 
     }
 }
 
+// Head kinds of a key-block item, as a compile-time tag so that each kind gets its own
+// tile loop: 0 every query head ordinary, 1 every one frozen, 2 mixed.
+template <int M>
+struct HeadKinds {
+    static constexpr int value = M;
+};
+
 struct DhParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;
     __nv_bfloat16* o;
@@ -96,6 +103,7 @@ struct DhParams {
     float* rowvec;         // [B, H, nqb, 256]: lse * log2(e) | D per query block
     uint32_t* status;
     int B, H, T, d, Tp, nqb;
+    int Hkv, G;            // key/value heads; query head h reads key/value head h / G
     float scale_log2;      // log2(e) / sqrt(d)
     float scale;           // 1 / sqrt(d)
     HeadMask mask;
@@ -132,6 +140,7 @@ __global__ void __launch_bounds__(kThreads, 2) dh_fwd_kernel(const __grid_consta
     const int qb = p.nqb - 1 - (int)blockIdx.x;   // the longest blocks first
     const int bh = blockIdx.y;
     const int h = bh % p.H;
+    const int bkv = (bh / p.H) * p.Hkv + h / p.G;   // key/value slice
     const bool frz = head_frozen(p.mask, h);
     const int nblk = qb + 1;
     if (threadIdx.x == 0) {
@@ -172,11 +181,11 @@ __global__ void __launch_bounds__(kThreads, 2) dh_fwd_kernel(const __grid_consta
                 if (!frz) {
                     if (!mbar_wait(&bars.k_empty, (j & 1) ^ 1u, abort, status, kStatusTimeout)) break;
                     mbar_expect_tx(&bars.k_full, kTile);
-                    load_tile(sm + FwdSmem::k, &p.tm_k, &bars.k_full, j * 128, bh);
+                    load_tile(sm + FwdSmem::k, &p.tm_k, &bars.k_full, j * 128, bkv);
                 }
                 if (!mbar_wait(&bars.v_empty, (j & 1) ^ 1u, abort, status, kStatusTimeout)) break;
                 mbar_expect_tx(&bars.v_full, frz ? kTile + 512 + 1024 : kTile);
-                load_tile(sm + FwdSmem::v, &p.tm_v, &bars.v_full, j * 128, bh);
+                load_tile(sm + FwdSmem::v, &p.tm_v, &bars.v_full, j * 128, bkv);
                 if (frz) {
                     bulk_load(vec, p.a2p + (size_t)h * p.Tp + (size_t)j * 128, 512, &bars.v_full);
                     bulk_load(vec + 128, p.r2p + (size_t)h * (p.Tp + 256) + (size_t)(qb - j) * 128, 1024,
@@ -360,8 +369,11 @@ __device__ __forceinline__ uint32_t chunk_col(int k, int second) {
 }
 
 // ---------------------------------------------------------------------------
-// Backward, key-block pass: dV, dK of key block kb of slice bh. Q, dO and the row
-// vectors of the next query tile load while this one runs (two stages).
+// Backward, key-block pass: dV, dK of key block kb of key/value slice bkv. The
+// tiles run over the G query heads that share the slice (one head in the
+// multi-head layer) and, for each, the query blocks kb .. nqb - 1; dV sums every
+// head's share, dK the ordinary heads' (zeros when the group has none). Q, dO and
+// the row vectors of the next query tile load while this one runs (two stages).
 // TMEM: S^T [0, 128) fp32, overwritten chunk by chunk with P^T and dS^T as bf16
 //       pairs (chunk c: P^T at [32 c, +16), dS^T at [32 c + 16, +16)) |
 //       dP^T [128, 256) | dV [256, 384) | dK [384, 512).
@@ -388,10 +400,12 @@ __global__ void __launch_bounds__(kThreadsBwd, 1) dh_bwd_kv_kernel(const __grid_
     grid_dep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kb = (int)blockIdx.x;
-    const int bh = blockIdx.y;
-    const int h = bh % p.H;
-    const bool frz = head_frozen(p.mask, h);
-    const int ntiles = p.nqb - kb;
+    const int bkv = blockIdx.y;                        // key/value slice
+    const int b = bkv / p.Hkv, h0 = (bkv - b * p.Hkv) * p.G;   // its query heads: h0 .. h0 + G - 1
+    const int nq = p.nqb - kb;                         // query tiles per query head
+    const int ntiles = p.G * nq;
+    bool any_ord = false, any_frz = false;
+    for (int gi = 0; gi < p.G; ++gi) (head_frozen(p.mask, h0 + gi) ? any_frz : any_ord) = true;
     if (threadIdx.x == 0) {
         abort_flag = 0;
         mbar_init(&bars.kv_full, 1);
@@ -418,11 +432,17 @@ __global__ void __launch_bounds__(kThreadsBwd, 1) dh_bwd_kv_kernel(const __grid_
 
     if (warp == 8) {
         if (lane == 0) {
-            mbar_expect_tx(&bars.kv_full, frz ? kTile : 2 * kTile);
-            if (!frz) load_tile(sm + KvSmem::k, &p.tm_k, &bars.kv_full, kb * 128, bh);
-            load_tile(sm + KvSmem::v, &p.tm_v, &bars.kv_full, kb * 128, bh);
-            for (int i = 0; i < ntiles; ++i) {
-                const int qb = kb + i, s = i & 1;
+            mbar_expect_tx(&bars.kv_full, any_ord ? 2 * kTile : kTile);
+            if (any_ord) load_tile(sm + KvSmem::k, &p.tm_k, &bars.kv_full, kb * 128, bkv);
+            load_tile(sm + KvSmem::v, &p.tm_v, &bars.kv_full, kb * 128, bkv);
+            for (int i = 0, gi = 0, qi = 0; i < ntiles; ++i) {   // tile i: query head h0 + gi, block kb + qi
+                const int qb = kb + qi, s = i & 1;
+                const int h = h0 + gi, bh = b * p.H + h;
+                const bool frz = head_frozen(p.mask, h);
+                if (++qi == nq) {
+                    qi = 0;
+                    ++gi;
+                }
                 if (!mbar_wait(&bars.st_empty[s], ((i >> 1) & 1) ^ 1u, abort, status, kStatusTimeout)) break;
                 uint8_t* st = sm + KvSmem::st + s * KvSmem::st_bytes;
                 float* vec = reinterpret_cast<float*>(st + KvSmem::st_vec);
@@ -431,7 +451,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 1) dh_bwd_kv_kernel(const __grid_
                 load_tile(st + KvSmem::st_do, &p.tm_do, &bars.st_full[s], qb * 128, bh);
                 bulk_load(vec, p.rowvec + ((size_t)bh * p.nqb + qb) * 256, 1024, &bars.st_full[s]);
                 if (frz)
-                    bulk_load(vec + 256, p.r2p + (size_t)h * (p.Tp + 256) + (size_t)i * 128, 1024, &bars.st_full[s]);
+                    bulk_load(vec + 256, p.r2p + (size_t)h * (p.Tp + 256) + (size_t)(qb - kb) * 128, 1024,
+                              &bars.st_full[s]);
             }
         }
     } else if (warp == 9) {
@@ -440,33 +461,50 @@ __global__ void __launch_bounds__(kThreadsBwd, 1) dh_bwd_kv_kernel(const __grid_
             const uint32_t id_n = idesc_bf16(128, 128, 0, 1);   // dV += P^T dO, dK += dS^T Q (B MN-major)
             const uint32_t sk = smem_u32(sm + KvSmem::k), sv = smem_u32(sm + KvSmem::v);
             bool ok = mbar_wait(&bars.kv_full, 0, abort, status, kStatusTimeout);
-            for (int i = 0; i < ntiles && ok; ++i) {
-                const int s = i & 1;
-                if (!(ok = mbar_wait(&bars.st_full[s], (i >> 1) & 1, abort, status, kStatusTimeout))) break;
-                tc_fence_after();
-                const uint32_t st = smem_u32(sm + KvSmem::st + s * KvSmem::st_bytes);
-                const uint32_t sq = st + KvSmem::st_q, sdo = st + KvSmem::st_do;
-                if (!frz) {
-                    // after the previous tile's dV and dK MMAs, which read columns [0, 128)
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) mma_ss(tmem, kmaj(sk, k), kmaj(sq, k), id_s, k > 0);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) mma_ss(tmem + 128, kmaj(sv, k), kmaj(sdo, k), id_s, k > 0);
-                    mma_commit(&bars.sdp_full);
-                }
-                if (!(ok = mbar_wait(&bars.pds_ready, i & 1, abort, status, kStatusTimeout))) break;
-                tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    mma_ts(tmem + 256, tmem + chunk_col(k, 0), mnmaj(sdo, k), id_n, (i > 0 || k > 0) ? 1u : 0u);
-                if (!frz) {
-#pragma unroll
+            auto tiles = [&](auto kinds) {
+                constexpr int M = decltype(kinds)::value;
+                int nord = 0;   // ordinary tiles so far (the first one starts dK)
+                for (int i = 0, gi = 0, qi = 0; i < ntiles && ok; ++i) {
+                    const int s = i & 1;
+                    const bool frz = M == 0 ? false : M == 1 ? true : head_frozen(p.mask, h0 + gi);
+                    if (++qi == nq) {
+                        qi = 0;
+                        ++gi;
+                    }
+                    if (!(ok = mbar_wait(&bars.st_full[s], (i >> 1) & 1, abort, status, kStatusTimeout))) break;
+                    tc_fence_after();
+                    const uint32_t st = smem_u32(sm + KvSmem::st + s * KvSmem::st_bytes);
+                    const uint32_t sq = st + KvSmem::st_q, sdo = st + KvSmem::st_do;
+                    if (!frz) {
+                        // after the previous tile's dV and dK MMAs, which read columns [0, 128)
+    #pragma unroll
+                        for (int k = 0; k < 8; ++k) mma_ss(tmem, kmaj(sk, k), kmaj(sq, k), id_s, k > 0);
+    #pragma unroll
+                        for (int k = 0; k < 8; ++k) mma_ss(tmem + 128, kmaj(sv, k), kmaj(sdo, k), id_s, k > 0);
+                        mma_commit(&bars.sdp_full);
+                    }
+                    if (!(ok = mbar_wait(&bars.pds_ready, i & 1, abort, status, kStatusTimeout))) break;
+                    tc_fence_after();
+    #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        mma_ts(tmem + 384, tmem + chunk_col(k, 1), mnmaj(sq, k), id_n, (i > 0 || k > 0) ? 1u : 0u);
+                        mma_ts(tmem + 256, tmem + chunk_col(k, 0), mnmaj(sdo, k), id_n, (i > 0 || k > 0) ? 1u : 0u);
+                    if (!frz) {
+    #pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            mma_ts(tmem + 384, tmem + chunk_col(k, 1), mnmaj(sq, k), id_n,
+                                   (nord > 0 || k > 0) ? 1u : 0u);
+                        ++nord;
+                    }
+                    mma_commit(&bars.st_empty[s]);
+                    mma_commit(&bars.tile_done);
                 }
-                mma_commit(&bars.st_empty[s]);
-                mma_commit(&bars.tile_done);
-            }
+            };
+            if (!any_frz)
+                tiles(HeadKinds<0>{});
+            else if (!any_ord)
+                tiles(HeadKinds<1>{});
+            else
+                tiles(HeadKinds<2>{});
             mma_commit(&bars.mma_idle);
             mbar_wait_bounded(&bars.mma_idle, 0, kWaitLimitNs);
         }
@@ -476,66 +514,84 @@ __global__ void __launch_bounds__(kThreadsBwd, 1) dh_bwd_kv_kernel(const __grid_
         const int t = quarter * 32 + lane;   // key row of the block = TMEM lane
         const int key = kb * 128 + t;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-        const float a2k = frz ? p.a2p[(size_t)h * p.Tp + key] : 0.f;
         bool ok = true;
-        for (int i = 0; i < ntiles; ++i) {
-            const bool diag = i == 0;
-            const int s = i & 1;
-            if (!(ok = mbar_wait(&bars.st_full[s], (i >> 1) & 1, abort, status, kStatusTimeout))) break;
-            const float* vec =
-                reinterpret_cast<const float*>(sm + KvSmem::st + s * KvSmem::st_bytes + KvSmem::st_vec);
-            if (!frz) {
-                // S^T, dP^T of this tile; their commit also means the previous tile's MMAs are done
-                if (!(ok = mbar_wait(&bars.sdp_full, i & 1, abort, status, kStatusTimeout))) break;
-                tc_fence_after();
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    const int c4 = 2 * half + cc;   // chunk of 32 queries
-                    uint32_t su[32], du[32], pk[16], dk[16];
-                    tmem_ld32(lane_base + 32 * c4, su);
-                    tmem_ld32(lane_base + 128 + 32 * c4, du);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const int q0 = 32 * c4 + e;
-                        float p0 = fast_exp2(__uint_as_float(su[e]) * p.scale_log2 - vec[q0]);
-                        float p1 = fast_exp2(__uint_as_float(su[e + 1]) * p.scale_log2 - vec[q0 + 1]);
-                        if (diag && q0 < t) p0 = 0.f;
-                        if (diag && q0 + 1 < t) p1 = 0.f;
-                        const float d0 = p0 * (__uint_as_float(du[e]) - vec[128 + q0]);
-                        const float d1 = p1 * (__uint_as_float(du[e + 1]) - vec[128 + q0 + 1]);
-                        pk[e >> 1] = pack_bf16(p0, p1);
-                        dk[e >> 1] = pack_bf16(d0, d1);
-                    }
-                    // chunk c4's own columns, already read
-                    tmem_st16(lane_base + 32 * c4, pk);
-                    tmem_st16(lane_base + 32 * c4 + 16, dk);
+        auto tiles = [&](auto kinds) {
+            constexpr int M = decltype(kinds)::value;
+            int nord = 0;     // ordinary tiles so far: phases of sdp_full
+            float a2k = 0.f;  // a * log2(e) of my key for the current query head (frozen heads)
+            for (int i = 0, gi = 0, qi = 0; i < ntiles; ++i) {
+                const bool diag = qi == 0;   // the query head's first tile: query block kb
+                const int h = h0 + gi;
+                const bool frz = M == 0 ? false : M == 1 ? true : head_frozen(p.mask, h);
+                if (frz && diag) a2k = p.a2p[(size_t)h * p.Tp + key];   // in flight during the wait below
+                if (++qi == nq) {
+                    qi = 0;
+                    ++gi;
                 }
-            } else {
-                // W^T(key, q) = exp2(a2[key] + r2[q - key] - log2 Z(q)); the band holds r at
-                // distance i 128 + c - t at entry 127 + c - t. The previous tile's dV MMA has
-                // read its W^T before this one is written.
-                if (i > 0 && !(ok = mbar_wait(&bars.tile_done, (i - 1) & 1, abort, status, kStatusTimeout))) break;
-                tc_fence_after();
-                const float* band = vec + 256 + 127 - t;
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    const int c4 = 2 * half + cc;
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const int c = 32 * c4 + e;
-                        pk[e >> 1] = pack_bf16(fast_exp2(a2k + band[c] - vec[c]),
-                                               fast_exp2(a2k + band[c + 1] - vec[c + 1]));
+                const int s = i & 1;
+                if (!(ok = mbar_wait(&bars.st_full[s], (i >> 1) & 1, abort, status, kStatusTimeout))) break;
+                const float* vec =
+                    reinterpret_cast<const float*>(sm + KvSmem::st + s * KvSmem::st_bytes + KvSmem::st_vec);
+                if (!frz) {
+                    // S^T, dP^T of this tile; their commit also means the previous tile's MMAs are done
+                    if (!(ok = mbar_wait(&bars.sdp_full, nord & 1, abort, status, kStatusTimeout))) break;
+                    ++nord;
+                    tc_fence_after();
+    #pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const int c4 = 2 * half + cc;   // chunk of 32 queries
+                        uint32_t su[32], du[32], pk[16], dk[16];
+                        tmem_ld32(lane_base + 32 * c4, su);
+                        tmem_ld32(lane_base + 128 + 32 * c4, du);
+                        tmem_ld_wait();
+    #pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            const int q0 = 32 * c4 + e;
+                            float p0 = fast_exp2(__uint_as_float(su[e]) * p.scale_log2 - vec[q0]);
+                            float p1 = fast_exp2(__uint_as_float(su[e + 1]) * p.scale_log2 - vec[q0 + 1]);
+                            if (diag && q0 < t) p0 = 0.f;
+                            if (diag && q0 + 1 < t) p1 = 0.f;
+                            const float d0 = p0 * (__uint_as_float(du[e]) - vec[128 + q0]);
+                            const float d1 = p1 * (__uint_as_float(du[e + 1]) - vec[128 + q0 + 1]);
+                            pk[e >> 1] = pack_bf16(p0, p1);
+                            dk[e >> 1] = pack_bf16(d0, d1);
+                        }
+                        // chunk c4's own columns, already read
+                        tmem_st16(lane_base + 32 * c4, pk);
+                        tmem_st16(lane_base + 32 * c4 + 16, dk);
                     }
-                    tmem_st16(lane_base + 32 * c4, pk);
+                } else {
+                    // W^T(key, q) = exp2(a2[key] + r2[q - key] - log2 Z(q)); the band holds r at
+                    // distance i 128 + c - t at entry 127 + c - t. The previous tile's dV MMA has
+                    // read its W^T before this one is written.
+                    if (i > 0 && !(ok = mbar_wait(&bars.tile_done, (i - 1) & 1, abort, status, kStatusTimeout))) break;
+                    tc_fence_after();
+                    const float* band = vec + 256 + 127 - t;
+    #pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const int c4 = 2 * half + cc;
+                        uint32_t pk[16];
+    #pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            const int c = 32 * c4 + e;
+                            pk[e >> 1] = pack_bf16(fast_exp2(a2k + band[c] - vec[c]),
+                                                   fast_exp2(a2k + band[c + 1] - vec[c + 1]));
+                        }
+                        tmem_st16(lane_base + 32 * c4, pk);
+                    }
                 }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars.pds_ready);
             }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars.pds_ready);
-        }
+        };
+        if (!any_frz)
+            tiles(HeadKinds<0>{});
+        else if (!any_ord)
+            tiles(HeadKinds<1>{});
+        else
+            tiles(HeadKinds<2>{});
         // tcgen05.ld is warp-collective: every lane loads, only rows inside T are stored;
         // each half of the warps writes its 64 columns of dV and dK (those inside d)
         if (ok && mbar_wait_warp(&bars.tile_done, (ntiles - 1) & 1, abort, status, kStatusTimeout)) {
@@ -546,8 +602,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 1) dh_bwd_kv_kernel(const __grid_
             tmem_ld32(lane_base + 256 + c0, v);
             tmem_ld32(lane_base + 256 + c0 + 32, v + 32);
             tmem_ld_wait();
-            store_rows_cols(p.dv + ((size_t)bh * p.T + key0) * p.d, p.d, p.T - key0, c0, n, v, 1.f);
-            if (!frz) {
+            store_rows_cols(p.dv + ((size_t)bkv * p.T + key0) * p.d, p.d, p.T - key0, c0, n, v, 1.f);
+            if (any_ord) {
                 tmem_ld32(lane_base + 384 + c0, v);
                 tmem_ld32(lane_base + 384 + c0 + 32, v + 32);
                 tmem_ld_wait();
@@ -555,7 +611,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1) dh_bwd_kv_kernel(const __grid_
 #pragma unroll
                 for (int c = 0; c < 64; ++c) v[c] = 0u;
             }
-            store_rows_cols(p.dk + ((size_t)bh * p.T + key0) * p.d, p.d, p.T - key0, c0, n, v, p.scale);
+            store_rows_cols(p.dk + ((size_t)bkv * p.T + key0) * p.d, p.d, p.T - key0, c0, n, v, p.scale);
         }
     }
 
@@ -597,6 +653,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1) dh_bwd_q_kernel(const __grid_c
     const int qb = p.nqb - 1 - (int)blockIdx.x;
     const int bh = blockIdx.y;
     const int h = bh % p.H;
+    const int bkv = (bh / p.H) * p.Hkv + h / p.G;   // key/value slice
     if (head_frozen(p.mask, h)) {
         // dQ of a frozen head is exactly zero
         if (threadIdx.x < 128) {
@@ -643,8 +700,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 1) dh_bwd_q_kernel(const __grid_c
                 if (!mbar_wait(&bars.st_empty[s], ((j >> 1) & 1) ^ 1u, abort, status, kStatusTimeout)) break;
                 uint8_t* st = sm + QSmem::st + s * QSmem::st_bytes;
                 mbar_expect_tx(&bars.st_full[s], 2 * kTile);
-                load_tile(st + QSmem::st_k, &p.tm_k, &bars.st_full[s], j * 128, bh);
-                load_tile(st + QSmem::st_v, &p.tm_v, &bars.st_full[s], j * 128, bh);
+                load_tile(st + QSmem::st_k, &p.tm_k, &bars.st_full[s], j * 128, bkv);
+                load_tile(st + QSmem::st_v, &p.tm_v, &bars.st_full[s], j * 128, bkv);
             }
         }
     } else if (warp == 9) {
@@ -748,14 +805,16 @@ DhParams make_params(const LayerArgs& a) {
     p.a2p = a.a2p;
     p.r2p = a.r2p;
     p.rowvec = a.rowvec;
+    p.Hkv = a.Hkv > 0 ? a.Hkv : a.H;
+    p.G = a.H / p.Hkv;
     return p;
 }
 
 bool make_maps(DhParams& p, const LayerArgs& a, bool backward) {
-    const int BH = a.B * a.H;
-    bool ok = make_tmap_bf16_3d(&p.tm_v, a.v, a.d, a.T, BH, 64, 128);
+    const int BH = a.B * a.H, BHkv = a.B * p.Hkv;
+    bool ok = make_tmap_bf16_3d(&p.tm_v, a.v, a.d, a.T, BHkv, 64, 128);
     if (a.q) ok = ok && make_tmap_bf16_3d(&p.tm_q, a.q, a.d, a.T, BH, 64, 128);
-    if (a.k) ok = ok && make_tmap_bf16_3d(&p.tm_k, a.k, a.d, a.T, BH, 64, 128);
+    if (a.k) ok = ok && make_tmap_bf16_3d(&p.tm_k, a.k, a.d, a.T, BHkv, 64, 128);
     if (backward) ok = ok && make_tmap_bf16_3d(&p.tm_do, a.dO, a.d, a.T, BH, 64, 128);
     return ok;
 }
@@ -796,7 +855,8 @@ cudaError_t launch_dh_bwd(const LayerArgs& a, cudaStream_t s) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(dh_bwd_q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_q);
     if (e != cudaSuccess) return e;
     before_launch(SAF_KERNEL_BWD_KV, s);
-    e = launch_ex(dh_bwd_kv_kernel, grid, dim3(kThreadsBwd), (size_t)smem_kv, s, true, 1, p);
+    e = launch_ex(dh_bwd_kv_kernel, dim3((unsigned)p.nqb, (unsigned)(a.B * p.Hkv)), dim3(kThreadsBwd),
+                  (size_t)smem_kv, s, true, 1, p);
     after_launch(SAF_KERNEL_BWD_KV, s);
     if (e != cudaSuccess) return e;
     before_launch(SAF_KERNEL_BWD_Q, s);

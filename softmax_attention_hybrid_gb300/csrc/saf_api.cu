@@ -215,7 +215,6 @@ int saf_attn_fwd_gqa(const void* q, const void* k, const void* v, const float* a
     Common c;
     int st = validate(q, k, v, a, r, ld_prior, frozen, B, H, T, d, dt, workspace, ws_bytes, 0, &c);
     if (st != SAF_OK) return st;
-    if (dt == SAF_BF16 && d != kHeadDim && Hkv != H) return SAF_EUNSUPPORTED;
     if (B == 0 || T == 0) return SAF_OK;
     if (!o || !lse) return SAF_EINVAL;
     if (!aligned16(o) || !aligned16(lse)) return SAF_EALIGN;
@@ -271,7 +270,6 @@ int saf_attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
     Common c;
     int st = validate(q, k, v, a, r, ld_prior, frozen, B, H, T, d, dt, workspace, ws_bytes, 1, &c);
     if (st != SAF_OK) return st;
-    if (dt == SAF_BF16 && d != kHeadDim && Hkv != H) return SAF_EUNSUPPORTED;
     if (B == 0 || T == 0) return SAF_OK;
     if (!o || !dO || !lse || !dq || !dk || !dv) return SAF_EINVAL;
     if (!aligned16(o) || !aligned16(dO) || !aligned16(lse) || !aligned16(dq) || !aligned16(dk) ||

@@ -14,6 +14,8 @@ dimension 64 at T=4096, the systems runs use B=8; the 1B study runs T=8192):
     1b_25         B=2  H=32 F=8  T=8192  d=64 bf16
     prefill_16k   B=1  H=12 F=3  T=16384 d=64 bf16, forward only
     gqa_32q8kv_4k B=4  H=32 (over Hkv=8 key/value heads) F=8 T=4096 d=64 bf16
+    gqa_32q8kv_d128 the same at head dimension 128
+    1b_d96        B=2  H=16 F=4  T=8192  d=96 bf16
 
 In every workload a[j] ~ N(0,1) (absolute key preference) and
 r[δ] = -slope*δ + 0.5 N(0,1) (relative distance preference), one row per
@@ -64,6 +66,8 @@ WORKLOADS = {
     # 32 query heads over 8 key/value heads (the grouped-query layout of the paper's
     # Qwen3-4B study, App. C.6) at head dimension 64, one frozen query head per group
     "gqa_32q8kv_4k": Workload("gqa_32q8kv_4k", 4, 32, 8, 4096, 64, "bf16", 0.5, 0.02, Hkv=8),
+    # the same layout at Qwen3-4B's own head dimension, 128 (App. C.6)
+    "gqa_32q8kv_d128": Workload("gqa_32q8kv_d128", 4, 32, 8, 4096, 128, "bf16", 0.5, 0.02, Hkv=8),
     # the paper's 1B layer at its own head dimension (App. C.5: 16 heads of d 96),
     # a quarter of them frozen, at the 8K context of the long-sequence runs
     "1b_d96": Workload("1b_d96", 2, 16, 4, 8192, 96, "bf16", 0.5, 0.01),

@@ -244,9 +244,13 @@ def test_gqa_argument_errors(saf):
     assert bwd(Hkv=-1) == saf.SAF_EINVAL
     assert bwd(Hkv=5) == saf.SAF_EINVAL
     assert bwd(T=0) == saf.SAF_OK
-    # bf16 at d = 96 / 128 serves the multi-head layout only
-    assert bwd(d=128) == saf.SAF_EUNSUPPORTED
-    assert lib.saf_attn_fwd_gqa(F, F, F, F, F, 256, None, 1, 8, 2, 256, 96, 0, F, F, F, 1 << 30,
+    # bf16 at d = 96 / 128 serves the grouped layout too: these calls get past the head
+    # dimension and stop at the missing output (o, dq = NULL), before any device work
+    assert lib.saf_attn_bwd_gqa(F, F, F, F, F, F, F, F, 256, None, 1, 8, 2, 256, 128, 0, None, F, F, F, 1 << 30,
+                                None) == saf.SAF_EINVAL
+    assert lib.saf_attn_fwd_gqa(F, F, F, F, F, 256, None, 1, 8, 2, 256, 96, 0, None, F, F, 1 << 30,
+                                None) == saf.SAF_EINVAL
+    assert lib.saf_attn_fwd_gqa(F, F, F, F, F, 256, None, 1, 8, 2, 256, 80, 0, None, F, F, 1 << 30,
                                 None) == saf.SAF_EUNSUPPORTED
 
 

@@ -109,6 +109,26 @@ def test_qwen_shaped_group_layout(saf):
     _check(saf, w, 8, seed=74, case="gqa H32/Hkv8 T1024 bf16")
 
 
+@pytest.mark.parametrize("d", [96, 128])
+def test_groups_at_wide_head_dims(saf, d):
+    # the d = 96 / 128 kernels in the grouped layout: 8 query heads over 4 key/value
+    # heads, groups {0, 1} and {2, 3} mixed, {4, 5} every head frozen (dK exactly zero),
+    # {6, 7} ordinary; T not a multiple of 128
+    w = custom_workload(2, 8, 300, d=d, frozen=(1, 3, 4, 5), slope=0.03)
+    _check(saf, w, 4, seed=76 + d, case=f"gqa H8/Hkv4 T300 d{d} bf16")
+
+
+def test_qwen_shaped_groups_at_head_dim_128(saf):
+    # Qwen3-4B's layout at its own head dimension (App. C.6): 32 query heads over 8
+    # key/value heads, d 128, one frozen query head per group, plus q = k = NULL when
+    # every head is frozen
+    fz = tuple(h for h in range(32) if h % 4 == 3)
+    w = custom_workload(1, 32, 640, d=128, frozen=fz, slope=0.01)
+    _check(saf, w, 8, seed=78, case="gqa H32/Hkv8 T640 d128 bf16")
+    w = custom_workload(1, 8, 200, d=128, frozen=tuple(range(8)), slope=0.05)
+    _check(saf, w, 2, seed=79, with_qk=False, case="gqa d128 all frozen, q = k = NULL")
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 def test_one_query_head_per_group_is_the_multi_head_layer(saf, dtype):
     # Hkv = H: the grouped-query entry points compute exactly what saf_attn_fwd /
@@ -129,7 +149,8 @@ def test_one_query_head_per_group_is_the_multi_head_layer(saf, dtype):
     assert (b1[0].float() - b2[0].float()).abs().max().item() <= TOL[dtype][1]
 
 
-def test_full_size_grouped_layer_sampled(saf):
+@pytest.mark.parametrize("name", ["gqa_32q8kv_4k", "gqa_32q8kv_d128"])
+def test_full_size_grouped_layer_sampled(saf, name):
     # the grouped-query bench workload (B4, 32 query heads over 8 key/value heads,
     # T 4096, one frozen query head per group) in the launch configuration the
     # benchmark times; two whole groups are compared element by element (every query
@@ -137,7 +158,7 @@ def test_full_size_grouped_layer_sampled(saf):
     # for finiteness and exact zeros
     import concurrent.futures as cf
     from softmax_attention_hybrid_gb300.inputs import WORKLOADS, make_inputs
-    w = WORKLOADS["gqa_32q8kv_4k"]
+    w = WORKLOADS[name]
     x = make_inputs(w, seed=0)
     out = _run(saf, x)
     G = w.H // w.Hkv
@@ -162,7 +183,7 @@ def test_full_size_grouped_layer_sampled(saf):
                 dv_ref += dvh
         for nm, ref in (("dk", dk_ref), ("dv", dv_ref)):
             err[nm] = max(err.get(nm, 0.0), float(np.max(np.abs(_np(out[nm][b, hk]) - ref))))
-    _parity_log.record("gqa_32q8kv_4k (2 groups)", err,
+    _parity_log.record(f"{name} (2 groups)", err,
                        {nm: (tol_o if nm in ("o", "lse") else tol_g) for nm in err})
     assert err["o"] <= tol_o and err["lse"] <= tol_o, err
     assert max(err["dq"], err["dk"], err["dv"]) <= tol_g, err
