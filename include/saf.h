@@ -23,8 +23,8 @@
  *  - Tensors q, k, v, o, dO, dq, dk, dv have layout [B, H, T, d], contiguous,
  *    element type `dt` (bf16 or fp32). lse and the normalisers are fp32.
  *    d = 64, 96 or 128. SAF_BF16 runs on tensor-core kernels (at 96 and 128
- *    for the multi-head layout with per-call normalisers: the grouped-query
- *    and prepared-state calls take d = 64 in bf16); SAF_FP32 on CUDA-core
+ *    for the multi-head and grouped-query layouts with per-call normalisers:
+ *    the prepared-state calls take d = 64 in bf16); SAF_FP32 on CUDA-core
  *    kernels. Other values return SAF_EUNSUPPORTED.
  *    Every tensor pointer must be 16-byte aligned (SAF_EALIGN otherwise).
  *  - a, r: fp32 [H, ld_prior] device arrays, ld_prior >= T; row h holds the
