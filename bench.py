@@ -479,8 +479,7 @@ def measure_workload(saf, w, args, dev, world, rank, stream, flush, peaks, peak_
         out["all_ordinary"] = {"ms_per_step": ao, "speedup": ao / step_ms,
                                "ideal_speedup": F.layer_flops(w.B, w.H, 0, w.T, w.d, not w.fwd_only) /
                                F.layer_flops(w.B, w.H, w.F, w.T, w.d, not w.fwd_only)}
-        if w.d == 64 or w.dtype == "fp32":   # the prepared calls take d = 64 in bf16
-            out["prepared_normalisers"] = time_prepared(saf, lay, args, dom, flush, stream, world, dev, flops, ao)
+        out["prepared_normalisers"] = time_prepared(saf, lay, args, dom, flush, stream, world, dev, flops, ao)
         if not w.fwd_only and w.d == 64 and not lay.gqa:
             lay.step(lay.frozen)
             out["trainable_patterns"] = time_pattern_grad(saf, lay, args, flush, stream, world, dev, step_ms,
@@ -552,7 +551,7 @@ def run_ours(args, w):
 
     prepared = None
     trainable = None
-    if w.F > 0 and (d == 64 or w.dtype == "fp32"):
+    if w.F > 0:
         prepared = time_prepared(saf, lay, args, dom, flush, stream, world, dev, total_flops,
                                  allord["ms_per_step"] if allord else None)
     if w.F > 0:

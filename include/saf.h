@@ -22,10 +22,9 @@
  * ---------------------------------------
  *  - Tensors q, k, v, o, dO, dq, dk, dv have layout [B, H, T, d], contiguous,
  *    element type `dt` (bf16 or fp32). lse and the normalisers are fp32.
- *    d = 64, 96 or 128. SAF_BF16 runs on tensor-core kernels (at 96 and 128
- *    for the multi-head and grouped-query layouts with per-call normalisers:
- *    the prepared-state calls take d = 64 in bf16); SAF_FP32 on CUDA-core
- *    kernels. Other values return SAF_EUNSUPPORTED.
+ *    d = 64, 96 or 128. SAF_BF16 runs on tensor-core kernels, SAF_FP32 on
+ *    CUDA-core kernels, for the multi-head and grouped-query layouts, with
+ *    per-call or prepared normalisers. Other values return SAF_EUNSUPPORTED.
  *    Every tensor pointer must be 16-byte aligned (SAF_EALIGN otherwise).
  *  - a, r: fp32 [H, ld_prior] device arrays, ld_prior >= T; row h holds the
  *    absolute-key preference a and the relative-distance preference r of

@@ -375,7 +375,6 @@ int saf_attn_fwd_prepared(const void* q, const void* k, const void* v, const flo
     Common c;
     int st = validate(q, k, v, a, r, ld_prior, frozen, B, H, T, d, dt, workspace, ws_bytes, 0, &c);
     if (st != SAF_OK) return st;
-    if (dt == SAF_BF16 && d != kHeadDim) return SAF_EUNSUPPORTED;
     if (B == 0 || T == 0) return SAF_OK;
     if (!o || !lse) return SAF_EINVAL;
     if (!aligned16(o) || !aligned16(lse)) return SAF_EALIGN;
@@ -391,7 +390,8 @@ int saf_attn_fwd_prepared(const void* q, const void* k, const void* v, const flo
     p.lse_out = lse;
     cudaError_t e = clear_call(p, bf16, s);
     use_state(p, state, H, T, bf16);
-    if (e == cudaSuccess) e = bf16 ? launch_tc_fwd(p, s) : launch_simt_fwd(p, false, s);
+    if (e == cudaSuccess)
+        e = !bf16 ? launch_simt_fwd(p, false, s) : d == kHeadDim ? launch_tc_fwd(p, s) : launch_dh_fwd(p, s);
     return launch_status(e);
 }
 
@@ -403,7 +403,6 @@ int saf_attn_bwd_prepared(const void* q, const void* k, const void* v, const voi
     Common c;
     int st = validate(q, k, v, a, r, ld_prior, frozen, B, H, T, d, dt, workspace, ws_bytes, 1, &c);
     if (st != SAF_OK) return st;
-    if (dt == SAF_BF16 && d != kHeadDim) return SAF_EUNSUPPORTED;
     if (B == 0 || T == 0) return SAF_OK;
     if (!o || !dO || !lse || !dq || !dk || !dv) return SAF_EINVAL;
     if (!aligned16(o) || !aligned16(dO) || !aligned16(lse) || !aligned16(dq) || !aligned16(dk) ||
@@ -425,7 +424,9 @@ int saf_attn_bwd_prepared(const void* q, const void* k, const void* v, const voi
     p.dv = dv;
     cudaError_t e = clear_call(p, bf16, s);
     use_state(p, state, H, T, bf16);
-    if (bf16) {
+    if (bf16 && d != kHeadDim) {
+        if (e == cudaSuccess) e = launch_dh_bwd(p, s);
+    } else if (bf16) {
         if (e == cudaSuccess) e = launch_bwd_prep(p, s, false);
         if (e == cudaSuccess) e = launch_tc_bwd(p, s);
     } else {

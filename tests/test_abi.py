@@ -317,6 +317,8 @@ def test_prepared_state_argument_errors(saf):
                                                  256, 64, 0, F, F, F, 1 << 30, None)
     assert fwd(st=None) == saf.SAF_EWORKSPACE
     assert fwd(hkv=3) == saf.SAF_EINVAL
-    # the prepared calls take d = 64 in bf16
-    assert lib.saf_attn_fwd_prepared(F, F, F, F, F, 256, fz, F, 1, 4, 4, 256, 128, 0, F, F, F, 1 << 30,
+    # the prepared calls take d = 96 and 128 in bf16 too (these stop at o = NULL), not 80
+    assert lib.saf_attn_fwd_prepared(F, F, F, F, F, 256, fz, F, 1, 4, 4, 256, 128, 0, None, F, F, 1 << 30,
+                                     None) == saf.SAF_EINVAL
+    assert lib.saf_attn_fwd_prepared(F, F, F, F, F, 256, fz, F, 1, 4, 4, 256, 80, 0, None, F, F, 1 << 30,
                                      None) == saf.SAF_EUNSUPPORTED

@@ -58,6 +58,36 @@ def test_prepared_layer_matches_per_call_normalisers(saf, dtype):
     assert torch.all(dq[:, fz] == 0) and torch.all(dk[:, fz] == 0)
 
 
+@pytest.mark.parametrize("d", [96, 128])
+def test_prepared_layer_at_wide_head_dims(saf, d):
+    # the d = 96 / 128 kernels with the state: the forward equals the per-call one bit
+    # for bit, and so does the backward (its passes add in a fixed order); one state
+    # also serves the grouped layout
+    w = custom_workload(2, 8, 300, d=d, frozen=(1, 4, 5), slope=0.03)
+    dev = torch.device("cuda:0")
+    for Hkv in (8, 2):
+        x = make_gqa_inputs(w, Hkv, seed=93 + d)
+        g = {n: x[n].to(dev) for n in ("q", "k", "v", "do", "a", "r")}
+        state = saf.saf_frozen_prepare(g["a"], g["r"], x["frozen"], w.T, torch.bfloat16)
+        o1, l1 = saf.saf_attn_fwd_gqa(g["q"], g["k"], g["v"], g["a"], g["r"], x["frozen"])
+        o2, l2 = saf.saf_attn_fwd_prepared(g["q"], g["k"], g["v"], g["a"], g["r"], x["frozen"], state)
+        b1 = saf.saf_attn_bwd_gqa(g["q"], g["k"], g["v"], o1, g["do"], l1, g["a"], g["r"], x["frozen"])
+        b2 = saf.saf_attn_bwd_prepared(g["q"], g["k"], g["v"], o2, g["do"], l2, g["a"], g["r"], x["frozen"], state)
+        torch.cuda.synchronize()
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+        for t1, t2 in zip(b1, b2):
+            assert torch.equal(t1, t2)
+    # and against the oracle, for the last (grouped) layout
+    q, k, v, do = (x[n].double().numpy() for n in ("q", "k", "v", "do"))
+    a, r = x["a"].double().numpy(), x["r"].double().numpy()
+    o_ref, _ = oracle.gqa_fwd(q, k, v, a, r, x["frozen"], threads=8)
+    refs = oracle.gqa_bwd(q, k, v, do, a, r, x["frozen"], threads=8)
+    err = {"o": float(np.max(np.abs(_np(o2) - o_ref)))}
+    err.update({nm: float(np.max(np.abs(_np(t) - ref))) for nm, t, ref in zip(("dq", "dk", "dv"), b2, refs)})
+    _parity_log.record(f"prepared state bf16 d{d} H8/Hkv2", err, {nm: TOL["bf16"][nm != "o"] for nm in err})
+    assert err["o"] <= TOL["bf16"][0] and max(err["dq"], err["dk"], err["dv"]) <= TOL["bf16"][1], err
+
+
 def test_one_state_serves_every_batch_and_the_grouped_layout(saf):
     # the state is per head and sequence length, not per batch entry: prepared once,
     # it serves a multi-head batch of 1 and a grouped-query batch of 3
