@@ -50,7 +50,8 @@ from softmax_attention_hybrid_gb300.inputs import WORKLOADS, make_inputs, Worklo
 METRIC = "hybrid attention fwd+bwd TFLOP/s and tokens/s at 1 GB300; % of bf16 tensor peak"
 DEFAULT_WORKLOAD = "gpt2_124m_25"
 # timed after the headline workload in the same run, each with its all-ordinary run
-OTHER_WORKLOADS = ("gpt2_124m_50", "1b_25", "prefill_16k", "gqa_32q8kv_4k", "gqa_32q8kv_d128", "1b_d96")
+OTHER_WORKLOADS = ("gpt2_124m_50", "1b_25", "prefill_16k", "prefill_b64_4k", "prefill_b64_4k_50", "gqa_32q8kv_4k",
+                   "gqa_32q8kv_d128", "1b_d96")
 L2_FLUSH_BYTES = 256 << 20  # larger than the 129 MB L2
 
 

@@ -13,6 +13,7 @@ dimension 64 at T=4096, the systems runs use B=8; the 1B study runs T=8192):
     gpt2_124m_50  B=8  H=12 F=6  T=4096  d=64 bf16
     1b_25         B=2  H=32 F=8  T=8192  d=64 bf16
     prefill_16k   B=1  H=12 F=3  T=16384 d=64 bf16, forward only
+    prefill_b64_4k, prefill_b64_4k_50  B=64 H=12 F=3 / 6 T=4096 d=64 bf16, forward only
     gqa_32q8kv_4k B=4  H=32 (over Hkv=8 key/value heads) F=8 T=4096 d=64 bf16
     gqa_32q8kv_d128 the same at head dimension 128
     1b_d96        B=2  H=16 F=4  T=8192  d=96 bf16
@@ -63,6 +64,10 @@ WORKLOADS = {
     "gpt2_124m_50": Workload("gpt2_124m_50", 8, 12, 6, 4096, 64, "bf16", 0.5, 0.02),
     "1b_25": Workload("1b_25", 2, 32, 8, 8192, 64, "bf16", 0.5, 0.01),
     "prefill_16k": Workload("prefill_16k", 1, 12, 3, 16384, 64, "bf16", 0.5, 0.005, fwd_only=True),
+    # batched causal prefill (App. D.3, Table 29: B 64 at 4K, a quarter and a half of the
+    # 12 heads replaced), one layer, forward only
+    "prefill_b64_4k": Workload("prefill_b64_4k", 64, 12, 3, 4096, 64, "bf16", 0.5, 0.02, fwd_only=True),
+    "prefill_b64_4k_50": Workload("prefill_b64_4k_50", 64, 12, 6, 4096, 64, "bf16", 0.5, 0.02, fwd_only=True),
     # 32 query heads over 8 key/value heads (the grouped-query layout of the paper's
     # Qwen3-4B study, App. C.6) at head dimension 64, one frozen query head per group
     "gqa_32q8kv_4k": Workload("gqa_32q8kv_4k", 4, 32, 8, 4096, 64, "bf16", 0.5, 0.02, Hkv=8),

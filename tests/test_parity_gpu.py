@@ -325,7 +325,7 @@ def _sample_slices(w, frozen, n_each=4):
     return picks
 
 
-@pytest.mark.parametrize("name", ["gpt2_124m_50", "1b_25", "1b_d96"])
+@pytest.mark.parametrize("name", ["gpt2_124m_50", "1b_25", "1b_d96", "prefill_b64_4k"])
 def test_full_size_sampled(saf, name):
     w = WORKLOADS[name]
     x = make_inputs(w, seed=0)
