@@ -412,6 +412,14 @@ def time_prepared(saf, lay, args, dom, flush, stream, world, dev, flops, ao_ms):
     return out
 
 
+def backward_ms(kms):
+    """Time of the backward kernels of a step: the fused kernel (d = 64), or the
+    key-block and query-block passes (d = 96, 128)."""
+    if "bwd" in kms:
+        return kms["bwd"]
+    return (kms.get("bwd_kv", 0.0) + kms.get("bwd_q", 0.0)) or None
+
+
 def time_pattern_grad(saf, lay, args, flush, stream, world, dev, step_ms, bwd_ms):
     """The trainable-pattern variant's extra work (App. C.3.2): da, dr of the frozen
     heads from the step's V, dO, o and lse through saf_pattern_grad_tc, each call
@@ -481,10 +489,10 @@ def measure_workload(saf, w, args, dev, world, rank, stream, flush, peaks, peak_
                                "ideal_speedup": F.layer_flops(w.B, w.H, 0, w.T, w.d, not w.fwd_only) /
                                F.layer_flops(w.B, w.H, w.F, w.T, w.d, not w.fwd_only)}
         out["prepared_normalisers"] = time_prepared(saf, lay, args, dom, flush, stream, world, dev, flops, ao)
-        if not w.fwd_only and w.d == 64 and not lay.gqa:
+        if not w.fwd_only and not lay.gqa:
             lay.step(lay.frozen)
             out["trainable_patterns"] = time_pattern_grad(saf, lay, args, flush, stream, world, dev, step_ms,
-                                                          kms.get("bwd"))
+                                                          backward_ms(kms))
     del lay
     torch.cuda.empty_cache()
     return out
@@ -556,9 +564,9 @@ def run_ours(args, w):
         prepared = time_prepared(saf, lay, args, dom, flush, stream, world, dev, total_flops,
                                  allord["ms_per_step"] if allord else None)
     if w.F > 0:
-        if not w.fwd_only and d == 64 and not lay.gqa:
+        if not w.fwd_only and not lay.gqa:
             lay.step(frozen)   # o and lse of the frozen-mask step
-            trainable = time_pattern_grad(saf, lay, args, flush, stream, world, dev, step_ms, kms.get("bwd"))
+            trainable = time_pattern_grad(saf, lay, args, flush, stream, world, dev, step_ms, backward_ms(kms))
 
     # end to end: host buffers in, host buffers out, through the same C ABI
     e2e = None

@@ -342,8 +342,8 @@ SAF_API int saf_pattern_grad(const void* v, const void* dO, const void* o, const
                              const float* r, int ld_prior, const uint8_t* frozen, int B, int H, int T, int d,
                              saf_dtype_t dt, float* da, float* dr, void* stream);
 
-/* The same gradients on the tensor cores (bf16 inputs, d = 64), with sums in a
- * fixed order: the results have the same bits on every run.
+/* The same gradients on the tensor cores (bf16 inputs, d = 64, 96 or 128), with
+ * sums in a fixed order: the results have the same bits on every run.
  * G^T = V dO^T is formed per causal 128 x 128 tile with tcgen05 MMAs (fp32 in
  * tensor memory); W is rebuilt from a, r and the log Z rows of lse in the form
  * the layer's backward uses (factorised, or exact when a head's log Z' falls
@@ -351,7 +351,7 @@ SAF_API int saf_pattern_grad(const void* v, const void* dO, const void* o, const
  * each thread summing its elements of one distance i - j over the band in
  * registers, and the per-tile key sums and per-band distance sums are written
  * to the workspace and added up by a last kernel.
- * In:  v, dO, o [B, H, T, 64] bf16, 16-byte aligned; lse [B, H, T] fp32 as
+ * In:  v, dO, o [B, H, T, d] bf16, 16-byte aligned; lse [B, H, T] fp32 as
  *      saf_attn_fwd wrote it; a, r, ld_prior, frozen as for saf_attn_fwd.
  * Out: da, dr: DEVICE fp32 [H, T], overwritten; rows of ordinary heads zero.
  * workspace: DEVICE scratch of saf_pattern_grad_tc_workspace_bytes(B, H, T,
@@ -360,8 +360,9 @@ SAF_API int saf_pattern_grad(const void* v, const void* dO, const void* o, const
  * saf_device_status reads after the call (SAF_ETIMEOUT when a bounded
  * wait of the kernel expired).
  * Errors: SAF_EINVAL (sizes, NULL), SAF_EALIGN, SAF_EWORKSPACE,
- * SAF_EUNSUPPORTED (d != 64, device), all before any work is enqueued;
- * SAF_ELAUNCH. saf_pattern_grad_tc_workspace_bytes returns 0 for invalid sizes. */
+ * SAF_EUNSUPPORTED (d not 64, 96 or 128; device), all before any work is
+ * enqueued; SAF_ELAUNCH. saf_pattern_grad_tc_workspace_bytes returns 0 for
+ * invalid sizes. */
 SAF_API size_t saf_pattern_grad_tc_workspace_bytes(int B, int H, int T, int n_frozen);
 SAF_API int saf_pattern_grad_tc(const void* v, const void* dO, const void* o, const float* lse, const float* a,
                                 const float* r, int ld_prior, const uint8_t* frozen, int B, int H, int T, int d,

@@ -54,7 +54,7 @@ using namespace tc;
 
 constexpr int kTileBytes = 128 * 64 * 2;   // one 128 x 64 bf16 tile
 constexpr int kThreads = 320;
-constexpr int kStages = 5;
+constexpr int kStagesMax = 5;   // load stages at d = 64 (PgSmem::stages for the wider heads)
 constexpr int kRing = 4;
 constexpr int kScrCols = 96;               // a warp's 95 distances, + 1
 constexpr int kScrRows = 8;                // rows of a warp's skew buffer (4 rounds of 8 lanes)
@@ -79,6 +79,7 @@ struct PgParams {
     float* dr_part;        // [B, F, nqb (band), 256]: entry e = distance 128 band + e - 128
     uint32_t* status;
     int B, H, T, Tp, nqb, F, n_items;
+    int d;                 // head dimension (64, 96 or 128)
     uint8_t frz_heads[SAF_MAX_HEADS];
 };
 
@@ -95,21 +96,27 @@ __host__ __device__ __forceinline__ int qperm(int c) {
 // thread (m = 0..3) at 32 quarter + 4 rho + m, one float4 per thread.
 __host__ __device__ __forceinline__ int kperm(int j) { return (j & 96) + (j & 7) * 4 + ((j >> 3) & 3); }
 
+// Shared memory for head dimensions up to kD (64, or 128 for d = 96 and 128: a tile is
+// then two 128-byte-swizzled atoms of 64 columns, and TMA fills the columns past d
+// with zeros, which add nothing to G).
+template <int kD>
 struct PgSmem {
+    static constexpr int atoms = kD / 64;
+    static constexpr int stages = kD == 64 ? kStagesMax : 2;
     // per stage: V tile of key block kb, dO tile of query block kb + band, row vectors
     static constexpr int st_v = 0;
-    static constexpr int st_do = kTileBytes;
+    static constexpr int st_do = atoms * kTileBytes;
     // row vectors, factorised form: 1/Z' [128] | -D/Z' [128] | ea [128] | er band [256];
     // exact form: log2 Z | D | a * log2(e) | r * log2(e) band (the first three in tile order)
-    static constexpr int st_vec = 2 * kTileBytes;
+    static constexpr int st_vec = 2 * atoms * kTileBytes;
     static constexpr int vec_bytes = 512 * 3 + 1024;
-    static constexpr int st_bytes = 2 * kTileBytes + 3072;   // 35 KB, 1024-aligned
-    static constexpr int scr = kStages * st_bytes;           // 8 warps x [8 x 98] fp32
-    static constexpr int wsum = scr + 8 * kScrRows * kScrStride * 4; // 2 (band parity) x 8 warps x 96 fp32
+    static constexpr int st_bytes = 2 * atoms * kTileBytes + 3072;   // 1024-aligned
+    static constexpr int scr = stages * st_bytes;                      // 8 warps x [8 x 98] fp32
+    static constexpr int wsum = scr + 8 * kScrRows * kScrStride * 4;  // 2 (band parity) x 8 warps x 96 fp32
     static constexpr int total = wsum + 2 * 8 * kScrCols * 4;
+    static_assert(st_bytes % 1024 == 0, "stage tiles must stay 1024-aligned");
+    static_assert(total + 1024 <= 227 * 1024, "shared memory");
 };
-static_assert(PgSmem::st_bytes % 1024 == 0, "stage tiles must stay 1024-aligned");
-static_assert(PgSmem::total + 1024 <= 227 * 1024, "shared memory");
 
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
@@ -179,13 +186,17 @@ __device__ __forceinline__ void pg_block(const uint32_t (&g)[32], int blk, const
 
 struct PgBarriers {
     uint64_t item_full[kRing], item_empty[kRing];
-    uint64_t st_full[kStages], st_empty[kStages];
+    uint64_t st_full[kStagesMax], st_empty[kStagesMax];
     uint64_t g_full[2], g_free[2];
     uint64_t band_sync;
     uint64_t mma_idle;
 };
 
+template <int kD>
 __global__ void __launch_bounds__(kThreads, 1) pg_tc_kernel(const __grid_constant__ PgParams p) {
+    using PgSmem = saf::PgSmem<kD>;
+    constexpr int kStages = PgSmem::stages;
+    constexpr int kAtoms = PgSmem::atoms;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     __shared__ PgBarriers bars;
@@ -271,9 +282,12 @@ __global__ void __launch_bounds__(kThreads, 1) pg_tc_kernel(const __grid_constan
                     uint8_t* st = sm + stage * PgSmem::st_bytes;
                     float* vec = reinterpret_cast<float*>(st + PgSmem::st_vec);
                     uint64_t* full = &bars.st_full[stage];
-                    mbar_expect_tx(full, 2 * kTileBytes + PgSmem::vec_bytes);
-                    tma_load_3d(st + PgSmem::st_v, &p.tm_v, full, 0, kb * 128, bh);
-                    tma_load_3d(st + PgSmem::st_do, &p.tm_do, full, 0, qb * 128, bh);
+                    mbar_expect_tx(full, 2 * kAtoms * kTileBytes + PgSmem::vec_bytes);
+#pragma unroll
+                    for (int at = 0; at < kAtoms; ++at) {   // 64 columns per atom
+                        tma_load_3d(st + PgSmem::st_v + at * kTileBytes, &p.tm_v, full, 64 * at, kb * 128, bh);
+                        tma_load_3d(st + PgSmem::st_do + at * kTileBytes, &p.tm_do, full, 64 * at, qb * 128, bh);
+                    }
                     bulk_load(vec, zrow + (size_t)qb * 128, 512, full);
                     bulk_load(vec + 128, yrow + (size_t)qb * 128, 512, full);
                     bulk_load(vec + 256, erow + (size_t)kb * 128, 512, full);
@@ -314,8 +328,10 @@ __global__ void __launch_bounds__(kThreads, 1) pg_tc_kernel(const __grid_constan
                     const uint64_t d_v = sdesc_sw128(st + PgSmem::st_v, 16, 1024);
                     const uint64_t d_do = sdesc_sw128(st + PgSmem::st_do, 16, 1024);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_ss(tmem + 128 * gb, sdesc_advance(d_v, 32 * k), sdesc_advance(d_do, 32 * k), id_g, k > 0);
+                    for (int k = 0; k < 4 * kAtoms; ++k) {   // K = 16 per step, 4 steps per atom
+                        const uint32_t off = (k >> 2) * kTileBytes + (k & 3) * 32;
+                        mma_ss(tmem + 128 * gb, sdesc_advance(d_v, off), sdesc_advance(d_do, off), id_g, k > 0);
+                    }
                     mma_commit(&bars.g_full[gb]);
                     mma_commit(&bars.st_empty[s]);
                     stage = (stage + 1) % kStages;
@@ -538,16 +554,28 @@ pg_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restr
         float d = 0.f;
         if (i < p.T) {
             const size_t row = ((size_t)b * p.H + h) * p.T + i;
-            const uint4* po = reinterpret_cast<const uint4*>(o + row * kHeadDim) + 2 * part;
-            const uint4* pd = reinterpret_cast<const uint4*>(dO + row * kHeadDim) + 2 * part;
-            const uint4 x0 = __ldg(po), x1 = __ldg(po + 1), y0 = __ldg(pd), y1 = __ldg(pd + 1);
-            const uint32_t xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-            const uint32_t ys[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+            // 4 threads per row, d / 4 elements (d / 32 chunks of 8) each
+            const int nc = p.d >> 5;
+            const uint4* po = reinterpret_cast<const uint4*>(o + row * p.d) + nc * part;
+            const uint4* pd = reinterpret_cast<const uint4*>(dO + row * p.d) + nc * part;
+            uint4 xv[4], yv[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                d = fmaf(__uint_as_float(xs[e] << 16), __uint_as_float(ys[e] << 16), d);
-                d = fmaf(__uint_as_float(xs[e] & 0xffff0000u), __uint_as_float(ys[e] & 0xffff0000u), d);
-            }
+            for (int c = 0; c < 4; ++c)
+                if (c < nc) {
+                    xv[c] = __ldg(po + c);
+                    yv[c] = __ldg(pd + c);
+                }
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                if (c < nc) {
+                    const uint32_t xs[4] = {xv[c].x, xv[c].y, xv[c].z, xv[c].w};
+                    const uint32_t ys[4] = {yv[c].x, yv[c].y, yv[c].z, yv[c].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        d = fmaf(__uint_as_float(xs[e] << 16), __uint_as_float(ys[e] << 16), d);
+                        d = fmaf(__uint_as_float(xs[e] & 0xffff0000u), __uint_as_float(ys[e] & 0xffff0000u), d);
+                    }
+                }
         }
         d += __shfl_xor_sync(0xffffffffu, d, 1);
         d += __shfl_xor_sync(0xffffffffu, d, 2);
@@ -693,7 +721,7 @@ extern "C" int saf_pattern_grad_tc(const void* v, const void* dO, const void* o,
                                    const float* r, int ld_prior, const uint8_t* frozen, int B, int H, int T, int d,
                                    float* da, float* dr, void* workspace, size_t ws_bytes, void* stream) {
     if (B < 0 || H <= 0 || H > SAF_MAX_HEADS || T < 0) return SAF_EINVAL;
-    if (d != kHeadDim) return SAF_EUNSUPPORTED;
+    if (d != 64 && d != 96 && d != 128) return SAF_EUNSUPPORTED;
     if ((long long)B * H * T * d > (1ll << 40)) return SAF_EINVAL;
     if (!da || !dr) return SAF_EINVAL;
     if (((uintptr_t)da & 3u) || ((uintptr_t)dr & 3u)) return SAF_EALIGN;
@@ -763,7 +791,7 @@ extern "C" int saf_pattern_grad_tc(const void* v, const void* dO, const void* o,
     la.erp = (float*)(ws + W.erp);
 
     const int BH = B * H;
-    if (!make_tmap_bf16_3d(&p.tm_v, v, 64, T, BH, 64, 128) || !make_tmap_bf16_3d(&p.tm_do, dO, 64, T, BH, 64, 128))
+    if (!make_tmap_bf16_3d(&p.tm_v, v, d, T, BH, 64, 128) || !make_tmap_bf16_3d(&p.tm_do, dO, d, T, BH, 64, 128))
         return SAF_ELAUNCH;
     p.yx = (float*)(ws + L.yx);
     p.yf = (float*)(ws + L.yf);
@@ -784,6 +812,7 @@ extern "C" int saf_pattern_grad_tc(const void* v, const void* dO, const void* o,
     p.Tp = p.nqb * 128;
     p.F = F;
     p.n_items = B * F * p.nqb;
+    p.d = d;
 
     trace_begin(SAF_KERNEL_PATTERN_GRAD, s);
     cudaError_t e = launch_call_init(la, true, false, s);
@@ -794,12 +823,15 @@ extern "C" int saf_pattern_grad_tc(const void* v, const void* dO, const void* o,
                       (const __nv_bfloat16*)o, (const __nv_bfloat16*)dO, lse, p, (const float*)la.amax,
                       (const float*)la.a2p, (const float*)la.eap, la.hflag);
     }
-    const int smem = PgSmem::total + 1024;
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(pg_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const bool wide = d > 64;
+    const int smem = (wide ? PgSmem<128>::total : PgSmem<64>::total) + 1024;
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(wide ? pg_tc_kernel<128> : pg_tc_kernel<64>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess) {
         note_launch();
-        e = launch_ex(pg_tc_kernel, dim3((unsigned)(p.n_items < sms ? p.n_items : sms)), dim3(kThreads),
-                      (size_t)smem, s, true, 1, p);
+        e = launch_ex(wide ? pg_tc_kernel<128> : pg_tc_kernel<64>, dim3((unsigned)(p.n_items < sms ? p.n_items : sms)),
+                      dim3(kThreads), (size_t)smem, s, true, 1, p);
     }
     if (e == cudaSuccess) {
         note_launch();

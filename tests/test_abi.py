@@ -203,7 +203,8 @@ def test_pattern_grad_tc_argument_errors(saf):
 
     assert pg(H=0) == saf.SAF_EINVAL
     assert pg(B=-1) == saf.SAF_EINVAL
-    assert pg(d=128) == saf.SAF_EUNSUPPORTED
+    assert pg(d=80) == saf.SAF_EUNSUPPORTED
+    assert pg(d=128, da=None) == saf.SAF_EINVAL   # d = 96 and 128 are served: the next check answers
     assert pg(da=None) == saf.SAF_EINVAL
     assert pg(dr=F + 1) == saf.SAF_EALIGN
     assert pg(T=0) == saf.SAF_OK

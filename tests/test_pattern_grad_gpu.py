@@ -121,6 +121,16 @@ def test_pattern_grad_tc_matches_oracle(saf, B, H, T, frozen):
     _check_tc(x, *_run_tc(saf, x))
 
 
+@pytest.mark.parametrize("d", [96, 128])
+@pytest.mark.parametrize("B,H,T,frozen", [(2, 3, 321, (0, 2)), (1, 2, 129, (0,))])
+def test_pattern_grad_tc_wide_heads(saf, d, B, H, T, frozen):
+    # head dimensions 96 and 128: G = dO V^T over two 64-column atoms per tile (columns
+    # past 96 zero-filled), several tiles and bands and a ragged last block
+    w = custom_workload(B, H, T, d=d, frozen=frozen, slope=0.05)
+    x = make_inputs(w, seed=80 + T + d)
+    _check_tc(x, *_run_tc(saf, x))
+
+
 def test_pattern_grad_tc_exact_form_head(saf):
     # head 1: a sink of weight e^100 at key 0 and a steep distance penalty, so
     # log Z' < -64 on far rows and the kernel takes the exact form for it;
@@ -164,7 +174,7 @@ def test_pattern_grad_tc_without_frozen_heads_gives_zeros(saf):
     assert not torch.any(da) and not torch.any(dr)
 
 
-@pytest.mark.parametrize("name", ["gpt2_124m_25", "gpt2_124m_50"])
+@pytest.mark.parametrize("name", ["gpt2_124m_25", "gpt2_124m_50", "1b_d96"])
 def test_pattern_grad_tc_full_size_sampled(saf, name):
     # the bench's workloads at full size, in the launch configuration bench.py times
     # (one call on the layer's own o and lse): sampled entries of da and dr against
