@@ -332,8 +332,9 @@ SAF_API int saf_fit_from_target(const float* A, int H, int T, int steps, float l
  *   dL(i, j) = W(i, j) (G(i, j) - D_i),
  *   da(j) = sum_b sum_{i >= j} dL(i, j),   dr(d) = sum_b sum_{i >= d} dL(i, i - d).
  *
- * In:  v, dO, o [B, H, T, d] (dt), lse [B, H, T] as saf_attn_fwd wrote it (the
- *      frozen rows hold log Z), a, r, ld_prior, frozen as for saf_attn_fwd.
+ * In:  v, dO, o [B, H, T, d] (dt, d = 64, 96 or 128), lse [B, H, T] as
+ *      saf_attn_fwd wrote it (the frozen rows hold log Z), a, r, ld_prior,
+ *      frozen as for saf_attn_fwd.
  * Out: da, dr: DEVICE fp32 [H, T]; rows of ordinary heads are zero. They are
  *      overwritten (cleared on `stream` first).
  * fp32 arithmetic on CUDA cores; the additions into da and dr are atomic, so

@@ -31,7 +31,7 @@ template <typename E>
 __global__ void __launch_bounds__(256)
 pattern_grad_kernel(const E* __restrict__ v, const E* __restrict__ dO, const E* __restrict__ o,
                     const float* __restrict__ lse, const float* __restrict__ a_all, const float* __restrict__ r_all,
-                    int ld, HeadMask mask, int H, int T, int F, int ntq, float* __restrict__ da,
+                    int ld, HeadMask mask, int H, int T, int d, int F, int ntq, float* __restrict__ da,
                     float* __restrict__ dr) {
     // tile (qt, kt), kt <= qt, numbered row by row: x = qt (qt + 1) / 2 + kt
     const int x = blockIdx.x;
@@ -55,40 +55,46 @@ pattern_grad_kernel(const E* __restrict__ v, const E* __restrict__ dO, const E* 
     __shared__ float sCol[16][kPgTile];
     __shared__ float sDiag[2 * kPgTile - 1];
     const int tid = threadIdx.x;
-    for (int e = tid; e < kPgTile * kPgTile; e += 256) {
-        const int rr = e / kPgTile, cc = e % kPgTile;
-        const int i = i0 + rr;
-        sA[rr][cc] = i < T ? to_f(dO[(slice + i) * kHeadDim + cc]) : 0.f;
-        sB[rr][cc] = i < T ? to_f(o[(slice + i) * kHeadDim + cc]) : 0.f;
-    }
     if (tid < 2 * kPgTile - 1) sDiag[tid] = 0.f;
-    __syncthreads();
-    if (tid < kPgTile) {
-        float s = 0.f;
-        for (int c = 0; c < kHeadDim; ++c) s = fmaf(sA[tid][c], sB[tid][c], s);
-        sD[tid] = s;   // D_i = dO_i . O_i
-    }
-    __syncthreads();
-    for (int e = tid; e < kPgTile * kPgTile; e += 256) {
-        const int rr = e / kPgTile, cc = e % kPgTile;
-        const int j = j0 + rr;
-        sB[rr][cc] = j < T ? to_f(v[(slice + j) * kHeadDim + cc]) : 0.f;
-    }
-    __syncthreads();
-    // G block: rows 4 ty .. +3, keys 4 tx .. +3
+    if (tid < kPgTile) sD[tid] = 0.f;
+    // G block: rows 4 ty .. +3, keys 4 tx .. +3; D and G summed over the head
+    // dimension in chunks of 64 columns (zeros past d)
     const int ty = tid >> 4, tx = tid & 15;
     float g[4][4] = {};
-    for (int c = 0; c < kHeadDim; ++c) {
-        float av[4], bv[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            av[u] = sA[4 * ty + u][c];
-            bv[u] = sB[4 * tx + u][c];
+    for (int c0 = 0; c0 < d; c0 += kPgTile) {
+        for (int e = tid; e < kPgTile * kPgTile; e += 256) {
+            const int rr = e / kPgTile, cc = e % kPgTile;
+            const int i = i0 + rr;
+            const bool in = i < T && c0 + cc < d;
+            sA[rr][cc] = in ? to_f(dO[(slice + i) * d + c0 + cc]) : 0.f;
+            sB[rr][cc] = in ? to_f(o[(slice + i) * d + c0 + cc]) : 0.f;
         }
+        __syncthreads();
+        if (tid < kPgTile) {
+            float s = 0.f;
+            for (int c = 0; c < kPgTile; ++c) s = fmaf(sA[tid][c], sB[tid][c], s);
+            sD[tid] += s;   // D_i = dO_i . O_i
+        }
+        __syncthreads();
+        for (int e = tid; e < kPgTile * kPgTile; e += 256) {
+            const int rr = e / kPgTile, cc = e % kPgTile;
+            const int j = j0 + rr;
+            sB[rr][cc] = (j < T && c0 + cc < d) ? to_f(v[(slice + j) * d + c0 + cc]) : 0.f;
+        }
+        __syncthreads();
+        for (int c = 0; c < kPgTile; ++c) {
+            float av[4], bv[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < 4; ++u) {
+                av[u] = sA[4 * ty + u][c];
+                bv[u] = sB[4 * tx + u][c];
+            }
 #pragma unroll
-            for (int w = 0; w < 4; ++w) g[u][w] = fmaf(av[u], bv[w], g[u][w]);
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int w = 0; w < 4; ++w) g[u][w] = fmaf(av[u], bv[w], g[u][w]);
+        }
+        __syncthreads();   // sA, sB are loaded again for the next chunk
     }
     float col[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -132,7 +138,7 @@ extern "C" int saf_pattern_grad(const void* v, const void* dO, const void* o, co
                                 saf_dtype_t dt, float* da, float* dr, void* stream) {
     if (B < 0 || H <= 0 || H > SAF_MAX_HEADS || T < 0) return SAF_EINVAL;
     if (dt != SAF_BF16 && dt != SAF_FP32) return SAF_EINVAL;
-    if (d != kHeadDim) return SAF_EUNSUPPORTED;
+    if (d != 64 && d != 96 && d != 128) return SAF_EUNSUPPORTED;
     if (!da || !dr) return SAF_EINVAL;
     if (((uintptr_t)da & 3u) || ((uintptr_t)dr & 3u)) return SAF_EALIGN;
     HeadMask mask;
@@ -171,10 +177,10 @@ extern "C" int saf_pattern_grad(const void* v, const void* dO, const void* o, co
     if (dt == SAF_BF16)
         pattern_grad_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
             (const __nv_bfloat16*)v, (const __nv_bfloat16*)dO, (const __nv_bfloat16*)o, lse, a, r, ld_prior, mask, H,
-            T, F, ntq, da, dr);
+            T, d, F, ntq, da, dr);
     else
         pattern_grad_kernel<float><<<grid, 256, 0, s>>>((const float*)v, (const float*)dO, (const float*)o, lse, a, r,
-                                                         ld_prior, mask, H, T, F, ntq, da, dr);
+                                                         ld_prior, mask, H, T, d, F, ntq, da, dr);
     if (cudaGetLastError() != cudaSuccess) return SAF_ELAUNCH;
     return SAF_OK;
 }

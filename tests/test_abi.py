@@ -166,7 +166,8 @@ def test_pattern_grad_argument_errors(saf):
                                     a["H"], a["T"], a["d"], a["dt"], a["da"], a["dr"], None)
 
     assert pg(H=0) == saf.SAF_EINVAL
-    assert pg(d=96) == saf.SAF_EUNSUPPORTED
+    assert pg(d=80) == saf.SAF_EUNSUPPORTED
+    assert pg(d=96, da=None) == saf.SAF_EINVAL   # d = 96 and 128 are served: the next check answers
     assert pg(dt=5) == saf.SAF_EINVAL
     assert pg(da=None) == saf.SAF_EINVAL
     assert pg(dr=F + 1) == saf.SAF_EALIGN

@@ -44,8 +44,28 @@ def test_pattern_grad_matches_oracle(saf, dtype, T, tol):
         assert abs(da[h].sum()) <= tol * scale * T ** 0.5 and abs(dr[h].sum()) <= tol * scale * T ** 0.5
 
 
+@pytest.mark.parametrize("dtype,d", [("fp32", 96), ("bf16", 128)])
+def test_pattern_grad_wide_heads_matches_oracle(saf, dtype, d):
+    # head dimensions 96 and 128 on CUDA cores: G and D summed over 64-column chunks
+    T, tol = 257, (1e-3 if dtype == "fp32" else 3e-2)
+    w = custom_workload(2, 3, T, d=d, dtype=dtype, frozen=(0, 2), slope=0.05)
+    x = make_inputs(w, seed=60 + d)
+    g = {n: x[n].to("cuda") for n in ("q", "k", "v", "do", "a", "r")}
+    o, lse = saf.saf_attn_fwd(g["q"], g["k"], g["v"], g["a"], g["r"], x["frozen"])
+    da, dr = saf.saf_pattern_grad(g["v"], g["do"], o, lse, g["a"], g["r"], x["frozen"])
+    torch.cuda.synchronize()
+    da, dr = da.double().cpu().numpy(), dr.double().cpu().numpy()
+    v, do = (x[n].double().numpy() for n in ("v", "do"))
+    ra, rr = oracle.attn_pattern_grad(v, do, x["a"].double().numpy(), x["r"].double().numpy(), x["frozen"])
+    assert not np.any(da[1]) and not np.any(dr[1])
+    for h in (0, 2):
+        scale = max(1.0, np.max(np.abs(ra[h])), np.max(np.abs(rr[h])))
+        assert np.max(np.abs(da[h] - ra[h])) <= tol * scale
+        assert np.max(np.abs(dr[h] - rr[h])) <= tol * scale
+
+
 # ---------------------------------------------------------------------------
-# Tensor-core form (saf_pattern_grad_tc): bf16, d = 64, fixed summation order
+# Tensor-core form (saf_pattern_grad_tc): bf16, d = 64, 96, 128, fixed summation order
 # ---------------------------------------------------------------------------
 #
 # The kernel takes D_i = dO_i . o_i from the bf16 forward output o it is given,
