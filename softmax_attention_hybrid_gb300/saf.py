@@ -448,7 +448,8 @@ def saf_pattern_grad_tc_workspace_bytes(B, H, T, n_frozen):
 
 def saf_pattern_grad_tc(v, do, o, lse, a, r, frozen, da=None, dr=None, workspace=None, stream=None):
     """Gradients of a and r of the frozen heads on the tensor cores (bf16 v, do, o
-    [B, H, T, 64]); fp32 CUDA tensors [H, T], the same bits on every run.
+    [B, H, T, d], d = 64, 96 or 128); fp32 CUDA tensors [H, T], the same bits on
+    every run.
     `workspace` (uint8 CUDA tensor) is allocated when not given."""
     B, H, T, d = v.shape
     fz = _frozen_bytes(frozen, H)
