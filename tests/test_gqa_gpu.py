@@ -129,6 +129,15 @@ def test_qwen_shaped_groups_at_head_dim_128(saf):
     _check(saf, w, 2, seed=79, with_qk=False, case="gqa d128 all frozen, q = k = NULL")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_maximum_head_count_grouped(saf, d):
+    # 256 query heads over 64 key/value heads: one frozen query head in every group,
+    # and the last group frozen throughout (its dK exactly zero)
+    fz = tuple(h for h in range(256) if h % 4 == 3 or h >= 252)
+    w = custom_workload(1, 256, 65, d=d, frozen=fz, slope=0.05)
+    _check(saf, w, 64, seed=95 + d, case=f"gqa H256/Hkv64 T65 d{d} bf16")
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 def test_one_query_head_per_group_is_the_multi_head_layer(saf, dtype):
     # Hkv = H: the grouped-query entry points compute exactly what saf_attn_fwd /

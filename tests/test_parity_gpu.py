@@ -362,6 +362,15 @@ def test_full_size_sampled(saf, name):
         assert torch.equal(out["lse"][0, h], out["lse"][-1, h])
 
 
+@pytest.mark.parametrize("d,dtype", [(64, "bf16"), (128, "bf16"), (64, "fp32")])
+def test_maximum_head_count(saf, d, dtype):
+    # H = 256, the most heads the boundary takes: the head masks span four 64-bit
+    # words, and frozen heads sit in each word and at both ends of the range
+    fz = (0, 3, 63, 64, 130, 191, 192, 255)
+    w = custom_workload(1, 256, 65, d=d, dtype=dtype, frozen=fz, scale=0.5, slope=0.05)
+    _check_full(saf, w, seed=90 + d, case=f"H=256 T=65 d{d} {dtype}")
+
+
 def test_stiff_pattern_uses_exact_form(saf):
     # a huge attention sink at key 0 and a steep distance penalty: rows far from
     # the sink have Z' = Z / exp(max a + max r) far below 1e-28, so the
