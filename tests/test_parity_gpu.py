@@ -371,6 +371,28 @@ def test_maximum_head_count(saf, d, dtype):
     _check_full(saf, w, seed=90 + d, case=f"H=256 T=65 d{d} {dtype}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_long_sequence_forward_sampled(saf, d):
+    # T = 65,536, four times the pages' longest runs: T^2 overflows 32-bit integers,
+    # the normalisers sum 2^31 products per frozen head, and there are 512 query
+    # blocks; sampled rows across the range against the oracle, every row finite
+    T = 65536
+    w = custom_workload(1, 2, T, d=d, frozen=(1,), slope=0.002)
+    x = make_inputs(w, seed=99)
+    out = _run(saf, x, backward=False)
+    rows = [0, 1, 127, 128, 4095, 32767, 32768, 65534, 65535]
+    a, r = x["a"].double().numpy(), x["r"].double().numpy()
+    err = {"o": 0.0, "lse": 0.0}
+    for h in range(w.H):
+        q, k, v = (x[n][0, h].double().numpy() for n in ("q", "k", "v"))
+        o_ref, lse_ref = oracle.head_fwd(q, k, v, a[h], r[h], bool(x["frozen"][h]), rows=rows)
+        err["o"] = max(err["o"], float(np.max(np.abs(_np(out["o"][0, h, rows]) - o_ref))))
+        err["lse"] = max(err["lse"], float(np.max(np.abs(_np(out["lse"][0, h, rows]) - lse_ref))))
+    _parity_log.record(f"T=65536 d{d} bf16 (9 rows per head)", err, {"o": 1e-2, "lse": 1e-2})
+    assert err["o"] <= 1e-2 and err["lse"] <= 1e-2, err
+    assert torch.isfinite(out["o"]).all() and torch.isfinite(out["lse"]).all()
+
+
 def test_stiff_pattern_uses_exact_form(saf):
     # a huge attention sink at key 0 and a steep distance penalty: rows far from
     # the sink have Z' = Z / exp(max a + max r) far below 1e-28, so the
